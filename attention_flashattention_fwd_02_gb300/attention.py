@@ -1,0 +1,61 @@
+"""Allocate-and-call helpers over the C ABI (torch only allocates memory and supplies the
+stream; the computation runs in the CUDA library).
+
+``forward`` returns (o, lse); ``backward`` returns (dq, dk, dv). Layout arguments follow
+include/attn.h: BHSD views; ``cu_seqlens`` given with ``compact=False`` selects padded
+varlen, with ``compact=True`` compact varlen over (1, H, T, D) views.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+__all__ = ["forward", "backward", "bwd_workspace"]
+
+
+def _lse_like(q: torch.Tensor) -> torch.Tensor:
+    return torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+
+
+def forward(q, k, v, sm_scale: Optional[float] = None, causal: bool = False,
+            cu_seqlens_q=None, cu_seqlens_k=None, compact: bool = False, max_seqlen_q: int = 0,
+            max_seqlen_k: int = 0, out=None, lse=None, workspace=None, stream=None):
+    sm_scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else sm_scale
+    o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if out is None else out
+    lse = _lse_like(q) if lse is None else lse
+    if compact:
+        _lib.attn_fwd_compact_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k,
+                                     cu_seqlens_q.numel() - 1, max_seqlen_q, max_seqlen_k,
+                                     sm_scale, causal, workspace, stream)
+    else:
+        _lib.attn_fwd(q, k, v, o, lse, sm_scale, causal, cu_seqlens_q, cu_seqlens_k,
+                      workspace, stream)
+    return o, lse
+
+
+def bwd_workspace(q: torch.Tensor) -> torch.Tensor:
+    B, H, S, D = q.shape
+    n = _lib.attn_bwd_workspace_size(B, H, S, D)
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def backward(q, k, v, o, lse, do, sm_scale: Optional[float] = None, causal: bool = False,
+             cu_seqlens_q=None, cu_seqlens_k=None, compact: bool = False, max_seqlen_q: int = 0,
+             max_seqlen_k: int = 0, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    sm_scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else sm_scale
+    dq = torch.empty(q.shape, dtype=q.dtype, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=k.dtype, device=k.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=v.dtype, device=v.device) if dv is None else dv
+    ws = bwd_workspace(q) if workspace is None else workspace
+    if compact:
+        _lib.attn_bwd_compact_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
+                                     cu_seqlens_q.numel() - 1, max_seqlen_q, max_seqlen_k,
+                                     sm_scale, causal, ws, stream)
+    else:
+        _lib.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, sm_scale, causal, ws, cu_seqlens_q,
+                      cu_seqlens_k, stream)
+    return dq, dk, dv

@@ -1,0 +1,486 @@
+// C ABI of the attention library (declared in include/attn.h): argument validation,
+// workspace layout, TMA tensor-map encoding and kernel launches. Host code only.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_launch.h"
+
+using namespace attn_sm103;
+
+namespace {
+
+constexpr int64_t kMaxI32 = 2147483647;
+
+// ----------------------------------------------------------------------------- driver entry
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// The current device must be sm_103 (GB300); cached per device ordinal.
+attn_status check_device() {
+  static int cache[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev] == 1 ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  return ok ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+}
+
+// ----------------------------------------------------------------------------- validation
+attn_status check_tensor4(const attn_tensor4* t) {
+  if (t == nullptr || t->data == nullptr) return ATTN_ERR_NULL;
+  for (int i = 0; i < 4; ++i)
+    if (t->size[i] < 0 || t->size[i] > kMaxI32) return ATTN_ERR_SHAPE;
+  if (t->stride[3] != 1) return ATTN_ERR_STRIDE;
+  for (int i = 0; i < 3; ++i)
+    if (t->size[i] > 1 && (t->stride[i] <= 0 || t->stride[i] % 8 != 0)) return ATTN_ERR_STRIDE;
+  if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0) return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
+attn_status check_tensor3(const attn_tensor3* t) {
+  if (t == nullptr || t->data == nullptr) return ATTN_ERR_NULL;
+  for (int i = 0; i < 3; ++i) {
+    if (t->size[i] < 0 || t->size[i] > kMaxI32) return ATTN_ERR_SHAPE;
+    if (t->size[i] > 1 && t->stride[i] <= 0) return ATTN_ERR_STRIDE;
+  }
+  if (reinterpret_cast<uintptr_t>(t->data) % 4 != 0) return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
+bool same_shape(const attn_tensor4* a, const attn_tensor4* b) {
+  for (int i = 0; i < 4; ++i)
+    if (a->size[i] != b->size[i]) return false;
+  return true;
+}
+
+// The problem every entry point reduces to.
+struct Problem {
+  int mode;          // kDense / kPadded / kCompact
+  int B, H, Sq, Sk, D;
+  int units;         // grid z: B, or num_seqs for compact
+  int max_q, max_k;  // per-unit length bounds (grid extents)
+  const int* cu_q;
+  const int* cu_k;
+};
+
+// Shapes of q (B,H,Sq,D) and k/v (B,H,Sk,D); mode from cu_seqlens / num_seqs.
+attn_status make_problem(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                         const int32_t* cu_q, const int32_t* cu_k, int compact, int32_t num_seqs,
+                         int32_t max_seqlen_q, int32_t max_seqlen_k, Problem* pr) {
+  attn_status s;
+  if ((s = check_tensor4(q)) != ATTN_OK) return s;
+  if ((s = check_tensor4(k)) != ATTN_OK) return s;
+  if ((s = check_tensor4(v)) != ATTN_OK) return s;
+  if (!same_shape(k, v)) return ATTN_ERR_SHAPE;
+  if (q->size[0] != k->size[0] || q->size[1] != k->size[1] || q->size[3] != k->size[3])
+    return ATTN_ERR_SHAPE;
+  const int64_t D = q->size[3];
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (q->size[1] > 65535) return ATTN_ERR_UNSUPPORTED;  // grid y
+  pr->B = (int)q->size[0];
+  pr->H = (int)q->size[1];
+  pr->Sq = (int)q->size[2];
+  pr->Sk = (int)k->size[2];
+  pr->D = (int)D;
+  if (compact) {
+    if (q->size[0] != 1) return ATTN_ERR_SHAPE;  // compact varlen takes batch exactly 1
+    if (cu_q == nullptr || cu_k == nullptr) return ATTN_ERR_NULL;
+    if (num_seqs < 0 || num_seqs > 65535) return ATTN_ERR_SHAPE;
+    pr->mode = kCompact;
+    pr->units = num_seqs;
+    pr->max_q = max_seqlen_q > 0 ? (max_seqlen_q < pr->Sq ? max_seqlen_q : pr->Sq) : pr->Sq;
+    pr->max_k = max_seqlen_k > 0 ? (max_seqlen_k < pr->Sk ? max_seqlen_k : pr->Sk) : pr->Sk;
+  } else {
+    if ((cu_q == nullptr) != (cu_k == nullptr)) return ATTN_ERR_NULL;
+    if (pr->B > 65535) return ATTN_ERR_UNSUPPORTED;  // grid z
+    pr->mode = cu_q ? kPadded : kDense;
+    pr->units = pr->B;
+    pr->max_q = pr->Sq;
+    pr->max_k = pr->Sk;
+  }
+  pr->cu_q = cu_q;
+  pr->cu_k = cu_k;
+  return ATTN_OK;
+}
+
+attn_status check_lse(const attn_tensor3* lse, const Problem& pr) {
+  attn_status s = check_tensor3(lse);
+  if (s != ATTN_OK) return s;
+  if (lse->size[0] != pr.B || lse->size[1] != pr.H || lse->size[2] != pr.Sq) return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
+
+SeqAddr seq_addr(const Problem& pr) {
+  SeqAddr a;
+  a.cu_q = pr.cu_q;
+  a.cu_k = pr.cu_k;
+  a.mode = pr.mode;
+  a.Sq = pr.Sq;
+  a.Sk = pr.Sk;
+  a.max_q = pr.max_q;
+  a.max_k = pr.max_k;
+  return a;
+}
+
+// 4-D tensor map over a BHSD view: dims (D, S, H, B) innermost first, box (64, rows, 1, 1),
+// 128-byte swizzle. Strides of size-1 dimensions are never used; they are replaced by a
+// valid dummy so that any view of such a dimension is accepted.
+attn_status make_map(CUtensorMap* m, const attn_tensor4* t, int box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  const int64_t B = t->size[0], H = t->size[1], S = t->size[2], D = t->size[3];
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)(S > 0 ? S : 1), (cuuint64_t)(H > 0 ? H : 1),
+                        (cuuint64_t)(B > 0 ? B : 1)};
+  const int64_t ss = (S > 1) ? t->stride[2] : D;
+  const int64_t sh = (H > 1) ? t->stride[1] : ss * (S > 0 ? S : 1);
+  const int64_t sb = (B > 1) ? t->stride[0] : sh * (H > 0 ? H : 1);
+  cuuint64_t strides[3] = {(cuuint64_t)ss * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+  for (int i = 0; i < 3; ++i)
+    if (strides[i] % 16 != 0 || strides[i] >= (1ull << 40)) return ATTN_ERR_STRIDE;
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct BwdWorkspace {
+  size_t delta_off, dq_off, total;
+};
+
+BwdWorkspace bwd_layout(int64_t B, int64_t H, int64_t rows, int64_t D) {
+  BwdWorkspace w;
+  const size_t n = (size_t)(B > 0 ? B : 0) * (size_t)(H > 0 ? H : 0) * (size_t)(rows > 0 ? rows : 0);
+  w.delta_off = 256;
+  w.dq_off = w.delta_off + align256(n * 4);
+  w.total = w.dq_off + n * (size_t)D * 4;
+  return w;
+}
+
+bool valid_scale(float s) { return isfinite(s) && s > 0.f; }
+
+// ----------------------------------------------------------------------------- forward
+attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                       const int32_t* cu_q, const int32_t* cu_k, int compact, int32_t num_seqs,
+                       int32_t max_q, int32_t max_k, float sm_scale, int causal,
+                       const attn_tensor4* o, const attn_tensor3* lse, void* ws, size_t ws_bytes,
+                       void* stream) {
+  Problem pr;
+  attn_status s = make_problem(q, k, v, cu_q, cu_k, compact, num_seqs, max_q, max_k, &pr);
+  if (s != ATTN_OK) return s;
+  if ((s = check_tensor4(o)) != ATTN_OK) return s;
+  if (!same_shape(q, o)) return ATTN_ERR_SHAPE;
+  if ((s = check_lse(lse, pr)) != ATTN_OK) return s;
+  if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
+  if (ws != nullptr && ws_bytes < attn_fwd_workspace_size(pr.B, pr.H, pr.Sq, pr.D))
+    return ATTN_ERR_WORKSPACE;
+  if (ws != nullptr && reinterpret_cast<uintptr_t>(ws) % 16 != 0) return ATTN_ERR_ALIGN;
+  if ((s = check_device()) != ATTN_OK) return s;
+  if (pr.units == 0 || pr.max_q == 0 || pr.H == 0) return ATTN_OK;
+
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  const int BM = fwd_block_m();
+  if ((s = make_map(&p.tm_q, q, BM)) != ATTN_OK) return s;
+  if ((s = make_map(&p.tm_k, k, 128)) != ATTN_OK) return s;
+  if ((s = make_map(&p.tm_v, v, 128)) != ATTN_OK) return s;
+  p.o = reinterpret_cast<__nv_bfloat16*>(o->data);
+  p.o_sb = o->stride[0];
+  p.o_sh = o->stride[1];
+  p.o_ss = o->stride[2];
+  p.lse = reinterpret_cast<float*>(lse->data);
+  p.l_sb = lse->stride[0];
+  p.l_sh = lse->stride[1];
+  p.l_ss = lse->stride[2];
+  p.seq = seq_addr(pr);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.status = reinterpret_cast<int*>(ws);
+  dim3 grid((pr.max_q + BM - 1) / BM, pr.H, pr.units);
+  cudaError_t e = launch_attn_fwd(p, pr.D, grid, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------- backward
+struct BwdArgs {
+  const attn_tensor4 *q, *k, *v, *o, *dout, *dq, *dk, *dv;
+  const attn_tensor3* lse;
+};
+
+attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float sm_scale,
+                      int causal, void* ws, size_t ws_bytes, void* stream) {
+  const BwdWorkspace w = bwd_layout(pr.B, pr.H, pr.Sq, pr.D);
+  if (ws == nullptr || ws_bytes < w.total) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return ATTN_ERR_ALIGN;
+  attn_status s = check_device();
+  if (s != ATTN_OK) return s;
+  if (pr.units == 0 || pr.H == 0) return ATTN_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+  float* delta = reinterpret_cast<float*>(base + w.delta_off);
+  float* dq_acc = reinterpret_cast<float*>(base + w.dq_off);
+  int* status = reinterpret_cast<int*>(base);
+  const SeqAddr sa = seq_addr(pr);
+
+  if (stage_mask & 1) {
+    BwdPreParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.o = reinterpret_cast<const __nv_bfloat16*>(a.o->data);
+    pp.dout = reinterpret_cast<const __nv_bfloat16*>(a.dout->data);
+    pp.o_sb = a.o->stride[0]; pp.o_sh = a.o->stride[1]; pp.o_ss = a.o->stride[2];
+    pp.do_sb = a.dout->stride[0]; pp.do_sh = a.dout->stride[1]; pp.do_ss = a.dout->stride[2];
+    pp.delta = delta;
+    pp.dq_acc = dq_acc;
+    pp.units = pr.units; pp.H = pr.H; pp.rows = pr.Sq; pp.D = pr.D;
+    pp.seq = sa;
+    pp.status = status;
+    if (launch_bwd_preprocess(pp, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  if (stage_mask & 2) {
+    if (pr.max_k > 0) {
+      BwdParams p;
+      memset(&p, 0, sizeof(p));
+      const int BM = bwd_block_m(pr.D), BN = bwd_block_n();
+      if ((s = make_map(&p.tm_q, a.q, BM)) != ATTN_OK) return s;
+      if ((s = make_map(&p.tm_do, a.dout, BM)) != ATTN_OK) return s;
+      if ((s = make_map(&p.tm_k, a.k, BN)) != ATTN_OK) return s;
+      if ((s = make_map(&p.tm_v, a.v, BN)) != ATTN_OK) return s;
+      p.lse = reinterpret_cast<const float*>(a.lse->data);
+      p.l_sb = a.lse->stride[0]; p.l_sh = a.lse->stride[1]; p.l_ss = a.lse->stride[2];
+      p.delta = delta;
+      p.dq_acc = dq_acc;
+      p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk->data);
+      p.dk_sb = a.dk->stride[0]; p.dk_sh = a.dk->stride[1]; p.dk_ss = a.dk->stride[2];
+      p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv->data);
+      p.dv_sb = a.dv->stride[0]; p.dv_sh = a.dv->stride[1]; p.dv_ss = a.dv->stride[2];
+      p.H = pr.H;
+      p.rows_q = pr.Sq;
+      p.seq = sa;
+      p.causal = causal ? 1 : 0;
+      p.scale_log2 = sm_scale * 1.4426950408889634f;
+      p.sm_scale = sm_scale;
+      p.status = status;
+      dim3 grid((pr.max_k + BN - 1) / BN, pr.H, pr.units);
+      if (launch_bwd_main(p, pr.D, grid, st) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+  }
+  if (stage_mask & 4) {
+    BwdPostParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.dq_acc = dq_acc;
+    pp.dq = reinterpret_cast<__nv_bfloat16*>(a.dq->data);
+    pp.dq_sb = a.dq->stride[0]; pp.dq_sh = a.dq->stride[1]; pp.dq_ss = a.dq->stride[2];
+    pp.units = pr.units; pp.H = pr.H; pp.rows = pr.Sq; pp.D = pr.D;
+    pp.seq = sa;
+    pp.sm_scale = sm_scale;
+    if (launch_bwd_dq_epilogue(pp, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+attn_status bwd_common(const BwdArgs& a, const int32_t* cu_q, const int32_t* cu_k, int compact,
+                       int32_t num_seqs, int32_t max_q, int32_t max_k, float sm_scale,
+                       int causal, void* ws, size_t ws_bytes, void* stream) {
+  Problem pr;
+  attn_status s =
+      make_problem(a.q, a.k, a.v, cu_q, cu_k, compact, num_seqs, max_q, max_k, &pr);
+  if (s != ATTN_OK) return s;
+  const attn_tensor4* qshaped[] = {a.o, a.dout, a.dq};
+  for (const attn_tensor4* t : qshaped) {
+    if ((s = check_tensor4(t)) != ATTN_OK) return s;
+    if (!same_shape(a.q, t)) return ATTN_ERR_SHAPE;
+  }
+  const attn_tensor4* kshaped[] = {a.dk, a.dv};
+  for (const attn_tensor4* t : kshaped) {
+    if ((s = check_tensor4(t)) != ATTN_OK) return s;
+    if (!same_shape(a.k, t)) return ATTN_ERR_SHAPE;
+  }
+  if ((s = check_lse(a.lse, pr)) != ATTN_OK) return s;
+  if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
+  return bwd_stage(7, a, pr, sm_scale, causal, ws, ws_bytes, stream);
+}
+
+}  // namespace
+
+// =============================================================================== C ABI
+extern "C" {
+
+size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D) {
+  (void)B; (void)H; (void)Sq; (void)D;
+  return 256;
+}
+
+size_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D) {
+  return bwd_layout(B, H, Sq, D).total;
+}
+
+attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, float sm_scale,
+                     int causal, const attn_tensor4* o, const attn_tensor3* lse,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_common(q, k, v, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, causal, o, lse,
+                    workspace, workspace_bytes, stream);
+}
+
+attn_status attn_fwd_padded_varlen(const attn_tensor4* q, const attn_tensor4* k,
+                                   const attn_tensor4* v, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, float sm_scale, int causal,
+                                   const attn_tensor4* o, const attn_tensor3* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return ATTN_ERR_NULL;
+  return attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, sm_scale, causal, o, lse, workspace,
+                  workspace_bytes, stream);
+}
+
+attn_status attn_fwd_compact_varlen(const attn_tensor4* q, const attn_tensor4* k,
+                                    const attn_tensor4* v, const int32_t* cu_seqlens_q,
+                                    const int32_t* cu_seqlens_k, int32_t num_seqs,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k, float sm_scale,
+                                    int causal, const attn_tensor4* o, const attn_tensor3* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_common(q, k, v, cu_seqlens_q, cu_seqlens_k, 1, num_seqs, max_seqlen_q, max_seqlen_k,
+                    sm_scale, causal, o, lse, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                     const attn_tensor4* o, const attn_tensor3* lse, const attn_tensor4* dout,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, float sm_scale,
+                     int causal, const attn_tensor4* dq, const attn_tensor4* dk,
+                     const attn_tensor4* dv, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse};
+  return bwd_common(a, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, causal, workspace,
+                    workspace_bytes, stream);
+}
+
+attn_status attn_bwd_padded_varlen(const attn_tensor4* q, const attn_tensor4* k,
+                                   const attn_tensor4* v, const attn_tensor4* o,
+                                   const attn_tensor3* lse, const attn_tensor4* dout,
+                                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                   float sm_scale, int causal, const attn_tensor4* dq,
+                                   const attn_tensor4* dk, const attn_tensor4* dv,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return ATTN_ERR_NULL;
+  return attn_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, sm_scale, causal, dq, dk,
+                  dv, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_compact_varlen(const attn_tensor4* q, const attn_tensor4* k,
+                                    const attn_tensor4* v, const attn_tensor4* o,
+                                    const attn_tensor3* lse, const attn_tensor4* dout,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                    int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                    float sm_scale, int causal, const attn_tensor4* dq,
+                                    const attn_tensor4* dk, const attn_tensor4* dv,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse};
+  return bwd_common(a, cu_seqlens_q, cu_seqlens_k, 1, num_seqs, max_seqlen_q, max_seqlen_k,
+                    sm_scale, causal, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_preprocess(const attn_tensor4* o, const attn_tensor4* dout,
+                                const int32_t* cu_seqlens_q, int32_t num_seqs,
+                                int32_t max_seqlen_q, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  // Shapes come from o; k/v are not needed by this stage, o stands in for them.
+  Problem pr;
+  const int compact = num_seqs >= 0;
+  attn_status s = make_problem(o, o, o, cu_seqlens_q, cu_seqlens_q, compact, num_seqs,
+                               max_seqlen_q, max_seqlen_q, &pr);
+  if (s != ATTN_OK) return s;
+  if ((s = check_tensor4(dout)) != ATTN_OK) return s;
+  if (!same_shape(o, dout)) return ATTN_ERR_SHAPE;
+  BwdArgs a{o, o, o, o, dout, nullptr, nullptr, nullptr, nullptr};
+  return bwd_stage(1, a, pr, 1.f, 0, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_main(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                          const attn_tensor3* lse, const attn_tensor4* dout,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                          float sm_scale, int causal, const attn_tensor4* dk,
+                          const attn_tensor4* dv, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  Problem pr;
+  const int compact = num_seqs >= 0;
+  attn_status s = make_problem(q, k, v, cu_seqlens_q, cu_seqlens_k, compact, num_seqs,
+                               max_seqlen_q, max_seqlen_k, &pr);
+  if (s != ATTN_OK) return s;
+  if ((s = check_tensor4(dout)) != ATTN_OK) return s;
+  if (!same_shape(q, dout)) return ATTN_ERR_SHAPE;
+  const attn_tensor4* kshaped[] = {dk, dv};
+  for (const attn_tensor4* t : kshaped) {
+    if ((s = check_tensor4(t)) != ATTN_OK) return s;
+    if (!same_shape(k, t)) return ATTN_ERR_SHAPE;
+  }
+  if ((s = check_lse(lse, pr)) != ATTN_OK) return s;
+  if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
+  BwdArgs a{q, k, v, q, dout, nullptr, dk, dv, lse};
+  return bwd_stage(2, a, pr, sm_scale, causal, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_dq_epilogue(const attn_tensor4* dq, const int32_t* cu_seqlens_q,
+                                 int32_t num_seqs, int32_t max_seqlen_q, float sm_scale,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  Problem pr;
+  const int compact = num_seqs >= 0;
+  attn_status s = make_problem(dq, dq, dq, cu_seqlens_q, cu_seqlens_q, compact, num_seqs,
+                               max_seqlen_q, max_seqlen_q, &pr);
+  if (s != ATTN_OK) return s;
+  if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
+  BwdArgs a{dq, dq, dq, dq, dq, dq, nullptr, nullptr, nullptr};
+  return bwd_stage(4, a, pr, sm_scale, 0, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_read_device_status(void* workspace, void* stream, int32_t* out) {
+  if (workspace == nullptr || out == nullptr) return ATTN_ERR_NULL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(workspace, 0, sizeof(v), st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  *out = v;
+  return ATTN_OK;
+}
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "inconsistent tensor sizes";
+    case ATTN_ERR_STRIDE: return "unsupported strides (D stride must be 1, others multiples of 8)";
+    case ATTN_ERR_ALIGN: return "base pointer not 16-byte aligned";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported case (d_head, device, sm_scale or size limits)";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA runtime or driver error";
+    case ATTN_ERR_DEVICE_BAD_SEQLENS: return "device: inconsistent cu_seqlens (sequence skipped)";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "device: pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,495 @@
+// Backward pass of fused scaled-dot-product attention on sm_103a: three kernels.
+//
+//  1. attn_bwd_pre_kernel    Delta_i = sum_d dO_id O_id (fp32) and zeroing of the fp32 dQ
+//                            accumulator rows. Memory-bound.
+//  2. attn_bwd_main_kernel   one CTA per 128-key tile (K_n, V_n loaded once), looping over
+//                            the query tiles that can see those keys:
+//                              S^T  = K_n Q_m^T           (tcgen05, TMEM)
+//                              dP^T = V_n dO_m^T          (tcgen05, TMEM)
+//                              P^T  = exp2(S^T c2 - LSE2), dS^T = P^T (dP^T - Delta)
+//                              dV  += P^T dO_m            (tcgen05, TMEM accumulator)
+//                              dK  += dS^T Q_m            (tcgen05, TMEM accumulator)
+//                              dQ_m partial = dS K_n      (tcgen05, TMEM) -> fp32 atomics
+//                            then dK * sm_scale and dV are written. P is rebuilt from the
+//                            LSE that the forward pass stashed.
+//  3. attn_bwd_post_kernel   dQ = bf16(sm_scale * accumulator). Memory-bound.
+//
+// Main-kernel warp roles (320 threads): warps 0..3 compute P^T / dS^T (thread j owns key row
+// j = TMEM lane j) and write dK / dV at the end; warps 4..7 drain the dQ partial from TMEM
+// into the global accumulator; warp 8 is the TMA producer; warp 9 allocates TMEM and issues
+// the MMAs. Tile sizes: 128 keys per CTA; 64 query rows per step when d_head = 128 (dQ is
+// formed transposed, K_n^T dS^T, so that every MMA has M = 128), 128 when d_head = 64.
+#include "attn_common.cuh"
+#include "attn_launch.h"
+
+namespace attn_sm103 {
+
+__device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// =========================================================================== preprocess
+// One group of D/8 threads per row: each thread reads 8 elements (16 bytes) of O and dO.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant__ BwdPreParams p) {
+  constexpr int TPR = D / 8;             // threads per row
+  constexpr int ROWS = 256 / TPR;        // rows per block
+  const int h = blockIdx.y, z = blockIdx.z;
+  SeqView sv;
+  if (!decode_seq(p.seq, z, threadIdx.x == 0 ? p.status : nullptr, sv)) return;
+  const int r = blockIdx.x * ROWS + threadIdx.x / TPR;
+  const int part = threadIdx.x % TPR;
+  if (blockIdx.x * ROWS >= sv.len_q) return;
+  float acc = 0.f;
+  const bool valid = r < sv.len_q;
+  const int64_t grow = sv.row0_q + r;
+  if (valid) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p.o + sv.batch * p.o_sb + h * p.o_sh +
+                                                    grow * p.o_ss + part * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(p.dout + sv.batch * p.do_sb + h * p.do_sh +
+                                                    grow * p.do_ss + part * 8);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa = __bfloat1622float2(a2[e]);
+      const float2 fb = __bfloat1622float2(b2[e]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (valid) {
+    const int64_t idx = ((int64_t)sv.batch * p.H + h) * p.rows + grow;
+    if (part == 0) p.delta[idx] = acc;
+    float4* dst = reinterpret_cast<float4*>(p.dq_acc + idx * D + part * 8);
+    dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream) {
+  const int rows_per_block = 256 / (p.D / 8);
+  const int max_len = p.seq.mode == kCompact ? p.seq.max_q : p.seq.Sq;
+  dim3 grid((max_len + rows_per_block - 1) / rows_per_block, p.H, p.units);
+  if (grid.x == 0 || grid.z == 0) return cudaSuccess;
+  if (p.D == 128)
+    attn_bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(p);
+  else
+    attn_bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// =========================================================================== dQ epilogue
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_post_kernel(const __grid_constant__ BwdPostParams p) {
+  constexpr int TPR = D / 8;
+  constexpr int ROWS = 256 / TPR;
+  const int h = blockIdx.y, z = blockIdx.z;
+  SeqView sv;
+  if (!decode_seq(p.seq, z, nullptr, sv)) return;
+  const int r = blockIdx.x * ROWS + threadIdx.x / TPR;
+  const int part = threadIdx.x % TPR;
+  if (r >= sv.len_q) return;
+  const int64_t grow = sv.row0_q + r;
+  const int64_t idx = ((int64_t)sv.batch * p.H + h) * p.rows + grow;
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + idx * D + part * 8);
+  const float4 a = src[0], b = src[1];
+  uint4 v;
+  v.x = pack_bf16x2(a.x * p.sm_scale, a.y * p.sm_scale);
+  v.y = pack_bf16x2(a.z * p.sm_scale, a.w * p.sm_scale);
+  v.z = pack_bf16x2(b.x * p.sm_scale, b.y * p.sm_scale);
+  v.w = pack_bf16x2(b.z * p.sm_scale, b.w * p.sm_scale);
+  *reinterpret_cast<uint4*>(p.dq + sv.batch * p.dq_sb + h * p.dq_sh + grow * p.dq_ss + part * 8) = v;
+}
+
+cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream) {
+  const int rows_per_block = 256 / (p.D / 8);
+  const int max_len = p.seq.mode == kCompact ? p.seq.max_q : p.seq.Sq;
+  dim3 grid((max_len + rows_per_block - 1) / rows_per_block, p.H, p.units);
+  if (grid.x == 0 || grid.z == 0) return cudaSuccess;
+  if (p.D == 128)
+    attn_bwd_post_kernel<128><<<grid, 256, 0, stream>>>(p);
+  else
+    attn_bwd_post_kernel<64><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// =========================================================================== main kernel
+template <int D>
+struct BwdCfg {
+  static constexpr int BN = 128;                 // keys per CTA (MMA M for S^T, dP^T, dK, dV)
+  static constexpr int BM = (D == 128) ? 64 : 128;  // query rows per step
+  static constexpr bool DQ_T = (D == 128);       // dQ^T = K^T dS^T (M = D) vs dQ = dS K (M = BM)
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int P_BYTES = BN * BM * 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;   // 2 stages
+  static constexpr int OFF_DO = OFF_Q + 2 * Q_BYTES;  // 2 stages
+  static constexpr int OFF_P = OFF_DO + 2 * Q_BYTES;
+  static constexpr int OFF_DS = OFF_P + P_BYTES;
+  static constexpr int SMEM_BYTES = OFF_DS + P_BYTES + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_DK = 0, COL_DV = D, COL_S = 2 * D, COL_DP = 2 * D + BM,
+                            COL_DQ = 384;
+  static_assert(2 * D + 2 * BM <= 384, "TMEM layout overlaps");
+  static constexpr int NTHREADS = 320;
+};
+
+template <int BM>
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full, s_empty, p_full, p_empty, dq_full, dq_empty, dkdv_full;
+  uint32_t tmem_base;
+  int abort;
+  float lse2[2][BM];
+  float delta[2][BM];
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int BN = C::BN, BM = C::BM;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ BwdBars<BM> bars;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tile = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+
+  SeqView sv;
+  if (!decode_seq(p.seq, z, threadIdx.x == 0 ? p.status : nullptr, sv)) return;
+  const int k_lo = n_tile * BN;
+  if (k_lo >= sv.len_k) return;
+  const int m_begin = p.causal ? k_lo / BM : 0;
+  const int m_end = (sv.len_q + BM - 1) / BM;
+  const int n_steps = max(0, m_end - m_begin);
+  const int64_t zh = (int64_t)sv.batch * p.H + h;
+
+  if (n_steps == 0) {  // no query sees these keys: dK = dV = 0
+    if (warp < 4) {
+      const int key = k_lo + threadIdx.x;
+      if (key < sv.len_k) {
+        const int64_t grow = sv.row0_k + key;
+        __nv_bfloat16* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
+        __nv_bfloat16* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
+        for (int d = 0; d < D; d += 8) {
+          *reinterpret_cast<uint4*>(kr + d) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vr + d) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    return;
+  }
+
+  uint8_t* smem = align1024b(smem_raw);
+  const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+  const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+  const uint32_t sP = smem_u32(smem + C::OFF_P), sDS = smem_u32(smem + C::OFF_DS);
+
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(smem_u32(&bars.kv_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars.q_full[s]), 33);  // producer lane 0 (tx) + 32 lanes (LSE/Delta)
+      mbar_init(smem_u32(&bars.q_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars.s_full), 1);
+    mbar_init(smem_u32(&bars.s_empty), 128);
+    mbar_init(smem_u32(&bars.p_full), 128);
+    mbar_init(smem_u32(&bars.p_empty), 1);
+    mbar_init(smem_u32(&bars.dq_full), 1);
+    mbar_init(smem_u32(&bars.dq_empty), 128);
+    mbar_init(smem_u32(&bars.dkdv_full), 1);
+    mbar_fence_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&bars.tmem_base), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  volatile int* abort = &bars.abort;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&p.tm_q);
+      tma_prefetch_map(&p.tm_k);
+      tma_prefetch_map(&p.tm_v);
+      tma_prefetch_map(&p.tm_do);
+      const uint32_t kvb = smem_u32(&bars.kv_full);
+      mbar_arrive_expect_tx(kvb, 2 * C::KV_BYTES);
+#pragma unroll
+      for (int s = 0; s < D / 64; ++s) {
+        tma_load_4d(sK + s * BN * 128, &p.tm_k, kvb, s * 64, sv.row0_k + k_lo, h, sv.batch);
+        tma_load_4d(sV + s * BN * 128, &p.tm_v, kvb, s * 64, sv.row0_k + k_lo, h, sv.batch);
+      }
+    }
+    for (int it = 0; it < n_steps; ++it) {
+      const int st = it & 1;
+      if (it >= 2 &&
+          !mbar_wait(smem_u32(&bars.q_empty[st]), ((it >> 1) - 1) & 1, abort, kWaitTimeoutNs))
+        break;
+      const int q_lo = (m_begin + it) * BM;
+      const uint32_t qb = smem_u32(&bars.q_full[st]);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(qb, 2 * C::Q_BYTES);
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s) {
+          tma_load_4d(sQ + st * C::Q_BYTES + s * BM * 128, &p.tm_q, qb, s * 64, sv.row0_q + q_lo, h,
+                      sv.batch);
+          tma_load_4d(sDO + st * C::Q_BYTES + s * BM * 128, &p.tm_do, qb, s * 64, sv.row0_q + q_lo,
+                      h, sv.batch);
+        }
+      }
+      for (int i = lane; i < BM; i += 32) {
+        const int q = q_lo + i;
+        float l2 = 0.f, dl = 0.f;
+        if (q < sv.len_q) {
+          const int64_t grow = sv.row0_q + q;
+          l2 = p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] * kLog2e;
+          dl = p.delta[zh * p.rows_q + grow];
+        }
+        bars.lse2[st][i] = l2;
+        bars.delta[st][i] = dl;
+      }
+      mbar_arrive(qb);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, BM, false, false);   // S^T, dP^T
+      constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);     // dV, dK
+      constexpr uint32_t idQ = C::DQ_T ? idesc_bf16_f32(128, BM, true, true)   // dQ^T
+                                       : idesc_bf16_f32(128, D, true, true);   // dQ
+      const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP;
+      const uint32_t tDK = tmem + C::COL_DK, tDV = tmem + C::COL_DV, tDQ = tmem + C::COL_DQ;
+      bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort, kWaitTimeoutNs);
+      for (int it = 0; ok && it <= n_steps; ++it) {
+        if (it < n_steps) {
+          const int st = it & 1;
+          if (!mbar_wait(smem_u32(&bars.q_full[st]), (it >> 1) & 1, abort, kWaitTimeoutNs)) break;
+          if (it > 0 && !mbar_wait(smem_u32(&bars.s_empty), (it - 1) & 1, abort, kWaitTimeoutNs))
+            break;
+          tc_fence_after();
+          const uint32_t q = sQ + st * C::Q_BYTES, dO = sDO + st * C::Q_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tS, desc_kmajor(sK, BN, kk), desc_kmajor(q, BM, kk), idS, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tDP, desc_kmajor(sV, BN, kk), desc_kmajor(dO, BM, kk), idS, kk > 0);
+          umma_commit(smem_u32(&bars.s_full));
+        }
+        if (it > 0) {
+          const int prev = it - 1, pst = prev & 1;
+          if (!mbar_wait(smem_u32(&bars.p_full), prev & 1, abort, kWaitTimeoutNs)) break;
+          tc_fence_after();
+          const uint32_t q = sQ + pst * C::Q_BYTES, dO = sDO + pst * C::Q_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            umma_ss(tDV, desc_kmajor(sP, BN, kk), desc_mnmajor(dO, BM, kk), idG,
+                    (prev > 0 || kk > 0));
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            umma_ss(tDK, desc_kmajor(sDS, BN, kk), desc_mnmajor(q, BM, kk), idG,
+                    (prev > 0 || kk > 0));
+          if (prev > 0 &&
+              !mbar_wait(smem_u32(&bars.dq_empty), (prev - 1) & 1, abort, kWaitTimeoutNs))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            if (C::DQ_T)
+              umma_ss(tDQ, desc_mnmajor(sK, BN, kk), desc_mnmajor(sDS, BN, kk), idQ, kk > 0);
+            else
+              umma_ss(tDQ, desc_mnmajor(sDS, BN, kk), desc_mnmajor(sK, BN, kk), idQ, kk > 0);
+          }
+          umma_commit(smem_u32(&bars.p_empty));
+          umma_commit(smem_u32(&bars.q_empty[pst]));
+          umma_commit(smem_u32(&bars.dq_full));
+        }
+      }
+      umma_commit(smem_u32(&bars.dkdv_full));
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ P^T / dS^T compute
+    const int j = threadIdx.x;  // key row in tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int key = k_lo + j;
+    const float c2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_steps; ++it) {
+      const int st = it & 1;
+      const int q_lo = (m_begin + it) * BM;
+      if (!mbar_wait(smem_u32(&bars.s_full), it & 1, abort, kWaitTimeoutNs) ||
+          !mbar_wait(smem_u32(&bars.q_full[st]), (it >> 1) & 1, abort, kWaitTimeoutNs)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool need_mask = (q_lo + BM > sv.len_q) || (k_lo + BN > sv.len_k) ||
+                             (p.causal && k_lo + BN - 1 > q_lo);
+      // first visible query index for this key row (top-left causal: q >= key)
+      const int q_min = p.causal ? key : 0;
+      const bool key_ok = key < sv.len_k;
+      uint32_t pp[BM / 2], pd[BM / 2];
+#pragma unroll
+      for (int c = 0; c < BM / 32; ++c) {
+        float s[32], dp[32];
+        ATTN_TMEM_LD_X32(tmem + C::COL_S + lane_off + c * 32, reinterpret_cast<uint32_t*>(s));
+        ATTN_TMEM_LD_X32(tmem + C::COL_DP + lane_off + c * 32, reinterpret_cast<uint32_t*>(dp));
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int i = c * 32 + e;
+          float pv0 = ex2_approx(fmaf(s[e], c2, -bars.lse2[st][i]));
+          float pv1 = ex2_approx(fmaf(s[e + 1], c2, -bars.lse2[st][i + 1]));
+          float ds0 = pv0 * (dp[e] - bars.delta[st][i]);
+          float ds1 = pv1 * (dp[e + 1] - bars.delta[st][i + 1]);
+          if (need_mask) {
+            const int q0 = q_lo + i, q1 = q0 + 1;
+            const bool v0 = key_ok && q0 < sv.len_q && q0 >= q_min;
+            const bool v1 = key_ok && q1 < sv.len_q && q1 >= q_min;
+            pv0 = v0 ? pv0 : 0.f;
+            ds0 = v0 ? ds0 : 0.f;
+            pv1 = v1 ? pv1 : 0.f;
+            ds1 = v1 ? ds1 : 0.f;
+          }
+          pp[i / 2] = pack_bf16x2(pv0, pv1);
+          pd[i / 2] = pack_bf16x2(ds0, ds1);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.s_empty));
+      if (it > 0 && !mbar_wait(smem_u32(&bars.p_empty), (it - 1) & 1, abort, kWaitTimeoutNs)) {
+        ok = false;
+        break;
+      }
+      uint8_t* gP = smem + C::OFF_P;
+      uint8_t* gDS = smem + C::OFF_DS;
+#pragma unroll
+      for (int c8 = 0; c8 < BM / 8; ++c8) {
+        const uint32_t off = sw128_offset(j, c8 * 8, BN);
+        *reinterpret_cast<uint4*>(gP + off) =
+            make_uint4(pp[c8 * 4 + 0], pp[c8 * 4 + 1], pp[c8 * 4 + 2], pp[c8 * 4 + 3]);
+        *reinterpret_cast<uint4*>(gDS + off) =
+            make_uint4(pd[c8 * 4 + 0], pd[c8 * 4 + 1], pd[c8 * 4 + 2], pd[c8 * 4 + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bars.p_full));
+    }
+    // ---- epilogue: dK = sm_scale * acc, dV = acc
+    if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, kWaitTimeoutNs);
+    tc_fence_after();
+    if (ok) {
+      const bool valid = key < sv.len_k;
+      const int64_t grow = sv.row0_k + key;
+      __nv_bfloat16* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
+      __nv_bfloat16* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32], b[32];
+        ATTN_TMEM_LD_X32(tmem + C::COL_DK + lane_off + c * 32, a);
+        ATTN_TMEM_LD_X32(tmem + C::COL_DV + lane_off + c * 32, b);
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 vk, vv;
+            const float sc = p.sm_scale;
+            vk.x = pack_bf16x2(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc);
+            vk.y = pack_bf16x2(__uint_as_float(a[e + 2]) * sc, __uint_as_float(a[e + 3]) * sc);
+            vk.z = pack_bf16x2(__uint_as_float(a[e + 4]) * sc, __uint_as_float(a[e + 5]) * sc);
+            vk.w = pack_bf16x2(__uint_as_float(a[e + 6]) * sc, __uint_as_float(a[e + 7]) * sc);
+            vv.x = pack_bf16x2(__uint_as_float(b[e]), __uint_as_float(b[e + 1]));
+            vv.y = pack_bf16x2(__uint_as_float(b[e + 2]), __uint_as_float(b[e + 3]));
+            vv.z = pack_bf16x2(__uint_as_float(b[e + 4]), __uint_as_float(b[e + 5]));
+            vv.w = pack_bf16x2(__uint_as_float(b[e + 6]), __uint_as_float(b[e + 7]));
+            *reinterpret_cast<uint4*>(kr + c * 32 + e) = vk;
+            *reinterpret_cast<uint4*>(vr + c * 32 + e) = vv;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ dQ drain (warps 4..7)
+    const int t = threadIdx.x - 128;  // TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    float* acc_base = p.dq_acc + (zh * p.rows_q + sv.row0_q) * D;
+    for (int it = 0; it < n_steps; ++it) {
+      if (!mbar_wait(smem_u32(&bars.dq_full), it & 1, abort, kWaitTimeoutNs)) break;
+      tc_fence_after();
+      const int q_lo = (m_begin + it) * BM;
+      if (C::DQ_T) {
+        // lanes = d, columns = query rows of the step
+        float v[BM];
+#pragma unroll
+        for (int c = 0; c < BM / 32; ++c)
+          ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + c * 32, reinterpret_cast<uint32_t*>(&v[c * 32]));
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dq_empty));
+        const int d = t;
+        const int nvalid = min(BM, sv.len_q - q_lo);
+#pragma unroll
+        for (int i = 0; i < BM; ++i)
+          if (i < nvalid) atomicAdd(acc_base + (int64_t)(q_lo + i) * D + d, v[i]);
+      } else {
+        // lanes = query rows, columns = d
+        float v[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + c * 32, reinterpret_cast<uint32_t*>(&v[c * 32]));
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dq_empty));
+        const int q = q_lo + t;
+        if (q < sv.len_q) {
+          float4* dst = reinterpret_cast<float4*>(acc_base + (int64_t)q * D);
+#pragma unroll
+          for (int e = 0; e < D / 4; ++e)
+            atomicAdd(dst + e, make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && bars.abort && p.status != nullptr) atomicCAS(p.status, 0, kStatusTimeout);
+}
+
+template <int D>
+static cudaError_t launch_bwd_main_impl(const BwdParams& p, dim3 grid, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  attn_bwd_main_kernel<D><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdParams& p, int D, dim3 grid, cudaStream_t stream) {
+  return D == 128 ? launch_bwd_main_impl<128>(p, grid, stream)
+                  : launch_bwd_main_impl<64>(p, grid, stream);
+}
+
+int bwd_block_m(int D) { return D == 128 ? BwdCfg<128>::BM : BwdCfg<64>::BM; }
+int bwd_block_n() { return 128; }
+
+}  // namespace attn_sm103

@@ -1,0 +1,111 @@
+// Kernel parameter blocks and the per-tile sequence decode shared by the forward and
+// backward kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sm103_ptx.cuh"
+
+namespace attn_sm103 {
+
+// Sequence addressing modes.
+enum : int { kDense = 0, kPadded = 1, kCompact = 2 };
+
+// Device status codes (same values as attn_status in include/attn.h).
+enum : int { kStatusBadSeqlens = 8, kStatusTimeout = 9 };
+
+// A bounded wait gives up after this long (a correct pipeline waits microseconds).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+struct SeqAddr {
+  const int* cu_q;  // int32 prefix sums (padded: [B+1], compact: [num_seqs+1]); null = dense
+  const int* cu_k;
+  int mode;         // kDense / kPadded / kCompact
+  int Sq, Sk;       // token extents of the tensors (dense/padded: S; compact: T)
+  int max_q, max_k; // grid bounds on per-sequence lengths
+};
+
+// Per-(batch or sequence) view: valid lengths, first row in the token axis, batch index of
+// the rank-4 tensors. Follows the AOTriton padded-varlen prologue: padded sequences start
+// at row 0 of their own batch; compact sequences start at cu[s] of the single batch.
+struct SeqView {
+  int len_q, len_k, row0_q, row0_k, batch;
+};
+
+// Returns false (and reports) when the cu_seqlens of unit z are inconsistent with the
+// tensors or the grid; the caller then skips the unit without touching memory.
+__device__ __forceinline__ bool decode_seq(const SeqAddr& a, int z, int* status, SeqView& v) {
+  if (a.mode == kDense) {
+    v.len_q = a.Sq; v.len_k = a.Sk; v.row0_q = 0; v.row0_k = 0; v.batch = z;
+    return true;
+  }
+  const int q0 = __ldg(a.cu_q + z), q1 = __ldg(a.cu_q + z + 1);
+  const int k0 = __ldg(a.cu_k + z), k1 = __ldg(a.cu_k + z + 1);
+  bool ok = q0 >= 0 && q1 >= q0 && k0 >= 0 && k1 >= k0;
+  v.len_q = q1 - q0;
+  v.len_k = k1 - k0;
+  if (a.mode == kPadded) {
+    ok = ok && v.len_q <= a.Sq && v.len_k <= a.Sk;
+    v.row0_q = 0; v.row0_k = 0; v.batch = z;
+  } else {
+    ok = ok && q1 <= a.Sq && k1 <= a.Sk && v.len_q <= a.max_q && v.len_k <= a.max_k;
+    v.row0_q = q0; v.row0_k = k0; v.batch = 0;
+  }
+  if (!ok && status != nullptr) atomicCAS(status, 0, kStatusBadSeqlens);
+  return ok;
+}
+
+struct FwdParams {
+  CUtensorMap tm_q, tm_k, tm_v;   // 4-D (D, S, H, B) bf16, box (64, 128, 1, 1), SW128
+  __nv_bfloat16* o;
+  int64_t o_sb, o_sh, o_ss;       // element strides of o (D stride is 1)
+  float* lse;
+  int64_t l_sb, l_sh, l_ss;
+  SeqAddr seq;
+  int causal;
+  float scale_log2;               // sm_scale * log2(e)
+  int* status;                    // device status word, may be null
+};
+
+struct BwdPreParams {
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dout;
+  int64_t o_sb, o_sh, o_ss, do_sb, do_sh, do_ss;
+  float* delta;                   // [B*H or H][rows] fp32, row index = token row
+  float* dq_acc;                  // [B*H or H][rows][D] fp32
+  int units, H, rows, D;          // units = B (dense/padded) or num_seqs (compact);
+                                  // rows = Sq (dense/padded) or Tq (compact)
+  SeqAddr seq;
+  int* status;
+};
+
+struct BwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 4-D maps; Q/dO box rows = BM, K/V box rows = BN
+  const float* lse;
+  int64_t l_sb, l_sh, l_ss;
+  const float* delta;             // [z-major][rows] as written by the preprocess kernel
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  int64_t dk_sb, dk_sh, dk_ss;
+  __nv_bfloat16* dv;
+  int64_t dv_sb, dv_sh, dv_ss;
+  int H, rows_q;                  // rows_q: per-(batch, head) row count of delta / dq_acc
+  SeqAddr seq;
+  int causal;
+  float scale_log2;               // sm_scale * log2(e)
+  float sm_scale;
+  int* status;
+};
+
+struct BwdPostParams {
+  const float* dq_acc;
+  __nv_bfloat16* dq;
+  int64_t dq_sb, dq_sh, dq_ss;
+  int units, H, rows, D;          // as in BwdPreParams
+  SeqAddr seq;
+  float sm_scale;
+};
+
+}  // namespace attn_sm103

@@ -1,0 +1,20 @@
+// Internal launch entry points between the C ABI (attn_api.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "attn_common.cuh"
+
+namespace attn_sm103 {
+
+// Forward: grid = (query tiles, H, B or num_seqs); query tiles of fwd_block_m() rows.
+int fwd_block_m();
+cudaError_t launch_attn_fwd(const FwdParams& p, int D, dim3 grid, cudaStream_t stream);
+
+// Backward stages.
+int bwd_block_m(int D);  // query rows per inner step of the main kernel
+int bwd_block_n();       // key rows per CTA of the main kernel
+cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdParams& p, int D, dim3 grid, cudaStream_t stream);
+cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream);
+
+}  // namespace attn_sm103

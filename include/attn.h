@@ -1,0 +1,201 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused scaled-dot-product attention library.
+ *
+ * The operation is FlashAttention-style scaled dot-product attention ("Investigate a new
+ * SDPA IR node", nvFuser issue #2278): for every (batch or sequence, head)
+ *
+ *     S = sm_scale * Q K^T,  P = softmax(S) over the visible keys,  O = P V,
+ *     LSE_i = log sum_j exp(S_ij)   (natural log, stored by the forward pass),
+ *
+ * and the backward pass rebuilds P from LSE to produce dQ, dK, dV of a loss whose gradient
+ * with respect to O is dO. The forward pass returns LSE because backward consumes it: the
+ * nvFuser page splits the op into a forward node that stashes what backward needs and a
+ * backward node that consumes it (SdpaOpFwd / SdpaOpBwd).
+ *
+ * Layout. Every tensor is rank 4, (B, H, S, D) ("BHSD", the only layout of the AOTriton
+ * flash API -- "Add varlen support to AOTriton's Flash Attention", last comment: new layouts
+ * get new APIs, not flags). Strides are in ELEMENTS and arbitrary, except that the D stride
+ * must be 1, the other strides must be multiples of 8 elements (16 bytes) and base pointers
+ * 16-byte aligned (tensor-memory-accelerator requirements). Q, K, V, O, dO, dQ, dK, dV are
+ * bf16; LSE is fp32 with shape (B, H, Sq). Q/K/V/O share B, H and D; seqlen_q and seqlen_k
+ * may differ ("[RFC] Goal for triton.ops.flash_attention" lists a different number of
+ * queries and keys as a missing case; the AOTriton issue #12 page states that QKVO share a
+ * dtype and shape except for seqlen_q vs seqlen_k). d_head must be 64 or 128.
+ *
+ * Masking. causal != 0 applies a top-left aligned mask: query i sees key j iff j <= i,
+ * indices local to the sequence. Keys at or past a sequence's length are never seen.
+ *
+ * Variable length (AOTriton PR #31, "Add varlen support to AOTriton's Flash Attention"):
+ *   - compact varlen: the *_compact_varlen calls; tensors are (1, H, T, D) -- a THD tensor
+ *     viewed with transpose + unsqueeze -- and sequence s owns rows [cu[s], cu[s+1]).
+ *     Batch must be exactly 1 (the page says extra batches are not processed; here they
+ *     are an error, never silently ignored).
+ *   - padded varlen: attn_fwd / attn_bwd with non-NULL cu_seqlens (or the *_padded_varlen
+ *     aliases); batch b is valid on rows [0, cu[b+1]-cu[b]) of its own (B, H, S, D) slice,
+ *     i.e. data starts at offset 0 inside each batch, as in the padded-varlen kernel
+ *     prologue quoted on that page.
+ *   All sequence-length arguments and cu_seqlens entries are int32 (same page, note 3).
+ *
+ * Output contract. Rows at or past a sequence's length are not written (the kernel
+ * prologue on the AOTriton page returns early for them). A sequence with no keys gets
+ * O = 0 and LSE = -inf on its valid rows and zero dQ.
+ *
+ * Ownership and asynchrony. The caller owns every buffer (inputs, outputs, workspace);
+ * the library allocates nothing and keeps no per-call state. Pointers passed as "device"
+ * must be device memory of the current device. Calls are asynchronous and ordered on the
+ * given CUDA stream (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *
+ * Errors. Argument errors are detected on the host, return a status != ATTN_OK and launch
+ * nothing ("no silently incorrect results": the RFC page above warns that the Triton demo
+ * can silently return wrong answers on unexpected shapes or strides). Errors only visible
+ * on the device (inconsistent cu_seqlens, a pipeline wait that timed out) are written to a
+ * status word at offset 0 of the workspace; read it with attn_read_device_status. A
+ * sequence whose cu_seqlens are inconsistent is skipped, never read out of bounds.
+ */
+#ifndef ATTN_SM103_ATTN_H_
+#define ATTN_SM103_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A rank-4 (B, H, S, D) tensor view; strides in elements. */
+typedef struct {
+  void* data;
+  int64_t size[4];
+  int64_t stride[4];
+} attn_tensor4;
+
+/* A rank-3 (B, H, S) fp32 tensor view (LSE); strides in elements. */
+typedef struct {
+  void* data;
+  int64_t size[3];
+  int64_t stride[3];
+} attn_tensor3;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = 1,          /* a required pointer is NULL */
+  ATTN_ERR_SHAPE = 2,         /* inconsistent sizes (B, H, D, S), or compact batch != 1 */
+  ATTN_ERR_STRIDE = 3,        /* D stride != 1, or a stride not a multiple of 8 elements */
+  ATTN_ERR_ALIGN = 4,         /* base pointer not 16-byte aligned */
+  ATTN_ERR_UNSUPPORTED = 5,   /* d_head not 64/128, device is not sm_103, or size limits */
+  ATTN_ERR_WORKSPACE = 6,     /* workspace NULL or smaller than the *_workspace_size value */
+  ATTN_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed (launch, tensor map) */
+  ATTN_ERR_DEVICE_BAD_SEQLENS = 8, /* device: cu_seqlens not monotone or past the tensor */
+  ATTN_ERR_DEVICE_TIMEOUT = 9 /* device: a bounded pipeline wait gave up */
+} attn_status;
+
+/* Workspace bytes needed by attn_fwd* for Q of shape (B, H, Sq, D) (compact: B = 1,
+ * Sq = total query tokens). Holds the device status word only. */
+size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D);
+
+/* Workspace bytes needed by attn_bwd* (status word, per-row Delta = rowsum(dO * O) in fp32,
+ * and an fp32 dQ accumulator of shape (B, H, Sq, D)). */
+size_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D);
+
+/*
+ * Forward pass, dense (cu_seqlens_q == cu_seqlens_k == NULL) or padded varlen (both
+ * non-NULL, int32 device arrays of B+1 prefix sums; only the differences are used).
+ *   q: (B, H, Sq, D) bf16     k, v: (B, H, Sk, D) bf16
+ *   o: (B, H, Sq, D) bf16 out lse: (B, H, Sq) fp32 out (natural-log logsumexp)
+ *   workspace: device, >= attn_fwd_workspace_size bytes (may be NULL with 0 bytes: device
+ *   errors are then not reported). stream: cudaStream_t.
+ */
+attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, float sm_scale,
+                     int causal, const attn_tensor4* o, const attn_tensor3* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward pass matching attn_fwd (same q, k, v, cu_seqlens, sm_scale, causal; o and lse
+ * as returned by attn_fwd). dout: (B, H, Sq, D) bf16. Writes dq (B, H, Sq, D), dk and dv
+ * (B, H, Sk, D), all bf16. workspace: device, >= attn_bwd_workspace_size bytes, required.
+ * Runs three kernels in stream order: attn_bwd_preprocess, attn_bwd_main and
+ * attn_bwd_dq_epilogue below.
+ */
+attn_status attn_bwd(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                     const attn_tensor4* o, const attn_tensor3* lse, const attn_tensor4* dout,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, float sm_scale,
+                     int causal, const attn_tensor4* dq, const attn_tensor4* dk,
+                     const attn_tensor4* dv, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* Compact varlen forward: q, o (1, H, Tq, D); k, v (1, H, Tk, D); lse (1, H, Tq).
+ * cu_seqlens_q / cu_seqlens_k: int32 device arrays of num_seqs+1 prefix sums into the
+ * token axis. max_seqlen_q / max_seqlen_k: host upper bounds on the sequence lengths, used
+ * only to size the grid (pass <= 0 to use Tq / Tk); a length above the bound is reported
+ * as ATTN_ERR_DEVICE_BAD_SEQLENS and that sequence is skipped. */
+attn_status attn_fwd_compact_varlen(const attn_tensor4* q, const attn_tensor4* k,
+                                    const attn_tensor4* v, const int32_t* cu_seqlens_q,
+                                    const int32_t* cu_seqlens_k, int32_t num_seqs,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k, float sm_scale,
+                                    int causal, const attn_tensor4* o, const attn_tensor3* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Compact varlen backward; arguments as in attn_fwd_compact_varlen and attn_bwd. */
+attn_status attn_bwd_compact_varlen(const attn_tensor4* q, const attn_tensor4* k,
+                                    const attn_tensor4* v, const attn_tensor4* o,
+                                    const attn_tensor3* lse, const attn_tensor4* dout,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                    int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                    float sm_scale, int causal, const attn_tensor4* dq,
+                                    const attn_tensor4* dk, const attn_tensor4* dv,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Padded varlen under its own name (the AOTriton page plans "attn_?wd_padded_varlen");
+ * identical to attn_fwd / attn_bwd except that cu_seqlens must be non-NULL. */
+attn_status attn_fwd_padded_varlen(const attn_tensor4* q, const attn_tensor4* k,
+                                   const attn_tensor4* v, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, float sm_scale, int causal,
+                                   const attn_tensor4* o, const attn_tensor3* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+attn_status attn_bwd_padded_varlen(const attn_tensor4* q, const attn_tensor4* k,
+                                   const attn_tensor4* v, const attn_tensor4* o,
+                                   const attn_tensor3* lse, const attn_tensor4* dout,
+                                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                   float sm_scale, int causal, const attn_tensor4* dq,
+                                   const attn_tensor4* dk, const attn_tensor4* dv,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The three stages of attn_bwd / attn_bwd_compact_varlen, callable one by one (timing,
+ * profiling). num_seqs < 0 selects the dense / padded form (cu_seqlens NULL = dense),
+ * num_seqs >= 0 the compact form. Each validates its own arguments like attn_bwd.
+ *  - attn_bwd_preprocess: Delta_i = sum_d dO_id * O_id into the workspace and zeroes the
+ *    fp32 dQ accumulator. Memory-bound.
+ *  - attn_bwd_main: recomputes P from LSE per key tile, accumulates dK and dV in tensor
+ *    memory and writes them, and adds dS K into the dQ accumulator.
+ *  - attn_bwd_dq_epilogue: dq = bf16(sm_scale * accumulator). Memory-bound.
+ */
+attn_status attn_bwd_preprocess(const attn_tensor4* o, const attn_tensor4* dout,
+                                const int32_t* cu_seqlens_q, int32_t num_seqs,
+                                int32_t max_seqlen_q, void* workspace, size_t workspace_bytes,
+                                void* stream);
+attn_status attn_bwd_main(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                          const attn_tensor3* lse, const attn_tensor4* dout,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                          float sm_scale, int causal, const attn_tensor4* dk,
+                          const attn_tensor4* dv, void* workspace, size_t workspace_bytes,
+                          void* stream);
+attn_status attn_bwd_dq_epilogue(const attn_tensor4* dq, const int32_t* cu_seqlens_q,
+                                 int32_t num_seqs, int32_t max_seqlen_q, float sm_scale,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Reads the device status word at offset 0 of `workspace` after synchronising `stream`
+ * (the only blocking call of the library) and clears it. *out receives ATTN_OK or one of
+ * the ATTN_ERR_DEVICE_* codes. */
+attn_status attn_read_device_status(void* workspace, void* stream, int32_t* out);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(attn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SM103_ATTN_H_ */

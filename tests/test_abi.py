@@ -1,0 +1,170 @@
+"""The C ABI library on the CPU (no GPU needed): it loads, exports every function that
+include/attn.h declares, and rejects invalid arguments on the host with the documented
+status codes before any CUDA call. No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_flashattention_fwd_02_gb300 import _lib
+from attention_flashattention_fwd_02_gb300 import build as _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+ATTN_OK, ERR_NULL, ERR_SHAPE, ERR_STRIDE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE = range(7)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_build.lib_path()):
+        _build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(attn_[a-z0-9_]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 13
+    assert sorted(_lib.EXPORTED_SYMBOLS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(10):
+        assert _lib.attn_status_string(s)
+    assert _lib.attn_status_string(0) == "ok"
+
+
+def test_workspace_sizes(lib):
+    assert _lib.attn_fwd_workspace_size(2, 3, 100, 64) >= 4
+    B, H, S, D = 2, 3, 100, 64
+    n = _lib.attn_bwd_workspace_size(B, H, S, D)
+    # status word + Delta (fp32 per row) + fp32 dQ accumulator
+    assert n >= 4 + B * H * S * 4 + B * H * S * D * 4
+    assert _lib.attn_bwd_workspace_size(0, 3, 100, 64) >= 4
+
+
+# ------------------------------------------------------------------ host-side validation
+FAKE = 1 << 40  # an aligned, never-dereferenced address: validation fails before any use
+
+
+def t4(shape, stride=None, ptr=FAKE):
+    if stride is None:
+        stride = [shape[1] * shape[2] * shape[3], shape[2] * shape[3], shape[3], 1]
+    v = _lib.Tensor4()
+    v.data = ptr
+    v.size[:] = list(shape)
+    v.stride[:] = list(stride)
+    return v
+
+
+def t3(shape, ptr=FAKE):
+    v = _lib.Tensor3()
+    v.data = ptr
+    v.size[:] = list(shape)
+    v.stride[:] = [shape[1] * shape[2], shape[2], 1]
+    return v
+
+
+def call_fwd(lib, q, k, v, o, lse, scale=0.125, cu_q=None, cu_k=None):
+    r = ctypes.byref
+    return lib.attn_fwd(r(q), r(k), r(v), cu_q, cu_k, scale, 0, r(o), r(lse), None, 0, None)
+
+
+GOOD = (1, 2, 128, 64)
+
+
+def good():
+    return t4(GOOD), t4(GOOD), t4(GOOD), t4(GOOD), t3(GOOD[:3])
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("null_q", ERR_NULL),
+    ("d_stride", ERR_STRIDE),
+    ("s_stride_not_mult8", ERR_STRIDE),
+    ("misaligned", ERR_ALIGN),
+    ("d_head_96", ERR_UNSUPPORTED),
+    ("kv_shape", ERR_SHAPE),
+    ("o_shape", ERR_SHAPE),
+    ("lse_shape", ERR_SHAPE),
+    ("neg_scale", ERR_UNSUPPORTED),
+    ("nan_scale", ERR_UNSUPPORTED),
+    ("one_cu_null", ERR_NULL),
+])
+def test_fwd_rejects(lib, case, expect):
+    q, k, v, o, lse = good()
+    scale, cu_q, cu_k = 0.125, None, None
+    if case == "null_q":
+        q = t4(GOOD, ptr=0)
+    elif case == "d_stride":
+        q = t4(GOOD, stride=[128 * 64 * 2, 128 * 64, 64, 2])
+    elif case == "s_stride_not_mult8":
+        q = t4(GOOD)
+        q.stride[2] = 65
+    elif case == "misaligned":
+        q = t4(GOOD, ptr=FAKE + 8)
+    elif case == "d_head_96":
+        q, k, v, o = (t4((1, 2, 128, 96)) for _ in range(4))
+    elif case == "kv_shape":
+        v = t4((1, 2, 64, 64))
+    elif case == "o_shape":
+        o = t4((1, 2, 64, 64))
+    elif case == "lse_shape":
+        lse = t3((1, 2, 64))
+    elif case == "neg_scale":
+        scale = -0.1
+    elif case == "nan_scale":
+        scale = float("nan")
+    elif case == "one_cu_null":
+        cu_q = FAKE
+    assert call_fwd(lib, q, k, v, o, lse, scale, cu_q, cu_k) == expect
+
+
+def test_compact_requires_batch_one(lib):
+    r = ctypes.byref
+    q = t4((2, 2, 64, 64))
+    st = lib.attn_fwd_compact_varlen(r(q), r(q), r(q), FAKE, FAKE, 1, 0, 0, 0.125, 1, r(q),
+                                     r(t3((2, 2, 64))), None, 0, None)
+    assert st == ERR_SHAPE
+    q = t4((1, 2, 64, 64))
+    st = lib.attn_fwd_compact_varlen(r(q), r(q), r(q), None, FAKE, 1, 0, 0, 0.125, 1, r(q),
+                                     r(t3((1, 2, 64))), None, 0, None)
+    assert st == ERR_NULL
+
+
+def test_bwd_workspace_checked(lib):
+    r = ctypes.byref
+    q = t4(GOOD)
+    lse = t3(GOOD[:3])
+    st = lib.attn_bwd(r(q), r(q), r(q), r(q), r(lse), r(q), None, None, 0.125, 0, r(q), r(q),
+                      r(q), None, 0, None)
+    assert st == ERR_WORKSPACE
+    st = lib.attn_bwd(r(q), r(q), r(q), r(q), r(lse), r(q), None, None, 0.125, 0, r(q), r(q),
+                      r(q), FAKE, 16, None)
+    assert st == ERR_WORKSPACE
+
+
+def test_padded_alias_requires_cu(lib):
+    r = ctypes.byref
+    q, k, v, o, lse = good()
+    st = lib.attn_fwd_padded_varlen(r(q), r(k), r(v), None, None, 0.125, 1, r(o), r(lse),
+                                    None, 0, None)
+    assert st == ERR_NULL
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """The product path has no fallback: without the built library every call raises."""
+    monkeypatch.setattr(_lib, "_LIB", None)
+    monkeypatch.setattr(_build, "BUILD", str(tmp_path))
+    with pytest.raises(RuntimeError, match="not found"):
+        _lib.load()
