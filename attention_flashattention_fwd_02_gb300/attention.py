@@ -40,7 +40,7 @@ def forward(q, k, v, sm_scale: Optional[float] = None, causal: bool = False,
 def bwd_workspace(q: torch.Tensor) -> torch.Tensor:
     B, H, S, D = q.shape
     n = _lib.attn_bwd_workspace_size(B, H, S, D)
-    return torch.empty(n, dtype=torch.uint8, device=q.device)
+    return torch.zeros(n, dtype=torch.uint8, device=q.device)  # status word starts at 0
 
 
 def backward(q, k, v, o, lse, do, sm_scale: Optional[float] = None, causal: bool = False,

@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Attention fwd+bwd throughput on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole path over the workload's batch: for every mask variant of
+the workload, the forward kernel, then the backward preprocess, main and dQ-epilogue
+kernels. ``value`` is algorithmic TFLOPS (fwd 4*D*pairs + bwd 10*D*pairs over the unmasked
+(query, key) pairs), device-timed with CUDA events around each step, inputs resident in HBM
+and L2 flushed (256 MiB write) before every step. ``e2e`` is the same metric through the
+public API with pinned host buffers, host<->device copies inside the timed region.
+
+``--impl reference`` times the float64 CPU oracle on the host cores instead (bounded sample
+of the same workload per step). Under torchrun each rank runs the same per-GPU workload
+(independent replicas, weak scaling); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
+# Workloads a bench line can be quoted on: name -> mask variants run in one step.
+BENCH_WORKLOADS = {
+    "dense2048": ("dense2048", "dense2048_causal"),
+    "cross": ("cross",),
+    "compact": ("compact",),
+    "padded": ("padded",),
+    "sweep4k": ("sweep4k", "sweep4k_causal"),
+    "sweep8k": ("sweep8k", "sweep8k_causal"),
+    "sweep16k": ("sweep16k", "sweep16k_causal"),
+}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="dense2048")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--settle-s", type=float, default=1.0,
+                    help="seconds of untimed steps before the timed region (clock settling)")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def flops_of(wl, x):
+    from attention_flashattention_fwd_02_gb300.workloads import unmasked_pairs
+    if wl.layout in ("compact", "padded"):
+        pairs = wl.H * sum(unmasked_pairs(int(n), int(n), wl.causal) for n in x["lengths"])
+    else:
+        pairs = wl.B * wl.H * unmasked_pairs(wl.Sq, wl.Sk, wl.causal)
+    return 4 * wl.D * pairs, 10 * wl.D * pairs
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [s for s in sm if mx is None or s > 0.3 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, dist):
+    import torch
+
+    from attention_flashattention_fwd_02_gb300 import _lib
+    from attention_flashattention_fwd_02_gb300.workloads import WORKLOADS, make_inputs
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    dev = torch.device("cuda")
+    _lib.load()
+    stream = torch.cuda.current_stream()
+    variants = []
+    for name in BENCH_WORKLOADS[args.workload]:
+        wl = WORKLOADS[name]
+        x = make_inputs(wl, seed=wl.seed + 7919 * rank)
+        f_fwd, f_bwd = flops_of(wl, x)
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+        q, k, v, do = g["q"], g["k"], g["v"], g["do"]
+        o = torch.empty(q.shape, dtype=q.dtype, device=dev)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.zeros(_lib.attn_bwd_workspace_size(*q.shape), dtype=torch.uint8, device=dev)
+        compact = wl.layout == "compact"
+        padded = wl.layout == "padded"
+        cu_q = g.get("cu_seqlens_q")
+        cu_k = g.get("cu_seqlens_k")
+        nseq = (cu_q.numel() - 1) if compact else -1
+        maxl = int(x["lengths"].max()) if compact else 0
+        variants.append(dict(wl=wl, x=x, q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv,
+                             ws=ws, compact=compact, padded=padded, cu_q=cu_q, cu_k=cu_k,
+                             nseq=nseq, maxl=maxl, f_fwd=f_fwd, f_bwd=f_bwd))
+
+    def launch(vt, kern):
+        wl = vt["wl"]
+        sc, cz = wl.sm_scale, wl.causal
+        if kern == "fwd":
+            if vt["compact"]:
+                _lib.attn_fwd_compact_varlen(vt["q"], vt["k"], vt["v"], vt["o"], vt["lse"],
+                                             vt["cu_q"], vt["cu_k"], vt["nseq"], vt["maxl"],
+                                             vt["maxl"], sc, cz, vt["ws"])
+            else:
+                _lib.attn_fwd(vt["q"], vt["k"], vt["v"], vt["o"], vt["lse"], sc, cz,
+                              vt["cu_q"], vt["cu_k"], vt["ws"])
+        elif kern == "bwd_pre":
+            _lib.attn_bwd_preprocess(vt["o"], vt["do"], vt["ws"], vt["cu_q"], vt["nseq"], vt["maxl"])
+        elif kern == "bwd_main":
+            _lib.attn_bwd_main(vt["q"], vt["k"], vt["v"], vt["lse"], vt["do"], vt["dk"], vt["dv"],
+                               sc, cz, vt["ws"], vt["cu_q"], vt["cu_k"], vt["nseq"], vt["maxl"],
+                               vt["maxl"])
+        elif kern == "bwd_post":
+            _lib.attn_bwd_dq_epilogue(vt["dq"], sc, vt["ws"], vt["cu_q"], vt["nseq"], vt["maxl"])
+
+    KERNELS = ("fwd", "bwd_pre", "bwd_main", "bwd_post")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(events=None):
+        for vi, vt in enumerate(variants):
+            for kern in KERNELS:
+                if events is not None:
+                    events[(vi, kern)][0].record(stream)
+                launch(vt, kern)
+                if events is not None:
+                    events[(vi, kern)][1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    # keep the GPU busy ~1 s before the timed region so that clocks settle
+    t_end = time.time() + args.settle_s
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) if rank == 0 else None
+    time.sleep(0.3)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    step_ev = [(ev(), ev()) for _ in range(args.steps)]
+    kern_ev = [{(vi, kn): (ev(), ev()) for vi in range(len(variants)) for kn in KERNELS}
+               for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)  # evict the previous step's data from L2 (untimed)
+        step_ev[i][0].record(stream)
+        step(kern_ev[i])
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+
+    step_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    ktime = {}
+    for kn in KERNELS:
+        for vi in range(len(variants)):
+            ktime[(vi, kn)] = sum(kern_ev[i][(vi, kn)][0].elapsed_time(kern_ev[i][(vi, kn)][1])
+                                  for i in range(args.steps))
+    total_ms = step_ms
+    if dist is not None:
+        import torch.distributed as tdist
+        t = torch.tensor([total_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    flops_step = sum(vt["f_fwd"] + vt["f_bwd"] for vt in variants)
+    value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+    peak_b, peak_s, _, peak_src = peaks()
+
+    # per-kernel roofline figures (tensor-bound kernels: algorithmic flops / event time)
+    per_kernel = {}
+    for kn in KERNELS:
+        ms = sum(ktime[(vi, kn)] for vi in range(len(variants)))
+        per_kernel[kn] = ms
+    fwd_fl = sum(vt["f_fwd"] for vt in variants) * args.steps
+    bwd_fl = sum(vt["f_bwd"] for vt in variants) * args.steps
+    dominant = max(("fwd", "bwd_main"), key=lambda k: per_kernel[k])
+    dom_fl = fwd_fl if dominant == "fwd" else bwd_fl
+    achieved = dom_fl / (per_kernel[dominant] * 1e-3) / 1e12
+    traffic = load_traffic(args.workload, dominant)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs rounded to bf16)",
+        "config": workload_config(args.workload, variants),
+        "roofline": {"bound": "tensor", "kernel": "attn_" + dominant, "achieved": round(achieved, 2),
+                     "peak": peak_b, "unit": "TFLOP/s", "frac": round(achieved / peak_b, 4),
+                     "peak_source": f"{peak_src} bf16 burst", "traffic": traffic,
+                     "frac_of_sustained": round(achieved / peak_s, 4)},
+        "kernels": {
+            "fwd_tflops": round(fwd_fl / (per_kernel["fwd"] * 1e-3) / 1e12, 2),
+            "bwd_main_tflops": round(bwd_fl / (per_kernel["bwd_main"] * 1e-3) / 1e12, 2),
+            "bwd_tflops": round(bwd_fl / (sum(per_kernel[k] for k in KERNELS[1:]) * 1e-3) / 1e12, 2),
+            "fwd_frac_of_peak": round(fwd_fl / (per_kernel["fwd"] * 1e-3) / 1e12 / peak_b, 4),
+            "bwd_frac_of_peak": round(bwd_fl / (sum(per_kernel[k] for k in KERNELS[1:]) * 1e-3)
+                                      / 1e12 / peak_b, 4),
+            "ms_per_step": {k: round(per_kernel[k] / args.steps, 4) for k in KERNELS},
+        },
+        "gpu_launches": len(variants) * len(KERNELS) * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, variants, launch, KERNELS, stream, dist, world)
+    return result
+
+
+def load_traffic(workload, dominant):
+    """DRAM bytes per launch from a committed ncu summary (profiles/), or None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))
+        return d.get(workload, {}).get(dominant)
+    except Exception:
+        return None
+
+
+def workload_config(name, variants):
+    wl = variants[0]["wl"]
+    cfg = {"workload": name, "B": wl.B, "H": wl.H, "d_head": wl.D,
+           "masks": ["causal" if vt["wl"].causal else "non-causal" for vt in variants],
+           "layout": wl.layout, "l2": "flushed before every step (256 MiB write)"}
+    if wl.layout in ("compact", "padded"):
+        cfg["lengths"] = [int(n) for n in variants[0]["x"]["lengths"]]
+        if wl.layout == "padded":
+            cfg["S_max"] = wl.Sq
+    else:
+        cfg["seqlen_q"], cfg["seqlen_k"] = wl.Sq, wl.Sk
+    return cfg
+
+
+def run_e2e(args, variants, launch, kernels, stream, dist, world):
+    """Same metric through the public API from pinned host buffers: H2D of q, k, v, dO
+    (and cu_seqlens), the whole path, D2H of o, lse, dq, dk, dv; all inside the events."""
+    import torch
+
+    host = []
+    h2d = d2h = 0
+    for vt in variants:
+        hv = {}
+        for n in ("q", "k", "v", "do"):
+            hv[n] = torch.empty_like(vt[n], device="cpu").pin_memory()
+            hv[n].copy_(vt[n])
+            h2d += vt[n].numel() * vt[n].element_size()
+        for n in ("o", "lse", "dq", "dk", "dv"):
+            hv["out_" + n] = torch.empty(vt[n].shape, dtype=vt[n].dtype).pin_memory()
+            d2h += vt[n].numel() * vt[n].element_size()
+        if vt["cu_q"] is not None:
+            hv["cu_q"] = vt["cu_q"].cpu().pin_memory()
+            hv["cu_k"] = vt["cu_k"].cpu().pin_memory()
+            h2d += 2 * vt["cu_q"].numel() * 4
+        host.append(hv)
+
+    def e2e_step():
+        for vt, hv in zip(variants, host):
+            for n in ("q", "k", "v", "do"):
+                vt[n].copy_(hv[n], non_blocking=True)
+            if vt["cu_q"] is not None:
+                vt["cu_q"].copy_(hv["cu_q"], non_blocking=True)
+                vt["cu_k"].copy_(hv["cu_k"], non_blocking=True)
+            for kern in kernels:
+                launch(vt, kern)
+            for n in ("o", "lse", "dq", "dk", "dv"):
+                hv["out_" + n].copy_(vt[n], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    a.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if dist is not None:
+        import torch.distributed as tdist
+        t = torch.tensor([ms], device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms = float(t.item())
+    fl = sum(vt["f_fwd"] + vt["f_bwd"] for vt in variants) * steps * world
+    return {"value": round(fl / (ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+def oracle_sample(workload, budget_s=12.0, seed_offset=0):
+    """Times the float64 oracle on whole heads of the workload until ~budget_s of CPU work;
+    returns (TFLOPS, seconds, description)."""
+    import numpy as np
+
+    from attention_flashattention_fwd_02_gb300.workloads import WORKLOADS, make_inputs, unmasked_pairs
+    from oracle import attention_ref as ref
+
+    t_total, fl_total, n_heads = 0.0, 0.0, 0
+    variants = BENCH_WORKLOADS[workload]
+    inputs = {name: make_inputs(WORKLOADS[name]) for name in variants}
+    h = 0
+    while t_total < budget_s and n_heads < 64:
+        for name in variants:
+            wl = WORKLOADS[name]
+            x = inputs[name]
+            if wl.layout == "compact":
+                cu = x["cu_seqlens_q"].numpy()
+                s = h % (len(cu) - 1)
+                a, b = int(cu[s]), int(cu[s + 1])
+                sl = lambda t: t[0, (h + seed_offset) % wl.H, a:b].double().numpy()
+                n_q = n_k = b - a
+            elif wl.layout == "padded":
+                bi = h % wl.B
+                n = int(x["lengths"][bi])
+                sl = lambda t: t[bi, (h + seed_offset) % wl.H, :n].double().numpy()
+                n_q = n_k = n
+            else:
+                bi = h % wl.B
+                sl = lambda t: t[bi, (h + seed_offset) % wl.H].double().numpy()
+                n_q, n_k = wl.Sq, wl.Sk
+            Q, K, V, dO = (sl(x[nm]) for nm in ("q", "k", "v", "do"))
+            t0 = time.perf_counter()
+            ref.attention_forward(Q, K, V, wl.sm_scale, wl.causal)
+            ref.attention_backward(Q, K, V, dO, wl.sm_scale, wl.causal)
+            t_total += time.perf_counter() - t0
+            fl_total += 14 * wl.D * unmasked_pairs(n_q, n_k, wl.causal)
+        n_heads += 1
+        h += 1
+    desc = (f"{n_heads} head(s) per mask variant of {workload} (fwd+bwd, float64 NumPy oracle), "
+            f"{t_total:.1f} s")
+    return fl_total / t_total / 1e12, t_total, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step times one bounded sample."""
+    per_step_budget = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, budget_s=per_step_budget / 4)
+    vals, secs = [], 0.0
+    desc = ""
+    for i in range(args.steps):
+        v, s, desc = oracle_sample(args.workload, budget_s=per_step_budget, seed_offset=i)
+        vals.append(v)
+        secs += s
+    value = statistics.mean(vals)
+    cores = cpu_cores()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / max(1, args.steps) * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# --------------------------------------------------------------------------- main
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    result = run_ours(args, rank, world, dist)
+    if rank == 0 and not args.no_cpu_baseline:
+        v, s, desc = oracle_sample(args.workload)
+        result["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOPS", "cores": cpu_cores(),
+                                  "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

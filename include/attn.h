@@ -49,8 +49,10 @@
  * nothing ("no silently incorrect results": the RFC page above warns that the Triton demo
  * can silently return wrong answers on unexpected shapes or strides). Errors only visible
  * on the device (inconsistent cu_seqlens, a pipeline wait that timed out) are written to a
- * status word at offset 0 of the workspace; read it with attn_read_device_status. A
- * sequence whose cu_seqlens are inconsistent is skipped, never read out of bounds.
+ * status word (int32) at offset 0 of the workspace; read it with attn_read_device_status.
+ * The word is sticky: kernels only ever set it, so the caller zeroes it once when the
+ * workspace is allocated, and attn_read_device_status clears it after reading. A sequence
+ * whose cu_seqlens are inconsistent is skipped, never read out of bounds.
  */
 #ifndef ATTN_SM103_ATTN_H_
 #define ATTN_SM103_ATTN_H_
