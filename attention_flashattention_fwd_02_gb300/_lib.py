@@ -21,14 +21,14 @@ __all__ = [
     "attn_fwd_padded_varlen", "attn_bwd_padded_varlen",
     "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_dq_epilogue",
     "attn_fwd_workspace_size", "attn_bwd_workspace_size",
-    "attn_read_device_status", "attn_status_string", "EXPORTED_SYMBOLS",
+    "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "attn_fwd_workspace_size", "attn_bwd_workspace_size", "attn_fwd", "attn_bwd",
     "attn_fwd_compact_varlen", "attn_bwd_compact_varlen", "attn_fwd_padded_varlen",
     "attn_bwd_padded_varlen", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_dq_epilogue",
-    "attn_read_device_status", "attn_status_string",
+    "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
 )
 
 
@@ -75,6 +75,7 @@ _SIGS = {
                             VP, SZ, VP]),
     "attn_bwd_dq_epilogue": (INT, [P4, I32P, I32, I32, F32, VP, SZ, VP]),
     "attn_read_device_status": (INT, [VP, VP, ctypes.POINTER(I32)]),
+    "attn_bwd_noalloc": (INT, [P4, P4, P4, P4, P3, P4, I32P, I32P, F32, INT, P4, P4, P4, VP]),
     "attn_status_string": (ctypes.c_char_p, [INT]),
 }
 
@@ -271,3 +272,15 @@ def attn_read_device_status(workspace, stream=None) -> int:
     _check(load().attn_read_device_status(workspace.data_ptr(), _stream(stream),
                                           ctypes.byref(out)), "attn_read_device_status")
     return int(out.value)
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, cu_seqlens_q=None,
+                     cu_seqlens_k=None, stream=None):
+    """attn_bwd without a workspace argument: the library's fixed device scratch array is
+    used (for callers that cannot allocate; see include/attn.h)."""
+    _bf16(q, k, v, o, dout, dq, dk, dv)
+    tq, tk, tv, to, tl, tdo = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse), _t4(dout)
+    tdq, tdk, tdv = _t4(dq), _t4(dk), _t4(dv)
+    _check(load().attn_bwd_noalloc(*_keep(tq, tk, tv, to, tl, tdo), _ptr(cu_seqlens_q),
+                                   _ptr(cu_seqlens_k), float(sm_scale), int(bool(causal)),
+                                   *_keep(tdq, tdk, tdv), _stream(stream)), "attn_bwd_noalloc")

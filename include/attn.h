@@ -188,6 +188,28 @@ attn_status attn_bwd_dq_epilogue(const attn_tensor4* dq, const int32_t* cu_seqle
                                  int32_t num_seqs, int32_t max_seqlen_q, float sm_scale,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Backward pass for callers that cannot allocate device memory (allocator-free runtimes,
+ * plugins that may not allocate while executing, fixed up-front memory budgets). The pages
+ * have no counterpart of this entry point; it exists for such callers only.
+ * Same arguments and results as attn_bwd (dense or padded varlen), without a workspace:
+ * the scratch space (status word, Delta, fp32 dQ accumulator) comes from a fixed array of
+ * ATTN_NOALLOC_SCRATCH_BYTES in the library's own device memory, which every GPU that loads
+ * the library holds until the process exits. Nothing is allocated. Returns
+ * ATTN_ERR_WORKSPACE when attn_bwd_workspace_size(B, H, Sq, D) exceeds that size. The first
+ * call on each device looks up the array's device address (with that device current) and
+ * should come before any stream capture. All calls share the array: calls whose executions
+ * overlap on the GPU race. Device-side errors are not observable through this call (its
+ * status word is cleared at the start of every call).
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+attn_status attn_bwd_noalloc(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                             const attn_tensor4* o, const attn_tensor3* lse,
+                             const attn_tensor4* dout, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, float sm_scale, int causal,
+                             const attn_tensor4* dq, const attn_tensor4* dk,
+                             const attn_tensor4* dv, void* stream);
+
 /* Reads the device status word at offset 0 of `workspace` after synchronising `stream`
  * (the only blocking call of the library) and clears it. *out receives ATTN_OK or one of
  * the ATTN_ERR_DEVICE_* codes. */
