@@ -14,11 +14,14 @@
 //                            LSE that the forward pass stashed.
 //  3. attn_bwd_post_kernel   dQ = bf16(sm_scale * accumulator). Memory-bound.
 //
-// Main-kernel warp roles (320 threads): warps 0..3 compute P^T / dS^T (thread j owns key row
-// j = TMEM lane j) and write dK / dV at the end; warps 4..7 drain the dQ partial from TMEM
-// into the global accumulator; warp 8 is the TMA producer; warp 9 allocates TMEM and issues
-// the MMAs. Tile sizes: 128 keys per CTA; 64 query rows per step when d_head = 128 (dQ is
-// formed transposed, K_n^T dS^T, so that every MMA has M = 128), 128 when d_head = 64.
+// Main-kernel warp roles (448 threads): warps 0..7 are two compute warpgroups that split
+// the query columns of each key row (thread row j = TMEM lane j) to form P^T (written to
+// TMEM, where it is the A operand of the dV MMA) and dS^T (written to shared memory for the
+// dK and dQ MMAs), and write dK / dV at the end; warps 8..11 drain the dQ partial from TMEM
+// into the global fp32 accumulator with fire-and-forget reductions; warp 12 is the TMA
+// producer; warp 13 allocates TMEM and issues the MMAs. Tile sizes: 128 keys per CTA; 64
+// query rows per step when d_head = 128 (dQ is formed transposed, K_n^T dS^T, so that every
+// MMA has M = 128), 128 when d_head = 64.
 #include "attn_common.cuh"
 #include "attn_launch.h"
 
@@ -121,41 +124,56 @@ cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream) 
 // =========================================================================== main kernel
 template <int D>
 struct BwdCfg {
-  static constexpr int BN = 128;                 // keys per CTA (MMA M for S^T, dP^T, dK, dV)
+  static constexpr int BN = 128;                    // keys per CTA (MMA M for S^T, dP^T, dK, dV)
   static constexpr int BM = (D == 128) ? 64 : 128;  // query rows per step
-  static constexpr bool DQ_T = (D == 128);       // dQ^T = K^T dS^T (M = D) vs dQ = dS K (M = BM)
+  static constexpr bool DQ_T = (D == 128);          // dQ^T = K^T dS^T (M = D) vs dQ = dS K (M = BM)
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int Q_BYTES = BM * D * 2;
-  static constexpr int P_BYTES = BN * BM * 2;
+  static constexpr int DS_BYTES = BN * BM * 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;   // 2 stages
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;      // 2 stages
   static constexpr int OFF_DO = OFF_Q + 2 * Q_BYTES;  // 2 stages
-  static constexpr int OFF_P = OFF_DO + 2 * Q_BYTES;
-  static constexpr int OFF_DS = OFF_P + P_BYTES;
-  static constexpr int SMEM_BYTES = OFF_DS + P_BYTES + 1024;
+  static constexpr int OFF_DS = OFF_DO + 2 * Q_BYTES; // 2 buffers
+  static constexpr int SMEM_BYTES = OFF_DS + 2 * DS_BYTES + 1024;
+  // TMEM columns: dK, dV accumulators; S^T, dP^T of the current step; the dQ partial; and P^T
+  // (bf16, two values per column) as the A operand of the dV MMA.
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_DK = 0, COL_DV = D, COL_S = 2 * D, COL_DP = 2 * D + BM,
-                            COL_DQ = 384;
-  static_assert(2 * D + 2 * BM <= 384, "TMEM layout overlaps");
-  static constexpr int NTHREADS = 320;
+  static constexpr uint32_t COL_DK = 0, COL_DV = D, COL_S = 2 * D, COL_DP = 2 * D + BM;
+  static constexpr uint32_t COL_DQ = 2 * D + 2 * BM;
+  static constexpr uint32_t COL_P = COL_DQ + (DQ_T ? BM : D);
+  static_assert(COL_P + BM / 2 <= TMEM_COLS, "TMEM layout does not fit");
+  static constexpr int NTHREADS = 448;  // 2 compute WGs, 1 dQ-drain WG, producer, MMA
+  static constexpr int WARP_PRODUCER = 12, WARP_MMA = 13;
 };
 
 template <int BM>
 struct BwdBars {
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2];
-  uint64_t s_full, s_empty, p_full, p_empty, dq_full, dq_empty, dkdv_full;
+  uint64_t s_full, p_full;
+  uint64_t ds_full[2], ds_empty[2];
+  uint64_t dq_full, dq_empty, dkdv_full;
   uint32_t tmem_base;
   int abort;
-  float lse2[2][BM];
-  float delta[2][BM];
+  alignas(16) float lse2[2][BM];
+  alignas(16) float delta[2][BM];
 };
 
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int BN = C::BN, BM = C::BM;
+  constexpr int HALF = BM / 2;  // score columns per compute warpgroup
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdBars<BM> bars;
 
@@ -172,7 +190,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
   const int64_t zh = (int64_t)sv.batch * p.H + h;
 
   if (n_steps == 0) {  // no query sees these keys: dK = dV = 0
-    if (warp < 4) {
+    if (threadIdx.x < BN) {
       const int key = k_lo + threadIdx.x;
       if (key < sv.len_k) {
         const int64_t grow = sv.row0_k + key;
@@ -190,7 +208,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
   uint8_t* smem = align1024b(smem_raw);
   const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
   const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
-  const uint32_t sP = smem_u32(smem + C::OFF_P), sDS = smem_u32(smem + C::OFF_DS);
+  const uint32_t sDS = smem_u32(smem + C::OFF_DS);
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
@@ -198,17 +216,17 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.q_full[s]), 33);  // producer lane 0 (tx) + 32 lanes (LSE/Delta)
       mbar_init(smem_u32(&bars.q_empty[s]), 1);
+      mbar_init(smem_u32(&bars.ds_full[s]), 256);
+      mbar_init(smem_u32(&bars.ds_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars.s_full), 1);
-    mbar_init(smem_u32(&bars.s_empty), 128);
-    mbar_init(smem_u32(&bars.p_full), 128);
-    mbar_init(smem_u32(&bars.p_empty), 1);
+    mbar_init(smem_u32(&bars.p_full), 256);
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_empty), 128);
     mbar_init(smem_u32(&bars.dkdv_full), 1);
     mbar_fence_init();
   }
-  if (warp == 9) {
+  if (warp == C::WARP_MMA) {
     tmem_alloc(smem_u32(&bars.tmem_base), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -218,7 +236,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort = &bars.abort;
 
-  if (warp == 8) {
+  if (warp == C::WARP_PRODUCER) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_map(&p.tm_q);
@@ -263,69 +281,75 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       }
       mbar_arrive(qb);
     }
-  } else if (warp == 9) {
+  } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
+    // Issue order per step: dV(it) [P from TMEM], S/dP(it+1), dK(it), dQ(it). The S/dP MMAs
+    // of the next step overlap the P/dS math of the compute warpgroups.
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, BM, false, false);   // S^T, dP^T
-      constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);     // dV, dK
-      constexpr uint32_t idQ = C::DQ_T ? idesc_bf16_f32(128, BM, true, true)   // dQ^T
-                                       : idesc_bf16_f32(128, D, true, true);   // dQ
-      const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP;
+      constexpr uint32_t idS = idesc_bf16_f32(128, BM, false, false);  // S^T, dP^T
+      constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);    // dV, dK
+      constexpr uint32_t idQ = C::DQ_T ? idesc_bf16_f32(128, BM, true, true)  // dQ^T
+                                       : idesc_bf16_f32(128, D, true, true);  // dQ
+      const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP, tP = tmem + C::COL_P;
       const uint32_t tDK = tmem + C::COL_DK, tDV = tmem + C::COL_DV, tDQ = tmem + C::COL_DQ;
-      bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort, kWaitTimeoutNs);
-      for (int it = 0; ok && it <= n_steps; ++it) {
-        if (it < n_steps) {
-          const int st = it & 1;
-          if (!mbar_wait(smem_u32(&bars.q_full[st]), (it >> 1) & 1, abort, kWaitTimeoutNs)) break;
-          if (it > 0 && !mbar_wait(smem_u32(&bars.s_empty), (it - 1) & 1, abort, kWaitTimeoutNs))
-            break;
-          tc_fence_after();
-          const uint32_t q = sQ + st * C::Q_BYTES, dO = sDO + st * C::Q_BYTES;
+      auto issue_sdp = [&](int it) -> bool {
+        const int st = it & 1;
+        if (!mbar_wait(smem_u32(&bars.q_full[st]), (it >> 1) & 1, abort, kWaitTimeoutNs))
+          return false;
+        tc_fence_after();
+        const uint32_t q = sQ + st * C::Q_BYTES, dO = sDO + st * C::Q_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tS, desc_kmajor(sK, BN, kk), desc_kmajor(q, BM, kk), idS, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tS, desc_kmajor(sK, BN, kk), desc_kmajor(q, BM, kk), idS, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tDP, desc_kmajor(sV, BN, kk), desc_kmajor(dO, BM, kk), idS, kk > 0);
-          umma_commit(smem_u32(&bars.s_full));
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tDP, desc_kmajor(sV, BN, kk), desc_kmajor(dO, BM, kk), idS, kk > 0);
+        umma_commit(smem_u32(&bars.s_full));
+        return true;
+      };
+      bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort, kWaitTimeoutNs) && issue_sdp(0);
+      for (int it = 0; ok && it < n_steps; ++it) {
+        const int st = it & 1;
+        const uint32_t q = sQ + st * C::Q_BYTES, dO = sDO + st * C::Q_BYTES;
+        const uint32_t dS = sDS + st * C::DS_BYTES;
+        if (!mbar_wait(smem_u32(&bars.p_full), it & 1, abort, kWaitTimeoutNs)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_ts(tDV, tP + kk * 8, desc_mnmajor(dO, BM, kk), idG, (it > 0 || kk > 0));
+        if (it + 1 < n_steps && !issue_sdp(it + 1)) break;
+        if (!mbar_wait(smem_u32(&bars.ds_full[st]), (it >> 1) & 1, abort, kWaitTimeoutNs)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_ss(tDK, desc_kmajor(dS, BN, kk), desc_mnmajor(q, BM, kk), idG, (it > 0 || kk > 0));
+        if (it > 0 &&
+            !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, kWaitTimeoutNs))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          if (C::DQ_T)
+            umma_ss(tDQ, desc_mnmajor(sK, BN, kk), desc_mnmajor(dS, BN, kk), idQ, kk > 0);
+          else
+            umma_ss(tDQ, desc_mnmajor(dS, BN, kk), desc_mnmajor(sK, BN, kk), idQ, kk > 0);
         }
-        if (it > 0) {
-          const int prev = it - 1, pst = prev & 1;
-          if (!mbar_wait(smem_u32(&bars.p_full), prev & 1, abort, kWaitTimeoutNs)) break;
-          tc_fence_after();
-          const uint32_t q = sQ + pst * C::Q_BYTES, dO = sDO + pst * C::Q_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk)
-            umma_ss(tDV, desc_kmajor(sP, BN, kk), desc_mnmajor(dO, BM, kk), idG,
-                    (prev > 0 || kk > 0));
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk)
-            umma_ss(tDK, desc_kmajor(sDS, BN, kk), desc_mnmajor(q, BM, kk), idG,
-                    (prev > 0 || kk > 0));
-          if (prev > 0 &&
-              !mbar_wait(smem_u32(&bars.dq_empty), (prev - 1) & 1, abort, kWaitTimeoutNs))
-            break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            if (C::DQ_T)
-              umma_ss(tDQ, desc_mnmajor(sK, BN, kk), desc_mnmajor(sDS, BN, kk), idQ, kk > 0);
-            else
-              umma_ss(tDQ, desc_mnmajor(sDS, BN, kk), desc_mnmajor(sK, BN, kk), idQ, kk > 0);
-          }
-          umma_commit(smem_u32(&bars.p_empty));
-          umma_commit(smem_u32(&bars.q_empty[pst]));
-          umma_commit(smem_u32(&bars.dq_full));
-        }
+        umma_commit(smem_u32(&bars.ds_empty[st]));
+        umma_commit(smem_u32(&bars.q_empty[st]));
+        umma_commit(smem_u32(&bars.dq_full));
       }
       umma_commit(smem_u32(&bars.dkdv_full));
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------------ P^T / dS^T compute
-    const int j = threadIdx.x;  // key row in tile = TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // Two warpgroups; warpgroup g owns score columns [g*HALF, (g+1)*HALF) of every key row.
+    const int g = warp >> 2;
+    const int j = (warp & 3) * 32 + lane;  // key row in tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int key = k_lo + j;
+    const bool key_ok = key < sv.len_k;
     const float c2 = p.scale_log2;
+    const int c_base = g * HALF;
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
       const int st = it & 1;
@@ -338,72 +362,75 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       tc_fence_after();
       const bool need_mask = (q_lo + BM > sv.len_q) || (k_lo + BN > sv.len_k) ||
                              (p.causal && k_lo + BN - 1 > q_lo);
-      // first visible query index for this key row (top-left causal: q >= key)
-      const int q_min = p.causal ? key : 0;
-      const bool key_ok = key < sv.len_k;
-      uint32_t pp[BM / 2], pd[BM / 2];
+      const int q_min = p.causal ? key : 0;  // top-left causal: query q sees key iff q >= key
+      uint32_t pd[HALF / 2];
 #pragma unroll
-      for (int c = 0; c < BM / 32; ++c) {
+      for (int ch = 0; ch < HALF / 32; ++ch) {
+        const int c0 = c_base + ch * 32;
         float s[32], dp[32];
-        ATTN_TMEM_LD_X32(tmem + C::COL_S + lane_off + c * 32, reinterpret_cast<uint32_t*>(s));
-        ATTN_TMEM_LD_X32(tmem + C::COL_DP + lane_off + c * 32, reinterpret_cast<uint32_t*>(dp));
+        ATTN_TMEM_LD_X32(tmem + C::COL_S + lane_off + c0, reinterpret_cast<uint32_t*>(s));
+        ATTN_TMEM_LD_X32(tmem + C::COL_DP + lane_off + c0, reinterpret_cast<uint32_t*>(dp));
+        uint32_t pp[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int i = c * 32 + e;
-          float pv0 = ex2_approx(fmaf(s[e], c2, -bars.lse2[st][i]));
-          float pv1 = ex2_approx(fmaf(s[e + 1], c2, -bars.lse2[st][i + 1]));
-          float ds0 = pv0 * (dp[e] - bars.delta[st][i]);
-          float ds1 = pv1 * (dp[e + 1] - bars.delta[st][i + 1]);
-          if (need_mask) {
-            const int q0 = q_lo + i, q1 = q0 + 1;
-            const bool v0 = key_ok && q0 < sv.len_q && q0 >= q_min;
-            const bool v1 = key_ok && q1 < sv.len_q && q1 >= q_min;
-            pv0 = v0 ? pv0 : 0.f;
-            ds0 = v0 ? ds0 : 0.f;
-            pv1 = v1 ? pv1 : 0.f;
-            ds1 = v1 ? ds1 : 0.f;
+        for (int e4 = 0; e4 < 32; e4 += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(&bars.lse2[st][c0 + e4]);
+          const float4 d4 = *reinterpret_cast<const float4*>(&bars.delta[st][c0 + e4]);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], ds[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            pv[u] = ex2_approx(fmaf(s[e4 + u], c2, -lv[u]));
+            ds[u] = pv[u] * (dp[e4 + u] - dv[u]);
+            if (need_mask) {
+              const int qq = q_lo + c0 + e4 + u;
+              const bool valid = key_ok && qq < sv.len_q && qq >= q_min;
+              pv[u] = valid ? pv[u] : 0.f;
+              ds[u] = valid ? ds[u] : 0.f;
+            }
           }
-          pp[i / 2] = pack_bf16x2(pv0, pv1);
-          pd[i / 2] = pack_bf16x2(ds0, ds1);
+          pp[e4 / 2] = pack_bf16x2(pv[0], pv[1]);
+          pp[e4 / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+          pd[ch * 16 + e4 / 2] = pack_bf16x2(ds[0], ds[1]);
+          pd[ch * 16 + e4 / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
+        ATTN_TMEM_ST_X16(tmem + C::COL_P + lane_off + c0 / 2, pp);
       }
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.s_empty));
-      if (it > 0 && !mbar_wait(smem_u32(&bars.p_empty), (it - 1) & 1, abort, kWaitTimeoutNs)) {
+      mbar_arrive(smem_u32(&bars.p_full));
+      if (it >= 2 &&
+          !mbar_wait(smem_u32(&bars.ds_empty[st]), ((it >> 1) - 1) & 1, abort, kWaitTimeoutNs)) {
         ok = false;
         break;
       }
-      uint8_t* gP = smem + C::OFF_P;
-      uint8_t* gDS = smem + C::OFF_DS;
+      uint8_t* gDS = smem + C::OFF_DS + st * C::DS_BYTES;
 #pragma unroll
-      for (int c8 = 0; c8 < BM / 8; ++c8) {
-        const uint32_t off = sw128_offset(j, c8 * 8, BN);
-        *reinterpret_cast<uint4*>(gP + off) =
-            make_uint4(pp[c8 * 4 + 0], pp[c8 * 4 + 1], pp[c8 * 4 + 2], pp[c8 * 4 + 3]);
+      for (int c8 = 0; c8 < HALF / 8; ++c8) {
+        const uint32_t off = sw128_offset(j, c_base + c8 * 8, BN);
         *reinterpret_cast<uint4*>(gDS + off) =
             make_uint4(pd[c8 * 4 + 0], pd[c8 * 4 + 1], pd[c8 * 4 + 2], pd[c8 * 4 + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bars.p_full));
+      mbar_arrive(smem_u32(&bars.ds_full[st]));
     }
-    // ---- epilogue: dK = sm_scale * acc, dV = acc
+    // ---- epilogue: dK = sm_scale * acc, dV = acc; warpgroup g writes columns [g*D/2, +D/2)
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, kWaitTimeoutNs);
     tc_fence_after();
     if (ok) {
-      const bool valid = key < sv.len_k;
       const int64_t grow = sv.row0_k + key;
       __nv_bfloat16* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
       __nv_bfloat16* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
+      const float sc = p.sm_scale;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = g * (D / 2); c < (g + 1) * (D / 2); c += 32) {
         uint32_t a[32], b[32];
-        ATTN_TMEM_LD_X32(tmem + C::COL_DK + lane_off + c * 32, a);
-        ATTN_TMEM_LD_X32(tmem + C::COL_DV + lane_off + c * 32, b);
-        if (valid) {
+        ATTN_TMEM_LD_X32(tmem + C::COL_DK + lane_off + c, a);
+        ATTN_TMEM_LD_X32(tmem + C::COL_DV + lane_off + c, b);
+        if (key_ok) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 vk, vv;
-            const float sc = p.sm_scale;
             vk.x = pack_bf16x2(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc);
             vk.y = pack_bf16x2(__uint_as_float(a[e + 2]) * sc, __uint_as_float(a[e + 3]) * sc);
             vk.z = pack_bf16x2(__uint_as_float(a[e + 4]) * sc, __uint_as_float(a[e + 5]) * sc);
@@ -412,48 +439,48 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
             vv.y = pack_bf16x2(__uint_as_float(b[e + 2]), __uint_as_float(b[e + 3]));
             vv.z = pack_bf16x2(__uint_as_float(b[e + 4]), __uint_as_float(b[e + 5]));
             vv.w = pack_bf16x2(__uint_as_float(b[e + 6]), __uint_as_float(b[e + 7]));
-            *reinterpret_cast<uint4*>(kr + c * 32 + e) = vk;
-            *reinterpret_cast<uint4*>(vr + c * 32 + e) = vv;
+            *reinterpret_cast<uint4*>(kr + c + e) = vk;
+            *reinterpret_cast<uint4*>(vr + c + e) = vv;
           }
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------------ dQ drain (warps 4..7)
-    const int t = threadIdx.x - 128;  // TMEM lane
+  } else if (warp < 12) {
+    // ------------------------------------------------------------------ dQ drain (warps 8..11)
+    const int t = (warp & 3) * 32 + lane;  // TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     float* acc_base = p.dq_acc + (zh * p.rows_q + sv.row0_q) * D;
     for (int it = 0; it < n_steps; ++it) {
       if (!mbar_wait(smem_u32(&bars.dq_full), it & 1, abort, kWaitTimeoutNs)) break;
       tc_fence_after();
       const int q_lo = (m_begin + it) * BM;
+      constexpr int NCOL = C::DQ_T ? BM : D;
+      float v[NCOL];
+#pragma unroll
+      for (int c = 0; c < NCOL / 32; ++c)
+        ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + c * 32, reinterpret_cast<uint32_t*>(&v[c * 32]));
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.dq_empty));
       if (C::DQ_T) {
-        // lanes = d, columns = query rows of the step
-        float v[BM];
-#pragma unroll
-        for (int c = 0; c < BM / 32; ++c)
-          ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + c * 32, reinterpret_cast<uint32_t*>(&v[c * 32]));
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.dq_empty));
-        const int d = t;
+        // lanes = d, columns = query rows of the step: a warp adds 32 consecutive floats
         const int nvalid = min(BM, sv.len_q - q_lo);
+        float* col = acc_base + (int64_t)q_lo * D + t;
+        if (nvalid == BM) {
 #pragma unroll
-        for (int i = 0; i < BM; ++i)
-          if (i < nvalid) atomicAdd(acc_base + (int64_t)(q_lo + i) * D + d, v[i]);
+          for (int i = 0; i < BM; ++i) red_add_f32(col + (int64_t)i * D, v[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < BM; ++i)
+            if (i < nvalid) red_add_f32(col + (int64_t)i * D, v[i]);
+        }
       } else {
         // lanes = query rows, columns = d
-        float v[D];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c)
-          ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + c * 32, reinterpret_cast<uint32_t*>(&v[c * 32]));
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.dq_empty));
         const int q = q_lo + t;
         if (q < sv.len_q) {
-          float4* dst = reinterpret_cast<float4*>(acc_base + (int64_t)q * D);
+          float* row = acc_base + (int64_t)q * D;
 #pragma unroll
           for (int e = 0; e < D / 4; ++e)
-            atomicAdd(dst + e, make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]));
+            red_add_v4_f32(row + 4 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
       }
     }
@@ -461,7 +488,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }

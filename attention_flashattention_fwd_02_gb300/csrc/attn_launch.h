@@ -6,8 +6,10 @@
 
 namespace attn_sm103 {
 
-// Forward: grid = (query tiles, H, B or num_seqs); query tiles of fwd_block_m() rows.
+// Forward: grid = (query blocks, H, B or num_seqs); a block covers fwd_block_m() query rows,
+// loaded with a Q tensor map whose box has fwd_box_rows() rows.
 int fwd_block_m();
+int fwd_box_rows();
 cudaError_t launch_attn_fwd(const FwdParams& p, int D, dim3 grid, cudaStream_t stream);
 
 // Backward stages.
