@@ -132,9 +132,10 @@ struct BwdCfg {
   static constexpr int DS_BYTES = BN * BM * 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;      // 2 stages
-  static constexpr int OFF_DO = OFF_Q + 2 * Q_BYTES;  // 2 stages
-  static constexpr int OFF_DS = OFF_DO + 2 * Q_BYTES; // 2 buffers
+  static constexpr int QST = 3;                        // Q / dO / LSE / Delta stages
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;        // QST stages
+  static constexpr int OFF_DO = OFF_Q + QST * Q_BYTES;  // QST stages
+  static constexpr int OFF_DS = OFF_DO + QST * Q_BYTES; // 2 buffers
   static constexpr int SMEM_BYTES = OFF_DS + 2 * DS_BYTES + 1024;
   // TMEM columns: dK, dV accumulators; S^T, dP^T of the current step; the dQ partial; and P^T
   // (bf16, two values per column) as the A operand of the dV MMA.
@@ -147,17 +148,17 @@ struct BwdCfg {
   static constexpr int WARP_PRODUCER = 12, WARP_MMA = 13;
 };
 
-template <int BM>
+template <int BM, int QST>
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[QST], q_empty[QST];
   uint64_t s_full, p_full;
   uint64_t ds_full[2], ds_empty[2];
   uint64_t dq_full, dq_empty, dkdv_full;
   uint32_t tmem_base;
   int abort;
-  alignas(16) float lse2[2][BM];
-  alignas(16) float delta[2][BM];
+  alignas(16) float lse2[QST][BM];
+  alignas(16) float delta[QST][BM];
 };
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
@@ -175,7 +176,8 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
   constexpr int BN = C::BN, BM = C::BM;
   constexpr int HALF = BM / 2;  // score columns per compute warpgroup
   extern __shared__ uint8_t smem_raw[];
-  __shared__ BwdBars<BM> bars;
+  constexpr int QST = C::QST;
+  __shared__ BwdBars<BM, QST> bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
@@ -188,6 +190,14 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
   const int m_end = (sv.len_q + BM - 1) / BM;
   const int n_steps = max(0, m_end - m_begin);
   const int64_t zh = (int64_t)sv.batch * p.H + h;
+  // Query tile of step it. Without a causal mask every key tile visits all query tiles; the
+  // starting tile is rotated by the key-tile index so that the CTAs of one head do not add
+  // into the same dQ rows at the same time.
+  const int rot = p.causal ? 0 : (n_steps > 0 ? n_tile % n_steps : 0);
+  auto q_tile = [&](int it) {
+    const int r = it + rot;
+    return m_begin + (r >= n_steps ? r - n_steps : r);
+  };
 
   if (n_steps == 0) {  // no query sees these keys: dK = dV = 0
     if (threadIdx.x < BN) {
@@ -213,9 +223,11 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(smem_u32(&bars.kv_full), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < QST; ++s) {
       mbar_init(smem_u32(&bars.q_full[s]), 33);  // producer lane 0 (tx) + 32 lanes (LSE/Delta)
       mbar_init(smem_u32(&bars.q_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.ds_full[s]), 256);
       mbar_init(smem_u32(&bars.ds_empty[s]), 1);
     }
@@ -252,11 +264,11 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
       }
     }
     for (int it = 0; it < n_steps; ++it) {
-      const int st = it & 1;
-      if (it >= 2 &&
-          !mbar_wait(smem_u32(&bars.q_empty[st]), ((it >> 1) - 1) & 1, abort, kWaitTimeoutNs))
+      const int st = it % QST;
+      if (it >= QST &&
+          !mbar_wait(smem_u32(&bars.q_empty[st]), ((it / QST) - 1) & 1, abort, kWaitTimeoutNs))
         break;
-      const int q_lo = (m_begin + it) * BM;
+      const int q_lo = q_tile(it) * BM;
       const uint32_t qb = smem_u32(&bars.q_full[st]);
       if (lane == 0) {
         mbar_arrive_expect_tx(qb, 2 * C::Q_BYTES);
@@ -293,8 +305,8 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
       const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP, tP = tmem + C::COL_P;
       const uint32_t tDK = tmem + C::COL_DK, tDV = tmem + C::COL_DV, tDQ = tmem + C::COL_DQ;
       auto issue_sdp = [&](int it) -> bool {
-        const int st = it & 1;
-        if (!mbar_wait(smem_u32(&bars.q_full[st]), (it >> 1) & 1, abort, kWaitTimeoutNs))
+        const int st = it % QST;
+        if (!mbar_wait(smem_u32(&bars.q_full[st]), (it / QST) & 1, abort, kWaitTimeoutNs))
           return false;
         tc_fence_after();
         const uint32_t q = sQ + st * C::Q_BYTES, dO = sDO + st * C::Q_BYTES;
@@ -309,16 +321,16 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
       };
       bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort, kWaitTimeoutNs) && issue_sdp(0);
       for (int it = 0; ok && it < n_steps; ++it) {
-        const int st = it & 1;
+        const int st = it % QST, bs = it & 1;
         const uint32_t q = sQ + st * C::Q_BYTES, dO = sDO + st * C::Q_BYTES;
-        const uint32_t dS = sDS + st * C::DS_BYTES;
+        const uint32_t dS = sDS + bs * C::DS_BYTES;
         if (!mbar_wait(smem_u32(&bars.p_full), it & 1, abort, kWaitTimeoutNs)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           umma_ts(tDV, tP + kk * 8, desc_mnmajor(dO, BM, kk), idG, (it > 0 || kk > 0));
         if (it + 1 < n_steps && !issue_sdp(it + 1)) break;
-        if (!mbar_wait(smem_u32(&bars.ds_full[st]), (it >> 1) & 1, abort, kWaitTimeoutNs)) break;
+        if (!mbar_wait(smem_u32(&bars.ds_full[bs]), (it >> 1) & 1, abort, kWaitTimeoutNs)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
           else
             umma_ss(tDQ, desc_mnmajor(dS, BN, kk), desc_mnmajor(sK, BN, kk), idQ, kk > 0);
         }
-        umma_commit(smem_u32(&bars.ds_empty[st]));
+        umma_commit(smem_u32(&bars.ds_empty[bs]));
         umma_commit(smem_u32(&bars.q_empty[st]));
         umma_commit(smem_u32(&bars.dq_full));
       }
@@ -352,10 +364,10 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
     const int c_base = g * HALF;
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
-      const int st = it & 1;
-      const int q_lo = (m_begin + it) * BM;
+      const int st = it % QST, bs = it & 1;
+      const int q_lo = q_tile(it) * BM;
       if (!mbar_wait(smem_u32(&bars.s_full), it & 1, abort, kWaitTimeoutNs) ||
-          !mbar_wait(smem_u32(&bars.q_full[st]), (it >> 1) & 1, abort, kWaitTimeoutNs)) {
+          !mbar_wait(smem_u32(&bars.q_full[st]), (it / QST) & 1, abort, kWaitTimeoutNs)) {
         ok = false;
         break;
       }
@@ -400,11 +412,11 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full));
       if (it >= 2 &&
-          !mbar_wait(smem_u32(&bars.ds_empty[st]), ((it >> 1) - 1) & 1, abort, kWaitTimeoutNs)) {
+          !mbar_wait(smem_u32(&bars.ds_empty[bs]), ((it >> 1) - 1) & 1, abort, kWaitTimeoutNs)) {
         ok = false;
         break;
       }
-      uint8_t* gDS = smem + C::OFF_DS + st * C::DS_BYTES;
+      uint8_t* gDS = smem + C::OFF_DS + bs * C::DS_BYTES;
 #pragma unroll
       for (int c8 = 0; c8 < HALF / 8; ++c8) {
         const uint32_t off = sw128_offset(j, c_base + c8 * 8, BN);
@@ -412,7 +424,7 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
             make_uint4(pd[c8 * 4 + 0], pd[c8 * 4 + 1], pd[c8 * 4 + 2], pd[c8 * 4 + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bars.ds_full[st]));
+      mbar_arrive(smem_u32(&bars.ds_full[bs]));
     }
     // ---- epilogue: dK = sm_scale * acc, dV = acc; warpgroup g writes columns [g*D/2, +D/2)
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, kWaitTimeoutNs);
@@ -453,7 +465,7 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
     for (int it = 0; it < n_steps; ++it) {
       if (!mbar_wait(smem_u32(&bars.dq_full), it & 1, abort, kWaitTimeoutNs)) break;
       tc_fence_after();
-      const int q_lo = (m_begin + it) * BM;
+      const int q_lo = q_tile(it) * BM;
       constexpr int NCOL = C::DQ_T ? BM : D;
       float v[NCOL];
 #pragma unroll
