@@ -157,8 +157,8 @@ struct BwdBars {
   uint64_t dq_full, dq_empty, dkdv_full;
   uint32_t tmem_base;
   int abort;
-  alignas(16) float lse2[QST][BM];
-  alignas(16) float delta[QST][BM];
+  alignas(16) float nlse2[QST][BM];   // -LSE * log2(e) of the step's query rows
+  alignas(16) float ndelta[QST][BM];  // -Delta
 };
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
@@ -288,8 +288,8 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
           l2 = p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] * kLog2e;
           dl = p.delta[zh * p.rows_q + grow];
         }
-        bars.lse2[st][i] = l2;
-        bars.delta[st][i] = dl;
+        bars.nlse2[st][i] = -l2;
+        bars.ndelta[st][i] = -dl;
       }
       mbar_arrive(qb);
     }
@@ -375,25 +375,37 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
       const bool need_mask = (q_lo + BM > sv.len_q) || (k_lo + BN > sv.len_k) ||
                              (p.causal && k_lo + BN - 1 > q_lo);
       const int q_min = p.causal ? key : 0;  // top-left causal: query q sees key iff q >= key
-      uint32_t pd[HALF / 2];
+      // The dS^T buffer of this step was last read by the dK / dQ MMAs two steps ago.
+      if (it >= 2 &&
+          !mbar_wait(smem_u32(&bars.ds_empty[bs]), ((it >> 1) - 1) & 1, abort, kWaitTimeoutNs)) {
+        ok = false;
+        break;
+      }
+      uint8_t* gDS = smem + C::OFF_DS + bs * C::DS_BYTES;
 #pragma unroll
       for (int ch = 0; ch < HALF / 32; ++ch) {
         const int c0 = c_base + ch * 32;
         float s[32], dp[32];
-        ATTN_TMEM_LD_X32(tmem + C::COL_S + lane_off + c0, reinterpret_cast<uint32_t*>(s));
-        ATTN_TMEM_LD_X32(tmem + C::COL_DP + lane_off + c0, reinterpret_cast<uint32_t*>(dp));
-        uint32_t pp[16];
+        ATTN_TMEM_LD2_X32(tmem + C::COL_S + lane_off + c0, tmem + C::COL_DP + lane_off + c0,
+                          reinterpret_cast<uint32_t*>(s), reinterpret_cast<uint32_t*>(dp));
+        uint32_t pp[16], pd[16];
+        const uint64_t c2x2 = f2_pack(c2, c2);
 #pragma unroll
         for (int e4 = 0; e4 < 32; e4 += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(&bars.lse2[st][c0 + e4]);
-          const float4 d4 = *reinterpret_cast<const float4*>(&bars.delta[st][c0 + e4]);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], ds[4];
+          const float4 l4 = *reinterpret_cast<const float4*>(&bars.nlse2[st][c0 + e4]);
+          const float4 d4 = *reinterpret_cast<const float4*>(&bars.ndelta[st][c0 + e4]);
+          float pv[4], ds[4], x[4], y[4];
+          // P = 2^(S c2 - LSE2); dS = P (dP - Delta): paired fp32 instructions
+          f2_unpack(f2_fma(f2_pack(s[e4], s[e4 + 1]), c2x2, f2_pack(l4.x, l4.y)), x[0], x[1]);
+          f2_unpack(f2_fma(f2_pack(s[e4 + 2], s[e4 + 3]), c2x2, f2_pack(l4.z, l4.w)), x[2], x[3]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) pv[u] = ex2_approx(x[u]);
+          f2_unpack(f2_add(f2_pack(dp[e4], dp[e4 + 1]), f2_pack(d4.x, d4.y)), y[0], y[1]);
+          f2_unpack(f2_add(f2_pack(dp[e4 + 2], dp[e4 + 3]), f2_pack(d4.z, d4.w)), y[2], y[3]);
+          f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), f2_pack(y[0], y[1])), ds[0], ds[1]);
+          f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), f2_pack(y[2], y[3])), ds[2], ds[3]);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            pv[u] = ex2_approx(fmaf(s[e4 + u], c2, -lv[u]));
-            ds[u] = pv[u] * (dp[e4 + u] - dv[u]);
             if (need_mask) {
               const int qq = q_lo + c0 + e4 + u;
               const bool valid = key_ok && qq < sv.len_q && qq >= q_min;
@@ -403,26 +415,20 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
           }
           pp[e4 / 2] = pack_bf16x2(pv[0], pv[1]);
           pp[e4 / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-          pd[ch * 16 + e4 / 2] = pack_bf16x2(ds[0], ds[1]);
-          pd[ch * 16 + e4 / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+          pd[e4 / 2] = pack_bf16x2(ds[0], ds[1]);
+          pd[e4 / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
         ATTN_TMEM_ST_X16(tmem + C::COL_P + lane_off + c0 / 2, pp);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          const uint32_t off = sw128_offset(j, c0 + c8 * 8, BN);
+          *reinterpret_cast<uint4*>(gDS + off) =
+              make_uint4(pd[c8 * 4 + 0], pd[c8 * 4 + 1], pd[c8 * 4 + 2], pd[c8 * 4 + 3]);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full));
-      if (it >= 2 &&
-          !mbar_wait(smem_u32(&bars.ds_empty[bs]), ((it >> 1) - 1) & 1, abort, kWaitTimeoutNs)) {
-        ok = false;
-        break;
-      }
-      uint8_t* gDS = smem + C::OFF_DS + bs * C::DS_BYTES;
-#pragma unroll
-      for (int c8 = 0; c8 < HALF / 8; ++c8) {
-        const uint32_t off = sw128_offset(j, c_base + c8 * 8, BN);
-        *reinterpret_cast<uint4*>(gDS + off) =
-            make_uint4(pd[c8 * 4 + 0], pd[c8 * 4 + 1], pd[c8 * 4 + 2], pd[c8 * 4 + 3]);
-      }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.ds_full[bs]));
     }
@@ -437,8 +443,7 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
 #pragma unroll
       for (int c = g * (D / 2); c < (g + 1) * (D / 2); c += 32) {
         uint32_t a[32], b[32];
-        ATTN_TMEM_LD_X32(tmem + C::COL_DK + lane_off + c, a);
-        ATTN_TMEM_LD_X32(tmem + C::COL_DV + lane_off + c, b);
+        ATTN_TMEM_LD2_X32(tmem + C::COL_DK + lane_off + c, tmem + C::COL_DV + lane_off + c, a, b);
         if (key_ok) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {

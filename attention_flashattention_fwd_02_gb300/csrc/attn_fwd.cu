@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     const float c2 = p.scale_log2;
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; ok && j < n; ++j) {
       if (!mbar_wait(smem_u32(&bars.s_full[t]), j & 1, abort, kWaitTimeoutNs)) {
         ok = false;
         break;
@@ -243,9 +243,10 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       tc_fence_after();
       float s[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t* u = reinterpret_cast<uint32_t*>(&s[c * 32]);
-        ATTN_TMEM_LD_X32(tSt + c * 32, u);
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t* u0 = reinterpret_cast<uint32_t*>(&s[c * 64]);
+        uint32_t* u1 = reinterpret_cast<uint32_t*>(&s[c * 64 + 32]);
+        ATTN_TMEM_LD2_X32(tSt + c * 64, tSt + c * 64 + 32, u0, u1);
       }
       const int k0 = j * BN;
       if (k0 + BN > sv.len_k || (p.causal && k0 + BN - 1 > q_lo[t])) {
@@ -254,14 +255,18 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         for (int c = 0; c < BN; ++c)
           if (k0 + c > kmax) s[c] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      // row maximum: four independent chains of three-input max
+      float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+      float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
 #pragma unroll
-      for (int c = 4; c < BN; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+      for (int c = 12; c + 8 <= BN; c += 8) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
       }
+      mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
+      mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
       const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
       float m_new = m_use, scale = 1.f;
       if (mxs > m_use + 8.f) {
@@ -269,22 +274,25 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         scale = ex2_approx(m_use - m_new);
       }
       const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
-      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+      // p = 2^(s c2 - m): scale-and-shift and the row sum run on paired fp32 instructions
+      const uint64_t c2x2 = f2_pack(c2, c2), negm2 = f2_pack(neg_m, neg_m);
+      uint64_t rs0 = 0, rs1 = 0;  // two pairs of partial sums (0.0f bit pattern is 0)
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN / 2; c += 2) {
-        const float p0 = ex2_approx(fmaf(s[2 * c], c2, neg_m));
-        const float p1 = ex2_approx(fmaf(s[2 * c + 1], c2, neg_m));
-        const float p2 = ex2_approx(fmaf(s[2 * c + 2], c2, neg_m));
-        const float p3 = ex2_approx(fmaf(s[2 * c + 3], c2, neg_m));
-        rs0 += p0;
-        rs1 += p1;
-        rs2 += p2;
-        rs3 += p3;
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), c2x2, negm2), x0, x1);
+        f2_unpack(f2_fma(f2_pack(s[2 * c + 2], s[2 * c + 3]), c2x2, negm2), x2, x3);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+        rs0 = f2_add(rs0, f2_pack(p0, p1));
+        rs1 = f2_add(rs1, f2_pack(p2, p3));
         pk[c] = pack_bf16x2(p0, p1);
         pk[c + 1] = pack_bf16x2(p2, p3);
       }
-      l = l * scale + ((rs0 + rs1) + (rs2 + rs3));
+      float a0, a1;
+      f2_unpack(f2_add(rs0, rs1), a0, a1);
+      l = l * scale + (a0 + a1);
       m_use = m_new;
       if (j > 0) {
         if (!mbar_wait(smem_u32(&bars.o_done[t]), (j - 1) & 1, abort, kWaitTimeoutNs)) {
@@ -293,12 +301,19 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         }
         tc_fence_after();
         if (__any_sync(0xffffffffu, scale != 1.f)) {
+          const uint64_t sc2 = f2_pack(scale, scale);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             ATTN_TMEM_LD_X32(tOt + c * 32, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * scale);
+            for (int e = 0; e < 32; e += 2) {
+              float y0, y1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), sc2),
+                        y0, y1);
+              o[e] = __float_as_uint(y0);
+              o[e + 1] = __float_as_uint(y1);
+            }
             ATTN_TMEM_ST_X32(tOt + c * 32, o);
           }
         }
