@@ -14,12 +14,13 @@
 //                            LSE that the forward pass stashed.
 //  3. attn_bwd_post_kernel   dQ = bf16(sm_scale * accumulator). Memory-bound.
 //
-// Main-kernel warp roles (448 threads): warps 0..7 are two compute warpgroups that split
+// Main-kernel warp roles (320 threads): warps 0..7 are two compute warpgroups that split
 // the query columns of each key row (thread row j = TMEM lane j) to form P^T (written to
 // TMEM, where it is the A operand of the dV MMA) and dS^T (written to shared memory for the
-// dK and dQ MMAs), and write dK / dV at the end; warps 8..11 drain the dQ partial from TMEM
-// into the global fp32 accumulator with fire-and-forget reductions; warp 12 is the TMA
-// producer; warp 13 allocates TMEM and issues the MMAs. Tile sizes: 128 keys per CTA; 64
+// dK and dQ MMAs); after each step they drain their half of the previous step's dQ partial
+// from TMEM into the global fp32 accumulator with fire-and-forget reductions, and at the
+// end they write dK / dV; warp 8 is the TMA producer; warp 9 allocates TMEM and issues the
+// MMAs. Tile sizes: 128 keys per CTA; 64
 // query rows per step when d_head = 128 (dQ is formed transposed, K_n^T dS^T, so that every
 // MMA has M = 128), 128 when d_head = 64.
 #include "attn_common.cuh"
@@ -144,8 +145,8 @@ struct BwdCfg {
   static constexpr uint32_t COL_DQ = 2 * D + 2 * BM;
   static constexpr uint32_t COL_P = COL_DQ + (DQ_T ? BM : D);
   static_assert(COL_P + BM / 2 <= TMEM_COLS, "TMEM layout does not fit");
-  static constexpr int NTHREADS = 448;  // 2 compute WGs, 1 dQ-drain WG, producer, MMA
-  static constexpr int WARP_PRODUCER = 12, WARP_MMA = 13;
+  static constexpr int NTHREADS = 320;  // 2 compute warpgroups, producer, MMA
+  static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
 };
 
 template <int BM, int QST>
@@ -171,7 +172,7 @@ __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float
 }
 
 template <int D>
-__global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int BN = C::BN, BM = C::BM;
   constexpr int HALF = BM / 2;  // score columns per compute warpgroup
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
     mbar_init(smem_u32(&bars.s_full), 1);
     mbar_init(smem_u32(&bars.p_full), 256);
     mbar_init(smem_u32(&bars.dq_full), 1);
-    mbar_init(smem_u32(&bars.dq_empty), 128);
+    mbar_init(smem_u32(&bars.dq_empty), 256);
     mbar_init(smem_u32(&bars.dkdv_full), 1);
     mbar_fence_init();
   }
@@ -362,6 +363,41 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
     const bool key_ok = key < sv.len_k;
     const float c2 = p.scale_log2;
     const int c_base = g * HALF;
+    float* acc_base = p.dq_acc + (zh * p.rows_q + sv.row0_q) * D;
+    // Drains warpgroup g's 32 columns of the dQ partial of step itd from TMEM into the fp32
+    // accumulator with fire-and-forget reductions. dQ^T (d_head 128): lanes are d, columns
+    // are the step's query rows; dQ (d_head 64): lanes are query rows, columns are d.
+    auto drain_dq = [&](int itd) -> bool {
+      if (!mbar_wait(smem_u32(&bars.dq_full), itd & 1, abort, kWaitTimeoutNs)) return false;
+      tc_fence_after();
+      float v[32];
+      ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + g * 32, reinterpret_cast<uint32_t*>(v));
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.dq_empty));
+      const int q_lo_d = q_tile(itd) * BM;
+      if (C::DQ_T) {
+        const int i0 = q_lo_d + g * 32;  // first query row of these columns
+        const int nvalid = min(32, sv.len_q - i0);
+        float* col = acc_base + (int64_t)i0 * D + j;
+        if (nvalid >= 32) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) red_add_f32(col + (int64_t)i * D, v[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < nvalid) red_add_f32(col + (int64_t)i * D, v[i]);
+        }
+      } else {
+        const int q = q_lo_d + j;
+        if (q < sv.len_q) {
+          float* row = acc_base + (int64_t)q * D + g * 32;
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            red_add_v4_f32(row + 4 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
+      }
+      return true;
+    };
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
       const int st = it % QST, bs = it & 1;
@@ -382,12 +418,24 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
         break;
       }
       uint8_t* gDS = smem + C::OFF_DS + bs * C::DS_BYTES;
+      // All of this warpgroup's S^T and dP^T columns are fetched behind one wait.
+      float sv_all[HALF], dpv_all[HALF];
+      if constexpr (HALF == 64) {
+        ATTN_TMEM_LD4_X32(tmem + C::COL_S + lane_off + c_base, tmem + C::COL_S + lane_off + c_base + 32,
+                          tmem + C::COL_DP + lane_off + c_base,
+                          tmem + C::COL_DP + lane_off + c_base + 32,
+                          reinterpret_cast<uint32_t*>(sv_all), reinterpret_cast<uint32_t*>(sv_all + 32),
+                          reinterpret_cast<uint32_t*>(dpv_all),
+                          reinterpret_cast<uint32_t*>(dpv_all + 32));
+      } else {
+        ATTN_TMEM_LD2_X32(tmem + C::COL_S + lane_off + c_base, tmem + C::COL_DP + lane_off + c_base,
+                          reinterpret_cast<uint32_t*>(sv_all), reinterpret_cast<uint32_t*>(dpv_all));
+      }
 #pragma unroll
       for (int ch = 0; ch < HALF / 32; ++ch) {
         const int c0 = c_base + ch * 32;
-        float s[32], dp[32];
-        ATTN_TMEM_LD2_X32(tmem + C::COL_S + lane_off + c0, tmem + C::COL_DP + lane_off + c0,
-                          reinterpret_cast<uint32_t*>(s), reinterpret_cast<uint32_t*>(dp));
+        const float* s = sv_all + ch * 32;
+        const float* dp = dpv_all + ch * 32;
         uint32_t pp[16], pd[16];
         const uint64_t c2x2 = f2_pack(c2, c2);
 #pragma unroll
@@ -431,7 +479,13 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
       mbar_arrive(smem_u32(&bars.p_full));
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.ds_full[bs]));
+      // dQ partial of the previous step (its MMA ran while this step's P/dS were formed)
+      if (it > 0 && !drain_dq(it - 1)) {
+        ok = false;
+        break;
+      }
     }
+    if (ok && n_steps > 0) ok = drain_dq(n_steps - 1);
     // ---- epilogue: dK = sm_scale * acc, dV = acc; warpgroup g writes columns [g*D/2, +D/2)
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, kWaitTimeoutNs);
     tc_fence_after();
@@ -459,45 +513,6 @@ __global__ void __launch_bounds__(448, 1) attn_bwd_main_kernel(const __grid_cons
             *reinterpret_cast<uint4*>(kr + c + e) = vk;
             *reinterpret_cast<uint4*>(vr + c + e) = vv;
           }
-        }
-      }
-    }
-  } else if (warp < 12) {
-    // ------------------------------------------------------------------ dQ drain (warps 8..11)
-    const int t = (warp & 3) * 32 + lane;  // TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    float* acc_base = p.dq_acc + (zh * p.rows_q + sv.row0_q) * D;
-    for (int it = 0; it < n_steps; ++it) {
-      if (!mbar_wait(smem_u32(&bars.dq_full), it & 1, abort, kWaitTimeoutNs)) break;
-      tc_fence_after();
-      const int q_lo = q_tile(it) * BM;
-      constexpr int NCOL = C::DQ_T ? BM : D;
-      float v[NCOL];
-#pragma unroll
-      for (int c = 0; c < NCOL / 32; ++c)
-        ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + c * 32, reinterpret_cast<uint32_t*>(&v[c * 32]));
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars.dq_empty));
-      if (C::DQ_T) {
-        // lanes = d, columns = query rows of the step: a warp adds 32 consecutive floats
-        const int nvalid = min(BM, sv.len_q - q_lo);
-        float* col = acc_base + (int64_t)q_lo * D + t;
-        if (nvalid == BM) {
-#pragma unroll
-          for (int i = 0; i < BM; ++i) red_add_f32(col + (int64_t)i * D, v[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < BM; ++i)
-            if (i < nvalid) red_add_f32(col + (int64_t)i * D, v[i]);
-        }
-      } else {
-        // lanes = query rows, columns = d
-        const int q = q_lo + t;
-        if (q < sv.len_q) {
-          float* row = acc_base + (int64_t)q * D;
-#pragma unroll
-          for (int e = 0; e < D / 4; ++e)
-            red_add_v4_f32(row + 4 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
       }
     }

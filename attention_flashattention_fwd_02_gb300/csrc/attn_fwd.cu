@@ -242,12 +242,10 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       }
       tc_fence_after();
       float s[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t* u0 = reinterpret_cast<uint32_t*>(&s[c * 64]);
-        uint32_t* u1 = reinterpret_cast<uint32_t*>(&s[c * 64 + 32]);
-        ATTN_TMEM_LD2_X32(tSt + c * 64, tSt + c * 64 + 32, u0, u1);
-      }
+      static_assert(BN == 128, "one four-way TMEM load covers the score row");
+      ATTN_TMEM_LD4_X32(tSt, tSt + 32, tSt + 64, tSt + 96, reinterpret_cast<uint32_t*>(s),
+                        reinterpret_cast<uint32_t*>(s + 32), reinterpret_cast<uint32_t*>(s + 64),
+                        reinterpret_cast<uint32_t*>(s + 96));
       const int k0 = j * BN;
       if (k0 + BN > sv.len_k || (p.causal && k0 + BN - 1 > q_lo[t])) {
         const int kmax = p.causal ? min(row, sv.len_k - 1) : sv.len_k - 1;
