@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--settle-s", type=float, default=1.0,
                     help="seconds of untimed steps before the timed region (clock settling)")
+    ap.add_argument("--targets-workload", default="sweep8k",
+                    help="second workload whose fwd / bwd fractions of peak are reported under "
+                         "'targets' (d_head 128, seqlen >= 4096); 'none' to skip")
     return ap.parse_args()
 
 
@@ -122,7 +125,7 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- our arm
-def run_ours(args, rank, world, dist):
+def run_ours(args, rank, world, dist, clocks_on=True):
     import torch
 
     from attention_flashattention_fwd_02_gb300 import _lib
@@ -195,7 +198,7 @@ def run_ours(args, rank, world, dist):
         step()
         torch.cuda.synchronize()
 
-    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) if rank == 0 else None
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) if (rank == 0 and clocks_on) else None
     time.sleep(0.3)
     ev = lambda: torch.cuda.Event(enable_timing=True)
     step_ev = [(ev(), ev()) for _ in range(args.steps)]
@@ -448,6 +451,20 @@ def main():
         tdist.init_process_group("nccl")
         dist = tdist
     result = run_ours(args, rank, world, dist)
+    if args.targets_workload != "none":
+        import copy
+        targs = copy.copy(args)
+        targs.workload = args.targets_workload
+        targs.steps = max(3, min(args.steps, 10))
+        targs.settle_s = 0.3
+        targs.no_e2e = True
+        t = run_ours(targs, rank, world, dist, clocks_on=False)
+        result["targets"] = {"workload": t["config"], "fwd_tflops": t["kernels"]["fwd_tflops"],
+                             "fwd_frac_of_peak": t["kernels"]["fwd_frac_of_peak"],
+                             "bwd_tflops": t["kernels"]["bwd_tflops"],
+                             "bwd_frac_of_peak": t["kernels"]["bwd_frac_of_peak"],
+                             "bwd_main_tflops": t["kernels"]["bwd_main_tflops"],
+                             "steps": t["steps"], "gpu_launches": t["gpu_launches"]}
     if rank == 0 and not args.no_cpu_baseline:
         v, s, desc = oracle_sample(args.workload)
         result["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOPS", "cores": cpu_cores(),
