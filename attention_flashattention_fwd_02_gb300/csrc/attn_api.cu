@@ -2,6 +2,7 @@
 // workspace layout, TMA tensor-map encoding and kernel launches. Host code only.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -182,6 +183,16 @@ BwdWorkspace bwd_layout(int64_t B, int64_t H, int64_t rows, int64_t D) {
 
 bool valid_scale(float s) { return isfinite(s) && s > 0.f; }
 
+// Test hook for the failure-detection path: when the environment variable
+// ATTN_TEST_WITHHOLD_KV_TILE holds a key-tile index, the forward producer never loads that
+// tile and every wait is bounded by 50 ms, so the kernel gives up, reports
+// ATTN_ERR_DEVICE_TIMEOUT in the status word and returns (no trap, no fault).
+int withheld_tile_for_test() {
+  const char* v = getenv("ATTN_TEST_WITHHOLD_KV_TILE");
+  if (v == nullptr || *v == 0) return -1;
+  return atoi(v);
+}
+
 // ----------------------------------------------------------------------------- forward
 attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
                        const int32_t* cu_q, const int32_t* cu_k, int compact, int32_t num_seqs,
@@ -219,6 +230,8 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   p.causal = causal ? 1 : 0;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.status = reinterpret_cast<int*>(ws);
+  p.withhold_tile = withheld_tile_for_test();
+  p.timeout_ns = p.withhold_tile >= 0 ? 50000000ull : kWaitTimeoutNs;
   dim3 grid((pr.max_q + BM - 1) / BM, pr.H, pr.units);
   cudaError_t e = launch_attn_fwd(p, pr.D, grid, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

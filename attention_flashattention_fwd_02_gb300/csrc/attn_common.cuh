@@ -67,6 +67,8 @@ struct FwdParams {
   int causal;
   float scale_log2;               // sm_scale * log2(e)
   int* status;                    // device status word, may be null
+  uint64_t timeout_ns;            // bound on every pipeline wait
+  int withhold_tile;              // test hook: key tile the producer never loads (-1: none)
 };
 
 struct BwdPreParams {

@@ -153,8 +153,9 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
                       sv.row0_q + q_lo[t], h, sv.batch);
       for (int j = 0; j < n_max; ++j) {
         const int st = j % NST;
+        if (j == p.withhold_tile) continue;  // failure-detection test: this stage never fills
         if (j >= NST &&
-            !mbar_wait(smem_u32(&bars.kv_empty[st]), ((j / NST) - 1) & 1, abort, kWaitTimeoutNs))
+            !mbar_wait(smem_u32(&bars.kv_empty[st]), ((j / NST) - 1) & 1, abort, p.timeout_ns))
           break;
         const int krow = sv.row0_k + j * BN;
         const uint32_t kb = smem_u32(&bars.k_full[st]);
@@ -184,8 +185,8 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
           umma_ss(tS[t], desc_kmajor(qbase, BM, kk), desc_kmajor(kbase, BN, kk), idS, kk > 0);
         umma_commit(smem_u32(&bars.s_full[t]));
       };
-      bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort, kWaitTimeoutNs) &&
-                mbar_wait(smem_u32(&bars.k_full[0]), 0, abort, kWaitTimeoutNs);
+      bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort, p.timeout_ns) &&
+                mbar_wait(smem_u32(&bars.k_full[0]), 0, abort, p.timeout_ns);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
@@ -193,11 +194,11 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       }
       for (int j = 0; ok && j < n_max; ++j) {
         const int st = j % NST;
-        if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / NST) & 1, abort, kWaitTimeoutNs)) break;
+        if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / NST) & 1, abort, p.timeout_ns)) break;
         bool next_k_ready = false;
         for (int t = 0; t < 2; ++t) {
           if (j >= n_t[t]) continue;
-          if (!mbar_wait(smem_u32(&bars.p_full[t]), j & 1, abort, kWaitTimeoutNs)) {
+          if (!mbar_wait(smem_u32(&bars.p_full[t]), j & 1, abort, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
           if (j + 1 < n_t[t]) {
             if (!next_k_ready) {
               if (!mbar_wait(smem_u32(&bars.k_full[(j + 1) % NST]), ((j + 1) / NST) & 1, abort,
-                             kWaitTimeoutNs)) {
+                             p.timeout_ns)) {
                 ok = false;
                 break;
               }
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; ok && j < n; ++j) {
-      if (!mbar_wait(smem_u32(&bars.s_full[t]), j & 1, abort, kWaitTimeoutNs)) {
+      if (!mbar_wait(smem_u32(&bars.s_full[t]), j & 1, abort, p.timeout_ns)) {
         ok = false;
         break;
       }
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       l = l * scale + (a0 + a1);
       m_use = m_new;
       if (j > 0) {
-        if (!mbar_wait(smem_u32(&bars.o_done[t]), (j - 1) & 1, abort, kWaitTimeoutNs)) {
+        if (!mbar_wait(smem_u32(&bars.o_done[t]), (j - 1) & 1, abort, p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       mbar_arrive(smem_u32(&bars.p_full[t]));
     }
     if (n > 0) {
-      if (ok) ok = mbar_wait(smem_u32(&bars.o_done[t]), (n - 1) & 1, abort, kWaitTimeoutNs);
+      if (ok) ok = mbar_wait(smem_u32(&bars.o_done[t]), (n - 1) & 1, abort, p.timeout_ns);
       tc_fence_after();
     }
     if (ok) {
