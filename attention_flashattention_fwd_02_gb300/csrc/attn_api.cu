@@ -166,6 +166,21 @@ attn_status make_map(CUtensorMap* m, const attn_tensor4* t, int box_rows) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// 2-D fp32 tensor map over the dQ accumulator viewed as [rows][D]: box (32, 128), 128-byte
+// swizzle (32 floats = 128 bytes per box row).
+attn_status make_map_acc(CUtensorMap* m, float* acc, int64_t rows, int64_t D) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct BwdWorkspace {
@@ -281,6 +296,9 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       if ((s = make_map(&p.tm_do, a.dout, BM)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_k, a.k, BN)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_v, a.v, BN)) != ATTN_OK) return s;
+      if (pr.D == 64 &&
+          (s = make_map_acc(&p.tm_dq, dq_acc, (int64_t)pr.B * pr.H * pr.Sq, pr.D)) != ATTN_OK)
+        return s;
       p.lse = reinterpret_cast<const float*>(a.lse->data);
       p.l_sb = a.lse->stride[0]; p.l_sh = a.lse->stride[1]; p.l_ss = a.lse->stride[2];
       p.delta = delta;

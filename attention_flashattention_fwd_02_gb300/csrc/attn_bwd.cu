@@ -156,6 +156,7 @@ struct BwdBars {
   uint64_t s_full, p_full;
   uint64_t ds_full[2], ds_empty[2];
   uint64_t dq_full, dq_empty, dkdv_full;
+  uint64_t wg_sync[2];  // per-compute-warpgroup rendezvous (bounded, unlike bar.sync)
   uint32_t tmem_base;
   int abort;
   alignas(16) float nlse2[QST][BM];   // -LSE * log2(e) of the step's query rows
@@ -237,6 +238,8 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_empty), 256);
     mbar_init(smem_u32(&bars.dkdv_full), 1);
+    mbar_init(smem_u32(&bars.wg_sync[0]), 128);
+    mbar_init(smem_u32(&bars.wg_sync[1]), 128);
     mbar_fence_init();
   }
   if (warp == C::WARP_MMA) {
@@ -364,6 +367,15 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     const float c2 = p.scale_log2;
     const int c_base = g * HALF;
     float* acc_base = p.dq_acc + (zh * p.rows_q + sv.row0_q) * D;
+    // Rendezvous of the 128 threads of this warpgroup through an mbarrier, so that the wait
+    // is bounded like every other wait of the kernel.
+    uint32_t wg_phase = 0;
+    auto wg_sync = [&]() -> bool {
+      mbar_arrive(smem_u32(&bars.wg_sync[g]));
+      const bool r = mbar_wait(smem_u32(&bars.wg_sync[g]), wg_phase, abort, kWaitTimeoutNs);
+      wg_phase ^= 1;
+      return r;
+    };
     // Drains warpgroup g's 32 columns of the dQ partial of step itd from TMEM into the fp32
     // accumulator with fire-and-forget reductions. dQ^T (d_head 128): lanes are d, columns
     // are the step's query rows; dQ (d_head 64): lanes are query rows, columns are d.
@@ -388,12 +400,23 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
             if (i < nvalid) red_add_f32(col + (int64_t)i * D, v[i]);
         }
       } else {
-        const int q = q_lo_d + j;
-        if (q < sv.len_q) {
-          float* row = acc_base + (int64_t)q * D + g * 32;
+        // Lanes hold query rows. The warpgroup stages its 128 x 32 fp32 block in its own slab
+        // of the dS^T buffer of step itd (the dK / dQ MMAs of that step are complete and the
+        // slab is rewritten by this warpgroup only two steps later, after the reduce has read
+        // it), then one thread reduces the block into the accumulator with a single TMA
+        // reduce-add. Rows past the sequence carry exact zeros (their dS was masked), so the
+        // whole box can be added.
+        uint8_t* stage = smem + C::OFF_DS + (itd & 1) * C::DS_BYTES + g * (C::DS_BYTES / 2);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            red_add_v4_f32(row + 4 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(stage + j * 128 + 16 * (c ^ (j & 7))) =
+              make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        fence_proxy_async_smem();
+        if (!wg_sync()) return false;
+        if (j == 0) {
+          tma_reduce_add_2d(&p.tm_dq, smem_u32(stage), g * 32,
+                            (int)(zh * p.rows_q + sv.row0_q + q_lo_d));
+          bulk_commit_group();
         }
       }
       return true;
@@ -418,6 +441,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         break;
       }
       uint8_t* gDS = smem + C::OFF_DS + bs * C::DS_BYTES;
+      if (!C::DQ_T && it >= 2) {
+        // this warpgroup's slab of the buffer staged dQ two steps ago: wait for that reduce
+        if (j == 0) bulk_wait_group_read0();
+        if (!wg_sync()) {
+          ok = false;
+          break;
+        }
+      }
       // All of this warpgroup's S^T and dP^T columns are fetched behind one wait.
       float sv_all[HALF], dpv_all[HALF];
       if constexpr (HALF == 64) {
@@ -486,6 +517,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       }
     }
     if (ok && n_steps > 0) ok = drain_dq(n_steps - 1);
+    if (!C::DQ_T && j == 0) bulk_wait_group0();  // reduces complete before the CTA exits
     // ---- epilogue: dK = sm_scale * acc, dV = acc; warpgroup g writes columns [g*D/2, +D/2)
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, kWaitTimeoutNs);
     tc_fence_after();
