@@ -1,0 +1,66 @@
+"""The training-facing autograd layer against the float64 oracle (GPU), and its layout
+helpers (CPU)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention_ref as ref
+from attention_flashattention_fwd_02_gb300.autograd import (
+    bhsd_to_thd, bshd_to_bhsd, flash_attention, flash_attention_varlen, thd_to_bhsd)
+
+from _helpers import assert_fwd_close, assert_grads_close, np64
+
+
+def test_layout_helpers_are_views():
+    x = torch.randn(10, 3, 64)
+    v = thd_to_bhsd(x)
+    assert v.shape == (1, 3, 10, 64) and v.data_ptr() == x.data_ptr()
+    assert torch.equal(bhsd_to_thd(v), x)
+    y = torch.randn(2, 7, 3, 64)
+    w = bshd_to_bhsd(y)
+    assert w.shape == (2, 3, 7, 64) and w.stride() == (7 * 3 * 64, 64, 3 * 64, 1)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,causal,bshd", [(64, True, False), (128, False, True)])
+def test_autograd_dense(D, causal, bshd):
+    gen = torch.Generator().manual_seed(D + causal)
+    B, H, S = 2, 2, 200
+    shape = (B, S, H, D) if bshd else (B, H, S, D)
+    base = [torch.randn(shape, generator=gen).bfloat16().cuda().requires_grad_(True)
+            for _ in range(3)]
+    q, k, v = (bshd_to_bhsd(t) if bshd else t for t in base)
+    w = torch.randn(B, H, S, D, generator=gen).bfloat16().cuda()
+    o = flash_attention(q, k, v, causal=causal)
+    (o.float() * w.float()).sum().backward()
+    scale = 1.0 / math.sqrt(D)
+    qn, kn, vn, wn = (np64(t) for t in (q, k, v, w))
+    o_r, lse_r = ref.fwd_bhsd(qn, kn, vn, scale, causal)
+    g_r = ref.bwd_bhsd(qn, kn, vn, wn, scale, causal)
+    assert_fwd_close(o.detach(), torch.zeros(lse_r.shape), o_r, np.zeros_like(lse_r), what="autograd")
+    grads = [bshd_to_bhsd(t.grad) if bshd else t.grad for t in base]
+    assert_grads_close(grads, g_r, what="autograd")
+
+
+@pytest.mark.gpu
+def test_autograd_varlen_thd():
+    gen = torch.Generator().manual_seed(77)
+    lengths = [50, 130, 7]
+    T, H, D = sum(lengths), 2, 128
+    q, k, v = (torch.randn(T, H, D, generator=gen).bfloat16().cuda().requires_grad_(True)
+               for _ in range(3))
+    w = torch.randn(T, H, D, generator=gen).bfloat16().cuda()
+    cu = torch.tensor([0, 50, 180, 187], dtype=torch.int32, device="cuda")
+    o = flash_attention_varlen(q, k, v, cu, cu, max_seqlen_q=130, max_seqlen_k=130, causal=True)
+    assert o.shape == (T, H, D)
+    (o.float() * w.float()).sum().backward()
+    scale = 1.0 / math.sqrt(D)
+    qn, kn, vn, wn = (np64(thd_to_bhsd(t)) for t in (q, k, v, w))
+    cun = cu.cpu().numpy()
+    o_r, lse_r = ref.fwd_compact_varlen(qn, kn, vn, cun, cun, scale, True)
+    g_r = ref.bwd_compact_varlen(qn, kn, vn, wn, cun, cun, scale, True)
+    assert_fwd_close(thd_to_bhsd(o.detach()), torch.zeros(lse_r.shape), o_r, np.zeros_like(lse_r),
+                     what="autograd varlen")
+    assert_grads_close([thd_to_bhsd(t.grad) for t in (q, k, v)], g_r, what="autograd varlen")
