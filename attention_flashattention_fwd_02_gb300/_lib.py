@@ -34,7 +34,11 @@ EXPORTED_SYMBOLS = (
 
 class Tensor4(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("size", ctypes.c_int64 * 4),
-                ("stride", ctypes.c_int64 * 4)]
+                ("stride", ctypes.c_int64 * 4), ("dtype", ctypes.c_int32)]
+
+
+# attn_dtype codes of include/attn.h
+DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1}
 
 
 class Tensor3(ctypes.Structure):
@@ -117,6 +121,7 @@ def _t4(t: Optional[torch.Tensor]):
     v.data = t.data_ptr()
     v.size[:] = list(t.shape)
     v.stride[:] = list(t.stride())
+    v.dtype = DTYPE_CODES.get(t.dtype, -1)
     return ctypes.byref(v), v
 
 
@@ -132,10 +137,11 @@ def _t3(t: Optional[torch.Tensor]):
     return ctypes.byref(v), v
 
 
-def _bf16(*ts):
+def _check16(*ts):
+    """Rank-4 tensors must be bf16 or fp16 (the library checks that they agree)."""
     for t in ts:
-        if t is not None and t.dtype != torch.bfloat16:
-            raise TypeError(f"expected bfloat16 tensors, got {t.dtype}")
+        if t is not None and t.dtype not in DTYPE_CODES:
+            raise TypeError(f"expected bfloat16 or float16 tensors, got {t.dtype}")
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -179,7 +185,7 @@ def attn_bwd_workspace_size(B: int, H: int, Sq: int, D: int) -> int:
 
 def attn_fwd(q, k, v, o, lse, sm_scale, causal, cu_seqlens_q=None, cu_seqlens_k=None,
              workspace=None, stream=None, _name="attn_fwd"):
-    _bf16(q, k, v, o)
+    _check16(q, k, v, o)
     tq, tk, tv, to, tl = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse)
     ws, nws = _ws(workspace)
     f = getattr(load(), _name)
@@ -196,7 +202,7 @@ def attn_fwd_padded_varlen(q, k, v, o, lse, sm_scale, causal, cu_seqlens_q, cu_s
 def attn_fwd_compact_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs,
                             max_seqlen_q, max_seqlen_k, sm_scale, causal, workspace=None,
                             stream=None):
-    _bf16(q, k, v, o)
+    _check16(q, k, v, o)
     tq, tk, tv, to, tl = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse)
     ws, nws = _ws(workspace)
     _check(load().attn_fwd_compact_varlen(
@@ -207,7 +213,7 @@ def attn_fwd_compact_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seq
 
 def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, workspace,
              cu_seqlens_q=None, cu_seqlens_k=None, stream=None, _name="attn_bwd"):
-    _bf16(q, k, v, o, dout, dq, dk, dv)
+    _check16(q, k, v, o, dout, dq, dk, dv)
     tq, tk, tv, to, tl, tdo = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse), _t4(dout)
     tdq, tdk, tdv = _t4(dq), _t4(dk), _t4(dv)
     ws, nws = _ws(workspace)
@@ -226,7 +232,7 @@ def attn_bwd_padded_varlen(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, 
 def attn_bwd_compact_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
                             num_seqs, max_seqlen_q, max_seqlen_k, sm_scale, causal, workspace,
                             stream=None):
-    _bf16(q, k, v, o, dout, dq, dk, dv)
+    _check16(q, k, v, o, dout, dq, dk, dv)
     tq, tk, tv, to, tl, tdo = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse), _t4(dout)
     tdq, tdk, tdv = _t4(dq), _t4(dk), _t4(dv)
     ws, nws = _ws(workspace)
@@ -238,7 +244,7 @@ def attn_bwd_compact_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_
 
 def attn_bwd_preprocess(o, dout, workspace, cu_seqlens_q=None, num_seqs=-1, max_seqlen_q=0,
                         stream=None):
-    _bf16(o, dout)
+    _check16(o, dout)
     to, tdo = _t4(o), _t4(dout)
     ws, nws = _ws(workspace)
     _check(load().attn_bwd_preprocess(*_keep(to, tdo), _ptr(cu_seqlens_q), int(num_seqs),
@@ -248,7 +254,7 @@ def attn_bwd_preprocess(o, dout, workspace, cu_seqlens_q=None, num_seqs=-1, max_
 
 def attn_bwd_main(q, k, v, lse, dout, dk, dv, sm_scale, causal, workspace, cu_seqlens_q=None,
                   cu_seqlens_k=None, num_seqs=-1, max_seqlen_q=0, max_seqlen_k=0, stream=None):
-    _bf16(q, k, v, dout, dk, dv)
+    _check16(q, k, v, dout, dk, dv)
     tq, tk, tv, tl, tdo, tdk, tdv = _t4(q), _t4(k), _t4(v), _t3(lse), _t4(dout), _t4(dk), _t4(dv)
     ws, nws = _ws(workspace)
     _check(load().attn_bwd_main(*_keep(tq, tk, tv, tl, tdo), _ptr(cu_seqlens_q),
@@ -259,7 +265,7 @@ def attn_bwd_main(q, k, v, lse, dout, dk, dv, sm_scale, causal, workspace, cu_se
 
 def attn_bwd_dq_epilogue(dq, sm_scale, workspace, cu_seqlens_q=None, num_seqs=-1,
                          max_seqlen_q=0, stream=None):
-    _bf16(dq)
+    _check16(dq)
     tdq = _t4(dq)
     ws, nws = _ws(workspace)
     _check(load().attn_bwd_dq_epilogue(*_keep(tdq), _ptr(cu_seqlens_q), int(num_seqs),
@@ -278,7 +284,7 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, cu_seq
                      cu_seqlens_k=None, stream=None):
     """attn_bwd without a workspace argument: the library's fixed device scratch array is
     used (for callers that cannot allocate; see include/attn.h)."""
-    _bf16(q, k, v, o, dout, dq, dk, dv)
+    _check16(q, k, v, o, dout, dq, dk, dv)
     tq, tk, tv, to, tl, tdo = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse), _t4(dout)
     tdq, tdk, tdv = _t4(dq), _t4(dk), _t4(dv)
     _check(load().attn_bwd_noalloc(*_keep(tq, tk, tv, to, tl, tdo), _ptr(cu_seqlens_q),

@@ -36,7 +36,7 @@ def bhsd_to_thd(x: torch.Tensor) -> torch.Tensor:
 
 
 class FlashAttentionFunction(torch.autograd.Function):
-    """Fused attention with gradients for q, k, v (bf16, BHSD views)."""
+    """Fused attention with gradients for q, k, v (bf16 or fp16, BHSD views)."""
 
     @staticmethod
     def forward(ctx, q, k, v, sm_scale, causal, cu_seqlens_q, cu_seqlens_k, compact,

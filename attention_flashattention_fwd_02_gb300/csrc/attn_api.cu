@@ -49,6 +49,7 @@ attn_status check_device() {
 // ----------------------------------------------------------------------------- validation
 attn_status check_tensor4(const attn_tensor4* t) {
   if (t == nullptr || t->data == nullptr) return ATTN_ERR_NULL;
+  if (t->dtype != ATTN_DTYPE_BF16 && t->dtype != ATTN_DTYPE_F16) return ATTN_ERR_UNSUPPORTED;
   for (int i = 0; i < 4; ++i)
     if (t->size[i] < 0 || t->size[i] > kMaxI32) return ATTN_ERR_SHAPE;
   if (t->stride[3] != 1) return ATTN_ERR_STRIDE;
@@ -68,6 +69,8 @@ attn_status check_tensor3(const attn_tensor3* t) {
   return ATTN_OK;
 }
 
+bool same_dtype(const attn_tensor4* a, const attn_tensor4* b) { return a->dtype == b->dtype; }
+
 bool same_shape(const attn_tensor4* a, const attn_tensor4* b) {
   for (int i = 0; i < 4; ++i)
     if (a->size[i] != b->size[i]) return false;
@@ -78,6 +81,7 @@ bool same_shape(const attn_tensor4* a, const attn_tensor4* b) {
 struct Problem {
   int mode;          // kDense / kPadded / kCompact
   int B, H, Sq, Sk, D;
+  bool f16;          // element type of every rank-4 tensor
   int units;         // grid z: B, or num_seqs for compact
   int max_q, max_k;  // per-unit length bounds (grid extents)
   const int* cu_q;
@@ -93,6 +97,7 @@ attn_status make_problem(const attn_tensor4* q, const attn_tensor4* k, const att
   if ((s = check_tensor4(k)) != ATTN_OK) return s;
   if ((s = check_tensor4(v)) != ATTN_OK) return s;
   if (!same_shape(k, v)) return ATTN_ERR_SHAPE;
+  if (!same_dtype(q, k) || !same_dtype(q, v)) return ATTN_ERR_DTYPE;
   if (q->size[0] != k->size[0] || q->size[1] != k->size[1] || q->size[3] != k->size[3])
     return ATTN_ERR_SHAPE;
   const int64_t D = q->size[3];
@@ -103,6 +108,7 @@ attn_status make_problem(const attn_tensor4* q, const attn_tensor4* k, const att
   pr->Sq = (int)q->size[2];
   pr->Sk = (int)k->size[2];
   pr->D = (int)D;
+  pr->f16 = q->dtype == ATTN_DTYPE_F16;
   if (compact) {
     if (q->size[0] != 1) return ATTN_ERR_SHAPE;  // compact varlen takes batch exactly 1
     if (cu_q == nullptr || cu_k == nullptr) return ATTN_ERR_NULL;
@@ -160,7 +166,9 @@ attn_status make_map(CUtensorMap* m, const attn_tensor4* t, int box_rows) {
     if (strides[i] % 16 != 0 || strides[i] >= (1ull << 40)) return ATTN_ERR_STRIDE;
   cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, es,
+  const CUtensorMapDataType ty =
+      t->dtype == ATTN_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(m, ty, 4, t->data, dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
@@ -219,6 +227,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   if (s != ATTN_OK) return s;
   if ((s = check_tensor4(o)) != ATTN_OK) return s;
   if (!same_shape(q, o)) return ATTN_ERR_SHAPE;
+  if (!same_dtype(q, o)) return ATTN_ERR_DTYPE;
   if ((s = check_lse(lse, pr)) != ATTN_OK) return s;
   if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
   if (ws != nullptr && ws_bytes < attn_fwd_workspace_size(pr.B, pr.H, pr.Sq, pr.D))
@@ -233,7 +242,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   if ((s = make_map(&p.tm_q, q, fwd_box_rows())) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_k, k, 128)) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_v, v, 128)) != ATTN_OK) return s;
-  p.o = reinterpret_cast<__nv_bfloat16*>(o->data);
+  p.o = reinterpret_cast<uint16_t*>(o->data);
   p.o_sb = o->stride[0];
   p.o_sh = o->stride[1];
   p.o_ss = o->stride[2];
@@ -248,7 +257,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   p.withhold_tile = withheld_tile_for_test();
   p.timeout_ns = p.withhold_tile >= 0 ? 50000000ull : kWaitTimeoutNs;
   dim3 grid((pr.max_q + BM - 1) / BM, pr.H, pr.units);
-  cudaError_t e = launch_attn_fwd(p, pr.D, grid, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_attn_fwd(p, pr.D, pr.f16, grid, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -276,8 +285,9 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
   if (stage_mask & 1) {
     BwdPreParams pp;
     memset(&pp, 0, sizeof(pp));
-    pp.o = reinterpret_cast<const __nv_bfloat16*>(a.o->data);
-    pp.dout = reinterpret_cast<const __nv_bfloat16*>(a.dout->data);
+    pp.o = reinterpret_cast<const uint16_t*>(a.o->data);
+    pp.dout = reinterpret_cast<const uint16_t*>(a.dout->data);
+    pp.f16 = pr.f16 ? 1 : 0;
     pp.o_sb = a.o->stride[0]; pp.o_sh = a.o->stride[1]; pp.o_ss = a.o->stride[2];
     pp.do_sb = a.dout->stride[0]; pp.do_sh = a.dout->stride[1]; pp.do_ss = a.dout->stride[2];
     pp.delta = delta;
@@ -303,9 +313,9 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       p.l_sb = a.lse->stride[0]; p.l_sh = a.lse->stride[1]; p.l_ss = a.lse->stride[2];
       p.delta = delta;
       p.dq_acc = dq_acc;
-      p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk->data);
+      p.dk = reinterpret_cast<uint16_t*>(a.dk->data);
       p.dk_sb = a.dk->stride[0]; p.dk_sh = a.dk->stride[1]; p.dk_ss = a.dk->stride[2];
-      p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv->data);
+      p.dv = reinterpret_cast<uint16_t*>(a.dv->data);
       p.dv_sb = a.dv->stride[0]; p.dv_sh = a.dv->stride[1]; p.dv_ss = a.dv->stride[2];
       p.H = pr.H;
       p.rows_q = pr.Sq;
@@ -315,14 +325,15 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       p.sm_scale = sm_scale;
       p.status = status;
       dim3 grid((pr.max_k + BN - 1) / BN, pr.H, pr.units);
-      if (launch_bwd_main(p, pr.D, grid, st) != cudaSuccess) return ATTN_ERR_CUDA;
+      if (launch_bwd_main(p, pr.D, pr.f16, grid, st) != cudaSuccess) return ATTN_ERR_CUDA;
     }
   }
   if (stage_mask & 4) {
     BwdPostParams pp;
     memset(&pp, 0, sizeof(pp));
     pp.dq_acc = dq_acc;
-    pp.dq = reinterpret_cast<__nv_bfloat16*>(a.dq->data);
+    pp.dq = reinterpret_cast<uint16_t*>(a.dq->data);
+    pp.f16 = pr.f16 ? 1 : 0;
     pp.dq_sb = a.dq->stride[0]; pp.dq_sh = a.dq->stride[1]; pp.dq_ss = a.dq->stride[2];
     pp.units = pr.units; pp.H = pr.H; pp.rows = pr.Sq; pp.D = pr.D;
     pp.seq = sa;
@@ -343,11 +354,13 @@ attn_status bwd_common(const BwdArgs& a, const int32_t* cu_q, const int32_t* cu_
   for (const attn_tensor4* t : qshaped) {
     if ((s = check_tensor4(t)) != ATTN_OK) return s;
     if (!same_shape(a.q, t)) return ATTN_ERR_SHAPE;
+    if (!same_dtype(a.q, t)) return ATTN_ERR_DTYPE;
   }
   const attn_tensor4* kshaped[] = {a.dk, a.dv};
   for (const attn_tensor4* t : kshaped) {
     if ((s = check_tensor4(t)) != ATTN_OK) return s;
     if (!same_shape(a.k, t)) return ATTN_ERR_SHAPE;
+    if (!same_dtype(a.q, t)) return ATTN_ERR_DTYPE;
   }
   if ((s = check_lse(a.lse, pr)) != ATTN_OK) return s;
   if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
@@ -444,6 +457,7 @@ attn_status attn_bwd_preprocess(const attn_tensor4* o, const attn_tensor4* dout,
   if (s != ATTN_OK) return s;
   if ((s = check_tensor4(dout)) != ATTN_OK) return s;
   if (!same_shape(o, dout)) return ATTN_ERR_SHAPE;
+  if (!same_dtype(o, dout)) return ATTN_ERR_DTYPE;
   BwdArgs a{o, o, o, o, dout, nullptr, nullptr, nullptr, nullptr};
   return bwd_stage(1, a, pr, 1.f, 0, workspace, workspace_bytes, stream);
 }
@@ -462,10 +476,12 @@ attn_status attn_bwd_main(const attn_tensor4* q, const attn_tensor4* k, const at
   if (s != ATTN_OK) return s;
   if ((s = check_tensor4(dout)) != ATTN_OK) return s;
   if (!same_shape(q, dout)) return ATTN_ERR_SHAPE;
+  if (!same_dtype(q, dout)) return ATTN_ERR_DTYPE;
   const attn_tensor4* kshaped[] = {dk, dv};
   for (const attn_tensor4* t : kshaped) {
     if ((s = check_tensor4(t)) != ATTN_OK) return s;
     if (!same_shape(k, t)) return ATTN_ERR_SHAPE;
+    if (!same_dtype(q, t)) return ATTN_ERR_DTYPE;
   }
   if ((s = check_lse(lse, pr)) != ATTN_OK) return s;
   if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
@@ -505,11 +521,13 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_SHAPE: return "inconsistent tensor sizes";
     case ATTN_ERR_STRIDE: return "unsupported strides (D stride must be 1, others multiples of 8)";
     case ATTN_ERR_ALIGN: return "base pointer not 16-byte aligned";
-    case ATTN_ERR_UNSUPPORTED: return "unsupported case (d_head, device, sm_scale or size limits)";
+    case ATTN_ERR_UNSUPPORTED:
+      return "unsupported case (d_head, element type, device, sm_scale or size limits)";
     case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
     case ATTN_ERR_CUDA: return "CUDA runtime or driver error";
     case ATTN_ERR_DEVICE_BAD_SEQLENS: return "device: inconsistent cu_seqlens (sequence skipped)";
     case ATTN_ERR_DEVICE_TIMEOUT: return "device: pipeline wait timed out";
+    case ATTN_ERR_DTYPE: return "tensors of one call have different element types";
   }
   return "unknown status";
 }

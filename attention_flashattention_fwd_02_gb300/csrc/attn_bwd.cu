@@ -12,7 +12,7 @@
 //                              dQ_m partial = dS K_n      (tcgen05, TMEM) -> fp32 atomics
 //                            then dK * sm_scale and dV are written. P is rebuilt from the
 //                            LSE that the forward pass stashed.
-//  3. attn_bwd_post_kernel   dQ = bf16(sm_scale * accumulator). Memory-bound.
+//  3. attn_bwd_post_kernel   dQ = sm_scale * accumulator, rounded to the element type.
 //
 // Main-kernel warp roles (320 threads): warps 0..7 are two compute warpgroups that split
 // the query columns of each key row (thread row j = TMEM lane j) to form P^T (written to
@@ -36,7 +36,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // =========================================================================== preprocess
 // One group of D/8 threads per row: each thread reads 8 elements (16 bytes) of O and dO.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant__ BwdPreParams p) {
   constexpr int TPR = D / 8;             // threads per row
   constexpr int ROWS = 256 / TPR;        // rows per block
@@ -54,12 +54,11 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant
                                                     grow * p.o_ss + part * 8);
     const uint4 b = *reinterpret_cast<const uint4*>(p.dout + sv.batch * p.do_sb + h * p.do_sh +
                                                     grow * p.do_ss + part * 8);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 fa = __bfloat1622float2(a2[e]);
-      const float2 fb = __bfloat1622float2(b2[e]);
+      const float2 fa = unpack2<F16>(aw[e]);
+      const float2 fb = unpack2<F16>(bw[e]);
       acc = fmaf(fa.x, fb.x, acc);
       acc = fmaf(fa.y, fb.y, acc);
     }
@@ -80,15 +79,18 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream) {
   const int max_len = p.seq.mode == kCompact ? p.seq.max_q : p.seq.Sq;
   dim3 grid((max_len + rows_per_block - 1) / rows_per_block, p.H, p.units);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  if (p.D == 128)
-    attn_bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(p);
-  else
-    attn_bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(p);
+  if (p.D == 128) {
+    if (p.f16) attn_bwd_pre_kernel<128, true><<<grid, 256, 0, stream>>>(p);
+    else attn_bwd_pre_kernel<128, false><<<grid, 256, 0, stream>>>(p);
+  } else {
+    if (p.f16) attn_bwd_pre_kernel<64, true><<<grid, 256, 0, stream>>>(p);
+    else attn_bwd_pre_kernel<64, false><<<grid, 256, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
 // =========================================================================== dQ epilogue
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const __grid_constant__ BwdPostParams p) {
   constexpr int TPR = D / 8;
   constexpr int ROWS = 256 / TPR;
@@ -103,10 +105,10 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const __grid_constan
   const float4* src = reinterpret_cast<const float4*>(p.dq_acc + idx * D + part * 8);
   const float4 a = src[0], b = src[1];
   uint4 v;
-  v.x = pack_bf16x2(a.x * p.sm_scale, a.y * p.sm_scale);
-  v.y = pack_bf16x2(a.z * p.sm_scale, a.w * p.sm_scale);
-  v.z = pack_bf16x2(b.x * p.sm_scale, b.y * p.sm_scale);
-  v.w = pack_bf16x2(b.z * p.sm_scale, b.w * p.sm_scale);
+  v.x = pack2<F16>(a.x * p.sm_scale, a.y * p.sm_scale);
+  v.y = pack2<F16>(a.z * p.sm_scale, a.w * p.sm_scale);
+  v.z = pack2<F16>(b.x * p.sm_scale, b.y * p.sm_scale);
+  v.w = pack2<F16>(b.z * p.sm_scale, b.w * p.sm_scale);
   *reinterpret_cast<uint4*>(p.dq + sv.batch * p.dq_sb + h * p.dq_sh + grow * p.dq_ss + part * 8) = v;
 }
 
@@ -115,10 +117,13 @@ cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream) 
   const int max_len = p.seq.mode == kCompact ? p.seq.max_q : p.seq.Sq;
   dim3 grid((max_len + rows_per_block - 1) / rows_per_block, p.H, p.units);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  if (p.D == 128)
-    attn_bwd_post_kernel<128><<<grid, 256, 0, stream>>>(p);
-  else
-    attn_bwd_post_kernel<64><<<grid, 256, 0, stream>>>(p);
+  if (p.D == 128) {
+    if (p.f16) attn_bwd_post_kernel<128, true><<<grid, 256, 0, stream>>>(p);
+    else attn_bwd_post_kernel<128, false><<<grid, 256, 0, stream>>>(p);
+  } else {
+    if (p.f16) attn_bwd_post_kernel<64, true><<<grid, 256, 0, stream>>>(p);
+    else attn_bwd_post_kernel<64, false><<<grid, 256, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
@@ -139,7 +144,7 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_DO + QST * Q_BYTES; // 2 buffers
   static constexpr int SMEM_BYTES = OFF_DS + 2 * DS_BYTES + 1024;
   // TMEM columns: dK, dV accumulators; S^T, dP^T of the current step; the dQ partial; and P^T
-  // (bf16, two values per column) as the A operand of the dV MMA.
+  // (16-bit, two values per column) as the A operand of the dV MMA.
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_DK = 0, COL_DV = D, COL_S = 2 * D, COL_DP = 2 * D + BM;
   static constexpr uint32_t COL_DQ = 2 * D + 2 * BM;
@@ -172,7 +177,7 @@ __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float
                : "memory");
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int BN = C::BN, BM = C::BM;
@@ -206,8 +211,8 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       const int key = k_lo + threadIdx.x;
       if (key < sv.len_k) {
         const int64_t grow = sv.row0_k + key;
-        __nv_bfloat16* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
-        __nv_bfloat16* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
+        uint16_t* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
+        uint16_t* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
         for (int d = 0; d < D; d += 8) {
           *reinterpret_cast<uint4*>(kr + d) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(vr + d) = make_uint4(0, 0, 0, 0);
@@ -302,10 +307,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     // Issue order per step: dV(it) [P from TMEM], S/dP(it+1), dK(it), dQ(it). The S/dP MMAs
     // of the next step overlap the P/dS math of the compute warpgroups.
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, BM, false, false);  // S^T, dP^T
-      constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);    // dV, dK
-      constexpr uint32_t idQ = C::DQ_T ? idesc_bf16_f32(128, BM, true, true)  // dQ^T
-                                       : idesc_bf16_f32(128, D, true, true);  // dQ
+      constexpr uint32_t idS = idesc_f32acc(128, BM, false, false, F16);  // S^T, dP^T
+      constexpr uint32_t idG = idesc_f32acc(128, D, false, true, F16);    // dV, dK
+      constexpr uint32_t idQ = C::DQ_T ? idesc_f32acc(128, BM, true, true, F16)  // dQ^T
+                                       : idesc_f32acc(128, D, true, true, F16);  // dQ
       const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP, tP = tmem + C::COL_P;
       const uint32_t tDK = tmem + C::COL_DK, tDV = tmem + C::COL_DV, tDQ = tmem + C::COL_DQ;
       auto issue_sdp = [&](int it) -> bool {
@@ -492,10 +497,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
               ds[u] = valid ? ds[u] : 0.f;
             }
           }
-          pp[e4 / 2] = pack_bf16x2(pv[0], pv[1]);
-          pp[e4 / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-          pd[e4 / 2] = pack_bf16x2(ds[0], ds[1]);
-          pd[e4 / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+          pp[e4 / 2] = pack2<F16>(pv[0], pv[1]);
+          pp[e4 / 2 + 1] = pack2<F16>(pv[2], pv[3]);
+          pd[e4 / 2] = pack2<F16>(ds[0], ds[1]);
+          pd[e4 / 2 + 1] = pack2<F16>(ds[2], ds[3]);
         }
         ATTN_TMEM_ST_X16(tmem + C::COL_P + lane_off + c0 / 2, pp);
 #pragma unroll
@@ -523,8 +528,8 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     tc_fence_after();
     if (ok) {
       const int64_t grow = sv.row0_k + key;
-      __nv_bfloat16* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
-      __nv_bfloat16* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
+      uint16_t* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
+      uint16_t* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
       const float sc = p.sm_scale;
 #pragma unroll
       for (int c = g * (D / 2); c < (g + 1) * (D / 2); c += 32) {
@@ -534,14 +539,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 vk, vv;
-            vk.x = pack_bf16x2(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc);
-            vk.y = pack_bf16x2(__uint_as_float(a[e + 2]) * sc, __uint_as_float(a[e + 3]) * sc);
-            vk.z = pack_bf16x2(__uint_as_float(a[e + 4]) * sc, __uint_as_float(a[e + 5]) * sc);
-            vk.w = pack_bf16x2(__uint_as_float(a[e + 6]) * sc, __uint_as_float(a[e + 7]) * sc);
-            vv.x = pack_bf16x2(__uint_as_float(b[e]), __uint_as_float(b[e + 1]));
-            vv.y = pack_bf16x2(__uint_as_float(b[e + 2]), __uint_as_float(b[e + 3]));
-            vv.z = pack_bf16x2(__uint_as_float(b[e + 4]), __uint_as_float(b[e + 5]));
-            vv.w = pack_bf16x2(__uint_as_float(b[e + 6]), __uint_as_float(b[e + 7]));
+            vk.x = pack2<F16>(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc);
+            vk.y = pack2<F16>(__uint_as_float(a[e + 2]) * sc, __uint_as_float(a[e + 3]) * sc);
+            vk.z = pack2<F16>(__uint_as_float(a[e + 4]) * sc, __uint_as_float(a[e + 5]) * sc);
+            vk.w = pack2<F16>(__uint_as_float(a[e + 6]) * sc, __uint_as_float(a[e + 7]) * sc);
+            vv.x = pack2<F16>(__uint_as_float(b[e]), __uint_as_float(b[e + 1]));
+            vv.y = pack2<F16>(__uint_as_float(b[e + 2]), __uint_as_float(b[e + 3]));
+            vv.z = pack2<F16>(__uint_as_float(b[e + 4]), __uint_as_float(b[e + 5]));
+            vv.w = pack2<F16>(__uint_as_float(b[e + 6]), __uint_as_float(b[e + 7]));
             *reinterpret_cast<uint4*>(kr + c + e) = vk;
             *reinterpret_cast<uint4*>(vr + c + e) = vv;
           }
@@ -559,25 +564,28 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
   if (threadIdx.x == 0 && bars.abort && p.status != nullptr) atomicCAS(p.status, 0, kStatusTimeout);
 }
 
-template <int D>
+template <int D, bool F16>
 static cudaError_t launch_bwd_main_impl(const BwdParams& p, dim3 grid, cudaStream_t stream) {
   using C = BwdCfg<D>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  attn_bwd_main_kernel<D><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
+  attn_bwd_main_kernel<D, F16><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main(const BwdParams& p, int D, dim3 grid, cudaStream_t stream) {
-  return D == 128 ? launch_bwd_main_impl<128>(p, grid, stream)
-                  : launch_bwd_main_impl<64>(p, grid, stream);
+cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, dim3 grid, cudaStream_t stream) {
+  if (D == 128)
+    return f16 ? launch_bwd_main_impl<128, true>(p, grid, stream)
+               : launch_bwd_main_impl<128, false>(p, grid, stream);
+  return f16 ? launch_bwd_main_impl<64, true>(p, grid, stream)
+             : launch_bwd_main_impl<64, false>(p, grid, stream);
 }
 
 int bwd_block_m(int D) { return D == 128 ? BwdCfg<128>::BM : BwdCfg<64>::BM; }

@@ -58,8 +58,8 @@ __device__ __forceinline__ bool decode_seq(const SeqAddr& a, int z, int* status,
 }
 
 struct FwdParams {
-  CUtensorMap tm_q, tm_k, tm_v;   // 4-D (D, S, H, B) bf16, box (64, 128, 1, 1), SW128
-  __nv_bfloat16* o;
+  CUtensorMap tm_q, tm_k, tm_v;   // 4-D (D, S, H, B) 16-bit, box (64, 128, 1, 1), SW128
+  uint16_t* o;                    // bf16 or fp16 elements (the kernel's element type)
   int64_t o_sb, o_sh, o_ss;       // element strides of o (D stride is 1)
   float* lse;
   int64_t l_sb, l_sh, l_ss;
@@ -72,13 +72,14 @@ struct FwdParams {
 };
 
 struct BwdPreParams {
-  const __nv_bfloat16* o;
-  const __nv_bfloat16* dout;
+  const uint16_t* o;              // 16-bit elements
+  const uint16_t* dout;
   int64_t o_sb, o_sh, o_ss, do_sb, do_sh, do_ss;
   float* delta;                   // [B*H or H][rows] fp32, row index = token row
   float* dq_acc;                  // [B*H or H][rows][D] fp32
   int units, H, rows, D;          // units = B (dense/padded) or num_seqs (compact);
                                   // rows = Sq (dense/padded) or Tq (compact)
+  int f16;                        // element type: 0 bf16, 1 fp16
   SeqAddr seq;
   int* status;
 };
@@ -91,9 +92,9 @@ struct BwdParams {
   int64_t l_sb, l_sh, l_ss;
   const float* delta;             // [z-major][rows] as written by the preprocess kernel
   float* dq_acc;
-  __nv_bfloat16* dk;
+  uint16_t* dk;
   int64_t dk_sb, dk_sh, dk_ss;
-  __nv_bfloat16* dv;
+  uint16_t* dv;
   int64_t dv_sb, dv_sh, dv_ss;
   int H, rows_q;                  // rows_q: per-(batch, head) row count of delta / dq_acc
   SeqAddr seq;
@@ -105,9 +106,10 @@ struct BwdParams {
 
 struct BwdPostParams {
   const float* dq_acc;
-  __nv_bfloat16* dq;
+  uint16_t* dq;
   int64_t dq_sb, dq_sh, dq_ss;
   int units, H, rows, D;          // as in BwdPreParams
+  int f16;                        // element type: 0 bf16, 1 fp16
   SeqAddr seq;
   float sm_scale;
 };

@@ -5,7 +5,7 @@
 //   S_t = Q_t K_j^T            tcgen05 MMA into TMEM, t = 0, 1
 //   online softmax of S_t      one thread per query row (TMEM lane), base-2 exponent
 //   O_t += P_t V_j             tcgen05 MMA, P_t read from TMEM where it overwrote S_t
-// and at the end O_t / l (bf16) and LSE = (m + log2 l) ln 2 are stored. Forward keeps LSE
+// and at the end O_t / l (16-bit) and LSE = (m + log2 l) ln 2 are stored. Forward keeps LSE
 // so that the backward pass can rebuild P (the stash / recompute split of the nvFuser SDPA
 // page).
 //
@@ -69,7 +69,7 @@ __device__ __forceinline__ int key_tiles(int q_lo, int q_hi, int len_k, int caus
   return n;
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   constexpr int BM = C::BM, BN = C::BN, NST = C::NST;
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       const int row = blk_lo + threadIdx.x;
       if (row < sv.len_q) {
         const int64_t grow = sv.row0_q + row;
-        __nv_bfloat16* orow = p.o + sv.batch * p.o_sb + h * p.o_sh + grow * p.o_ss;
+        uint16_t* orow = p.o + sv.batch * p.o_sb + h * p.o_sh + grow * p.o_ss;
         for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
         p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] = -INFINITY;
       }
@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, BN, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idS = idesc_f32acc(128, BN, false, false, F16);
+      constexpr uint32_t idO = idesc_f32acc(128, D, false, true, F16);
       const uint32_t tS[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
       const uint32_t tO[2] = {tmem + C::COL_O0, tmem + C::COL_O1};
       auto issue_s = [&](int t, int j) {
@@ -286,8 +286,8 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
         rs0 = f2_add(rs0, f2_pack(p0, p1));
         rs1 = f2_add(rs1, f2_pack(p2, p3));
-        pk[c] = pack_bf16x2(p0, p1);
-        pk[c + 1] = pack_bf16x2(p2, p3);
+        pk[c] = pack2<F16>(p0, p1);
+        pk[c + 1] = pack2<F16>(p2, p3);
       }
       float a0, a1;
       f2_unpack(f2_add(rs0, rs1), a0, a1);
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const bool valid = row < sv.len_q;
       const int64_t grow = sv.row0_q + row;
-      __nv_bfloat16* orow = p.o + sv.batch * p.o_sb + h * p.o_sh + grow * p.o_ss;
+      uint16_t* orow = p.o + sv.batch * p.o_sb + h * p.o_sh + grow * p.o_ss;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -345,10 +345,10 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l);
+            v.x = pack2<F16>(__uint_as_float(o[e + 0]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
+            v.y = pack2<F16>(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+            v.z = pack2<F16>(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l);
+            v.w = pack2<F16>(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l);
             *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
           }
         }
@@ -368,24 +368,26 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
   if (threadIdx.x == 0 && bars.abort && p.status != nullptr) atomicCAS(p.status, 0, kStatusTimeout);
 }
 
-template <int D>
+template <int D, bool F16>
 static cudaError_t launch_fwd_impl(const FwdParams& p, dim3 grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  attn_fwd_kernel<D><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
+  attn_fwd_kernel<D, F16><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_fwd(const FwdParams& p, int D, dim3 grid, cudaStream_t stream) {
-  return D == 128 ? launch_fwd_impl<128>(p, grid, stream) : launch_fwd_impl<64>(p, grid, stream);
+cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, dim3 grid, cudaStream_t stream) {
+  if (D == 128)
+    return f16 ? launch_fwd_impl<128, true>(p, grid, stream) : launch_fwd_impl<128, false>(p, grid, stream);
+  return f16 ? launch_fwd_impl<64, true>(p, grid, stream) : launch_fwd_impl<64, false>(p, grid, stream);
 }
 
 // Query rows per CTA (two 128-row tiles). The 4-D Q tensor map uses a 128-row box.

@@ -10,13 +10,13 @@ namespace attn_sm103 {
 // loaded with a Q tensor map whose box has fwd_box_rows() rows.
 int fwd_block_m();
 int fwd_box_rows();
-cudaError_t launch_attn_fwd(const FwdParams& p, int D, dim3 grid, cudaStream_t stream);
+cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, dim3 grid, cudaStream_t stream);
 
 // Backward stages.
 int bwd_block_m(int D);  // query rows per inner step of the main kernel
 int bwd_block_n();       // key rows per CTA of the main kernel
 cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_main(const BwdParams& p, int D, dim3 grid, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, dim3 grid, cudaStream_t stream);
 cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream);
 
 }  // namespace attn_sm103

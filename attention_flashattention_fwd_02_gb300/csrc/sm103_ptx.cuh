@@ -184,11 +184,15 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D. a_mn / b_mn select the
-// MN-major ("transposed") operand layouts.
+// Instruction descriptor, kind::f16 with fp32 D; A and B are both bf16 (f16 == false) or
+// both fp16 (f16 == true). a_mn / b_mn select the MN-major ("transposed") operand layouts.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn, bool b_mn, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+  return idesc_f32acc(M, N, a_mn, b_mn, false);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
@@ -391,6 +395,29 @@ __device__ __forceinline__ float ex2_poly(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two floats rounded (to nearest even) to the 16-bit element type, low half first.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+// Two packed 16-bit elements widened to float.
+template <bool F16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  float2 r;
+  if (F16) {
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "r"(v));
+  } else {
+    r.x = __uint_as_float(v << 16);
+    r.y = __uint_as_float(v & 0xffff0000u);
+  }
   return r;
 }
 

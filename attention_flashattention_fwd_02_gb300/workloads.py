@@ -5,8 +5,8 @@ attention arithmetic. Both the CUDA path's tests/benchmark and the CPU oracle's 
 their inputs from here, so the two sides see identical values.
 
 Recipe: a CPU ``torch.Generator`` seeded per workload; draw order is sequence lengths
-(varlen workloads only), then Q, K, V, dO as float32 N(0, 1), each rounded to bf16 (round to
-nearest even). Layouts:
+(varlen workloads only), then Q, K, V, dO as float32 N(0, 1), each rounded (to nearest even)
+to the 16-bit element type, bf16 unless fp16 is asked for. Layouts:
   * "bhsd"     contiguous (B, H, S, D);
   * "kv_bshd"  Q/dO contiguous BHSD, K/V allocated as (B, Sk, H, D) and passed as the
                transposed BHSD view (strides (Sk*H*D, D, H*D, 1));
@@ -70,8 +70,8 @@ WORKLOADS = {
 }
 
 
-def _randn_bf16(shape, g):
-    return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+def _randn16(shape, g, dtype=torch.bfloat16):
+    return torch.randn(*shape, generator=g, dtype=torch.float32).to(dtype)
 
 
 def _cu(lengths: torch.Tensor) -> torch.Tensor:
@@ -80,13 +80,14 @@ def _cu(lengths: torch.Tensor) -> torch.Tensor:
     return cu.to(torch.int32)
 
 
-def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None):
+def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None, dtype=torch.bfloat16):
     """Draw the inputs of workload ``wl`` on the CPU.
 
-    Returns a dict with bf16 tensors q, k, v, do (BHSD views, see the module docstring),
+    Returns a dict with 16-bit tensors q, k, v, do (BHSD views, see the module docstring),
     and for varlen layouts int32 ``cu_seqlens_q``/``cu_seqlens_k`` (equal: the same
     lengths serve queries and keys) plus ``lengths``. ``lengths`` may be passed to fix the
-    varlen lengths instead of drawing them (edge-case tests).
+    varlen lengths instead of drawing them (edge-case tests). ``dtype`` is the 16-bit element
+    type the fp32 draws are rounded to (bf16 or fp16).
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(wl.seed if seed is None else seed)
@@ -97,7 +98,7 @@ def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None):
             lengths = torch.randint(wl.len_lo, wl.len_hi + 1, (wl.n_seqs,), generator=g)
         lengths = torch.as_tensor(lengths, dtype=torch.int64)
         T = int(lengths.sum())
-        thd = [_randn_bf16((T, H, D), g) for _ in range(4)]
+        thd = [_randn16((T, H, D), g, dtype) for _ in range(4)]
         q, k, v, do = (t.transpose(0, 1).unsqueeze(0) for t in thd)
         cu = _cu(lengths)
         out.update(cu_seqlens_q=cu, cu_seqlens_k=cu.clone(), lengths=lengths)
@@ -105,22 +106,22 @@ def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None):
         if lengths is None:
             lengths = torch.randint(wl.len_lo, wl.len_hi + 1, (B,), generator=g)
         lengths = torch.as_tensor(lengths, dtype=torch.int64)
-        q = _randn_bf16((B, H, wl.Sq, D), g)
-        k = _randn_bf16((B, H, wl.Sk, D), g)
-        v = _randn_bf16((B, H, wl.Sk, D), g)
-        do = _randn_bf16((B, H, wl.Sq, D), g)
+        q = _randn16((B, H, wl.Sq, D), g, dtype)
+        k = _randn16((B, H, wl.Sk, D), g, dtype)
+        v = _randn16((B, H, wl.Sk, D), g, dtype)
+        do = _randn16((B, H, wl.Sq, D), g, dtype)
         cu = _cu(lengths)
         out.update(cu_seqlens_q=cu, cu_seqlens_k=cu.clone(), lengths=lengths)
     elif wl.layout == "kv_bshd":
-        q = _randn_bf16((B, H, wl.Sq, D), g)
-        k = _randn_bf16((B, wl.Sk, H, D), g).transpose(1, 2)
-        v = _randn_bf16((B, wl.Sk, H, D), g).transpose(1, 2)
-        do = _randn_bf16((B, H, wl.Sq, D), g)
+        q = _randn16((B, H, wl.Sq, D), g, dtype)
+        k = _randn16((B, wl.Sk, H, D), g, dtype).transpose(1, 2)
+        v = _randn16((B, wl.Sk, H, D), g, dtype).transpose(1, 2)
+        do = _randn16((B, H, wl.Sq, D), g, dtype)
     elif wl.layout == "bhsd":
-        q = _randn_bf16((B, H, wl.Sq, D), g)
-        k = _randn_bf16((B, H, wl.Sk, D), g)
-        v = _randn_bf16((B, H, wl.Sk, D), g)
-        do = _randn_bf16((B, H, wl.Sq, D), g)
+        q = _randn16((B, H, wl.Sq, D), g, dtype)
+        k = _randn16((B, H, wl.Sk, D), g, dtype)
+        v = _randn16((B, H, wl.Sk, D), g, dtype)
+        do = _randn16((B, H, wl.Sq, D), g, dtype)
     else:
         raise ValueError(f"unknown layout {wl.layout!r}")
     out.update(q=q, k=k, v=v, do=do)

@@ -16,8 +16,9 @@
  * flash API -- "Add varlen support to AOTriton's Flash Attention", last comment: new layouts
  * get new APIs, not flags). Strides are in ELEMENTS and arbitrary, except that the D stride
  * must be 1, the other strides must be multiples of 8 elements (16 bytes) and base pointers
- * 16-byte aligned (tensor-memory-accelerator requirements). Q, K, V, O, dO, dQ, dK, dV are
- * bf16; LSE is fp32 with shape (B, H, Sq). Q/K/V/O share B, H and D; seqlen_q and seqlen_k
+ * 16-byte aligned (tensor-memory-accelerator requirements). Q, K, V, O, dO, dQ, dK, dV share
+ * one 16-bit element type, bf16 or fp16 (attn_tensor4.dtype); arithmetic accumulates in fp32.
+ * LSE is fp32 with shape (B, H, Sq). Q/K/V/O share B, H and D; seqlen_q and seqlen_k
  * may differ ("[RFC] Goal for triton.ops.flash_attention" lists a different number of
  * queries and keys as a missing case; the AOTriton issue #12 page states that QKVO share a
  * dtype and shape except for seqlen_q vs seqlen_k). d_head must be 64 or 128.
@@ -64,11 +65,15 @@
 extern "C" {
 #endif
 
-/* A rank-4 (B, H, S, D) tensor view; strides in elements. */
+/* Element types of the rank-4 tensors. */
+typedef enum { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F16 = 1 } attn_dtype;
+
+/* A rank-4 (B, H, S, D) tensor view; strides in elements; dtype is an attn_dtype. */
 typedef struct {
   void* data;
   int64_t size[4];
   int64_t stride[4];
+  int32_t dtype;
 } attn_tensor4;
 
 /* A rank-3 (B, H, S) fp32 tensor view (LSE); strides in elements. */
@@ -88,7 +93,8 @@ typedef enum {
   ATTN_ERR_WORKSPACE = 6,     /* workspace NULL or smaller than the *_workspace_size value */
   ATTN_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed (launch, tensor map) */
   ATTN_ERR_DEVICE_BAD_SEQLENS = 8, /* device: cu_seqlens not monotone or past the tensor */
-  ATTN_ERR_DEVICE_TIMEOUT = 9 /* device: a bounded pipeline wait gave up */
+  ATTN_ERR_DEVICE_TIMEOUT = 9, /* device: a bounded pipeline wait gave up */
+  ATTN_ERR_DTYPE = 10          /* tensors of one call with different element types */
 } attn_status;
 
 /* Workspace bytes needed by attn_fwd* for Q of shape (B, H, Sq, D) (compact: B = 1,
@@ -102,8 +108,8 @@ size_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D);
 /*
  * Forward pass, dense (cu_seqlens_q == cu_seqlens_k == NULL) or padded varlen (both
  * non-NULL, int32 device arrays of B+1 prefix sums; only the differences are used).
- *   q: (B, H, Sq, D) bf16     k, v: (B, H, Sk, D) bf16
- *   o: (B, H, Sq, D) bf16 out lse: (B, H, Sq) fp32 out (natural-log logsumexp)
+ *   q: (B, H, Sq, D)          k, v: (B, H, Sk, D)          (bf16 or fp16, one type)
+ *   o: (B, H, Sq, D) out      lse: (B, H, Sq) fp32 out (natural-log logsumexp)
  *   workspace: device, >= attn_fwd_workspace_size bytes (may be NULL with 0 bytes: device
  *   errors are then not reported). stream: cudaStream_t.
  */
@@ -114,8 +120,9 @@ attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_te
 
 /*
  * Backward pass matching attn_fwd (same q, k, v, cu_seqlens, sm_scale, causal; o and lse
- * as returned by attn_fwd). dout: (B, H, Sq, D) bf16. Writes dq (B, H, Sq, D), dk and dv
- * (B, H, Sk, D), all bf16. workspace: device, >= attn_bwd_workspace_size bytes, required.
+ * as returned by attn_fwd). dout: (B, H, Sq, D). Writes dq (B, H, Sq, D), dk and dv
+ * (B, H, Sk, D), all in q's element type. workspace: device, >= attn_bwd_workspace_size
+ * bytes, required.
  * Runs three kernels in stream order: attn_bwd_preprocess, attn_bwd_main and
  * attn_bwd_dq_epilogue below.
  */
@@ -171,7 +178,7 @@ attn_status attn_bwd_padded_varlen(const attn_tensor4* q, const attn_tensor4* k,
  *    fp32 dQ accumulator. Memory-bound.
  *  - attn_bwd_main: recomputes P from LSE per key tile, accumulates dK and dV in tensor
  *    memory and writes them, and adds dS K into the dQ accumulator.
- *  - attn_bwd_dq_epilogue: dq = bf16(sm_scale * accumulator). Memory-bound.
+ *  - attn_bwd_dq_epilogue: dq = sm_scale * accumulator in dq's element type. Memory-bound.
  */
 attn_status attn_bwd_preprocess(const attn_tensor4* o, const attn_tensor4* dout,
                                 const int32_t* cu_seqlens_q, int32_t num_seqs,

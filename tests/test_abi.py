@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(10):
+    for s in range(11):
         assert _lib.attn_status_string(s)
     assert _lib.attn_status_string(0) == "ok"
 
@@ -168,3 +168,17 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_build, "BUILD", str(tmp_path))
     with pytest.raises(RuntimeError, match="not found"):
         _lib.load()
+
+
+def test_dtype_checks(lib):
+    """Rank-4 tensors share one element type (bf16 = 0, fp16 = 1); others are rejected."""
+    q, k, v, o, lse = good()
+    v.dtype = 1
+    assert call_fwd(lib, q, k, v, o, lse) == 10  # ATTN_ERR_DTYPE
+    q, k, v, o, lse = good()
+    o.dtype = 1
+    assert call_fwd(lib, q, k, v, o, lse) == 10
+    q, k, v, o, lse = good()
+    for t in (q, k, v, o):
+        t.dtype = 7
+    assert call_fwd(lib, q, k, v, o, lse) == ERR_UNSUPPORTED

@@ -221,3 +221,36 @@ def test_bad_cu_seqlens_reported_not_read():
     _lib.attn_fwd_compact_varlen(q, q, q, o, lse, cu, cu, 2, 0, 0, 0.125, False, ws)
     assert _lib.attn_read_device_status(ws) == 8
     assert torch.isnan(o[:, :, 32:]).all()
+
+
+FP16_CASES = [
+    # (layout, D, causal)
+    ("bhsd", 64, True),
+    ("kv_bshd", 128, False),
+    ("padded", 128, True),
+    ("compact", 64, True),
+]
+
+
+@pytest.mark.parametrize("layout,D,causal", FP16_CASES)
+def test_fp16_parity(layout, D, causal):
+    """fp16 inputs and outputs (P and dS rounded to fp16 before their products)."""
+    if layout == "compact":
+        wl = WORKLOADS["compact"].replace(H=2, D=D, causal=causal, n_seqs=4, seed=41)
+        x = make_inputs(wl, lengths=[3, 200, 129, 64], dtype=torch.float16)
+        o, lse, grads = _run_compact(x, wl.sm_scale, causal)
+        q, k, v, do = (np64(x[n]) for n in ("q", "k", "v", "do"))
+        cu = x["cu_seqlens_q"].numpy()
+        o_r, lse_r = ref.fwd_compact_varlen(q, k, v, cu, cu, wl.sm_scale, causal)
+        g_r = ref.bwd_compact_varlen(q, k, v, do, cu, cu, wl.sm_scale, causal)
+    else:
+        padded = layout == "padded"
+        base = WORKLOADS["padded" if padded else "cross"]
+        wl = base.replace(B=2, H=2, Sq=300, Sk=300 if layout != "kv_bshd" else 460, D=D,
+                          causal=causal, layout=layout, seed=43)
+        x = make_inputs(wl, lengths=[300, 77] if padded else None, dtype=torch.float16)
+        o, lse, grads = _run_dense(x, wl.sm_scale, causal, padded=padded)
+        o_r, lse_r, g_r = _oracle_dense(x, wl.sm_scale, causal, padded=padded)
+    assert o.dtype == torch.float16 and grads[0].dtype == torch.float16
+    assert_fwd_close(o, lse, o_r, lse_r, what=f"fp16 {layout}")
+    assert_grads_close(grads, g_r, what=f"fp16 {layout}")
