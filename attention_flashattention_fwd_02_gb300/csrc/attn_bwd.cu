@@ -305,45 +305,53 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
     // Issue order per step: dV(it) [P from TMEM], S/dP(it+1), dK(it), dQ(it). The S/dP MMAs
-    // of the next step overlap the P/dS math of the compute warpgroups.
-    if (lane == 0) {
+    // of the next step overlap the P/dS math of the compute warpgroups. The whole warp walks
+    // the schedule, so that every descriptor is warp-uniform; one elected lane issues.
+    {
       constexpr uint32_t idS = idesc_f32acc(128, BM, false, false, F16);  // S^T, dP^T
       constexpr uint32_t idG = idesc_f32acc(128, D, false, true, F16);    // dV, dK
       constexpr uint32_t idQ = C::DQ_T ? idesc_f32acc(128, BM, true, true, F16)  // dQ^T
                                        : idesc_f32acc(128, D, true, true, F16);  // dQ
       const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP, tP = tmem + C::COL_P;
       const uint32_t tDK = tmem + C::COL_DK, tDV = tmem + C::COL_DV, tDQ = tmem + C::COL_DQ;
+      const uint64_t k_kd = desc_kmajor(sK, BN, 0), v_kd = desc_kmajor(sV, BN, 0);
+      const uint64_t k_mn = desc_mnmajor(sK, BN, 0);
+      const uint64_t q_kd = desc_kmajor(sQ, BM, 0), do_kd = desc_kmajor(sDO, BM, 0);
+      const uint64_t q_mn = desc_mnmajor(sQ, BM, 0), do_mn = desc_mnmajor(sDO, BM, 0);
+      const uint64_t ds_kd = desc_kmajor(sDS, BN, 0), ds_mn = desc_mnmajor(sDS, BN, 0);
+      constexpr uint32_t QSTEP = C::Q_BYTES >> 4, DSSTEP = C::DS_BYTES >> 4;
       auto issue_sdp = [&](int it) -> bool {
         const int st = it % QST;
         if (!mbar_wait(smem_u32(&bars.q_full[st]), (it / QST) & 1, abort, kWaitTimeoutNs))
           return false;
         tc_fence_after();
-        const uint32_t q = sQ + st * C::Q_BYTES, dO = sDO + st * C::Q_BYTES;
+        const uint32_t qo = st * QSTEP;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tS, desc_kmajor(sK, BN, kk), desc_kmajor(q, BM, kk), idS, kk > 0);
+          umma_ss_w(tS, k_kd + kmajor_step(BN, kk), q_kd + qo + kmajor_step(BM, kk), idS, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tDP, desc_kmajor(sV, BN, kk), desc_kmajor(dO, BM, kk), idS, kk > 0);
-        umma_commit(smem_u32(&bars.s_full));
+          umma_ss_w(tDP, v_kd + kmajor_step(BN, kk), do_kd + qo + kmajor_step(BM, kk), idS,
+                    kk > 0);
+        umma_commit_w(smem_u32(&bars.s_full));
         return true;
       };
       bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort, kWaitTimeoutNs) && issue_sdp(0);
       for (int it = 0; ok && it < n_steps; ++it) {
         const int st = it % QST, bs = it & 1;
-        const uint32_t q = sQ + st * C::Q_BYTES, dO = sDO + st * C::Q_BYTES;
-        const uint32_t dS = sDS + bs * C::DS_BYTES;
+        const uint32_t qo = st * QSTEP, dso = bs * DSSTEP;
         if (!mbar_wait(smem_u32(&bars.p_full), it & 1, abort, kWaitTimeoutNs)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts(tDV, tP + kk * 8, desc_mnmajor(dO, BM, kk), idG, (it > 0 || kk > 0));
+          umma_ts_w(tDV, tP + kk * 8, do_mn + qo + mnmajor_step(kk), idG, (it > 0 || kk > 0));
         if (it + 1 < n_steps && !issue_sdp(it + 1)) break;
         if (!mbar_wait(smem_u32(&bars.ds_full[bs]), (it >> 1) & 1, abort, kWaitTimeoutNs)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ss(tDK, desc_kmajor(dS, BN, kk), desc_mnmajor(q, BM, kk), idG, (it > 0 || kk > 0));
+          umma_ss_w(tDK, ds_kd + dso + kmajor_step(BN, kk), q_mn + qo + mnmajor_step(kk), idG,
+                    (it > 0 || kk > 0));
         if (it > 0 &&
             !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, kWaitTimeoutNs))
           break;
@@ -351,15 +359,15 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           if (C::DQ_T)
-            umma_ss(tDQ, desc_mnmajor(sK, BN, kk), desc_mnmajor(dS, BN, kk), idQ, kk > 0);
+            umma_ss_w(tDQ, k_mn + mnmajor_step(kk), ds_mn + dso + mnmajor_step(kk), idQ, kk > 0);
           else
-            umma_ss(tDQ, desc_mnmajor(dS, BN, kk), desc_mnmajor(sK, BN, kk), idQ, kk > 0);
+            umma_ss_w(tDQ, ds_mn + dso + mnmajor_step(kk), k_mn + mnmajor_step(kk), idQ, kk > 0);
         }
-        umma_commit(smem_u32(&bars.ds_empty[bs]));
-        umma_commit(smem_u32(&bars.q_empty[st]));
-        umma_commit(smem_u32(&bars.dq_full));
+        umma_commit_w(smem_u32(&bars.ds_empty[bs]));
+        umma_commit_w(smem_u32(&bars.q_empty[st]));
+        umma_commit_w(smem_u32(&bars.dq_full));
       }
-      umma_commit(smem_u32(&bars.dkdv_full));
+      umma_commit_w(smem_u32(&bars.dkdv_full));
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ P^T / dS^T compute

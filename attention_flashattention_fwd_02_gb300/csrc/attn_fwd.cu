@@ -172,57 +172,61 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_f32acc(128, BN, false, false, F16);
-      constexpr uint32_t idO = idesc_f32acc(128, D, false, true, F16);
-      const uint32_t tS[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
-      const uint32_t tO[2] = {tmem + C::COL_O0, tmem + C::COL_O1};
-      auto issue_s = [&](int t, int j) {
-        const uint32_t kbase = sK + (j % NST) * C::KV_BYTES;
-        const uint32_t qbase = sQ + t * C::Q_BYTES;
+    // The whole warp walks the schedule, so that every descriptor is warp-uniform; one
+    // elected lane issues the MMAs and their commits.
+    constexpr uint32_t idS = idesc_f32acc(128, BN, false, false, F16);
+    constexpr uint32_t idO = idesc_f32acc(128, D, false, true, F16);
+    const uint64_t q_desc = desc_kmajor(sQ, BM, 0);
+    const uint64_t k_desc = desc_kmajor(sK, BN, 0);
+    const uint64_t v_desc = desc_mnmajor(sV, BN, 0);
+    auto issue_s = [&](int t, int j) {
+      const uint32_t tS = tmem + (t ? C::COL_S1 : C::COL_S0);
+      const uint64_t qd = q_desc + (uint32_t)(t * (C::Q_BYTES >> 4));
+      const uint64_t kd = k_desc + (uint32_t)((j % NST) * (C::KV_BYTES >> 4));
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tS[t], desc_kmajor(qbase, BM, kk), desc_kmajor(kbase, BN, kk), idS, kk > 0);
-        umma_commit(smem_u32(&bars.s_full[t]));
-      };
-      bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort, p.timeout_ns) &&
-                mbar_wait(smem_u32(&bars.k_full[0]), 0, abort, p.timeout_ns);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (n_t[t] > 0) issue_s(t, 0);
-      }
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int st = j % NST;
-        if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / NST) & 1, abort, p.timeout_ns)) break;
-        bool next_k_ready = false;
-        for (int t = 0; t < 2; ++t) {
-          if (j >= n_t[t]) continue;
-          if (!mbar_wait(smem_u32(&bars.p_full[t]), j & 1, abort, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t vbase = sV + st * C::KV_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            umma_ts(tO[t], tS[t] + kk * 8, desc_mnmajor(vbase, BN, kk), idO, (j > 0 || kk > 0));
-          umma_commit(smem_u32(&bars.o_done[t]));
-          if (j + 1 < n_t[t]) {
-            if (!next_k_ready) {
-              if (!mbar_wait(smem_u32(&bars.k_full[(j + 1) % NST]), ((j + 1) / NST) & 1, abort,
-                             p.timeout_ns)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              next_k_ready = true;
-            }
-            issue_s(t, j + 1);
-          }
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma_ss_w(tS, qd + kmajor_step(BM, kk), kd + kmajor_step(BN, kk), idS, kk > 0);
+      umma_commit_w(smem_u32(&bars.s_full[t]));
+    };
+    bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort, p.timeout_ns) &&
+              mbar_wait(smem_u32(&bars.k_full[0]), 0, abort, p.timeout_ns);
+    if (ok) {
+      tc_fence_after();
+      for (int t = 0; t < 2; ++t)
+        if (n_t[t] > 0) issue_s(t, 0);
+    }
+    for (int j = 0; ok && j < n_max; ++j) {
+      const int st = j % NST;
+      if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / NST) & 1, abort, p.timeout_ns)) break;
+      const uint64_t vd = v_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
+      bool next_k_ready = false;
+      for (int t = 0; t < 2; ++t) {
+        if (j >= n_t[t]) continue;
+        if (!mbar_wait(smem_u32(&bars.p_full[t]), j & 1, abort, p.timeout_ns)) {
+          ok = false;
+          break;
         }
-        umma_commit(smem_u32(&bars.kv_empty[st]));
+        tc_fence_after();
+        const uint32_t tS = tmem + (t ? C::COL_S1 : C::COL_S0);
+        const uint32_t tO = tmem + (t ? C::COL_O1 : C::COL_O0);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ts_w(tO, tS + kk * 8, vd + mnmajor_step(kk), idO, (j > 0 || kk > 0));
+        umma_commit_w(smem_u32(&bars.o_done[t]));
+        if (j + 1 < n_t[t]) {
+          if (!next_k_ready) {
+            if (!mbar_wait(smem_u32(&bars.k_full[(j + 1) % NST]), ((j + 1) / NST) & 1, abort,
+                           p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            next_k_ready = true;
+          }
+          issue_s(t, j + 1);
+        }
       }
+      umma_commit_w(smem_u32(&bars.kv_empty[st]));
     }
   } else {
     // ------------------------------------------------------------------ softmax / epilogue

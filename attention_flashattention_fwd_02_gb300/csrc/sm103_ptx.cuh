@@ -177,6 +177,40 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// Warp-collective forms of the two MMA shapes and of the commit: every lane of the warp
+// executes them with the same (warp-uniform) operands and elect.sync picks the one lane that
+// issues. elect.sync with a full mask always elects the same lane, so the MMAs and the commits
+// that track them come from one thread. Keeping the issuing code convergent lets the operands
+// live in uniform registers.
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n"
+      ::"r"(bar)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
@@ -218,6 +252,14 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int rows, int kk)
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int krows, int kk) {
   return sdesc_sw128(base + (uint32_t)(kk * 2048), (uint32_t)(krows * 128), 1024);
 }
+
+// Descriptor increments (in the descriptor's 16-byte address units) of the kk-th K=16 step.
+// desc(base + off) == desc(base) + off / 16 while base + off stays below 256 KB, which every
+// shared-memory address does, so a loop can add these to one precomputed descriptor.
+__host__ __device__ constexpr uint32_t kmajor_step(int rows, int kk) {
+  return (uint32_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint32_t mnmajor_step(int kk) { return (uint32_t)(kk * 2048 >> 4); }
 
 // Byte offset of element (row, col) inside an SW128-slab tile with `rows` rows.
 __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int rows) {
