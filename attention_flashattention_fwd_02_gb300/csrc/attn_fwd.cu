@@ -9,14 +9,26 @@
 // so that the backward pass can rebuild P (the stash / recompute split of the nvFuser SDPA
 // page).
 //
-// Warp roles (320 threads):
+// Warp roles (320 threads at d_head 128, 352 at d_head 64):
 //   warps 0..3   softmax, O correction and epilogue of query tile 0 (thread r owns row r)
 //   warps 4..7   the same for query tile 1
 //   warp 8       TMA producer: Q_0, Q_1 once, then K_j / V_j into an NST-deep stage ring
-//   warp 9       TMEM allocator and MMA issuer (one thread)
-// The two softmax warpgroups ping-pong: the MMA thread issues PV_0(j), S_0(j+1), PV_1(j),
-// S_1(j+1), ..., so while one warpgroup exponentiates its scores the tensor pipe runs the
-// other tile's products. TMEM (512 columns): S_0 at 0, S_1 at 128, O_0 at 256, O_1 at 256+D.
+//   warp 9       TMEM allocator and MMA issuer (at d_head 64: PV products only)
+//   warp 10      d_head 64 only: issuer of the score products S = Q K^T
+// Each issuing warp walks its schedule as a whole; one elected lane issues.
+// Score buffers rotate: the score tiles S_t(j) are numbered k = 0, 1, ... (S_0(0), S_1(0),
+// S_0(1), S_1(1), ...; once one query tile has run out of key tiles, only the other's), and S
+// number k lives in TMEM buffer k mod NSB, where its P overwrites it. PV(k) is issued as soon
+// as P(k) is published, and S(k + NSB) goes into the buffer PV(k) reads.
+//   d_head 128, NSB = 2: one warp issues S(0), S(1), then PV(k), S(k + 2) for every k; the
+//     tensor pipe runs them in issue order, so S(k + 2) needs no wait for PV(k). This is the
+//     ping-pong of two query tiles.
+//   d_head 64, NSB = 3 (TMEM has room for a third 128-column buffer): the products are short
+//     and one warp that waits, issues and commits all of them spends more cycles per step
+//     than the tensor pipe does, so a second warp issues the score products; S(k) waits until
+//     PV(k - NSB) has completed. The next score tile of a query tile is computed while its
+//     softmax runs.
+// TMEM (512 columns): NSB score buffers of 128 columns, then O_0 and O_1 (D columns each).
 //
 // Online softmax in base 2 with a lazy rescale: a row's reference maximum m only moves when
 // a new row maximum exceeds it by more than 8 (so p <= 2^8); O and l are rescaled by
@@ -42,17 +54,20 @@ struct FwdCfg {
   static constexpr int OFF_K = NQ * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
   static constexpr int SMEM_BYTES = OFF_V + NST * KV_BYTES + 1024;  // + alignment slack
+  static constexpr int NSB = (D == 64) ? 3 : 2;  // rotating score / P buffers
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
-  static constexpr int NTHREADS = 320;
-  static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
+  static constexpr uint32_t COL_O0 = NSB * 128, COL_O1 = NSB * 128 + D;
+  static_assert(COL_O1 + D <= TMEM_COLS, "TMEM budget");
+  static constexpr bool SPLIT_ISSUE = (NSB == 3);  // separate S and PV issuing warps
+  static constexpr int NTHREADS = SPLIT_ISSUE ? 352 : 320;
+  static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_SMMA = 10;
 };
 
-template <int NST>
+template <int NST, int NSB>
 struct FwdBars {
   uint64_t q_full;
   uint64_t k_full[NST], v_full[NST], kv_empty[NST];
-  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t s_full[NSB], p_full[NSB], buf_free[NSB], o_done[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -60,6 +75,19 @@ struct FwdBars {
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
+
+// Issue order of the score tiles of the two query tiles (n0, n1 key tiles each): S number k
+// belongs to query tile t_of(k) and key tile j_of(k); k_of is the inverse.
+struct ScoreOrder {
+  int n_min, t_long, total;
+  __device__ ScoreOrder(int n0, int n1)
+      : n_min(min(n0, n1)), t_long(n1 > n0 ? 1 : 0), total(n0 + n1) {}
+  __device__ __forceinline__ int k_of(int t, int j) const {
+    return j < n_min ? 2 * j + t : n_min + j;
+  }
+  __device__ __forceinline__ int t_of(int k) const { return k < 2 * n_min ? (k & 1) : t_long; }
+  __device__ __forceinline__ int j_of(int k) const { return k < 2 * n_min ? (k >> 1) : k - n_min; }
+};
 
 // Number of key tiles a query tile [q_lo, q_hi) must visit.
 __device__ __forceinline__ int key_tiles(int q_lo, int q_hi, int len_k, int causal, int BN) {
@@ -70,11 +98,11 @@ __device__ __forceinline__ int key_tiles(int q_lo, int q_hi, int len_k, int caus
 }
 
 template <int D, bool F16>
-__global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
-  constexpr int BM = C::BM, BN = C::BN, NST = C::NST;
+  constexpr int BM = C::BM, BN = C::BN, NST = C::NST, NSB = C::NSB;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ FwdBars<NST> bars;
+  __shared__ FwdBars<NST, NSB> bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y, z = blockIdx.z;
@@ -93,6 +121,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     n_t[t] = key_tiles(q_lo[t], q_hi[t], sv.len_k, p.causal, BN);
   }
   const int n_max = max(n_t[0], n_t[1]);
+  const ScoreOrder order(n_t[0], n_t[1]);
 
   if (n_max == 0) {  // no visible keys: O = 0, LSE = -inf on the valid rows
     if (warp < 8) {
@@ -120,11 +149,12 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       mbar_init(smem_u32(&bars.v_full[s]), 1);
       mbar_init(smem_u32(&bars.kv_empty[s]), 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&bars.s_full[t]), 1);
-      mbar_init(smem_u32(&bars.p_full[t]), 128);
-      mbar_init(smem_u32(&bars.o_done[t]), 1);
+    for (int b = 0; b < NSB; ++b) {
+      mbar_init(smem_u32(&bars.s_full[b]), 1);
+      mbar_init(smem_u32(&bars.p_full[b]), 128);
+      mbar_init(smem_u32(&bars.buf_free[b]), 1);
     }
+    for (int t = 0; t < 2; ++t) mbar_init(smem_u32(&bars.o_done[t]), 1);
     mbar_fence_init();
   }
   if (warp == C::WARP_MMA) {
@@ -172,61 +202,86 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
-    // The whole warp walks the schedule, so that every descriptor is warp-uniform; one
-    // elected lane issues the MMAs and their commits.
-    constexpr uint32_t idS = idesc_f32acc(128, BN, false, false, F16);
     constexpr uint32_t idO = idesc_f32acc(128, D, false, true, F16);
+    const uint64_t v_desc = desc_mnmajor(sV, BN, 0);
+    const int total = order.total;
+    constexpr uint32_t idS = idesc_f32acc(128, BN, false, false, F16);
     const uint64_t q_desc = desc_kmajor(sQ, BM, 0);
     const uint64_t k_desc = desc_kmajor(sK, BN, 0);
-    const uint64_t v_desc = desc_mnmajor(sV, BN, 0);
-    auto issue_s = [&](int t, int j) {
-      const uint32_t tS = tmem + (t ? C::COL_S1 : C::COL_S0);
+    int k_seen = -1;  // key tile whose K stage was last seen full
+    // S number k into buffer k mod NSB (single-issuer schedule); false when a wait gave up.
+    auto issue_s = [&](int k) -> bool {
+      const int t = order.t_of(k), j = order.j_of(k), st = j % NST;
+      if (j != k_seen) {
+        if (!mbar_wait(smem_u32(&bars.k_full[st]), (j / NST) & 1, abort, p.timeout_ns))
+          return false;
+        k_seen = j;
+        tc_fence_after();
+      }
+      const int bsel = k % NSB;
+      const uint32_t tS = tmem + bsel * 128;
       const uint64_t qd = q_desc + (uint32_t)(t * (C::Q_BYTES >> 4));
-      const uint64_t kd = k_desc + (uint32_t)((j % NST) * (C::KV_BYTES >> 4));
+      const uint64_t kd = k_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         umma_ss_w(tS, qd + kmajor_step(BM, kk), kd + kmajor_step(BN, kk), idS, kk > 0);
-      umma_commit_w(smem_u32(&bars.s_full[t]));
+      umma_commit_w(smem_u32(&bars.s_full[bsel]));
+      return true;
     };
-    bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort, p.timeout_ns) &&
-              mbar_wait(smem_u32(&bars.k_full[0]), 0, abort, p.timeout_ns);
-    if (ok) {
-      tc_fence_after();
-      for (int t = 0; t < 2; ++t)
-        if (n_t[t] > 0) issue_s(t, 0);
+    bool ok = true;
+    if (!C::SPLIT_ISSUE) {
+      ok = mbar_wait(smem_u32(&bars.q_full), 0, abort, p.timeout_ns);
+      for (int k = 0; ok && k < min(NSB, total); ++k) ok = issue_s(k);
     }
-    for (int j = 0; ok && j < n_max; ++j) {
-      const int st = j % NST;
-      if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / NST) & 1, abort, p.timeout_ns)) break;
-      const uint64_t vd = v_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
-      bool next_k_ready = false;
-      for (int t = 0; t < 2; ++t) {
-        if (j >= n_t[t]) continue;
-        if (!mbar_wait(smem_u32(&bars.p_full[t]), j & 1, abort, p.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tS = tmem + (t ? C::COL_S1 : C::COL_S0);
-        const uint32_t tO = tmem + (t ? C::COL_O1 : C::COL_O0);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ts_w(tO, tS + kk * 8, vd + mnmajor_step(kk), idO, (j > 0 || kk > 0));
-        umma_commit_w(smem_u32(&bars.o_done[t]));
-        if (j + 1 < n_t[t]) {
-          if (!next_k_ready) {
-            if (!mbar_wait(smem_u32(&bars.k_full[(j + 1) % NST]), ((j + 1) / NST) & 1, abort,
-                           p.timeout_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            next_k_ready = true;
-          }
-          issue_s(t, j + 1);
-        }
+    int v_seen = -1;  // key tile whose V stage was last seen full
+    for (int k = 0; ok && k < total; ++k) {
+      const int t = order.t_of(k), j = order.j_of(k), st = j % NST, bsel = k % NSB;
+      if (j != v_seen) {
+        if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / NST) & 1, abort, p.timeout_ns)) break;
+        v_seen = j;
       }
-      umma_commit_w(smem_u32(&bars.kv_empty[st]));
+      if (!mbar_wait(smem_u32(&bars.p_full[bsel]), (k / NSB) & 1, abort, p.timeout_ns)) break;
+      tc_fence_after();
+      const uint32_t tS = tmem + bsel * 128;
+      const uint32_t tO = tmem + (t ? C::COL_O1 : C::COL_O0);
+      const uint64_t vd = v_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        umma_ts_w(tO, tS + kk * 8, vd + mnmajor_step(kk), idO, (j > 0 || kk > 0));
+      umma_commit_w(smem_u32(&bars.o_done[t]));
+      if (C::SPLIT_ISSUE && k + NSB < total) umma_commit_w(smem_u32(&bars.buf_free[bsel]));
+      // Stage st is free once the last product reading V_j is done; the score products that
+      // read K_j finished before their P was published, hence before this PV.
+      if (k + 1 == total || order.j_of(k + 1) != j) umma_commit_w(smem_u32(&bars.kv_empty[st]));
+      if (!C::SPLIT_ISSUE && k + NSB < total) ok = issue_s(k + NSB);
+    }
+  } else if (C::SPLIT_ISSUE && warp == C::WARP_SMMA) {
+    // ------------------------------------------------------------------ S issuer (d_head 64)
+    constexpr uint32_t idS = idesc_f32acc(128, BN, false, false, F16);
+    const uint64_t q_desc = desc_kmajor(sQ, BM, 0);
+    const uint64_t k_desc = desc_kmajor(sK, BN, 0);
+    const int total = order.total;
+    bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort, p.timeout_ns);
+    int k_seen = -1;  // key tile whose K stage was last seen full
+    for (int k = 0; ok && k < total; ++k) {
+      const int t = order.t_of(k), j = order.j_of(k), st = j % NST, bsel = k % NSB;
+      // PV(k - NSB) read this buffer; its release cannot run a phase ahead, since the next
+      // release of the buffer needs S(k), issued below.
+      if (k >= NSB &&
+          !mbar_wait(smem_u32(&bars.buf_free[bsel]), ((k - NSB) / NSB) & 1, abort, p.timeout_ns))
+        break;
+      if (j != k_seen) {
+        if (!mbar_wait(smem_u32(&bars.k_full[st]), (j / NST) & 1, abort, p.timeout_ns)) break;
+        k_seen = j;
+      }
+      tc_fence_after();
+      const uint32_t tS = tmem + bsel * 128;
+      const uint64_t qd = q_desc + (uint32_t)(t * (C::Q_BYTES >> 4));
+      const uint64_t kd = k_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma_ss_w(tS, qd + kmajor_step(BM, kk), kd + kmajor_step(BN, kk), idS, kk > 0);
+      umma_commit_w(smem_u32(&bars.s_full[bsel]));
     }
   } else {
     // ------------------------------------------------------------------ softmax / epilogue
@@ -235,13 +290,14 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int row = q_lo[t] + r;             // local query index
     const int n = n_t[t];
-    const uint32_t tSt = tmem + (t ? C::COL_S1 : C::COL_S0) + lane_off;
     const uint32_t tOt = tmem + (t ? C::COL_O1 : C::COL_O0) + lane_off;
     const float c2 = p.scale_log2;
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; ok && j < n; ++j) {
-      if (!mbar_wait(smem_u32(&bars.s_full[t]), j & 1, abort, p.timeout_ns)) {
+      const int k = order.k_of(t, j), bsel = k % NSB;
+      const uint32_t tSt = tmem + bsel * 128 + lane_off;
+      if (!mbar_wait(smem_u32(&bars.s_full[bsel]), (k / NSB) & 1, abort, p.timeout_ns)) {
         ok = false;
         break;
       }
@@ -297,35 +353,36 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       f2_unpack(f2_add(rs0, rs1), a0, a1);
       l = l * scale + (a0 + a1);
       m_use = m_new;
-      if (j > 0) {
+      // O_t is rescaled only when the reference maximum moved. PV_t(j-1) must have finished
+      // first; PV_t(j) cannot start before this thread publishes P_t(j), so the o_done phase
+      // is at most one ahead of the one waited for and its parity identifies it.
+      if (j > 0 && __any_sync(0xffffffffu, scale != 1.f)) {
         if (!mbar_wait(smem_u32(&bars.o_done[t]), (j - 1) & 1, abort, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, scale != 1.f)) {
-          const uint64_t sc2 = f2_pack(scale, scale);
+        const uint64_t sc2 = f2_pack(scale, scale);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            ATTN_TMEM_LD_X32(tOt + c * 32, o);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          ATTN_TMEM_LD_X32(tOt + c * 32, o);
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float y0, y1;
-              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), sc2),
-                        y0, y1);
-              o[e] = __float_as_uint(y0);
-              o[e + 1] = __float_as_uint(y1);
-            }
-            ATTN_TMEM_ST_X32(tOt + c * 32, o);
+          for (int e = 0; e < 32; e += 2) {
+            float y0, y1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), sc2),
+                      y0, y1);
+            o[e] = __float_as_uint(y0);
+            o[e + 1] = __float_as_uint(y1);
           }
+          ATTN_TMEM_ST_X32(tOt + c * 32, o);
         }
       }
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) ATTN_TMEM_ST_X16(tSt + c * 16, (&pk[c * 16]));
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.p_full[t]));
+      mbar_arrive(smem_u32(&bars.p_full[bsel]));
     }
     if (n > 0) {
       if (ok) ok = mbar_wait(smem_u32(&bars.o_done[t]), (n - 1) & 1, abort, p.timeout_ns);
