@@ -174,14 +174,15 @@ attn_status make_map(CUtensorMap* m, const attn_tensor4* t, int box_rows) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// 2-D fp32 tensor map over the dQ accumulator viewed as [rows][D]: box (32, 128), 128-byte
-// swizzle (32 floats = 128 bytes per box row).
+// 2-D fp32 tensor map over the dQ accumulator viewed as [rows][D]: box (32, 32), 128-byte
+// swizzle (32 floats = 128 bytes per box row). Each warp of the backward kernel adds one such
+// 32 x 32 block per step.
 attn_status make_map_acc(CUtensorMap* m, float* acc, int64_t rows, int64_t D) {
   auto enc = encode_fn();
   if (enc == nullptr) return ATTN_ERR_CUDA;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {(cuuint64_t)D * 4};
-  cuuint32_t box[2] = {32, 128};
+  cuuint32_t box[2] = {32, 32};
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -306,8 +307,7 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       if ((s = make_map(&p.tm_do, a.dout, BM)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_k, a.k, BN)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_v, a.v, BN)) != ATTN_OK) return s;
-      if (pr.D == 64 &&
-          (s = make_map_acc(&p.tm_dq, dq_acc, (int64_t)pr.B * pr.H * pr.Sq, pr.D)) != ATTN_OK)
+      if ((s = make_map_acc(&p.tm_dq, dq_acc, (int64_t)pr.B * pr.H * pr.Sq, pr.D)) != ATTN_OK)
         return s;
       p.lse = reinterpret_cast<const float*>(a.lse->data);
       p.l_sb = a.lse->stride[0]; p.l_sh = a.lse->stride[1]; p.l_ss = a.lse->stride[2];

@@ -142,7 +142,11 @@ struct BwdCfg {
   static constexpr int OFF_Q = OFF_V + KV_BYTES;        // QST stages
   static constexpr int OFF_DO = OFF_Q + QST * Q_BYTES;  // QST stages
   static constexpr int OFF_DS = OFF_DO + QST * Q_BYTES; // 2 buffers
-  static constexpr int SMEM_BYTES = OFF_DS + 2 * DS_BYTES + 1024;
+  // dQ staging, 4 KB per compute warp (one 32 x 32 fp32 block). At d_head 64 each warp stages
+  // in the rows of the finished dS^T buffer that only it writes, so no extra space is needed.
+  static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;
+  static constexpr int STG_BYTES = DQ_T ? 8 * 4096 : 0;
+  static constexpr int SMEM_BYTES = OFF_STG + STG_BYTES + 1024;
   // TMEM columns: dK, dV accumulators; S^T, dP^T of the current step; the dQ partial; and P^T
   // (16-bit, two values per column) as the A operand of the dV MMA.
   static constexpr uint32_t TMEM_COLS = 512;
@@ -161,21 +165,11 @@ struct BwdBars {
   uint64_t s_full, p_full;
   uint64_t ds_full[2], ds_empty[2];
   uint64_t dq_full, dq_empty, dkdv_full;
-  uint64_t wg_sync[2];  // per-compute-warpgroup rendezvous (bounded, unlike bar.sync)
   uint32_t tmem_base;
   int abort;
   alignas(16) float nlse2[QST][BM];   // -LSE * log2(e) of the step's query rows
   alignas(16) float ndelta[QST][BM];  // -Delta
 };
-
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
 
 template <int D, bool F16>
 __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
@@ -243,8 +237,6 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_empty), 256);
     mbar_init(smem_u32(&bars.dkdv_full), 1);
-    mbar_init(smem_u32(&bars.wg_sync[0]), 128);
-    mbar_init(smem_u32(&bars.wg_sync[1]), 128);
     mbar_fence_init();
   }
   if (warp == C::WARP_MMA) {
@@ -379,19 +371,12 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     const bool key_ok = key < sv.len_k;
     const float c2 = p.scale_log2;
     const int c_base = g * HALF;
-    float* acc_base = p.dq_acc + (zh * p.rows_q + sv.row0_q) * D;
-    // Rendezvous of the 128 threads of this warpgroup through an mbarrier, so that the wait
-    // is bounded like every other wait of the kernel.
-    uint32_t wg_phase = 0;
-    auto wg_sync = [&]() -> bool {
-      mbar_arrive(smem_u32(&bars.wg_sync[g]));
-      const bool r = mbar_wait(smem_u32(&bars.wg_sync[g]), wg_phase, abort, kWaitTimeoutNs);
-      wg_phase ^= 1;
-      return r;
-    };
-    // Drains warpgroup g's 32 columns of the dQ partial of step itd from TMEM into the fp32
-    // accumulator with fire-and-forget reductions. dQ^T (d_head 128): lanes are d, columns
-    // are the step's query rows; dQ (d_head 64): lanes are query rows, columns are d.
+    // Drains warpgroup g's 32 columns of the dQ partial of step itd. Every warp stages its
+    // 32 x 32 fp32 block in shared memory (128-byte swizzle) and adds it to the fp32
+    // accumulator with one TMA tensor reduce-add issued by its lane 0, so no warp waits for
+    // another. dQ^T (d_head 128): lanes are d, columns the step's query rows; dQ (d_head 64):
+    // lanes are query rows, columns d. Query rows past the sequence hold exact zeros (their dS
+    // was masked), so whole blocks can be added.
     auto drain_dq = [&](int itd) -> bool {
       if (!mbar_wait(smem_u32(&bars.dq_full), itd & 1, abort, kWaitTimeoutNs)) return false;
       tc_fence_after();
@@ -400,37 +385,37 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.dq_empty));
       const int q_lo_d = q_tile(itd) * BM;
+      uint8_t* stage;
+      int c0, r0;  // block origin: column d, query row within the sequence
       if (C::DQ_T) {
-        const int i0 = q_lo_d + g * 32;  // first query row of these columns
-        const int nvalid = min(32, sv.len_q - i0);
-        float* col = acc_base + (int64_t)i0 * D + j;
-        if (nvalid >= 32) {
+        stage = smem + C::OFF_STG + warp * 4096;
+        // this warp's previous reduce must have read the block before it is rewritten
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) red_add_f32(col + (int64_t)i * D, v[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < nvalid) red_add_f32(col + (int64_t)i * D, v[i]);
-        }
+        for (int i = 0; i < 32; ++i)  // row i = query row, column = this lane's d
+          *reinterpret_cast<float*>(stage + i * 128 + 16 * ((lane >> 2) ^ (i & 7)) +
+                                    4 * (lane & 3)) = v[i];
+        c0 = (warp & 3) * 32;
+        r0 = q_lo_d + g * 32;
       } else {
-        // Lanes hold query rows. The warpgroup stages its 128 x 32 fp32 block in its own slab
-        // of the dS^T buffer of step itd (the dK / dQ MMAs of that step are complete and the
-        // slab is rewritten by this warpgroup only two steps later, after the reduce has read
-        // it), then one thread reduces the block into the accumulator with a single TMA
-        // reduce-add. Rows past the sequence carry exact zeros (their dS was masked), so the
-        // whole box can be added.
-        uint8_t* stage = smem + C::OFF_DS + (itd & 1) * C::DS_BYTES + g * (C::DS_BYTES / 2);
+        // rows [32 (warp & 3), +32) of warpgroup g's slab of the dS^T buffer of step itd: the
+        // dK / dQ MMAs of that step are complete, and only this warp writes these rows again
+        // (two steps later, after waiting for this reduce to read them)
+        stage = smem + C::OFF_DS + (itd & 1) * C::DS_BYTES + g * (C::DS_BYTES / 2) +
+                (warp & 3) * 4096;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<float4*>(stage + j * 128 + 16 * (c ^ (j & 7))) =
+          *reinterpret_cast<float4*>(stage + lane * 128 + 16 * (c ^ (lane & 7))) =
               make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-        fence_proxy_async_smem();
-        if (!wg_sync()) return false;
-        if (j == 0) {
-          tma_reduce_add_2d(&p.tm_dq, smem_u32(stage), g * 32,
-                            (int)(zh * p.rows_q + sv.row0_q + q_lo_d));
-          bulk_commit_group();
-        }
+        c0 = g * 32;
+        r0 = q_lo_d + (warp & 3) * 32;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_2d(&p.tm_dq, smem_u32(stage), c0, (int)(zh * p.rows_q + sv.row0_q + r0));
+        bulk_commit_group();
       }
       return true;
     };
@@ -455,12 +440,9 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       }
       uint8_t* gDS = smem + C::OFF_DS + bs * C::DS_BYTES;
       if (!C::DQ_T && it >= 2) {
-        // this warpgroup's slab of the buffer staged dQ two steps ago: wait for that reduce
-        if (j == 0) bulk_wait_group_read0();
-        if (!wg_sync()) {
-          ok = false;
-          break;
-        }
+        // this warp's rows of the buffer staged dQ two steps ago: wait for that reduce
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
       }
       // All of this warpgroup's S^T and dP^T columns are fetched behind one wait.
       float sv_all[HALF], dpv_all[HALF];
@@ -530,7 +512,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       }
     }
     if (ok && n_steps > 0) ok = drain_dq(n_steps - 1);
-    if (!C::DQ_T && j == 0) bulk_wait_group0();  // reduces complete before the CTA exits
+    if (lane == 0) bulk_wait_group0();  // this warp's reduces complete before the CTA exits
     // ---- epilogue: dK = sm_scale * acc, dV = acc; warpgroup g writes columns [g*D/2, +D/2)
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, kWaitTimeoutNs);
     tc_fence_after();
