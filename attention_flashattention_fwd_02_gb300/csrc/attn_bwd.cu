@@ -9,7 +9,7 @@
 //                              P^T  = exp2(S^T c2 - LSE2), dS^T = P^T (dP^T - Delta)
 //                              dV  += P^T dO_m            (tcgen05, TMEM accumulator)
 //                              dK  += dS^T Q_m            (tcgen05, TMEM accumulator)
-//                              dQ_m partial = dS K_n      (tcgen05, TMEM) -> fp32 atomics
+//                              dQ_m partial = dS K_n      (tcgen05, TMEM) -> TMA reduce-add
 //                            then dK * sm_scale and dV are written. P is rebuilt from the
 //                            LSE that the forward pass stashed.
 //  3. attn_bwd_post_kernel   dQ = sm_scale * accumulator, rounded to the element type.
@@ -17,12 +17,12 @@
 // Main-kernel warp roles (320 threads): warps 0..7 are two compute warpgroups that split
 // the query columns of each key row (thread row j = TMEM lane j) to form P^T (written to
 // TMEM, where it is the A operand of the dV MMA) and dS^T (written to shared memory for the
-// dK and dQ MMAs); after each step they drain their half of the previous step's dQ partial
-// from TMEM into the global fp32 accumulator with fire-and-forget reductions, and at the
-// end they write dK / dV; warp 8 is the TMA producer; warp 9 allocates TMEM and issues the
-// MMAs. Tile sizes: 128 keys per CTA; 64
-// query rows per step when d_head = 128 (dQ is formed transposed, K_n^T dS^T, so that every
-// MMA has M = 128), 128 when d_head = 64.
+// dK and dQ MMAs); after each step every compute warp drains its 32 x 32 block of the
+// previous step's dQ partial from TMEM into the global fp32 accumulator with one TMA
+// reduce-add, and at the end they write dK / dV. Warp 8 is the TMA producer; warp 9
+// allocates TMEM and issues the MMAs. Tile sizes: 128 keys per CTA; 64 query rows per step
+// when d_head = 128 (dQ is formed transposed, K_n^T dS^T, so that every MMA has M = 128),
+// 128 when d_head = 64.
 #include "attn_common.cuh"
 #include "attn_launch.h"
 
@@ -146,7 +146,17 @@ struct BwdCfg {
   // in the rows of the finished dS^T buffer that only it writes, so no extra space is needed.
   static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;
   static constexpr int STG_BYTES = DQ_T ? 8 * 4096 : 0;
-  static constexpr int SMEM_BYTES = OFF_STG + STG_BYTES + 1024;
+  // d_head 64: the score products also subtract LSE / sm_scale and Delta, through one more
+  // K = 16 step that multiplies a tile of ones by those values (each split into three bf16
+  // parts), so the compute warps read neither per column. The K = 16 operand tiles (32 bytes
+  // per row) are packed as the 32-byte column groups of two 128-row SW128 slabs: group 0 the
+  // ones, groups 1..QST the LSE rows of the Q stages, groups 4..3+QST the Delta rows.
+  static constexpr bool AUG = (D == 64);
+  static constexpr int OFF_AUG = OFF_STG + STG_BYTES;
+  static constexpr int AUG_BYTES = AUG ? 2 * BN * 128 : 0;
+  static_assert(!AUG || (BM == BN && QST <= 3), "augmented operand packing");
+  static constexpr int LSE_ST = AUG ? 1 : QST;  // stages of the per-column LSE / Delta arrays
+  static constexpr int SMEM_BYTES = OFF_AUG + AUG_BYTES + 1024;
   // TMEM columns: dK, dV accumulators; S^T, dP^T of the current step; the dQ partial; and P^T
   // (16-bit, two values per column) as the A operand of the dV MMA.
   static constexpr uint32_t TMEM_COLS = 512;
@@ -158,17 +168,17 @@ struct BwdCfg {
   static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
 };
 
-template <int BM, int QST>
+template <int BM, int QST, int LSE_ST>
 struct BwdBars {
   uint64_t kv_full;
   uint64_t q_full[QST], q_empty[QST];
-  uint64_t s_full, p_full;
+  uint64_t s_full, s_free, p_full, p_empty;
   uint64_t ds_full[2], ds_empty[2];
   uint64_t dq_full, dq_empty, dkdv_full;
   uint32_t tmem_base;
   int abort;
-  alignas(16) float nlse2[QST][BM];   // -LSE * log2(e) of the step's query rows
-  alignas(16) float ndelta[QST][BM];  // -Delta
+  alignas(16) float nlse2[LSE_ST][BM];   // -LSE * log2(e) of the step's query rows
+  alignas(16) float ndelta[LSE_ST][BM];  // -Delta
 };
 
 template <int D, bool F16>
@@ -178,7 +188,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
   constexpr int HALF = BM / 2;  // score columns per compute warpgroup
   extern __shared__ uint8_t smem_raw[];
   constexpr int QST = C::QST;
-  __shared__ BwdBars<BM, QST> bars;
+  __shared__ BwdBars<BM, QST, C::LSE_ST> bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
@@ -220,6 +230,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
   const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
   const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
   const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+  const uint32_t sAUG = smem_u32(smem + C::OFF_AUG);
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
@@ -233,7 +244,9 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       mbar_init(smem_u32(&bars.ds_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars.s_full), 1);
+    mbar_init(smem_u32(&bars.s_free), 256);
     mbar_init(smem_u32(&bars.p_full), 256);
+    mbar_init(smem_u32(&bars.p_empty), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_empty), 256);
     mbar_init(smem_u32(&bars.dkdv_full), 1);
@@ -264,6 +277,23 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         tma_load_4d(sV + s * BN * 128, &p.tm_v, kvb, s * 64, sv.row0_k + k_lo, h, sv.batch);
       }
     }
+    // Row r of 32-byte column group grp of the augmented operands: (a, b, c, 0, ..., 0) as bf16.
+    auto aug_row = [&](int grp, int r, float a, float b, float c) {
+      uint8_t* row = smem + C::OFF_AUG + (grp >> 2) * (BN * 128) + r * 128;
+      const int c0 = 2 * (grp & 3);
+      *reinterpret_cast<uint4*>(row + 16 * (c0 ^ (r & 7))) =
+          make_uint4(pack_bf16x2(a, b), pack_bf16x2(c, 0.f), 0u, 0u);
+      *reinterpret_cast<uint4*>(row + 16 * ((c0 + 1) ^ (r & 7))) = make_uint4(0u, 0u, 0u, 0u);
+    };
+    // v as the sum of three bf16 values (about 24 significant bits)
+    auto aug_split = [&](int grp, int r, float v) {
+      const float hi = __bfloat162float(__float2bfloat16_rn(v));
+      const float r1 = v - hi;
+      const float mid = __bfloat162float(__float2bfloat16_rn(r1));
+      aug_row(grp, r, hi, mid, r1 - mid);
+    };
+    if (C::AUG)  // the ones tile, made visible to the MMAs by the first step's q_full arrival
+      for (int r = lane; r < BN; r += 32) aug_row(0, r, 1.f, 1.f, 1.f);
     for (int it = 0; it < n_steps; ++it) {
       const int st = it % QST;
       if (it >= QST &&
@@ -289,16 +319,24 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
           l2 = p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] * kLog2e;
           dl = p.delta[zh * p.rows_q + grow];
         }
-        bars.nlse2[st][i] = -l2;
-        bars.ndelta[st][i] = -dl;
+        if constexpr (C::AUG) {
+          // c2 (S + a) = c2 S - LSE log2(e) with a = -LSE / sm_scale
+          aug_split(1 + st, i, -l2 / p.scale_log2);
+          aug_split(4 + st, i, -dl);
+        } else {
+          bars.nlse2[st][i] = -l2;
+          bars.ndelta[st][i] = -dl;
+        }
       }
+      if (C::AUG) fence_proxy_async_smem();  // the rows are read by the MMAs (async proxy)
       mbar_arrive(qb);
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
-    // Issue order per step: dV(it) [P from TMEM], S/dP(it+1), dK(it), dQ(it). The S/dP MMAs
-    // of the next step overlap the P/dS math of the compute warpgroups. The whole warp walks
-    // the schedule, so that every descriptor is warp-uniform; one elected lane issues.
+    // Issue order per step: S/dP(it+1) as soon as the compute warpgroups have loaded S^T and
+    // dP^T of step it (so the next step's scores are ready when their P/dS math ends), then
+    // dV(it) [P from TMEM], dK(it), dQ(it). The whole warp walks the schedule, so that every
+    // descriptor is warp-uniform; one elected lane issues.
     {
       constexpr uint32_t idS = idesc_f32acc(128, BM, false, false, F16);  // S^T, dP^T
       constexpr uint32_t idG = idesc_f32acc(128, D, false, true, F16);    // dV, dK
@@ -311,6 +349,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       const uint64_t q_kd = desc_kmajor(sQ, BM, 0), do_kd = desc_kmajor(sDO, BM, 0);
       const uint64_t q_mn = desc_mnmajor(sQ, BM, 0), do_mn = desc_mnmajor(sDO, BM, 0);
       const uint64_t ds_kd = desc_kmajor(sDS, BN, 0), ds_mn = desc_mnmajor(sDS, BN, 0);
+      const uint64_t aug_kd = desc_kmajor(sAUG, BN, 0);
       constexpr uint32_t QSTEP = C::Q_BYTES >> 4, DSSTEP = C::DS_BYTES >> 4;
       auto issue_sdp = [&](int it) -> bool {
         const int st = it % QST;
@@ -325,6 +364,11 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss_w(tDP, v_kd + kmajor_step(BN, kk), do_kd + qo + kmajor_step(BM, kk), idS,
                     kk > 0);
+        if constexpr (C::AUG) {  // S^T - LSE / sm_scale and dP^T - Delta (always bf16 operands)
+          constexpr uint32_t idA = idesc_f32acc(128, BM, false, false, false);
+          umma_ss_w(tS, aug_kd, aug_kd + kmajor_step(BN, 1 + st), idA, 1);
+          umma_ss_w(tDP, aug_kd, aug_kd + kmajor_step(BN, 4 + st), idA, 1);
+        }
         umma_commit_w(smem_u32(&bars.s_full));
         return true;
       };
@@ -332,12 +376,17 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       for (int it = 0; ok && it < n_steps; ++it) {
         const int st = it % QST, bs = it & 1;
         const uint32_t qo = st * QSTEP, dso = bs * DSSTEP;
+        if (it + 1 < n_steps) {
+          // S^T / dP^T of step it are in registers of the compute warpgroups: overwrite them
+          if (!mbar_wait(smem_u32(&bars.s_free), it & 1, abort, kWaitTimeoutNs)) break;
+          if (!issue_sdp(it + 1)) break;
+        }
         if (!mbar_wait(smem_u32(&bars.p_full), it & 1, abort, kWaitTimeoutNs)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           umma_ts_w(tDV, tP + kk * 8, do_mn + qo + mnmajor_step(kk), idG, (it > 0 || kk > 0));
-        if (it + 1 < n_steps && !issue_sdp(it + 1)) break;
+        umma_commit_w(smem_u32(&bars.p_empty));  // P^T of step it read: the next P may land
         if (!mbar_wait(smem_u32(&bars.ds_full[bs]), (it >> 1) & 1, abort, kWaitTimeoutNs)) break;
         tc_fence_after();
 #pragma unroll
@@ -457,6 +506,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         ATTN_TMEM_LD2_X32(tmem + C::COL_S + lane_off + c_base, tmem + C::COL_DP + lane_off + c_base,
                           reinterpret_cast<uint32_t*>(sv_all), reinterpret_cast<uint32_t*>(dpv_all));
       }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.s_free));  // the MMA warp may compute the next S^T / dP^T
+      // P^T of the previous step must have been read by its dV MMA before this step's lands
+      if (it > 0 && !mbar_wait(smem_u32(&bars.p_empty), (it - 1) & 1, abort, kWaitTimeoutNs)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
 #pragma unroll
       for (int ch = 0; ch < HALF / 32; ++ch) {
         const int c0 = c_base + ch * 32;
@@ -466,18 +523,29 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         const uint64_t c2x2 = f2_pack(c2, c2);
 #pragma unroll
         for (int e4 = 0; e4 < 32; e4 += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(&bars.nlse2[st][c0 + e4]);
-          const float4 d4 = *reinterpret_cast<const float4*>(&bars.ndelta[st][c0 + e4]);
-          float pv[4], ds[4], x[4], y[4];
-          // P = 2^(S c2 - LSE2); dS = P (dP - Delta): paired fp32 instructions
-          f2_unpack(f2_fma(f2_pack(s[e4], s[e4 + 1]), c2x2, f2_pack(l4.x, l4.y)), x[0], x[1]);
-          f2_unpack(f2_fma(f2_pack(s[e4 + 2], s[e4 + 3]), c2x2, f2_pack(l4.z, l4.w)), x[2], x[3]);
+          float pv[4], ds[4], x[4];
+          if constexpr (C::AUG) {
+            // S and dP arrive with LSE / sm_scale and Delta already subtracted
+            f2_unpack(f2_mul(f2_pack(s[e4], s[e4 + 1]), c2x2), x[0], x[1]);
+            f2_unpack(f2_mul(f2_pack(s[e4 + 2], s[e4 + 3]), c2x2), x[2], x[3]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) pv[u] = ex2_approx(x[u]);
-          f2_unpack(f2_add(f2_pack(dp[e4], dp[e4 + 1]), f2_pack(d4.x, d4.y)), y[0], y[1]);
-          f2_unpack(f2_add(f2_pack(dp[e4 + 2], dp[e4 + 3]), f2_pack(d4.z, d4.w)), y[2], y[3]);
-          f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), f2_pack(y[0], y[1])), ds[0], ds[1]);
-          f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), f2_pack(y[2], y[3])), ds[2], ds[3]);
+            for (int u = 0; u < 4; ++u) pv[u] = ex2_approx(x[u]);
+            f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), f2_pack(dp[e4], dp[e4 + 1])), ds[0], ds[1]);
+            f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), f2_pack(dp[e4 + 2], dp[e4 + 3])), ds[2], ds[3]);
+          } else {
+            const float4 l4 = *reinterpret_cast<const float4*>(&bars.nlse2[st][c0 + e4]);
+            const float4 d4 = *reinterpret_cast<const float4*>(&bars.ndelta[st][c0 + e4]);
+            float y[4];
+            // P = 2^(S c2 - LSE2); dS = P (dP - Delta): paired fp32 instructions
+            f2_unpack(f2_fma(f2_pack(s[e4], s[e4 + 1]), c2x2, f2_pack(l4.x, l4.y)), x[0], x[1]);
+            f2_unpack(f2_fma(f2_pack(s[e4 + 2], s[e4 + 3]), c2x2, f2_pack(l4.z, l4.w)), x[2], x[3]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pv[u] = ex2_approx(x[u]);
+            f2_unpack(f2_add(f2_pack(dp[e4], dp[e4 + 1]), f2_pack(d4.x, d4.y)), y[0], y[1]);
+            f2_unpack(f2_add(f2_pack(dp[e4 + 2], dp[e4 + 3]), f2_pack(d4.z, d4.w)), y[2], y[3]);
+            f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), f2_pack(y[0], y[1])), ds[0], ds[1]);
+            f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), f2_pack(y[2], y[3])), ds[2], ds[3]);
+          }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             if (need_mask) {
