@@ -301,7 +301,8 @@ def workload_config(name, variants):
 def run_e2e(args, variants, launch, kernels, stream, dist, world):
     """Same metric through the public API from pinned host buffers: every step copies q, k,
     v, dO (and cu_seqlens) host-to-device, runs the whole path and copies o, lse, dq, dk, dv
-    device-to-host, all inside the timed region (copies pipelined against compute)."""
+    device-to-host, all inside the timed region (copies of neighbouring steps overlap the
+    step's kernels through double-buffered device tensors)."""
     import torch
 
     host = []
@@ -321,23 +322,38 @@ def run_e2e(args, variants, launch, kernels, stream, dist, world):
             h2d += 2 * vt["cu_q"].numel() * 4
         host.append(hv)
 
-    # Three streams: host-to-device copies, compute, device-to-host copies. Each variant's
-    # transfers overlap the other variant's kernels; events keep every buffer's reuse in
-    # order (inputs are overwritten only after the kernels that read them finished, outputs
-    # only after their previous copy-out finished).
+    # Two sets of device buffers per variant, used by alternate steps, so that the copy-in of
+    # step s+1 and the copy-out of step s-1 run while step s computes (a training loop that
+    # prefetches its next batch). Three streams: host-to-device copies, compute,
+    # device-to-host copies; events keep every buffer's reuse in order (a set's inputs are
+    # overwritten only after the kernels that read them finished, its outputs only after
+    # their previous copy-out finished). The workspace is shared: compute is one stream.
+    sets = []
+    for vt in variants:
+        alt = dict(vt)
+        for n in ("q", "k", "v", "do", "o", "lse", "dq", "dk", "dv"):
+            alt[n] = torch.empty_like(vt[n])
+        if vt["cu_q"] is not None:
+            alt["cu_q"], alt["cu_k"] = vt["cu_q"].clone(), vt["cu_k"].clone()
+        sets.append((vt, alt))
     s_h2d, s_comp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
-    comp_done = [ev() for _ in variants]
-    d2h_done = [ev() for _ in variants]
-    for e in comp_done + d2h_done:
-        e.record(stream)
+    comp_done = [[ev(), ev()] for _ in variants]
+    d2h_done = [[ev(), ev()] for _ in variants]
+    for pair in comp_done + d2h_done:
+        for e in pair:
+            e.record(stream)
     torch.cuda.synchronize()
+    counter = [0]
 
     def e2e_step():
-        for i, (vt, hv) in enumerate(zip(variants, host)):
+        b = counter[0] % 2
+        counter[0] += 1
+        for i, hv in enumerate(host):
+            vt = sets[i][b]
             h2d_done = ev()
             with torch.cuda.stream(s_h2d):
-                s_h2d.wait_event(comp_done[i])
+                s_h2d.wait_event(comp_done[i][b])
                 for n in ("q", "k", "v", "do"):
                     vt[n].copy_(hv[n], non_blocking=True)
                 if vt["cu_q"] is not None:
@@ -346,15 +362,15 @@ def run_e2e(args, variants, launch, kernels, stream, dist, world):
                 h2d_done.record(s_h2d)
             with torch.cuda.stream(s_comp):
                 s_comp.wait_event(h2d_done)
-                s_comp.wait_event(d2h_done[i])
+                s_comp.wait_event(d2h_done[i][b])
                 for kern in kernels:
                     launch(vt, kern)
-                comp_done[i].record(s_comp)
+                comp_done[i][b].record(s_comp)
             with torch.cuda.stream(s_d2h):
-                s_d2h.wait_event(comp_done[i])
+                s_d2h.wait_event(comp_done[i][b])
                 for n in ("o", "lse", "dq", "dk", "dv"):
                     hv["out_" + n].copy_(vt[n], non_blocking=True)
-                d2h_done[i].record(s_d2h)
+                d2h_done[i][b].record(s_d2h)
 
     for _ in range(3):
         e2e_step()
@@ -366,8 +382,9 @@ def run_e2e(args, variants, launch, kernels, stream, dist, world):
     a.record(s_h2d)
     for _ in range(steps):
         e2e_step()
-    for e in d2h_done + comp_done:
-        s_d2h.wait_event(e)
+    for pair in d2h_done + comp_done:
+        for e in pair:
+            s_d2h.wait_event(e)
     b.record(s_d2h)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
