@@ -190,6 +190,16 @@ attn_status make_map_acc(CUtensorMap* m, float* acc, int64_t rows, int64_t D) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Causal tiles differ in work. With the tile index as the slowest grid dimension the CTAs
+// are dispatched heaviest first across all (unit, head) pairs, which removes the tail that
+// a per-head heaviest-first order leaves (the last head's heaviest tile starts near the
+// end). It also spreads the CTAs of one head over the whole launch, so the operands they
+// share must stay in L2 between them: the order is used when those bytes are at most 72 MB
+// (L2 is 129 MB) and the tile count fits grid z.
+bool tile_major_order(int causal, double shared_bytes, int tiles) {
+  return causal && shared_bytes <= 72.0 * 1024 * 1024 && tiles <= 65535;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct BwdWorkspace {
@@ -257,7 +267,9 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   p.status = reinterpret_cast<int*>(ws);
   p.withhold_tile = withheld_tile_for_test();
   p.timeout_ns = p.withhold_tile >= 0 ? 50000000ull : kWaitTimeoutNs;
-  dim3 grid((pr.max_q + BM - 1) / BM, pr.H, pr.units);
+  const int n_blk = (pr.max_q + BM - 1) / BM;
+  p.tile_major = tile_major_order(p.causal, (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
+  const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_blk) : dim3(n_blk, pr.H, pr.units);
   cudaError_t e = launch_attn_fwd(p, pr.D, pr.f16, grid, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -324,7 +336,11 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       p.scale_log2 = sm_scale * 1.4426950408889634f;
       p.sm_scale = sm_scale;
       p.status = status;
-      dim3 grid((pr.max_k + BN - 1) / BN, pr.H, pr.units);
+      const int n_tiles = (pr.max_k + BN - 1) / BN;
+      // the operands every CTA of a head visits: Q, dO (16-bit) and the fp32 dQ accumulator
+      p.tile_major = tile_major_order(p.causal, (double)pr.units * pr.H * pr.max_q * pr.D * 8,
+                                      n_tiles);
+      const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_tiles) : dim3(n_tiles, pr.H, pr.units);
       if (launch_bwd_main(p, pr.D, pr.f16, grid, st) != cudaSuccess) return ATTN_ERR_CUDA;
     }
   }

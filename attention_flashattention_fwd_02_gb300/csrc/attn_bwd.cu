@@ -191,7 +191,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
   __shared__ BwdBars<BM, QST, C::LSE_ST> bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tile = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+  // grid (key tiles, H, units), or (units, H, key tiles) for a longest-first causal order
+  const int h = blockIdx.y;
+  const int n_tile = p.tile_major ? (int)blockIdx.z : (int)blockIdx.x;
+  const int z = p.tile_major ? (int)blockIdx.x : (int)blockIdx.z;
 
   SeqView sv;
   if (!decode_seq(p.seq, z, threadIdx.x == 0 ? p.status : nullptr, sv)) return;

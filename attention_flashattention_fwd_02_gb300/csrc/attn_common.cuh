@@ -69,6 +69,7 @@ struct FwdParams {
   int* status;                    // device status word, may be null
   uint64_t timeout_ns;            // bound on every pipeline wait
   int withhold_tile;              // test hook: key tile the producer never loads (-1: none)
+  int tile_major;                 // grid (units, H, tiles) instead of (tiles, H, units)
 };
 
 struct BwdPreParams {
@@ -99,6 +100,7 @@ struct BwdParams {
   int H, rows_q;                  // rows_q: per-(batch, head) row count of delta / dq_acc
   SeqAddr seq;
   int causal;
+  int tile_major;                 // grid (units, H, key tiles) instead of (key tiles, H, units)
   float scale_log2;               // sm_scale * log2(e)
   float sm_scale;
   int* status;

@@ -105,8 +105,13 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
   __shared__ FwdBars<NST, NSB> bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y, z = blockIdx.z;
-  const int m_blk = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  // grid (query blocks, H, units), or (units, H, query blocks) for a longest-first order across
+  // the whole grid; causal blocks are visited from the last (heaviest) one down
+  const int h = blockIdx.y;
+  const int z = p.tile_major ? (int)blockIdx.x : (int)blockIdx.z;
+  const int blk = p.tile_major ? (int)blockIdx.z : (int)blockIdx.x;
+  const int n_blk = p.tile_major ? (int)gridDim.z : (int)gridDim.x;
+  const int m_blk = p.causal ? n_blk - 1 - blk : blk;
 
   SeqView sv;
   if (!decode_seq(p.seq, z, threadIdx.x == 0 ? p.status : nullptr, sv)) return;

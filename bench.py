@@ -232,7 +232,7 @@ def run_ours(args, rank, world, dist, clocks_on=True):
 
     flops_step = sum(vt["f_fwd"] + vt["f_bwd"] for vt in variants)
     value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
-    peak_b, peak_s, _, peak_src = peaks()
+    peak_b, peak_s, peak_h, peak_src = peaks()
 
     # per-kernel roofline figures (tensor-bound kernels: algorithmic flops / event time)
     per_kernel = {}
@@ -241,6 +241,18 @@ def run_ours(args, rank, world, dist, clocks_on=True):
         per_kernel[kn] = ms
     fwd_fl = sum(vt["f_fwd"] for vt in variants) * args.steps
     bwd_fl = sum(vt["f_bwd"] for vt in variants) * args.steps
+    # HBM-bound kernels: algorithmic bytes over the valid query rows (preprocess reads O and dO,
+    # writes Delta and zeroes the fp32 dQ accumulator row; the epilogue reads the accumulator
+    # and writes dQ)
+    def valid_rows(vt):
+        wl = vt["wl"]
+        if wl.layout in ("compact", "padded"):
+            return wl.H * int(vt["x"]["lengths"].sum())
+        return wl.B * wl.H * wl.Sq
+    pre_b = sum(valid_rows(vt) * (2 * 2 * vt["wl"].D + 4 * vt["wl"].D + 4) for vt in variants)
+    post_b = sum(valid_rows(vt) * (4 * vt["wl"].D + 2 * vt["wl"].D) for vt in variants)
+    pre_gbs = pre_b * args.steps / (per_kernel["bwd_pre"] * 1e-3) / 1e9
+    post_gbs = post_b * args.steps / (per_kernel["bwd_post"] * 1e-3) / 1e9
     dominant = max(("fwd", "bwd_main"), key=lambda k: per_kernel[k])
     dom_fl = fwd_fl if dominant == "fwd" else bwd_fl
     achieved = dom_fl / (per_kernel[dominant] * 1e-3) / 1e12
@@ -264,6 +276,9 @@ def run_ours(args, rank, world, dist, clocks_on=True):
             "fwd_frac_of_peak": round(fwd_fl / (per_kernel["fwd"] * 1e-3) / 1e12 / peak_b, 4),
             "bwd_frac_of_peak": round(bwd_fl / (sum(per_kernel[k] for k in KERNELS[1:]) * 1e-3)
                                       / 1e12 / peak_b, 4),
+            "bwd_pre_gbs": round(pre_gbs, 1), "bwd_pre_frac_of_hbm": round(pre_gbs / peak_h, 4),
+            "bwd_post_gbs": round(post_gbs, 1), "bwd_post_frac_of_hbm": round(post_gbs / peak_h, 4),
+            "hbm_peak_gbs": peak_h,
             "ms_per_step": {k: round(per_kernel[k] / args.steps, 4) for k in KERNELS},
         },
         "gpu_launches": len(variants) * len(KERNELS) * args.steps,
