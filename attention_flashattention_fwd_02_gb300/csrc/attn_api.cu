@@ -101,7 +101,7 @@ attn_status make_problem(const attn_tensor4* q, const attn_tensor4* k, const att
   if (q->size[0] != k->size[0] || q->size[1] != k->size[1] || q->size[3] != k->size[3])
     return ATTN_ERR_SHAPE;
   const int64_t D = q->size[3];
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 32 && D != 64 && D != 96 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (q->size[1] > 65535) return ATTN_ERR_UNSUPPORTED;  // grid y
   pr->B = (int)q->size[0];
   pr->H = (int)q->size[1];
@@ -196,6 +196,11 @@ attn_status make_map_acc(CUtensorMap* m, float* acc, int64_t rows, int64_t D) {
 // end). It also spreads the CTAs of one head over the whole launch, so the operands they
 // share must stay in L2 between them: the order is used when those bytes are at most 72 MB
 // (L2 is 129 MB) and the tile count fits grid z.
+// Head sizes 32 and 96 run on the kernels built for 64 and 128: the TMA loads (box 64
+// columns wide) fill the columns past the head size with zeros, which add nothing to any
+// product, and only the real columns are stored.
+int kernel_width(int D) { return D <= 64 ? 64 : 128; }
+
 bool tile_major_order(int causal, double shared_bytes, int tiles) {
   return causal && shared_bytes <= 72.0 * 1024 * 1024 && tiles <= 65535;
 }
@@ -270,7 +275,9 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   const int n_blk = (pr.max_q + BM - 1) / BM;
   p.tile_major = tile_major_order(p.causal, (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
   const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_blk) : dim3(n_blk, pr.H, pr.units);
-  cudaError_t e = launch_attn_fwd(p, pr.D, pr.f16, grid, reinterpret_cast<cudaStream_t>(stream));
+  p.d_out = pr.D;
+  cudaError_t e = launch_attn_fwd(p, kernel_width(pr.D), pr.f16, grid,
+                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -314,7 +321,7 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
     if (pr.max_k > 0) {
       BwdParams p;
       memset(&p, 0, sizeof(p));
-      const int BM = bwd_block_m(pr.D), BN = bwd_block_n();
+      const int BM = bwd_block_m(kernel_width(pr.D)), BN = bwd_block_n();
       if ((s = make_map(&p.tm_q, a.q, BM)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_do, a.dout, BM)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_k, a.k, BN)) != ATTN_OK) return s;
@@ -341,7 +348,9 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       p.tile_major = tile_major_order(p.causal, (double)pr.units * pr.H * pr.max_q * pr.D * 8,
                                       n_tiles);
       const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_tiles) : dim3(n_tiles, pr.H, pr.units);
-      if (launch_bwd_main(p, pr.D, pr.f16, grid, st) != cudaSuccess) return ATTN_ERR_CUDA;
+      p.d_out = pr.D;
+      if (launch_bwd_main(p, kernel_width(pr.D), pr.f16, grid, st) != cudaSuccess)
+        return ATTN_ERR_CUDA;
     }
   }
   if (stage_mask & 4) {

@@ -35,10 +35,11 @@ __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // =========================================================================== preprocess
-// One group of D/8 threads per row: each thread reads 8 elements (16 bytes) of O and dO.
-template <int D, bool F16>
+// One group of W/8 threads per row, W = the head size rounded up to a power of two: each
+// thread reads 8 elements (16 bytes) of O and dO; threads past the head size (p.D) add zero.
+template <int W, bool F16>
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant__ BwdPreParams p) {
-  constexpr int TPR = D / 8;             // threads per row
+  constexpr int TPR = W / 8;             // threads per row
   constexpr int ROWS = 256 / TPR;        // rows per block
   const int h = blockIdx.y, z = blockIdx.z;
   SeqView sv;
@@ -48,8 +49,9 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant
   if (blockIdx.x * ROWS >= sv.len_q) return;
   float acc = 0.f;
   const bool valid = r < sv.len_q;
+  const bool cols = part * 8 < p.D;
   const int64_t grow = sv.row0_q + r;
-  if (valid) {
+  if (valid && cols) {
     const uint4 a = *reinterpret_cast<const uint4*>(p.o + sv.batch * p.o_sb + h * p.o_sh +
                                                     grow * p.o_ss + part * 8);
     const uint4 b = *reinterpret_cast<const uint4*>(p.dout + sv.batch * p.do_sb + h * p.do_sh +
@@ -68,41 +70,51 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant
   if (valid) {
     const int64_t idx = ((int64_t)sv.batch * p.H + h) * p.rows + grow;
     if (part == 0) p.delta[idx] = acc;
-    float4* dst = reinterpret_cast<float4*>(p.dq_acc + idx * D + part * 8);
+  }
+  if (valid && cols) {
+    const int64_t idx = ((int64_t)sv.batch * p.H + h) * p.rows + grow;
+    float4* dst = reinterpret_cast<float4*>(p.dq_acc + idx * p.D + part * 8);
     dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
+// Power-of-two thread-group width covering head size D.
+static int pow2_width(int D) { return D <= 32 ? 32 : (D <= 64 ? 64 : 128); }
+
 cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream) {
-  const int rows_per_block = 256 / (p.D / 8);
+  const int W = pow2_width(p.D);
+  const int rows_per_block = 256 / (W / 8);
   const int max_len = p.seq.mode == kCompact ? p.seq.max_q : p.seq.Sq;
   dim3 grid((max_len + rows_per_block - 1) / rows_per_block, p.H, p.units);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  if (p.D == 128) {
+  if (W == 128) {
     if (p.f16) attn_bwd_pre_kernel<128, true><<<grid, 256, 0, stream>>>(p);
     else attn_bwd_pre_kernel<128, false><<<grid, 256, 0, stream>>>(p);
-  } else {
+  } else if (W == 64) {
     if (p.f16) attn_bwd_pre_kernel<64, true><<<grid, 256, 0, stream>>>(p);
     else attn_bwd_pre_kernel<64, false><<<grid, 256, 0, stream>>>(p);
+  } else {
+    if (p.f16) attn_bwd_pre_kernel<32, true><<<grid, 256, 0, stream>>>(p);
+    else attn_bwd_pre_kernel<32, false><<<grid, 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }
 
 // =========================================================================== dQ epilogue
-template <int D, bool F16>
+template <int W, bool F16>
 __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const __grid_constant__ BwdPostParams p) {
-  constexpr int TPR = D / 8;
+  constexpr int TPR = W / 8;
   constexpr int ROWS = 256 / TPR;
   const int h = blockIdx.y, z = blockIdx.z;
   SeqView sv;
   if (!decode_seq(p.seq, z, nullptr, sv)) return;
   const int r = blockIdx.x * ROWS + threadIdx.x / TPR;
   const int part = threadIdx.x % TPR;
-  if (r >= sv.len_q) return;
+  if (r >= sv.len_q || part * 8 >= p.D) return;
   const int64_t grow = sv.row0_q + r;
   const int64_t idx = ((int64_t)sv.batch * p.H + h) * p.rows + grow;
-  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + idx * D + part * 8);
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + idx * p.D + part * 8);
   const float4 a = src[0], b = src[1];
   uint4 v;
   v.x = pack2<F16>(a.x * p.sm_scale, a.y * p.sm_scale);
@@ -113,16 +125,20 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const __grid_constan
 }
 
 cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream) {
-  const int rows_per_block = 256 / (p.D / 8);
+  const int W = pow2_width(p.D);
+  const int rows_per_block = 256 / (W / 8);
   const int max_len = p.seq.mode == kCompact ? p.seq.max_q : p.seq.Sq;
   dim3 grid((max_len + rows_per_block - 1) / rows_per_block, p.H, p.units);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  if (p.D == 128) {
+  if (W == 128) {
     if (p.f16) attn_bwd_post_kernel<128, true><<<grid, 256, 0, stream>>>(p);
     else attn_bwd_post_kernel<128, false><<<grid, 256, 0, stream>>>(p);
-  } else {
+  } else if (W == 64) {
     if (p.f16) attn_bwd_post_kernel<64, true><<<grid, 256, 0, stream>>>(p);
     else attn_bwd_post_kernel<64, false><<<grid, 256, 0, stream>>>(p);
+  } else {
+    if (p.f16) attn_bwd_post_kernel<32, true><<<grid, 256, 0, stream>>>(p);
+    else attn_bwd_post_kernel<32, false><<<grid, 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }
@@ -220,7 +236,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         const int64_t grow = sv.row0_k + key;
         uint16_t* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
         uint16_t* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
-        for (int d = 0; d < D; d += 8) {
+        for (int d = 0; d < p.d_out; d += 8) {
           *reinterpret_cast<uint4*>(kr + d) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(vr + d) = make_uint4(0, 0, 0, 0);
         }
@@ -465,7 +481,8 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
+      // blocks wholly in the zero padding past the head size add nothing: skip them
+      if (lane == 0 && c0 < p.d_out) {
         tma_reduce_add_2d(&p.tm_dq, smem_u32(stage), c0, (int)(zh * p.rows_q + sv.row0_q + r0));
         bulk_commit_group();
       }
@@ -596,7 +613,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       for (int c = g * (D / 2); c < (g + 1) * (D / 2); c += 32) {
         uint32_t a[32], b[32];
         ATTN_TMEM_LD2_X32(tmem + C::COL_DK + lane_off + c, tmem + C::COL_DV + lane_off + c, a, b);
-        if (key_ok) {
+        if (key_ok && c < p.d_out) {  // columns past the head size are zero padding
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 vk, vv;

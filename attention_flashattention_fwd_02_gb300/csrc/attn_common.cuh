@@ -70,6 +70,8 @@ struct FwdParams {
   uint64_t timeout_ns;            // bound on every pipeline wait
   int withhold_tile;              // test hook: key tile the producer never loads (-1: none)
   int tile_major;                 // grid (units, H, tiles) instead of (tiles, H, units)
+  int d_out;                      // head size of the tensors (<= the kernel's D; the TMA
+                                  // loads fill the columns past it with zeros)
 };
 
 struct BwdPreParams {
@@ -100,6 +102,7 @@ struct BwdParams {
   int H, rows_q;                  // rows_q: per-(batch, head) row count of delta / dq_acc
   SeqAddr seq;
   int causal;
+  int d_out;                      // head size of the tensors (<= the kernel's D)
   int tile_major;                 // grid (units, H, key tiles) instead of (key tiles, H, units)
   float scale_log2;               // sm_scale * log2(e)
   float sm_scale;

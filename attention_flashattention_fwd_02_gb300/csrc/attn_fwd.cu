@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
       if (row < sv.len_q) {
         const int64_t grow = sv.row0_q + row;
         uint16_t* orow = p.o + sv.batch * p.o_sb + h * p.o_sh + grow * p.o_ss;
-        for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+        for (int d = 0; d < p.d_out; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
         p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] = -INFINITY;
       }
     }
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
-        if (valid) {
+        if (valid && c * 32 < p.d_out) {  // columns past the head size are zero padding
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 v;

@@ -21,7 +21,9 @@
  * LSE is fp32 with shape (B, H, Sq). Q/K/V/O share B, H and D; seqlen_q and seqlen_k
  * may differ ("[RFC] Goal for triton.ops.flash_attention" lists a different number of
  * queries and keys as a missing case; the AOTriton issue #12 page states that QKVO share a
- * dtype and shape except for seqlen_q vs seqlen_k). d_head must be 64 or 128.
+ * dtype and shape except for seqlen_q vs seqlen_k). d_head must be 32, 64, 96 or 128 (32
+ * and 96 run on the 64- and 128-wide kernels with zero-filled columns; only the real
+ * columns of the outputs are written).
  *
  * Masking. causal != 0 applies a top-left aligned mask: query i sees key j iff j <= i,
  * indices local to the sequence. Keys at or past a sequence's length are never seen.
@@ -89,7 +91,7 @@ typedef enum {
   ATTN_ERR_SHAPE = 2,         /* inconsistent sizes (B, H, D, S), or compact batch != 1 */
   ATTN_ERR_STRIDE = 3,        /* D stride != 1, or a stride not a multiple of 8 elements */
   ATTN_ERR_ALIGN = 4,         /* base pointer not 16-byte aligned */
-  ATTN_ERR_UNSUPPORTED = 5,   /* d_head not 64/128, device is not sm_103, or size limits */
+  ATTN_ERR_UNSUPPORTED = 5,   /* d_head not 32/64/96/128, device not sm_103, or size limits */
   ATTN_ERR_WORKSPACE = 6,     /* workspace NULL or smaller than the *_workspace_size value */
   ATTN_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed (launch, tensor map) */
   ATTN_ERR_DEVICE_BAD_SEQLENS = 8, /* device: cu_seqlens not monotone or past the tensor */

@@ -93,7 +93,9 @@ def good():
     ("d_stride", ERR_STRIDE),
     ("s_stride_not_mult8", ERR_STRIDE),
     ("misaligned", ERR_ALIGN),
-    ("d_head_96", ERR_UNSUPPORTED),
+    ("d_head_48", ERR_UNSUPPORTED),
+    ("d_head_80", ERR_UNSUPPORTED),
+    ("d_head_256", ERR_UNSUPPORTED),
     ("kv_shape", ERR_SHAPE),
     ("o_shape", ERR_SHAPE),
     ("lse_shape", ERR_SHAPE),
@@ -113,8 +115,9 @@ def test_fwd_rejects(lib, case, expect):
         q.stride[2] = 65
     elif case == "misaligned":
         q = t4(GOOD, ptr=FAKE + 8)
-    elif case == "d_head_96":
-        q, k, v, o = (t4((1, 2, 128, 96)) for _ in range(4))
+    elif case.startswith("d_head_"):
+        dh = int(case.split("_")[-1])
+        q, k, v, o = (t4((1, 2, 128, dh)) for _ in range(4))
     elif case == "kv_shape":
         v = t4((1, 2, 64, 64))
     elif case == "o_shape":

@@ -254,3 +254,43 @@ def test_fp16_parity(layout, D, causal):
     assert o.dtype == torch.float16 and grads[0].dtype == torch.float16
     assert_fwd_close(o, lse, o_r, lse_r, what=f"fp16 {layout}")
     assert_grads_close(grads, g_r, what=f"fp16 {layout}")
+
+
+# Head sizes 32 and 96 run on the 64- and 128-wide kernels with zero-filled columns.
+ODD_D_CASES = [
+    # (layout, D, causal)
+    ("bhsd", 32, True),
+    ("bhsd", 96, False),
+    ("kv_bshd", 32, False),
+    ("kv_bshd", 96, True),
+    ("padded", 32, False),
+    ("padded", 96, True),
+    ("compact", 32, True),
+    ("compact", 96, False),
+]
+
+
+@pytest.mark.parametrize("layout,D,causal", ODD_D_CASES)
+def test_odd_head_size_parity(layout, D, causal):
+    if layout == "compact":
+        wl = WORKLOADS["compact"].replace(H=2, D=D, causal=causal, n_seqs=4, seed=61 + D)
+        x = make_inputs(wl, lengths=[1, 200, 129, 64])
+        o, lse, grads = _run_compact(x, wl.sm_scale, causal, T_extra=9)
+        T = 394
+        q, k, v, do = (np64(x[n]) for n in ("q", "k", "v", "do"))
+        cu = x["cu_seqlens_q"].numpy()
+        o_r, lse_r = ref.fwd_compact_varlen(q, k, v, cu, cu, wl.sm_scale, causal)
+        g_r = ref.bwd_compact_varlen(q, k, v, do, cu, cu, wl.sm_scale, causal)
+        assert_fwd_close(o[:, :, :T], lse[:, :, :T], o_r, lse_r, what=f"compact D={D}")
+        assert_grads_close(tuple(g[:, :, :T] for g in grads), g_r, what=f"compact D={D}")
+        return
+    padded = layout == "padded"
+    base = WORKLOADS["padded" if padded else "cross"]
+    wl = base.replace(B=2, H=2, Sq=300, Sk=300 if layout != "kv_bshd" else 410, D=D,
+                      causal=causal, layout=layout, seed=67 + D)
+    x = make_inputs(wl, lengths=[300, 77] if padded else None)
+    o, lse, grads = _run_dense(x, wl.sm_scale, causal, padded=padded)
+    o_r, lse_r, g_r = _oracle_dense(x, wl.sm_scale, causal, padded=padded)
+    assert o.shape[-1] == D and grads[0].shape[-1] == D
+    assert_fwd_close(o, lse, o_r, lse_r, what=f"{layout} D={D}")
+    assert_grads_close(grads, g_r, what=f"{layout} D={D}")
