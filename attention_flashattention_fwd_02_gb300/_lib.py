@@ -21,7 +21,9 @@ __all__ = [
     "attn_fwd_padded_varlen", "attn_bwd_padded_varlen",
     "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_dq_epilogue",
     "attn_fwd_workspace_size", "attn_bwd_workspace_size",
-    "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc", "EXPORTED_SYMBOLS",
+    "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
+    "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
+    "attn_bwd_deterministic_workspace_size", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -29,6 +31,8 @@ EXPORTED_SYMBOLS = (
     "attn_fwd_compact_varlen", "attn_bwd_compact_varlen", "attn_fwd_padded_varlen",
     "attn_bwd_padded_varlen", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_dq_epilogue",
     "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
+    "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
+    "attn_bwd_deterministic_workspace_size",
 )
 
 
@@ -65,6 +69,7 @@ INT = ctypes.c_int
 _SIGS = {
     "attn_fwd_workspace_size": (SZ, [ctypes.c_int64] * 4),
     "attn_bwd_workspace_size": (SZ, [ctypes.c_int64] * 4),
+    "attn_bwd_deterministic_workspace_size": (SZ, [ctypes.c_int64] * 4),
     "attn_fwd": (INT, [P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
     "attn_fwd_padded_varlen": (INT, [P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
     "attn_fwd_compact_varlen": (INT, [P4, P4, P4, I32P, I32P, I32, I32, I32, F32, INT, P4, P3,
@@ -74,6 +79,10 @@ _SIGS = {
                                      VP, SZ, VP]),
     "attn_bwd_compact_varlen": (INT, [P4, P4, P4, P4, P3, P4, I32P, I32P, I32, I32, I32, F32,
                                       INT, P4, P4, P4, VP, SZ, VP]),
+    "attn_bwd_deterministic": (INT, [P4, P4, P4, P4, P3, P4, I32P, I32P, F32, INT, P4, P4, P4,
+                                     VP, SZ, VP]),
+    "attn_bwd_compact_varlen_deterministic": (INT, [P4, P4, P4, P4, P3, P4, I32P, I32P, I32,
+                                                    I32, I32, F32, INT, P4, P4, P4, VP, SZ, VP]),
     "attn_bwd_preprocess": (INT, [P4, P4, I32P, I32, I32, VP, SZ, VP]),
     "attn_bwd_main": (INT, [P4, P4, P4, P3, P4, I32P, I32P, I32, I32, I32, F32, INT, P4, P4,
                             VP, SZ, VP]),
@@ -231,15 +240,35 @@ def attn_bwd_padded_varlen(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, 
 
 def attn_bwd_compact_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
                             num_seqs, max_seqlen_q, max_seqlen_k, sm_scale, causal, workspace,
-                            stream=None):
+                            stream=None, _name="attn_bwd_compact_varlen"):
     _check16(q, k, v, o, dout, dq, dk, dv)
     tq, tk, tv, to, tl, tdo = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse), _t4(dout)
     tdq, tdk, tdv = _t4(dq), _t4(dk), _t4(dv)
     ws, nws = _ws(workspace)
-    _check(load().attn_bwd_compact_varlen(
+    _check(getattr(load(), _name)(
         *_keep(tq, tk, tv, to, tl, tdo), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(num_seqs),
         int(max_seqlen_q), int(max_seqlen_k), float(sm_scale), int(bool(causal)),
-        *_keep(tdq, tdk, tdv), ws, nws, _stream(stream)), "attn_bwd_compact_varlen")
+        *_keep(tdq, tdk, tdv), ws, nws, _stream(stream)), _name)
+
+
+def attn_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, workspace,
+                           cu_seqlens_q=None, cu_seqlens_k=None, stream=None):
+    """attn_bwd with run-to-run identical results (dQ without reductions)."""
+    attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, workspace, cu_seqlens_q,
+             cu_seqlens_k, stream, _name="attn_bwd_deterministic")
+
+
+def attn_bwd_compact_varlen_deterministic(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q,
+                                          cu_seqlens_k, num_seqs, max_seqlen_q, max_seqlen_k,
+                                          sm_scale, causal, workspace, stream=None):
+    """attn_bwd_compact_varlen with run-to-run identical results."""
+    attn_bwd_compact_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
+                            num_seqs, max_seqlen_q, max_seqlen_k, sm_scale, causal, workspace,
+                            stream, _name="attn_bwd_compact_varlen_deterministic")
+
+
+def attn_bwd_deterministic_workspace_size(B, H, Sq, D) -> int:
+    return int(load().attn_bwd_deterministic_workspace_size(int(B), int(H), int(Sq), int(D)))
 
 
 def attn_bwd_preprocess(o, dout, workspace, cu_seqlens_q=None, num_seqs=-1, max_seqlen_q=0,

@@ -40,38 +40,41 @@ class FlashAttentionFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, sm_scale, causal, cu_seqlens_q, cu_seqlens_k, compact,
-                max_seqlen_q, max_seqlen_k):
+                max_seqlen_q, max_seqlen_k, deterministic=False):
         o, lse = attention.forward(q, k, v, sm_scale, causal, cu_seqlens_q, cu_seqlens_k,
                                    compact=compact, max_seqlen_q=max_seqlen_q,
                                    max_seqlen_k=max_seqlen_k)
         ctx.save_for_backward(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k)
-        ctx.cfg = (sm_scale, causal, compact, max_seqlen_q, max_seqlen_k)
+        ctx.cfg = (sm_scale, causal, compact, max_seqlen_q, max_seqlen_k, deterministic)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse, cu_q, cu_k = ctx.saved_tensors
-        sm_scale, causal, compact, max_q, max_k = ctx.cfg
+        sm_scale, causal, compact, max_q, max_k, det = ctx.cfg
         do = do.contiguous() if do.stride(-1) != 1 else do
         dq, dk, dv = attention.backward(q, k, v, o, lse, do, sm_scale, causal, cu_q, cu_k,
-                                        compact=compact, max_seqlen_q=max_q, max_seqlen_k=max_k)
-        return dq, dk, dv, None, None, None, None, None, None, None
+                                        compact=compact, max_seqlen_q=max_q, max_seqlen_k=max_k,
+                                        deterministic=det)
+        return dq, dk, dv, None, None, None, None, None, None, None, None
 
 
 def flash_attention(q, k, v, sm_scale: Optional[float] = None, causal: bool = False,
-                    cu_seqlens_q=None, cu_seqlens_k=None):
-    """Dense (cu_seqlens None) or padded-varlen attention on BHSD views, differentiable."""
+                    cu_seqlens_q=None, cu_seqlens_k=None, deterministic: bool = False):
+    """Dense (cu_seqlens None) or padded-varlen attention on BHSD views, differentiable.
+    deterministic=True makes the gradients identical from run to run."""
     scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else float(sm_scale)
     return FlashAttentionFunction.apply(q, k, v, scale, bool(causal), cu_seqlens_q, cu_seqlens_k,
-                                        False, 0, 0)
+                                        False, 0, 0, bool(deterministic))
 
 
 def flash_attention_varlen(q_thd, k_thd, v_thd, cu_seqlens_q, cu_seqlens_k,
                            max_seqlen_q: int = 0, max_seqlen_k: int = 0,
-                           sm_scale: Optional[float] = None, causal: bool = False):
+                           sm_scale: Optional[float] = None, causal: bool = False,
+                           deterministic: bool = False):
     """Compact varlen attention on packed (T, H, D) tensors; returns (T, H, D)."""
     scale = 1.0 / math.sqrt(q_thd.shape[-1]) if sm_scale is None else float(sm_scale)
     o = FlashAttentionFunction.apply(thd_to_bhsd(q_thd), thd_to_bhsd(k_thd), thd_to_bhsd(v_thd),
                                      scale, bool(causal), cu_seqlens_q, cu_seqlens_k, True,
-                                     int(max_seqlen_q), int(max_seqlen_k))
+                                     int(max_seqlen_q), int(max_seqlen_k), bool(deterministic))
     return bhsd_to_thd(o)

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libattn_sm103.so"
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_noalloc.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_dq.cu", "attn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr"]

@@ -287,10 +287,14 @@ struct BwdArgs {
   const attn_tensor3* lse;
 };
 
+// Stages: 1 preprocess, 2 key-tile kernel, 4 dQ epilogue, 8 deterministic dQ kernel. In
+// deterministic mode the preprocess leaves the fp32 accumulator alone, the key-tile kernel
+// skips its dQ products and the workspace needs only the status word and Delta.
 attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float sm_scale,
-                      int causal, void* ws, size_t ws_bytes, void* stream) {
+                      int causal, void* ws, size_t ws_bytes, void* stream,
+                      bool deterministic = false) {
   const BwdWorkspace w = bwd_layout(pr.B, pr.H, pr.Sq, pr.D);
-  if (ws == nullptr || ws_bytes < w.total) return ATTN_ERR_WORKSPACE;
+  if (ws == nullptr || ws_bytes < (deterministic ? w.dq_off : w.total)) return ATTN_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return ATTN_ERR_ALIGN;
   attn_status s = check_device();
   if (s != ATTN_OK) return s;
@@ -311,7 +315,7 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
     pp.o_sb = a.o->stride[0]; pp.o_sh = a.o->stride[1]; pp.o_ss = a.o->stride[2];
     pp.do_sb = a.dout->stride[0]; pp.do_sh = a.dout->stride[1]; pp.do_ss = a.dout->stride[2];
     pp.delta = delta;
-    pp.dq_acc = dq_acc;
+    pp.dq_acc = deterministic ? nullptr : dq_acc;
     pp.units = pr.units; pp.H = pr.H; pp.rows = pr.Sq; pp.D = pr.D;
     pp.seq = sa;
     pp.status = status;
@@ -326,7 +330,9 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       if ((s = make_map(&p.tm_do, a.dout, BM)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_k, a.k, BN)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_v, a.v, BN)) != ATTN_OK) return s;
-      if ((s = make_map_acc(&p.tm_dq, dq_acc, (int64_t)pr.B * pr.H * pr.Sq, pr.D)) != ATTN_OK)
+      p.with_dq = deterministic ? 0 : 1;
+      if (p.with_dq &&
+          (s = make_map_acc(&p.tm_dq, dq_acc, (int64_t)pr.B * pr.H * pr.Sq, pr.D)) != ATTN_OK)
         return s;
       p.lse = reinterpret_cast<const float*>(a.lse->data);
       p.l_sb = a.lse->stride[0]; p.l_sh = a.lse->stride[1]; p.l_ss = a.lse->stride[2];
@@ -365,12 +371,40 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
     pp.sm_scale = sm_scale;
     if (launch_bwd_dq_epilogue(pp, st) != cudaSuccess) return ATTN_ERR_CUDA;
   }
+  if (stage_mask & 8) {
+    BwdDqParams p;
+    memset(&p, 0, sizeof(p));
+    const int BMq = bwd_dq_block_m();
+    if ((s = make_map(&p.tm_q, a.q, BMq)) != ATTN_OK) return s;
+    if ((s = make_map(&p.tm_do, a.dout, BMq)) != ATTN_OK) return s;
+    if ((s = make_map(&p.tm_k, a.k, 128)) != ATTN_OK) return s;
+    if ((s = make_map(&p.tm_v, a.v, 128)) != ATTN_OK) return s;
+    p.lse = reinterpret_cast<const float*>(a.lse->data);
+    p.l_sb = a.lse->stride[0]; p.l_sh = a.lse->stride[1]; p.l_ss = a.lse->stride[2];
+    p.delta = delta;
+    p.dq = reinterpret_cast<uint16_t*>(a.dq->data);
+    p.dq_sb = a.dq->stride[0]; p.dq_sh = a.dq->stride[1]; p.dq_ss = a.dq->stride[2];
+    p.H = pr.H;
+    p.rows_q = pr.Sq;
+    p.seq = sa;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.sm_scale = sm_scale;
+    p.status = status;
+    p.d_out = pr.D;
+    const int n_blk = (pr.max_q + BMq - 1) / BMq;
+    // the operands every CTA of a head visits: K and V
+    p.tile_major = tile_major_order(p.causal, (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
+    const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_blk) : dim3(n_blk, pr.H, pr.units);
+    if (launch_bwd_dq(p, kernel_width(pr.D), pr.f16, grid, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
   return ATTN_OK;
 }
 
 attn_status bwd_common(const BwdArgs& a, const int32_t* cu_q, const int32_t* cu_k, int compact,
                        int32_t num_seqs, int32_t max_q, int32_t max_k, float sm_scale,
-                       int causal, void* ws, size_t ws_bytes, void* stream) {
+                       int causal, void* ws, size_t ws_bytes, void* stream,
+                       bool deterministic = false) {
   Problem pr;
   attn_status s =
       make_problem(a.q, a.k, a.v, cu_q, cu_k, compact, num_seqs, max_q, max_k, &pr);
@@ -389,6 +423,7 @@ attn_status bwd_common(const BwdArgs& a, const int32_t* cu_q, const int32_t* cu_
   }
   if ((s = check_lse(a.lse, pr)) != ATTN_OK) return s;
   if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
+  if (deterministic) return bwd_stage(1 | 2 | 8, a, pr, sm_scale, causal, ws, ws_bytes, stream, true);
   return bwd_stage(7, a, pr, sm_scale, causal, ws, ws_bytes, stream);
 }
 
@@ -404,6 +439,10 @@ size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D) {
 
 size_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D) {
   return bwd_layout(B, H, Sq, D).total;
+}
+
+size_t attn_bwd_deterministic_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D) {
+  return bwd_layout(B, H, Sq, D).dq_off;  // status word and Delta
 }
 
 attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
@@ -468,6 +507,29 @@ attn_status attn_bwd_compact_varlen(const attn_tensor4* q, const attn_tensor4* k
   BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse};
   return bwd_common(a, cu_seqlens_q, cu_seqlens_k, 1, num_seqs, max_seqlen_q, max_seqlen_k,
                     sm_scale, causal, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_deterministic(const attn_tensor4* q, const attn_tensor4* k,
+                                   const attn_tensor4* v, const attn_tensor4* o,
+                                   const attn_tensor3* lse, const attn_tensor4* dout,
+                                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                   float sm_scale, int causal, const attn_tensor4* dq,
+                                   const attn_tensor4* dk, const attn_tensor4* dv,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse};
+  return bwd_common(a, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, causal, workspace,
+                    workspace_bytes, stream, true);
+}
+
+attn_status attn_bwd_compact_varlen_deterministic(
+    const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v, const attn_tensor4* o,
+    const attn_tensor3* lse, const attn_tensor4* dout, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+    float sm_scale, int causal, const attn_tensor4* dq, const attn_tensor4* dk,
+    const attn_tensor4* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse};
+  return bwd_common(a, cu_seqlens_q, cu_seqlens_k, 1, num_seqs, max_seqlen_q, max_seqlen_k,
+                    sm_scale, causal, workspace, workspace_bytes, stream, true);
 }
 
 attn_status attn_bwd_preprocess(const attn_tensor4* o, const attn_tensor4* dout,

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant
     const int64_t idx = ((int64_t)sv.batch * p.H + h) * p.rows + grow;
     if (part == 0) p.delta[idx] = acc;
   }
-  if (valid && cols) {
+  if (valid && cols && p.dq_acc != nullptr) {
     const int64_t idx = ((int64_t)sv.batch * p.H + h) * p.rows + grow;
     float4* dst = reinterpret_cast<float4*>(p.dq_acc + idx * p.D + part * 8);
     dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -412,20 +412,22 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         for (int kk = 0; kk < BM / 16; ++kk)
           umma_ss_w(tDK, ds_kd + dso + kmajor_step(BN, kk), q_mn + qo + mnmajor_step(kk), idG,
                     (it > 0 || kk > 0));
-        if (it > 0 &&
-            !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, kWaitTimeoutNs))
-          break;
-        tc_fence_after();
+        if (p.with_dq) {
+          if (it > 0 &&
+              !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, kWaitTimeoutNs))
+            break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          if (C::DQ_T)
-            umma_ss_w(tDQ, k_mn + mnmajor_step(kk), ds_mn + dso + mnmajor_step(kk), idQ, kk > 0);
-          else
-            umma_ss_w(tDQ, ds_mn + dso + mnmajor_step(kk), k_mn + mnmajor_step(kk), idQ, kk > 0);
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            if (C::DQ_T)
+              umma_ss_w(tDQ, k_mn + mnmajor_step(kk), ds_mn + dso + mnmajor_step(kk), idQ, kk > 0);
+            else
+              umma_ss_w(tDQ, ds_mn + dso + mnmajor_step(kk), k_mn + mnmajor_step(kk), idQ, kk > 0);
+          }
         }
         umma_commit_w(smem_u32(&bars.ds_empty[bs]));
         umma_commit_w(smem_u32(&bars.q_empty[st]));
-        umma_commit_w(smem_u32(&bars.dq_full));
+        if (p.with_dq) umma_commit_w(smem_u32(&bars.dq_full));
       }
       umma_commit_w(smem_u32(&bars.dkdv_full));
     }
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         break;
       }
       uint8_t* gDS = smem + C::OFF_DS + bs * C::DS_BYTES;
-      if (!C::DQ_T && it >= 2) {
+      if (!C::DQ_T && p.with_dq && it >= 2) {
         // this warp's rows of the buffer staged dQ two steps ago: wait for that reduce
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
@@ -594,12 +596,12 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.ds_full[bs]));
       // dQ partial of the previous step (its MMA ran while this step's P/dS were formed)
-      if (it > 0 && !drain_dq(it - 1)) {
+      if (p.with_dq && it > 0 && !drain_dq(it - 1)) {
         ok = false;
         break;
       }
     }
-    if (ok && n_steps > 0) ok = drain_dq(n_steps - 1);
+    if (p.with_dq && ok && n_steps > 0) ok = drain_dq(n_steps - 1);
     if (lane == 0) bulk_wait_group0();  // this warp's reduces complete before the CTA exits
     // ---- epilogue: dK = sm_scale * acc, dV = acc; warpgroup g writes columns [g*D/2, +D/2)
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, kWaitTimeoutNs);

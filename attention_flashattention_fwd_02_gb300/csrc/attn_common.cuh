@@ -79,7 +79,7 @@ struct BwdPreParams {
   const uint16_t* dout;
   int64_t o_sb, o_sh, o_ss, do_sb, do_sh, do_ss;
   float* delta;                   // [B*H or H][rows] fp32, row index = token row
-  float* dq_acc;                  // [B*H or H][rows][D] fp32
+  float* dq_acc;                  // [B*H or H][rows][D] fp32, zeroed here; may be null
   int units, H, rows, D;          // units = B (dense/padded) or num_seqs (compact);
                                   // rows = Sq (dense/padded) or Tq (compact)
   int f16;                        // element type: 0 bf16, 1 fp16
@@ -103,6 +103,7 @@ struct BwdParams {
   SeqAddr seq;
   int causal;
   int d_out;                      // head size of the tensors (<= the kernel's D)
+  int with_dq;                    // 0: no dQ products (the deterministic dQ kernel makes dQ)
   int tile_major;                 // grid (units, H, key tiles) instead of (key tiles, H, units)
   float scale_log2;               // sm_scale * log2(e)
   float sm_scale;
@@ -117,6 +118,25 @@ struct BwdPostParams {
   int f16;                        // element type: 0 bf16, 1 fp16
   SeqAddr seq;
   float sm_scale;
+};
+
+// Deterministic dQ kernel: one CTA per 128 query rows, walking the key tiles in order.
+struct BwdDqParams {
+  CUtensorMap tm_q, tm_do;        // 4-D 16-bit maps, box (64, 128, 1, 1)
+  CUtensorMap tm_k, tm_v;         // box (64, 128, 1, 1)
+  const float* lse;
+  int64_t l_sb, l_sh, l_ss;
+  const float* delta;             // [B*H or H][rows_q] fp32
+  uint16_t* dq;
+  int64_t dq_sb, dq_sh, dq_ss;
+  int H, rows_q;
+  SeqAddr seq;
+  int causal;
+  float scale_log2;               // sm_scale * log2(e)
+  float sm_scale;
+  int* status;
+  int tile_major;                 // grid (units, H, query blocks) instead of (blocks, H, units)
+  int d_out;                      // head size of the tensors (<= the kernel's D)
 };
 
 }  // namespace attn_sm103

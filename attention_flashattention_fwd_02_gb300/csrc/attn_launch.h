@@ -18,5 +18,8 @@ int bwd_block_n();       // key rows per CTA of the main kernel
 cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, dim3 grid, cudaStream_t stream);
 cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream);
+// Deterministic dQ: grid = (query blocks, H, units); a block covers bwd_dq_block_m() rows.
+int bwd_dq_block_m();
+cudaError_t launch_bwd_dq(const BwdDqParams& p, int D, bool f16, dim3 grid, cudaStream_t stream);
 
 }  // namespace attn_sm103

@@ -135,6 +135,26 @@ attn_status attn_bwd(const attn_tensor4* q, const attn_tensor4* k, const attn_te
                      const attn_tensor4* dv, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/*
+ * Deterministic backward: same arguments and results as attn_bwd, and the same bits on every
+ * run. attn_bwd adds each key tile's dQ contribution into an fp32 accumulator with
+ * reductions whose order varies from run to run; here a second kernel owns each block of
+ * 128 query rows, walks the key tiles in order and accumulates dQ in tensor memory, while
+ * the key-tile kernel computes only dK and dV. S and dP are therefore computed twice (seven
+ * products per tile instead of five). workspace: device, >= attn_bwd_workspace_size bytes
+ * is always enough; only the status word and Delta are used (the fp32 accumulator is not),
+ * so attn_bwd_deterministic_workspace_size bytes suffice. Determinism assumes the same
+ * device, inputs and launch configuration.
+ */
+size_t attn_bwd_deterministic_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D);
+attn_status attn_bwd_deterministic(const attn_tensor4* q, const attn_tensor4* k,
+                                   const attn_tensor4* v, const attn_tensor4* o,
+                                   const attn_tensor3* lse, const attn_tensor4* dout,
+                                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                   float sm_scale, int causal, const attn_tensor4* dq,
+                                   const attn_tensor4* dk, const attn_tensor4* dv,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Compact varlen forward: q, o (1, H, Tq, D); k, v (1, H, Tk, D); lse (1, H, Tq).
  * cu_seqlens_q / cu_seqlens_k: int32 device arrays of num_seqs+1 prefix sums into the
  * token axis. max_seqlen_q / max_seqlen_k: host upper bounds on the sequence lengths, used
@@ -156,6 +176,15 @@ attn_status attn_bwd_compact_varlen(const attn_tensor4* q, const attn_tensor4* k
                                     float sm_scale, int causal, const attn_tensor4* dq,
                                     const attn_tensor4* dk, const attn_tensor4* dv,
                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Deterministic compact varlen backward; arguments as in attn_bwd_compact_varlen, results and
+ * workspace as in attn_bwd_deterministic. */
+attn_status attn_bwd_compact_varlen_deterministic(
+    const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v, const attn_tensor4* o,
+    const attn_tensor3* lse, const attn_tensor4* dout, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+    float sm_scale, int causal, const attn_tensor4* dq, const attn_tensor4* dk,
+    const attn_tensor4* dv, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Padded varlen under its own name (the AOTriton page plans "attn_?wd_padded_varlen");
  * identical to attn_fwd / attn_bwd except that cu_seqlens must be non-NULL. */
