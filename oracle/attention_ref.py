@@ -34,6 +34,12 @@ Variable-length batches follow "Add varlen support to AOTriton's Flash Attention
     on that page resets the start offsets to 0 and indexes the batch by its program id).
 Rows at or past a sequence's valid length are not outputs: the oracle returns NaN there.
 
+Additive bias (the bias argument the AOTriton varlen page reserves): an optional tensor b,
+broadcastable over batch and head, of shape [Sq, Sk] per head, enters as
+    S = c * Q K^T + b
+before the mask and the softmax (so LSE is that of the biased logits); its gradient is
+dS itself, summed over the dimensions it was broadcast along.
+
 Readings where the pages are silent (each is listed in the design notes):
   * an empty key set (Sk_valid == 0) gives O = 0, LSE = -inf and zero gradients;
   * P and dS are exact here (no bf16 rounding); the GPU tolerances cover the difference.
@@ -69,21 +75,22 @@ def _allowed(rows: np.ndarray, Sk_valid: int, Sk: int, causal: bool) -> np.ndarr
     return np.broadcast_to(ok, (len(rows), Sk))
 
 
-def attention_probs(Q, K, c, causal, Sk_valid=None):
+def attention_probs(Q, K, c, causal, Sk_valid=None, bias=None):
     """Softmax probabilities P (rows over allowed keys) and LSE for one head.
 
-    Q: [Sq, D], K: [Sk, D] float64. Returns (P [Sq, Sk], LSE [Sq]). Rows whose allowed
-    key set is empty get P = 0 and LSE = -inf.
+    Q: [Sq, D], K: [Sk, D] float64; bias: optional [Sq, Sk]. Returns (P [Sq, Sk], LSE [Sq]).
+    Rows whose allowed key set is empty (or whose biased logits are all -inf) get P = 0 and
+    LSE = -inf.
     """
     return _probs_rows(np.asarray(Q, np.float64), np.asarray(K, np.float64), c, causal,
-                       Sk_valid, 0)
+                       Sk_valid, 0, None if bias is None else np.asarray(bias, np.float64))
 
 
-def attention_forward(Q, K, V, c, causal, Sk_valid=None):
-    """O = softmax(c Q K^T, masked) V and the natural-log row logsumexp, for one head.
+def attention_forward(Q, K, V, c, causal, Sk_valid=None, bias=None):
+    """O = softmax(c Q K^T + bias, masked) V and the natural-log row logsumexp, for one head.
 
-    Q: [Sq, D], K/V: [Sk, D]. Returns (O [Sq, D], LSE [Sq]) in float64. Processed in query
-    row chunks; every chunk materialises its S and P.
+    Q: [Sq, D], K/V: [Sk, D], bias: optional [Sq, Sk]. Returns (O [Sq, D], LSE [Sq]) in
+    float64. Processed in query row chunks; every chunk materialises its S and P.
     """
     Q = np.asarray(Q, dtype=np.float64)
     K = np.asarray(K, dtype=np.float64)
@@ -93,17 +100,21 @@ def attention_forward(Q, K, V, c, causal, Sk_valid=None):
     LSE = np.zeros(Sq)
     for r0 in range(0, Sq, row_chunk):
         r1 = min(Sq, r0 + row_chunk)
-        P, lse = _probs_rows(Q[r0:r1], K, c, causal, Sk_valid, r0)
+        b = None if bias is None else np.asarray(bias[r0:r1], np.float64)
+        P, lse = _probs_rows(Q[r0:r1], K, c, causal, Sk_valid, r0, b)
         O[r0:r1] = P @ V
         LSE[r0:r1] = lse
     return O, LSE
 
 
-def _probs_rows(Qc, K, c, causal, Sk_valid, r0):
-    """attention_probs for the query rows r0 .. r0+len(Qc)-1 of a head."""
+def _probs_rows(Qc, K, c, causal, Sk_valid, r0, bias_rows=None):
+    """attention_probs for the query rows r0 .. r0+len(Qc)-1 of a head (bias_rows: the
+    matching rows of the bias, or None)."""
     Sk = K.shape[0]
     Sk_valid = Sk if Sk_valid is None else Sk_valid
     S = c * (Qc @ K.T)
+    if bias_rows is not None:
+        S = S + bias_rows
     ok = _allowed(np.arange(r0, r0 + Qc.shape[0]), Sk_valid, Sk, causal)
     Sm = np.where(ok, S, -np.inf)
     m = Sm.max(axis=1, initial=-np.inf)
@@ -123,8 +134,9 @@ def attention_delta(O, dO):
     return np.einsum("sd,sd->s", np.asarray(dO, np.float64), np.asarray(O, np.float64))
 
 
-def attention_backward(Q, K, V, dO, c, causal, Sk_valid=None):
-    """Gradients (dQ, dK, dV) of L = sum(O * dO) for one head, float64.
+def attention_backward(Q, K, V, dO, c, causal, Sk_valid=None, bias=None):
+    """Gradients (dQ, dK, dV) of L = sum(O * dO) for one head, float64; with a bias
+    [Sq, Sk], (dQ, dK, dV, dBias) where dBias = dS.
 
     P is rebuilt from the definition (not from a stored LSE); the softmax Jacobian is
     applied row by row as dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik).
@@ -137,9 +149,11 @@ def attention_backward(Q, K, V, dO, c, causal, Sk_valid=None):
     dQ = np.zeros_like(Q)
     dK = np.zeros_like(K)
     dV = np.zeros_like(V)
+    dB = None if bias is None else np.zeros((Sq, K.shape[0]))
     for r0 in range(0, Sq, row_chunk):
         r1 = min(Sq, r0 + row_chunk)
-        P, _ = _probs_rows(Q[r0:r1], K, c, causal, Sk_valid, r0)
+        b = None if bias is None else np.asarray(bias[r0:r1], np.float64)
+        P, _ = _probs_rows(Q[r0:r1], K, c, causal, Sk_valid, r0, b)
         dOc = dO[r0:r1]
         dV += P.T @ dOc
         dP = dOc @ V.T
@@ -147,6 +161,10 @@ def attention_backward(Q, K, V, dO, c, causal, Sk_valid=None):
         dS = P * (dP - rowdot)
         dQ[r0:r1] = c * (dS @ K)
         dK += c * (dS.T @ Q[r0:r1])
+        if dB is not None:
+            dB[r0:r1] = dS
+    if dB is not None:
+        return dQ, dK, dV, dB
     return dQ, dK, dV
 
 
@@ -163,13 +181,23 @@ def _as64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def fwd_bhsd(q, k, v, c, causal, cu_seqlens_q=None, cu_seqlens_k=None):
+def _bias_slice(bias, b, h, nq, nk):
+    """The [nq, nk] bias block of batch b, head h (bias [Bb, Hb, Sq, Sk], Bb in {1, B},
+    Hb in {1, H}: size-1 dimensions broadcast)."""
+    if bias is None:
+        return None
+    return bias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0, :nq, :nk]
+
+
+def fwd_bhsd(q, k, v, c, causal, cu_seqlens_q=None, cu_seqlens_k=None, bias=None):
     """Dense (cu_seqlens None) or padded-varlen forward over BHSD arrays.
 
-    q: [B, H, Sq, D], k/v: [B, H, Sk, D]. Padded varlen: batch b is valid on query rows
-    [0, cu_q[b+1]-cu_q[b]) and key rows [0, cu_k[b+1]-cu_k[b]). Returns (o, lse) with NaN
-    on rows that are not outputs.
+    q: [B, H, Sq, D], k/v: [B, H, Sk, D]; bias: optional [Bb, Hb, Sq, Sk] added to the
+    scaled scores (Bb in {1, B}, Hb in {1, H}). Padded varlen: batch b is valid on query
+    rows [0, cu_q[b+1]-cu_q[b]) and key rows [0, cu_k[b+1]-cu_k[b]), and its bias block
+    starts at offset 0 as well. Returns (o, lse) with NaN on rows that are not outputs.
     """
+    bias = None if bias is None else _as64(bias)
     q, k, v = _as64(q), _as64(k), _as64(v)
     B, H, Sq, D = q.shape
     Sk = k.shape[2]
@@ -180,15 +208,20 @@ def fwd_bhsd(q, k, v, c, causal, cu_seqlens_q=None, cu_seqlens_k=None):
     for b in range(B):
         for h in range(H):
             nq, nk = int(lq[b]), int(lk[b])
-            O, L = attention_forward(q[b, h, :nq], k[b, h, :nk], v[b, h, :nk], c, causal)
+            O, L = attention_forward(q[b, h, :nq], k[b, h, :nk], v[b, h, :nk], c, causal,
+                                     bias=_bias_slice(bias, b, h, nq, nk))
             o[b, h, :nq] = O
             lse[b, h, :nq] = L
     return o, lse
 
 
-def bwd_bhsd(q, k, v, do, c, causal, cu_seqlens_q=None, cu_seqlens_k=None):
-    """Dense or padded-varlen backward over BHSD arrays: (dq, dk, dv), NaN off-sequence."""
+def bwd_bhsd(q, k, v, do, c, causal, cu_seqlens_q=None, cu_seqlens_k=None, bias=None):
+    """Dense or padded-varlen backward over BHSD arrays: (dq, dk, dv), NaN off-sequence.
+    With a bias, (dq, dk, dv, dbias): dbias has the bias's shape, sums dS over the
+    broadcast dimensions and is 0 outside every sequence's block."""
     q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    bias = None if bias is None else _as64(bias)
+    dbias = None if bias is None else np.zeros(bias.shape)
     B, H, Sq, D = q.shape
     Sk = k.shape[2]
     lq = _lengths(cu_seqlens_q) if cu_seqlens_q is not None else np.full(B, Sq)
@@ -200,8 +233,13 @@ def bwd_bhsd(q, k, v, do, c, causal, cu_seqlens_q=None, cu_seqlens_k=None):
         for h in range(H):
             nq, nk = int(lq[b]), int(lk[b])
             g = attention_backward(q[b, h, :nq], k[b, h, :nk], v[b, h, :nk], do[b, h, :nq],
-                                   c, causal)
-            dq[b, h, :nq], dk[b, h, :nk], dv[b, h, :nk] = g
+                                   c, causal, bias=_bias_slice(bias, b, h, nq, nk))
+            dq[b, h, :nq], dk[b, h, :nk], dv[b, h, :nk] = g[:3]
+            if bias is not None:
+                dbias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0,
+                      :nq, :nk] += g[3]
+    if bias is not None:
+        return dq, dk, dv, dbias
     return dq, dk, dv
 
 
