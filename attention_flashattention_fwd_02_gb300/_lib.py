@@ -23,7 +23,7 @@ __all__ = [
     "attn_fwd_workspace_size", "attn_bwd_workspace_size",
     "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
     "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
-    "attn_bwd_deterministic_workspace_size", "EXPORTED_SYMBOLS",
+    "attn_bwd_deterministic_workspace_size", "attn_fwd_bias", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "attn_bwd_padded_varlen", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_dq_epilogue",
     "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
     "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
-    "attn_bwd_deterministic_workspace_size",
+    "attn_bwd_deterministic_workspace_size", "attn_fwd_bias",
 )
 
 
@@ -72,6 +72,7 @@ _SIGS = {
     "attn_bwd_deterministic_workspace_size": (SZ, [ctypes.c_int64] * 4),
     "attn_fwd": (INT, [P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
     "attn_fwd_padded_varlen": (INT, [P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
+    "attn_fwd_bias": (INT, [P4, P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
     "attn_fwd_compact_varlen": (INT, [P4, P4, P4, I32P, I32P, I32, I32, I32, F32, INT, P4, P3,
                                       VP, SZ, VP]),
     "attn_bwd": (INT, [P4, P4, P4, P4, P3, P4, I32P, I32P, F32, INT, P4, P4, P4, VP, SZ, VP]),
@@ -206,6 +207,22 @@ def attn_fwd_padded_varlen(q, k, v, o, lse, sm_scale, causal, cu_seqlens_q, cu_s
                            workspace=None, stream=None):
     attn_fwd(q, k, v, o, lse, sm_scale, causal, cu_seqlens_q, cu_seqlens_k, workspace, stream,
              _name="attn_fwd_padded_varlen")
+
+
+def attn_fwd_bias(q, k, v, bias, o, lse, sm_scale, causal, workspace=None, cu_seqlens_q=None,
+                  cu_seqlens_k=None, stream=None):
+    """attn_fwd with an additive bias (Bb, Hb, Sq, Sk); bias None is plain attn_fwd."""
+    _check16(q, k, v, o)
+    tb = None
+    if bias is not None:
+        _check16(bias)
+        tb = _t4(bias)
+    tq, tk, tv, to, tl = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse)
+    ws, nws = _ws(workspace)
+    _check(load().attn_fwd_bias(
+        *_keep(tq, tk, tv, tb), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_k), float(sm_scale), int(bool(causal)), *_keep(to, tl), ws, nws,
+        _stream(stream)), "attn_fwd_bias")
 
 
 def attn_fwd_compact_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs,

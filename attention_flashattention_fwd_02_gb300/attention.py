@@ -23,11 +23,18 @@ def _lse_like(q: torch.Tensor) -> torch.Tensor:
 
 def forward(q, k, v, sm_scale: Optional[float] = None, causal: bool = False,
             cu_seqlens_q=None, cu_seqlens_k=None, compact: bool = False, max_seqlen_q: int = 0,
-            max_seqlen_k: int = 0, out=None, lse=None, workspace=None, stream=None):
+            max_seqlen_k: int = 0, out=None, lse=None, workspace=None, stream=None, bias=None):
+    """bias: optional additive bias (Bb, Hb, Sq, Sk), Bb in {1, B}, Hb in {1, H}, its Sq
+    stride a multiple of 8 elements (dense and padded forms)."""
     sm_scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else sm_scale
     o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if out is None else out
     lse = _lse_like(q) if lse is None else lse
-    if compact:
+    if bias is not None:
+        if compact:
+            raise ValueError("an additive bias is supported for dense and padded inputs only")
+        _lib.attn_fwd_bias(q, k, v, bias, o, lse, sm_scale, causal, workspace, cu_seqlens_q,
+                           cu_seqlens_k, stream)
+    elif compact:
         _lib.attn_fwd_compact_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k,
                                      cu_seqlens_q.numel() - 1, max_seqlen_q, max_seqlen_k,
                                      sm_scale, causal, workspace, stream)

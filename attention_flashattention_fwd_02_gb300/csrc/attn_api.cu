@@ -237,10 +237,20 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
                        const int32_t* cu_q, const int32_t* cu_k, int compact, int32_t num_seqs,
                        int32_t max_q, int32_t max_k, float sm_scale, int causal,
                        const attn_tensor4* o, const attn_tensor3* lse, void* ws, size_t ws_bytes,
-                       void* stream) {
+                       void* stream, const attn_tensor4* bias = nullptr) {
   Problem pr;
   attn_status s = make_problem(q, k, v, cu_q, cu_k, compact, num_seqs, max_q, max_k, &pr);
   if (s != ATTN_OK) return s;
+  if (bias != nullptr) {
+    // (Bb, Hb, Sq, Sk), Bb in {1, B}, Hb in {1, H}; dense or padded forms only
+    if (compact) return ATTN_ERR_UNSUPPORTED;
+    if ((s = check_tensor4(bias)) != ATTN_OK) return s;
+    if (!same_dtype(q, bias)) return ATTN_ERR_DTYPE;
+    if (bias->size[2] != q->size[2] || bias->size[3] != k->size[2] ||
+        (bias->size[0] != 1 && bias->size[0] != q->size[0]) ||
+        (bias->size[1] != 1 && bias->size[1] != q->size[1]))
+      return ATTN_ERR_SHAPE;
+  }
   if ((s = check_tensor4(o)) != ATTN_OK) return s;
   if (!same_shape(q, o)) return ATTN_ERR_SHAPE;
   if (!same_dtype(q, o)) return ATTN_ERR_DTYPE;
@@ -258,6 +268,11 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   if ((s = make_map(&p.tm_q, q, fwd_box_rows())) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_k, k, 128)) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_v, v, 128)) != ATTN_OK) return s;
+  if (bias != nullptr) {
+    if ((s = make_map(&p.tm_b, bias, 128)) != ATTN_OK) return s;
+    p.bias_b_bcast = bias->size[0] == 1 && pr.B > 1;
+    p.bias_h_bcast = bias->size[1] == 1 && pr.H > 1;
+  }
   p.o = reinterpret_cast<uint16_t*>(o->data);
   p.o_sb = o->stride[0];
   p.o_sh = o->stride[1];
@@ -276,7 +291,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   p.tile_major = tile_major_order(p.causal, (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
   const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_blk) : dim3(n_blk, pr.H, pr.units);
   p.d_out = pr.D;
-  cudaError_t e = launch_attn_fwd(p, kernel_width(pr.D), pr.f16, grid,
+  cudaError_t e = launch_attn_fwd(p, kernel_width(pr.D), pr.f16, bias != nullptr, grid,
                                   reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -451,6 +466,15 @@ attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_te
                      void* workspace, size_t workspace_bytes, void* stream) {
   return fwd_common(q, k, v, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, causal, o, lse,
                     workspace, workspace_bytes, stream);
+}
+
+attn_status attn_fwd_bias(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                          const attn_tensor4* bias, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_k, float sm_scale, int causal,
+                          const attn_tensor4* o, const attn_tensor3* lse, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  return fwd_common(q, k, v, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, causal, o, lse,
+                    workspace, workspace_bytes, stream, bias);
 }
 
 attn_status attn_fwd_padded_varlen(const attn_tensor4* q, const attn_tensor4* k,

@@ -44,16 +44,23 @@
 
 namespace attn_sm103 {
 
-template <int D>
+// BIAS: the additive bias tile of each score tile (128 query rows x 128 keys, 16-bit) is
+// staged in shared memory in NBS slots, filled in score-tile order (slot k mod NBS) and
+// refilled once the softmax warps that read it are done: two slots at d_head 64, one at
+// d_head 128, where shared memory holds no more.
+template <int D, bool BIAS = false>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128, NQ = 2;  // two query tiles per CTA
   static constexpr int NST = (D == 128) ? 2 : 4;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int NBS = BIAS ? ((D == 128) ? 1 : 2) : 0;
+  static constexpr int B_BYTES = BM * BN * 2;  // one bias slot
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = NQ * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
-  static constexpr int SMEM_BYTES = OFF_V + NST * KV_BYTES + 1024;  // + alignment slack
+  static constexpr int OFF_B = OFF_V + NST * KV_BYTES;
+  static constexpr int SMEM_BYTES = OFF_B + NBS * B_BYTES + 1024;  // + alignment slack
   static constexpr int NSB = (D == 64) ? 3 : 2;  // rotating score / P buffers
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O0 = NSB * 128, COL_O1 = NSB * 128 + D;
@@ -68,6 +75,7 @@ struct FwdBars {
   uint64_t q_full;
   uint64_t k_full[NST], v_full[NST], kv_empty[NST];
   uint64_t s_full[NSB], p_full[NSB], buf_free[NSB], o_done[2];
+  uint64_t b_full[2], b_empty[2];  // bias slots (NBS of them used)
   uint32_t tmem_base;
   int abort;
 };
@@ -97,9 +105,9 @@ __device__ __forceinline__ int key_tiles(int q_lo, int q_hi, int len_k, int caus
   return n;
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool BIAS>
 __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, BIAS>;
   constexpr int BM = C::BM, BN = C::BN, NST = C::NST, NSB = C::NSB;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdBars<NST, NSB> bars;
@@ -159,7 +167,11 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
       mbar_init(smem_u32(&bars.p_full[b]), 128);
       mbar_init(smem_u32(&bars.buf_free[b]), 1);
     }
-    for (int t = 0; t < 2; ++t) mbar_init(smem_u32(&bars.o_done[t]), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bars.o_done[t]), 1);
+      mbar_init(smem_u32(&bars.b_full[t]), 1);
+      mbar_init(smem_u32(&bars.b_empty[t]), 128);
+    }
     mbar_fence_init();
   }
   if (warp == C::WARP_MMA) {
@@ -174,6 +186,26 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
 
   if (warp == C::WARP_PRODUCER) {
     // ------------------------------------------------------------------ TMA producer
+    if (BIAS && lane == 1) {
+      // bias tiles in score-tile order: slot k mod NBS, refilled once the softmax warps that
+      // read its previous tile are done (they wait on nothing this lane does afterwards)
+      constexpr int NBS = C::NBS > 0 ? C::NBS : 1;
+      tma_prefetch_map(&p.tm_b);
+      const uint32_t sB = smem_u32(smem + C::OFF_B);
+      const int hb = p.bias_h_bcast ? 0 : h, bb = p.bias_b_bcast ? 0 : sv.batch;
+      for (int k = 0; k < order.total; ++k) {
+        const int t = order.t_of(k), j = order.j_of(k), slot = k % NBS;
+        if (k >= NBS && !mbar_wait(smem_u32(&bars.b_empty[slot]), ((k / NBS) - 1) & 1, abort,
+                                   p.timeout_ns))
+          break;
+        const uint32_t bf = smem_u32(&bars.b_full[slot]);
+        mbar_arrive_expect_tx(bf, C::B_BYTES);
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          tma_load_4d(sB + slot * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
+                      sv.row0_q + q_lo[t], hb, bb);
+      }
+    }
     if (lane == 0) {
       tma_prefetch_map(&p.tm_q);
       tma_prefetch_map(&p.tm_k);
@@ -312,6 +344,35 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
       ATTN_TMEM_LD4_X32(tSt, tSt + 32, tSt + 64, tSt + 96, reinterpret_cast<uint32_t*>(s),
                         reinterpret_cast<uint32_t*>(s + 32), reinterpret_cast<uint32_t*>(s + 64),
                         reinterpret_cast<uint32_t*>(s + 96));
+      if constexpr (BIAS) {
+        // s <- s c2 + bias log2(e): the scores in base-2 units, bias included
+        constexpr int NBS = C::NBS > 0 ? C::NBS : 1;
+        const int slot = k % NBS;
+        if (!mbar_wait(smem_u32(&bars.b_full[slot]), (k / NBS) & 1, abort, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* brow = smem + C::OFF_B + slot * C::B_BYTES + r * 128;
+        const uint64_t c2x2b = f2_pack(c2, c2), l2e = f2_pack(1.4426950408889634f, 1.4426950408889634f);
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 w = *reinterpret_cast<const uint4*>(brow + sl * BM * 128 +
+                                                            16 * (ch ^ (r & 7)));
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = sl * 64 + ch * 8 + 2 * e;
+              const float2 bv = unpack2<F16>(wv[e]);
+              f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), c2x2b, f2_mul(f2_pack(bv.x, bv.y), l2e)),
+                        s[c], s[c + 1]);
+            }
+          }
+        mbar_arrive(smem_u32(&bars.b_empty[slot]));
+      }
+      // with a bias the scores are already scaled
+      const float cs = BIAS ? 1.f : c2;
       const int k0 = j * BN;
       if (k0 + BN > sv.len_k || (p.causal && k0 + BN - 1 > q_lo[t])) {
         const int kmax = p.causal ? min(row, sv.len_k - 1) : sv.len_k - 1;
@@ -331,7 +392,7 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
       }
       mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
       mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
-      const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
+      const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs;
       float m_new = m_use, scale = 1.f;
       if (mxs > m_use + 8.f) {
         m_new = mxs;
@@ -339,7 +400,7 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
       }
       const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
       // p = 2^(s c2 - m): scale-and-shift and the row sum run on paired fp32 instructions
-      const uint64_t c2x2 = f2_pack(c2, c2), negm2 = f2_pack(neg_m, neg_m);
+      const uint64_t c2x2 = f2_pack(cs, cs), negm2 = f2_pack(neg_m, neg_m);
       uint64_t rs0 = 0, rs1 = 0;  // two pairs of partial sums (0.0f bit pattern is 0)
       uint32_t pk[BN / 2];
 #pragma unroll
@@ -434,26 +495,36 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
   if (threadIdx.x == 0 && bars.abort && p.status != nullptr) atomicCAS(p.status, 0, kStatusTimeout);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool BIAS>
 static cudaError_t launch_fwd_impl(const FwdParams& p, dim3 grid, cudaStream_t stream) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, BIAS>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F16>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F16, BIAS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  attn_fwd_kernel<D, F16><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
+  attn_fwd_kernel<D, F16, BIAS><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, dim3 grid, cudaStream_t stream) {
+template <bool BIAS>
+static cudaError_t launch_fwd_dispatch(const FwdParams& p, int D, bool f16, dim3 grid,
+                                       cudaStream_t stream) {
   if (D == 128)
-    return f16 ? launch_fwd_impl<128, true>(p, grid, stream) : launch_fwd_impl<128, false>(p, grid, stream);
-  return f16 ? launch_fwd_impl<64, true>(p, grid, stream) : launch_fwd_impl<64, false>(p, grid, stream);
+    return f16 ? launch_fwd_impl<128, true, BIAS>(p, grid, stream)
+               : launch_fwd_impl<128, false, BIAS>(p, grid, stream);
+  return f16 ? launch_fwd_impl<64, true, BIAS>(p, grid, stream)
+             : launch_fwd_impl<64, false, BIAS>(p, grid, stream);
+}
+
+cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3 grid,
+                            cudaStream_t stream) {
+  return bias ? launch_fwd_dispatch<true>(p, D, f16, grid, stream)
+              : launch_fwd_dispatch<false>(p, D, f16, grid, stream);
 }
 
 // Query rows per CTA (two 128-row tiles). The 4-D Q tensor map uses a 128-row box.

@@ -10,7 +10,8 @@ namespace attn_sm103 {
 // loaded with a Q tensor map whose box has fwd_box_rows() rows.
 int fwd_block_m();
 int fwd_box_rows();
-cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, dim3 grid, cudaStream_t stream);
+cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3 grid,
+                            cudaStream_t stream);
 
 // Backward stages.
 int bwd_block_m(int D);  // query rows per inner step of the main kernel

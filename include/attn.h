@@ -121,6 +121,26 @@ attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_te
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Forward pass with an additive attention bias (the bias argument that the AOTriton varlen
+ * page reserves): S = sm_scale * Q K^T + bias, then mask and softmax; lse is that of the
+ * biased scores. Arguments as in attn_fwd (dense, or padded varlen with cu_seqlens), plus
+ *   bias: (Bb, Hb, Sq, Sk) in q's element type, Bb in {1, B} and Hb in {1, H} (size 1
+ *         broadcasts; pass size-1 dimensions, not zero strides). D stride 1; the Sq stride
+ *         (and the other strides) a multiple of 8 elements, so a row of Sk keys is padded to
+ *         a multiple of 8 elements when Sk is not; 16-byte aligned base. Padded varlen uses
+ *         the block at offset 0 of each batch, like q. Compact varlen is not offered
+ *         (ATTN_ERR_UNSUPPORTED through this call with num_seqs semantics does not exist).
+ * A NULL bias is the same as attn_fwd. Errors as attn_fwd; ATTN_ERR_SHAPE for a bias whose
+ * sizes do not fit. No gradient for the bias is computed by this library (attn_bwd and the
+ * other backward calls take no bias).
+ */
+attn_status attn_fwd_bias(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                          const attn_tensor4* bias, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_k, float sm_scale, int causal,
+                          const attn_tensor4* o, const attn_tensor3* lse, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
  * Backward pass matching attn_fwd (same q, k, v, cu_seqlens, sm_scale, causal; o and lse
  * as returned by attn_fwd). dout: (B, H, Sq, D). Writes dq (B, H, Sq, D), dk and dv
  * (B, H, Sk, D), all in q's element type. workspace: device, >= attn_bwd_workspace_size

@@ -185,3 +185,31 @@ def test_dtype_checks(lib):
     for t in (q, k, v, o):
         t.dtype = 7
     assert call_fwd(lib, q, k, v, o, lse) == ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("bshape,expect", [
+    ((1, 2, 128, 72), ERR_SHAPE),     # Sk does not match k
+    ((1, 2, 64, 128), ERR_SHAPE),     # Sq does not match q
+    ((1, 3, 128, 128), ERR_SHAPE),    # head count neither 1 nor H
+    ((2, 2, 128, 128), ERR_SHAPE),    # batch neither 1 nor B
+])
+def test_bias_validation(lib, bshape, expect):
+    """attn_fwd_bias checks the bias (Bb, Hb, Sq, Sk) before touching the device."""
+    q, k, v, o, lse = good()
+    bias = t4(bshape)
+    r = ctypes.byref
+    got = lib.attn_fwd_bias(r(q), r(k), r(v), r(bias), None, None, 0.125, 0, r(o), r(lse),
+                            None, 0, None)
+    assert got == expect
+
+
+def test_bias_stride_and_dtype_checks(lib):
+    q, k, v, o, lse = good()
+    r = ctypes.byref
+    bias = t4((1, 1, 128, 128), stride=[128 * 130, 128 * 130, 130, 1])  # row stride 130
+    assert lib.attn_fwd_bias(r(q), r(k), r(v), r(bias), None, None, 0.125, 0, r(o), r(lse),
+                             None, 0, None) == ERR_STRIDE
+    bias = t4((1, 1, 128, 128))
+    bias.dtype = 1  # fp16 bias with bf16 q
+    assert lib.attn_fwd_bias(r(q), r(k), r(v), r(bias), None, None, 0.125, 0, r(o), r(lse),
+                             None, 0, None) == 10  # ATTN_ERR_DTYPE

@@ -1,0 +1,86 @@
+"""GPU parity of the forward pass with an additive bias (attn_fwd_bias) against the
+float64 oracle: full and broadcast biases, causal and not, padded varlen, transposed K/V
+views, fp16, d_head 64 / 96 / 128, and -inf entries (a key mask written into the bias).
+Rows that are not outputs keep their NaN sentinels."""
+import pytest
+import torch
+
+from oracle import attention_ref as ref
+from attention_flashattention_fwd_02_gb300 import _lib
+from attention_flashattention_fwd_02_gb300.attention import forward
+from attention_flashattention_fwd_02_gb300.workloads import WORKLOADS, make_inputs
+
+from _helpers import assert_fwd_close, np64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+CASES = [
+    # (layout, D, causal, bias batch, bias heads, dtype, with -inf keys)
+    ("bhsd", 64, True, "B", "H", torch.bfloat16, False),
+    ("bhsd", 64, False, 1, "H", torch.bfloat16, False),
+    ("bhsd", 128, True, "B", 1, torch.bfloat16, False),
+    ("bhsd", 128, False, 1, 1, torch.float16, False),
+    ("kv_bshd", 128, False, "B", "H", torch.bfloat16, False),
+    ("padded", 64, True, "B", "H", torch.bfloat16, False),
+    ("padded", 128, False, "B", 1, torch.bfloat16, False),
+    ("bhsd", 96, True, 1, "H", torch.bfloat16, False),
+    ("bhsd", 64, False, "B", "H", torch.bfloat16, True),
+]
+
+
+def _bias(x, wl, bb, bh, dtype, neg_inf, seed):
+    """Seeded N(0, 1) bias rounded to the element type; rows padded to a multiple of 8
+    keys (the Sq stride must be), passed as a view of the first Sk columns."""
+    B = wl.B if bb == "B" else 1
+    H = wl.H if bh == "H" else 1
+    Sq, Sk = x["q"].shape[2], x["k"].shape[2]
+    pad = (Sk + 7) // 8 * 8
+    g = torch.Generator().manual_seed(seed)
+    full = torch.randn(B, H, Sq, pad, generator=g).to(dtype)
+    if neg_inf:  # every fifth key hidden from every query (not key 0, so no row is empty)
+        full[..., 5::5] = float("-inf")
+    return full, Sk
+
+
+@pytest.mark.parametrize("layout,D,causal,bb,bh,dtype,neg_inf", CASES)
+def test_bias_forward_parity(layout, D, causal, bb, bh, dtype, neg_inf):
+    padded = layout == "padded"
+    base = WORKLOADS["padded" if padded else "cross"]
+    wl = base.replace(B=2, H=2, Sq=300, Sk=300 if layout != "kv_bshd" else 410, D=D,
+                      causal=causal, layout=layout, seed=91 + D)
+    x = make_inputs(wl, lengths=[300, 123] if padded else None, dtype=dtype)
+    full, Sk = _bias(x, wl, bb, bh, dtype, neg_inf, seed=97 + D)
+    bias = full[..., :Sk]
+    bias_dev = full.to(DEV)[..., :Sk]  # keeps the padded row stride
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    cu_q = g["cu_seqlens_q"] if padded else None
+    cu_k = g["cu_seqlens_k"] if padded else None
+    o = torch.full_like(g["q"], float("nan"))
+    lse = torch.full(g["q"].shape[:3], float("nan"), device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    forward(g["q"], g["k"], g["v"], wl.sm_scale, causal, cu_q, cu_k, out=o, lse=lse,
+            workspace=ws, bias=bias_dev)
+    torch.cuda.synchronize()
+    assert _lib.attn_read_device_status(ws) == 0
+    qn, kn, vn = (np64(x[n]) for n in ("q", "k", "v"))
+    o_r, lse_r = ref.fwd_bhsd(qn, kn, vn, wl.sm_scale, causal,
+                              x["cu_seqlens_q"].numpy() if padded else None,
+                              x["cu_seqlens_k"].numpy() if padded else None, bias=np64(bias))
+    assert_fwd_close(o, lse, o_r, lse_r, what=f"bias {layout} D={D}")
+    if padded:
+        for b, n in enumerate([300, 123]):
+            assert torch.isnan(o[b, :, n:]).all() and torch.isnan(lse[b, :, n:]).all()
+
+
+def test_zero_bias_equals_no_bias():
+    wl = WORKLOADS["cross"].replace(B=1, H=2, Sq=256, Sk=384, D=64, causal=True,
+                                    layout="bhsd", seed=5)
+    x = make_inputs(wl)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    o0, l0 = forward(q, k, v, wl.sm_scale, True)
+    zb = torch.zeros(1, 1, 256, 384, dtype=q.dtype, device=DEV)
+    o1, l1 = forward(q, k, v, wl.sm_scale, True, bias=zb)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(o1, o0, atol=2e-3, rtol=0)
+    torch.testing.assert_close(l1, l0, atol=1e-5, rtol=0)
