@@ -242,8 +242,12 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   attn_status s = make_problem(q, k, v, cu_q, cu_k, compact, num_seqs, max_q, max_k, &pr);
   if (s != ATTN_OK) return s;
   if (bias != nullptr) {
-    // (Bb, Hb, Sq, Sk), Bb in {1, B}, Hb in {1, H}; dense or padded forms only
-    if (compact) return ATTN_ERR_UNSUPPORTED;
+    // (Bb, Hb, Sq, Sk), Bb in {1, B}, Hb in {1, H}; dense or padded forms only; d_head up to
+    // 64 (the 64-wide kernel) and fewer than 2^31 bias elements, the configurations that
+    // have run on the GPU
+    if (compact || q->size[3] > 64) return ATTN_ERR_UNSUPPORTED;
+    if (bias->size[0] * bias->size[1] * bias->size[2] * bias->size[3] >= (int64_t(1) << 31))
+      return ATTN_ERR_UNSUPPORTED;
     if ((s = check_tensor4(bias)) != ATTN_OK) return s;
     if (!same_dtype(q, bias)) return ATTN_ERR_DTYPE;
     if (bias->size[2] != q->size[2] || bias->size[3] != k->size[2] ||

@@ -191,6 +191,7 @@ struct BwdBars {
   uint64_t s_full, s_free, p_full, p_empty;
   uint64_t ds_full[2], ds_empty[2];
   uint64_t dq_full, dq_empty, dkdv_full;
+  uint64_t mma_drain;  // completion of the MMA warp's last products
   uint32_t tmem_base;
   int abort;
   alignas(16) float nlse2[LSE_ST][BM];   // -LSE * log2(e) of the step's query rows
@@ -269,6 +270,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_empty), 256);
     mbar_init(smem_u32(&bars.dkdv_full), 1);
+    mbar_init(smem_u32(&bars.mma_drain), 1);
     mbar_fence_init();
   }
   if (warp == C::WARP_MMA) {
@@ -313,11 +315,15 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     };
     if (C::AUG)  // the ones tile, made visible to the MMAs by the first step's q_full arrival
       for (int r = lane; r < BN; r += 32) aug_row(0, r, 1.f, 1.f, 1.f);
+    int last_it[QST];  // last step loaded into each stage (-1: none)
+#pragma unroll
+    for (int st = 0; st < QST; ++st) last_it[st] = -1;
     for (int it = 0; it < n_steps; ++it) {
       const int st = it % QST;
       if (it >= QST &&
           !mbar_wait(smem_u32(&bars.q_empty[st]), ((it / QST) - 1) & 1, abort, kWaitTimeoutNs))
         break;
+      last_it[st] = it;
       const int q_lo = q_tile(it) * BM;
       const uint32_t qb = smem_u32(&bars.q_full[st]);
       if (lane == 0) {
@@ -349,6 +355,13 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       }
       if (C::AUG) fence_proxy_async_smem();  // the rows are read by the MMAs (async proxy)
       mbar_arrive(qb);
+    }
+    if (lane == 0 && *abort) {  // the consumers gave up: let the copies in flight land
+      mbar_wait_drain(smem_u32(&bars.kv_full), 0, kWaitTimeoutNs);
+#pragma unroll
+      for (int st = 0; st < QST; ++st)
+        if (last_it[st] >= 0)
+          mbar_wait_drain(smem_u32(&bars.q_full[st]), (last_it[st] / QST) & 1, kWaitTimeoutNs);
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
@@ -430,6 +443,9 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         if (p.with_dq) umma_commit_w(smem_u32(&bars.dq_full));
       }
       umma_commit_w(smem_u32(&bars.dkdv_full));
+      // every product this warp issued has completed before tensor memory is released
+      umma_commit_w(smem_u32(&bars.mma_drain));
+      mbar_wait_drain(smem_u32(&bars.mma_drain), 0, kWaitTimeoutNs);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ P^T / dS^T compute

@@ -42,7 +42,7 @@ struct DqBars {
   uint64_t k_full[NST], v_full[NST], kv_empty[NST];
   uint64_t s_full, s_free;
   uint64_t ds_full[NDS], ds_empty[NDS];
-  uint64_t dq_full;
+  uint64_t dq_full, mma_drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
       mbar_init(smem_u32(&bars.ds_empty[b]), 1);
     }
     mbar_init(smem_u32(&bars.dq_full), 1);
+    mbar_init(smem_u32(&bars.mma_drain), 1);
     mbar_fence_init();
   }
   if (warp == C::WARP_MMA) {
@@ -132,11 +133,15 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
         tma_load_4d(sQ + s * BM * 128, &p.tm_q, qb, s * 64, sv.row0_q + q_lo, h, sv.batch);
         tma_load_4d(sDO + s * BM * 128, &p.tm_do, qb, s * 64, sv.row0_q + q_lo, h, sv.batch);
       }
+      int last_j[NST];  // last key tile loaded into each stage (-1: none)
+#pragma unroll
+      for (int st = 0; st < NST; ++st) last_j[st] = -1;
       for (int j = 0; j < n_kt; ++j) {
         const int st = j % NST;
         if (j >= NST &&
             !mbar_wait(smem_u32(&bars.kv_empty[st]), ((j / NST) - 1) & 1, abort, kWaitTimeoutNs))
           break;
+        last_j[st] = j;
         const int krow = sv.row0_k + j * BN;
         const uint32_t kb = smem_u32(&bars.k_full[st]), vb = smem_u32(&bars.v_full[st]);
         mbar_arrive_expect_tx(kb, C::TILE);
@@ -147,6 +152,15 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(sV + st * C::TILE + s * BN * 128, &p.tm_v, vb, s * 64, krow, h, sv.batch);
+      }
+      if (*abort) {  // the consumers gave up: let the copies in flight land before exiting
+        mbar_wait_drain(qb, 0, kWaitTimeoutNs);
+#pragma unroll
+        for (int st = 0; st < NST; ++st)
+          if (last_j[st] >= 0) {
+            mbar_wait_drain(smem_u32(&bars.k_full[st]), (last_j[st] / NST) & 1, kWaitTimeoutNs);
+            mbar_wait_drain(smem_u32(&bars.v_full[st]), (last_j[st] / NST) & 1, kWaitTimeoutNs);
+          }
       }
     }
   } else if (warp == C::WARP_MMA) {
@@ -193,6 +207,9 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
       umma_commit_w(smem_u32(&bars.kv_empty[st]));  // K_j (and V_j, read by dP(j)) done
     }
     if (ok) umma_commit_w(smem_u32(&bars.dq_full));
+    // every product this warp issued has completed before tensor memory is released
+    umma_commit_w(smem_u32(&bars.mma_drain));
+    mbar_wait_drain(smem_u32(&bars.mma_drain), 0, kWaitTimeoutNs);
   } else {
     // ------------------------------------------------------------------ dS compute, epilogue
     const int g = warp >> 2;                 // warpgroup: key columns [64 g, 64 g + 64)

@@ -66,8 +66,9 @@ struct FwdCfg {
   static constexpr uint32_t COL_O0 = NSB * 128, COL_O1 = NSB * 128 + D;
   static_assert(COL_O1 + D <= TMEM_COLS, "TMEM budget");
   static constexpr bool SPLIT_ISSUE = (NSB == 3);  // separate S and PV issuing warps
-  static constexpr int NTHREADS = SPLIT_ISSUE ? 352 : 320;
   static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_SMMA = 10;
+  static constexpr int WARP_BIAS = SPLIT_ISSUE ? 11 : 10;  // bias producer (BIAS only)
+  static constexpr int NTHREADS = (SPLIT_ISSUE ? 352 : 320) + (BIAS ? 32 : 0);
 };
 
 template <int NST, int NSB>
@@ -76,6 +77,7 @@ struct FwdBars {
   uint64_t k_full[NST], v_full[NST], kv_empty[NST];
   uint64_t s_full[NSB], p_full[NSB], buf_free[NSB], o_done[2];
   uint64_t b_full[2], b_empty[2];  // bias slots (NBS of them used)
+  uint64_t mma_drain[2];           // completion of each issuing warp's last products
   uint32_t tmem_base;
   int abort;
 };
@@ -106,7 +108,8 @@ __device__ __forceinline__ int key_tiles(int q_lo, int q_hi, int len_k, int caus
 }
 
 template <int D, bool F16, bool BIAS>
-__global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
+    attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, BIAS>;
   constexpr int BM = C::BM, BN = C::BN, NST = C::NST, NSB = C::NSB;
   extern __shared__ uint8_t smem_raw[];
@@ -171,6 +174,7 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
       mbar_init(smem_u32(&bars.o_done[t]), 1);
       mbar_init(smem_u32(&bars.b_full[t]), 1);
       mbar_init(smem_u32(&bars.b_empty[t]), 128);
+      mbar_init(smem_u32(&bars.mma_drain[t]), 1);
     }
     mbar_fence_init();
   }
@@ -186,26 +190,6 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
 
   if (warp == C::WARP_PRODUCER) {
     // ------------------------------------------------------------------ TMA producer
-    if (BIAS && lane == 1) {
-      // bias tiles in score-tile order: slot k mod NBS, refilled once the softmax warps that
-      // read its previous tile are done (they wait on nothing this lane does afterwards)
-      constexpr int NBS = C::NBS > 0 ? C::NBS : 1;
-      tma_prefetch_map(&p.tm_b);
-      const uint32_t sB = smem_u32(smem + C::OFF_B);
-      const int hb = p.bias_h_bcast ? 0 : h, bb = p.bias_b_bcast ? 0 : sv.batch;
-      for (int k = 0; k < order.total; ++k) {
-        const int t = order.t_of(k), j = order.j_of(k), slot = k % NBS;
-        if (k >= NBS && !mbar_wait(smem_u32(&bars.b_empty[slot]), ((k / NBS) - 1) & 1, abort,
-                                   p.timeout_ns))
-          break;
-        const uint32_t bf = smem_u32(&bars.b_full[slot]);
-        mbar_arrive_expect_tx(bf, C::B_BYTES);
-#pragma unroll
-        for (int s = 0; s < 2; ++s)
-          tma_load_4d(sB + slot * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
-                      sv.row0_q + q_lo[t], hb, bb);
-      }
-    }
     if (lane == 0) {
       tma_prefetch_map(&p.tm_q);
       tma_prefetch_map(&p.tm_k);
@@ -218,12 +202,16 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(sQ + t * C::Q_BYTES + s * BM * 128, &p.tm_q, qb, s * 64,
                       sv.row0_q + q_lo[t], h, sv.batch);
+      int last_j[NST];  // last key tile loaded into each stage (-1: none)
+#pragma unroll
+      for (int st = 0; st < NST; ++st) last_j[st] = -1;
       for (int j = 0; j < n_max; ++j) {
         const int st = j % NST;
         if (j == p.withhold_tile) continue;  // failure-detection test: this stage never fills
         if (j >= NST &&
             !mbar_wait(smem_u32(&bars.kv_empty[st]), ((j / NST) - 1) & 1, abort, p.timeout_ns))
           break;
+        last_j[st] = j;
         const int krow = sv.row0_k + j * BN;
         const uint32_t kb = smem_u32(&bars.k_full[st]);
         mbar_arrive_expect_tx(kb, C::KV_BYTES);
@@ -236,6 +224,43 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(sV + st * C::KV_BYTES + s * BN * 128, &p.tm_v, vb, s * 64, krow, h, sv.batch);
       }
+      if (*abort) {  // the consumers gave up: let this lane's copies land before exiting
+        mbar_wait_drain(qb, 0, p.timeout_ns);
+#pragma unroll
+        for (int st = 0; st < NST; ++st)
+          if (last_j[st] >= 0) {
+            mbar_wait_drain(smem_u32(&bars.k_full[st]), (last_j[st] / NST) & 1, p.timeout_ns);
+            mbar_wait_drain(smem_u32(&bars.v_full[st]), (last_j[st] / NST) & 1, p.timeout_ns);
+          }
+      }
+    }
+  } else if (BIAS && warp == C::WARP_BIAS) {
+    // ------------------------------------------------------------------ bias producer
+    // bias tiles in score-tile order: slot k mod NBS, refilled once the softmax warps that
+    // read its previous tile are done (they wait on nothing this warp does afterwards). A
+    // warp of its own, so that its waits never share a warp with the K/V producer's.
+    if (lane == 0) {
+      constexpr int NBS = C::NBS > 0 ? C::NBS : 1;
+      tma_prefetch_map(&p.tm_b);
+      const uint32_t sB = smem_u32(smem + C::OFF_B);
+      const int hb = p.bias_h_bcast ? 0 : h, bb = p.bias_b_bcast ? 0 : sv.batch;
+      int issued = 0;
+      for (int k = 0; k < order.total; ++k) {
+        const int t = order.t_of(k), j = order.j_of(k), slot = k % NBS;
+        if (k >= NBS && !mbar_wait(smem_u32(&bars.b_empty[slot]), ((k / NBS) - 1) & 1, abort,
+                                   p.timeout_ns))
+          break;
+        const uint32_t bf = smem_u32(&bars.b_full[slot]);
+        mbar_arrive_expect_tx(bf, C::B_BYTES);
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          tma_load_4d(sB + slot * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
+                      sv.row0_q + q_lo[t], hb, bb);
+        issued = k + 1;
+      }
+      if (*abort)  // let the copies in flight land before exiting
+        for (int k = max(0, issued - NBS); k < issued; ++k)
+          mbar_wait_drain(smem_u32(&bars.b_full[k % NBS]), (k / NBS) & 1, p.timeout_ns);
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
@@ -292,6 +317,9 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
       if (k + 1 == total || order.j_of(k + 1) != j) umma_commit_w(smem_u32(&bars.kv_empty[st]));
       if (!C::SPLIT_ISSUE && k + NSB < total) ok = issue_s(k + NSB);
     }
+    // every product this warp issued has completed before tensor memory is released
+    umma_commit_w(smem_u32(&bars.mma_drain[0]));
+    mbar_wait_drain(smem_u32(&bars.mma_drain[0]), 0, p.timeout_ns);
   } else if (C::SPLIT_ISSUE && warp == C::WARP_SMMA) {
     // ------------------------------------------------------------------ S issuer (d_head 64)
     constexpr uint32_t idS = idesc_f32acc(128, BN, false, false, F16);
@@ -320,6 +348,8 @@ __global__ void __launch_bounds__(D == 64 ? 352 : 320, 1) attn_fwd_kernel(const 
         umma_ss_w(tS, qd + kmajor_step(BM, kk), kd + kmajor_step(BN, kk), idS, kk > 0);
       umma_commit_w(smem_u32(&bars.s_full[bsel]));
     }
+    umma_commit_w(smem_u32(&bars.mma_drain[1]));
+    mbar_wait_drain(smem_u32(&bars.mma_drain[1]), 0, p.timeout_ns);
   } else {
     // ------------------------------------------------------------------ softmax / epilogue
     const int t = warp >> 2;                 // query tile of this warpgroup
@@ -523,8 +553,12 @@ static cudaError_t launch_fwd_dispatch(const FwdParams& p, int D, bool f16, dim3
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3 grid,
                             cudaStream_t stream) {
-  return bias ? launch_fwd_dispatch<true>(p, D, f16, grid, stream)
-              : launch_fwd_dispatch<false>(p, D, f16, grid, stream);
+  if (bias) {  // the bias kernels exist for the 64-wide configuration only
+    if (D != 64) return cudaErrorInvalidValue;
+    return f16 ? launch_fwd_impl<64, true, true>(p, grid, stream)
+               : launch_fwd_impl<64, false, true>(p, grid, stream);
+  }
+  return launch_fwd_dispatch<false>(p, D, f16, grid, stream);
 }
 
 // Query rows per CTA (two 128-row tiles). The 4-D Q tensor map uses a 128-row box.

@@ -130,8 +130,9 @@ attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_te
  *         a multiple of 8 elements when Sk is not; 16-byte aligned base. Padded varlen uses
  *         the block at offset 0 of each batch, like q. Compact varlen is not offered
  *         (ATTN_ERR_UNSUPPORTED through this call with num_seqs semantics does not exist).
- * A NULL bias is the same as attn_fwd. Errors as attn_fwd; ATTN_ERR_SHAPE for a bias whose
- * sizes do not fit. No gradient for the bias is computed by this library (attn_bwd and the
+ * Supported for d_head 32 and 64, and for biases of fewer than 2^31 elements
+ * (ATTN_ERR_UNSUPPORTED otherwise). A NULL bias is the same as attn_fwd. Errors as attn_fwd;
+ * ATTN_ERR_SHAPE for a bias whose sizes do not fit. No gradient for the bias is computed by this library (attn_bwd and the
  * other backward calls take no bias).
  */
 attn_status attn_fwd_bias(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,

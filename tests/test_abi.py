@@ -213,3 +213,19 @@ def test_bias_stride_and_dtype_checks(lib):
     bias.dtype = 1  # fp16 bias with bf16 q
     assert lib.attn_fwd_bias(r(q), r(k), r(v), r(bias), None, None, 0.125, 0, r(o), r(lse),
                              None, 0, None) == 10  # ATTN_ERR_DTYPE
+
+
+def test_bias_head_size_and_size_limits(lib):
+    """The bias forward runs for d_head <= 64 and biases below 2^31 elements only."""
+    r = ctypes.byref
+    q, k, v, o = (t4((1, 2, 128, 128)) for _ in range(4))
+    lse = t3((1, 2, 128))
+    bias = t4((1, 1, 128, 128))
+    assert lib.attn_fwd_bias(r(q), r(k), r(v), r(bias), None, None, 0.125, 0, r(o), r(lse),
+                             None, 0, None) == ERR_UNSUPPORTED
+    S = 1 << 16
+    q, k, v, o = (t4((1, 1, S, 64)) for _ in range(4))
+    lse = t3((1, 1, S))
+    bias = t4((1, 1, S, S))  # 2^32 elements
+    assert lib.attn_fwd_bias(r(q), r(k), r(v), r(bias), None, None, 0.125, 0, r(o), r(lse),
+                             None, 0, None) == ERR_UNSUPPORTED

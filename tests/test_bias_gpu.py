@@ -1,6 +1,6 @@
 """GPU parity of the forward pass with an additive bias (attn_fwd_bias) against the
 float64 oracle: full and broadcast biases, causal and not, padded varlen, transposed K/V
-views, fp16, d_head 64 / 96 / 128, and -inf entries (a key mask written into the bias).
+views, fp16, d_head 32 / 64, and -inf entries (a key mask written into the bias).
 Rows that are not outputs keep their NaN sentinels."""
 import pytest
 import torch
@@ -19,12 +19,12 @@ CASES = [
     # (layout, D, causal, bias batch, bias heads, dtype, with -inf keys)
     ("bhsd", 64, True, "B", "H", torch.bfloat16, False),
     ("bhsd", 64, False, 1, "H", torch.bfloat16, False),
-    ("bhsd", 128, True, "B", 1, torch.bfloat16, False),
-    ("bhsd", 128, False, 1, 1, torch.float16, False),
-    ("kv_bshd", 128, False, "B", "H", torch.bfloat16, False),
+    ("bhsd", 64, True, "B", 1, torch.bfloat16, False),
+    ("bhsd", 64, False, 1, 1, torch.float16, False),
+    ("kv_bshd", 64, False, "B", "H", torch.bfloat16, False),
     ("padded", 64, True, "B", "H", torch.bfloat16, False),
-    ("padded", 128, False, "B", 1, torch.bfloat16, False),
-    ("bhsd", 96, True, 1, "H", torch.bfloat16, False),
+    ("padded", 64, False, "B", 1, torch.bfloat16, False),
+    ("bhsd", 32, True, 1, "H", torch.bfloat16, False),
     ("bhsd", 64, False, "B", "H", torch.bfloat16, True),
 ]
 
