@@ -23,7 +23,8 @@ __all__ = [
     "attn_fwd_workspace_size", "attn_bwd_workspace_size",
     "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
     "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
-    "attn_bwd_deterministic_workspace_size", "attn_fwd_bias", "EXPORTED_SYMBOLS",
+    "attn_bwd_deterministic_workspace_size", "attn_fwd_bias", "attn_bwd_bias",
+    "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -32,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "attn_bwd_padded_varlen", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_dq_epilogue",
     "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
     "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
-    "attn_bwd_deterministic_workspace_size", "attn_fwd_bias",
+    "attn_bwd_deterministic_workspace_size", "attn_fwd_bias", "attn_bwd_bias",
 )
 
 
@@ -73,6 +74,8 @@ _SIGS = {
     "attn_fwd": (INT, [P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
     "attn_fwd_padded_varlen": (INT, [P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
     "attn_fwd_bias": (INT, [P4, P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
+    "attn_bwd_bias": (INT, [P4, P4, P4, P4, P3, P4, P4, I32P, I32P, F32, INT, P4, P4, P4, P4,
+                            VP, SZ, VP]),
     "attn_fwd_compact_varlen": (INT, [P4, P4, P4, I32P, I32P, I32, I32, I32, F32, INT, P4, P3,
                                       VP, SZ, VP]),
     "attn_bwd": (INT, [P4, P4, P4, P4, P3, P4, I32P, I32P, F32, INT, P4, P4, P4, VP, SZ, VP]),
@@ -247,6 +250,21 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, workspace,
     _check(f(*_keep(tq, tk, tv, to, tl, tdo), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
              float(sm_scale), int(bool(causal)), *_keep(tdq, tdk, tdv), ws, nws,
              _stream(stream)), _name)
+
+
+def attn_bwd_bias(q, k, v, o, lse, dout, bias, dq, dk, dv, sm_scale, causal, workspace,
+                  dbias=None, cu_seqlens_q=None, cu_seqlens_k=None, stream=None):
+    """attn_bwd for a forward that took an additive bias; dbias (zeroed, full shape) gets dS."""
+    _check16(q, k, v, o, dout, dq, dk, dv, bias)
+    if dbias is not None:
+        _check16(dbias)
+    tq, tk, tv, to, tl, tdo = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse), _t4(dout)
+    tb, tdq, tdk, tdv, tdb = _t4(bias), _t4(dq), _t4(dk), _t4(dv), _t4(dbias)
+    ws, nws = _ws(workspace)
+    _check(load().attn_bwd_bias(
+        *_keep(tq, tk, tv, to, tl, tdo, tb), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        float(sm_scale), int(bool(causal)), *_keep(tdq, tdk, tdv, tdb), ws, nws,
+        _stream(stream)), "attn_bwd_bias")
 
 
 def attn_bwd_padded_varlen(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, workspace,

@@ -53,15 +53,23 @@ def bwd_workspace(q: torch.Tensor) -> torch.Tensor:
 def backward(q, k, v, o, lse, do, sm_scale: Optional[float] = None, causal: bool = False,
              cu_seqlens_q=None, cu_seqlens_k=None, compact: bool = False, max_seqlen_q: int = 0,
              max_seqlen_k: int = 0, dq=None, dk=None, dv=None, workspace=None, stream=None,
-             deterministic: bool = False):
+             deterministic: bool = False, bias=None, dbias=None):
     """dQ, dK, dV through the C ABI. deterministic=True takes the run-to-run reproducible
-    path (dQ accumulated per query block without reductions; S and dP computed twice)."""
+    path (dQ accumulated per query block without reductions; S and dP computed twice).
+    bias: the bias given to forward; dbias: optional zeroed full-shape tensor for its
+    gradient."""
     sm_scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else sm_scale
     dq = torch.empty(q.shape, dtype=q.dtype, device=q.device) if dq is None else dq
     dk = torch.empty(k.shape, dtype=k.dtype, device=k.device) if dk is None else dk
     dv = torch.empty(v.shape, dtype=v.dtype, device=v.device) if dv is None else dv
     ws = bwd_workspace(q) if workspace is None else workspace
-    if compact:
+    if bias is not None:
+        if compact or deterministic:
+            raise ValueError("the bias backward supports dense and padded inputs, "
+                             "non-deterministic")
+        _lib.attn_bwd_bias(q, k, v, o, lse, do, bias, dq, dk, dv, sm_scale, causal, ws, dbias,
+                           cu_seqlens_q, cu_seqlens_k, stream)
+    elif compact:
         f = (_lib.attn_bwd_compact_varlen_deterministic if deterministic
              else _lib.attn_bwd_compact_varlen)
         f(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q.numel() - 1,

@@ -36,36 +36,45 @@ def bhsd_to_thd(x: torch.Tensor) -> torch.Tensor:
 
 
 class FlashAttentionFunction(torch.autograd.Function):
-    """Fused attention with gradients for q, k, v (bf16 or fp16, BHSD views)."""
+    """Fused attention with gradients for q, k, v (bf16 or fp16, BHSD views) and, for a
+    full-shape additive bias that requires it, for the bias."""
 
     @staticmethod
     def forward(ctx, q, k, v, sm_scale, causal, cu_seqlens_q, cu_seqlens_k, compact,
-                max_seqlen_q, max_seqlen_k, deterministic=False):
+                max_seqlen_q, max_seqlen_k, deterministic=False, bias=None):
         o, lse = attention.forward(q, k, v, sm_scale, causal, cu_seqlens_q, cu_seqlens_k,
                                    compact=compact, max_seqlen_q=max_seqlen_q,
-                                   max_seqlen_k=max_seqlen_k)
-        ctx.save_for_backward(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k)
+                                   max_seqlen_k=max_seqlen_k, bias=bias)
+        ctx.save_for_backward(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, bias)
         ctx.cfg = (sm_scale, causal, compact, max_seqlen_q, max_seqlen_k, deterministic)
         return o
 
     @staticmethod
     def backward(ctx, do):
-        q, k, v, o, lse, cu_q, cu_k = ctx.saved_tensors
+        q, k, v, o, lse, cu_q, cu_k, bias = ctx.saved_tensors
         sm_scale, causal, compact, max_q, max_k, det = ctx.cfg
         do = do.contiguous() if do.stride(-1) != 1 else do
+        dbias = None
+        if bias is not None and ctx.needs_input_grad[11]:
+            if bias.shape[0] != q.shape[0] or bias.shape[1] != q.shape[1]:
+                raise NotImplementedError("a bias gradient needs a bias of shape (B, H, Sq, Sk)")
+            dbias = torch.zeros_like(bias)  # tiles the kernel does not visit stay zero
         dq, dk, dv = attention.backward(q, k, v, o, lse, do, sm_scale, causal, cu_q, cu_k,
                                         compact=compact, max_seqlen_q=max_q, max_seqlen_k=max_k,
-                                        deterministic=det)
-        return dq, dk, dv, None, None, None, None, None, None, None, None
+                                        deterministic=det, bias=bias, dbias=dbias)
+        return dq, dk, dv, None, None, None, None, None, None, None, None, dbias
 
 
 def flash_attention(q, k, v, sm_scale: Optional[float] = None, causal: bool = False,
-                    cu_seqlens_q=None, cu_seqlens_k=None, deterministic: bool = False):
+                    cu_seqlens_q=None, cu_seqlens_k=None, deterministic: bool = False,
+                    bias=None):
     """Dense (cu_seqlens None) or padded-varlen attention on BHSD views, differentiable.
-    deterministic=True makes the gradients identical from run to run."""
+    deterministic=True makes the gradients identical from run to run. bias: optional
+    additive bias (Bb, Hb, Sq, Sk) with its Sq stride a multiple of 8 elements (d_head <= 64);
+    it gets a gradient when it has the full shape (B, H, Sq, Sk) and requires one."""
     scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else float(sm_scale)
     return FlashAttentionFunction.apply(q, k, v, scale, bool(causal), cu_seqlens_q, cu_seqlens_k,
-                                        False, 0, 0, bool(deterministic))
+                                        False, 0, 0, bool(deterministic), bias)
 
 
 def flash_attention_varlen(q_thd, k_thd, v_thd, cu_seqlens_q, cu_seqlens_k,

@@ -304,6 +304,8 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
 struct BwdArgs {
   const attn_tensor4 *q, *k, *v, *o, *dout, *dq, *dk, *dv;
   const attn_tensor3* lse;
+  const attn_tensor4* bias = nullptr;   // optional additive bias (attn_bwd_bias)
+  const attn_tensor4* dbias = nullptr;  // optional gradient of the bias
 };
 
 // Stages: 1 preprocess, 2 key-tile kernel, 4 dQ epilogue, 8 deterministic dQ kernel. In
@@ -374,7 +376,21 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
                                       n_tiles);
       const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_tiles) : dim3(n_tiles, pr.H, pr.units);
       p.d_out = pr.D;
-      if (launch_bwd_main(p, kernel_width(pr.D), pr.f16, grid, st) != cudaSuccess)
+      if (a.bias != nullptr) {
+        // size-1 batch / head dimensions broadcast: stride 0
+        p.bias = reinterpret_cast<const uint16_t*>(a.bias->data);
+        p.b_sb = a.bias->size[0] == 1 ? 0 : a.bias->stride[0];
+        p.b_sh = a.bias->size[1] == 1 ? 0 : a.bias->stride[1];
+        p.b_ss = a.bias->stride[2];
+        if (a.dbias != nullptr) {
+          p.dbias = reinterpret_cast<uint16_t*>(a.dbias->data);
+          p.db_sb = a.dbias->stride[0];
+          p.db_sh = a.dbias->stride[1];
+          p.db_ss = a.dbias->stride[2];
+        }
+      }
+      if (launch_bwd_main(p, kernel_width(pr.D), pr.f16, a.bias != nullptr, grid, st) !=
+          cudaSuccess)
         return ATTN_ERR_CUDA;
     }
   }
@@ -442,6 +458,29 @@ attn_status bwd_common(const BwdArgs& a, const int32_t* cu_q, const int32_t* cu_
   }
   if ((s = check_lse(a.lse, pr)) != ATTN_OK) return s;
   if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
+  if (a.bias != nullptr) {
+    // as attn_fwd_bias: dense / padded forms, d_head <= 64, fewer than 2^31 elements; a
+    // gradient only for a full-shape bias (no broadcast sums)
+    if (compact || deterministic || pr.D > 64) return ATTN_ERR_UNSUPPORTED;
+    if ((s = check_tensor4(a.bias)) != ATTN_OK) return s;
+    if (!same_dtype(a.q, a.bias)) return ATTN_ERR_DTYPE;
+    if (a.bias->size[2] != a.q->size[2] || a.bias->size[3] != a.k->size[2] ||
+        (a.bias->size[0] != 1 && a.bias->size[0] != a.q->size[0]) ||
+        (a.bias->size[1] != 1 && a.bias->size[1] != a.q->size[1]))
+      return ATTN_ERR_SHAPE;
+    if (a.bias->size[0] * a.bias->size[1] * a.bias->size[2] * a.bias->size[3] >=
+        (int64_t(1) << 31))
+      return ATTN_ERR_UNSUPPORTED;
+    if (a.dbias != nullptr) {
+      if ((s = check_tensor4(a.dbias)) != ATTN_OK) return s;
+      if (!same_dtype(a.q, a.dbias)) return ATTN_ERR_DTYPE;
+      if (!same_shape(a.bias, a.dbias)) return ATTN_ERR_SHAPE;
+      if (a.bias->size[0] != a.q->size[0] || a.bias->size[1] != a.q->size[1])
+        return ATTN_ERR_UNSUPPORTED;
+    }
+  } else if (a.dbias != nullptr) {
+    return ATTN_ERR_NULL;
+  }
   if (deterministic) return bwd_stage(1 | 2 | 8, a, pr, sm_scale, causal, ws, ws_bytes, stream, true);
   return bwd_stage(7, a, pr, sm_scale, causal, ws, ws_bytes, stream);
 }
@@ -535,6 +574,19 @@ attn_status attn_bwd_compact_varlen(const attn_tensor4* q, const attn_tensor4* k
   BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse};
   return bwd_common(a, cu_seqlens_q, cu_seqlens_k, 1, num_seqs, max_seqlen_q, max_seqlen_k,
                     sm_scale, causal, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_bias(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                          const attn_tensor4* o, const attn_tensor3* lse, const attn_tensor4* dout,
+                          const attn_tensor4* bias, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_k, float sm_scale, int causal,
+                          const attn_tensor4* dq, const attn_tensor4* dk, const attn_tensor4* dv,
+                          const attn_tensor4* dbias, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (bias == nullptr) return ATTN_ERR_NULL;
+  BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse, bias, dbias};
+  return bwd_common(a, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, causal, workspace,
+                    workspace_bytes, stream);
 }
 
 attn_status attn_bwd_deterministic(const attn_tensor4* q, const attn_tensor4* k,

@@ -23,6 +23,8 @@
 // allocates TMEM and issues the MMAs. Tile sizes: 128 keys per CTA; 64 query rows per step
 // when d_head = 128 (dQ is formed transposed, K_n^T dS^T, so that every MMA has M = 128),
 // 128 when d_head = 64.
+#include <atomic>
+
 #include "attn_common.cuh"
 #include "attn_launch.h"
 
@@ -198,8 +200,13 @@ struct BwdBars {
   alignas(16) float ndelta[LSE_ST][BM];  // -Delta
 };
 
-template <int D, bool F16>
+// BIAS (the 64-wide configuration only): an additive bias enters the rebuilt scores. Each
+// compute thread (one key row) reads its key's column of the bias for the step's query rows
+// straight from global memory (a warp reads 32 consecutive keys of one query row per load)
+// and, when p.dbias is set, writes dS to the same places.
+template <int D, bool F16, bool BIAS = false>
 __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
+  static_assert(!BIAS || D == 64, "bias kernels exist for the 64-wide configuration only");
   using C = BwdCfg<D>;
   constexpr int BN = C::BN, BM = C::BM;
   constexpr int HALF = BM / 2;  // score columns per compute warpgroup
@@ -559,10 +566,37 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         const float* dp = dpv_all + ch * 32;
         uint32_t pp[16], pd[16];
         const uint64_t c2x2 = f2_pack(c2, c2);
+        // bias log2(e) of this key and the chunk's 32 query rows (0 off the sequence)
+        float bl[BIAS ? 32 : 1];
+        if constexpr (BIAS) {
+          const uint16_t* bcol = p.bias + sv.batch * p.b_sb + h * p.b_sh + key;
+          uint16_t raw[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int qq = q_lo + c0 + e;
+            raw[e] = (key_ok && qq < sv.len_q) ? bcol[(int64_t)qq * p.b_ss] : (uint16_t)0;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 b = unpack2<F16>((uint32_t)raw[e] | ((uint32_t)raw[e + 1] << 16));
+            bl[e] = b.x * 1.4426950408889634f;
+            bl[e + 1] = b.y * 1.4426950408889634f;
+          }
+        }
 #pragma unroll
         for (int e4 = 0; e4 < 32; e4 += 4) {
           float pv[4], ds[4], x[4];
-          if constexpr (C::AUG) {
+          if constexpr (C::AUG && BIAS) {
+            // S and dP arrive with LSE / sm_scale and Delta already subtracted; add the bias
+            f2_unpack(f2_fma(f2_pack(s[e4], s[e4 + 1]), c2x2, f2_pack(bl[e4], bl[e4 + 1])), x[0],
+                      x[1]);
+            f2_unpack(f2_fma(f2_pack(s[e4 + 2], s[e4 + 3]), c2x2, f2_pack(bl[e4 + 2], bl[e4 + 3])),
+                      x[2], x[3]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pv[u] = ex2_approx(x[u]);
+            f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), f2_pack(dp[e4], dp[e4 + 1])), ds[0], ds[1]);
+            f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), f2_pack(dp[e4 + 2], dp[e4 + 3])), ds[2], ds[3]);
+          } else if constexpr (C::AUG) {
             // S and dP arrive with LSE / sm_scale and Delta already subtracted
             f2_unpack(f2_mul(f2_pack(s[e4], s[e4 + 1]), c2x2), x[0], x[1]);
             f2_unpack(f2_mul(f2_pack(s[e4 + 2], s[e4 + 3]), c2x2), x[2], x[3]);
@@ -597,6 +631,17 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
           pp[e4 / 2 + 1] = pack2<F16>(pv[2], pv[3]);
           pd[e4 / 2] = pack2<F16>(ds[0], ds[1]);
           pd[e4 / 2 + 1] = pack2<F16>(ds[2], ds[3]);
+        }
+        if constexpr (BIAS) {
+          if (p.dbias != nullptr && key_ok) {  // dbias = dS (rounded like the dS operand)
+            uint16_t* dcol = p.dbias + sv.batch * p.db_sb + h * p.db_sh + key;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int qq = q_lo + c0 + e;
+              if (qq < sv.len_q)
+                dcol[(int64_t)qq * p.db_ss] = (uint16_t)(pd[e / 2] >> ((e & 1) * 16));
+            }
+          }
         }
         ATTN_TMEM_ST_X16(tmem + C::COL_P + lane_off + c0 / 2, pp);
 #pragma unroll
@@ -660,28 +705,34 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
   if (threadIdx.x == 0 && bars.abort && p.status != nullptr) atomicCAS(p.status, 0, kStatusTimeout);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool BIAS>
 static cudaError_t launch_bwd_main_impl(const BwdParams& p, dim3 grid, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D, F16>,
+  if (dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_main_kernel<D, F16, BIAS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
-  attn_bwd_main_kernel<D, F16><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
+  attn_bwd_main_kernel<D, F16, BIAS><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, dim3 grid, cudaStream_t stream) {
+cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, bool bias, dim3 grid,
+                            cudaStream_t stream) {
+  if (bias) {  // the bias kernels exist for the 64-wide configuration only
+    if (D != 64) return cudaErrorInvalidValue;
+    return f16 ? launch_bwd_main_impl<64, true, true>(p, grid, stream)
+               : launch_bwd_main_impl<64, false, true>(p, grid, stream);
+  }
   if (D == 128)
-    return f16 ? launch_bwd_main_impl<128, true>(p, grid, stream)
-               : launch_bwd_main_impl<128, false>(p, grid, stream);
-  return f16 ? launch_bwd_main_impl<64, true>(p, grid, stream)
-             : launch_bwd_main_impl<64, false>(p, grid, stream);
+    return f16 ? launch_bwd_main_impl<128, true, false>(p, grid, stream)
+               : launch_bwd_main_impl<128, false, false>(p, grid, stream);
+  return f16 ? launch_bwd_main_impl<64, true, false>(p, grid, stream)
+             : launch_bwd_main_impl<64, false, false>(p, grid, stream);
 }
 
 int bwd_block_m(int D) { return D == 128 ? BwdCfg<128>::BM : BwdCfg<64>::BM; }

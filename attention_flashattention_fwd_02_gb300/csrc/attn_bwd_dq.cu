@@ -15,6 +15,8 @@
 // warp 9 MMA issuer (whole warp walks the schedule, one elected lane issues). S/dP of step
 // j+1 are issued as soon as the compute warps have loaded those of step j. TMEM: S (128
 // columns), dP (128), dQ (D). dS goes through shared memory as the K-major A operand.
+#include <atomic>
+
 #include "attn_common.cuh"
 #include "attn_launch.h"
 
@@ -321,14 +323,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
 template <int D, bool F16>
 static cudaError_t launch_dq_impl(const BwdDqParams& p, dim3 grid, cudaStream_t stream) {
   using C = DqCfg<D>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   attn_bwd_dq_kernel<D, F16><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();

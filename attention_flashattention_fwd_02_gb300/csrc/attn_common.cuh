@@ -105,6 +105,10 @@ struct BwdParams {
   SeqAddr seq;
   int causal;
   int d_out;                      // head size of the tensors (<= the kernel's D)
+  const uint16_t* bias;           // BIAS kernels: bias element (b, h, q, key) at
+  int64_t b_sb, b_sh, b_ss;       //   b*b_sb + h*b_sh + q*b_ss + key (0 strides broadcast)
+  uint16_t* dbias;                // BIAS kernels, may be null: dS written at the same layout
+  int64_t db_sb, db_sh, db_ss;
   int with_dq;                    // 0: no dQ products (the deterministic dQ kernel makes dQ)
   int tile_major;                 // grid (units, H, key tiles) instead of (key tiles, H, units)
   float scale_log2;               // sm_scale * log2(e)

@@ -39,6 +39,8 @@
 // masks are applied only on tiles that straddle the diagonal or the key length. Query tiles
 // at or past the sequence's query length exit before doing anything (the AOTriton
 // padded-varlen kernel prologue returns early the same way).
+#include <atomic>
+
 #include "attn_common.cuh"
 #include "attn_launch.h"
 
@@ -528,14 +530,14 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
 template <int D, bool F16, bool BIAS>
 static cudaError_t launch_fwd_impl(const FwdParams& p, dim3 grid, cudaStream_t stream) {
   using C = FwdCfg<D, BIAS>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F16, BIAS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   attn_fwd_kernel<D, F16, BIAS><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();

@@ -17,7 +17,8 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3
 int bwd_block_m(int D);  // query rows per inner step of the main kernel
 int bwd_block_n();       // key rows per CTA of the main kernel
 cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, dim3 grid, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, bool bias, dim3 grid,
+                            cudaStream_t stream);
 cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream);
 // Deterministic dQ: grid = (query blocks, H, units); a block covers bwd_dq_block_m() rows.
 int bwd_dq_block_m();

@@ -132,8 +132,7 @@ attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_te
  *         (ATTN_ERR_UNSUPPORTED through this call with num_seqs semantics does not exist).
  * Supported for d_head 32 and 64, and for biases of fewer than 2^31 elements
  * (ATTN_ERR_UNSUPPORTED otherwise). A NULL bias is the same as attn_fwd. Errors as attn_fwd;
- * ATTN_ERR_SHAPE for a bias whose sizes do not fit. No gradient for the bias is computed by this library (attn_bwd and the
- * other backward calls take no bias).
+ * ATTN_ERR_SHAPE for a bias whose sizes do not fit. attn_bwd_bias is the matching backward.
  */
 attn_status attn_fwd_bias(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
                           const attn_tensor4* bias, const int32_t* cu_seqlens_q,
@@ -155,6 +154,23 @@ attn_status attn_bwd(const attn_tensor4* q, const attn_tensor4* k, const attn_te
                      int causal, const attn_tensor4* dq, const attn_tensor4* dk,
                      const attn_tensor4* dv, void* workspace, size_t workspace_bytes,
                      void* stream);
+
+/*
+ * Backward pass matching attn_fwd_bias: arguments as in attn_bwd plus the bias given to the
+ * forward pass (non-NULL, same limits: d_head 32 or 64, fewer than 2^31 elements, dense or
+ * padded forms). dbias, optional (NULL: no bias gradient), receives dS = the gradient with
+ * respect to the bias, rounded to the element type; it must have the bias's full shape
+ * (B, H, Sq, Sk) -- a broadcast bias gets no gradient here (ATTN_ERR_UNSUPPORTED) -- and is
+ * written only on the (query, key) tiles the kernel visits: entries in fully masked causal
+ * tiles and past a sequence's length are left as they are, so pass it zeroed.
+ */
+attn_status attn_bwd_bias(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                          const attn_tensor4* o, const attn_tensor3* lse, const attn_tensor4* dout,
+                          const attn_tensor4* bias, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_k, float sm_scale, int causal,
+                          const attn_tensor4* dq, const attn_tensor4* dk, const attn_tensor4* dv,
+                          const attn_tensor4* dbias, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /*
  * Deterministic backward: same arguments and results as attn_bwd, and the same bits on every

@@ -229,3 +229,21 @@ def test_bias_head_size_and_size_limits(lib):
     bias = t4((1, 1, S, S))  # 2^32 elements
     assert lib.attn_fwd_bias(r(q), r(k), r(v), r(bias), None, None, 0.125, 0, r(o), r(lse),
                              None, 0, None) == ERR_UNSUPPORTED
+
+
+def test_bwd_bias_validation(lib):
+    """attn_bwd_bias: bias required; d_head <= 64; a gradient only for a full-shape bias."""
+    r = ctypes.byref
+
+    def call(shape, bias, dbias):
+        q, k, v, o, do, dq, dk, dv = (t4(shape) for _ in range(8))
+        lse = t3(shape[:3])
+        return lib.attn_bwd_bias(r(q), r(k), r(v), r(o), r(lse), r(do),
+                                 r(bias) if bias is not None else None, None, None, 0.125, 0,
+                                 r(dq), r(dk), r(dv), r(dbias) if dbias is not None else None,
+                                 None, 0, None)
+
+    assert call((1, 2, 128, 64), None, None) == ERR_NULL
+    assert call((1, 2, 128, 128), t4((1, 2, 128, 128)), None) == ERR_UNSUPPORTED
+    assert call((2, 2, 128, 64), t4((1, 2, 128, 128)), t4((1, 2, 128, 128))) == ERR_UNSUPPORTED
+    assert call((1, 2, 128, 64), t4((1, 2, 128, 128)), t4((1, 2, 128, 136))) == ERR_SHAPE

@@ -64,3 +64,25 @@ def test_autograd_varlen_thd():
     assert_fwd_close(thd_to_bhsd(o.detach()), torch.zeros(lse_r.shape), o_r, np.zeros_like(lse_r),
                      what="autograd varlen")
     assert_grads_close([thd_to_bhsd(t.grad) for t in (q, k, v)], g_r, what="autograd varlen")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_autograd_bias(causal):
+    """flash_attention with a full-shape additive bias that requires a gradient."""
+    gen = torch.Generator().manual_seed(17 + causal)
+    B, H, S, D = 2, 2, 200, 64
+    q, k, v = (torch.randn(B, H, S, D, generator=gen).bfloat16().cuda().requires_grad_(True)
+               for _ in range(3))
+    bias = torch.randn(B, H, S, S, generator=gen).bfloat16().cuda().requires_grad_(True)
+    w = torch.randn(B, H, S, D, generator=gen).bfloat16().cuda()
+    o = flash_attention(q, k, v, causal=causal, bias=bias)
+    (o.float() * w.float()).sum().backward()
+    scale = 1.0 / math.sqrt(D)
+    qn, kn, vn, wn, bn = (np64(t) for t in (q, k, v, w, bias))
+    o_r, _ = ref.fwd_bhsd(qn, kn, vn, scale, causal, bias=bn)
+    g_r = ref.bwd_bhsd(qn, kn, vn, wn, scale, causal, bias=bn)
+    np.testing.assert_array_less(np.abs(np64(o) - o_r).max(), 1e-2)
+    assert_grads_close((q.grad, k.grad, v.grad), g_r[:3], what="autograd bias")
+    db = np64(bias.grad)
+    assert np.linalg.norm(db - g_r[3]) / np.linalg.norm(g_r[3]) <= 2e-2

@@ -84,3 +84,47 @@ def test_zero_bias_equals_no_bias():
     torch.cuda.synchronize()
     torch.testing.assert_close(o1, o0, atol=2e-3, rtol=0)
     torch.testing.assert_close(l1, l0, atol=1e-5, rtol=0)
+
+
+BWD_CASES = [
+    # (layout, D, causal, bias batch, bias heads, dtype, with dbias)
+    ("bhsd", 64, True, "B", "H", torch.bfloat16, True),
+    ("bhsd", 64, False, "B", "H", torch.bfloat16, True),
+    ("kv_bshd", 64, False, "B", "H", torch.float16, True),
+    ("padded", 64, True, "B", "H", torch.bfloat16, True),
+    ("bhsd", 32, False, "B", "H", torch.bfloat16, True),
+    ("bhsd", 64, True, 1, "H", torch.bfloat16, False),  # broadcast bias: no gradient
+]
+
+
+@pytest.mark.parametrize("layout,D,causal,bb,bh,dtype,with_db", BWD_CASES)
+def test_bias_backward_parity(layout, D, causal, bb, bh, dtype, with_db):
+    from attention_flashattention_fwd_02_gb300.attention import backward, bwd_workspace
+    from _helpers import assert_grads_close, rel_l2
+    padded = layout == "padded"
+    base = WORKLOADS["padded" if padded else "cross"]
+    wl = base.replace(B=2, H=2, Sq=300, Sk=300 if layout != "kv_bshd" else 410, D=D,
+                      causal=causal, layout=layout, seed=131 + D)
+    x = make_inputs(wl, lengths=[300, 123] if padded else None, dtype=dtype)
+    full, Sk = _bias(x, wl, bb, bh, dtype, False, seed=137 + D)
+    bias = full[..., :Sk]
+    bias_dev = full.to(DEV)[..., :Sk]
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    cu_q = g["cu_seqlens_q"] if padded else None
+    cu_k = g["cu_seqlens_k"] if padded else None
+    q, k, v, do = g["q"], g["k"], g["v"], g["do"]
+    o, lse = forward(q, k, v, wl.sm_scale, causal, cu_q, cu_k, bias=bias_dev)
+    dbias = torch.zeros_like(full, device=DEV)[..., :Sk] if with_db else None
+    ws = bwd_workspace(q)
+    dq, dk, dv = backward(q, k, v, o, lse, do, wl.sm_scale, causal, cu_q, cu_k, workspace=ws,
+                          bias=bias_dev, dbias=dbias)
+    torch.cuda.synchronize()
+    assert _lib.attn_read_device_status(ws) == 0
+    qn, kn, vn, don = (np64(x[n]) for n in ("q", "k", "v", "do"))
+    g_r = ref.bwd_bhsd(qn, kn, vn, don, wl.sm_scale, causal,
+                       x["cu_seqlens_q"].numpy() if padded else None,
+                       x["cu_seqlens_k"].numpy() if padded else None, bias=np64(bias))
+    assert_grads_close((dq, dk, dv), g_r[:3], what=f"bias bwd {layout} D={D}")
+    if with_db:
+        err = rel_l2(np64(dbias).ravel(), g_r[3].ravel())
+        assert err <= 2e-2, f"dbias rel-L2 {err:.3e}"
