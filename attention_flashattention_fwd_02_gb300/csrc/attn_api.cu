@@ -232,6 +232,13 @@ int withheld_tile_for_test() {
   return atoi(v);
 }
 
+// Test hook of the backward key-tile kernel: step whose Q / dO tile is never loaded.
+int withheld_step_for_test() {
+  const char* v = getenv("ATTN_TEST_WITHHOLD_Q_STEP");
+  if (v == nullptr || *v == 0) return -1;
+  return atoi(v);
+}
+
 // ----------------------------------------------------------------------------- forward
 attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
                        const int32_t* cu_q, const int32_t* cu_k, int compact, int32_t num_seqs,
@@ -352,6 +359,8 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       if ((s = make_map(&p.tm_k, a.k, BN)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_v, a.v, BN)) != ATTN_OK) return s;
       p.with_dq = deterministic ? 0 : 1;
+      p.withhold_step = withheld_step_for_test();
+      p.timeout_ns = p.withhold_step >= 0 ? 50000000ull : kWaitTimeoutNs;
       if (p.with_dq &&
           (s = make_map_acc(&p.tm_dq, dq_acc, (int64_t)pr.B * pr.H * pr.Sq, pr.D)) != ATTN_OK)
         return s;

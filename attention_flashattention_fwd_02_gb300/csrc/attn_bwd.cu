@@ -327,8 +327,9 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     for (int st = 0; st < QST; ++st) last_it[st] = -1;
     for (int it = 0; it < n_steps; ++it) {
       const int st = it % QST;
+      if (it == p.withhold_step) continue;  // failure-detection test: this stage never fills
       if (it >= QST &&
-          !mbar_wait(smem_u32(&bars.q_empty[st]), ((it / QST) - 1) & 1, abort, kWaitTimeoutNs))
+          !mbar_wait(smem_u32(&bars.q_empty[st]), ((it / QST) - 1) & 1, abort, p.timeout_ns))
         break;
       last_it[st] = it;
       const int q_lo = q_tile(it) * BM;
@@ -364,11 +365,11 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       mbar_arrive(qb);
     }
     if (lane == 0 && *abort) {  // the consumers gave up: let the copies in flight land
-      mbar_wait_drain(smem_u32(&bars.kv_full), 0, kWaitTimeoutNs);
+      mbar_wait_drain(smem_u32(&bars.kv_full), 0, p.timeout_ns);
 #pragma unroll
       for (int st = 0; st < QST; ++st)
         if (last_it[st] >= 0)
-          mbar_wait_drain(smem_u32(&bars.q_full[st]), (last_it[st] / QST) & 1, kWaitTimeoutNs);
+          mbar_wait_drain(smem_u32(&bars.q_full[st]), (last_it[st] / QST) & 1, p.timeout_ns);
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       constexpr uint32_t QSTEP = C::Q_BYTES >> 4, DSSTEP = C::DS_BYTES >> 4;
       auto issue_sdp = [&](int it) -> bool {
         const int st = it % QST;
-        if (!mbar_wait(smem_u32(&bars.q_full[st]), (it / QST) & 1, abort, kWaitTimeoutNs))
+        if (!mbar_wait(smem_u32(&bars.q_full[st]), (it / QST) & 1, abort, p.timeout_ns))
           return false;
         tc_fence_after();
         const uint32_t qo = st * QSTEP;
@@ -411,22 +412,22 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
         umma_commit_w(smem_u32(&bars.s_full));
         return true;
       };
-      bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort, kWaitTimeoutNs) && issue_sdp(0);
+      bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort, p.timeout_ns) && issue_sdp(0);
       for (int it = 0; ok && it < n_steps; ++it) {
         const int st = it % QST, bs = it & 1;
         const uint32_t qo = st * QSTEP, dso = bs * DSSTEP;
         if (it + 1 < n_steps) {
           // S^T / dP^T of step it are in registers of the compute warpgroups: overwrite them
-          if (!mbar_wait(smem_u32(&bars.s_free), it & 1, abort, kWaitTimeoutNs)) break;
+          if (!mbar_wait(smem_u32(&bars.s_free), it & 1, abort, p.timeout_ns)) break;
           if (!issue_sdp(it + 1)) break;
         }
-        if (!mbar_wait(smem_u32(&bars.p_full), it & 1, abort, kWaitTimeoutNs)) break;
+        if (!mbar_wait(smem_u32(&bars.p_full), it & 1, abort, p.timeout_ns)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           umma_ts_w(tDV, tP + kk * 8, do_mn + qo + mnmajor_step(kk), idG, (it > 0 || kk > 0));
         umma_commit_w(smem_u32(&bars.p_empty));  // P^T of step it read: the next P may land
-        if (!mbar_wait(smem_u32(&bars.ds_full[bs]), (it >> 1) & 1, abort, kWaitTimeoutNs)) break;
+        if (!mbar_wait(smem_u32(&bars.ds_full[bs]), (it >> 1) & 1, abort, p.timeout_ns)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
                     (it > 0 || kk > 0));
         if (p.with_dq) {
           if (it > 0 &&
-              !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, kWaitTimeoutNs))
+              !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, p.timeout_ns))
             break;
           tc_fence_after();
 #pragma unroll
@@ -452,7 +453,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       umma_commit_w(smem_u32(&bars.dkdv_full));
       // every product this warp issued has completed before tensor memory is released
       umma_commit_w(smem_u32(&bars.mma_drain));
-      mbar_wait_drain(smem_u32(&bars.mma_drain), 0, kWaitTimeoutNs);
+      mbar_wait_drain(smem_u32(&bars.mma_drain), 0, p.timeout_ns);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ P^T / dS^T compute
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     // lanes are query rows, columns d. Query rows past the sequence hold exact zeros (their dS
     // was masked), so whole blocks can be added.
     auto drain_dq = [&](int itd) -> bool {
-      if (!mbar_wait(smem_u32(&bars.dq_full), itd & 1, abort, kWaitTimeoutNs)) return false;
+      if (!mbar_wait(smem_u32(&bars.dq_full), itd & 1, abort, p.timeout_ns)) return false;
       tc_fence_after();
       float v[32];
       ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + g * 32, reinterpret_cast<uint32_t*>(v));
@@ -517,8 +518,8 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     for (int it = 0; it < n_steps; ++it) {
       const int st = it % QST, bs = it & 1;
       const int q_lo = q_tile(it) * BM;
-      if (!mbar_wait(smem_u32(&bars.s_full), it & 1, abort, kWaitTimeoutNs) ||
-          !mbar_wait(smem_u32(&bars.q_full[st]), (it / QST) & 1, abort, kWaitTimeoutNs)) {
+      if (!mbar_wait(smem_u32(&bars.s_full), it & 1, abort, p.timeout_ns) ||
+          !mbar_wait(smem_u32(&bars.q_full[st]), (it / QST) & 1, abort, p.timeout_ns)) {
         ok = false;
         break;
       }
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       const int q_min = p.causal ? key : 0;  // top-left causal: query q sees key iff q >= key
       // The dS^T buffer of this step was last read by the dK / dQ MMAs two steps ago.
       if (it >= 2 &&
-          !mbar_wait(smem_u32(&bars.ds_empty[bs]), ((it >> 1) - 1) & 1, abort, kWaitTimeoutNs)) {
+          !mbar_wait(smem_u32(&bars.ds_empty[bs]), ((it >> 1) - 1) & 1, abort, p.timeout_ns)) {
         ok = false;
         break;
       }
@@ -554,7 +555,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.s_free));  // the MMA warp may compute the next S^T / dP^T
       // P^T of the previous step must have been read by its dV MMA before this step's lands
-      if (it > 0 && !mbar_wait(smem_u32(&bars.p_empty), (it - 1) & 1, abort, kWaitTimeoutNs)) {
+      if (it > 0 && !mbar_wait(smem_u32(&bars.p_empty), (it - 1) & 1, abort, p.timeout_ns)) {
         ok = false;
         break;
       }
@@ -665,7 +666,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_main_kernel(const __grid_cons
     if (p.with_dq && ok && n_steps > 0) ok = drain_dq(n_steps - 1);
     if (lane == 0) bulk_wait_group0();  // this warp's reduces complete before the CTA exits
     // ---- epilogue: dK = sm_scale * acc, dV = acc; warpgroup g writes columns [g*D/2, +D/2)
-    if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, kWaitTimeoutNs);
+    if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, p.timeout_ns);
     tc_fence_after();
     if (ok) {
       const int64_t grow = sv.row0_k + key;

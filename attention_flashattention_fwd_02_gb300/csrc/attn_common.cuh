@@ -109,6 +109,8 @@ struct BwdParams {
   int64_t b_sb, b_sh, b_ss;       //   b*b_sb + h*b_sh + q*b_ss + key (0 strides broadcast)
   uint16_t* dbias;                // BIAS kernels, may be null: dS written at the same layout
   int64_t db_sb, db_sh, db_ss;
+  uint64_t timeout_ns;            // bound on every pipeline wait
+  int withhold_step;              // test hook: step whose Q / dO the producer never loads (-1)
   int with_dq;                    // 0: no dQ products (the deterministic dQ kernel makes dQ)
   int tile_major;                 // grid (units, H, key tiles) instead of (key tiles, H, units)
   float scale_log2;               // sm_scale * log2(e)

@@ -46,3 +46,34 @@ def test_withheld_tile_times_out_and_context_survives():
     assert _lib.attn_read_device_status(ws) == 0
     O, L = ref.attention_forward(np64(q[0, 0]), np64(k[0, 0]), np64(v[0, 0]), scale, False)
     assert_fwd_close(o[0, 0], lse[0, 0], O, L, what="after timeout")
+
+
+def test_backward_withheld_step_times_out_and_context_survives():
+    """Same for the backward key-tile kernel (hook ATTN_TEST_WITHHOLD_Q_STEP: the producer
+    skips one query step): its producer waits for the copies it issued and its MMA warp for
+    the products it issued before the CTA exits, and the next call is correct."""
+    from attention_flashattention_fwd_02_gb300.attention import backward, bwd_workspace
+    from _helpers import assert_grads_close
+    gen = torch.Generator().manual_seed(6)
+    q, do = (torch.randn(1, 1, 512, 64, generator=gen).bfloat16().cuda() for _ in range(2))
+    k, v = (torch.randn(1, 1, 128, 64, generator=gen).bfloat16().cuda() for _ in range(2))
+    scale = 1.0 / math.sqrt(64)
+    o, lse = forward(q, k, v, scale, False)
+    ws = bwd_workspace(q)
+    os.environ["ATTN_TEST_WITHHOLD_Q_STEP"] = "1"
+    try:
+        t0 = time.time()
+        backward(q, k, v, o, lse, do, scale, False, workspace=ws)
+        status = _lib.attn_read_device_status(ws)
+        elapsed = time.time() - t0
+    finally:
+        del os.environ["ATTN_TEST_WITHHOLD_Q_STEP"]
+    assert status == ATTN_ERR_DEVICE_TIMEOUT
+    assert elapsed < 10.0
+    ws = bwd_workspace(q)
+    dq, dk, dv = backward(q, k, v, o, lse, do, scale, False, workspace=ws)
+    torch.cuda.synchronize()
+    assert _lib.attn_read_device_status(ws) == 0
+    g = ref.attention_backward(np64(q[0, 0]), np64(k[0, 0]), np64(v[0, 0]), np64(do[0, 0]),
+                               scale, False)
+    assert_grads_close((dq[0, 0], dk[0, 0], dv[0, 0]), g, what="backward after timeout")
