@@ -279,6 +279,9 @@ def run_ours(args, rank, world, dist, clocks_on=True):
             "bwd_pre_gbs": round(pre_gbs, 1), "bwd_pre_frac_of_hbm": round(pre_gbs / peak_h, 4),
             "bwd_post_gbs": round(post_gbs, 1), "bwd_post_frac_of_hbm": round(post_gbs / peak_h, 4),
             "hbm_peak_gbs": peak_h,
+            "flops_convention": "exact unmasked (query, key) pairs: causal counts S(S+1)/2 per "
+                                "head, i.e. the usual 1/2-dense figure plus S/2; fwd 4*D and "
+                                "bwd 10*D FLOPs per pair",
             "ms_per_step": {k: round(per_kernel[k] / args.steps, 4) for k in KERNELS},
         },
         "gpu_launches": len(variants) * len(KERNELS) * args.steps,
