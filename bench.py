@@ -57,6 +57,23 @@ def parse_args():
     return ap.parse_args()
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (x itself without a process group). The device
+    is where the reduction tensor lives: the GPU under NCCL, the CPU under gloo."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's time (weak scaling,
+    each rank runs the same per-GPU workload)."""
+    return flops_per_rank_step * steps * world / (max_ms * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -223,15 +240,9 @@ def run_ours(args, rank, world, dist, clocks_on=True):
         for vi in range(len(variants)):
             ktime[(vi, kn)] = sum(kern_ev[i][(vi, kn)][0].elapsed_time(kern_ev[i][(vi, kn)][1])
                                   for i in range(args.steps))
-    total_ms = step_ms
-    if dist is not None:
-        import torch.distributed as tdist
-        t = torch.tensor([total_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_ms = float(t.item())
-
+    total_ms = max_over_ranks(step_ms, dist, dev)
     flops_step = sum(vt["f_fwd"] + vt["f_bwd"] for vt in variants)
-    value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops_step, args.steps, world, total_ms)
     peak_b, peak_s, peak_h, peak_src = peaks()
 
     # per-kernel roofline figures (tensor-bound kernels: algorithmic flops / event time)
@@ -405,14 +416,9 @@ def run_e2e(args, variants, launch, kernels, stream, dist, world):
             s_d2h.wait_event(e)
     b.record(s_d2h)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if dist is not None:
-        import torch.distributed as tdist
-        t = torch.tensor([ms], device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
-    fl = sum(vt["f_fwd"] + vt["f_bwd"] for vt in variants) * steps * world
-    return {"value": round(fl / (ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+    ms = max_over_ranks(a.elapsed_time(b), dist, "cuda")
+    fl = sum(vt["f_fwd"] + vt["f_bwd"] for vt in variants)
+    return {"value": round(job_throughput(fl, steps, world, ms), 2), "unit": "TFLOPS",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / steps, 4)}
 
