@@ -9,6 +9,7 @@
 
 #include "../../include/attn.h"
 #include "attn_launch.h"
+#include "attn_tune_table.h"
 
 using namespace attn_sm103;
 
@@ -194,15 +195,46 @@ attn_status make_map_acc(CUtensorMap* m, float* acc, int64_t rows, int64_t D) {
 // are dispatched heaviest first across all (unit, head) pairs, which removes the tail that
 // a per-head heaviest-first order leaves (the last head's heaviest tile starts near the
 // end). It also spreads the CTAs of one head over the whole launch, so the operands they
-// share must stay in L2 between them: the order is used when those bytes are at most 72 MB
-// (L2 is 129 MB) and the tile count fits grid z.
+// share must stay in L2 (129 MB) between them: the order is used when those bytes are at
+// most the kernel's limit in the measured table of attn_tune_table.h and the tile count
+// fits grid z.
 // Head sizes 32 and 96 run on the kernels built for 64 and 128: the TMA loads (box 64
 // columns wide) fill the columns past the head size with zeros, which add nothing to any
 // product, and only the real columns are stored.
 int kernel_width(int D) { return D <= 64 ? 64 : 128; }
 
-bool tile_major_order(int causal, double shared_bytes, int tiles) {
-  return causal && shared_bytes <= 72.0 * 1024 * 1024 && tiles <= 65535;
+// Tuning hook: ATTN_GRID_ORDER = "<kernel>:tile" or "<kernel>:seq" (comma-separated
+// entries) forces the order of that kernel's causal grids; the sweep that writes the table
+// times both orders this way.
+int grid_order_override(const char* kernel) {
+  const char* v = getenv("ATTN_GRID_ORDER");
+  if (v == nullptr) return -1;
+  const size_t n = strlen(kernel);
+  for (const char* e = v; *e;) {
+    if (strncmp(e, kernel, n) == 0 && e[n] == ':') {
+      if (strncmp(e + n + 1, "tile", 4) == 0) return 1;
+      if (strncmp(e + n + 1, "seq", 3) == 0) return 0;
+    }
+    const char* c = strchr(e, ',');
+    if (c == nullptr) break;
+    e = c + 1;
+  }
+  return -1;
+}
+
+double tile_major_limit(const char* kernel, int width) {
+  for (const GridOrderRule& r : kGridOrderRules)
+    if (r.width == width && strcmp(r.kernel, kernel) == 0) return r.max_tile_major_bytes;
+  return 0.0;
+}
+
+// kernel: "fwd", "bwd_main", "bwd_main_nodq" or "bwd_dq"; width: 64 or 128.
+bool tile_major_order(const char* kernel, int width, int causal, double shared_bytes,
+                      int tiles) {
+  if (!causal || tiles > 65535) return false;
+  const int forced = grid_order_override(kernel);
+  if (forced >= 0) return forced == 1;
+  return shared_bytes <= tile_major_limit(kernel, width);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -299,7 +331,8 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   p.withhold_tile = withheld_tile_for_test();
   p.timeout_ns = p.withhold_tile >= 0 ? 50000000ull : kWaitTimeoutNs;
   const int n_blk = (pr.max_q + BM - 1) / BM;
-  p.tile_major = tile_major_order(p.causal, (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
+  p.tile_major = tile_major_order("fwd", kernel_width(pr.D), p.causal,
+                                  (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
   const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_blk) : dim3(n_blk, pr.H, pr.units);
   p.d_out = pr.D;
   cudaError_t e = launch_attn_fwd(p, kernel_width(pr.D), pr.f16, bias != nullptr, grid,
@@ -380,9 +413,13 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       p.sm_scale = sm_scale;
       p.status = status;
       const int n_tiles = (pr.max_k + BN - 1) / BN;
-      // the operands every CTA of a head visits: Q, dO (16-bit) and the fp32 dQ accumulator
-      p.tile_major = tile_major_order(p.causal, (double)pr.units * pr.H * pr.max_q * pr.D * 8,
-                                      n_tiles);
+      // the operands every CTA of a head visits: Q, dO (16-bit) and, when this kernel
+      // accumulates dQ, the fp32 accumulator
+      p.tile_major = p.with_dq
+          ? tile_major_order("bwd_main", kernel_width(pr.D), p.causal,
+                             (double)pr.units * pr.H * pr.max_q * pr.D * 8, n_tiles)
+          : tile_major_order("bwd_main_nodq", kernel_width(pr.D), p.causal,
+                             (double)pr.units * pr.H * pr.max_q * pr.D * 4, n_tiles);
       const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_tiles) : dim3(n_tiles, pr.H, pr.units);
       p.d_out = pr.D;
       if (a.bias != nullptr) {
@@ -438,7 +475,8 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
     p.d_out = pr.D;
     const int n_blk = (pr.max_q + BMq - 1) / BMq;
     // the operands every CTA of a head visits: K and V
-    p.tile_major = tile_major_order(p.causal, (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
+    p.tile_major = tile_major_order("bwd_dq", kernel_width(pr.D), p.causal,
+                                    (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
     const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_blk) : dim3(n_blk, pr.H, pr.units);
     if (launch_bwd_dq(p, kernel_width(pr.D), pr.f16, grid, st) != cudaSuccess) return ATTN_ERR_CUDA;
   }

@@ -1,0 +1,60 @@
+"""Both CTA orders of the causal grids give the same results (the order only changes which
+CTA runs when): forward O and LSE, dK and dV, and the deterministic dQ bit for bit; the
+reduction-order-dependent dQ of attn_bwd within the oracle tolerance. Forced through the
+library's ATTN_GRID_ORDER tuning hook."""
+import os
+
+import pytest
+import torch
+
+from oracle import attention_ref as ref
+from attention_flashattention_fwd_02_gb300 import _lib
+from attention_flashattention_fwd_02_gb300.attention import backward, bwd_workspace, forward
+from attention_flashattention_fwd_02_gb300.workloads import WORKLOADS, make_inputs
+
+from _helpers import assert_grads_close, np64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+KERNELS = ("fwd", "bwd_main", "bwd_main_nodq", "bwd_dq")
+
+
+def _run(order, q, k, v, do, c, cu):
+    os.environ["ATTN_GRID_ORDER"] = ",".join(f"{n}:{order}" for n in KERNELS)
+    try:
+        # zero-filled outputs: rows past a sequence are not written and stay equal
+        o, lse = forward(q, k, v, c, True, cu, cu, out=torch.zeros_like(q),
+                         lse=torch.zeros(q.shape[:3], dtype=torch.float32, device=DEV))
+        out = {"o": o, "lse": lse}
+        for det in (False, True):
+            ws = bwd_workspace(q)
+            g = [torch.zeros_like(t) for t in (q, k, v)]
+            backward(q, k, v, o, lse, do, c, True, cu, cu, dq=g[0], dk=g[1], dv=g[2],
+                     workspace=ws, deterministic=det)
+            torch.cuda.synchronize()
+            assert _lib.attn_read_device_status(ws) == 0
+            out["det" if det else "reg"] = g
+        return out
+    finally:
+        os.environ.pop("ATTN_GRID_ORDER", None)
+
+
+@pytest.mark.parametrize("D,padded", [(64, False), (128, True), (96, False)])
+def test_orders_agree(D, padded):
+    base = WORKLOADS["padded" if padded else "tiny"]
+    wl = base.replace(B=3, H=2, Sq=700, Sk=700, D=D, causal=True, seed=91 + D,
+                      layout="padded" if padded else "bhsd")
+    x = make_inputs(wl, lengths=[700, 300, 513] if padded else None)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    cu = x["cu_seqlens_q"].to(DEV) if padded else None
+    a = _run("seq", q, k, v, do, wl.sm_scale, cu)
+    b = _run("tile", q, k, v, do, wl.sm_scale, cu)
+    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
+    for i in (1, 2):
+        assert torch.equal(a["reg"][i], b["reg"][i])
+    for i in range(3):
+        assert torch.equal(a["det"][i], b["det"][i])
+    cun = x["cu_seqlens_q"].numpy() if padded else None
+    g_r = ref.bwd_bhsd(*(np64(x[n]) for n in ("q", "k", "v", "do")), wl.sm_scale, True, cun, cun)
+    for g in (a["reg"], b["reg"]):
+        assert_grads_close(tuple(g), g_r, what=f"grid order D={D}")
