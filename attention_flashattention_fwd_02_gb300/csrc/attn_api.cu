@@ -102,7 +102,8 @@ attn_status make_problem(const attn_tensor4* q, const attn_tensor4* k, const att
   if (q->size[0] != k->size[0] || q->size[1] != k->size[1] || q->size[3] != k->size[3])
     return ATTN_ERR_SHAPE;
   const int64_t D = q->size[3];
-  if (D != 32 && D != 64 && D != 96 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  // 256: forward only (the backward stages reject it)
+  if (D != 32 && D != 64 && D != 96 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
   if (q->size[1] > 65535) return ATTN_ERR_UNSUPPORTED;  // grid y
   pr->B = (int)q->size[0];
   pr->H = (int)q->size[1];
@@ -201,7 +202,7 @@ attn_status make_map_acc(CUtensorMap* m, float* acc, int64_t rows, int64_t D) {
 // Head sizes 32 and 96 run on the kernels built for 64 and 128: the TMA loads (box 64
 // columns wide) fill the columns past the head size with zeros, which add nothing to any
 // product, and only the real columns are stored.
-int kernel_width(int D) { return D <= 64 ? 64 : 128; }
+int kernel_width(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : 256; }
 
 // Tuning hook: ATTN_GRID_ORDER = "<kernel>:tile" or "<kernel>:seq" (comma-separated
 // entries) forces the order of that kernel's causal grids; the sweep that writes the table
@@ -307,7 +308,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
 
   FwdParams p;
   memset(&p, 0, sizeof(p));
-  const int BM = fwd_block_m();
+  const int BM = fwd_block_m(kernel_width(pr.D));
   if ((s = make_map(&p.tm_q, q, fwd_box_rows())) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_k, k, 128)) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_v, v, 128)) != ATTN_OK) return s;
@@ -354,6 +355,8 @@ struct BwdArgs {
 attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float sm_scale,
                       int causal, void* ws, size_t ws_bytes, void* stream,
                       bool deterministic = false) {
+  // d_head 256: the key-tile kernel's dK and dV accumulators alone would fill TMEM
+  if (pr.D > 128) return ATTN_ERR_UNSUPPORTED;
   const BwdWorkspace w = bwd_layout(pr.B, pr.H, pr.Sq, pr.D);
   if (ws == nullptr || ws_bytes < (deterministic ? w.dq_off : w.total)) return ATTN_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return ATTN_ERR_ALIGN;

@@ -9,9 +9,9 @@
 // so that the backward pass can rebuild P (the stash / recompute split of the nvFuser SDPA
 // page).
 //
-// Warp roles (320 threads at d_head 128, 352 at d_head 64):
+// Warp roles (320 threads at d_head 128 and 256, 352 at d_head 64):
 //   warps 0..3   softmax, O correction and epilogue of query tile 0 (thread r owns row r)
-//   warps 4..7   the same for query tile 1
+//   warps 4..7   the same for query tile 1 (d_head 256: warp 4 loads V, 5..7 idle)
 //   warp 8       TMA producer: Q_0, Q_1 once, then K_j / V_j into an NST-deep stage ring
 //   warp 9       TMEM allocator and MMA issuer (at d_head 64: PV products only)
 //   warp 10      d_head 64 only: issuer of the score products S = Q K^T
@@ -29,6 +29,12 @@
 //     PV(k - NSB) has completed. The next score tile of a query tile is computed while its
 //     softmax runs.
 // TMEM (512 columns): NSB score buffers of 128 columns, then O_0 and O_1 (D columns each).
+//
+// d_head 256: O alone takes 256 columns, so a CTA owns one query tile (NQ = 1, 128 rows) and
+// two score buffers; Q, one K and one V stage (64 KB each) fill shared memory. K_j is
+// released as soon as its score product has completed and V_j once its PV product has, and
+// each has a producer warp of its own, so K_{j+1} streams in while PV_j runs and V_{j+1}
+// while S_{j+2} runs.
 //
 // Online softmax in base 2 with a lazy rescale: a row's reference maximum m only moves when
 // a new row maximum exceeds it by more than 8 (so p <= 2^8); O and l are rescaled by
@@ -52,8 +58,10 @@ namespace attn_sm103 {
 // d_head 128, where shared memory holds no more.
 template <int D, bool BIAS = false>
 struct FwdCfg {
-  static constexpr int BM = 128, BN = 128, NQ = 2;  // two query tiles per CTA
-  static constexpr int NST = (D == 128) ? 2 : 4;
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int NQ = (D == 256) ? 1 : 2;  // query tiles per CTA
+  static constexpr int NST = (D == 256) ? 1 : (D == 128) ? 2 : 4;
+  static constexpr bool SPLIT_KV = (D == 256);   // K and V released and loaded separately
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int NBS = BIAS ? ((D == 128) ? 1 : 2) : 0;
@@ -65,10 +73,13 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = OFF_B + NBS * B_BYTES + 1024;  // + alignment slack
   static constexpr int NSB = (D == 64) ? 3 : 2;  // rotating score / P buffers
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O0 = NSB * 128, COL_O1 = NSB * 128 + D;
-  static_assert(COL_O1 + D <= TMEM_COLS, "TMEM budget");
+  static constexpr uint32_t COL_O0 = NSB * 128, COL_O1 = NSB * 128 + (NQ == 2 ? D : 0);
+  static_assert(COL_O0 + NQ * D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
   static constexpr bool SPLIT_ISSUE = (NSB == 3);  // separate S and PV issuing warps
   static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_SMMA = 10;
+  static constexpr int WARP_VPROD = 4;  // V producer (SPLIT_KV only; a tile-1 warp otherwise)
+  static_assert(!SPLIT_KV || NQ == 1, "the V producer takes a warp of query tile 1");
   static constexpr int WARP_BIAS = SPLIT_ISSUE ? 11 : 10;  // bias producer (BIAS only)
   static constexpr int NTHREADS = (SPLIT_ISSUE ? 352 : 320) + (BIAS ? 32 : 0);
 };
@@ -77,7 +88,9 @@ template <int NST, int NSB>
 struct FwdBars {
   uint64_t q_full;
   uint64_t k_full[NST], v_full[NST], kv_empty[NST];
-  uint64_t s_full[NSB], p_full[NSB], buf_free[NSB], o_done[2];
+  uint64_t k_empty[NST];  // SPLIT_KV: K stage free (kv_empty then frees the V stage)
+  uint64_t s_full[NSB], p_full[NSB], buf_free[NSB];
+  uint64_t o_done[2][2];  // PV_t(j) completed: barrier [t][j mod 2] (see the rescale wait)
   uint64_t b_full[2], b_empty[2];  // bias slots (NBS of them used)
   uint64_t mma_drain[2];           // completion of each issuing warp's last products
   uint32_t tmem_base;
@@ -128,21 +141,21 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
 
   SeqView sv;
   if (!decode_seq(p.seq, z, threadIdx.x == 0 ? p.status : nullptr, sv)) return;
-  const int blk_lo = m_blk * (2 * BM);
+  const int blk_lo = m_blk * (C::NQ * BM);
   if (blk_lo >= sv.len_q) return;  // past this sequence's queries
 
-  int q_lo[2], q_hi[2], n_t[2];
+  int q_lo[2], q_hi[2], n_t[2];  // with one query tile per CTA, tile 1 is empty
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     q_lo[t] = blk_lo + t * BM;
-    q_hi[t] = min(q_lo[t] + BM, sv.len_q);
+    q_hi[t] = t < C::NQ ? min(q_lo[t] + BM, sv.len_q) : q_lo[t];
     n_t[t] = key_tiles(q_lo[t], q_hi[t], sv.len_k, p.causal, BN);
   }
   const int n_max = max(n_t[0], n_t[1]);
   const ScoreOrder order(n_t[0], n_t[1]);
 
   if (n_max == 0) {  // no visible keys: O = 0, LSE = -inf on the valid rows
-    if (warp < 8) {
+    if (warp < 4 * C::NQ) {
       const int row = blk_lo + threadIdx.x;
       if (row < sv.len_q) {
         const int64_t grow = sv.row0_q + row;
@@ -166,14 +179,15 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       mbar_init(smem_u32(&bars.k_full[s]), 1);
       mbar_init(smem_u32(&bars.v_full[s]), 1);
       mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+      mbar_init(smem_u32(&bars.k_empty[s]), 1);
     }
     for (int b = 0; b < NSB; ++b) {
       mbar_init(smem_u32(&bars.s_full[b]), 1);
       mbar_init(smem_u32(&bars.p_full[b]), 128);
       mbar_init(smem_u32(&bars.buf_free[b]), 1);
     }
+    for (int r = 0; r < 4; ++r) mbar_init(smem_u32(&bars.o_done[r >> 1][r & 1]), 1);
     for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&bars.o_done[t]), 1);
       mbar_init(smem_u32(&bars.b_full[t]), 1);
       mbar_init(smem_u32(&bars.b_empty[t]), 128);
       mbar_init(smem_u32(&bars.mma_drain[t]), 1);
@@ -197,9 +211,9 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       tma_prefetch_map(&p.tm_k);
       tma_prefetch_map(&p.tm_v);
       const uint32_t qb = smem_u32(&bars.q_full);
-      mbar_arrive_expect_tx(qb, 2 * C::Q_BYTES);
+      mbar_arrive_expect_tx(qb, C::NQ * C::Q_BYTES);
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+      for (int t = 0; t < C::NQ; ++t)
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(sQ + t * C::Q_BYTES + s * BM * 128, &p.tm_q, qb, s * 64,
@@ -210,9 +224,8 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       for (int j = 0; j < n_max; ++j) {
         const int st = j % NST;
         if (j == p.withhold_tile) continue;  // failure-detection test: this stage never fills
-        if (j >= NST &&
-            !mbar_wait(smem_u32(&bars.kv_empty[st]), ((j / NST) - 1) & 1, abort, p.timeout_ns))
-          break;
+        const uint32_t empty = C::SPLIT_KV ? smem_u32(&bars.k_empty[st]) : smem_u32(&bars.kv_empty[st]);
+        if (j >= NST && !mbar_wait(empty, ((j / NST) - 1) & 1, abort, p.timeout_ns)) break;
         last_j[st] = j;
         const int krow = sv.row0_k + j * BN;
         const uint32_t kb = smem_u32(&bars.k_full[st]);
@@ -220,6 +233,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(sK + st * C::KV_BYTES + s * BN * 128, &p.tm_k, kb, s * 64, krow, h, sv.batch);
+        if (C::SPLIT_KV) continue;  // V has its own producer warp
         const uint32_t vb = smem_u32(&bars.v_full[st]);
         mbar_arrive_expect_tx(vb, C::KV_BYTES);
 #pragma unroll
@@ -232,9 +246,36 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
         for (int st = 0; st < NST; ++st)
           if (last_j[st] >= 0) {
             mbar_wait_drain(smem_u32(&bars.k_full[st]), (last_j[st] / NST) & 1, p.timeout_ns);
-            mbar_wait_drain(smem_u32(&bars.v_full[st]), (last_j[st] / NST) & 1, p.timeout_ns);
+            if (!C::SPLIT_KV)
+              mbar_wait_drain(smem_u32(&bars.v_full[st]), (last_j[st] / NST) & 1, p.timeout_ns);
           }
       }
+    }
+  } else if (C::SPLIT_KV && warp == C::WARP_VPROD) {
+    // ------------------------------------------------------------------ V producer (d_head 256)
+    if (lane == 0) {
+      int last_j[NST];
+#pragma unroll
+      for (int st = 0; st < NST; ++st) last_j[st] = -1;
+      for (int j = 0; j < n_max; ++j) {
+        const int st = j % NST;
+        if (j == p.withhold_tile) continue;
+        if (j >= NST &&
+            !mbar_wait(smem_u32(&bars.kv_empty[st]), ((j / NST) - 1) & 1, abort, p.timeout_ns))
+          break;
+        last_j[st] = j;
+        const uint32_t vb = smem_u32(&bars.v_full[st]);
+        mbar_arrive_expect_tx(vb, C::KV_BYTES);
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(sV + st * C::KV_BYTES + s * BN * 128, &p.tm_v, vb, s * 64,
+                      sv.row0_k + j * BN, h, sv.batch);
+      }
+      if (*abort)
+#pragma unroll
+        for (int st = 0; st < NST; ++st)
+          if (last_j[st] >= 0)
+            mbar_wait_drain(smem_u32(&bars.v_full[st]), (last_j[st] / NST) & 1, p.timeout_ns);
     }
   } else if (BIAS && warp == C::WARP_BIAS) {
     // ------------------------------------------------------------------ bias producer
@@ -290,6 +331,8 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       for (int kk = 0; kk < D / 16; ++kk)
         umma_ss_w(tS, qd + kmajor_step(BM, kk), kd + kmajor_step(BN, kk), idS, kk > 0);
       umma_commit_w(smem_u32(&bars.s_full[bsel]));
+      // one query tile: K_j has no other reader once this product has completed
+      if (C::SPLIT_KV) umma_commit_w(smem_u32(&bars.k_empty[st]));
       return true;
     };
     bool ok = true;
@@ -312,7 +355,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
         umma_ts_w(tO, tS + kk * 8, vd + mnmajor_step(kk), idO, (j > 0 || kk > 0));
-      umma_commit_w(smem_u32(&bars.o_done[t]));
+      umma_commit_w(smem_u32(&bars.o_done[t][j & 1]));
       if (C::SPLIT_ISSUE && k + NSB < total) umma_commit_w(smem_u32(&bars.buf_free[bsel]));
       // Stage st is free once the last product reading V_j is done; the score products that
       // read K_j finished before their P was published, hence before this PV.
@@ -352,7 +395,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     }
     umma_commit_w(smem_u32(&bars.mma_drain[1]));
     mbar_wait_drain(smem_u32(&bars.mma_drain[1]), 0, p.timeout_ns);
-  } else {
+  } else if (warp < 4 * C::NQ) {
     // ------------------------------------------------------------------ softmax / epilogue
     const int t = warp >> 2;                 // query tile of this warpgroup
     const int r = (warp & 3) * 32 + lane;    // row in tile = TMEM lane
@@ -451,11 +494,13 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       f2_unpack(f2_add(rs0, rs1), a0, a1);
       l = l * scale + (a0 + a1);
       m_use = m_new;
-      // O_t is rescaled only when the reference maximum moved. PV_t(j-1) must have finished
-      // first; PV_t(j) cannot start before this thread publishes P_t(j), so the o_done phase
-      // is at most one ahead of the one waited for and its parity identifies it.
+      // O_t is rescaled only when the reference maximum moved; PV_t(j-1) must have finished
+      // first. PV_t(i) completes phase i / 2 of barrier [t][i mod 2], and the parity names the
+      // phase exactly: every schedule has completed PV(k - 3), hence PV_t(j - 3), once S_t(j)
+      // is in TMEM, and PV_t(j + 1) cannot run before this thread publishes P_t(j).
       if (j > 0 && __any_sync(0xffffffffu, scale != 1.f)) {
-        if (!mbar_wait(smem_u32(&bars.o_done[t]), (j - 1) & 1, abort, p.timeout_ns)) {
+        if (!mbar_wait(smem_u32(&bars.o_done[t][(j - 1) & 1]), ((j - 1) >> 1) & 1, abort,
+                       p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -482,8 +527,9 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full[bsel]));
     }
-    if (n > 0) {
-      if (ok) ok = mbar_wait(smem_u32(&bars.o_done[t]), (n - 1) & 1, abort, p.timeout_ns);
+    if (n > 0) {  // PV_t(n-1), exact as above: PV_t(n-3) has completed and no PV_t follows it
+      if (ok) ok = mbar_wait(smem_u32(&bars.o_done[t][(n - 1) & 1]), ((n - 1) >> 1) & 1, abort,
+                             p.timeout_ns);
       tc_fence_after();
     }
     if (ok) {
@@ -546,6 +592,9 @@ static cudaError_t launch_fwd_impl(const FwdParams& p, dim3 grid, cudaStream_t s
 template <bool BIAS>
 static cudaError_t launch_fwd_dispatch(const FwdParams& p, int D, bool f16, dim3 grid,
                                        cudaStream_t stream) {
+  if (D == 256)
+    return f16 ? launch_fwd_impl<256, true, BIAS>(p, grid, stream)
+               : launch_fwd_impl<256, false, BIAS>(p, grid, stream);
   if (D == 128)
     return f16 ? launch_fwd_impl<128, true, BIAS>(p, grid, stream)
                : launch_fwd_impl<128, false, BIAS>(p, grid, stream);
@@ -563,8 +612,9 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3
   return launch_fwd_dispatch<false>(p, D, f16, grid, stream);
 }
 
-// Query rows per CTA (two 128-row tiles). The 4-D Q tensor map uses a 128-row box.
-int fwd_block_m() { return 256; }
+// Query rows per CTA: two 128-row tiles, one at kernel width 256. The 4-D Q tensor map uses
+// a 128-row box.
+int fwd_block_m(int width) { return width == 256 ? 128 : 256; }
 int fwd_box_rows() { return 128; }
 
 }  // namespace attn_sm103

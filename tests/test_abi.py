@@ -95,7 +95,8 @@ def good():
     ("misaligned", ERR_ALIGN),
     ("d_head_48", ERR_UNSUPPORTED),
     ("d_head_80", ERR_UNSUPPORTED),
-    ("d_head_256", ERR_UNSUPPORTED),
+    ("d_head_192", ERR_UNSUPPORTED),
+    ("d_head_512", ERR_UNSUPPORTED),
     ("kv_shape", ERR_SHAPE),
     ("o_shape", ERR_SHAPE),
     ("lse_shape", ERR_SHAPE),
@@ -154,6 +155,28 @@ def test_bwd_workspace_checked(lib):
     assert st == ERR_WORKSPACE
     st = lib.attn_bwd(r(q), r(q), r(q), r(q), r(lse), r(q), None, None, 0.125, 0, r(q), r(q),
                       r(q), FAKE, 16, None)
+    assert st == ERR_WORKSPACE
+
+
+def test_d_head_256_forward_only(lib):
+    """d_head 256 passes the forward's argument checks (a bad LSE shape is the first error,
+    not the head size) and is refused by every backward call before anything else (no
+    workspace would otherwise be the error)."""
+    r = ctypes.byref
+    shape = (1, 2, 128, 256)
+    q = t4(shape)
+    assert call_fwd(lib, q, q, q, q, t3((1, 2, 64))) == ERR_SHAPE
+    lse = t3(shape[:3])
+    st = lib.attn_bwd(r(q), r(q), r(q), r(q), r(lse), r(q), None, None, 0.125, 0, r(q), r(q),
+                      r(q), None, 0, None)
+    assert st == ERR_UNSUPPORTED
+    st = lib.attn_bwd_deterministic(r(q), r(q), r(q), r(q), r(lse), r(q), None, None, 0.125,
+                                    0, r(q), r(q), r(q), None, 0, None)
+    assert st == ERR_UNSUPPORTED
+    # the same call at d_head 128 gets as far as the workspace check
+    q = t4((1, 2, 128, 128))
+    st = lib.attn_bwd(r(q), r(q), r(q), r(q), r(lse), r(q), None, None, 0.125, 0, r(q), r(q),
+                      r(q), None, 0, None)
     assert st == ERR_WORKSPACE
 
 

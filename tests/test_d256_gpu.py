@@ -1,0 +1,81 @@
+"""Forward parity at d_head 256 (one 128-row query tile per CTA; forward only).
+
+O and LSE against the float64 oracle on dense, cross-length with transposed K/V views,
+padded and compact varlen inputs, both masks, bf16 and fp16, several query and key tiles with
+ragged tails; rows past a sequence stay untouched. Every backward entry point refuses the
+head size with ATTN_ERR_UNSUPPORTED, before launching anything."""
+import pytest
+import torch
+
+from oracle import attention_ref as ref
+from attention_flashattention_fwd_02_gb300 import _lib
+from attention_flashattention_fwd_02_gb300.attention import backward, bwd_workspace, forward
+from attention_flashattention_fwd_02_gb300.workloads import WORKLOADS, make_inputs
+
+from _helpers import assert_fwd_close, np64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+D = 256
+
+CASES = [
+    # (layout, B, H, Sq, Sk, causal, dtype)
+    ("bhsd", 1, 2, 128, 128, False, torch.bfloat16),
+    ("bhsd", 2, 2, 300, 300, True, torch.bfloat16),
+    ("bhsd", 1, 3, 1100, 1100, False, torch.bfloat16),
+    ("bhsd", 1, 2, 1100, 1100, True, torch.float16),
+    ("kv_bshd", 2, 2, 200, 520, False, torch.bfloat16),
+    ("bhsd", 1, 2, 520, 200, True, torch.bfloat16),   # rows past the last key
+    ("bhsd", 1, 1, 1, 1, True, torch.bfloat16),
+    ("bhsd", 1, 2, 129, 1, False, torch.float16),
+    ("padded", 3, 2, 700, 700, True, torch.bfloat16),
+    ("compact", 1, 2, 0, 0, True, torch.bfloat16),
+    ("compact", 1, 2, 0, 0, False, torch.float16),
+]
+
+
+@pytest.mark.parametrize("layout,B,H,Sq,Sk,causal,dtype", CASES)
+def test_d256_forward_parity(layout, B, H, Sq, Sk, causal, dtype):
+    if layout == "compact":
+        wl = WORKLOADS["compact"].replace(H=H, D=D, causal=causal, n_seqs=4, seed=301)
+        x = make_inputs(wl, lengths=[1, 260, 129, 64], dtype=dtype)
+    else:
+        base = WORKLOADS["padded" if layout == "padded" else "cross"]
+        wl = base.replace(B=B, H=H, Sq=Sq, Sk=Sk, D=D, causal=causal, layout=layout,
+                          seed=303 + Sq)
+        x = make_inputs(wl, lengths=[700, 130, 257] if layout == "padded" else None, dtype=dtype)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    q, k, v = g["q"], g["k"], g["v"]
+    varlen = layout in ("padded", "compact")
+    cu_q = g["cu_seqlens_q"] if varlen else None
+    cu_k = g["cu_seqlens_k"] if varlen else None
+    o = torch.full(q.shape, float("nan"), dtype=dtype, device=DEV)
+    lse = torch.full(q.shape[:3], float("nan"), device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    forward(q, k, v, wl.sm_scale, causal, cu_q, cu_k, compact=layout == "compact", out=o,
+            lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    assert _lib.attn_read_device_status(ws) == 0
+    qn, kn, vn = (np64(x[n]) for n in ("q", "k", "v"))
+    if layout == "compact":
+        cu = x["cu_seqlens_q"].numpy()
+        o_r, lse_r = ref.fwd_compact_varlen(qn, kn, vn, cu, cu, wl.sm_scale, causal)
+    else:
+        cu = x["cu_seqlens_q"].numpy() if varlen else None
+        o_r, lse_r = ref.fwd_bhsd(qn, kn, vn, wl.sm_scale, causal, cu, cu)
+    assert_fwd_close(o, lse, o_r, lse_r, what=f"d256 {layout} causal={causal}")
+    if layout == "padded":  # rows past a sequence are never written
+        for b, n in enumerate(x["lengths"].tolist()):
+            assert torch.isnan(o[b, :, n:]).all() and torch.isnan(lse[b, :, n:]).all()
+
+
+def test_d256_backward_refused():
+    wl = WORKLOADS["cross"].replace(B=1, H=2, Sq=128, Sk=128, D=D, causal=False, layout="bhsd")
+    x = make_inputs(wl)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse = forward(q, k, v)
+    for det in (False, True):
+        dq = torch.full_like(q, 7.0)
+        with pytest.raises(_lib.AttnError, match=r"status 5 "):
+            backward(q, k, v, o, lse, do, dq=dq, workspace=bwd_workspace(q), deterministic=det)
+        assert (dq == 7.0).all()  # nothing launched
