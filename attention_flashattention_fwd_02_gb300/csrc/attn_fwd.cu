@@ -52,10 +52,11 @@
 
 namespace attn_sm103 {
 
-// BIAS: the additive bias tile of each score tile (128 query rows x 128 keys, 16-bit) is
-// staged in shared memory in NBS slots, filled in score-tile order (slot k mod NBS) and
-// refilled once the softmax warps that read it are done: two slots at d_head 64, one at
-// d_head 128, where shared memory holds no more.
+// BIAS (d_head 64 only): the additive bias tile of each score tile (128 query rows x 128
+// keys, 16-bit) is staged in shared memory, one slot per query tile: slot t holds tile t's
+// bias tiles in its key-tile order, each refilled once tile t's softmax warps have read the
+// previous one. A slot shared by both tiles would let a parity wait pass early where one
+// tile's key tiles run out and the other takes over its slot.
 template <int D, bool BIAS = false>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
@@ -64,7 +65,7 @@ struct FwdCfg {
   static constexpr bool SPLIT_KV = (D == 256);   // K and V released and loaded separately
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NBS = BIAS ? ((D == 128) ? 1 : 2) : 0;
+  static constexpr int NBS = BIAS ? 2 : 0;  // one bias slot per query tile
   static constexpr int B_BYTES = BM * BN * 2;  // one bias slot
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = NQ * Q_BYTES;
@@ -279,31 +280,33 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     }
   } else if (BIAS && warp == C::WARP_BIAS) {
     // ------------------------------------------------------------------ bias producer
-    // bias tiles in score-tile order: slot k mod NBS, refilled once the softmax warps that
-    // read its previous tile are done (they wait on nothing this warp does afterwards). A
-    // warp of its own, so that its waits never share a warp with the K/V producer's.
+    // bias tiles in score-tile order, tile t's into slot t (phase j for its key tile j),
+    // each slot refilled once tile t's softmax warps have read its previous tile (they wait on
+    // nothing this warp does afterwards). A warp of its own, so that its waits never share a
+    // warp with the K/V producer's.
     if (lane == 0) {
-      constexpr int NBS = C::NBS > 0 ? C::NBS : 1;
       tma_prefetch_map(&p.tm_b);
       const uint32_t sB = smem_u32(smem + C::OFF_B);
       const int hb = p.bias_h_bcast ? 0 : h, bb = p.bias_b_bcast ? 0 : sv.batch;
-      int issued = 0;
+      int last_j[2] = {-1, -1};  // last key tile loaded into each slot
       for (int k = 0; k < order.total; ++k) {
-        const int t = order.t_of(k), j = order.j_of(k), slot = k % NBS;
-        if (k >= NBS && !mbar_wait(smem_u32(&bars.b_empty[slot]), ((k / NBS) - 1) & 1, abort,
-                                   p.timeout_ns))
+        const int t = order.t_of(k), j = order.j_of(k);
+        if (j >= 1 &&
+            !mbar_wait(smem_u32(&bars.b_empty[t]), (j - 1) & 1, abort, p.timeout_ns))
           break;
-        const uint32_t bf = smem_u32(&bars.b_full[slot]);
+        const uint32_t bf = smem_u32(&bars.b_full[t]);
         mbar_arrive_expect_tx(bf, C::B_BYTES);
 #pragma unroll
         for (int s = 0; s < 2; ++s)
-          tma_load_4d(sB + slot * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
+          tma_load_4d(sB + t * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
                       sv.row0_q + q_lo[t], hb, bb);
-        issued = k + 1;
+        last_j[t] = j;
       }
       if (*abort)  // let the copies in flight land before exiting
-        for (int k = max(0, issued - NBS); k < issued; ++k)
-          mbar_wait_drain(smem_u32(&bars.b_full[k % NBS]), (k / NBS) & 1, p.timeout_ns);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (last_j[t] >= 0)
+            mbar_wait_drain(smem_u32(&bars.b_full[t]), last_j[t] & 1, p.timeout_ns);
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
@@ -421,9 +424,8 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
                         reinterpret_cast<uint32_t*>(s + 96));
       if constexpr (BIAS) {
         // s <- s c2 + bias log2(e): the scores in base-2 units, bias included
-        constexpr int NBS = C::NBS > 0 ? C::NBS : 1;
-        const int slot = k % NBS;
-        if (!mbar_wait(smem_u32(&bars.b_full[slot]), (k / NBS) & 1, abort, p.timeout_ns)) {
+        const int slot = t;  // slot t, phase j
+        if (!mbar_wait(smem_u32(&bars.b_full[slot]), j & 1, abort, p.timeout_ns)) {
           ok = false;
           break;
         }

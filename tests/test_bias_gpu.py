@@ -73,6 +73,35 @@ def test_bias_forward_parity(layout, D, causal, bb, bh, dtype, neg_inf):
             assert torch.isnan(o[b, :, n:]).all() and torch.isnan(lse[b, :, n:]).all()
 
 
+@pytest.mark.parametrize("S,causal,lengths", [(1000, True, None), (1000, False, None),
+                                               (700, True, [700, 290, 129])])
+def test_bias_forward_long(S, causal, lengths):
+    """Many key tiles per query tile, and CTAs whose two query tiles see different numbers
+    of key tiles (causal) or whose second tile is empty (ragged lengths): each query tile's
+    bias tiles pass through its own slot in key order."""
+    padded = lengths is not None
+    base = WORKLOADS["padded" if padded else "cross"]
+    wl = base.replace(B=len(lengths) if padded else 1, H=2, Sq=S, Sk=S, D=64, causal=causal,
+                      layout="padded" if padded else "bhsd", seed=131)
+    x = make_inputs(wl, lengths=lengths)
+    full, Sk = _bias(x, wl, "B", "H", torch.bfloat16, False, seed=137)
+    bias_dev = full.to(DEV)[..., :Sk]
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    cu = g["cu_seqlens_q"] if padded else None
+    o = torch.full_like(g["q"], float("nan"))
+    lse = torch.full(g["q"].shape[:3], float("nan"), device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    forward(g["q"], g["k"], g["v"], wl.sm_scale, causal, cu, cu, out=o, lse=lse, workspace=ws,
+            bias=bias_dev)
+    torch.cuda.synchronize()
+    assert _lib.attn_read_device_status(ws) == 0
+    qn, kn, vn = (np64(x[n]) for n in ("q", "k", "v"))
+    cun = x["cu_seqlens_q"].numpy() if padded else None
+    o_r, lse_r = ref.fwd_bhsd(qn, kn, vn, wl.sm_scale, causal, cun, cun,
+                              bias=np64(full[..., :Sk]))
+    assert_fwd_close(o, lse, o_r, lse_r, what=f"bias S={S} causal={causal}")
+
+
 def test_zero_bias_equals_no_bias():
     wl = WORKLOADS["cross"].replace(B=1, H=2, Sq=256, Sk=384, D=64, causal=True,
                                     layout="bhsd", seed=5)
