@@ -79,3 +79,25 @@ def test_d256_backward_refused():
         with pytest.raises(_lib.AttnError, match=r"status 5 "):
             backward(q, k, v, o, lse, do, dq=dq, workspace=bwd_workspace(q), deterministic=det)
         assert (dq == 7.0).all()  # nothing launched
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_d256_fullsize_sampled_heads(causal):
+    """The timed shape (B4 H16 S4096 D256) in one call; two sampled heads against the oracle
+    element by element, every head finite."""
+    import numpy as np
+    wl = WORKLOADS["sweep4k"].replace(B=4, H=16, Sq=4096, Sk=4096, D=D, causal=causal,
+                                      seed=311 + causal)
+    x = make_inputs(wl)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    o, lse = forward(q, k, v, wl.sm_scale, causal, workspace=ws)
+    torch.cuda.synchronize()
+    assert _lib.attn_read_device_status(ws) == 0
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(7 + causal)
+    for _ in range(2):
+        b, h = int(rng.integers(wl.B)), int(rng.integers(wl.H))
+        Q, K, V = (np64(x[n][b, h]) for n in ("q", "k", "v"))
+        O_r, L_r = ref.attention_forward(Q, K, V, wl.sm_scale, causal)
+        assert_fwd_close(o[b, h], lse[b, h], O_r, L_r, what=f"d256 full b{b} h{h}")

@@ -19,18 +19,18 @@ DEV = "cuda"
 KERNELS = ("fwd", "bwd_main", "bwd_main_nodq", "bwd_dq")
 
 
-def _run(order, q, k, v, do, c, cu):
+def _run(order, q, k, v, do, c, cu, compact=False):
     os.environ["ATTN_GRID_ORDER"] = ",".join(f"{n}:{order}" for n in KERNELS)
     try:
         # zero-filled outputs: rows past a sequence are not written and stay equal
-        o, lse = forward(q, k, v, c, True, cu, cu, out=torch.zeros_like(q),
+        o, lse = forward(q, k, v, c, True, cu, cu, compact=compact, out=torch.zeros_like(q),
                          lse=torch.zeros(q.shape[:3], dtype=torch.float32, device=DEV))
         out = {"o": o, "lse": lse}
         for det in (False, True):
             ws = bwd_workspace(q)
             g = [torch.zeros_like(t) for t in (q, k, v)]
-            backward(q, k, v, o, lse, do, c, True, cu, cu, dq=g[0], dk=g[1], dv=g[2],
-                     workspace=ws, deterministic=det)
+            backward(q, k, v, o, lse, do, c, True, cu, cu, compact=compact, dq=g[0], dk=g[1],
+                     dv=g[2], workspace=ws, deterministic=det)
             torch.cuda.synchronize()
             assert _lib.attn_read_device_status(ws) == 0
             out["det" if det else "reg"] = g
@@ -58,3 +58,22 @@ def test_orders_agree(D, padded):
     g_r = ref.bwd_bhsd(*(np64(x[n]) for n in ("q", "k", "v", "do")), wl.sm_scale, True, cun, cun)
     for g in (a["reg"], b["reg"]):
         assert_grads_close(tuple(g), g_r, what=f"grid order D={D}")
+
+
+def test_orders_agree_compact():
+    wl = WORKLOADS["compact"].replace(H=2, D=64, causal=True, n_seqs=4, seed=97)
+    x = make_inputs(wl, lengths=[700, 1, 300, 513])
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    cu = x["cu_seqlens_q"].to(DEV)
+    a = _run("seq", q, k, v, do, wl.sm_scale, cu, compact=True)
+    b = _run("tile", q, k, v, do, wl.sm_scale, cu, compact=True)
+    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
+    for i in (1, 2):
+        assert torch.equal(a["reg"][i], b["reg"][i])
+    for i in range(3):
+        assert torch.equal(a["det"][i], b["det"][i])
+    cun = x["cu_seqlens_q"].numpy()
+    g_r = ref.bwd_compact_varlen(*(np64(x[n]) for n in ("q", "k", "v", "do")), cun, cun,
+                                 wl.sm_scale, True)
+    for g in (a["reg"], b["reg"]):
+        assert_grads_close(tuple(g), g_r, what="grid order compact")
