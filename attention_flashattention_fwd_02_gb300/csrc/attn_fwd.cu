@@ -33,8 +33,8 @@
 // d_head 256: O alone takes 256 columns, so a CTA owns one query tile (NQ = 1, 128 rows) and
 // two score buffers; Q, one K and one V stage (64 KB each) fill shared memory. K_j is
 // released as soon as its score product has completed and V_j once its PV product has, and
-// each has a producer warp of its own, so K_{j+1} streams in while PV_j runs and V_{j+1}
-// while S_{j+2} runs.
+// each has a producer warp of its own: K_{j+1} streams in while the softmax of S_j and
+// PV_{j-1} run, V_{j+1} while S_{j+2} runs.
 //
 // Online softmax in base 2 with a lazy rescale: a row's reference maximum m only moves when
 // a new row maximum exceeds it by more than 8 (so p <= 2^8); O and l are rescaled by
