@@ -80,6 +80,26 @@ def _cu(lengths: torch.Tensor) -> torch.Tensor:
     return cu.to(torch.int32)
 
 
+def _generator(wl: Workload, seed: Optional[int]) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(wl.seed if seed is None else seed)
+    return g
+
+
+def _draw_lengths(wl: Workload, g: torch.Generator) -> Optional[torch.Tensor]:
+    """The varlen lengths: the first draw from the workload's generator (None if dense)."""
+    if wl.layout == "compact":
+        return torch.randint(wl.len_lo, wl.len_hi + 1, (wl.n_seqs,), generator=g)
+    if wl.layout == "padded":
+        return torch.randint(wl.len_lo, wl.len_hi + 1, (wl.B,), generator=g)
+    return None
+
+
+def draw_lengths(wl: Workload, seed: Optional[int] = None) -> Optional[torch.Tensor]:
+    """The lengths make_inputs draws for a varlen workload, without drawing the tensors."""
+    return _draw_lengths(wl, _generator(wl, seed))
+
+
 def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None, dtype=torch.bfloat16):
     """Draw the inputs of workload ``wl`` on the CPU.
 
@@ -89,13 +109,12 @@ def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None, dtype=to
     varlen lengths instead of drawing them (edge-case tests). ``dtype`` is the 16-bit element
     type the fp32 draws are rounded to (bf16 or fp16).
     """
-    g = torch.Generator(device="cpu")
-    g.manual_seed(wl.seed if seed is None else seed)
+    g = _generator(wl, seed)
     out = {}
     B, H, D = wl.B, wl.H, wl.D
     if wl.layout == "compact":
         if lengths is None:
-            lengths = torch.randint(wl.len_lo, wl.len_hi + 1, (wl.n_seqs,), generator=g)
+            lengths = _draw_lengths(wl, g)
         lengths = torch.as_tensor(lengths, dtype=torch.int64)
         T = int(lengths.sum())
         thd = [_randn16((T, H, D), g, dtype) for _ in range(4)]
@@ -104,7 +123,7 @@ def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None, dtype=to
         out.update(cu_seqlens_q=cu, cu_seqlens_k=cu.clone(), lengths=lengths)
     elif wl.layout == "padded":
         if lengths is None:
-            lengths = torch.randint(wl.len_lo, wl.len_hi + 1, (B,), generator=g)
+            lengths = _draw_lengths(wl, g)
         lengths = torch.as_tensor(lengths, dtype=torch.int64)
         q = _randn16((B, H, wl.Sq, D), g, dtype)
         k = _randn16((B, H, wl.Sk, D), g, dtype)

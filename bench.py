@@ -275,7 +275,7 @@ def run_ours(args, rank, world, dist, clocks_on=True):
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) inputs rounded to bf16)",
-        "config": workload_config(args.workload, variants),
+        "config": workload_config(args.workload),
         "roofline": {"bound": "tensor", "kernel": "attn_" + dominant, "achieved": round(achieved, 2),
                      "peak": peak_b, "unit": "TFLOP/s", "frac": round(achieved / peak_b, 4),
                      "peak_source": f"{peak_src} bf16 burst", "traffic": traffic,
@@ -313,13 +313,16 @@ def load_traffic(workload, dominant):
         return None
 
 
-def workload_config(name, variants):
-    wl = variants[0]["wl"]
+def workload_config(name):
+    """The workload a bench line is quoted on; both arms report this same object."""
+    from attention_flashattention_fwd_02_gb300.workloads import WORKLOADS, draw_lengths
+    wls = [WORKLOADS[n] for n in BENCH_WORKLOADS[name]]
+    wl = wls[0]
     cfg = {"workload": name, "B": wl.B, "H": wl.H, "d_head": wl.D,
-           "masks": ["causal" if vt["wl"].causal else "non-causal" for vt in variants],
+           "masks": ["causal" if w.causal else "non-causal" for w in wls],
            "layout": wl.layout, "l2": "flushed before every step (256 MiB write)"}
     if wl.layout in ("compact", "padded"):
-        cfg["lengths"] = [int(n) for n in variants[0]["x"]["lengths"]]
+        cfg["lengths"] = [int(n) for n in draw_lengths(wl)]
         if wl.layout == "padded":
             cfg["S_max"] = wl.Sq
     else:
@@ -493,7 +496,7 @@ def run_reference(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / max(1, args.steps) * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload},
+        "config": workload_config(args.workload),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,

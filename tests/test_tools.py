@@ -21,3 +21,22 @@ def test_tune_from_stored_sweep_without_gpu(tmp_path, capsys):
     tune_grid_order.main(["--from-json", sweep, "--out", str(out)])
     assert out.exists()
     assert "max_tile_major_bytes" in capsys.readouterr().out
+
+
+@pytest.mark.parametrize("name", ["compact", "padded"])
+def test_draw_lengths_matches_make_inputs(name):
+    """The bench's config (both arms) reports the lengths the inputs are drawn with."""
+    from attention_flashattention_fwd_02_gb300.workloads import WORKLOADS, draw_lengths, make_inputs
+    wl = WORKLOADS[name].replace(H=1, D=8)  # same seed and lengths, small tensors
+    assert draw_lengths(wl).tolist() == make_inputs(wl)["lengths"].tolist()
+
+
+def test_bench_config_identical_for_both_arms():
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    cfg = bench.workload_config("dense2048")
+    assert cfg["workload"] == "dense2048" and cfg["masks"] == ["non-causal", "causal"]
+    assert cfg["seqlen_q"] == cfg["seqlen_k"] == 2048 and cfg["d_head"] == 64
+    assert len(bench.workload_config("compact")["lengths"]) == 16
