@@ -431,24 +431,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// 2^x on the FMA pipe, for x in [-125, 127] (inputs below -125 are clamped there, so the
-// result is never exactly 0: callers use it only where no element is masked to -inf).
-// Range reduction x = n + f with n = rint(x) (the 1.5 * 2^23 shifter puts n in the low
-// mantissa bits) and f in [-1/2, 1/2]; 2^f from a cubic fitted here by iteratively
-// reweighted least squares on the relative error (max relative error 7.6e-5, well below
-// bf16's 2^-9 rounding of P); 2^n enters by adding n to the exponent field.
-__device__ __forceinline__ float ex2_poly(float x) {
-  x = fmaxf(x, -125.f);
-  const float shifter = 12582912.f;
-  const float t = __fadd_rn(x, shifter);
-  const float f = __fsub_rn(x, __fsub_rn(t, shifter));
-  float p = fmaf(0.05517047643661499f, f, 0.2426084578037262f);
-  p = fmaf(p, f, 0.6932609677314758f);
-  p = fmaf(p, f, 0.9999282360076904f);
-  const int n = __float_as_int(t) - 0x4B400000;
-  return __int_as_float(__float_as_int(p) + (n << 23));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
