@@ -28,22 +28,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
-
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t.reg .b32 r;\n\t"
-      "elect.sync r|P, 0xffffffff;\n\t"
-      "selp.u32 %0, 1, 0, P;\n\t}\n"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 // --------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -119,15 +103,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
 // 2-D tiled reduce-add (fp32) of a shared-memory tile into global memory, bulk-group
 // completion. The tile uses the tensor map's layout (here: 128-byte swizzle).
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int c0,
@@ -170,28 +145,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc)^T, bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D(tmem) (+)= A(tmem) * B(smem desc)^T.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Warp-collective forms of the two MMA shapes and of the commit: every lane of the warp
 // executes them with the same (warp-uniform) operands and elect.sync picks the one lane that
 // issues. elect.sync with a full mask always elects the same lane, so the MMAs and the commits
@@ -226,22 +179,12 @@ __device__ __forceinline__ void umma_commit_w(uint32_t bar) {
       : "memory");
 }
 
-// Arrive (once) on `bar` when every tcgen05 operation issued so far by this thread is done.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
 // Instruction descriptor, kind::f16 with fp32 D; A and B are both bf16 (f16 == false) or
 // both fp16 (f16 == true). a_mn / b_mn select the MN-major ("transposed") operand layouts.
 __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn, bool b_mn, bool f16) {
   return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
          ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
-}
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return idesc_f32acc(M, N, a_mn, b_mn, false);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
@@ -354,17 +297,6 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int 
         "=r"(rd[24]), "=r"(rd[25]), "=r"(rd[26]), "=r"(rd[27]), "=r"(rd[28]), "=r"(rd[29]), \
         "=r"(rd[30]), "=r"(rd[31]) \
       : "r"(ta), "r"(tb), "r"(tc), "r"(td) \
-      : "memory")
-
-#define ATTN_TMEM_LD_X16(taddr, r)                                                            \
-  asm volatile(                                                                             \
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
-      "%14,%15}, [%16];\n\t"                                                                  \
-      "tcgen05.wait::ld.sync.aligned;"                                                        \
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),   \
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),             \
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                                                 \
-      : "r"(taddr)                                                                            \
       : "memory")
 
 #define ATTN_TMEM_ST_X16(taddr, r)                                                            \
