@@ -57,6 +57,16 @@
  * The word is sticky: kernels only ever set it, so the caller zeroes it once when the
  * workspace is allocated, and attn_read_device_status clears it after reading. A sequence
  * whose cu_seqlens are inconsistent is skipped, never read out of bounds.
+ *
+ * Environment. The library reads three variables, none needed in normal use:
+ *   ATTN_GRID_ORDER="<kernel>:tile|seq[,...]" forces the CTA order of a kernel's causal grids
+ *     (kernel = fwd, bwd_main, bwd_main_nodq or bwd_dq); otherwise the order comes from a
+ *     table measured on GB300 (the sweep that writes the table sets it). Results do not
+ *     depend on the order.
+ *   ATTN_TEST_WITHHOLD_KV_TILE=j / ATTN_TEST_WITHHOLD_Q_STEP=i (failure-detection tests):
+ *     the forward never loads key tile j / the backward never loads query step i, and every
+ *     wait gives up after 50 ms, so the call ends with ATTN_ERR_DEVICE_TIMEOUT in the status
+ *     word instead of hanging.
  */
 #ifndef ATTN_SM103_ATTN_H_
 #define ATTN_SM103_ATTN_H_
