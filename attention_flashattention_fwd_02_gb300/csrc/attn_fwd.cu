@@ -529,7 +529,14 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full[bsel]));
     }
-    if (n > 0) {  // PV_t(n-1), exact as above: PV_t(n-3) has completed and no PV_t follows it
+    if (n > 0) {
+      // PV_t(n-1) last. Its wait needs PV_t(n-3) complete, which S_t(n-1) in TMEM does not
+      // imply where the two issuing warps run one query tile's consecutive score tiles (it
+      // implies PV(k - 3) only); PV_t(n-2) first, whose wait needs PV_t(n-4) = PV(<= k - 3).
+      // No PV_t follows either, so neither barrier can run a phase ahead.
+      if (ok && n > 1)
+        ok = mbar_wait(smem_u32(&bars.o_done[t][(n - 2) & 1]), ((n - 2) >> 1) & 1, abort,
+                       p.timeout_ns);
       if (ok) ok = mbar_wait(smem_u32(&bars.o_done[t][(n - 1) & 1]), ((n - 1) >> 1) & 1, abort,
                              p.timeout_ns);
       tc_fence_after();
