@@ -1,0 +1,284 @@
+"""A model of the backward key-tile kernel's pipeline (no GPU): are its mbarrier waits exact,
+and do its buffers never get overwritten while read, nor read before written?
+
+A wait on a parity is exact only if, when it starts, the barrier has completed either the
+phase before the target or the target itself, and it cannot complete two more phases before
+the waiter sees the flip. The roles of the kernel, with the same waits, arrivals and commits
+in the same order, run as coroutines tick by tick with random durations over an in-order
+tensor pipe (a commit arrives when every product issued before it has completed):
+  producer     Q / dO / LSE / Delta of step it into stage it mod QST after q_empty
+  MMA warp     S/dP(it+1) after s_free(it); dV(it) after p_full(it), commit p_empty;
+               dK(it) after ds_full; dQ(it) after dq_empty(it-1); commit ds_empty, q_empty,
+               dq_full
+  warpgroups   (two, arriving independently) wait s_full, q_full, ds_empty(it-2); read
+               S^T/dP^T, arrive s_free; wait p_empty(it-1); write P^T, arrive p_full; write
+               dS^T, arrive ds_full; drain dQ(it-1): wait dq_full, read it, arrive dq_empty
+Buffers (the Q/dO stages, TMEM S^T/dP^T, P^T and dQ, the two dS^T buffers) carry the step
+whose contents they hold: a read must find its step's contents completely written, and a
+write must come after every read of the contents it replaces has completed.
+"""
+import random
+
+import pytest
+
+
+class Sim:
+    def __init__(self, rng):
+        self.rng = rng
+        self.count, self.arrivals, self.expected = {}, {}, {}
+        self.pipe, self.pipe_i, self.cur, self.busy_until = [], 0, None, 0
+        self.content = {}  # buffer -> [step, write end tick, {reader: end tick or None}]
+        self.readers = {}  # buffer -> set of reader names every content must see
+        self.violations = []
+        self.tick = 0
+
+    # ------------------------------------------------------------------ barriers
+    def barrier(self, name, expected):
+        self.count[name], self.arrivals[name], self.expected[name] = 0, 0, expected
+
+    def arrive(self, name):
+        self.arrivals[name] += 1
+        if self.arrivals[name] == self.expected[name]:
+            self.arrivals[name] = 0
+            self.count[name] += 1
+
+    # ------------------------------------------------------------------ buffers
+    def buffer(self, name, readers):
+        self.readers[name] = set(readers)
+        self.content[name] = None
+
+    def write(self, buf, step, end):
+        cur = self.content[buf]
+        if cur is not None:
+            pending = [r for r in self.readers[buf]
+                       if cur[2].get(r) is None or cur[2][r] > self.tick]
+            if pending:
+                self.violations.append(("overwrite", buf, cur[0], step, tuple(sorted(pending))))
+        self.content[buf] = [step, end, {}]
+
+    def read(self, buf, step, who, end):
+        cur = self.content[buf]
+        if cur is None or cur[0] != step or cur[1] > self.tick:
+            self.violations.append(("stale read", buf, step, who, None if cur is None else cur[0]))
+            return
+        cur[2][who] = end
+
+    # ------------------------------------------------------------------ tensor pipe
+    def step_pipe(self):
+        while True:
+            if self.cur is not None:
+                if self.tick < self.busy_until:
+                    return
+                if self.cur[0] == "commit":
+                    self.arrive(self.cur[1])
+                self.cur = None
+            if self.pipe_i >= len(self.pipe):
+                return
+            self.cur = self.pipe[self.pipe_i]
+            self.pipe_i += 1
+            if self.cur[0] == "commit":
+                self.busy_until = self.tick
+                continue
+            _, who, reads, writes = self.cur
+            self.busy_until = self.tick + self.rng.randint(1, 6)
+            for buf, step in reads:
+                self.read(buf, step, who, self.busy_until)
+            for buf, step in writes:
+                self.write(buf, step, self.busy_until)
+
+    def run(self, agents, max_ticks=100000):
+        """agents: generators yielding ('wait', bar, phase), ('arrive', bar), ('delay', n),
+        ('mma', who, reads, writes), ('commit', bar), ('read', buf, step, who, ticks) or
+        ('write', buf, step[, ticks])."""
+        state = [{"gen": g, "pending": None, "until": 0, "done": False} for g in agents]
+        for self.tick in range(max_ticks):
+            self.step_pipe()
+            for a in state:
+                while not a["done"]:
+                    p = a["pending"]
+                    if p is not None:
+                        if p[0] == "delay":
+                            if self.tick < a["until"]:
+                                break
+                        elif p[0] == "wait":
+                            c = self.count[p[1]]
+                            if c < p[2] + 1:
+                                break
+                            if c != p[2] + 1:
+                                self.violations.append(("missed phase", p[1], p[2], c))
+                        a["pending"] = None
+                    try:
+                        act = next(a["gen"])
+                    except StopIteration:
+                        a["done"] = True
+                        break
+                    kind = act[0]
+                    if kind == "wait":
+                        c = self.count[act[1]]
+                        if c not in (act[2], act[2] + 1):
+                            self.violations.append(("wait start", act[1], act[2], c))
+                        a["pending"] = act
+                        break
+                    if kind == "delay":
+                        a["pending"], a["until"] = act, self.tick + act[1]
+                        break
+                    if kind == "arrive":
+                        self.arrive(act[1])
+                    elif kind in ("mma", "commit"):
+                        self.pipe.append(act)
+                    elif kind == "read":  # a read that takes act[4] ticks (a TMEM load)
+                        self.read(act[1], act[2], act[3], self.tick + act[4])
+                        a["pending"], a["until"] = ("delay",), self.tick + act[4]
+                        break
+                    elif kind == "write":  # completes after act[3] ticks (a TMA copy)
+                        self.write(act[1], act[2], self.tick + (act[3] if len(act) > 3 else 0))
+            if all(a["done"] for a in state) and self.pipe_i >= len(self.pipe) \
+                    and self.cur is None:
+                return self.violations
+        self.violations.append(("no progress",))
+        return self.violations
+
+
+def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True):
+    """The kernel's roles; `skip` names waits to leave out (to check that the model sees
+    what they prevent); ds_empty=False drops the dS-buffer release (the commit after dK / dQ
+    and the wait for it before the buffer is rewritten two steps later)."""
+    sim.barrier("kv_full", 1)
+    for st in range(qst):
+        sim.barrier(f"q_full{st}", 1)
+        sim.barrier(f"q_empty{st}", 1)
+    for b in range(2):
+        sim.barrier(f"ds_full{b}", 2)
+        sim.barrier(f"ds_empty{b}", 1)
+    for name, n in (("s_full", 1), ("s_free", 2), ("p_full", 2), ("p_empty", 1),
+                    ("dq_full", 1), ("dq_empty", 2), ("dkdv_full", 1)):
+        sim.barrier(name, n)
+    wg = ("wg0", "wg1")
+    for st in range(qst):  # Q / dO stage: the products of its step, and the LSE rows
+        sim.buffer(f"QS{st}", ("SdP", "dV", "dK") + wg)
+    sim.buffer("SDP", wg)
+    sim.buffer("P", ("dV",))
+    for b in range(2):
+        sim.buffer(f"DS{b}", ("dK", "dQ") if with_dq else ("dK",))
+    sim.buffer("DQ", wg)
+
+    def wait(bar, phase):
+        if bar.rstrip("0123456789") not in skip:
+            yield ("wait", bar, phase)
+
+    def producer():
+        yield ("delay", rng.randint(0, 5))
+        sim.arrive("kv_full")
+        for it in range(n_steps):
+            st = it % qst
+            if it >= qst:
+                yield from wait(f"q_empty{st}", it // qst - 1)
+            land = rng.randint(1, 8)  # TMA copies and the LSE / Delta rows land
+            yield ("write", f"QS{st}", it, land)
+            yield ("delay", land)
+            yield ("arrive", f"q_full{st}")
+
+    def mma():
+        yield from wait("kv_full", 0)
+
+        def issue_sdp(it):
+            st = it % qst
+            yield from wait(f"q_full{st}", it // qst)
+            yield ("mma", "SdP", [(f"QS{st}", it)], [("SDP", it)])
+            yield ("commit", "s_full")
+
+        yield from issue_sdp(0)
+        for it in range(n_steps):
+            st, bs = it % qst, it & 1
+            if it + 1 < n_steps:
+                yield from wait("s_free", it)
+                yield from issue_sdp(it + 1)
+            yield from wait("p_full", it)
+            yield ("mma", "dV", [("P", it), (f"QS{st}", it)], [])
+            yield ("commit", "p_empty")
+            yield from wait(f"ds_full{bs}", it >> 1)
+            yield ("mma", "dK", [(f"DS{bs}", it), (f"QS{st}", it)], [])
+            if with_dq:
+                if it > 0:
+                    yield from wait("dq_empty", it - 1)
+                yield ("mma", "dQ", [(f"DS{bs}", it)], [("DQ", it)])
+            if ds_empty:
+                yield ("commit", f"ds_empty{bs}")
+            yield ("commit", f"q_empty{st}")
+            if with_dq:
+                yield ("commit", "dq_full")
+        yield ("commit", "dkdv_full")
+
+    def warpgroup(me):
+        def drain(itd):
+            yield from wait("dq_full", itd)
+            yield ("read", "DQ", itd, me, rng.randint(1, 4))
+            yield ("arrive", "dq_empty")
+            yield ("delay", rng.randint(0, 4))  # staging and the reduce-add
+
+        for it in range(n_steps):
+            st, bs = it % qst, it & 1
+            yield from wait("s_full", it)
+            yield from wait(f"q_full{st}", it // qst)
+            if ds_empty and it >= 2:
+                yield from wait(f"ds_empty{bs}", (it >> 1) - 1)
+            yield ("read", "SDP", it, me, rng.randint(1, 4))
+            yield ("read", f"QS{st}", it, me, 0)
+            yield ("delay", rng.randint(0, 3))
+            yield ("arrive", "s_free")
+            if it > 0:
+                yield from wait("p_empty", it - 1)
+            yield ("delay", rng.randint(1, 10))  # P and dS
+            if me == "wg0":  # one write event stands for both warpgroups' halves
+                yield ("write", "P", it)
+            yield ("arrive", "p_full")
+            # dS^T was stored with P^T, but the MMAs (async proxy) see it only after the
+            # proxy fence that precedes the ds_full arrival
+            yield ("delay", rng.randint(0, 8))
+            if me == "wg0":
+                yield ("write", f"DS{bs}", it)
+            yield ("arrive", f"ds_full{bs}")
+            if with_dq and it > 0:
+                yield from drain(it - 1)
+        if with_dq and n_steps > 0:
+            yield from drain(n_steps - 1)
+        yield from wait("dkdv_full", 0)
+
+    return [producer(), mma(), warpgroup("wg0"), warpgroup("wg1")]
+
+
+@pytest.mark.parametrize("n_steps", [1, 2, 3, 4, 7])
+@pytest.mark.parametrize("qst", [2, 3])
+@pytest.mark.parametrize("with_dq", [True, False])
+def test_backward_pipeline_is_exact_and_race_free(n_steps, qst, with_dq):
+    rng = random.Random(n_steps * 10 + qst + 100 * with_dq)
+    for _ in range(150):
+        sim = Sim(rng)
+        assert sim.run(backward_protocol(sim, n_steps, qst, with_dq, rng)) == []
+
+
+@pytest.mark.parametrize("dropped,kind", [
+    ("s_full", "stale read"), ("s_free", "overwrite"), ("p_full", "stale read"),
+    ("p_empty", "overwrite"), ("ds_full", "stale read"), ("q_full", "stale read"),
+    ("q_empty", "overwrite"), ("dq_full", "stale read"), ("dq_empty", "overwrite")])
+def test_model_catches_a_missing_wait(dropped, kind):
+    """Each of these waits protects something: without it the model must report a violation
+    of the kind that wait prevents."""
+    rng = random.Random(5)
+    found = []
+    for _ in range(300):
+        sim = Sim(rng)
+        found += sim.run(backward_protocol(sim, 6, 3, True, rng, skip=(dropped,)))
+    assert any(v[0] == kind for v in found), found[:3]
+
+
+@pytest.mark.parametrize("qst", [2, 3])
+def test_ds_release_is_implied(qst):
+    """The dS-buffer release adds nothing: the warpgroups write dS(it+2) only after
+    s_full(it+2), whose commit follows dK(it) and dQ(it) in the MMA warp's issue order and so
+    arrives only once those readers of the buffer have completed. Without the release the
+    protocol stays exact and race-free."""
+    rng = random.Random(9 + qst)
+    for _ in range(300):
+        sim = Sim(rng)
+        assert sim.run(backward_protocol(sim, 6, qst, True, rng, ds_empty=False)) == []
