@@ -21,122 +21,7 @@ import random
 
 import pytest
 
-
-class Sim:
-    def __init__(self, rng):
-        self.rng = rng
-        self.count, self.arrivals, self.expected = {}, {}, {}
-        self.pipe, self.pipe_i, self.cur, self.busy_until = [], 0, None, 0
-        self.content = {}  # buffer -> [step, write end tick, {reader: end tick or None}]
-        self.readers = {}  # buffer -> set of reader names every content must see
-        self.violations = []
-        self.tick = 0
-
-    # ------------------------------------------------------------------ barriers
-    def barrier(self, name, expected):
-        self.count[name], self.arrivals[name], self.expected[name] = 0, 0, expected
-
-    def arrive(self, name):
-        self.arrivals[name] += 1
-        if self.arrivals[name] == self.expected[name]:
-            self.arrivals[name] = 0
-            self.count[name] += 1
-
-    # ------------------------------------------------------------------ buffers
-    def buffer(self, name, readers):
-        self.readers[name] = set(readers)
-        self.content[name] = None
-
-    def write(self, buf, step, end):
-        cur = self.content[buf]
-        if cur is not None:
-            pending = [r for r in self.readers[buf]
-                       if cur[2].get(r) is None or cur[2][r] > self.tick]
-            if pending:
-                self.violations.append(("overwrite", buf, cur[0], step, tuple(sorted(pending))))
-        self.content[buf] = [step, end, {}]
-
-    def read(self, buf, step, who, end):
-        cur = self.content[buf]
-        if cur is None or cur[0] != step or cur[1] > self.tick:
-            self.violations.append(("stale read", buf, step, who, None if cur is None else cur[0]))
-            return
-        cur[2][who] = end
-
-    # ------------------------------------------------------------------ tensor pipe
-    def step_pipe(self):
-        while True:
-            if self.cur is not None:
-                if self.tick < self.busy_until:
-                    return
-                if self.cur[0] == "commit":
-                    self.arrive(self.cur[1])
-                self.cur = None
-            if self.pipe_i >= len(self.pipe):
-                return
-            self.cur = self.pipe[self.pipe_i]
-            self.pipe_i += 1
-            if self.cur[0] == "commit":
-                self.busy_until = self.tick
-                continue
-            _, who, reads, writes = self.cur
-            self.busy_until = self.tick + self.rng.randint(1, 6)
-            for buf, step in reads:
-                self.read(buf, step, who, self.busy_until)
-            for buf, step in writes:
-                self.write(buf, step, self.busy_until)
-
-    def run(self, agents, max_ticks=100000):
-        """agents: generators yielding ('wait', bar, phase), ('arrive', bar), ('delay', n),
-        ('mma', who, reads, writes), ('commit', bar), ('read', buf, step, who, ticks) or
-        ('write', buf, step[, ticks])."""
-        state = [{"gen": g, "pending": None, "until": 0, "done": False} for g in agents]
-        for self.tick in range(max_ticks):
-            self.step_pipe()
-            for a in state:
-                while not a["done"]:
-                    p = a["pending"]
-                    if p is not None:
-                        if p[0] == "delay":
-                            if self.tick < a["until"]:
-                                break
-                        elif p[0] == "wait":
-                            c = self.count[p[1]]
-                            if c < p[2] + 1:
-                                break
-                            if c != p[2] + 1:
-                                self.violations.append(("missed phase", p[1], p[2], c))
-                        a["pending"] = None
-                    try:
-                        act = next(a["gen"])
-                    except StopIteration:
-                        a["done"] = True
-                        break
-                    kind = act[0]
-                    if kind == "wait":
-                        c = self.count[act[1]]
-                        if c not in (act[2], act[2] + 1):
-                            self.violations.append(("wait start", act[1], act[2], c))
-                        a["pending"] = act
-                        break
-                    if kind == "delay":
-                        a["pending"], a["until"] = act, self.tick + act[1]
-                        break
-                    if kind == "arrive":
-                        self.arrive(act[1])
-                    elif kind in ("mma", "commit"):
-                        self.pipe.append(act)
-                    elif kind == "read":  # a read that takes act[4] ticks (a TMEM load)
-                        self.read(act[1], act[2], act[3], self.tick + act[4])
-                        a["pending"], a["until"] = ("delay",), self.tick + act[4]
-                        break
-                    elif kind == "write":  # completes after act[3] ticks (a TMA copy)
-                        self.write(act[1], act[2], self.tick + (act[3] if len(act) > 3 else 0))
-            if all(a["done"] for a in state) and self.pipe_i >= len(self.pipe) \
-                    and self.cur is None:
-                return self.violations
-        self.violations.append(("no progress",))
-        return self.violations
+from _pipeline_sim import Sim
 
 
 def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True):

@@ -1,22 +1,27 @@
-"""A model of the forward kernel's MMA / softmax pipeline (no GPU): are the parity waits on the
-O-completion barriers exact?
+"""A model of the forward kernel's pipeline (no GPU): are its mbarrier waits exact, and are
+its buffers never overwritten while read, nor read before written?
 
-An mbarrier wait on a parity only tells the two most recent phases apart, so it is correct
-only while the barrier is within one phase of the waited one. The kernel's softmax warps wait
-for PV_t(j-1) before a rescale, and for PV_t(n-2) and then PV_t(n-1) before the epilogue.
-This test runs the kernel's issue schedules tick by tick with random durations:
-  - one MMA-issuing warp (d_head 128 and 256): S(0), S(1), then PV(k), S(k + 2);
-  - two issuing warps (d_head 64): S(k) after PV(k - 3) has completed, PV(k) after P(k);
-  - two query tiles with equal or unequal key-tile counts, or one (d_head 256);
-and an in-order tensor pipe. At every wait it checks that the parity check passes only once
-the waited product has really completed, for the kernel's scheme (two barriers per query
-tile, one per parity of the key-tile index j) and for the two earlier schemes, which the model
-must catch failing: one barrier per query tile, and the per-parity barriers with a single
-epilogue wait.
+The roles of attn_fwd_kernel run as coroutines (tests/_pipeline_sim.py) with the kernel's
+waits, arrivals and commits, in its order, for the three configurations:
+  d_head 64    two query tiles, 3 score buffers, 4 K/V stages, S and PV issued by two warps
+               (S(k) after buf_free: PV(k - 3) complete), optional bias slots
+  d_head 128   two query tiles, 2 score buffers, 2 K/V stages, one issuing warp:
+               S(0), S(1), then PV(k), S(k + 2)
+  d_head 256   one query tile, 2 score buffers, 1 K and 1 V stage released separately
+               (K after its score product, V after its PV) by two producer warps
+Buffers: the K and V stages (contents: key tile j), the score / P TMEM buffers (S(k) written
+by the MMA and read by the softmax warps; P(k) written by them and read by PV(k)), each query
+tile's O accumulator (contents: how many PVs it holds; read and rewritten by a rescale, read
+by the epilogue) and the bias slots. O completion uses the kernel's scheme, two barriers per
+query tile (one per parity of the key-tile index j), with the epilogue waiting for PV_t(n-2)
+and then PV_t(n-1). The earlier schemes must be caught: one barrier per tile, a single
+epilogue wait, and bias slots shared by the two tiles.
 """
 import random
 
 import pytest
+
+from _pipeline_sim import Sim
 
 
 class Order:
@@ -38,137 +43,229 @@ class Order:
         return (k >> 1) if k < 2 * self.n_min else k - self.n_min
 
 
-def simulate(n0, n1, nsb, split, scheme, rng, max_ticks=20000):
-    """Returns a list of violations (empty when every wait was exact)."""
+CONFIGS = {  # score buffers, K/V stages, split issue, split K/V release
+    64: (3, 4, True, False),
+    128: (2, 2, False, False),
+    256: (2, 1, False, True),
+}
+
+
+def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_slots="tile",
+                     skip=(), copy_ticks=(1, 8)):
+    """copy_ticks: range of a TMA copy's duration."""
+    nsb, nst, split, split_kv = CONFIGS[D]
     od = Order(n0, n1)
-    total = od.total
-    published, done = set(), set()
-    queue, qi = [], 0
-    cur, busy_until = None, 0
+    n, total, n_max = od.n, od.total, max(n0, n1)
 
-    # issuer programs: lists of (op, k); preconditions checked each tick
-    if split:
-        progs = [[("S", k) for k in range(total)], [("PV", k) for k in range(total)]]
-    else:
-        prog = [("S", k) for k in range(min(nsb, total))]
+    def wait(bar, phase):
+        if bar.rstrip("0123456789_") not in skip:
+            yield ("wait", bar, phase)
+
+    sim.barrier("q_full", 1)
+    for st in range(nst):
+        for b in ("k_full", "v_full", "kv_empty", "k_empty"):
+            sim.barrier(f"{b}{st}", 1)
+        sim.buffer(f"KS{st}", lambda j: {f"S{t}" for t in (0, 1) if j < n[t]})
+        sim.buffer(f"VS{st}", lambda j: {f"PV{t}" for t in (0, 1) if j < n[t]})
+    for b in range(nsb):
+        for name, cnt in (("s_full", 1), ("p_full", 1), ("buf_free", 1)):
+            sim.barrier(f"{name}{b}", cnt)
+        # S(k) is read by its tile's softmax warps, P(k) by PV(k)
+        sim.buffer(f"SP{b}", lambda c: {("sm" if c[0] == "S" else "PV") + str(od.t_of(c[1]))})
+    for t in range(2):
+        for b in range(2):
+            sim.barrier(f"o_done{t}_{b}", 1)
+        sim.barrier(f"o_one{t}", 1)
+        sim.barrier(f"b_full{t}", 1)
+        sim.barrier(f"b_empty{t}", 1)
+        sim.buffer(f"O{t}", ())  # checked through its contents (the PVs it holds)
+        sim.buffer(f"BS{t}", lambda c: {f"sm{c[0]}"})
+
+    def o_bar(t, i):
+        """(barrier, phase) that PV_t(i) completes."""
+        if o_scheme == "single":
+            return f"o_one{t}", i
+        return f"o_done{t}_{i & 1}", i >> 1
+
+    def producer():
+        yield ("delay", rng.randint(0, 3))
+        sim.arrive("q_full")
+        for j in range(n_max):
+            st = j % nst
+            if j >= nst:
+                yield from wait(("k_empty" if split_kv else "kv_empty") + str(st), j // nst - 1)
+            land = rng.randint(*copy_ticks)
+            yield ("write", f"KS{st}", j, land)
+            yield ("arrive_after", f"k_full{st}", land)
+            if not split_kv:
+                land = rng.randint(*copy_ticks)
+                yield ("write", f"VS{st}", j, land)
+                yield ("arrive_after", f"v_full{st}", land)
+
+    def v_producer():
+        for j in range(n_max):
+            st = j % nst
+            if j >= nst:
+                yield from wait(f"kv_empty{st}", j // nst - 1)
+            land = rng.randint(*copy_ticks)
+            yield ("write", f"VS{st}", j, land)
+            yield ("arrive_after", f"v_full{st}", land)
+
+    def bias_producer():
         for k in range(total):
-            prog.append(("PV", k))
-            if k + nsb < total:
-                prog.append(("S", k + nsb))
-        progs = [prog]
-    pcs = [0] * len(progs)
+            t, j = od.t_of(k), od.j_of(k)
+            if bias_slots == "tile":
+                slot, phase = t, j
+            else:  # the earlier scheme: slot k mod 2, shared by the tiles
+                slot, phase = k % 2, k // 2
+            if phase >= 1:
+                yield from wait(f"b_empty{slot}", phase - 1)
+            land = rng.randint(*copy_ticks)
+            yield ("write", f"BS{slot}", (t, j), land)
+            yield ("arrive_after", f"b_full{slot}", land)
 
-    def ready(op, k):
-        if op == "PV":
-            return k in published
-        if split and k >= nsb:  # the score buffer is free once PV(k - nsb) has completed
-            return ("PV", k - nsb) in done
-        return True
+    def issue_s(k, seen):
+        t, j = od.t_of(k), od.j_of(k)
+        st, b = j % nst, k % nsb
+        if j != seen[0]:
+            yield from wait(f"k_full{st}", j // nst)
+            seen[0] = j
+        yield ("mma", f"S{t}", [(f"KS{st}", j)], [(f"SP{b}", ("S", k))])
+        yield ("commit", f"s_full{b}")
+        if split_kv:
+            yield ("commit", f"k_empty{st}")
 
-    def pv_done(t, j):
-        return ("PV", od.k_of(t, j)) in done
+    def mma():
+        seen_k, seen_v = [-1], -1
+        if not split:
+            yield from wait("q_full", 0)
+            for k in range(min(nsb, total)):
+                yield from issue_s(k, seen_k)
+        for k in range(total):
+            t, j = od.t_of(k), od.j_of(k)
+            st, b = j % nst, k % nsb
+            if j != seen_v:
+                yield from wait(f"v_full{st}", j // nst)
+                seen_v = j
+            yield from wait(f"p_full{b}", k // nsb)
+            reads = [(f"SP{b}", ("P", k)), (f"VS{st}", j)]
+            if j > 0:  # PV_t(0) overwrites O_t (accumulate off)
+                reads.append((f"O{t}", j))
+            yield ("mma", f"PV{t}", reads, [(f"O{t}", j + 1)])
+            yield ("commit", o_bar(t, j)[0])
+            if split and k + nsb < total:
+                yield ("commit", f"buf_free{b}")
+            if k + 1 == total or od.j_of(k + 1) != j:
+                yield ("commit", f"kv_empty{st}")
+            if not split and k + nsb < total:
+                yield from issue_s(k + nsb, seen_k)
 
-    def barrier_count(t, i):
-        """Completed phases of the barrier that PV_t(i) completes."""
-        if scheme == "single":
-            return sum(pv_done(t, x) for x in range(od.n[t]))
-        return sum(pv_done(t, x) for x in range(i & 1, od.n[t], 2))
+    def s_warp():
+        seen = [-1]
+        yield from wait("q_full", 0)
+        for k in range(total):
+            b = k % nsb
+            if k >= nsb:
+                yield from wait(f"buf_free{b}", (k - nsb) // nsb)
+            yield from issue_s(k, seen)
 
-    def phase_of(i):
-        return i if scheme == "single" else i >> 1
+    def softmax(t):
+        me = f"sm{t}"
+        for j in range(n[t]):
+            k = od.k_of(t, j)
+            b = k % nsb
+            yield from wait(f"s_full{b}", k // nsb)
+            yield ("read", f"SP{b}", ("S", k), me, rng.randint(0, 3))
+            if bias:
+                slot, phase = (t, j) if bias_slots == "tile" else (k % 2, k // 2)
+                yield from wait(f"b_full{slot}", phase)
+                yield ("read", f"BS{slot}", (t, j), me, 0)
+                yield ("arrive", f"b_empty{slot}")
+            yield ("delay", rng.randint(1, 8))  # the exponentials
+            if j > 0 and rng.random() < 0.6:  # the row maximum moved: rescale O_t
+                yield from wait(*o_bar(t, j - 1))
+                yield ("read", f"O{t}", j, me, rng.randint(1, 3))
+                yield ("write", f"O{t}", j)
+            land = rng.randint(0, 2)  # P to TMEM, then tcgen05.wait::st
+            yield ("write", f"SP{b}", ("P", k), land)
+            yield ("delay", land)
+            yield ("arrive", f"p_full{b}")
+        if n[t] == 0:
+            return
+        one = o_scheme in ("single", "parity_one_wait") or n[t] < 2
+        for i in ([n[t] - 1] if one else [n[t] - 2, n[t] - 1]):
+            yield from wait(*o_bar(t, i))
+        yield ("read", f"O{t}", n[t], me, rng.randint(1, 3))
 
-    violations = []
-    sm = [{"j": 0, "state": "wait_s", "until": 0, "rescale": False} for _ in range(2)]
-    for tick in range(max_ticks):
-        # tensor pipe, in issue order
-        if cur is not None and tick >= busy_until:
-            done.add(cur)
-            cur = None
-        if cur is None and qi < len(queue):
-            cur = queue[qi]
-            qi += 1
-            busy_until = tick + rng.randint(1, 12)
-        # issuing warps: one instruction per tick each
-        for p, prog in enumerate(progs):
-            if pcs[p] < len(prog) and ready(*prog[pcs[p]]):
-                queue.append(prog[pcs[p]])
-                pcs[p] += 1
-        # softmax warpgroups
-        for t in range(2):
-            s = sm[t]
-            n = od.n[t]
-            if s["state"] == "done":
-                continue
-            j = s["j"]
-            if s["state"] == "wait_s":
-                if j == n:  # epilogue: PV_t(n-2) then PV_t(n-1) (earlier schemes: n-1 only)
-                    one = scheme in ("single", "parity_one_wait") or n < 2
-                    s["waits"] = [n - 1] if one else [n - 2, n - 1]
-                    s["state"], s["i"] = "wait_o", s["waits"].pop(0)
-                    if n == 0:
-                        s["state"] = "done"
-                    continue
-                if ("S", od.k_of(t, j)) in done:
-                    s["state"], s["until"] = "compute", tick + rng.randint(1, 8)
-                    s["rescale"] = j > 0 and rng.random() < 0.7
-                continue
-            if s["state"] == "compute" and tick >= s["until"]:
-                if s["rescale"]:
-                    s["state"], s["i"] = "wait_o", j - 1
-                else:
-                    published.add(od.k_of(t, j))
-                    s["j"], s["state"] = j + 1, "wait_s"
-                continue
-            if s["state"] == "wait_o":
-                i = s["i"]
-                parity = phase_of(i) & 1
-                c = barrier_count(t, i)
-                if (c & 1) != parity:  # try_wait.parity succeeds
-                    if not pv_done(t, i):
-                        violations.append((t, i, "early"))
-                    if j == n:
-                        if s["waits"]:
-                            s["i"] = s["waits"].pop(0)
-                        else:
-                            s["state"] = "done"
-                    else:
-                        published.add(od.k_of(t, j))
-                        s["j"], s["state"] = j + 1, "wait_s"
-        if all(s["state"] == "done" for s in sm) and len(done) == 2 * total:
-            return violations
-    violations.append((-1, -1, "no progress"))
-    return violations
-
-
-SCHEDULES = [
-    # (n0, n1, score buffers, split issue) as the kernels run them
-    (5, 5, 2, False), (5, 6, 2, False), (6, 0, 2, False), (1, 2, 2, False),  # d_head 128
-    (5, 5, 3, True), (5, 6, 3, True), (6, 0, 3, True), (2, 1, 3, True),      # d_head 64
-    (7, 0, 2, False), (2, 0, 2, False), (1, 0, 2, False),                    # d_head 256
-    (8, 0, 3, True), (3, 4, 3, True), (4, 3, 2, False), (0, 1, 3, True),
-]
+    agents = [producer(), mma(), softmax(0), softmax(1)]
+    if split:
+        agents.append(s_warp())
+    if split_kv:
+        agents.append(v_producer())
+    if bias:
+        agents.append(bias_producer())
+    return agents
 
 
-@pytest.mark.parametrize("n0,n1,nsb,split", SCHEDULES)
-def test_per_parity_barriers_are_exact(n0, n1, nsb, split):
-    rng = random.Random(n0 * 100 + n1 * 10 + nsb + split)
-    for _ in range(600):
-        assert simulate(n0, n1, nsb, split, "parity", rng) == []
+TILES = [(5, 5), (5, 6), (6, 0), (1, 2), (2, 1), (3, 0), (1, 0), (4, 5)]
+CASES = [(D, n0, n1) for D in (64, 128) for n0, n1 in TILES] + \
+        [(256, n0, 0) for n0 in (1, 2, 3, 7)]
 
 
-def test_single_barrier_is_caught():
-    """The scheme the kernel used before: one barrier per query tile. With one query tile and
-    one issuing warp (d_head 256), the epilogue's wait can pass while PV_t(n-2) and PV_t(n-1)
-    are still queued; the model must find such a schedule."""
-    rng = random.Random(7)
-    found = [v for _ in range(500) for v in simulate(6, 0, 2, False, "single", rng)]
-    assert any(kind == "early" for _, _, kind in found)
+SLOW = dict(mma_ticks=(1, 30), copy_ticks=(1, 90))  # long copies and products
+
+
+def _runs(D, n0, n1, seed, trials, slow=False, **kw):
+    rng = random.Random(seed)
+    out = []
+    for _ in range(trials):
+        sim = Sim(rng, mma_ticks=SLOW["mma_ticks"] if slow else (1, 6))
+        if slow:
+            kw = dict(kw, copy_ticks=SLOW["copy_ticks"])
+        out += sim.run(forward_protocol(sim, D, n0, n1, rng, **kw))
+    return out
+
+
+@pytest.mark.parametrize("D,n0,n1", CASES)
+def test_forward_pipeline_is_exact_and_race_free(D, n0, n1):
+    seed = D * 1000 + n0 * 10 + n1
+    assert _runs(D, n0, n1, seed, 120) == []
+    assert _runs(D, n0, n1, seed + 1, 80, slow=True) == []
+
+
+@pytest.mark.parametrize("n0,n1", [(5, 5), (5, 6), (6, 0), (2, 1), (2, 3)])
+def test_bias_forward_pipeline(n0, n1):
+    assert _runs(64, n0, n1, n0 * 10 + n1, 120, bias=True) == []
+    assert _runs(64, n0, n1, n0 * 10 + n1 + 1, 120, slow=True, bias=True) == []
+
+
+def _found(D, n0, n1, trials=400, **kw):
+    """Violations over many runs with long copies and products, which widen the windows a
+    missing or inexact wait leaves open."""
+    return _runs(D, n0, n1, 3, trials, slow=True, **kw)
+
+
+def test_single_o_barrier_is_caught():
+    assert _found(256, 6, 0, o_scheme="single")
+    assert _found(128, 5, 6, o_scheme="single")
 
 
 def test_single_epilogue_wait_is_caught():
-    """Per-parity barriers but one epilogue wait: with two issuing warps (d_head 64) and a
-    single active query tile, S(k) in TMEM implies only PV(k - 3), and the wait for
-    PV_t(n-1) can pass while PV_t(n-3) is still queued."""
-    rng = random.Random(11)
-    found = [v for _ in range(500) for v in simulate(6, 0, 3, True, "parity_one_wait", rng)]
-    assert any(kind == "early" for _, _, kind in found)
+    assert _found(64, 6, 0, o_scheme="parity_one_wait")
+
+
+def test_shared_bias_slots_are_caught():
+    assert _found(64, 5, 6, bias=True, bias_slots="shared")
+
+
+@pytest.mark.parametrize("D,dropped", [
+    (64, "buf_free"), (64, "kv_empty"), (64, "s_full"), (64, "p_full"), (64, "k_full"),
+    (64, "v_full"), (128, "kv_empty"), (128, "p_full"), (256, "k_empty"), (256, "kv_empty"),
+    (256, "v_full")])
+def test_model_catches_a_missing_wait(D, dropped):
+    assert _found(D, 5 if D < 256 else 6, 5 if D < 256 else 0, skip=(dropped,))
+
+
+@pytest.mark.parametrize("dropped", ["b_full", "b_empty"])
+def test_model_catches_a_missing_bias_wait(dropped):
+    assert _found(64, 5, 5, bias=True, skip=(dropped,))
