@@ -224,7 +224,9 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       for (int st = 0; st < NST; ++st) last_j[st] = -1;
       for (int j = 0; j < n_max; ++j) {
         const int st = j % NST;
-        if (j == p.withhold_tile) continue;  // failure-detection test: this stage never fills
+        // failure-detection test: no key tile from this one on is loaded (skipping only this
+        // one would leave the next wait on its stage aiming at a phase that never completes)
+        if (j == p.withhold_tile) break;
         const uint32_t empty = C::SPLIT_KV ? smem_u32(&bars.k_empty[st]) : smem_u32(&bars.kv_empty[st]);
         if (j >= NST && !mbar_wait(empty, ((j / NST) - 1) & 1, abort, p.timeout_ns)) break;
         last_j[st] = j;
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       for (int st = 0; st < NST; ++st) last_j[st] = -1;
       for (int j = 0; j < n_max; ++j) {
         const int st = j % NST;
-        if (j == p.withhold_tile) continue;
+        if (j == p.withhold_tile) break;
         if (j >= NST &&
             !mbar_wait(smem_u32(&bars.kv_empty[st]), ((j / NST) - 1) & 1, abort, p.timeout_ns))
           break;

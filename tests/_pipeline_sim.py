@@ -11,6 +11,12 @@ Agents are generators that yield actions:
                                   before it has completed
   ('read', buf, contents, who, ticks)   read a buffer (a TMEM load, ...) for `ticks` ticks
   ('write', buf, contents[, ticks])     write a buffer, complete after `ticks` (a TMA copy)
+  ('drain', bar, phase)           a wait that ignores the abort flag (leaving after a failure)
+With a timeout, a wait that has not succeeded after `timeout` ticks fails and raises the
+CTA's abort flag; once it is raised every wait fails at once (the agent receives False from
+its yield) and drains still wait. With exit_check, nothing may be in flight when the last
+agent has finished: no product in the tensor pipe, no copy still landing (the CTA would
+release its tensor and shared memory under them).
 Checked: every wait starts with its barrier at the phase before the target or the target
 itself and proceeds exactly one phase past it (a parity wait is exact only then); every read
 finds its contents completely written; every write comes after all reads of the contents it
@@ -20,8 +26,10 @@ the contents).
 
 
 class Sim:
-    def __init__(self, rng, mma_ticks=(1, 6)):
+    def __init__(self, rng, mma_ticks=(1, 6), timeout=None, exit_check=False):
         self.rng = rng
+        self.timeout, self.exit_check, self.abort = timeout, exit_check, False
+        self.write_until = 0  # the last copy's landing tick
         self.mma_ticks = mma_ticks  # range of a product's duration
         self.count, self.arrivals, self.expected = {}, {}, {}
         self.pipe, self.pipe_i, self.cur, self.busy_until = [], 0, None, 0
@@ -54,6 +62,7 @@ class Sim:
             if pending:
                 self.violations.append(("overwrite", buf, cur[0], step, tuple(sorted(pending))))
         self.content[buf] = [step, end, {}]
+        self.write_until = max(self.write_until, end)
 
     def read(self, buf, step, who, end):
         cur = self.content[buf]
@@ -89,7 +98,8 @@ class Sim:
         """agents: generators yielding ('wait', bar, phase), ('arrive', bar), ('delay', n),
         ('mma', who, reads, writes), ('commit', bar), ('read', buf, step, who, ticks) or
         ('write', buf, step[, ticks])."""
-        state = [{"gen": g, "pending": None, "until": 0, "done": False} for g in agents]
+        state = [{"gen": g, "pending": None, "until": 0, "done": False, "send": None}
+                 for g in agents]
         for self.tick in range(max_ticks):
             for due in [x for x in self.later if x[0] <= self.tick]:
                 self.later.remove(due)
@@ -102,24 +112,34 @@ class Sim:
                         if p[0] == "delay":
                             if self.tick < a["until"]:
                                 break
-                        elif p[0] == "wait":
+                        elif p[0] in ("wait", "drain"):
                             c = self.count[p[1]]
+                            a["send"] = True
                             if c < p[2] + 1:
-                                break
-                            if c != p[2] + 1:
+                                timed_out = (self.timeout is not None
+                                             and self.tick - a["since"] >= self.timeout)
+                                if p[0] == "wait" and (self.abort or timed_out):
+                                    self.abort, a["send"] = True, False
+                                elif p[0] == "drain" and timed_out:
+                                    self.violations.append(("drain timed out", p[1], p[2], c))
+                                    a["send"] = False
+                                else:
+                                    break
+                            elif c != p[2] + 1:
                                 self.violations.append(("missed phase", p[1], p[2], c))
                         a["pending"] = None
                     try:
-                        act = next(a["gen"])
+                        act = a["gen"].send(a["send"])
+                        a["send"] = None
                     except StopIteration:
                         a["done"] = True
                         break
                     kind = act[0]
-                    if kind == "wait":
+                    if kind in ("wait", "drain"):
                         c = self.count[act[1]]
                         if c not in (act[2], act[2] + 1):
                             self.violations.append(("wait start", act[1], act[2], c))
-                        a["pending"] = act
+                        a["pending"], a["since"] = act, self.tick
                         break
                     if kind == "delay":
                         a["pending"], a["until"] = act, self.tick + act[1]
@@ -136,6 +156,12 @@ class Sim:
                         break
                     elif kind == "write":  # completes after act[3] ticks (a TMA copy)
                         self.write(act[1], act[2], self.tick + (act[3] if len(act) > 3 else 0))
+            if self.exit_check and all(a["done"] for a in state):
+                if self.cur is not None or self.pipe_i < len(self.pipe):
+                    self.violations.append(("product in flight at exit",))
+                if self.write_until > self.tick or self.later:
+                    self.violations.append(("copy in flight at exit",))
+                return self.violations
             if all(a["done"] for a in state) and self.pipe_i >= len(self.pipe) \
                     and self.cur is None and not self.later:
                 return self.violations

@@ -51,17 +51,25 @@ CONFIGS = {  # score buffers, K/V stages, split issue, split K/V release
 
 
 def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_slots="tile",
-                     skip=(), copy_ticks=(1, 8)):
-    """copy_ticks: range of a TMA copy's duration."""
+                     skip=(), copy_ticks=(1, 8), withhold=-1, hook="break"):
+    """copy_ticks: range of a TMA copy's duration; withhold: the key tile from which the
+    producers stop loading (the kernel's failure-detection hook; hook="continue" skips only
+    that tile, as the hook once did), so that waits time out and roles leave."""
     nsb, nst, split, split_kv = CONFIGS[D]
     od = Order(n0, n1)
     n, total, n_max = od.n, od.total, max(n0, n1)
 
     def wait(bar, phase):
-        if bar.rstrip("0123456789_") not in skip:
-            yield ("wait", bar, phase)
+        """The kernel's bounded wait: False once it gave up (or another role did)."""
+        if bar.rstrip("0123456789_") in skip:
+            return True
+        ok = yield ("wait", bar, phase)
+        return ok is not False
 
+    sim.barrier("mma_drain0", 1)
+    sim.barrier("mma_drain1", 1)
     sim.barrier("q_full", 1)
+    sim.buffer("QS", ())  # the query tiles, loaded once
     for st in range(nst):
         for b in ("k_full", "v_full", "kv_empty", "k_empty"):
             sim.barrier(f"{b}{st}", 1)
@@ -88,12 +96,20 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
         return f"o_done{t}_{i & 1}", i >> 1
 
     def producer():
-        yield ("delay", rng.randint(0, 3))
-        sim.arrive("q_full")
+        land = rng.randint(0, 3)
+        yield ("write", "QS", 0, land)
+        yield ("arrive_after", "q_full", land)
+        last = [-1] * nst
         for j in range(n_max):
             st = j % nst
-            if j >= nst:
-                yield from wait(("k_empty" if split_kv else "kv_empty") + str(st), j // nst - 1)
+            if j == withhold:
+                if hook == "break":
+                    break
+                continue
+            if j >= nst and not (yield from wait(
+                    ("k_empty" if split_kv else "kv_empty") + str(st), j // nst - 1)):
+                break
+            last[st] = j
             land = rng.randint(*copy_ticks)
             yield ("write", f"KS{st}", j, land)
             yield ("arrive_after", f"k_full{st}", land)
@@ -101,53 +117,85 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
                 land = rng.randint(*copy_ticks)
                 yield ("write", f"VS{st}", j, land)
                 yield ("arrive_after", f"v_full{st}", land)
+        if sim.abort:  # let the copies in flight land before leaving
+            yield ("drain", "q_full", 0)
+            for st in range(nst):
+                if last[st] >= 0:
+                    yield ("drain", f"k_full{st}", last[st] // nst)
+                    if not split_kv:
+                        yield ("drain", f"v_full{st}", last[st] // nst)
 
     def v_producer():
+        last = [-1] * nst
         for j in range(n_max):
             st = j % nst
-            if j >= nst:
-                yield from wait(f"kv_empty{st}", j // nst - 1)
+            if j == withhold:
+                if hook == "break":
+                    break
+                continue
+            if j >= nst and not (yield from wait(f"kv_empty{st}", j // nst - 1)):
+                break
+            last[st] = j
             land = rng.randint(*copy_ticks)
             yield ("write", f"VS{st}", j, land)
             yield ("arrive_after", f"v_full{st}", land)
+        if sim.abort:
+            for st in range(nst):
+                if last[st] >= 0:
+                    yield ("drain", f"v_full{st}", last[st] // nst)
 
     def bias_producer():
+        last = [-1, -1]
         for k in range(total):
             t, j = od.t_of(k), od.j_of(k)
             if bias_slots == "tile":
                 slot, phase = t, j
             else:  # the earlier scheme: slot k mod 2, shared by the tiles
                 slot, phase = k % 2, k // 2
-            if phase >= 1:
-                yield from wait(f"b_empty{slot}", phase - 1)
+            if phase >= 1 and not (yield from wait(f"b_empty{slot}", phase - 1)):
+                break
+            last[slot] = phase
             land = rng.randint(*copy_ticks)
             yield ("write", f"BS{slot}", (t, j), land)
             yield ("arrive_after", f"b_full{slot}", land)
+        if sim.abort:
+            for slot in range(2):
+                if last[slot] >= 0:
+                    yield ("drain", f"b_full{slot}", last[slot])
 
     def issue_s(k, seen):
         t, j = od.t_of(k), od.j_of(k)
         st, b = j % nst, k % nsb
         if j != seen[0]:
-            yield from wait(f"k_full{st}", j // nst)
+            if not (yield from wait(f"k_full{st}", j // nst)):
+                return False
             seen[0] = j
-        yield ("mma", f"S{t}", [(f"KS{st}", j)], [(f"SP{b}", ("S", k))])
+        yield ("mma", f"S{t}", [("QS", 0), (f"KS{st}", j)], [(f"SP{b}", ("S", k))])
         yield ("commit", f"s_full{b}")
         if split_kv:
             yield ("commit", f"k_empty{st}")
+        return True
 
     def mma():
         seen_k, seen_v = [-1], -1
+        ok = True
         if not split:
-            yield from wait("q_full", 0)
+            ok = yield from wait("q_full", 0)
             for k in range(min(nsb, total)):
-                yield from issue_s(k, seen_k)
+                if not ok:
+                    break
+                ok = yield from issue_s(k, seen_k)
         for k in range(total):
+            if not ok:
+                break
             t, j = od.t_of(k), od.j_of(k)
             st, b = j % nst, k % nsb
             if j != seen_v:
-                yield from wait(f"v_full{st}", j // nst)
+                if not (yield from wait(f"v_full{st}", j // nst)):
+                    break
                 seen_v = j
-            yield from wait(f"p_full{b}", k // nsb)
+            if not (yield from wait(f"p_full{b}", k // nsb)):
+                break
             reads = [(f"SP{b}", ("P", k)), (f"VS{st}", j)]
             if j > 0:  # PV_t(0) overwrites O_t (accumulate off)
                 reads.append((f"O{t}", j))
@@ -158,32 +206,42 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
             if k + 1 == total or od.j_of(k + 1) != j:
                 yield ("commit", f"kv_empty{st}")
             if not split and k + nsb < total:
-                yield from issue_s(k + nsb, seen_k)
+                ok = yield from issue_s(k + nsb, seen_k)
+        # every product this warp issued has completed before tensor memory is released
+        yield ("commit", "mma_drain0")
+        yield ("drain", "mma_drain0", 0)
 
     def s_warp():
         seen = [-1]
-        yield from wait("q_full", 0)
+        ok = yield from wait("q_full", 0)
         for k in range(total):
+            if not ok:
+                break
             b = k % nsb
-            if k >= nsb:
-                yield from wait(f"buf_free{b}", (k - nsb) // nsb)
-            yield from issue_s(k, seen)
+            if k >= nsb and not (yield from wait(f"buf_free{b}", (k - nsb) // nsb)):
+                break
+            ok = yield from issue_s(k, seen)
+        yield ("commit", "mma_drain1")
+        yield ("drain", "mma_drain1", 0)
 
     def softmax(t):
         me = f"sm{t}"
         for j in range(n[t]):
             k = od.k_of(t, j)
             b = k % nsb
-            yield from wait(f"s_full{b}", k // nsb)
+            if not (yield from wait(f"s_full{b}", k // nsb)):
+                return
             yield ("read", f"SP{b}", ("S", k), me, rng.randint(0, 3))
             if bias:
                 slot, phase = (t, j) if bias_slots == "tile" else (k % 2, k // 2)
-                yield from wait(f"b_full{slot}", phase)
+                if not (yield from wait(f"b_full{slot}", phase)):
+                    return
                 yield ("read", f"BS{slot}", (t, j), me, 0)
                 yield ("arrive", f"b_empty{slot}")
             yield ("delay", rng.randint(1, 8))  # the exponentials
             if j > 0 and rng.random() < 0.6:  # the row maximum moved: rescale O_t
-                yield from wait(*o_bar(t, j - 1))
+                if not (yield from wait(*o_bar(t, j - 1))):
+                    return
                 yield ("read", f"O{t}", j, me, rng.randint(1, 3))
                 yield ("write", f"O{t}", j)
             land = rng.randint(0, 2)  # P to TMEM, then tcgen05.wait::st
@@ -194,7 +252,8 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
             return
         one = o_scheme in ("single", "parity_one_wait") or n[t] < 2
         for i in ([n[t] - 1] if one else [n[t] - 2, n[t] - 1]):
-            yield from wait(*o_bar(t, i))
+            if not (yield from wait(*o_bar(t, i))):
+                return
         yield ("read", f"O{t}", n[t], me, rng.randint(1, 3))
 
     agents = [producer(), mma(), softmax(0), softmax(1)]
@@ -269,3 +328,32 @@ def test_model_catches_a_missing_wait(D, dropped):
 @pytest.mark.parametrize("dropped", ["b_full", "b_empty"])
 def test_model_catches_a_missing_bias_wait(dropped):
     assert _found(64, 5, 5, bias=True, skip=(dropped,))
+
+
+@pytest.mark.parametrize("D,n0,n1,withhold,bias", [
+    (64, 5, 6, 0, False), (64, 5, 6, 3, False), (64, 6, 0, 5, False), (64, 5, 5, 2, True),
+    (128, 5, 6, 0, False), (128, 5, 5, 4, False), (128, 3, 0, 1, False),
+    (256, 6, 0, 0, False), (256, 6, 0, 3, False), (256, 2, 0, 1, False)])
+def test_withheld_tile_every_role_leaves_and_nothing_is_in_flight(D, n0, n1, withhold, bias):
+    """The failure-detection path: a key tile is never loaded, so some wait gives up and
+    raises the abort flag; every other wait then fails, producers wait for the copies they
+    issued and issuing warps for their products. When the last role is done nothing may
+    still be landing or running, since the CTA then frees its memory."""
+    rng = random.Random(D + n0 + n1 + withhold)
+    for _ in range(100):
+        sim = Sim(rng, timeout=200, exit_check=True)
+        v = sim.run(forward_protocol(sim, D, n0, n1, rng, bias=bias, withhold=withhold))
+        assert sim.abort
+        assert v == [], v[:3]
+
+
+def test_skipping_only_the_withheld_tile_is_caught():
+    """With one K stage (d_head 256), a producer that skips only the withheld tile then waits
+    for the release of a tile that was never loaded: a phase that never completes, so the
+    parity wait can pass while the stage is still read."""
+    rng = random.Random(1)
+    found = []
+    for _ in range(100):
+        sim = Sim(rng, timeout=200, exit_check=True)
+        found += sim.run(forward_protocol(sim, 256, 6, 0, rng, withhold=3, hook="continue"))
+    assert any(v[0] == "wait start" for v in found)
