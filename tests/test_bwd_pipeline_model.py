@@ -24,10 +24,11 @@ import pytest
 from _pipeline_sim import Sim
 
 
-def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True):
+def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True, withhold=-1):
     """The kernel's roles; `skip` names waits to leave out (to check that the model sees
     what they prevent); ds_empty=False drops the dS-buffer release (the commit after dK / dQ
-    and the wait for it before the buffer is rewritten two steps later)."""
+    and the wait for it before the buffer is rewritten two steps later); withhold: a step
+    whose Q / dO the producer skips (the kernel's failure-detection hook)."""
     sim.barrier("kv_full", 1)
     for st in range(qst):
         sim.barrier(f"q_full{st}", 1)
@@ -39,6 +40,7 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True):
                     ("dq_full", 1), ("dq_empty", 2), ("dkdv_full", 1)):
         sim.barrier(name, n)
     wg = ("wg0", "wg1")
+    sim.buffer("KV", ())  # the key tile's K and V, loaded once
     for st in range(qst):  # Q / dO stage: the products of its step, and the LSE rows
         sim.buffer(f"QS{st}", ("SdP", "dV", "dK") + wg)
     sim.buffer("SDP", wg)
@@ -48,44 +50,63 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True):
     sim.buffer("DQ", wg)
 
     def wait(bar, phase):
-        if bar.rstrip("0123456789") not in skip:
-            yield ("wait", bar, phase)
+        """The kernel's bounded wait: False once it gave up (or another role did)."""
+        if bar.rstrip("0123456789") in skip:
+            return True
+        ok = yield ("wait", bar, phase)
+        return ok is not False
+
+    sim.barrier("mma_drain", 1)
 
     def producer():
-        yield ("delay", rng.randint(0, 5))
-        sim.arrive("kv_full")
+        land = rng.randint(0, 5)
+        yield ("write", "KV", 0, land)
+        yield ("arrive_after", "kv_full", land)
+        last = [-1] * qst
         for it in range(n_steps):
             st = it % qst
-            if it >= qst:
-                yield from wait(f"q_empty{st}", it // qst - 1)
+            if it == withhold:
+                continue
+            if it >= qst and not (yield from wait(f"q_empty{st}", it // qst - 1)):
+                break
+            last[st] = it
             land = rng.randint(1, 8)  # TMA copies and the LSE / Delta rows land
             yield ("write", f"QS{st}", it, land)
             yield ("delay", land)
             yield ("arrive", f"q_full{st}")
+        if sim.abort:  # let the copies in flight land before leaving
+            yield ("drain", "kv_full", 0)
+            for st in range(qst):
+                if last[st] >= 0:
+                    yield ("drain", f"q_full{st}", last[st] // qst)
 
     def mma():
-        yield from wait("kv_full", 0)
-
         def issue_sdp(it):
             st = it % qst
-            yield from wait(f"q_full{st}", it // qst)
-            yield ("mma", "SdP", [(f"QS{st}", it)], [("SDP", it)])
+            if not (yield from wait(f"q_full{st}", it // qst)):
+                return False
+            yield ("mma", "SdP", [("KV", 0), (f"QS{st}", it)], [("SDP", it)])
             yield ("commit", "s_full")
+            return True
 
-        yield from issue_sdp(0)
+        ok = (yield from wait("kv_full", 0)) and (yield from issue_sdp(0))
         for it in range(n_steps):
+            if not ok:
+                break
             st, bs = it % qst, it & 1
             if it + 1 < n_steps:
-                yield from wait("s_free", it)
-                yield from issue_sdp(it + 1)
-            yield from wait("p_full", it)
+                if not (yield from wait("s_free", it)) or not (yield from issue_sdp(it + 1)):
+                    break
+            if not (yield from wait("p_full", it)):
+                break
             yield ("mma", "dV", [("P", it), (f"QS{st}", it)], [])
             yield ("commit", "p_empty")
-            yield from wait(f"ds_full{bs}", it >> 1)
+            if not (yield from wait(f"ds_full{bs}", it >> 1)):
+                break
             yield ("mma", "dK", [(f"DS{bs}", it), (f"QS{st}", it)], [])
             if with_dq:
-                if it > 0:
-                    yield from wait("dq_empty", it - 1)
+                if it > 0 and not (yield from wait("dq_empty", it - 1)):
+                    break
                 yield ("mma", "dQ", [(f"DS{bs}", it)], [("DQ", it)])
             if ds_empty:
                 yield ("commit", f"ds_empty{bs}")
@@ -93,26 +114,32 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True):
             if with_dq:
                 yield ("commit", "dq_full")
         yield ("commit", "dkdv_full")
+        # every product this warp issued has completed before tensor memory is released
+        yield ("commit", "mma_drain")
+        yield ("drain", "mma_drain", 0)
 
     def warpgroup(me):
         def drain(itd):
-            yield from wait("dq_full", itd)
+            if not (yield from wait("dq_full", itd)):
+                return False
             yield ("read", "DQ", itd, me, rng.randint(1, 4))
             yield ("arrive", "dq_empty")
             yield ("delay", rng.randint(0, 4))  # staging and the reduce-add
+            return True
 
         for it in range(n_steps):
             st, bs = it % qst, it & 1
-            yield from wait("s_full", it)
-            yield from wait(f"q_full{st}", it // qst)
-            if ds_empty and it >= 2:
-                yield from wait(f"ds_empty{bs}", (it >> 1) - 1)
+            if not (yield from wait("s_full", it)) or \
+                    not (yield from wait(f"q_full{st}", it // qst)):
+                return
+            if ds_empty and it >= 2 and not (yield from wait(f"ds_empty{bs}", (it >> 1) - 1)):
+                return
             yield ("read", "SDP", it, me, rng.randint(1, 4))
             yield ("read", f"QS{st}", it, me, 0)
             yield ("delay", rng.randint(0, 3))
             yield ("arrive", "s_free")
-            if it > 0:
-                yield from wait("p_empty", it - 1)
+            if it > 0 and not (yield from wait("p_empty", it - 1)):
+                return
             yield ("delay", rng.randint(1, 10))  # P and dS
             if me == "wg0":  # one write event stands for both warpgroups' halves
                 yield ("write", "P", it)
@@ -123,10 +150,10 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True):
             if me == "wg0":
                 yield ("write", f"DS{bs}", it)
             yield ("arrive", f"ds_full{bs}")
-            if with_dq and it > 0:
-                yield from drain(it - 1)
-        if with_dq and n_steps > 0:
-            yield from drain(n_steps - 1)
+            if with_dq and it > 0 and not (yield from drain(it - 1)):
+                return
+        if with_dq and n_steps > 0 and not (yield from drain(n_steps - 1)):
+            return
         yield from wait("dkdv_full", 0)
 
     return [producer(), mma(), warpgroup("wg0"), warpgroup("wg1")]
@@ -167,3 +194,18 @@ def test_ds_release_is_implied(qst):
     for _ in range(300):
         sim = Sim(rng)
         assert sim.run(backward_protocol(sim, 6, qst, True, rng, ds_empty=False)) == []
+
+
+@pytest.mark.parametrize("qst", [2, 3])
+@pytest.mark.parametrize("withhold", [0, 1, 3])
+@pytest.mark.parametrize("with_dq", [True, False])
+def test_withheld_step_every_role_leaves_and_nothing_is_in_flight(qst, withhold, with_dq):
+    """The failure-detection path: the producer skips one step, a wait gives up and raises
+    the abort flag; every role leaves, the producer drains its copies and the MMA warp its
+    products, and nothing is in flight when the last role is done."""
+    rng = random.Random(qst * 10 + withhold + 100 * with_dq)
+    for _ in range(100):
+        sim = Sim(rng, timeout=200, exit_check=True)
+        v = sim.run(backward_protocol(sim, 6, qst, with_dq, rng, withhold=withhold))
+        assert sim.abort
+        assert v == [], v[:3]
