@@ -256,8 +256,8 @@ BwdWorkspace bwd_layout(int64_t B, int64_t H, int64_t rows, int64_t D) {
 bool valid_scale(float s) { return isfinite(s) && s > 0.f; }
 
 // Test hook for the failure-detection path: when the environment variable
-// ATTN_TEST_WITHHOLD_KV_TILE holds a key-tile index, the forward producer never loads that
-// tile and every wait is bounded by 50 ms, so the kernel gives up, reports
+// ATTN_TEST_WITHHOLD_KV_TILE holds a key-tile index, the forward producers load no key tile
+// from that one on and every wait is bounded by 50 ms, so the kernel gives up, reports
 // ATTN_ERR_DEVICE_TIMEOUT in the status word and returns (no trap, no fault).
 int withheld_tile_for_test() {
   const char* v = getenv("ATTN_TEST_WITHHOLD_KV_TILE");

@@ -64,7 +64,7 @@
  *     table measured on GB300 (the sweep that writes the table sets it). Results do not
  *     depend on the order.
  *   ATTN_TEST_WITHHOLD_KV_TILE=j / ATTN_TEST_WITHHOLD_Q_STEP=i (failure-detection tests):
- *     the forward never loads key tile j / the backward never loads query step i, and every
+ *     the forward loads no key tile from j on / the backward skips query step i, and every
  *     wait gives up after 50 ms, so the call ends with ATTN_ERR_DEVICE_TIMEOUT in the status
  *     word instead of hanging.
  */

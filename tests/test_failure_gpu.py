@@ -1,6 +1,6 @@
 """Failure detection on the GPU without a fault: a pipeline wait that nothing satisfies.
 
-The test hook ATTN_TEST_WITHHOLD_KV_TILE makes the forward producer skip one key tile, so
+The test hook ATTN_TEST_WITHHOLD_KV_TILE makes the forward producer stop at one key tile, so
 the MMA issuer's bounded wait for it runs out (50 ms under the hook). The kernel must then
 leave every pipeline loop, free its tensor memory, record ATTN_ERR_DEVICE_TIMEOUT in the
 workspace status word and return; the CUDA context must stay usable for the next call."""
