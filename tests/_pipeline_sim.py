@@ -12,6 +12,10 @@ Agents are generators that yield actions:
   ('read', buf, contents, who, ticks)   read a buffer (a TMEM load, ...) for `ticks` ticks
   ('write', buf, contents[, ticks])     write a buffer, complete after `ticks` (a TMA copy)
   ('drain', bar, phase)           a wait that ignores the abort flag (leaving after a failure)
+  ('read_async', buf, contents, who, ticks)  a read by an asynchronous engine (a TMA store
+                                  or reduce from shared memory); the agent does not wait
+  ('wait_read', buf, who)         block until `who`'s read of the buffer's current contents
+                                  has finished (cp.async.bulk.wait_group.read)
 With a timeout, a wait that has not succeeded after `timeout` ticks fails and raises the
 CTA's abort flag; once it is raised every wait fails at once (the agent receives False from
 its yield) and drains still wait. With exit_check, nothing may be in flight when the last
@@ -150,6 +154,14 @@ class Sim:
                         self.later.append((self.tick + act[2], act[1]))
                     elif kind in ("mma", "commit"):
                         self.pipe.append(act)
+                    elif kind == "read_async":
+                        self.read(act[1], act[2], act[3], self.tick + act[4])
+                    elif kind == "wait_read":
+                        cur = self.content[act[1]]
+                        end = None if cur is None else cur[2].get(act[2])
+                        if end is not None and end > self.tick:
+                            a["pending"], a["until"] = ("delay",), end
+                            break
                     elif kind == "read":  # a read that takes act[4] ticks (a TMEM load)
                         self.read(act[1], act[2], act[3], self.tick + act[4])
                         a["pending"], a["until"] = ("delay",), self.tick + act[4]
@@ -161,6 +173,9 @@ class Sim:
                     self.violations.append(("product in flight at exit",))
                 if self.write_until > self.tick or self.later:
                     self.violations.append(("copy in flight at exit",))
+                if any(end is not None and end > self.tick for c in self.content.values()
+                       if c is not None for end in c[2].values()):
+                    self.violations.append(("read in flight at exit",))
                 return self.violations
             if all(a["done"] for a in state) and self.pipe_i >= len(self.pipe) \
                     and self.cur is None and not self.later:

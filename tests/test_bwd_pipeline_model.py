@@ -24,11 +24,15 @@ import pytest
 from _pipeline_sim import Sim
 
 
-def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True, withhold=-1):
+def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True, withhold=-1,
+                      stage_in_ds=True):
     """The kernel's roles; `skip` names waits to leave out (to check that the model sees
     what they prevent); ds_empty=False drops the dS-buffer release (the commit after dK / dQ
     and the wait for it before the buffer is rewritten two steps later); withhold: a step
-    whose Q / dO the producer skips (the kernel's failure-detection hook)."""
+    whose Q / dO the producer skips (the kernel's failure-detection hook); stage_in_ds: the
+    d_head 64 layout, where each warpgroup stages its dQ block in its own half of the dS
+    buffer it has just released and waits for the reduce-add to finish reading it before
+    writing that half again (skip "read_wait" drops that wait)."""
     sim.barrier("kv_full", 1)
     for st in range(qst):
         sim.barrier(f"q_full{st}", 1)
@@ -46,7 +50,9 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True, w
     sim.buffer("SDP", wg)
     sim.buffer("P", ("dV",))
     for b in range(2):
-        sim.buffer(f"DS{b}", ("dK", "dQ") if with_dq else ("dK",))
+        for h in range(2):  # the halves the two warpgroups write
+            sim.buffer(f"DS{b}{h}", lambda c, h=h: ({"dK", "dQ"} if with_dq else {"dK"})
+                       if c[0] == "dS" else {f"tma{h}"})
     sim.buffer("DQ", wg)
 
     def wait(bar, phase):
@@ -103,11 +109,12 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True, w
             yield ("commit", "p_empty")
             if not (yield from wait(f"ds_full{bs}", it >> 1)):
                 break
-            yield ("mma", "dK", [(f"DS{bs}", it), (f"QS{st}", it)], [])
+            ds = [(f"DS{bs}{h}", ("dS", it)) for h in range(2)]
+            yield ("mma", "dK", ds + [(f"QS{st}", it)], [])
             if with_dq:
                 if it > 0 and not (yield from wait("dq_empty", it - 1)):
                     break
-                yield ("mma", "dQ", [(f"DS{bs}", it)], [("DQ", it)])
+                yield ("mma", "dQ", ds, [("DQ", it)])
             if ds_empty:
                 yield ("commit", f"ds_empty{bs}")
             yield ("commit", f"q_empty{st}")
@@ -119,12 +126,19 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True, w
         yield ("drain", "mma_drain", 0)
 
     def warpgroup(me):
+        h = int(me[-1])
+
         def drain(itd):
             if not (yield from wait("dq_full", itd)):
                 return False
             yield ("read", "DQ", itd, me, rng.randint(1, 4))
             yield ("arrive", "dq_empty")
-            yield ("delay", rng.randint(0, 4))  # staging and the reduce-add
+            if stage_in_ds:  # stage in this warpgroup's half of dS(itd), reduce-add from it
+                yield ("write", f"DS{itd & 1}{h}", ("stg", itd))
+                yield ("read_async", f"DS{itd & 1}{h}", ("stg", itd), f"tma{h}",
+                       rng.randint(1, 12))
+            else:
+                yield ("delay", rng.randint(0, 4))  # a staging area of its own
             return True
 
         for it in range(n_steps):
@@ -134,6 +148,8 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True, w
                 return
             if ds_empty and it >= 2 and not (yield from wait(f"ds_empty{bs}", (it >> 1) - 1)):
                 return
+            if stage_in_ds and with_dq and it >= 2 and "read_wait" not in skip:
+                yield ("wait_read", f"DS{bs}{h}", f"tma{h}")  # the reduce has read this half
             yield ("read", "SDP", it, me, rng.randint(1, 4))
             yield ("read", f"QS{st}", it, me, 0)
             yield ("delay", rng.randint(0, 3))
@@ -147,8 +163,7 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True, w
             # dS^T was stored with P^T, but the MMAs (async proxy) see it only after the
             # proxy fence that precedes the ds_full arrival
             yield ("delay", rng.randint(0, 8))
-            if me == "wg0":
-                yield ("write", f"DS{bs}", it)
+            yield ("write", f"DS{bs}{h}", ("dS", it))
             yield ("arrive", f"ds_full{bs}")
             if with_dq and it > 0 and not (yield from drain(it - 1)):
                 return
@@ -156,17 +171,25 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), ds_empty=True, w
             return
         yield from wait("dkdv_full", 0)
 
-    return [producer(), mma(), warpgroup("wg0"), warpgroup("wg1")]
+    def warpgroup_role(me):
+        yield from warpgroup(me)
+        if stage_in_ds and with_dq:  # on every exit path: all of this warp's reduces done
+            for b in range(2):
+                yield ("wait_read", f"DS{b}{me[-1]}", f"tma{me[-1]}")
+
+    return [producer(), mma(), warpgroup_role("wg0"), warpgroup_role("wg1")]
 
 
 @pytest.mark.parametrize("n_steps", [1, 2, 3, 4, 7])
 @pytest.mark.parametrize("qst", [2, 3])
 @pytest.mark.parametrize("with_dq", [True, False])
-def test_backward_pipeline_is_exact_and_race_free(n_steps, qst, with_dq):
-    rng = random.Random(n_steps * 10 + qst + 100 * with_dq)
-    for _ in range(150):
-        sim = Sim(rng)
-        assert sim.run(backward_protocol(sim, n_steps, qst, with_dq, rng)) == []
+@pytest.mark.parametrize("stage_in_ds", [True, False])  # d_head 64, 128
+def test_backward_pipeline_is_exact_and_race_free(n_steps, qst, with_dq, stage_in_ds):
+    rng = random.Random(n_steps * 10 + qst + 100 * with_dq + 1000 * stage_in_ds)
+    for _ in range(120):
+        sim = Sim(rng, exit_check=True)
+        assert sim.run(backward_protocol(sim, n_steps, qst, with_dq, rng,
+                                         stage_in_ds=stage_in_ds)) == []
 
 
 @pytest.mark.parametrize("dropped,kind", [
@@ -209,3 +232,15 @@ def test_withheld_step_every_role_leaves_and_nothing_is_in_flight(qst, withhold,
         v = sim.run(backward_protocol(sim, 6, qst, with_dq, rng, withhold=withhold))
         assert sim.abort
         assert v == [], v[:3]
+
+
+def test_staging_needs_the_reduce_read_wait():
+    """d_head 64 stages each dQ block in the warpgroup's half of the dS buffer it has just
+    released; without waiting for the reduce-add to finish reading it, the next dS write
+    into that half can overwrite the block while it is read."""
+    rng = random.Random(21)
+    found = []
+    for _ in range(300):
+        sim = Sim(rng, mma_ticks=(1, 3))
+        found += sim.run(backward_protocol(sim, 6, 3, True, rng, skip=("read_wait",)))
+    assert any(v[0] == "overwrite" for v in found)
