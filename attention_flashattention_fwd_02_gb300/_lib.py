@@ -125,9 +125,19 @@ def attn_status_string(status: int) -> str:
 
 
 # ------------------------------------------------------------------------------ marshalling
+def _on_device(t: torch.Tensor, what: str) -> None:
+    """Every pointer the library dereferences is device memory of the current device."""
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor, got one on {t.device}")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{what} is on {t.device}, not on the current device "
+                         f"cuda:{torch.cuda.current_device()}")
+
+
 def _t4(t: Optional[torch.Tensor]):
     if t is None:
         return None
+    _on_device(t, "a rank-4 tensor")
     if t.dim() != 4:
         raise ValueError(f"expected a rank-4 (B, H, S, D) tensor, got shape {tuple(t.shape)}")
     v = Tensor4()
@@ -141,6 +151,7 @@ def _t4(t: Optional[torch.Tensor]):
 def _t3(t: Optional[torch.Tensor]):
     if t is None:
         return None
+    _on_device(t, "lse")
     if t.dim() != 3:
         raise ValueError(f"expected a rank-3 (B, H, S) tensor, got shape {tuple(t.shape)}")
     v = Tensor3()
@@ -160,6 +171,7 @@ def _check16(*ts):
 def _ptr(t: Optional[torch.Tensor]):
     if t is None:
         return None
+    _on_device(t, "cu_seqlens")
     if t.dtype != torch.int32:
         raise TypeError(f"cu_seqlens must be int32, got {t.dtype}")
     return t.data_ptr()
@@ -168,6 +180,7 @@ def _ptr(t: Optional[torch.Tensor]):
 def _ws(ws: Optional[torch.Tensor]):
     if ws is None:
         return None, 0
+    _on_device(ws, "the workspace")
     return ws.data_ptr(), ws.numel() * ws.element_size()
 
 
@@ -338,6 +351,7 @@ def attn_bwd_dq_epilogue(dq, sm_scale, workspace, cu_seqlens_q=None, num_seqs=-1
 
 
 def attn_read_device_status(workspace, stream=None) -> int:
+    _on_device(workspace, "the workspace")
     out = I32(0)
     _check(load().attn_read_device_status(workspace.data_ptr(), _stream(stream),
                                           ctypes.byref(out)), "attn_read_device_status")

@@ -270,3 +270,17 @@ def test_bwd_bias_validation(lib):
     assert call((1, 2, 128, 128), t4((1, 2, 128, 128)), None) == ERR_UNSUPPORTED
     assert call((2, 2, 128, 64), t4((1, 2, 128, 128)), t4((1, 2, 128, 128))) == ERR_UNSUPPORTED
     assert call((1, 2, 128, 64), t4((1, 2, 128, 128)), t4((1, 2, 128, 136))) == ERR_SHAPE
+
+
+def test_binding_rejects_host_tensors(lib):
+    """The Python binding checks that every tensor it passes is on the current CUDA device
+    before calling the library (which dereferences them as device pointers)."""
+    import torch
+    q = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 128)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        _lib.attn_fwd(q, q, q, q, lse, 0.125, False)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        _lib.attn_read_device_status(torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        _lib._ptr(torch.zeros(3, dtype=torch.int32))
