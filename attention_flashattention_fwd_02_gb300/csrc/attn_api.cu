@@ -486,11 +486,11 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
   return ATTN_OK;
 }
 
-attn_status bwd_common(const BwdArgs& a, const int32_t* cu_q, const int32_t* cu_k, int compact,
-                       int32_t num_seqs, int32_t max_q, int32_t max_k, float sm_scale,
-                       int causal, void* ws, size_t ws_bytes, void* stream,
-                       bool deterministic = false) {
-  Problem pr;
+// Host checks of a backward call's arguments (everything but the workspace); fills *pr.
+attn_status bwd_validate(const BwdArgs& a, const int32_t* cu_q, const int32_t* cu_k, int compact,
+                         int32_t num_seqs, int32_t max_q, int32_t max_k, float sm_scale,
+                         bool deterministic, Problem* pr_out) {
+  Problem& pr = *pr_out;
   attn_status s =
       make_problem(a.q, a.k, a.v, cu_q, cu_k, compact, num_seqs, max_q, max_k, &pr);
   if (s != ATTN_OK) return s;
@@ -531,11 +531,40 @@ attn_status bwd_common(const BwdArgs& a, const int32_t* cu_q, const int32_t* cu_
   } else if (a.dbias != nullptr) {
     return ATTN_ERR_NULL;
   }
+  return ATTN_OK;
+}
+
+attn_status bwd_common(const BwdArgs& a, const int32_t* cu_q, const int32_t* cu_k, int compact,
+                       int32_t num_seqs, int32_t max_q, int32_t max_k, float sm_scale,
+                       int causal, void* ws, size_t ws_bytes, void* stream,
+                       bool deterministic = false) {
+  Problem pr;
+  attn_status s = bwd_validate(a, cu_q, cu_k, compact, num_seqs, max_q, max_k, sm_scale,
+                               deterministic, &pr);
+  if (s != ATTN_OK) return s;
   if (deterministic) return bwd_stage(1 | 2 | 8, a, pr, sm_scale, causal, ws, ws_bytes, stream, true);
   return bwd_stage(7, a, pr, sm_scale, causal, ws, ws_bytes, stream);
 }
 
 }  // namespace
+
+namespace attn_sm103 {
+
+attn_status bwd_check_args(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                           const attn_tensor4* o, const attn_tensor3* lse,
+                           const attn_tensor4* dout, const int32_t* cu_seqlens_q,
+                           const int32_t* cu_seqlens_k, float sm_scale,
+                           const attn_tensor4* dq, const attn_tensor4* dk,
+                           const attn_tensor4* dv) {
+  BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse};
+  Problem pr;
+  attn_status s = bwd_validate(a, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, false, &pr);
+  if (s != ATTN_OK) return s;
+  if (pr.D > 128) return ATTN_ERR_UNSUPPORTED;  // as bwd_stage
+  return check_device();
+}
+
+}  // namespace attn_sm103
 
 // =============================================================================== C ABI
 extern "C" {

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include "../../include/attn.h"
 #include "attn_common.cuh"
 
 namespace attn_sm103 {
@@ -24,5 +25,14 @@ cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream);
 // Deterministic dQ: grid = (query blocks, H, units); a block covers bwd_dq_block_m() rows.
 int bwd_dq_block_m();
 cudaError_t launch_bwd_dq(const BwdDqParams& p, int D, bool f16, dim3 grid, cudaStream_t stream);
+
+// Every host check attn_bwd (dense or padded varlen) makes before it touches the stream, the
+// workspace aside: arguments, head size and device. Launches nothing.
+attn_status bwd_check_args(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
+                           const attn_tensor4* o, const attn_tensor3* lse,
+                           const attn_tensor4* dout, const int32_t* cu_seqlens_q,
+                           const int32_t* cu_seqlens_k, float sm_scale,
+                           const attn_tensor4* dq, const attn_tensor4* dk,
+                           const attn_tensor4* dv);
 
 }  // namespace attn_sm103

@@ -3,10 +3,13 @@ profiling a single shape (e.g. under ncu) without the benchmark's full step.
 
   python -m attention_flashattention_fwd_02_gb300.run_case --B 2 --H 16 --S 4096 --D 256 \
          --fwd-only --warmup 1 --iters 2
+  python -m attention_flashattention_fwd_02_gb300.run_case --workload padded --B 2
 
 Inputs are i.i.d. N(0, 1) drawn on the device from a fixed seed and rounded to the element
 type; times are CUDA-event medians on the current stream (L2 not flushed). The device status
-word is checked after the timed calls.
+word is checked after the timed calls. --workload takes a varlen benchmark workload (padded
+or compact) with its own sizes and mask, keeping the first --B of its drawn lengths (batch
+entries or sequences); its inputs come from the seeded workload generator.
 """
 from __future__ import annotations
 
@@ -18,7 +21,7 @@ import torch
 
 from . import _lib
 from .attention import backward, bwd_workspace, forward
-from .workloads import unmasked_pairs
+from .workloads import WORKLOADS, draw_lengths, make_inputs, unmasked_pairs
 
 
 def main(argv=None):
@@ -34,7 +37,10 @@ def main(argv=None):
     ap.add_argument("--deterministic", action="store_true", help="deterministic backward")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--iters", type=int, default=10)
+    ap.add_argument("--workload", choices=("padded", "compact"), default=None)
     a = ap.parse_args(argv)
+    if a.workload:
+        return run_varlen(a)
 
     dev = torch.device("cuda")
     dt = torch.float16 if a.fp16 else torch.bfloat16
@@ -57,6 +63,48 @@ def main(argv=None):
         backward(q, k, v, o, lse, do, c, a.causal, dq=grads[0], dk=grads[1], dv=grads[2],
                  workspace=ws_b, deterministic=a.deterministic)
 
+    pairs = a.B * a.H * unmasked_pairs(Sq, Sk, a.causal)
+    out = {"B": a.B, "H": a.H, "Sq": Sq, "Sk": Sk, "D": a.D, "causal": a.causal,
+           "dtype": "fp16" if a.fp16 else "bf16"}
+    _time_and_report(a, run_fwd, None if a.fwd_only else run_bwd, a.D, pairs, out,
+                     (ws_f, ws_b))
+
+
+def run_varlen(a):
+    """The --workload form: a padded or compact benchmark workload cut to its first a.B
+    lengths."""
+    wl = WORKLOADS[a.workload]
+    lengths = draw_lengths(wl)[: a.B]
+    wl = wl.replace(B=a.B) if wl.layout == "padded" else wl.replace(n_seqs=a.B)
+    dt = torch.float16 if a.fp16 else torch.bfloat16
+    x = make_inputs(wl, lengths=lengths, dtype=dt)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    q, k, v, do = g["q"], g["k"], g["v"], g["do"]
+    cu_q, cu_k = g["cu_seqlens_q"], g["cu_seqlens_k"]
+    compact = wl.layout == "compact"
+    maxl = int(lengths.max()) if compact else 0
+    vl = dict(compact=compact, max_seqlen_q=maxl, max_seqlen_k=maxl)
+    c = wl.sm_scale
+    ws_f = torch.zeros(_lib.attn_fwd_workspace_size(*q.shape), dtype=torch.uint8, device="cuda")
+    o, lse = forward(q, k, v, c, wl.causal, cu_q, cu_k, workspace=ws_f, **vl)
+    ws_b = None if a.fwd_only else bwd_workspace(q)
+    grads = [torch.empty_like(t) for t in (q, k, v)]
+
+    def run_fwd():
+        forward(q, k, v, c, wl.causal, cu_q, cu_k, out=o, lse=lse, workspace=ws_f, **vl)
+
+    def run_bwd():
+        backward(q, k, v, o, lse, do, c, wl.causal, cu_q, cu_k, dq=grads[0], dk=grads[1],
+                 dv=grads[2], workspace=ws_b, deterministic=a.deterministic, **vl)
+
+    pairs = wl.H * sum(unmasked_pairs(int(n), int(n), wl.causal) for n in lengths)
+    out = {"workload": a.workload, "lengths": [int(n) for n in lengths], "H": wl.H, "D": wl.D,
+           "causal": wl.causal, "dtype": "fp16" if a.fp16 else "bf16", "pairs": pairs}
+    _time_and_report(a, run_fwd, None if a.fwd_only else run_bwd, wl.D, pairs, out,
+                     (ws_f, ws_b))
+
+
+def _time_and_report(a, run_fwd, run_bwd, D, pairs, out, workspaces):
     def timed(fn):
         for _ in range(a.warmup):
             fn()
@@ -70,17 +118,14 @@ def main(argv=None):
         ts = sorted(s.elapsed_time(e) for s, e in ev)
         return ts[len(ts) // 2] if ts else float("nan")
 
-    pairs = a.B * a.H * unmasked_pairs(Sq, Sk, a.causal)
-    out = {"B": a.B, "H": a.H, "Sq": Sq, "Sk": Sk, "D": a.D, "causal": a.causal,
-           "dtype": "fp16" if a.fp16 else "bf16"}
     t = timed(run_fwd)
     out["fwd_ms"] = round(t, 4)
-    out["fwd_tflops"] = round(4 * a.D * pairs / (t * 1e-3) / 1e12, 1)
-    if not a.fwd_only:
+    out["fwd_tflops"] = round(4 * D * pairs / (t * 1e-3) / 1e12, 1)
+    if run_bwd is not None:
         t = timed(run_bwd)
         out["bwd_ms"] = round(t, 4)
-        out["bwd_tflops"] = round(10 * a.D * pairs / (t * 1e-3) / 1e12, 1)
-    for ws in (ws_f, ws_b):
+        out["bwd_tflops"] = round(10 * D * pairs / (t * 1e-3) / 1e12, 1)
+    for ws in workspaces:
         if ws is not None:
             st = _lib.attn_read_device_status(ws)
             if st != 0:

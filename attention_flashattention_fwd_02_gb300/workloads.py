@@ -100,14 +100,17 @@ def draw_lengths(wl: Workload, seed: Optional[int] = None) -> Optional[torch.Ten
     return _draw_lengths(wl, _generator(wl, seed))
 
 
-def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None, dtype=torch.bfloat16):
+def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None, dtype=torch.bfloat16,
+                lengths_k=None):
     """Draw the inputs of workload ``wl`` on the CPU.
 
     Returns a dict with 16-bit tensors q, k, v, do (BHSD views, see the module docstring),
-    and for varlen layouts int32 ``cu_seqlens_q``/``cu_seqlens_k`` (equal: the same
-    lengths serve queries and keys) plus ``lengths``. ``lengths`` may be passed to fix the
-    varlen lengths instead of drawing them (edge-case tests). ``dtype`` is the 16-bit element
-    type the fp32 draws are rounded to (bf16 or fp16).
+    and for varlen layouts int32 ``cu_seqlens_q``/``cu_seqlens_k`` plus ``lengths``. The same
+    lengths serve queries and keys unless ``lengths_k`` gives the key lengths (then
+    ``lengths_k`` is returned too; compact K/V tensors have sum(lengths_k) tokens, padded
+    ones keep the workload's Sk rows). ``lengths`` may be passed to fix the varlen lengths
+    instead of drawing them (edge-case tests). ``dtype`` is the 16-bit element type the fp32
+    draws are rounded to (bf16 or fp16).
     """
     g = _generator(wl, seed)
     out = {}
@@ -116,11 +119,14 @@ def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None, dtype=to
         if lengths is None:
             lengths = _draw_lengths(wl, g)
         lengths = torch.as_tensor(lengths, dtype=torch.int64)
-        T = int(lengths.sum())
-        thd = [_randn16((T, H, D), g, dtype) for _ in range(4)]
+        lk = lengths if lengths_k is None else torch.as_tensor(lengths_k, dtype=torch.int64)
+        Tq, Tk = int(lengths.sum()), int(lk.sum())
+        thd = [_randn16((T, H, D), g, dtype) for T in (Tq, Tk, Tk, Tq)]
         q, k, v, do = (t.transpose(0, 1).unsqueeze(0) for t in thd)
         cu = _cu(lengths)
-        out.update(cu_seqlens_q=cu, cu_seqlens_k=cu.clone(), lengths=lengths)
+        out.update(cu_seqlens_q=cu, cu_seqlens_k=_cu(lk), lengths=lengths)
+        if lengths_k is not None:
+            out["lengths_k"] = lk
     elif wl.layout == "padded":
         if lengths is None:
             lengths = _draw_lengths(wl, g)
@@ -130,7 +136,10 @@ def make_inputs(wl: Workload, seed: Optional[int] = None, lengths=None, dtype=to
         v = _randn16((B, H, wl.Sk, D), g, dtype)
         do = _randn16((B, H, wl.Sq, D), g, dtype)
         cu = _cu(lengths)
-        out.update(cu_seqlens_q=cu, cu_seqlens_k=cu.clone(), lengths=lengths)
+        lk = lengths if lengths_k is None else torch.as_tensor(lengths_k, dtype=torch.int64)
+        out.update(cu_seqlens_q=cu, cu_seqlens_k=_cu(lk), lengths=lengths)
+        if lengths_k is not None:
+            out["lengths_k"] = lk
     elif wl.layout == "kv_bshd":
         q = _randn16((B, H, wl.Sq, D), g, dtype)
         k = _randn16((B, wl.Sk, H, D), g, dtype).transpose(1, 2)

@@ -45,15 +45,31 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="dense2048")
+    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="padded")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--settle-s", type=float, default=1.0,
                     help="seconds of untimed steps before the timed region (clock settling)")
     ap.add_argument("--targets-workload", default="sweep8k",
                     help="second workload whose fwd / bwd fractions of peak are reported under "
-                         "'targets' (d_head 128, seqlen >= 4096); 'none' to skip")
+                         "'targets' (dense d_head 128, seqlen >= 4096); 'none' to skip")
+    ap.add_argument("--secondary", default="dense2048",
+                    help="comma-separated workloads reported as secondary lines under "
+                         "'secondary' (same measurement, fewer steps, no end-to-end leg); "
+                         "'none' to skip")
     return ap.parse_args()
+
+
+# tcgen05 kind::f16 dense rate per SM and clock (an M=128, N=256, K=16 product every 128
+# cycles, measured on GB300 with back-to-back MMAs): the clock-normalised denominator.
+TC_FLOP_PER_CLK_SM = 8192
+
+
+def clock_peak_tflops(sm_mhz, n_sm):
+    """Dense bf16 tensor peak at the SM clock seen during the timed region."""
+    if not sm_mhz or not n_sm:
+        return None
+    return sm_mhz * 1e6 * n_sm * TC_FLOP_PER_CLK_SM / 1e12
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -267,6 +283,8 @@ def run_ours(args, rank, world, dist, clocks_on=True):
     dom_fl = fwd_fl if dominant == "fwd" else bwd_fl
     achieved = dom_fl / (per_kernel[dominant] * 1e-3) / 1e12
     traffic = load_traffic(args.workload, dominant)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk_peak = clock_peak_tflops((clk or {}).get("sm_mhz"), n_sm)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
@@ -278,7 +296,12 @@ def run_ours(args, rank, world, dist, clocks_on=True):
         "roofline": {"bound": "tensor", "kernel": "attn_" + dominant, "achieved": round(achieved, 2),
                      "peak": peak_b, "unit": "TFLOP/s", "frac": round(achieved / peak_b, 4),
                      "peak_source": f"{peak_src} bf16 burst", "traffic": traffic,
-                     "frac_of_sustained": round(achieved / peak_s, 4)},
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
+                     "frac_of_sustained": round(achieved / peak_s, 4),
+                     "frac_clock": round(achieved / clk_peak, 4) if clk_peak else None,
+                     "clock_peak_tflops": round(clk_peak, 1) if clk_peak else None,
+                     "clock_peak_basis": f"median SM MHz x {n_sm} SMs x {TC_FLOP_PER_CLK_SM} "
+                                         "FLOP/clk/SM (tcgen05 dense bf16)"},
         "kernels": {
             "fwd_tflops": round(fwd_fl / (per_kernel["fwd"] * 1e-3) / 1e12, 2),
             "bwd_main_tflops": round(bwd_fl / (per_kernel["bwd_main"] * 1e-3) / 1e12, 2),
@@ -568,6 +591,25 @@ def main():
                              "bwd_frac_of_peak": t["kernels"]["bwd_frac_of_peak"],
                              "bwd_main_tflops": t["kernels"]["bwd_main_tflops"],
                              "steps": t["steps"], "gpu_launches": t["gpu_launches"]}
+    for name in ([] if args.secondary == "none" else args.secondary.split(",")):
+        if name == args.workload:
+            continue
+        import copy
+        sargs = copy.copy(args)
+        sargs.workload = name
+        sargs.steps = max(3, min(args.steps, 10))
+        sargs.settle_s = 0.3
+        sargs.no_e2e = True
+        t = run_ours(sargs, rank, world, dist)
+        result.setdefault("secondary", []).append(
+            {"config": t["config"], "value": t["value"], "unit": t["unit"],
+             "ms_per_step": t["ms_per_step"], "steps": t["steps"], "clocks": t["clocks"],
+             "roofline": {k: t["roofline"][k] for k in ("kernel", "achieved", "peak", "frac",
+                                                        "frac_clock", "traffic")},
+             "kernels": {k: t["kernels"][k] for k in ("fwd_tflops", "fwd_frac_of_peak",
+                                                      "bwd_main_tflops", "bwd_tflops",
+                                                      "bwd_frac_of_peak")},
+             "gpu_launches": t["gpu_launches"]})
     if rank == 0 and not args.no_cpu_baseline:
         v, s, desc = oracle_sample(args.workload)
         result["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOPS", "cores": cpu_cores(),

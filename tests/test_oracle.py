@@ -275,6 +275,92 @@ def test_dense_bhsd_matches_torch_sdpa():
     np.testing.assert_allclose(o, to.numpy(), atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_bhsd_dense_matches_torch_autograd(causal):
+    """The batched dense backward equals PyTorch's float64 SDPA autograd run on the whole
+    (B, H, S, D) tensors at once: every (b, h) gradient slice lands in its own place."""
+    wl = _small("cross", B=2, H=3, Sq=9, Sk=13, D=5, causal=causal, layout="bhsd")
+    x = make_inputs(wl)
+    q, k, v, do = (x[n].double() for n in ("q", "k", "v", "do"))
+    dq, dk, dv = ref.bwd_bhsd(q.numpy(), k.numpy(), v.numpy(), do.numpy(), wl.sm_scale, causal)
+    tq, tk, tv = (t.clone().requires_grad_(True) for t in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal,
+                                                          scale=wl.sm_scale)
+    to.backward(do)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def _torch_head(Q, K, V, dO, c, causal):
+    """O, LSE, dQ, dK, dV of one head from PyTorch's float64 SDPA, logsumexp and autograd
+    (top-left causal mask, as is_causal builds it)."""
+    tq, tk, tv = (torch.tensor(t, requires_grad=True) for t in (Q, K, V))
+    to = torch.nn.functional.scaled_dot_product_attention(tq[None], tk[None], tv[None],
+                                                          is_causal=causal, scale=c)[0]
+    to.backward(torch.tensor(dO))
+    S = c * torch.tensor(Q) @ torch.tensor(K).T
+    if causal:
+        S = S.masked_fill(~torch.ones(S.shape, dtype=torch.bool).tril(), float("-inf"))
+    return (to.detach().numpy(), torch.logsumexp(S, dim=1).numpy(), tq.grad.numpy(),
+            tk.grad.numpy(), tv.grad.numpy())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_padded_bhsd_distinct_q_and_k_lengths(causal):
+    """Padded varlen with different query and key lengths per batch and different Sq / Sk
+    tensor extents: batch b's queries are rows [0, lq[b]) and its keys rows [0, lk[b]) of its
+    own slice. Each (b, h) slice of the forward and backward equals PyTorch on that slice;
+    rows past lq (dQ, O, LSE) or lk (dK, dV) are not outputs. A swap of the query and key
+    lengths anywhere would change the slice shapes and fail."""
+    lq, lk = [24, 7, 1], [10, 24, 3]
+    wl = _small("padded", B=3, H=2, Sq=24, Sk=30, D=8, causal=causal)
+    x = make_inputs(wl, lengths=lq, lengths_k=lk)
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    cu_q, cu_k = x["cu_seqlens_q"].numpy(), x["cu_seqlens_k"].numpy()
+    assert list(cu_q) == [0, 24, 31, 32] and list(cu_k) == [0, 10, 34, 37]
+    c = wl.sm_scale
+    o, lse = ref.fwd_bhsd(q, k, v, c, causal, cu_q, cu_k)
+    dq, dk, dv = ref.bwd_bhsd(q, k, v, do, c, causal, cu_q, cu_k)
+    assert dk.shape == (3, 2, 30, 8) and dq.shape == (3, 2, 24, 8)
+    for b in range(3):
+        nq, nk = lq[b], lk[b]
+        assert np.isnan(o[b, :, nq:]).all() and np.isnan(lse[b, :, nq:]).all()
+        assert np.isnan(dq[b, :, nq:]).all()
+        assert np.isnan(dk[b, :, nk:]).all() and np.isnan(dv[b, :, nk:]).all()
+        for h in range(2):
+            O, L, gq, gk, gv = _torch_head(q[b, h, :nq], k[b, h, :nk], v[b, h, :nk],
+                                           do[b, h, :nq], c, causal)
+            np.testing.assert_allclose(o[b, h, :nq], O, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(lse[b, h, :nq], L, rtol=1e-13, atol=1e-13)
+            np.testing.assert_allclose(dq[b, h, :nq], gq, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(dk[b, h, :nk], gk, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(dv[b, h, :nk], gv, rtol=1e-10, atol=1e-12)
+
+
+def test_compact_distinct_q_and_k_lengths():
+    """Compact varlen with different query and key lengths: sequence s owns query rows
+    [cu_q[s], cu_q[s+1]) and key rows [cu_k[s], cu_k[s+1]); each slice equals PyTorch."""
+    lq, lk = [5, 1, 12, 9], [9, 4, 3, 9]
+    wl = _small("compact", H=2, D=6, n_seqs=4, causal=True)
+    x = make_inputs(wl, lengths=lq, lengths_k=lk)
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    assert q.shape[2] == sum(lq) and k.shape[2] == sum(lk)
+    cq, ck = x["cu_seqlens_q"].numpy(), x["cu_seqlens_k"].numpy()
+    o, lse = ref.fwd_compact_varlen(q, k, v, cq, ck, wl.sm_scale, True)
+    dq, dk, dv = ref.bwd_compact_varlen(q, k, v, do, cq, ck, wl.sm_scale, True)
+    for s in range(4):
+        qa, qb, ka, kb = cq[s], cq[s + 1], ck[s], ck[s + 1]
+        for h in range(2):
+            O, L, gq, gk, gv = _torch_head(q[0, h, qa:qb], k[0, h, ka:kb], v[0, h, ka:kb],
+                                           do[0, h, qa:qb], wl.sm_scale, True)
+            np.testing.assert_allclose(o[0, h, qa:qb], O, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(lse[0, h, qa:qb], L, rtol=1e-13, atol=1e-13)
+            np.testing.assert_allclose(dq[0, h, qa:qb], gq, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(dk[0, h, ka:kb], gk, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(dv[0, h, ka:kb], gv, rtol=1e-10, atol=1e-12)
+
+
 # ---------------------------------------------------------------- input recipe
 def test_workload_recipe_shapes_and_strides():
     x = make_inputs(WORKLOADS["cross"].replace(B=1, H=2, Sq=4, Sk=8, D=16))

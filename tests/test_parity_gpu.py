@@ -114,6 +114,28 @@ def test_padded_varlen_parity(D, causal):
             torch.testing.assert_close(g[b, :, :n], g2[b, :, :n], atol=2e-2, rtol=2e-2)
 
 
+@pytest.mark.parametrize("D,causal", [(128, True), (64, True), (128, False), (64, False)])
+def test_padded_distinct_q_and_k_lengths(D, causal):
+    """Padded varlen with cu_seqlens_q != cu_seqlens_k and Sq != Sk tensor extents: batch
+    b's queries are rows [0, lq[b]) and its keys rows [0, lk[b]) of its own slice. Query
+    rows past lq (O, LSE, dQ) and key rows past lk (dK, dV) keep their NaN sentinels."""
+    lq, lk = [300, 129, 1, 77, 0], [200, 410, 3, 1, 50]
+    wl = WORKLOADS["padded"].replace(B=5, H=2, Sq=300, Sk=410, D=D, causal=causal,
+                                     seed=13 + D + causal)
+    x = make_inputs(wl, lengths=lq, lengths_k=lk)
+    o, lse, grads = _run_dense(x, wl.sm_scale, causal, padded=True)
+    o_r, lse_r, grads_r = _oracle_dense(x, wl.sm_scale, causal, padded=True)
+    assert_fwd_close(o, lse, o_r, lse_r, what="padded lq != lk")
+    assert_grads_close(grads, grads_r, what="padded lq != lk")
+    for b in range(len(lq)):
+        assert torch.isnan(o[b, :, lq[b]:]).all() and torch.isnan(lse[b, :, lq[b]:]).all()
+        assert torch.isnan(grads[0][b, :, lq[b]:]).all()
+        assert torch.isnan(grads[1][b, :, lk[b]:]).all()
+        assert torch.isnan(grads[2][b, :, lk[b]:]).all()
+    # keys no query reaches (batch 4 has no queries) get zero dK and dV
+    assert torch.all(grads[1][4, :, :50] == 0) and torch.all(grads[2][4, :, :50] == 0)
+
+
 def _run_compact(x, scale, causal, T_extra=0, max_q=0, max_k=0):
     g = _cuda(x)
     q, k, v, do = g["q"], g["k"], g["v"], g["do"]
@@ -158,6 +180,23 @@ def test_compact_varlen_parity(D, causal):
     assert torch.isnan(o[:, :, T:]).all() and torch.isnan(lse[:, :, T:]).all()
     for g in grads:
         assert torch.isnan(g[:, :, T:]).all()
+
+
+@pytest.mark.parametrize("D,causal", [(128, True), (64, False)])
+def test_compact_distinct_q_and_k_lengths(D, causal):
+    """Compact varlen with different query and key lengths per sequence (and so different
+    token counts Tq and Tk)."""
+    lq, lk = [1, 130, 64, 257, 7, 128], [130, 1, 300, 64, 129, 7]
+    wl = WORKLOADS["compact"].replace(H=2, D=D, causal=causal, n_seqs=len(lq),
+                                      seed=23 + D + causal)
+    x = make_inputs(wl, lengths=lq, lengths_k=lk)
+    o, lse, grads = _run_compact(x, wl.sm_scale, causal)
+    q, k, v, do = (np64(x[n]) for n in ("q", "k", "v", "do"))
+    cq, ck = x["cu_seqlens_q"].numpy(), x["cu_seqlens_k"].numpy()
+    o_r, lse_r = ref.fwd_compact_varlen(q, k, v, cq, ck, wl.sm_scale, causal)
+    g_r = ref.bwd_compact_varlen(q, k, v, do, cq, ck, wl.sm_scale, causal)
+    assert_fwd_close(o, lse, o_r, lse_r, what="compact lq != lk")
+    assert_grads_close(grads, g_r, what="compact lq != lk")
 
 
 def test_compact_varlen_indexing_exact():
