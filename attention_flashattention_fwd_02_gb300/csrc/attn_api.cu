@@ -308,7 +308,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
 
   FwdParams p;
   memset(&p, 0, sizeof(p));
-  const int BM = fwd_block_m(kernel_width(pr.D));
+  const int BM = fwd_block_m(kernel_width(pr.D), bias != nullptr);
   if ((s = make_map(&p.tm_q, q, fwd_box_rows())) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_k, k, 128)) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_v, v, 128)) != ATTN_OK) return s;

@@ -14,18 +14,18 @@
 //                            LSE that the forward pass stashed.
 //  3. attn_bwd_post_kernel   dQ = sm_scale * accumulator, rounded to the element type.
 //
-// Main-kernel warp roles (512 threads, four warpgroups): warps 0..7 are two compute
-// warpgroups that split the query columns of each key row (thread row j = TMEM lane j) to
-// form P^T (written to TMEM, where it is the A operand of the dV MMA) and dS^T (written to
-// shared memory for the dK and dQ MMAs), and at the end write dK / dV. Warp 8 is the TMA
-// producer; warp 9 allocates TMEM and issues the MMAs; warps 10 and 11 have no role. Warps
-// 12..15 drain each step's dQ partial from TMEM into the global fp32 accumulator (each warp
-// the 32 TMEM lanes it can reach, staged in shared memory as two 32 x 32 blocks and added
-// with TMA reduce-adds) while the compute warps already work on the next step. Register
-// budgets are moved between the warpgroups (setmaxnreg): the compute warpgroups hold a step's
-// scores in registers. Tile sizes: 128 keys per CTA; 64 query rows per step when
-// d_head = 128 (dQ is formed transposed, K_n^T dS^T, so that every MMA has M = 128), 128
-// when d_head = 64.
+// Main-kernel warp roles: warps 0..7 are two compute warpgroups that split the query
+// columns of each key row (thread row j = TMEM lane j) to form P^T (written to TMEM, where it
+// is the A operand of the dV MMA) and dS^T (written to shared memory for the dK and dQ MMAs),
+// and at the end write dK / dV. Warp 8 is the TMA producer; warp 9 allocates TMEM and issues
+// the MMAs. Each step's dQ partial goes from TMEM into the global fp32 accumulator through
+// shared-memory staging and TMA reduce-adds: at d_head 128 (512 threads) warps 12..15 do this
+// (each the 32 TMEM lanes it can reach) while the compute warps already work on the next
+// step, and warps 10, 11 have no role; at d_head 64 (320 threads; the compute warps hold a
+// step's 128 score columns in registers, and a CTA of more warps would leave each fewer than
+// that needs) every compute warp drains its own 32 x 32 block after forming the next step's
+// P and dS. Tile sizes: 128 keys per CTA; 64 query rows per step when d_head = 128 (dQ is
+// formed transposed, K_n^T dS^T, so that every MMA has M = 128), 128 when d_head = 64.
 #include <atomic>
 
 #include "attn_common.cuh"
@@ -163,14 +163,13 @@ struct BwdCfg {
   static constexpr int OFF_Q = OFF_V + KV_BYTES;        // QST stages
   static constexpr int OFF_DO = OFF_Q + QST * Q_BYTES;  // QST stages
   static constexpr int OFF_DS = OFF_DO + QST * Q_BYTES; // 2 buffers
-  // dQ staging, 8 KB per drain warp (two 32 x 32 fp32 blocks). At d_head 64 the drain warps
-  // stage in the dS^T buffer of the step they drain, whose readers (the dK and dQ products)
-  // have completed, so no extra space is needed; the compute warps rewrite that buffer two
-  // steps later, once the reduce-adds have read it (stg_free).
-  static constexpr bool STAGE_IN_DS = !DQ_T;
+  // dQ drain: a warpgroup of its own at d_head 128, staging in a dedicated area (8 KB per
+  // drain warp: two 32 x 32 fp32 blocks); at d_head 64 the compute warps, each staging its
+  // 32 x 32 block in rows of the dS^T buffer it has just released (only that warp writes those
+  // rows again, two steps later, after waiting for the reduce to read them).
+  static constexpr bool DQ_WARPS = DQ_T;
   static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;
-  static constexpr int STG_BYTES = DQ_T ? 4 * 8192 : 0;
-  static_assert(STAGE_IN_DS ? DS_BYTES == 4 * 8192 : true, "one 8 KB slice per drain warp");
+  static constexpr int STG_BYTES = DQ_WARPS ? 4 * 8192 : 0;
   // d_head 64: the score products also subtract LSE / sm_scale and Delta, through one more
   // K = 16 step that multiplies a tile of ones by those values (each split into three bf16
   // parts), so the compute warps read neither per column. The K = 16 operand tiles (32 bytes
@@ -189,16 +188,10 @@ struct BwdCfg {
   static constexpr uint32_t COL_DQ = 2 * D + 2 * BM;
   static constexpr uint32_t COL_P = COL_DQ + (DQ_T ? BM : D);
   static_assert(COL_P + BM / 2 <= TMEM_COLS, "TMEM layout does not fit");
-  // warpgroups: 0, 1 compute; 2 producer (warp 8) and MMA issuer (warp 9); 3 dQ drain
-  static constexpr int NTHREADS = 512;
+  // warpgroups: 0, 1 compute; 2 producer (warp 8) and MMA issuer (warp 9); 3 (d_head 128)
+  // dQ drain. 512 threads leave 128 registers a thread, which the d_head 128 roles fit in
+  static constexpr int NTHREADS = DQ_WARPS ? 512 : 320;
   static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_DRAIN0 = 12;
-  // register budgets per thread (launch: 65536 / 512 = 128): every warp scheduler holds two
-  // compute warps, one warp of warpgroup 2 and one drain warp, 168 + 168 + 88 + 88 = 512 of
-  // its 512; the CTA total 128 x (2 x 168 + 88 + 88) = 65536 of 65536. Every warp returns to
-  // the launch budget before the common exit.
-  static constexpr uint32_t REG_LAUNCH = 128, REG_COMPUTE = 168, REG_AUX = 88, REG_DRAIN = 88;
-  static_assert(REG_LAUNCH * NTHREADS == 65536, "launch budget");
-  static_assert(128 * (2 * REG_COMPUTE + REG_AUX + REG_DRAIN) <= 65536, "register budgets");
 };
 
 template <int BM, int QST, int LSE_ST>
@@ -207,7 +200,6 @@ struct BwdBars {
   uint64_t q_full[QST], q_empty[QST];
   uint64_t s_full, s_free, p_full, p_empty;
   uint64_t ds_full[2];
-  uint64_t stg_free[2];  // d_head 64: the reduce-adds staged in dS buffer b have read it
   uint64_t dq_full, dq_empty, dkdv_full;
   uint64_t mma_drain;  // completion of the MMA warp's last products
   uint32_t tmem_base;
@@ -221,7 +213,8 @@ struct BwdBars {
 // straight from global memory (a warp reads 32 consecutive keys of one query row per load)
 // and, when p.dbias is set, writes dS to the same places.
 template <int D, bool F16, bool BIAS = false>
-__global__ void __launch_bounds__(512, 1) attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
+    attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   static_assert(!BIAS || D == 64, "bias kernels exist for the 64-wide configuration only");
   using C = BwdCfg<D>;
   constexpr int BN = C::BN, BM = C::BM;
@@ -282,16 +275,13 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_main_kernel(const __grid_cons
       mbar_init(smem_u32(&bars.q_full[s]), 33);  // producer lane 0 (tx) + 32 lanes (LSE/Delta)
       mbar_init(smem_u32(&bars.q_empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&bars.ds_full[s]), 256);
-      mbar_init(smem_u32(&bars.stg_free[s]), 4);  // lane 0 of each drain warp
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(smem_u32(&bars.ds_full[s]), 256);
     mbar_init(smem_u32(&bars.s_full), 1);
     mbar_init(smem_u32(&bars.s_free), 256);
     mbar_init(smem_u32(&bars.p_full), 256);
     mbar_init(smem_u32(&bars.p_empty), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
-    mbar_init(smem_u32(&bars.dq_empty), 128);  // the drain warps
+    mbar_init(smem_u32(&bars.dq_empty), C::DQ_WARPS ? 128 : 256);  // the draining warps
     mbar_init(smem_u32(&bars.dkdv_full), 1);
     mbar_init(smem_u32(&bars.mma_drain), 1);
     mbar_fence_init();
@@ -305,178 +295,171 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_main_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort = &bars.abort;
-  // Each warpgroup sets its register budget on entering its roles and returns to the launch
-  // budget before the common exit, so that every instruction runs under one known budget.
-  if (warp >= 8 && warp < C::WARP_DRAIN0) {
-    reg_budget_dec<C::REG_AUX>();
-    if (warp == C::WARP_PRODUCER) {
-      // ------------------------------------------------------------------ producer
-      if (lane == 0) {
-        tma_prefetch_map(&p.tm_q);
-        tma_prefetch_map(&p.tm_k);
-        tma_prefetch_map(&p.tm_v);
-        tma_prefetch_map(&p.tm_do);
-        const uint32_t kvb = smem_u32(&bars.kv_full);
-        mbar_arrive_expect_tx(kvb, 2 * C::KV_BYTES);
+  if (warp == C::WARP_PRODUCER) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&p.tm_q);
+      tma_prefetch_map(&p.tm_k);
+      tma_prefetch_map(&p.tm_v);
+      tma_prefetch_map(&p.tm_do);
+      const uint32_t kvb = smem_u32(&bars.kv_full);
+      mbar_arrive_expect_tx(kvb, 2 * C::KV_BYTES);
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s) {
-          tma_load_4d(sK + s * BN * 128, &p.tm_k, kvb, s * 64, sv.row0_k + k_lo, h, sv.batch);
-          tma_load_4d(sV + s * BN * 128, &p.tm_v, kvb, s * 64, sv.row0_k + k_lo, h, sv.batch);
-        }
-      }
-      // Row r of 32-byte column group grp of the augmented operands: (a, b, c, 0, ..., 0) as bf16.
-      auto aug_row = [&](int grp, int r, float a, float b, float c) {
-        uint8_t* row = smem + C::OFF_AUG + (grp >> 2) * (BN * 128) + r * 128;
-        const int c0 = 2 * (grp & 3);
-        *reinterpret_cast<uint4*>(row + 16 * (c0 ^ (r & 7))) =
-            make_uint4(pack_bf16x2(a, b), pack_bf16x2(c, 0.f), 0u, 0u);
-        *reinterpret_cast<uint4*>(row + 16 * ((c0 + 1) ^ (r & 7))) = make_uint4(0u, 0u, 0u, 0u);
-      };
-      // v as the sum of three bf16 values (about 24 significant bits)
-      auto aug_split = [&](int grp, int r, float v) {
-        const float hi = __bfloat162float(__float2bfloat16_rn(v));
-        const float r1 = v - hi;
-        const float mid = __bfloat162float(__float2bfloat16_rn(r1));
-        aug_row(grp, r, hi, mid, r1 - mid);
-      };
-      if (C::AUG)  // the ones tile, made visible to the MMAs by the first step's q_full arrival
-        for (int r = lane; r < BN; r += 32) aug_row(0, r, 1.f, 1.f, 1.f);
-      int last_it[QST];  // last step loaded into each stage (-1: none)
-#pragma unroll
-      for (int st = 0; st < QST; ++st) last_it[st] = -1;
-      for (int it = 0; it < n_steps; ++it) {
-        const int st = it % QST;
-        if (it == p.withhold_step) continue;  // failure-detection test: this stage never fills
-        if (it >= QST &&
-            !mbar_wait(smem_u32(&bars.q_empty[st]), ((it / QST) - 1) & 1, abort, p.timeout_ns))
-          break;
-        last_it[st] = it;
-        const int q_lo = q_tile(it) * BM;
-        const uint32_t qb = smem_u32(&bars.q_full[st]);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(qb, 2 * C::Q_BYTES);
-#pragma unroll
-          for (int s = 0; s < D / 64; ++s) {
-            tma_load_4d(sQ + st * C::Q_BYTES + s * BM * 128, &p.tm_q, qb, s * 64, sv.row0_q + q_lo, h,
-                        sv.batch);
-            tma_load_4d(sDO + st * C::Q_BYTES + s * BM * 128, &p.tm_do, qb, s * 64, sv.row0_q + q_lo,
-                        h, sv.batch);
-          }
-        }
-        for (int i = lane; i < BM; i += 32) {
-          const int q = q_lo + i;
-          float l2 = 0.f, dl = 0.f;
-          if (q < sv.len_q) {
-            const int64_t grow = sv.row0_q + q;
-            l2 = p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] * kLog2e;
-            dl = p.delta[zh * p.rows_q + grow];
-          }
-          if constexpr (C::AUG) {
-            // c2 (S + a) = c2 S - LSE log2(e) with a = -LSE / sm_scale
-            aug_split(1 + st, i, -l2 / p.scale_log2);
-            aug_split(4 + st, i, -dl);
-          } else {
-            bars.nlse2[st][i] = -l2;
-            bars.ndelta[st][i] = -dl;
-          }
-        }
-        if (C::AUG) fence_proxy_async_smem();  // the rows are read by the MMAs (async proxy)
-        mbar_arrive(qb);
-      }
-      if (lane == 0 && *abort) {  // the consumers gave up: let the copies in flight land
-        mbar_wait_drain(smem_u32(&bars.kv_full), 0, p.timeout_ns);
-#pragma unroll
-        for (int st = 0; st < QST; ++st)
-          if (last_it[st] >= 0)
-            mbar_wait_drain(smem_u32(&bars.q_full[st]), (last_it[st] / QST) & 1, p.timeout_ns);
-      }
-    } else if (warp == C::WARP_MMA) {
-      // ------------------------------------------------------------------ MMA issuer
-      // Issue order per step: S/dP(it+1) as soon as the compute warpgroups have loaded S^T and
-      // dP^T of step it (so the next step's scores are ready when their P/dS math ends), then
-      // dV(it) [P from TMEM], dK(it), dQ(it). The whole warp walks the schedule, so that every
-      // descriptor is warp-uniform; one elected lane issues.
-      {
-        constexpr uint32_t idS = idesc_f32acc(128, BM, false, false, F16);  // S^T, dP^T
-        constexpr uint32_t idG = idesc_f32acc(128, D, false, true, F16);    // dV, dK
-        constexpr uint32_t idQ = C::DQ_T ? idesc_f32acc(128, BM, true, true, F16)  // dQ^T
-                                         : idesc_f32acc(128, D, true, true, F16);  // dQ
-        const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP, tP = tmem + C::COL_P;
-        const uint32_t tDK = tmem + C::COL_DK, tDV = tmem + C::COL_DV, tDQ = tmem + C::COL_DQ;
-        const uint64_t k_kd = desc_kmajor(sK, BN, 0), v_kd = desc_kmajor(sV, BN, 0);
-        const uint64_t k_mn = desc_mnmajor(sK, BN, 0);
-        const uint64_t q_kd = desc_kmajor(sQ, BM, 0), do_kd = desc_kmajor(sDO, BM, 0);
-        const uint64_t q_mn = desc_mnmajor(sQ, BM, 0), do_mn = desc_mnmajor(sDO, BM, 0);
-        const uint64_t ds_kd = desc_kmajor(sDS, BN, 0), ds_mn = desc_mnmajor(sDS, BN, 0);
-        const uint64_t aug_kd = desc_kmajor(sAUG, BN, 0);
-        constexpr uint32_t QSTEP = C::Q_BYTES >> 4, DSSTEP = C::DS_BYTES >> 4;
-        auto issue_sdp = [&](int it) -> bool {
-          const int st = it % QST;
-          if (!mbar_wait(smem_u32(&bars.q_full[st]), (it / QST) & 1, abort, p.timeout_ns))
-            return false;
-          tc_fence_after();
-          const uint32_t qo = st * QSTEP;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss_w(tS, k_kd + kmajor_step(BN, kk), q_kd + qo + kmajor_step(BM, kk), idS, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss_w(tDP, v_kd + kmajor_step(BN, kk), do_kd + qo + kmajor_step(BM, kk), idS,
-                      kk > 0);
-          if constexpr (C::AUG) {  // S^T - LSE / sm_scale and dP^T - Delta (always bf16 operands)
-            constexpr uint32_t idA = idesc_f32acc(128, BM, false, false, false);
-            umma_ss_w(tS, aug_kd, aug_kd + kmajor_step(BN, 1 + st), idA, 1);
-            umma_ss_w(tDP, aug_kd, aug_kd + kmajor_step(BN, 4 + st), idA, 1);
-          }
-          umma_commit_w(smem_u32(&bars.s_full));
-          return true;
-        };
-        bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort, p.timeout_ns) && issue_sdp(0);
-        for (int it = 0; ok && it < n_steps; ++it) {
-          const int st = it % QST, bs = it & 1;
-          const uint32_t qo = st * QSTEP, dso = bs * DSSTEP;
-          if (it + 1 < n_steps) {
-            // S^T / dP^T of step it are in registers of the compute warpgroups: overwrite them
-            if (!mbar_wait(smem_u32(&bars.s_free), it & 1, abort, p.timeout_ns)) break;
-            if (!issue_sdp(it + 1)) break;
-          }
-          if (!mbar_wait(smem_u32(&bars.p_full), it & 1, abort, p.timeout_ns)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk)
-            umma_ts_w(tDV, tP + kk * 8, do_mn + qo + mnmajor_step(kk), idG, (it > 0 || kk > 0));
-          umma_commit_w(smem_u32(&bars.p_empty));  // P^T of step it read: the next P may land
-          if (!mbar_wait(smem_u32(&bars.ds_full[bs]), (it >> 1) & 1, abort, p.timeout_ns)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk)
-            umma_ss_w(tDK, ds_kd + dso + kmajor_step(BN, kk), q_mn + qo + mnmajor_step(kk), idG,
-                      (it > 0 || kk > 0));
-          if (p.with_dq) {
-            if (it > 0 &&
-                !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, p.timeout_ns))
-              break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              if (C::DQ_T)
-                umma_ss_w(tDQ, k_mn + mnmajor_step(kk), ds_mn + dso + mnmajor_step(kk), idQ, kk > 0);
-              else
-                umma_ss_w(tDQ, ds_mn + dso + mnmajor_step(kk), k_mn + mnmajor_step(kk), idQ, kk > 0);
-            }
-          }
-          umma_commit_w(smem_u32(&bars.q_empty[st]));
-          if (p.with_dq) umma_commit_w(smem_u32(&bars.dq_full));
-        }
-        umma_commit_w(smem_u32(&bars.dkdv_full));
-        // every product this warp issued has completed before tensor memory is released
-        umma_commit_w(smem_u32(&bars.mma_drain));
-        mbar_wait_drain(smem_u32(&bars.mma_drain), 0, p.timeout_ns);
+      for (int s = 0; s < D / 64; ++s) {
+        tma_load_4d(sK + s * BN * 128, &p.tm_k, kvb, s * 64, sv.row0_k + k_lo, h, sv.batch);
+        tma_load_4d(sV + s * BN * 128, &p.tm_v, kvb, s * 64, sv.row0_k + k_lo, h, sv.batch);
       }
     }
-    reg_budget_inc<C::REG_LAUNCH>();
+    // Row r of 32-byte column group grp of the augmented operands: (a, b, c, 0, ..., 0) as bf16.
+    auto aug_row = [&](int grp, int r, float a, float b, float c) {
+      uint8_t* row = smem + C::OFF_AUG + (grp >> 2) * (BN * 128) + r * 128;
+      const int c0 = 2 * (grp & 3);
+      *reinterpret_cast<uint4*>(row + 16 * (c0 ^ (r & 7))) =
+          make_uint4(pack_bf16x2(a, b), pack_bf16x2(c, 0.f), 0u, 0u);
+      *reinterpret_cast<uint4*>(row + 16 * ((c0 + 1) ^ (r & 7))) = make_uint4(0u, 0u, 0u, 0u);
+    };
+    // v as the sum of three bf16 values (about 24 significant bits)
+    auto aug_split = [&](int grp, int r, float v) {
+      const float hi = __bfloat162float(__float2bfloat16_rn(v));
+      const float r1 = v - hi;
+      const float mid = __bfloat162float(__float2bfloat16_rn(r1));
+      aug_row(grp, r, hi, mid, r1 - mid);
+    };
+    if (C::AUG)  // the ones tile, made visible to the MMAs by the first step's q_full arrival
+      for (int r = lane; r < BN; r += 32) aug_row(0, r, 1.f, 1.f, 1.f);
+    int last_it[QST];  // last step loaded into each stage (-1: none)
+#pragma unroll
+    for (int st = 0; st < QST; ++st) last_it[st] = -1;
+    for (int it = 0; it < n_steps; ++it) {
+      const int st = it % QST;
+      if (it == p.withhold_step) continue;  // failure-detection test: this stage never fills
+      if (it >= QST &&
+          !mbar_wait(smem_u32(&bars.q_empty[st]), ((it / QST) - 1) & 1, abort, p.timeout_ns))
+        break;
+      last_it[st] = it;
+      const int q_lo = q_tile(it) * BM;
+      const uint32_t qb = smem_u32(&bars.q_full[st]);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(qb, 2 * C::Q_BYTES);
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s) {
+          tma_load_4d(sQ + st * C::Q_BYTES + s * BM * 128, &p.tm_q, qb, s * 64, sv.row0_q + q_lo, h,
+                      sv.batch);
+          tma_load_4d(sDO + st * C::Q_BYTES + s * BM * 128, &p.tm_do, qb, s * 64, sv.row0_q + q_lo,
+                      h, sv.batch);
+        }
+      }
+      for (int i = lane; i < BM; i += 32) {
+        const int q = q_lo + i;
+        float l2 = 0.f, dl = 0.f;
+        if (q < sv.len_q) {
+          const int64_t grow = sv.row0_q + q;
+          l2 = p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] * kLog2e;
+          dl = p.delta[zh * p.rows_q + grow];
+        }
+        if constexpr (C::AUG) {
+          // c2 (S + a) = c2 S - LSE log2(e) with a = -LSE / sm_scale
+          aug_split(1 + st, i, -l2 / p.scale_log2);
+          aug_split(4 + st, i, -dl);
+        } else {
+          bars.nlse2[st][i] = -l2;
+          bars.ndelta[st][i] = -dl;
+        }
+      }
+      if (C::AUG) fence_proxy_async_smem();  // the rows are read by the MMAs (async proxy)
+      mbar_arrive(qb);
+    }
+    if (lane == 0 && *abort) {  // the consumers gave up: let the copies in flight land
+      mbar_wait_drain(smem_u32(&bars.kv_full), 0, p.timeout_ns);
+#pragma unroll
+      for (int st = 0; st < QST; ++st)
+        if (last_it[st] >= 0)
+          mbar_wait_drain(smem_u32(&bars.q_full[st]), (last_it[st] / QST) & 1, p.timeout_ns);
+    }
+  } else if (warp == C::WARP_MMA) {
+    // ------------------------------------------------------------------ MMA issuer
+    // Issue order per step: S/dP(it+1) as soon as the compute warpgroups have loaded S^T and
+    // dP^T of step it (so the next step's scores are ready when their P/dS math ends), then
+    // dV(it) [P from TMEM], dK(it), dQ(it). The whole warp walks the schedule, so that every
+    // descriptor is warp-uniform; one elected lane issues.
+    {
+      constexpr uint32_t idS = idesc_f32acc(128, BM, false, false, F16);  // S^T, dP^T
+      constexpr uint32_t idG = idesc_f32acc(128, D, false, true, F16);    // dV, dK
+      constexpr uint32_t idQ = C::DQ_T ? idesc_f32acc(128, BM, true, true, F16)  // dQ^T
+                                       : idesc_f32acc(128, D, true, true, F16);  // dQ
+      const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP, tP = tmem + C::COL_P;
+      const uint32_t tDK = tmem + C::COL_DK, tDV = tmem + C::COL_DV, tDQ = tmem + C::COL_DQ;
+      const uint64_t k_kd = desc_kmajor(sK, BN, 0), v_kd = desc_kmajor(sV, BN, 0);
+      const uint64_t k_mn = desc_mnmajor(sK, BN, 0);
+      const uint64_t q_kd = desc_kmajor(sQ, BM, 0), do_kd = desc_kmajor(sDO, BM, 0);
+      const uint64_t q_mn = desc_mnmajor(sQ, BM, 0), do_mn = desc_mnmajor(sDO, BM, 0);
+      const uint64_t ds_kd = desc_kmajor(sDS, BN, 0), ds_mn = desc_mnmajor(sDS, BN, 0);
+      const uint64_t aug_kd = desc_kmajor(sAUG, BN, 0);
+      constexpr uint32_t QSTEP = C::Q_BYTES >> 4, DSSTEP = C::DS_BYTES >> 4;
+      auto issue_sdp = [&](int it) -> bool {
+        const int st = it % QST;
+        if (!mbar_wait(smem_u32(&bars.q_full[st]), (it / QST) & 1, abort, p.timeout_ns))
+          return false;
+        tc_fence_after();
+        const uint32_t qo = st * QSTEP;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss_w(tS, k_kd + kmajor_step(BN, kk), q_kd + qo + kmajor_step(BM, kk), idS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss_w(tDP, v_kd + kmajor_step(BN, kk), do_kd + qo + kmajor_step(BM, kk), idS,
+                    kk > 0);
+        if constexpr (C::AUG) {  // S^T - LSE / sm_scale and dP^T - Delta (always bf16 operands)
+          constexpr uint32_t idA = idesc_f32acc(128, BM, false, false, false);
+          umma_ss_w(tS, aug_kd, aug_kd + kmajor_step(BN, 1 + st), idA, 1);
+          umma_ss_w(tDP, aug_kd, aug_kd + kmajor_step(BN, 4 + st), idA, 1);
+        }
+        umma_commit_w(smem_u32(&bars.s_full));
+        return true;
+      };
+      bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort, p.timeout_ns) && issue_sdp(0);
+      for (int it = 0; ok && it < n_steps; ++it) {
+        const int st = it % QST, bs = it & 1;
+        const uint32_t qo = st * QSTEP, dso = bs * DSSTEP;
+        if (it + 1 < n_steps) {
+          // S^T / dP^T of step it are in registers of the compute warpgroups: overwrite them
+          if (!mbar_wait(smem_u32(&bars.s_free), it & 1, abort, p.timeout_ns)) break;
+          if (!issue_sdp(it + 1)) break;
+        }
+        if (!mbar_wait(smem_u32(&bars.p_full), it & 1, abort, p.timeout_ns)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_ts_w(tDV, tP + kk * 8, do_mn + qo + mnmajor_step(kk), idG, (it > 0 || kk > 0));
+        umma_commit_w(smem_u32(&bars.p_empty));  // P^T of step it read: the next P may land
+        if (!mbar_wait(smem_u32(&bars.ds_full[bs]), (it >> 1) & 1, abort, p.timeout_ns)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_ss_w(tDK, ds_kd + dso + kmajor_step(BN, kk), q_mn + qo + mnmajor_step(kk), idG,
+                    (it > 0 || kk > 0));
+        if (p.with_dq) {
+          if (it > 0 &&
+              !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, p.timeout_ns))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            if (C::DQ_T)
+              umma_ss_w(tDQ, k_mn + mnmajor_step(kk), ds_mn + dso + mnmajor_step(kk), idQ, kk > 0);
+            else
+              umma_ss_w(tDQ, ds_mn + dso + mnmajor_step(kk), k_mn + mnmajor_step(kk), idQ, kk > 0);
+          }
+        }
+        umma_commit_w(smem_u32(&bars.q_empty[st]));
+        if (p.with_dq) umma_commit_w(smem_u32(&bars.dq_full));
+      }
+      umma_commit_w(smem_u32(&bars.dkdv_full));
+      // every product this warp issued has completed before tensor memory is released
+      umma_commit_w(smem_u32(&bars.mma_drain));
+      mbar_wait_drain(smem_u32(&bars.mma_drain), 0, p.timeout_ns);
+  }
   } else if (warp < 8) {
-    reg_budget_inc<C::REG_COMPUTE>();
     // ------------------------------------------------------------------ P^T / dS^T compute
     // Two warpgroups; warpgroup g owns score columns [g*HALF, (g+1)*HALF) of every key row.
     const int g = warp >> 2;
@@ -486,6 +469,36 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_main_kernel(const __grid_cons
     const bool key_ok = key < sv.len_k;
     const float c2 = p.scale_log2;
     const int c_base = g * HALF;
+    // d_head 64: drains warpgroup g's 32 columns of the dQ partial of step itd (lanes are
+    // query rows, columns d). The warp stages its 32 x 32 fp32 block in rows [32 (warp & 3),
+    // +32) of warpgroup g's slab of the dS^T buffer of step itd (128-byte swizzle; the dK / dQ
+    // products of that step are complete, and only this warp writes these rows again, two
+    // steps later, after waiting for this reduce to read them) and adds it to the fp32
+    // accumulator with one TMA tensor reduce-add issued by its lane 0. Query rows past the
+    // sequence hold exact zeros (their dS was masked), so whole blocks can be added.
+    auto drain_dq = [&](int itd) -> bool {
+      if (!mbar_wait(smem_u32(&bars.dq_full), itd & 1, abort, p.timeout_ns)) return false;
+      tc_fence_after();
+      float v[32];
+      ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + g * 32, reinterpret_cast<uint32_t*>(v));
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.dq_empty));
+      uint8_t* stage = smem + C::OFF_DS + (itd & 1) * C::DS_BYTES + g * (C::DS_BYTES / 2) +
+                       (warp & 3) * 4096;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(stage + lane * 128 + 16 * (c ^ (lane & 7))) =
+            make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      // a block wholly in the zero padding past the head size adds nothing: skip it
+      if (lane == 0 && g * 32 < p.d_out) {
+        tma_reduce_add_2d(&p.tm_dq, smem_u32(stage), g * 32,
+                          (int)(zh * p.rows_q + sv.row0_q + q_tile(itd) * BM + (warp & 3) * 32));
+        bulk_commit_group();
+      }
+      return true;
+    };
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
       const int st = it % QST, bs = it & 1;
@@ -501,14 +514,13 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_main_kernel(const __grid_cons
       const int q_min = p.causal ? key : 0;  // top-left causal: query q sees key iff q >= key
       // The dS^T buffer of this step was last read by the dK / dQ products of step it - 2,
       // which completed before s_full(it) (the MMA warp commits s_full(it) after issuing
-      // them). At d_head 64 the drain warps then staged dQ(it - 2) in it: wait until their
-      // reduce-adds have read it.
-      if (C::STAGE_IN_DS && p.with_dq && it >= 2 &&
-          !mbar_wait(smem_u32(&bars.stg_free[bs]), ((it >> 1) - 1) & 1, abort, p.timeout_ns)) {
-        ok = false;
-        break;
-      }
+      // them).
       uint8_t* gDS = smem + C::OFF_DS + bs * C::DS_BYTES;
+      if (!C::DQ_WARPS && p.with_dq && it >= 2) {
+        // this warp's rows of the buffer staged dQ two steps ago: wait for that reduce
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+      }
       // All of this warpgroup's S^T and dP^T columns are fetched behind one wait.
       float sv_all[HALF], dpv_all[HALF];
       if constexpr (HALF == 64) {
@@ -627,7 +639,15 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_main_kernel(const __grid_cons
       mbar_arrive(smem_u32(&bars.p_full));
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.ds_full[bs]));
+      // d_head 64: dQ partial of the previous step (its MMA ran while this step's P/dS were
+      // formed)
+      if (!C::DQ_WARPS && p.with_dq && it > 0 && !drain_dq(it - 1)) {
+        ok = false;
+        break;
+      }
     }
+    if (!C::DQ_WARPS && p.with_dq && ok && n_steps > 0) ok = drain_dq(n_steps - 1);
+    if (!C::DQ_WARPS && lane == 0) bulk_wait_group0();  // this warp's reduces are complete
     // ---- epilogue: dK = sm_scale * acc, dV = acc; warpgroup g writes columns [g*D/2, +D/2)
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, p.timeout_ns);
     tc_fence_after();
@@ -658,18 +678,15 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_main_kernel(const __grid_cons
         }
       }
     }
-    reg_budget_dec<C::REG_LAUNCH>();
-  } else {
-    reg_budget_dec<C::REG_DRAIN>();
-    // ------------------------------------------------------------------ dQ drain
-    // Each drain warp owns the 32 TMEM lanes its warp index reaches (quarter qw) of the dQ
-    // partial: dQ^T at d_head 128 (lanes are d, the 64 columns the step's query rows), dQ at
-    // d_head 64 (lanes are query rows, the 64 columns d). It loads them right after the
-    // products complete and releases the TMEM columns, stages two 32 x 32 fp32 blocks in
-    // shared memory (128-byte swizzle) and adds each to the fp32 accumulator with one TMA
-    // reduce-add. Query rows past the sequence hold exact zeros (their dS was masked), so
-    // whole blocks can be added; blocks wholly in the zero padding past the head size add
-    // nothing and are skipped.
+  } else if (C::DQ_WARPS && warp >= C::WARP_DRAIN0) {
+    // ------------------------------------------------------------------ dQ drain (d_head 128)
+    // Each drain warp owns the 32 TMEM lanes its warp index reaches (quarter qw) of the dQ^T
+    // partial (lanes are d, the 64 columns the step's query rows). It loads them right after
+    // the products complete and releases the TMEM columns, stages two 32 x 32 fp32 blocks in
+    // its own shared-memory area (128-byte swizzle) and adds each to the fp32 accumulator
+    // with one TMA reduce-add. Query rows past the sequence hold exact zeros (their dS was
+    // masked), so whole blocks can be added; blocks wholly in the zero padding past the head
+    // size add nothing and are skipped.
     const int qw = warp & 3;
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
     bool ok = p.with_dq != 0;
@@ -680,16 +697,10 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_main_kernel(const __grid_cons
       }
       tc_fence_after();
       const int q_lo = q_tile(it) * BM;
-      uint8_t* stage;
-      if (C::STAGE_IN_DS) {
-        // the dS^T buffer of step it: its readers (dK(it), dQ(it)) completed before dq_full
-        stage = smem + C::OFF_DS + (it & 1) * C::DS_BYTES + qw * 8192;
-      } else {
-        stage = smem + C::OFF_STG + qw * 8192;
-        // this warp's previous reduce-adds must have read the area before it is rewritten
-        if (lane == 0) bulk_wait_group_read0();
-        __syncwarp();
-      }
+      uint8_t* stage = smem + C::OFF_STG + qw * 8192;
+      // this warp's previous reduce-adds must have read the area before it is rewritten
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
       // one 32-column block at a time (32 registers of data live)
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
@@ -700,40 +711,24 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_main_kernel(const __grid_cons
           mbar_arrive(smem_u32(&bars.dq_empty));
         }
         uint8_t* blk = stage + b * 4096;
-        if (C::DQ_T) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)  // row i = query row 32 b + i, column = this lane's d
-            *reinterpret_cast<float*>(blk + i * 128 + 16 * ((lane >> 2) ^ (i & 7)) +
-                                      4 * (lane & 3)) = v[i];
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c)  // row = this lane's query row, columns d = 32 b + ...
-            *reinterpret_cast<float4*>(blk + lane * 128 + 16 * (c ^ (lane & 7))) =
-                make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-        }
+        for (int i = 0; i < 32; ++i)  // row i = query row 32 b + i, column = this lane's d
+          *reinterpret_cast<float*>(blk + i * 128 + 16 * ((lane >> 2) ^ (i & 7)) +
+                                    4 * (lane & 3)) = v[i];
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
+      // blocks: column d = 32 qw, query rows 32 b within the step
+      if (lane == 0 && qw * 32 < p.d_out) {
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          // block origin: column d, query row within the sequence
-          const int c0 = C::DQ_T ? qw * 32 : b * 32;
-          const int r0 = q_lo + (C::DQ_T ? b * 32 : qw * 32);
-          if (c0 < p.d_out)
-            tma_reduce_add_2d(&p.tm_dq, smem_u32(stage + b * 4096), c0,
-                              (int)(zh * p.rows_q + sv.row0_q + r0));
-        }
+        for (int b = 0; b < 2; ++b)
+          tma_reduce_add_2d(&p.tm_dq, smem_u32(stage + b * 4096), qw * 32,
+                            (int)(zh * p.rows_q + sv.row0_q + q_lo + b * 32));
         bulk_commit_group();
-        if (C::STAGE_IN_DS) {  // the compute warps may write dS(it + 2) here once read
-          bulk_wait_group_read0();
-          mbar_arrive(smem_u32(&bars.stg_free[it & 1]));
-        }
       }
       __syncwarp();
     }
     if (lane == 0) bulk_wait_group0();  // this warp's reduce-adds complete before the CTA exits
-    reg_budget_inc<C::REG_LAUNCH>();
   }
 
   tc_fence_before();

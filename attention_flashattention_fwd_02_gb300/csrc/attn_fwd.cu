@@ -52,21 +52,25 @@
 
 namespace attn_sm103 {
 
-// BIAS (d_head 64 only): the additive bias tile of each score tile (128 query rows x 128
-// keys, 16-bit) is staged in shared memory, one slot per query tile: slot t holds tile t's
-// bias tiles in its key-tile order, each refilled once tile t's softmax warps have read the
-// previous one. A slot shared by both tiles would let a parity wait pass early where one
-// tile's key tiles run out and the other takes over its slot.
+// BIAS (d_head 64 and 128): the additive bias tile of each score tile (128 query rows x 128
+// keys, 16-bit) is staged in shared memory, in slots that belong to one query tile each:
+// tile t's bias tiles go to its own slots in its key-tile order, each slot refilled once tile
+// t's softmax warps have read its previous tile. At d_head 64 each of the two query tiles has
+// one slot (slot t, phase j for key tile j); at d_head 128 a CTA owns one query tile (Q, two
+// K/V stages and two bias slots fill shared memory) and that tile has two slots (slot j mod
+// 2, phase j / 2). Slots shared by both tiles would let a parity wait pass on the other
+// tile's load.
 template <int D, bool BIAS = false>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
-  static constexpr int NQ = (D == 256) ? 1 : 2;  // query tiles per CTA
+  static constexpr int NQ = (D == 256 || (D == 128 && BIAS)) ? 1 : 2;  // query tiles per CTA
   static constexpr int NST = (D == 256) ? 1 : (D == 128) ? 2 : 4;
   static constexpr bool SPLIT_KV = (D == 256);   // K and V released and loaded separately
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NBS = BIAS ? 2 : 0;  // one bias slot per query tile
-  static constexpr int B_BYTES = BM * BN * 2;  // one bias slot
+  static constexpr int NBS = BIAS ? 2 : 0;       // bias slots
+  static constexpr int BS_T = NBS / NQ;            // bias slots per query tile
+  static constexpr int B_BYTES = BM * BN * 2;      // one bias slot
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = NQ * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
@@ -282,33 +286,37 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     }
   } else if (BIAS && warp == C::WARP_BIAS) {
     // ------------------------------------------------------------------ bias producer
-    // bias tiles in score-tile order, tile t's into slot t (phase j for its key tile j),
-    // each slot refilled once tile t's softmax warps have read its previous tile (they wait on
-    // nothing this warp does afterwards). A warp of its own, so that its waits never share a
-    // warp with the K/V producer's.
+    // bias tiles in score-tile order: key tile j of query tile t into slot
+    // t * BS_T + j mod BS_T (phase j / BS_T), each slot refilled once tile t's softmax warps
+    // have read its previous tile (they wait on nothing this warp does afterwards). A warp of
+    // its own, so that its waits never share a warp with the K/V producer's. Every unit
+    // (batch, or sequence of a compact batch) finds its bias block at offset 0 of its own
+    // slice of the bias's first dimension, so the key coordinate (the innermost, which a TMA
+    // copy needs 16-byte aligned) is always a multiple of 64 elements.
     if (lane == 0) {
       tma_prefetch_map(&p.tm_b);
       const uint32_t sB = smem_u32(smem + C::OFF_B);
-      const int hb = p.bias_h_bcast ? 0 : h, bb = p.bias_b_bcast ? 0 : sv.batch;
-      int last_j[2] = {-1, -1};  // last key tile loaded into each slot
+      const int hb = p.bias_h_bcast ? 0 : h, bb = p.bias_b_bcast ? 0 : z;
+      int last_ph[2] = {-1, -1};  // last phase loaded into each slot
       for (int k = 0; k < order.total; ++k) {
         const int t = order.t_of(k), j = order.j_of(k);
-        if (j >= 1 &&
-            !mbar_wait(smem_u32(&bars.b_empty[t]), (j - 1) & 1, abort, p.timeout_ns))
+        const int slot = t * C::BS_T + j % C::BS_T, ph = j / C::BS_T;
+        if (ph >= 1 &&
+            !mbar_wait(smem_u32(&bars.b_empty[slot]), (ph - 1) & 1, abort, p.timeout_ns))
           break;
-        const uint32_t bf = smem_u32(&bars.b_full[t]);
+        const uint32_t bf = smem_u32(&bars.b_full[slot]);
         mbar_arrive_expect_tx(bf, C::B_BYTES);
 #pragma unroll
         for (int s = 0; s < 2; ++s)
-          tma_load_4d(sB + t * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
-                      sv.row0_q + q_lo[t], hb, bb);
-        last_j[t] = j;
+          tma_load_4d(sB + slot * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
+                      q_lo[t], hb, bb);
+        last_ph[slot] = ph;
       }
       if (*abort)  // let the copies in flight land before exiting
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (last_j[t] >= 0)
-            mbar_wait_drain(smem_u32(&bars.b_full[t]), last_j[t] & 1, p.timeout_ns);
+        for (int sl = 0; sl < 2; ++sl)
+          if (last_ph[sl] >= 0)
+            mbar_wait_drain(smem_u32(&bars.b_full[sl]), last_ph[sl] & 1, p.timeout_ns);
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
@@ -426,8 +434,8 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
                         reinterpret_cast<uint32_t*>(s + 96));
       if constexpr (BIAS) {
         // s <- s c2 + bias log2(e): the scores in base-2 units, bias included
-        const int slot = t;  // slot t, phase j
-        if (!mbar_wait(smem_u32(&bars.b_full[slot]), j & 1, abort, p.timeout_ns)) {
+        const int slot = t * C::BS_T + j % C::BS_T;  // phase j / BS_T
+        if (!mbar_wait(smem_u32(&bars.b_full[slot]), (j / C::BS_T) & 1, abort, p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -615,7 +623,10 @@ static cudaError_t launch_fwd_dispatch(const FwdParams& p, int D, bool f16, dim3
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3 grid,
                             cudaStream_t stream) {
-  if (bias) {  // the bias kernels exist for the 64-wide configuration only
+  if (bias) {  // the bias kernels exist for the 64- and 128-wide configurations
+    if (D == 128)
+      return f16 ? launch_fwd_impl<128, true, true>(p, grid, stream)
+                 : launch_fwd_impl<128, false, true>(p, grid, stream);
     if (D != 64) return cudaErrorInvalidValue;
     return f16 ? launch_fwd_impl<64, true, true>(p, grid, stream)
                : launch_fwd_impl<64, false, true>(p, grid, stream);
@@ -623,9 +634,11 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3
   return launch_fwd_dispatch<false>(p, D, f16, grid, stream);
 }
 
-// Query rows per CTA: two 128-row tiles, one at kernel width 256. The 4-D Q tensor map uses
-// a 128-row box.
-int fwd_block_m(int width) { return width == 256 ? 128 : 256; }
+// Query rows per CTA: two 128-row tiles; one at kernel width 256, and at width 128 with a
+// bias. The 4-D Q tensor map uses a 128-row box.
+int fwd_block_m(int width, bool bias) {
+  return (width == 256 || (width == 128 && bias)) ? 128 : 256;
+}
 int fwd_box_rows() { return 128; }
 
 }  // namespace attn_sm103

@@ -7,10 +7,10 @@
 
 namespace attn_sm103 {
 
-// Forward: grid = (query blocks, H, B or num_seqs); a block covers fwd_block_m(width) query
-// rows (width = kernel width 64, 128 or 256), loaded with a Q tensor map whose box has
+// Forward: grid = (query blocks, H, B or num_seqs); a block covers fwd_block_m(width, bias)
+// query rows (width = kernel width 64, 128 or 256), loaded with a Q tensor map whose box has
 // fwd_box_rows() rows.
-int fwd_block_m(int width);
+int fwd_block_m(int width, bool bias);
 int fwd_box_rows();
 cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3 grid,
                             cudaStream_t stream);

@@ -324,21 +324,6 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// --------------------------------------------------------------------------- registers
-// Per-warpgroup register budgets: every warp of a warpgroup executes the same instruction.
-// A decrease returns registers to the CTA's pool; an increase waits until the pool has them,
-// so the budgets a kernel asks for must add up to at most what it was launched with.
-template <uint32_t N>
-__device__ __forceinline__ void reg_budget_inc() {
-  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg operand");
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void reg_budget_dec() {
-  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg operand");
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // --------------------------------------------------------------------------- numerics
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -38,7 +38,11 @@ Additive bias (the bias argument the AOTriton varlen page reserves): an optional
 broadcastable over batch and head, of shape [Sq, Sk] per head, enters as
     S = c * Q K^T + b
 before the mask and the softmax (so LSE is that of the biased logits); its gradient is
-dS itself, summed over the dimensions it was broadcast along.
+dS itself, summed over the dimensions it was broadcast along. The pages leave the bias's
+varlen layout open (they only reserve the argument); read the plainest way that matches
+the padded convention: every unit (a padded batch entry, or a sequence of a compact batch)
+finds its [len_q, len_k] bias block at offset 0 of its own slice of the bias's first
+dimension, which therefore has size 1 (broadcast) or the number of units.
 
 Readings where the pages are silent (each is listed in the design notes):
   * an empty key set (Sk_valid == 0) gives O = 0, LSE = -inf and zero gradients;
@@ -182,8 +186,8 @@ def _as64(x):
 
 
 def _bias_slice(bias, b, h, nq, nk):
-    """The [nq, nk] bias block of batch b, head h (bias [Bb, Hb, Sq, Sk], Bb in {1, B},
-    Hb in {1, H}: size-1 dimensions broadcast)."""
+    """The [nq, nk] bias block of unit b (a batch entry, or a compact sequence), head h (bias
+    [Bb, Hb, Sq, Sk], Bb in {1, units}, Hb in {1, H}: size-1 dimensions broadcast)."""
     if bias is None:
         return None
     return bias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0, :nq, :nk]
@@ -243,10 +247,13 @@ def bwd_bhsd(q, k, v, do, c, causal, cu_seqlens_q=None, cu_seqlens_k=None, bias=
     return dq, dk, dv
 
 
-def fwd_compact_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, c, causal):
+def fwd_compact_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, c, causal, bias=None):
     """Compact varlen forward: q [1, H, Tq, D], k/v [1, H, Tk, D]; sequence s owns rows
-    [cu[s], cu[s+1]) of the token axis. Rows outside every sequence are NaN."""
+    [cu[s], cu[s+1]) of the token axis. bias: optional [Bb, Hb, Sq_b, Sk_b], Bb in
+    {1, num_seqs}, Hb in {1, H}; sequence s's bias block is [:len_q, :len_k] of slice s (or
+    of slice 0 when Bb is 1). Rows outside every sequence are NaN."""
     q, k, v = _as64(q), _as64(k), _as64(v)
+    bias = None if bias is None else _as64(bias)
     assert q.shape[0] == 1, "compact varlen takes batch exactly 1"
     cq = np.asarray(cu_seqlens_q, np.int64)
     ck = np.asarray(cu_seqlens_k, np.int64)
@@ -256,15 +263,20 @@ def fwd_compact_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, c, causal):
     for s in range(len(cq) - 1):
         qa, qb, ka, kb = cq[s], cq[s + 1], ck[s], ck[s + 1]
         for h in range(H):
-            O, L = attention_forward(q[0, h, qa:qb], k[0, h, ka:kb], v[0, h, ka:kb], c, causal)
+            O, L = attention_forward(q[0, h, qa:qb], k[0, h, ka:kb], v[0, h, ka:kb], c, causal,
+                                     bias=_bias_slice(bias, s, h, qb - qa, kb - ka))
             o[0, h, qa:qb] = O
             lse[0, h, qa:qb] = L
     return o, lse
 
 
-def bwd_compact_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, c, causal):
-    """Compact varlen backward: (dq, dk, dv) per sequence slice, NaN outside sequences."""
+def bwd_compact_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, c, causal, bias=None):
+    """Compact varlen backward: (dq, dk, dv) per sequence slice, NaN outside sequences. With
+    a bias (layout as in fwd_compact_varlen), (dq, dk, dv, dbias): dbias has the bias's shape,
+    sums dS over the broadcast dimensions and is 0 outside every sequence's block."""
     q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    bias = None if bias is None else _as64(bias)
+    dbias = None if bias is None else np.zeros(bias.shape)
     assert q.shape[0] == 1, "compact varlen takes batch exactly 1"
     cq = np.asarray(cu_seqlens_q, np.int64)
     ck = np.asarray(cu_seqlens_k, np.int64)
@@ -276,6 +288,12 @@ def bwd_compact_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, c, causal):
         qa, qb, ka, kb = cq[s], cq[s + 1], ck[s], ck[s + 1]
         for h in range(H):
             g = attention_backward(q[0, h, qa:qb], k[0, h, ka:kb], v[0, h, ka:kb],
-                                   do[0, h, qa:qb], c, causal)
-            dq[0, h, qa:qb], dk[0, h, ka:kb], dv[0, h, ka:kb] = g
+                                   do[0, h, qa:qb], c, causal,
+                                   bias=_bias_slice(bias, s, h, qb - qa, kb - ka))
+            dq[0, h, qa:qb], dk[0, h, ka:kb], dv[0, h, ka:kb] = g[:3]
+            if bias is not None:
+                dbias[s if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0,
+                      :qb - qa, :kb - ka] += g[3]
+    if bias is not None:
+        return dq, dk, dv, dbias
     return dq, dk, dv

@@ -16,7 +16,9 @@ Agents are generators that yield actions:
                                   or reduce from shared memory); the agent does not wait
   ('wait_read', buf, who)         block until `who`'s read of the buffer's current contents
                                   has finished (cp.async.bulk.wait_group.read)
-With a timeout, a wait that has not succeeded after `timeout` ticks fails and raises the
+With parity_waits, a wait passes on the parity of the completed phase count alone, as the
+hardware's does (so an inexact wait can pass a phase early). With a timeout, a wait that has
+not succeeded after `timeout` ticks fails and raises the
 CTA's abort flag; once it is raised every wait fails at once (the agent receives False from
 its yield) and drains still wait. With exit_check, nothing may be in flight when the last
 agent has finished: no product in the tensor pipe, no copy still landing (the CTA would
@@ -30,8 +32,13 @@ the contents).
 
 
 class Sim:
-    def __init__(self, rng, mma_ticks=(1, 6), timeout=None, exit_check=False):
+    def __init__(self, rng, mma_ticks=(1, 6), timeout=None, exit_check=False,
+                 parity_waits=False):
         self.rng = rng
+        # parity_waits: a wait for phase k passes as the hardware's parity wait does, once the
+        # number of completed phases has the parity of k + 1 (possibly a phase early or late),
+        # to show what an inexact wait leads to
+        self.parity_waits = parity_waits
         self.timeout, self.exit_check, self.abort = timeout, exit_check, False
         self.write_until = 0  # the last copy's landing tick
         self.mma_ticks = mma_ticks  # range of a product's duration
@@ -119,7 +126,9 @@ class Sim:
                         elif p[0] in ("wait", "drain"):
                             c = self.count[p[1]]
                             a["send"] = True
-                            if c < p[2] + 1:
+                            passed = (c % 2 == (p[2] + 1) % 2) if self.parity_waits \
+                                else c >= p[2] + 1
+                            if not passed:
                                 timed_out = (self.timeout is not None
                                              and self.tick - a["since"] >= self.timeout)
                                 if p[0] == "wait" and (self.abort or timed_out):
@@ -129,7 +138,7 @@ class Sim:
                                     a["send"] = False
                                 else:
                                     break
-                            elif c != p[2] + 1:
+                            elif c != p[2] + 1 and not self.parity_waits:
                                 self.violations.append(("missed phase", p[1], p[2], c))
                         a["pending"] = None
                     try:

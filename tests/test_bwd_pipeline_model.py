@@ -9,21 +9,19 @@ tensor pipe (a commit arrives when every product issued before it has completed)
   producer     Q / dO / LSE / Delta of step it into stage it mod QST after q_empty
   MMA warp     S/dP(it+1) after s_free(it); dV(it) after p_full(it), commit p_empty;
                dK(it) after ds_full; dQ(it) after dq_empty(it-1); commit q_empty, dq_full
-  warpgroups   (two, arriving independently) wait s_full, q_full, and at d_head 64
-               stg_free(it-2); read S^T/dP^T, arrive s_free; wait p_empty(it-1); write P^T,
-               arrive p_full; write dS^T, arrive ds_full
-  drain warps  (modelled as two agents, arriving independently) wait dq_full(it); read the
-               dQ partial, arrive dq_empty; stage it and start the reduce-add: at d_head 64
-               in the dS^T buffer of step it, then wait for the reduce to read it and arrive
-               stg_free; at d_head 128 in an area of their own, after waiting for their
-               previous reduce to read it
+  warpgroups   (two, arriving independently) wait s_full, q_full; read S^T/dP^T, arrive
+               s_free; wait p_empty(it-1); write P^T, arrive p_full; write dS^T, arrive
+               ds_full; at d_head 64 then drain dQ(it-1): wait dq_full, read it, arrive
+               dq_empty, stage it in their half of the dS^T buffer of step it-1 and start the
+               reduce-add, which must have read it before they write dS^T there again
+  drain warps  (d_head 128; modelled as two agents, arriving independently) wait
+               dq_full(it); read the dQ partial, arrive dq_empty; wait for their previous
+               reduce-add to read their staging area, stage and start the next
 Buffers (the Q/dO stages, TMEM S^T/dP^T, P^T and dQ, the two dS^T buffers, the staging
 areas) carry the step whose contents they hold: a read must find its step's contents
 completely written, and a write must come after every read of the contents it replaces has
-completed. Each dS^T buffer is modelled as two parts, part h written by warpgroup h and used
-as staging by drain agent h: every wait between the two sides counts all warps of the other
-side, so the physical split of the buffer (by query columns for the warpgroups, by 8 KB
-slices for the drain warps) orders the same way.
+completed. The dS^T buffers have no release barrier of their own: a warpgroup writes dS(it)
+only after s_full(it), which the MMA warp commits after issuing dK(it-2) and dQ(it-2).
 """
 import random
 
@@ -35,20 +33,20 @@ from _pipeline_sim import Sim
 def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
                       stage_in_ds=True):
     """The kernel's roles; `skip` names waits to leave out (to check that the model sees
-    what they prevent; "read_wait" is the d_head 128 drain agent's wait for its previous
-    reduce-add to read its staging area); withhold: a step whose Q / dO the producer skips
-    (the kernel's failure-detection hook); stage_in_ds: the d_head 64 layout, where the
-    drain agents stage in the dS buffer of the step they drain."""
-    drains = ("dr0", "dr1")
+    what they prevent; "read_wait" is the wait of a draining warp for its previous
+    reduce-add to read its staging); withhold: a step whose Q / dO the producer skips (the
+    kernel's failure-detection hook); stage_in_ds: the d_head 64 layout (the compute
+    warpgroups drain dQ into the dS buffer they released), else the d_head 128 one (drain
+    warps with staging areas of their own)."""
+    drains = ("wg0", "wg1") if stage_in_ds else ("dr0", "dr1")
     sim.barrier("kv_full", 1)
     for st in range(qst):
         sim.barrier(f"q_full{st}", 1)
         sim.barrier(f"q_empty{st}", 1)
     for b in range(2):
         sim.barrier(f"ds_full{b}", 2)
-        sim.barrier(f"stg_free{b}", len(drains))
     for name, n in (("s_full", 1), ("s_free", 2), ("p_full", 2), ("p_empty", 1),
-                    ("dq_full", 1), ("dq_empty", len(drains)), ("dkdv_full", 1)):
+                    ("dq_full", 1), ("dq_empty", 2), ("dkdv_full", 1)):
         sim.barrier(name, n)
     wg = ("wg0", "wg1")
     sim.buffer("KV", ())  # the key tile's K and V, loaded once
@@ -57,7 +55,7 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
     sim.buffer("SDP", wg)
     sim.buffer("P", ("dV",))
     for b in range(2):
-        for h in range(2):
+        for h in range(2):  # the halves the two warpgroups write
             sim.buffer(f"DS{b}{h}", lambda c, h=h: ({"dK", "dQ"} if with_dq else {"dK"})
                        if c[0] == "dS" else {f"tma{h}"})
     for h in range(2):
@@ -132,6 +130,24 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
         yield ("commit", "mma_drain")
         yield ("drain", "mma_drain", 0)
 
+    def drain_step(me, h, itd):
+        """One step's dQ drain by `me` (a warpgroup at d_head 64, a drain agent at 128)."""
+        if not (yield from wait("dq_full", itd)):
+            return False
+        if not stage_in_ds:
+            yield ("delay", rng.randint(0, 24))  # the warp may be held up
+        yield ("read", "DQ", itd, me, rng.randint(1, 4))
+        yield ("arrive", "dq_empty")
+        if stage_in_ds:  # stage in this warpgroup's half of dS(itd), reduce-add from it
+            buf = f"DS{itd & 1}{h}"
+        else:  # an area of its own: its previous reduce-add must have read it
+            buf = f"STG{h}"
+            if "read_wait" not in skip:
+                yield ("wait_read", buf, f"tma{h}")
+        yield ("write", buf, ("stg", itd))
+        yield ("read_async", buf, ("stg", itd), f"tma{h}", rng.randint(1, 12))
+        return True
+
     def warpgroup(me):
         h = int(me[-1])
         for it in range(n_steps):
@@ -139,11 +155,8 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
             if not (yield from wait("s_full", it)) or \
                     not (yield from wait(f"q_full{st}", it // qst)):
                 return
-            # the dK / dQ products of step it-2 completed before s_full(it); at d_head 64 the
-            # drain agents staged dQ(it-2) in this buffer afterwards
-            if stage_in_ds and with_dq and it >= 2 and \
-                    not (yield from wait(f"stg_free{bs}", (it >> 1) - 1)):
-                return
+            if stage_in_ds and with_dq and it >= 2 and "read_wait" not in skip:
+                yield ("wait_read", f"DS{bs}{h}", f"tma{h}")  # the reduce has read this half
             yield ("read", "SDP", it, me, rng.randint(1, 4))
             yield ("read", f"QS{st}", it, me, 0)
             yield ("delay", rng.randint(0, 3))
@@ -159,34 +172,30 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
             yield ("delay", rng.randint(0, 8))
             yield ("write", f"DS{bs}{h}", ("dS", it))
             yield ("arrive", f"ds_full{bs}")
+            if stage_in_ds and with_dq and it > 0 and not (yield from drain_step(me, h, it - 1)):
+                return
+        if stage_in_ds and with_dq and n_steps > 0 and \
+                not (yield from drain_step(me, h, n_steps - 1)):
+            return
         yield from wait("dkdv_full", 0)
+
+    def warpgroup_role(me):
+        yield from warpgroup(me)
+        if stage_in_ds and with_dq:  # on every exit path: all of this warp's reduces done
+            for b in range(2):
+                yield ("wait_read", f"DS{b}{me[-1]}", f"tma{me[-1]}")
 
     def drain(me):
         h = int(me[-1])
         for it in range(n_steps if with_dq else 0):
-            if not (yield from wait("dq_full", it)):
+            if not (yield from drain_step(me, h, it)):
                 break
-            yield ("delay", rng.randint(0, 24))  # the warp may be held up (e.g. by staging)
-            yield ("read", "DQ", it, me, rng.randint(1, 4))
-            yield ("arrive", "dq_empty")
-            if stage_in_ds:
-                buf = f"DS{it & 1}{h}"
-                yield ("write", buf, ("stg", it))
-                yield ("read_async", buf, ("stg", it), f"tma{h}", rng.randint(1, 12))
-                if "stg_read" not in skip:
-                    yield ("wait_read", buf, f"tma{h}")
-                yield ("arrive", f"stg_free{it & 1}")
-            else:
-                if "read_wait" not in skip:
-                    yield ("wait_read", f"STG{h}", f"tma{h}")
-                yield ("write", f"STG{h}", ("stg", it))
-                yield ("read_async", f"STG{h}", ("stg", it), f"tma{h}", rng.randint(1, 12))
-        # on every exit path: all of this warp's reduce-adds complete
-        for buf in ([f"DS{b}{h}" for b in range(2)] if stage_in_ds else [f"STG{h}"]):
-            yield ("wait_read", buf, f"tma{h}")
+        yield ("wait_read", f"STG{h}", f"tma{h}")  # its reduce-adds complete before exit
 
-    return [producer(), mma(), warpgroup("wg0"), warpgroup("wg1"), drain("dr0"),
-            drain("dr1")]
+    agents = [producer(), mma(), warpgroup_role("wg0"), warpgroup_role("wg1")]
+    if not stage_in_ds:
+        agents += [drain("dr0"), drain("dr1")]
+    return agents
 
 
 @pytest.mark.parametrize("n_steps", [1, 2, 3, 4, 7])
@@ -205,44 +214,47 @@ def test_backward_pipeline_is_exact_and_race_free(n_steps, qst, with_dq, stage_i
     ("s_full", "stale read"), ("s_free", "overwrite"), ("p_full", "stale read"),
     ("p_empty", "overwrite"), ("ds_full", "stale read"), ("q_full", "stale read"),
     ("q_empty", "overwrite"), ("dq_full", "stale read"), ("dq_empty", "overwrite")])
-def test_model_catches_a_missing_wait(dropped, kind):
+@pytest.mark.parametrize("stage_in_ds", [True, False])
+def test_model_catches_a_missing_wait(dropped, kind, stage_in_ds):
     """Each of these waits protects something: without it the model must report a violation
     of the kind that wait prevents."""
     rng = random.Random(5)
     found = []
     for _ in range(300):
         sim = Sim(rng)
-        found += sim.run(backward_protocol(sim, 6, 3, True, rng, skip=(dropped,)))
+        found += sim.run(backward_protocol(sim, 6, 3, True, rng, skip=(dropped,),
+                                           stage_in_ds=stage_in_ds))
     assert any(v[0] == kind for v in found), found[:3]
 
 
 @pytest.mark.parametrize("qst", [2, 3])
 @pytest.mark.parametrize("withhold", [0, 1, 3])
 @pytest.mark.parametrize("with_dq", [True, False])
-def test_withheld_step_every_role_leaves_and_nothing_is_in_flight(qst, withhold, with_dq):
+@pytest.mark.parametrize("stage_in_ds", [True, False])
+def test_withheld_step_every_role_leaves_and_nothing_is_in_flight(qst, withhold, with_dq,
+                                                                  stage_in_ds):
     """The failure-detection path: the producer skips one step, a wait gives up and raises
     the abort flag; every role leaves, the producer drains its copies and the MMA warp its
     products, and nothing is in flight when the last role is done."""
     rng = random.Random(qst * 10 + withhold + 100 * with_dq)
     for _ in range(100):
         sim = Sim(rng, timeout=200, exit_check=True)
-        v = sim.run(backward_protocol(sim, 6, qst, with_dq, rng, withhold=withhold))
+        v = sim.run(backward_protocol(sim, 6, qst, with_dq, rng, withhold=withhold,
+                                      stage_in_ds=stage_in_ds))
         assert sim.abort
         assert v == [], v[:3]
 
 
-@pytest.mark.parametrize("stage_in_ds,dropped", [(True, "stg_free"), (True, "stg_read"),
-                                                  (False, "read_wait")])
-def test_staging_needs_its_waits(stage_in_ds, dropped):
-    """d_head 64 stages each dQ block in the dS buffer of the step being drained: without the
-    compute warps' wait for stg_free, or without the drain agent's wait for its reduce-add to
-    read the block before it arrives there, the next dS write can overwrite the block while it
-    is read. d_head 128 stages in an area of its own: without waiting for the previous
-    reduce-add to read it, the next block overwrites it."""
+@pytest.mark.parametrize("stage_in_ds", [True, False])
+def test_staging_needs_the_reduce_read_wait(stage_in_ds):
+    """d_head 64 stages each dQ block in the warpgroup's half of the dS buffer it has just
+    released; without waiting for the reduce-add to finish reading it, the next dS write
+    into that half can overwrite the block while it is read. d_head 128 stages in an area of
+    each drain warp's own: without the same wait, the next block overwrites it."""
     rng = random.Random(21)
     found = []
     for _ in range(300):
         sim = Sim(rng, mma_ticks=(1, 3))
-        found += sim.run(backward_protocol(sim, 6, 3, True, rng, skip=(dropped,),
+        found += sim.run(backward_protocol(sim, 6, 3, True, rng, skip=("read_wait",),
                                            stage_in_ds=stage_in_ds))
     assert any(v[0] == "overwrite" for v in found)

@@ -150,6 +150,8 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
             t, j = od.t_of(k), od.j_of(k)
             if bias_slots == "tile":
                 slot, phase = t, j
+            elif bias_slots == "one":  # the first 128-wide scheme: one slot for both tiles
+                slot, phase = 0, k
             else:  # the earlier scheme: slot k mod 2, shared by the tiles
                 slot, phase = k % 2, k // 2
             if phase >= 1 and not (yield from wait(f"b_empty{slot}", phase - 1)):
@@ -233,7 +235,7 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
                 return
             yield ("read", f"SP{b}", ("S", k), me, rng.randint(0, 3))
             if bias:
-                slot, phase = (t, j) if bias_slots == "tile" else (k % 2, k // 2)
+                slot, phase = {"tile": (t, j), "one": (0, k)}.get(bias_slots, (k % 2, k // 2))
                 if not (yield from wait(f"b_full{slot}", phase)):
                     return
                 yield ("read", f"BS{slot}", (t, j), me, 0)
@@ -315,6 +317,37 @@ def test_single_epilogue_wait_is_caught():
 
 def test_shared_bias_slots_are_caught():
     assert _found(64, 5, 6, bias=True, bias_slots="shared")
+
+
+def _parity_runs(D, tiles, scheme, seed):
+    """Runs with the hardware's parity waits (an inexact wait may pass a phase early) and the
+    exit check: which violations does a bias slot scheme lead to?"""
+    rng = random.Random(seed)
+    kinds = set()
+    for n0, n1 in tiles:
+        for slow in (False, True):
+            for _ in range(150):
+                sim = Sim(rng, mma_ticks=SLOW["mma_ticks"] if slow else (1, 6),
+                          exit_check=True, parity_waits=True, timeout=5000)
+                kw = dict(copy_ticks=SLOW["copy_ticks"]) if slow else {}
+                kinds |= {v[0] for v in sim.run(forward_protocol(
+                    sim, D, n0, n1, rng, bias=True, bias_slots=scheme, **kw))}
+    return kinds
+
+
+def test_one_bias_slot_for_both_tiles_leaves_a_copy_in_flight():
+    """The first 128-wide bias kernel staged every score tile's bias in one slot shared by
+    both query tiles (slot 0, phase k of score tile k). A tile's parity wait could then pass
+    on the previous tile's load: it read the slot while the next copy was writing it, and its
+    release counted toward the wrong phase, so the loads and the reads drifted apart until a
+    bias copy could still be landing when every role had finished and the CTA exited. That
+    128-wide kernel ended with an unspecified launch failure (Xid 43) at B8 H16 S4096; a TMA
+    write into the shared memory of an exited CTA is a fault. One slot per query tile (the
+    kernel's scheme) shows none of these, with the same parity waits."""
+    tiles = [(5, 5), (5, 6), (6, 6), (32, 32)]
+    old = _parity_runs(128, tiles, "one", 7)
+    assert {"stale read", "overwrite", "copy in flight at exit"} <= old, old
+    assert _parity_runs(128, tiles, "tile", 8) == set()
 
 
 @pytest.mark.parametrize("D,dropped", [

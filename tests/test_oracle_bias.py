@@ -119,3 +119,43 @@ def test_batched_broadcast_bias():
     O, L = ref.attention_forward(q[1, 2, :4], k[1, 2, :4], v[1, 2, :4], 0.5, True,
                                  bias=bias[1, 0, :4, :4])
     np.testing.assert_allclose(o1[1, 2, :4], O, atol=1e-13)
+
+
+@pytest.mark.parametrize("Bb,Hb", [(3, 2), (1, 2), (3, 1), (1, 1)])
+def test_compact_bias_per_sequence_slice(Bb, Hb):
+    """Compact varlen with a bias: sequence s (query rows [cu_q[s], cu_q[s+1]), key rows
+    [cu_k[s], cu_k[s+1])) takes the block [:len_q, :len_k] of bias slice s (slice 0 when
+    broadcast). Forward and gradients (the bias gradient summed over broadcast sequences and
+    heads) equal PyTorch's float64 SDPA with that block as a float attn_mask, per sequence
+    and head."""
+    r = rng(7 + Bb + 10 * Hb)
+    lq, lk = [5, 1, 7], [4, 6, 7]
+    H, D, c = 2, 3, 0.6
+    cq = np.concatenate([[0], np.cumsum(lq)])
+    ck = np.concatenate([[0], np.cumsum(lk)])
+    q, do = (r.standard_normal((1, H, cq[-1], D)) for _ in range(2))
+    k, v = (r.standard_normal((1, H, ck[-1], D)) for _ in range(2))
+    bias = r.standard_normal((Bb, Hb, 8, 9))  # larger than every block
+    o, lse = ref.fwd_compact_varlen(q, k, v, cq, ck, c, True, bias=bias)
+    dq, dk, dv, db = ref.bwd_compact_varlen(q, k, v, do, cq, ck, c, True, bias=bias)
+    db_t = np.zeros_like(bias)
+    for s in range(3):
+        qa, qb, ka, kb = cq[s], cq[s + 1], ck[s], ck[s + 1]
+        for h in range(H):
+            blk = torch.tensor(bias[s if Bb > 1 else 0, h if Hb > 1 else 0, :qb - qa, :kb - ka],
+                               requires_grad=True)
+            causal = torch.ones(qb - qa, kb - ka, dtype=torch.bool).tril()
+            mask = blk.masked_fill(~causal, float("-inf"))
+            tq, tk, tv = (torch.tensor(x[0, h, a:b], requires_grad=True)
+                          for x, a, b in ((q, qa, qb), (k, ka, kb), (v, ka, kb)))
+            to = torch.nn.functional.scaled_dot_product_attention(
+                tq[None], tk[None], tv[None], attn_mask=mask[None], scale=c)[0]
+            to.backward(torch.tensor(do[0, h, qa:qb]))
+            np.testing.assert_allclose(o[0, h, qa:qb], to.detach().numpy(), atol=1e-12)
+            np.testing.assert_allclose(dq[0, h, qa:qb], tq.grad.numpy(), atol=1e-11)
+            np.testing.assert_allclose(dk[0, h, ka:kb], tk.grad.numpy(), atol=1e-11)
+            np.testing.assert_allclose(dv[0, h, ka:kb], tv.grad.numpy(), atol=1e-11)
+            db_t[s if Bb > 1 else 0, h if Hb > 1 else 0, :qb - qa, :kb - ka] += \
+                blk.grad.numpy()
+    np.testing.assert_allclose(db, db_t, atol=1e-11)
+    assert np.all(db[..., 7:, :] == 0) and np.all(db[..., :, 7:] == 0)
