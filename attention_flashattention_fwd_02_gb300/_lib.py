@@ -24,7 +24,8 @@ __all__ = [
     "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
     "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
     "attn_bwd_deterministic_workspace_size", "attn_fwd_bias", "attn_bwd_bias",
-    "EXPORTED_SYMBOLS",
+    "attn_fwd_compact_varlen_bias", "attn_bwd_compact_varlen_bias",
+    "attn_bwd_bias_workspace_size", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -34,6 +35,8 @@ EXPORTED_SYMBOLS = (
     "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
     "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
     "attn_bwd_deterministic_workspace_size", "attn_fwd_bias", "attn_bwd_bias",
+    "attn_fwd_compact_varlen_bias", "attn_bwd_compact_varlen_bias",
+    "attn_bwd_bias_workspace_size",
 )
 
 
@@ -74,6 +77,11 @@ _SIGS = {
     "attn_fwd": (INT, [P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
     "attn_fwd_padded_varlen": (INT, [P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
     "attn_fwd_bias": (INT, [P4, P4, P4, P4, I32P, I32P, F32, INT, P4, P3, VP, SZ, VP]),
+    "attn_fwd_compact_varlen_bias": (INT, [P4, P4, P4, P4, I32P, I32P, I32, I32, I32, F32, INT,
+                                           P4, P3, VP, SZ, VP]),
+    "attn_bwd_compact_varlen_bias": (INT, [P4, P4, P4, P4, P3, P4, P4, I32P, I32P, I32, I32, I32,
+                                           F32, INT, P4, P4, P4, P4, VP, SZ, VP]),
+    "attn_bwd_bias_workspace_size": (SZ, [ctypes.c_int64] * 8),
     "attn_bwd_bias": (INT, [P4, P4, P4, P4, P3, P4, P4, I32P, I32P, F32, INT, P4, P4, P4, P4,
                             VP, SZ, VP]),
     "attn_fwd_compact_varlen": (INT, [P4, P4, P4, I32P, I32P, I32, I32, I32, F32, INT, P4, P3,
@@ -267,7 +275,10 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, workspace,
 
 def attn_bwd_bias(q, k, v, o, lse, dout, bias, dq, dk, dv, sm_scale, causal, workspace,
                   dbias=None, cu_seqlens_q=None, cu_seqlens_k=None, stream=None):
-    """attn_bwd for a forward that took an additive bias; dbias (zeroed, full shape) gets dS."""
+    """attn_bwd for a forward that took an additive bias; dbias (the bias's shape) gets the
+    bias gradient: dS on the visited tiles of a zeroed full-shape dbias, or the sums over the
+    shared dimensions of a bias with a size-1 batch or head dimension (workspace of
+    attn_bwd_bias_workspace_size bytes)."""
     _check16(q, k, v, o, dout, dq, dk, dv, bias)
     if dbias is not None:
         _check16(dbias)
@@ -278,6 +289,41 @@ def attn_bwd_bias(q, k, v, o, lse, dout, bias, dq, dk, dv, sm_scale, causal, wor
         *_keep(tq, tk, tv, to, tl, tdo, tb), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
         float(sm_scale), int(bool(causal)), *_keep(tdq, tdk, tdv, tdb), ws, nws,
         _stream(stream)), "attn_bwd_bias")
+
+
+def attn_fwd_compact_varlen_bias(q, k, v, bias, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs,
+                                 max_seqlen_q, max_seqlen_k, sm_scale, causal, workspace=None,
+                                 stream=None):
+    """attn_fwd_compact_varlen with an additive bias (Bb, Hb, >= max_seqlen_q,
+    >= max_seqlen_k): sequence s's block at offset 0 of bias slice s."""
+    _check16(q, k, v, o, bias)
+    tq, tk, tv, tb, to, tl = _t4(q), _t4(k), _t4(v), _t4(bias), _t4(o), _t3(lse)
+    ws, nws = _ws(workspace)
+    _check(load().attn_fwd_compact_varlen_bias(
+        *_keep(tq, tk, tv, tb), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(num_seqs),
+        int(max_seqlen_q), int(max_seqlen_k), float(sm_scale), int(bool(causal)),
+        *_keep(to, tl), ws, nws, _stream(stream)), "attn_fwd_compact_varlen_bias")
+
+
+def attn_bwd_compact_varlen_bias(q, k, v, o, lse, dout, bias, dq, dk, dv, cu_seqlens_q,
+                                 cu_seqlens_k, num_seqs, max_seqlen_q, max_seqlen_k, sm_scale,
+                                 causal, workspace, dbias=None, stream=None):
+    """attn_bwd_compact_varlen for a forward that took a bias; dbias as for attn_bwd_bias."""
+    _check16(q, k, v, o, dout, dq, dk, dv, bias)
+    if dbias is not None:
+        _check16(dbias)
+    tq, tk, tv, to, tl, tdo = _t4(q), _t4(k), _t4(v), _t4(o), _t3(lse), _t4(dout)
+    tb, tdq, tdk, tdv, tdb = _t4(bias), _t4(dq), _t4(dk), _t4(dv), _t4(dbias)
+    ws, nws = _ws(workspace)
+    _check(load().attn_bwd_compact_varlen_bias(
+        *_keep(tq, tk, tv, to, tl, tdo, tb), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        int(num_seqs), int(max_seqlen_q), int(max_seqlen_k), float(sm_scale),
+        int(bool(causal)), *_keep(tdq, tdk, tdv, tdb), ws, nws, _stream(stream)),
+        "attn_bwd_compact_varlen_bias")
+
+
+def attn_bwd_bias_workspace_size(B, H, Sq, D, Bb, Hb, Sq_b, Sk_b) -> int:
+    return int(load().attn_bwd_bias_workspace_size(B, H, Sq, D, Bb, Hb, Sq_b, Sk_b))
 
 
 def attn_bwd_padded_varlen(q, k, v, o, lse, dout, dq, dk, dv, sm_scale, causal, workspace,

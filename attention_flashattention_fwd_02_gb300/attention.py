@@ -24,14 +24,18 @@ def _lse_like(q: torch.Tensor) -> torch.Tensor:
 def forward(q, k, v, sm_scale: Optional[float] = None, causal: bool = False,
             cu_seqlens_q=None, cu_seqlens_k=None, compact: bool = False, max_seqlen_q: int = 0,
             max_seqlen_k: int = 0, out=None, lse=None, workspace=None, stream=None, bias=None):
-    """bias: optional additive bias (Bb, Hb, Sq, Sk), Bb in {1, B}, Hb in {1, H}, its Sq
-    stride a multiple of 8 elements (dense and padded forms)."""
+    """bias: optional additive bias, its Sq stride a multiple of 8 elements: (Bb, Hb, Sq, Sk)
+    with Bb in {1, B}, Hb in {1, H} for dense and padded inputs; (Bb, Hb, >= max_seqlen_q,
+    >= max_seqlen_k) with Bb in {1, num_seqs} for compact inputs, sequence s's block at offset
+    0 of slice s."""
     sm_scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else sm_scale
     o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if out is None else out
     lse = _lse_like(q) if lse is None else lse
-    if bias is not None:
-        if compact:
-            raise ValueError("an additive bias is supported for dense and padded inputs only")
+    if bias is not None and compact:
+        _lib.attn_fwd_compact_varlen_bias(q, k, v, bias, o, lse, cu_seqlens_q, cu_seqlens_k,
+                                          cu_seqlens_q.numel() - 1, max_seqlen_q, max_seqlen_k,
+                                          sm_scale, causal, workspace, stream)
+    elif bias is not None:
         _lib.attn_fwd_bias(q, k, v, bias, o, lse, sm_scale, causal, workspace, cu_seqlens_q,
                            cu_seqlens_k, stream)
     elif compact:
@@ -44,10 +48,15 @@ def forward(q, k, v, sm_scale: Optional[float] = None, causal: bool = False,
     return o, lse
 
 
-def bwd_workspace(q: torch.Tensor) -> torch.Tensor:
+def bwd_workspace(q: torch.Tensor, bias: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Zeroed backward workspace (the status word starts at 0); with a bias, room for the
+    sums of its gradient when it is shared over units or heads."""
     B, H, S, D = q.shape
-    n = _lib.attn_bwd_workspace_size(B, H, S, D)
-    return torch.zeros(n, dtype=torch.uint8, device=q.device)  # status word starts at 0
+    if bias is None:
+        n = _lib.attn_bwd_workspace_size(B, H, S, D)
+    else:
+        n = _lib.attn_bwd_bias_workspace_size(B, H, S, D, *bias.shape)
+    return torch.zeros(n, dtype=torch.uint8, device=q.device)
 
 
 def backward(q, k, v, o, lse, do, sm_scale: Optional[float] = None, causal: bool = False,
@@ -56,17 +65,21 @@ def backward(q, k, v, o, lse, do, sm_scale: Optional[float] = None, causal: bool
              deterministic: bool = False, bias=None, dbias=None):
     """dQ, dK, dV through the C ABI. deterministic=True takes the run-to-run reproducible
     path (dQ accumulated per query block without reductions; S and dP computed twice).
-    bias: the bias given to forward; dbias: optional zeroed full-shape tensor for its
-    gradient."""
+    bias: the bias given to forward; dbias: optional tensor of the bias's shape for its
+    gradient (zeroed when the bias has full batch and head dimensions: only the visited tiles
+    are written; every entry is written for a bias with a size-1 batch or head dimension)."""
     sm_scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else sm_scale
     dq = torch.empty(q.shape, dtype=q.dtype, device=q.device) if dq is None else dq
     dk = torch.empty(k.shape, dtype=k.dtype, device=k.device) if dk is None else dk
     dv = torch.empty(v.shape, dtype=v.dtype, device=v.device) if dv is None else dv
-    ws = bwd_workspace(q) if workspace is None else workspace
-    if bias is not None:
-        if compact or deterministic:
-            raise ValueError("the bias backward supports dense and padded inputs, "
-                             "non-deterministic")
+    ws = bwd_workspace(q, bias) if workspace is None else workspace
+    if bias is not None and deterministic:
+        raise ValueError("the bias backward has no deterministic form")
+    if bias is not None and compact:
+        _lib.attn_bwd_compact_varlen_bias(q, k, v, o, lse, do, bias, dq, dk, dv, cu_seqlens_q,
+                                          cu_seqlens_k, cu_seqlens_q.numel() - 1, max_seqlen_q,
+                                          max_seqlen_k, sm_scale, causal, ws, dbias, stream)
+    elif bias is not None:
         _lib.attn_bwd_bias(q, k, v, o, lse, do, bias, dq, dk, dv, sm_scale, causal, ws, dbias,
                            cu_seqlens_q, cu_seqlens_k, stream)
     elif compact:

@@ -36,8 +36,9 @@ def bhsd_to_thd(x: torch.Tensor) -> torch.Tensor:
 
 
 class FlashAttentionFunction(torch.autograd.Function):
-    """Fused attention with gradients for q, k, v (bf16 or fp16, BHSD views) and, for a
-    full-shape additive bias that requires it, for the bias."""
+    """Fused attention with gradients for q, k, v (bf16 or fp16, BHSD views) and, for an
+    additive bias that requires it, for the bias (summed over the batch entries, sequences or
+    heads a bias with a size-1 dimension is shared by)."""
 
     @staticmethod
     def forward(ctx, q, k, v, sm_scale, causal, cu_seqlens_q, cu_seqlens_k, compact,
@@ -56,9 +57,11 @@ class FlashAttentionFunction(torch.autograd.Function):
         do = do.contiguous() if do.stride(-1) != 1 else do
         dbias = None
         if bias is not None and ctx.needs_input_grad[11]:
-            if bias.shape[0] != q.shape[0] or bias.shape[1] != q.shape[1]:
-                raise NotImplementedError("a bias gradient needs a bias of shape (B, H, Sq, Sk)")
-            dbias = torch.zeros_like(bias)  # tiles the kernel does not visit stay zero
+            # a full-shape gradient is written on the tiles the kernel visits only; rows padded
+            # to a multiple of 8 keys (the library's stride rule)
+            Skb = bias.shape[-1]
+            dbias = torch.zeros(*bias.shape[:-1], (Skb + 7) // 8 * 8, dtype=bias.dtype,
+                                device=bias.device)[..., :Skb]
         dq, dk, dv = attention.backward(q, k, v, o, lse, do, sm_scale, causal, cu_q, cu_k,
                                         compact=compact, max_seqlen_q=max_q, max_seqlen_k=max_k,
                                         deterministic=det, bias=bias, dbias=dbias)
@@ -70,8 +73,8 @@ def flash_attention(q, k, v, sm_scale: Optional[float] = None, causal: bool = Fa
                     bias=None):
     """Dense (cu_seqlens None) or padded-varlen attention on BHSD views, differentiable.
     deterministic=True makes the gradients identical from run to run. bias: optional
-    additive bias (Bb, Hb, Sq, Sk) with its Sq stride a multiple of 8 elements (d_head <= 64);
-    it gets a gradient when it has the full shape (B, H, Sq, Sk) and requires one."""
+    additive bias (Bb, Hb, Sq, Sk), Bb in {1, B}, Hb in {1, H}, with its Sq stride a multiple
+    of 8 elements (d_head up to 128); it gets a gradient when it requires one."""
     scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else float(sm_scale)
     return FlashAttentionFunction.apply(q, k, v, scale, bool(causal), cu_seqlens_q, cu_seqlens_k,
                                         False, 0, 0, bool(deterministic), bias)
@@ -80,10 +83,13 @@ def flash_attention(q, k, v, sm_scale: Optional[float] = None, causal: bool = Fa
 def flash_attention_varlen(q_thd, k_thd, v_thd, cu_seqlens_q, cu_seqlens_k,
                            max_seqlen_q: int = 0, max_seqlen_k: int = 0,
                            sm_scale: Optional[float] = None, causal: bool = False,
-                           deterministic: bool = False):
-    """Compact varlen attention on packed (T, H, D) tensors; returns (T, H, D)."""
+                           deterministic: bool = False, bias=None):
+    """Compact varlen attention on packed (T, H, D) tensors; returns (T, H, D). bias:
+    optional additive bias (Bb, Hb, >= max_seqlen_q, >= max_seqlen_k), Bb in {1, num_seqs},
+    Hb in {1, H}; sequence s uses the block at offset 0 of slice s."""
     scale = 1.0 / math.sqrt(q_thd.shape[-1]) if sm_scale is None else float(sm_scale)
     o = FlashAttentionFunction.apply(thd_to_bhsd(q_thd), thd_to_bhsd(k_thd), thd_to_bhsd(v_thd),
                                      scale, bool(causal), cu_seqlens_q, cu_seqlens_k, True,
-                                     int(max_seqlen_q), int(max_seqlen_k), bool(deterministic))
+                                     int(max_seqlen_q), int(max_seqlen_k), bool(deterministic),
+                                     bias)
     return bhsd_to_thd(o)

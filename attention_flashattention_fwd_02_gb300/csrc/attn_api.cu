@@ -139,6 +139,36 @@ attn_status check_lse(const attn_tensor3* lse, const Problem& pr) {
   return ATTN_OK;
 }
 
+// An additive bias (Bb, Hb, Sq_b, Sk_b) in q's element type: Bb in {1, units} (units = B,
+// or num_seqs for compact varlen), Hb in {1, H}; dense and padded forms take Sq_b = Sq,
+// Sk_b = Sk; compact sequences index the block at offset 0 of their own slice, so Sq_b and
+// Sk_b must hold the longest sequence (the max_seqlen bounds). d_head up to 128.
+attn_status check_bias(const attn_tensor4* bias, const attn_tensor4* q, const attn_tensor4* k,
+                       const Problem& pr) {
+  if (pr.D > 128) return ATTN_ERR_UNSUPPORTED;
+  attn_status s = check_tensor4(bias);
+  if (s != ATTN_OK) return s;
+  if (!same_dtype(q, bias)) return ATTN_ERR_DTYPE;
+  if ((bias->size[0] != 1 && bias->size[0] != pr.units) ||
+      (bias->size[1] != 1 && bias->size[1] != pr.H))
+    return ATTN_ERR_SHAPE;
+  if (pr.mode == kCompact) {
+    if (bias->size[2] < pr.max_q || bias->size[3] < pr.max_k) return ATTN_ERR_SHAPE;
+  } else if (bias->size[2] != q->size[2] || bias->size[3] != k->size[2]) {
+    return ATTN_ERR_SHAPE;
+  }
+  return ATTN_OK;
+}
+
+// A bias with a size-1 batch or head dimension gets its gradient summed in fp32 in the
+// workspace, after the status word, Delta and the dQ accumulator.
+bool bias_shared(const attn_tensor4* bias) { return bias->size[0] == 1 || bias->size[1] == 1; }
+
+size_t dbias_acc_bytes(const attn_tensor4* bias) {
+  return (size_t)bias->size[0] * (size_t)bias->size[1] * (size_t)bias->size[2] *
+         (size_t)bias->size[3] * 4;
+}
+
 SeqAddr seq_addr(const Problem& pr) {
   SeqAddr a;
   a.cu_q = pr.cu_q;
@@ -281,20 +311,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   Problem pr;
   attn_status s = make_problem(q, k, v, cu_q, cu_k, compact, num_seqs, max_q, max_k, &pr);
   if (s != ATTN_OK) return s;
-  if (bias != nullptr) {
-    // (Bb, Hb, Sq, Sk), Bb in {1, B}, Hb in {1, H}; dense or padded forms only; d_head up to
-    // 64 (the 64-wide kernel) and fewer than 2^31 bias elements, the configurations that
-    // have run on the GPU
-    if (compact || q->size[3] > 64) return ATTN_ERR_UNSUPPORTED;
-    if (bias->size[0] * bias->size[1] * bias->size[2] * bias->size[3] >= (int64_t(1) << 31))
-      return ATTN_ERR_UNSUPPORTED;
-    if ((s = check_tensor4(bias)) != ATTN_OK) return s;
-    if (!same_dtype(q, bias)) return ATTN_ERR_DTYPE;
-    if (bias->size[2] != q->size[2] || bias->size[3] != k->size[2] ||
-        (bias->size[0] != 1 && bias->size[0] != q->size[0]) ||
-        (bias->size[1] != 1 && bias->size[1] != q->size[1]))
-      return ATTN_ERR_SHAPE;
-  }
+  if (bias != nullptr && (s = check_bias(bias, q, k, pr)) != ATTN_OK) return s;
   if ((s = check_tensor4(o)) != ATTN_OK) return s;
   if (!same_shape(q, o)) return ATTN_ERR_SHAPE;
   if (!same_dtype(q, o)) return ATTN_ERR_DTYPE;
@@ -314,7 +331,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   if ((s = make_map(&p.tm_v, v, 128)) != ATTN_OK) return s;
   if (bias != nullptr) {
     if ((s = make_map(&p.tm_b, bias, 128)) != ATTN_OK) return s;
-    p.bias_b_bcast = bias->size[0] == 1 && pr.B > 1;
+    p.bias_b_bcast = bias->size[0] == 1 && pr.units > 1;
     p.bias_h_bcast = bias->size[1] == 1 && pr.H > 1;
   }
   p.o = reinterpret_cast<uint16_t*>(o->data);
@@ -358,7 +375,12 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
   // d_head 256: the key-tile kernel's dK and dV accumulators alone would fill TMEM
   if (pr.D > 128) return ATTN_ERR_UNSUPPORTED;
   const BwdWorkspace w = bwd_layout(pr.B, pr.H, pr.Sq, pr.D);
-  if (ws == nullptr || ws_bytes < (deterministic ? w.dq_off : w.total)) return ATTN_ERR_WORKSPACE;
+  // the fp32 sums of a shared bias's gradient follow the regular workspace
+  const bool dbias_sum = a.bias != nullptr && a.dbias != nullptr && bias_shared(a.bias);
+  const size_t acc_off = align256(w.total);
+  const size_t need = dbias_sum ? acc_off + dbias_acc_bytes(a.bias)
+                                : (deterministic ? w.dq_off : w.total);
+  if (ws == nullptr || ws_bytes < need) return ATTN_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return ATTN_ERR_ALIGN;
   attn_status s = check_device();
   if (s != ATTN_OK) return s;
@@ -431,7 +453,17 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
         p.b_sb = a.bias->size[0] == 1 ? 0 : a.bias->stride[0];
         p.b_sh = a.bias->size[1] == 1 ? 0 : a.bias->stride[1];
         p.b_ss = a.bias->stride[2];
-        if (a.dbias != nullptr) {
+        if (dbias_sum) {
+          // summed in fp32 over the units / heads that share the bias, rounded afterwards
+          float* acc = reinterpret_cast<float*>(base + acc_off);
+          if (cudaMemsetAsync(acc, 0, dbias_acc_bytes(a.bias), st) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+          const int64_t Hb = a.bias->size[1], Sqb = a.bias->size[2], Skb = a.bias->size[3];
+          p.dbias_acc = acc;
+          p.dba_sb = a.bias->size[0] == 1 ? 0 : Hb * Sqb * Skb;
+          p.dba_sh = Hb == 1 ? 0 : Sqb * Skb;
+          p.dba_ss = Skb;
+        } else if (a.dbias != nullptr) {
           p.dbias = reinterpret_cast<uint16_t*>(a.dbias->data);
           p.db_sb = a.dbias->stride[0];
           p.db_sh = a.dbias->stride[1];
@@ -441,6 +473,21 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       if (launch_bwd_main(p, kernel_width(pr.D), pr.f16, a.bias != nullptr, grid, st) !=
           cudaSuccess)
         return ATTN_ERR_CUDA;
+    }
+    if (dbias_sum) {
+      DbiasPostParams dp;
+      memset(&dp, 0, sizeof(dp));
+      dp.acc = reinterpret_cast<const float*>(base + acc_off);
+      dp.dbias = reinterpret_cast<uint16_t*>(a.dbias->data);
+      dp.db_sb = a.dbias->stride[0];
+      dp.db_sh = a.dbias->stride[1];
+      dp.db_ss = a.dbias->stride[2];
+      dp.rows = a.bias->size[0] * a.bias->size[1] * a.bias->size[2];
+      dp.Hb = (int)a.bias->size[1];
+      dp.Sq = (int)a.bias->size[2];
+      dp.Sk = (int)a.bias->size[3];
+      dp.f16 = pr.f16 ? 1 : 0;
+      if (launch_dbias_epilogue(dp, st) != cudaSuccess) return ATTN_ERR_CUDA;
     }
   }
   if (stage_mask & 4) {
@@ -509,24 +556,13 @@ attn_status bwd_validate(const BwdArgs& a, const int32_t* cu_q, const int32_t* c
   if ((s = check_lse(a.lse, pr)) != ATTN_OK) return s;
   if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
   if (a.bias != nullptr) {
-    // as attn_fwd_bias: dense / padded forms, d_head <= 64, fewer than 2^31 elements; a
-    // gradient only for a full-shape bias (no broadcast sums)
-    if (compact || deterministic || pr.D > 64) return ATTN_ERR_UNSUPPORTED;
-    if ((s = check_tensor4(a.bias)) != ATTN_OK) return s;
-    if (!same_dtype(a.q, a.bias)) return ATTN_ERR_DTYPE;
-    if (a.bias->size[2] != a.q->size[2] || a.bias->size[3] != a.k->size[2] ||
-        (a.bias->size[0] != 1 && a.bias->size[0] != a.q->size[0]) ||
-        (a.bias->size[1] != 1 && a.bias->size[1] != a.q->size[1]))
-      return ATTN_ERR_SHAPE;
-    if (a.bias->size[0] * a.bias->size[1] * a.bias->size[2] * a.bias->size[3] >=
-        (int64_t(1) << 31))
-      return ATTN_ERR_UNSUPPORTED;
+    // as the biased forward; no deterministic form
+    if (deterministic) return ATTN_ERR_UNSUPPORTED;
+    if ((s = check_bias(a.bias, a.q, a.k, pr)) != ATTN_OK) return s;
     if (a.dbias != nullptr) {
       if ((s = check_tensor4(a.dbias)) != ATTN_OK) return s;
       if (!same_dtype(a.q, a.dbias)) return ATTN_ERR_DTYPE;
       if (!same_shape(a.bias, a.dbias)) return ATTN_ERR_SHAPE;
-      if (a.bias->size[0] != a.q->size[0] || a.bias->size[1] != a.q->size[1])
-        return ATTN_ERR_UNSUPPORTED;
     }
   } else if (a.dbias != nullptr) {
     return ATTN_ERR_NULL;
@@ -578,6 +614,14 @@ size_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D) {
   return bwd_layout(B, H, Sq, D).total;
 }
 
+size_t attn_bwd_bias_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D,
+                                    int64_t Bb, int64_t Hb, int64_t Sq_b, int64_t Sk_b) {
+  const size_t base = bwd_layout(B, H, Sq, D).total;
+  if (Bb != 1 && Hb != 1) return base;
+  const auto nn = [](int64_t x) { return (size_t)(x > 0 ? x : 0); };
+  return align256(base) + nn(Bb) * nn(Hb) * nn(Sq_b) * nn(Sk_b) * 4;
+}
+
 size_t attn_bwd_deterministic_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D) {
   return bwd_layout(B, H, Sq, D).dq_off;  // status word and Delta
 }
@@ -597,6 +641,19 @@ attn_status attn_fwd_bias(const attn_tensor4* q, const attn_tensor4* k, const at
                           size_t workspace_bytes, void* stream) {
   return fwd_common(q, k, v, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, causal, o, lse,
                     workspace, workspace_bytes, stream, bias);
+}
+
+attn_status attn_fwd_compact_varlen_bias(const attn_tensor4* q, const attn_tensor4* k,
+                                         const attn_tensor4* v, const attn_tensor4* bias,
+                                         const int32_t* cu_seqlens_q,
+                                         const int32_t* cu_seqlens_k, int32_t num_seqs,
+                                         int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                         float sm_scale, int causal, const attn_tensor4* o,
+                                         const attn_tensor3* lse, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (bias == nullptr) return ATTN_ERR_NULL;
+  return fwd_common(q, k, v, cu_seqlens_q, cu_seqlens_k, 1, num_seqs, max_seqlen_q, max_seqlen_k,
+                    sm_scale, causal, o, lse, workspace, workspace_bytes, stream, bias);
 }
 
 attn_status attn_fwd_padded_varlen(const attn_tensor4* q, const attn_tensor4* k,
@@ -666,6 +723,19 @@ attn_status attn_bwd_bias(const attn_tensor4* q, const attn_tensor4* k, const at
   BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse, bias, dbias};
   return bwd_common(a, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, causal, workspace,
                     workspace_bytes, stream);
+}
+
+attn_status attn_bwd_compact_varlen_bias(
+    const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v, const attn_tensor4* o,
+    const attn_tensor3* lse, const attn_tensor4* dout, const attn_tensor4* bias,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t max_seqlen_q, int32_t max_seqlen_k, float sm_scale, int causal,
+    const attn_tensor4* dq, const attn_tensor4* dk, const attn_tensor4* dv,
+    const attn_tensor4* dbias, void* workspace, size_t workspace_bytes, void* stream) {
+  if (bias == nullptr) return ATTN_ERR_NULL;
+  BwdArgs a{q, k, v, o, dout, dq, dk, dv, lse, bias, dbias};
+  return bwd_common(a, cu_seqlens_q, cu_seqlens_k, 1, num_seqs, max_seqlen_q, max_seqlen_k,
+                    sm_scale, causal, workspace, workspace_bytes, stream);
 }
 
 attn_status attn_bwd_deterministic(const attn_tensor4* q, const attn_tensor4* k,

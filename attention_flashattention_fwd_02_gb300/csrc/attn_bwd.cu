@@ -148,6 +148,30 @@ cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
+// =========================================================================== dbias epilogue
+// The gradient of a bias shared by several units or heads: dbias = the fp32 sums the
+// key-tile kernel added up, rounded to the element type, over the bias's whole shape (zero
+// wherever no sequence reached). One block per row, threads over its keys.
+template <bool F16>
+__global__ void __launch_bounds__(256) attn_dbias_post_kernel(const __grid_constant__ DbiasPostParams p) {
+  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+    const int64_t b = row / ((int64_t)p.Hb * p.Sq), hq = row % ((int64_t)p.Hb * p.Sq);
+    const int64_t hh = hq / p.Sq, q = hq % p.Sq;
+    const float* src = p.acc + row * p.Sk;
+    uint16_t* dst = p.dbias + b * p.db_sb + hh * p.db_sh + q * p.db_ss;
+    for (int k = threadIdx.x; k < p.Sk; k += blockDim.x)
+      dst[k] = (uint16_t)(pack2<F16>(src[k], 0.f) & 0xffffu);
+  }
+}
+
+cudaError_t launch_dbias_epilogue(const DbiasPostParams& p, cudaStream_t stream) {
+  if (p.rows == 0 || p.Sk == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)(p.rows < 65536 * 16 ? p.rows : 65536 * 16);
+  if (p.f16) attn_dbias_post_kernel<true><<<grid, 256, 0, stream>>>(p);
+  else attn_dbias_post_kernel<false><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 // =========================================================================== main kernel
 template <int D>
 struct BwdCfg {
@@ -208,14 +232,15 @@ struct BwdBars {
   alignas(16) float ndelta[LSE_ST][BM];  // -Delta
 };
 
-// BIAS (the 64-wide configuration only): an additive bias enters the rebuilt scores. Each
-// compute thread (one key row) reads its key's column of the bias for the step's query rows
-// straight from global memory (a warp reads 32 consecutive keys of one query row per load)
-// and, when p.dbias is set, writes dS to the same places.
+// BIAS: an additive bias enters the rebuilt scores. Each compute thread (one key row) reads
+// its key's column of the bias for the step's query rows straight from global memory (a warp
+// reads 32 consecutive keys of one query row per load); every unit (batch, or sequence of a
+// compact batch) finds its block at offset 0 of its own slice of the bias's first dimension.
+// With p.dbias set, dS is written to the same places; with p.dbias_acc set (a bias shared by
+// several units or heads), dS is added in fp32 to an accumulator of the bias's shape.
 template <int D, bool F16, bool BIAS = false>
 __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
-  static_assert(!BIAS || D == 64, "bias kernels exist for the 64-wide configuration only");
   using C = BwdCfg<D>;
   constexpr int BN = C::BN, BM = C::BM;
   constexpr int HALF = BM / 2;  // score columns per compute warpgroup
@@ -552,7 +577,7 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
         // bias log2(e) of this key and the chunk's 32 query rows (0 off the sequence)
         float bl[BIAS ? 32 : 1];
         if constexpr (BIAS) {
-          const uint16_t* bcol = p.bias + sv.batch * p.b_sb + h * p.b_sh + key;
+          const uint16_t* bcol = p.bias + z * p.b_sb + h * p.b_sh + key;
           uint16_t raw[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -591,9 +616,15 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
             const float4 l4 = *reinterpret_cast<const float4*>(&bars.nlse2[st][c0 + e4]);
             const float4 d4 = *reinterpret_cast<const float4*>(&bars.ndelta[st][c0 + e4]);
             float y[4];
-            // P = 2^(S c2 - LSE2); dS = P (dP - Delta): paired fp32 instructions
-            f2_unpack(f2_fma(f2_pack(s[e4], s[e4 + 1]), c2x2, f2_pack(l4.x, l4.y)), x[0], x[1]);
-            f2_unpack(f2_fma(f2_pack(s[e4 + 2], s[e4 + 3]), c2x2, f2_pack(l4.z, l4.w)), x[2], x[3]);
+            // P = 2^(S c2 [+ bias log2(e)] - LSE2); dS = P (dP - Delta): paired fp32
+            // instructions
+            uint64_t a01 = f2_pack(l4.x, l4.y), a23 = f2_pack(l4.z, l4.w);
+            if constexpr (BIAS) {
+              a01 = f2_add(a01, f2_pack(bl[e4], bl[e4 + 1]));
+              a23 = f2_add(a23, f2_pack(bl[e4 + 2], bl[e4 + 3]));
+            }
+            f2_unpack(f2_fma(f2_pack(s[e4], s[e4 + 1]), c2x2, a01), x[0], x[1]);
+            f2_unpack(f2_fma(f2_pack(s[e4 + 2], s[e4 + 3]), c2x2, a23), x[2], x[3]);
 #pragma unroll
             for (int u = 0; u < 4; ++u) pv[u] = ex2_approx(x[u]);
             f2_unpack(f2_add(f2_pack(dp[e4], dp[e4 + 1]), f2_pack(d4.x, d4.y)), y[0], y[1]);
@@ -610,6 +641,16 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
               ds[u] = valid ? ds[u] : 0.f;
             }
           }
+          if constexpr (BIAS) {
+            if (p.dbias_acc != nullptr && key_ok) {  // a shared bias: sum dS in fp32
+              float* acol = p.dbias_acc + z * p.dba_sb + h * p.dba_sh + key;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int qq = q_lo + c0 + e4 + u;
+                if (qq < sv.len_q && qq >= q_min) atomicAdd(acol + (int64_t)qq * p.dba_ss, ds[u]);
+              }
+            }
+          }
           pp[e4 / 2] = pack2<F16>(pv[0], pv[1]);
           pp[e4 / 2 + 1] = pack2<F16>(pv[2], pv[3]);
           pd[e4 / 2] = pack2<F16>(ds[0], ds[1]);
@@ -617,7 +658,7 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
         }
         if constexpr (BIAS) {
           if (p.dbias != nullptr && key_ok) {  // dbias = dS (rounded like the dS operand)
-            uint16_t* dcol = p.dbias + sv.batch * p.db_sb + h * p.db_sh + key;
+            uint16_t* dcol = p.dbias + z * p.db_sb + h * p.db_sh + key;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const int qq = q_lo + c0 + e;
@@ -758,8 +799,10 @@ static cudaError_t launch_bwd_main_impl(const BwdParams& p, dim3 grid, cudaStrea
 
 cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, bool bias, dim3 grid,
                             cudaStream_t stream) {
-  if (bias) {  // the bias kernels exist for the 64-wide configuration only
-    if (D != 64) return cudaErrorInvalidValue;
+  if (bias) {
+    if (D == 128)
+      return f16 ? launch_bwd_main_impl<128, true, true>(p, grid, stream)
+                 : launch_bwd_main_impl<128, false, true>(p, grid, stream);
     return f16 ? launch_bwd_main_impl<64, true, true>(p, grid, stream)
                : launch_bwd_main_impl<64, false, true>(p, grid, stream);
   }

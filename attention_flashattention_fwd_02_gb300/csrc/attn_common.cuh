@@ -109,6 +109,8 @@ struct BwdParams {
   int64_t b_sb, b_sh, b_ss;       //   b*b_sb + h*b_sh + q*b_ss + key (0 strides broadcast)
   uint16_t* dbias;                // BIAS kernels, may be null: dS written at the same layout
   int64_t db_sb, db_sh, db_ss;
+  float* dbias_acc;               // BIAS kernels, may be null: dS added (fp32) at element
+  int64_t dba_sb, dba_sh, dba_ss; //   b*dba_sb + h*dba_sh + q*dba_ss + key (0 strides sum)
   uint64_t timeout_ns;            // bound on every pipeline wait
   int withhold_step;              // test hook: step whose Q / dO the producer never loads (-1)
   int with_dq;                    // 0: no dQ products (the deterministic dQ kernel makes dQ)
@@ -126,6 +128,16 @@ struct BwdPostParams {
   int f16;                        // element type: 0 bf16, 1 fp16
   SeqAddr seq;
   float sm_scale;
+};
+
+// Rounds the fp32 gradient of a shared bias to the element type.
+struct DbiasPostParams {
+  const float* acc;               // [rows][Sk] fp32, rows = Bb * Hb * Sq
+  uint16_t* dbias;                // (Bb, Hb, Sq, Sk), element strides below (key stride 1)
+  int64_t db_sb, db_sh, db_ss;
+  int64_t rows;
+  int Hb, Sq, Sk;
+  int f16;
 };
 
 // Deterministic dQ kernel: one CTA per 128 query rows, walking the key tiles in order.

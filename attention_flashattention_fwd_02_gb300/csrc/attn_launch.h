@@ -22,6 +22,7 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, bool bias, dim3 grid,
                             cudaStream_t stream);
 cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream);
+cudaError_t launch_dbias_epilogue(const DbiasPostParams& p, cudaStream_t stream);
 // Deterministic dQ: grid = (query blocks, H, units); a block covers bwd_dq_block_m() rows.
 int bwd_dq_block_m();
 cudaError_t launch_bwd_dq(const BwdDqParams& p, int D, bool f16, dim3 grid, cudaStream_t stream);

@@ -134,23 +134,43 @@ attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_te
 
 /*
  * Forward pass with an additive attention bias (the bias argument that the AOTriton varlen
- * page reserves): S = sm_scale * Q K^T + bias, then mask and softmax; lse is that of the
- * biased scores. Arguments as in attn_fwd (dense, or padded varlen with cu_seqlens), plus
+ * page reserves, note 1 of "Add varlen support to AOTriton's Flash Attention"):
+ * S = sm_scale * Q K^T + bias, then mask and softmax; lse is that of the biased scores.
+ * Arguments as in attn_fwd (dense, or padded varlen with cu_seqlens), plus
  *   bias: (Bb, Hb, Sq, Sk) in q's element type, Bb in {1, B} and Hb in {1, H} (size 1
  *         broadcasts; pass size-1 dimensions, not zero strides). D stride 1; the Sq stride
  *         (and the other strides) a multiple of 8 elements, so a row of Sk keys is padded to
  *         a multiple of 8 elements when Sk is not; 16-byte aligned base. Padded varlen uses
- *         the block at offset 0 of each batch, like q. Compact varlen is not offered
- *         (ATTN_ERR_UNSUPPORTED through this call with num_seqs semantics does not exist).
- * Supported for d_head 32 and 64, and for biases of fewer than 2^31 elements
- * (ATTN_ERR_UNSUPPORTED otherwise). A NULL bias is the same as attn_fwd. Errors as attn_fwd;
- * ATTN_ERR_SHAPE for a bias whose sizes do not fit. attn_bwd_bias is the matching backward.
+ *         the block at offset 0 of each batch, like q.
+ * Supported for d_head 32, 64, 96 and 128 (ATTN_ERR_UNSUPPORTED for 256). A NULL bias is
+ * the same as attn_fwd. Errors as attn_fwd; ATTN_ERR_SHAPE for a bias whose sizes do not
+ * fit. attn_bwd_bias is the matching backward; attn_fwd_compact_varlen_bias the compact
+ * form.
  */
 attn_status attn_fwd_bias(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
                           const attn_tensor4* bias, const int32_t* cu_seqlens_q,
                           const int32_t* cu_seqlens_k, float sm_scale, int causal,
                           const attn_tensor4* o, const attn_tensor3* lse, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/*
+ * Compact varlen forward with an additive bias: arguments as in attn_fwd_compact_varlen plus
+ *   bias: (Bb, Hb, Sq_b, Sk_b), Bb in {1, num_seqs}, Hb in {1, H}, Sq_b >= max_seqlen_q and
+ *         Sk_b >= max_seqlen_k (the sequence-length bounds of the call; pass them). Sequence s
+ *         finds its [len_q, len_k] block at offset 0 of slice s of the first dimension (slice
+ *         0 when Bb = 1), as a padded batch entry does: the pages reserve the argument without
+ *         fixing its layout, and offset-0 blocks keep every tensor-memory-accelerator copy of
+ *         the bias on a 16-byte boundary. Strides as for attn_fwd_bias. Errors as
+ *         attn_fwd_compact_varlen, ATTN_ERR_SHAPE for a bias whose sizes do not fit.
+ */
+attn_status attn_fwd_compact_varlen_bias(const attn_tensor4* q, const attn_tensor4* k,
+                                         const attn_tensor4* v, const attn_tensor4* bias,
+                                         const int32_t* cu_seqlens_q,
+                                         const int32_t* cu_seqlens_k, int32_t num_seqs,
+                                         int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                         float sm_scale, int causal, const attn_tensor4* o,
+                                         const attn_tensor3* lse, void* workspace,
+                                         size_t workspace_bytes, void* stream);
 
 /*
  * Backward pass matching attn_fwd (same q, k, v, cu_seqlens, sm_scale, causal; o and lse
@@ -169,12 +189,18 @@ attn_status attn_bwd(const attn_tensor4* q, const attn_tensor4* k, const attn_te
 
 /*
  * Backward pass matching attn_fwd_bias: arguments as in attn_bwd plus the bias given to the
- * forward pass (non-NULL, same limits: d_head 32 or 64, fewer than 2^31 elements, dense or
- * padded forms). dbias, optional (NULL: no bias gradient), receives dS = the gradient with
- * respect to the bias, rounded to the element type; it must have the bias's full shape
- * (B, H, Sq, Sk) -- a broadcast bias gets no gradient here (ATTN_ERR_UNSUPPORTED) -- and is
- * written only on the (query, key) tiles the kernel visits: entries in fully masked causal
- * tiles and past a sequence's length are left as they are, so pass it zeroed.
+ * forward pass (non-NULL, same limits). dbias, optional (NULL: no bias gradient), has the
+ * bias's shape and receives the gradient with respect to the bias:
+ *   - a bias whose batch and head dimensions both have more than one entry: dS itself,
+ *     rounded to the element
+ *     type, written only on the (query, key) tiles the kernel visits -- entries in fully
+ *     masked causal tiles and past a sequence's length are left as they are, so pass it
+ *     zeroed;
+ *   - a bias with a size-1 batch or head dimension: dS summed over the units and heads that
+ *     share each entry, in fp32 in the workspace, then rounded; every entry of dbias is
+ *     written (zero where no sequence reaches). The workspace must then hold
+ *     attn_bwd_bias_workspace_size bytes. The fp32 sums are added in an order that varies
+ *     from run to run (last bits only).
  */
 attn_status attn_bwd_bias(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
                           const attn_tensor4* o, const attn_tensor3* lse, const attn_tensor4* dout,
@@ -183,6 +209,27 @@ attn_status attn_bwd_bias(const attn_tensor4* q, const attn_tensor4* k, const at
                           const attn_tensor4* dq, const attn_tensor4* dk, const attn_tensor4* dv,
                           const attn_tensor4* dbias, void* workspace, size_t workspace_bytes,
                           void* stream);
+
+/*
+ * Workspace bytes attn_bwd_bias and attn_bwd_compact_varlen_bias need for a bias of shape
+ * (Bb, Hb, Sq_b, Sk_b): attn_bwd_workspace_size(B, H, Sq, D), plus room for the fp32 sums
+ * of the bias gradient when Bb or Hb is 1 (used only when a dbias is requested).
+ */
+size_t attn_bwd_bias_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D, int64_t Bb,
+                                    int64_t Hb, int64_t Sq_b, int64_t Sk_b);
+
+/*
+ * Compact varlen backward with an additive bias: arguments as in attn_bwd_compact_varlen plus
+ * the bias given to attn_fwd_compact_varlen_bias and an optional dbias of its shape, written
+ * as described for attn_bwd_bias (the units are the sequences).
+ */
+attn_status attn_bwd_compact_varlen_bias(
+    const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v, const attn_tensor4* o,
+    const attn_tensor3* lse, const attn_tensor4* dout, const attn_tensor4* bias,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t max_seqlen_q, int32_t max_seqlen_k, float sm_scale, int causal,
+    const attn_tensor4* dq, const attn_tensor4* dk, const attn_tensor4* dv,
+    const attn_tensor4* dbias, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Deterministic backward: same arguments and results as attn_bwd, and the same bits on every

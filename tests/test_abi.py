@@ -238,38 +238,73 @@ def test_bias_stride_and_dtype_checks(lib):
                              None, 0, None) == 10  # ATTN_ERR_DTYPE
 
 
-def test_bias_head_size_and_size_limits(lib):
-    """The bias forward runs for d_head <= 64 and biases below 2^31 elements only."""
+def test_bias_head_size_limits(lib):
+    """The bias forward runs for d_head up to 128 (not 256); a 2^32-element bias passes the
+    checks (on a machine without a GPU the call then stops at the device check)."""
     r = ctypes.byref
-    q, k, v, o = (t4((1, 2, 128, 128)) for _ in range(4))
+    q, k, v, o = (t4((1, 2, 128, 256)) for _ in range(4))
     lse = t3((1, 2, 128))
     bias = t4((1, 1, 128, 128))
     assert lib.attn_fwd_bias(r(q), r(k), r(v), r(bias), None, None, 0.125, 0, r(o), r(lse),
                              None, 0, None) == ERR_UNSUPPORTED
     S = 1 << 16
-    q, k, v, o = (t4((1, 1, S, 64)) for _ in range(4))
+    q, k, v, o = (t4((1, 1, S, 128)) for _ in range(4))
     lse = t3((1, 1, S))
     bias = t4((1, 1, S, S))  # 2^32 elements
     assert lib.attn_fwd_bias(r(q), r(k), r(v), r(bias), None, None, 0.125, 0, r(o), r(lse),
-                             None, 0, None) == ERR_UNSUPPORTED
+                             None, 0, None) not in (ERR_UNSUPPORTED, ERR_SHAPE)
+
+
+def test_compact_bias_validation(lib):
+    """Compact varlen bias: (Bb, Hb, Sq_b, Sk_b), Bb in {1, num_seqs}, Hb in {1, H}, Sq_b and
+    Sk_b at least the max_seqlen bounds."""
+    r = ctypes.byref
+    q, k, v, o = (t4((1, 2, 300, 64)) for _ in range(4))
+    lse = t3((1, 2, 300))
+    cu = 1 << 20  # a device address the checks never dereference
+
+    def call(bias_shape, nseq=3, maxq=200, maxk=200):
+        bias = t4(bias_shape)
+        return lib.attn_fwd_compact_varlen_bias(r(q), r(k), r(v), r(bias), cu, cu, nseq, maxq,
+                                                maxk, 0.125, 1, r(o), r(lse), None, 0, None)
+
+    assert call((2, 2, 200, 200)) == ERR_SHAPE      # Bb neither 1 nor num_seqs
+    assert call((3, 3, 200, 200)) == ERR_SHAPE      # Hb neither 1 nor H
+    assert call((3, 2, 199, 200)) == ERR_SHAPE      # shorter than max_seqlen_q
+    assert call((1, 1, 200, 192)) == ERR_SHAPE      # narrower than max_seqlen_k
+    for shape in ((3, 2, 200, 200), (1, 1, 256, 208), (1, 2, 200, 200)):
+        assert call(shape) not in (ERR_SHAPE, ERR_UNSUPPORTED, ERR_NULL)
+    assert lib.attn_fwd_compact_varlen_bias(r(q), r(k), r(v), None, cu, cu, 3, 200, 200, 0.125,
+                                            1, r(o), r(lse), None, 0, None) == ERR_NULL
 
 
 def test_bwd_bias_validation(lib):
-    """attn_bwd_bias: bias required; d_head <= 64; a gradient only for a full-shape bias."""
+    """attn_bwd_bias: bias required; d_head up to 128; dbias of the bias's shape; a bias with a
+    size-1 batch or head dimension needs the larger workspace for its gradient's sums."""
     r = ctypes.byref
 
-    def call(shape, bias, dbias):
+    def call(shape, bias, dbias, ws=None, nws=0):
         q, k, v, o, do, dq, dk, dv = (t4(shape) for _ in range(8))
         lse = t3(shape[:3])
         return lib.attn_bwd_bias(r(q), r(k), r(v), r(o), r(lse), r(do),
                                  r(bias) if bias is not None else None, None, None, 0.125, 0,
                                  r(dq), r(dk), r(dv), r(dbias) if dbias is not None else None,
-                                 None, 0, None)
+                                 ws, nws, None)
 
     assert call((1, 2, 128, 64), None, None) == ERR_NULL
-    assert call((1, 2, 128, 128), t4((1, 2, 128, 128)), None) == ERR_UNSUPPORTED
-    assert call((2, 2, 128, 64), t4((1, 2, 128, 128)), t4((1, 2, 128, 128))) == ERR_UNSUPPORTED
+    assert call((1, 2, 128, 256), t4((1, 2, 128, 128)), None) == ERR_UNSUPPORTED
     assert call((1, 2, 128, 64), t4((1, 2, 128, 128)), t4((1, 2, 128, 136))) == ERR_SHAPE
+    base = lib.attn_bwd_workspace_size(2, 2, 128, 64)
+    full = lib.attn_bwd_bias_workspace_size(2, 2, 128, 64, 2, 2, 128, 128)
+    shared = lib.attn_bwd_bias_workspace_size(2, 2, 128, 64, 1, 2, 128, 128)
+    assert full == base and shared >= base + 2 * 128 * 128 * 4
+    ws = 1 << 20  # never dereferenced: the size check comes first
+    assert call((2, 2, 128, 64), t4((1, 2, 128, 128)), t4((1, 2, 128, 128)), ws,
+                base) == ERR_WORKSPACE
+    assert call((2, 2, 128, 64), t4((1, 2, 128, 128)), t4((1, 2, 128, 128)), ws,
+                shared) not in (ERR_WORKSPACE, ERR_SHAPE, ERR_UNSUPPORTED)
+    assert call((2, 2, 128, 64), t4((1, 2, 128, 128)), None, ws, base) not in (
+        ERR_WORKSPACE, ERR_SHAPE, ERR_UNSUPPORTED)
 
 
 def test_binding_rejects_host_tensors(lib):

@@ -86,3 +86,51 @@ def test_autograd_bias(causal):
     assert_grads_close((q.grad, k.grad, v.grad), g_r[:3], what="autograd bias")
     db = np64(bias.grad)
     assert np.linalg.norm(db - g_r[3]) / np.linalg.norm(g_r[3]) <= 2e-2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,bias_shape", [(128, (1, 2)), (64, (2, 1))])
+def test_autograd_shared_bias(D, bias_shape):
+    """flash_attention with a bias shared over the batch or the heads: its gradient is dS
+    summed over the entries that share it."""
+    gen = torch.Generator().manual_seed(19 + D)
+    B, H, S = 2, 2, 200
+    q, k, v = (torch.randn(B, H, S, D, generator=gen).bfloat16().cuda().requires_grad_(True)
+               for _ in range(3))
+    bias = torch.randn(*bias_shape, S, S, generator=gen).bfloat16().cuda().requires_grad_(True)
+    w = torch.randn(B, H, S, D, generator=gen).bfloat16().cuda()
+    o = flash_attention(q, k, v, causal=True, bias=bias)
+    (o.float() * w.float()).sum().backward()
+    scale = 1.0 / math.sqrt(D)
+    qn, kn, vn, wn, bn = (np64(t) for t in (q, k, v, w, bias))
+    g_r = ref.bwd_bhsd(qn, kn, vn, wn, scale, True, bias=bn)
+    assert_grads_close((q.grad, k.grad, v.grad), g_r[:3], what="autograd shared bias")
+    db = np64(bias.grad)
+    assert db.shape == g_r[3].shape
+    assert np.linalg.norm(db - g_r[3]) / np.linalg.norm(g_r[3]) <= 2e-2
+
+
+@pytest.mark.gpu
+def test_autograd_varlen_bias():
+    """flash_attention_varlen with a per-sequence bias (block at offset 0 of slice s)."""
+    gen = torch.Generator().manual_seed(23)
+    lengths, H, D = [70, 130, 5], 2, 128
+    T = sum(lengths)
+    cu = torch.tensor([0, 70, 200, 205], dtype=torch.int32).cuda()
+    q, k, v = (torch.randn(T, H, D, generator=gen).bfloat16().cuda().requires_grad_(True)
+               for _ in range(3))
+    bias = torch.randn(3, H, 130, 136, generator=gen).bfloat16().cuda()[..., :130]
+    bias.requires_grad_(True)
+    w = torch.randn(T, H, D, generator=gen).bfloat16().cuda()
+    o = flash_attention_varlen(q, k, v, cu, cu, 130, 130, causal=True, bias=bias)
+    (o.float() * w.float()).sum().backward()
+    scale = 1.0 / math.sqrt(D)
+    bhsd = lambda t: np64(t).transpose(1, 0, 2)[None]
+    cun = cu.cpu().numpy()
+    g_r = ref.bwd_compact_varlen(bhsd(q), bhsd(k), bhsd(v), bhsd(w), cun, cun, scale, True,
+                                 bias=np64(bias))
+    for name, g, r in zip(("dQ", "dK", "dV"), (q.grad, k.grad, v.grad), g_r[:3]):
+        gg = bhsd(g)
+        assert np.linalg.norm(gg - r) / np.linalg.norm(r) <= 2e-2, name
+    db = np64(bias.grad)
+    assert np.linalg.norm(db - g_r[3]) / np.linalg.norm(g_r[3]) <= 2e-2

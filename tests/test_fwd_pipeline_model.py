@@ -152,6 +152,8 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
                 slot, phase = t, j
             elif bias_slots == "one":  # the first 128-wide scheme: one slot for both tiles
                 slot, phase = 0, k
+            elif bias_slots == "tile2":  # one query tile with two slots (the 128-wide kernel)
+                slot, phase = 2 * t + j % 2, j // 2
             else:  # the earlier scheme: slot k mod 2, shared by the tiles
                 slot, phase = k % 2, k // 2
             if phase >= 1 and not (yield from wait(f"b_empty{slot}", phase - 1)):
@@ -235,7 +237,8 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
                 return
             yield ("read", f"SP{b}", ("S", k), me, rng.randint(0, 3))
             if bias:
-                slot, phase = {"tile": (t, j), "one": (0, k)}.get(bias_slots, (k % 2, k // 2))
+                slot, phase = {"tile": (t, j), "one": (0, k),
+                               "tile2": (2 * t + j % 2, j // 2)}.get(bias_slots, (k % 2, k // 2))
                 if not (yield from wait(f"b_full{slot}", phase)):
                     return
                 yield ("read", f"BS{slot}", (t, j), me, 0)
@@ -298,6 +301,16 @@ def test_forward_pipeline_is_exact_and_race_free(D, n0, n1):
 def test_bias_forward_pipeline(n0, n1):
     assert _runs(64, n0, n1, n0 * 10 + n1, 120, bias=True) == []
     assert _runs(64, n0, n1, n0 * 10 + n1 + 1, 120, slow=True, bias=True) == []
+
+
+@pytest.mark.parametrize("n0", [1, 2, 3, 6, 9])
+def test_bias_forward_pipeline_d128(n0):
+    """The 128-wide bias kernel: one query tile per CTA, its bias tiles alternating between
+    two slots (slot j mod 2, phase j / 2)."""
+    assert _runs(128, n0, 0, n0, 120, bias=True, bias_slots="tile2") == []
+    assert _runs(128, n0, 0, n0 + 1, 120, slow=True, bias=True, bias_slots="tile2") == []
+    tiles = [(n0, 0)]
+    assert _parity_runs(128, tiles, "tile2", n0 + 2) == set()
 
 
 def _found(D, n0, n1, trials=400, **kw):

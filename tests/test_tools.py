@@ -44,16 +44,12 @@ def test_bench_config_identical_for_both_arms():
 
 def test_attention_helpers_reject_unsupported_combinations():
     """Argument combinations the library has no kernel for are refused in Python, before any
-    device work: a bias with compact varlen, and a bias with the deterministic backward."""
+    device work: a bias with the deterministic backward."""
     import torch
-    from attention_flashattention_fwd_02_gb300.attention import backward, forward
+    from attention_flashattention_fwd_02_gb300.attention import backward
     q = torch.zeros(1, 2, 64, 64, dtype=torch.bfloat16)
     bias = torch.zeros(1, 2, 64, 64, dtype=torch.bfloat16)
-    cu = torch.tensor([0, 64], dtype=torch.int32)
-    with pytest.raises(ValueError, match="dense and padded"):
-        forward(q, q, q, causal=True, cu_seqlens_q=cu, cu_seqlens_k=cu, compact=True,
-                bias=bias)
     lse = torch.zeros(1, 2, 64)
     ws = torch.zeros(256, dtype=torch.uint8)
-    with pytest.raises(ValueError, match="non-deterministic"):
+    with pytest.raises(ValueError, match="no deterministic form"):
         backward(q, q, q, q, lse, q, deterministic=True, bias=bias, workspace=ws)
