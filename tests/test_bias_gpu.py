@@ -211,8 +211,12 @@ def test_compact_bias_parity(D, causal, bs, bh, with_db):
     lse = torch.full(q.shape[:3], float("nan"), device=DEV)
     forward(q, k, v, wl.sm_scale, causal, cu_q, cu_k, out=o, lse=lse, workspace=ws,
             bias=bias_dev, **vl)
-    dbias = torch.full_like(bias_dev, float("nan")) if (with_db and (Bb == 1 or Hb == 1)) \
-        else (torch.zeros_like(bias_dev) if with_db else None)
+    # views of row-padded tensors: the library wants the Sq stride a multiple of 8 elements
+    full_dev = full.to(DEV)
+    if with_db and (Bb == 1 or Hb == 1):  # every entry is written
+        dbias = torch.full_like(full_dev, float("nan"))[..., :maxk + 5]
+    else:
+        dbias = torch.zeros_like(full_dev)[..., :maxk + 5] if with_db else None
     bws = bwd_workspace(q, bias_dev)
     dq, dk, dv = backward(q, k, v, o, lse, do, wl.sm_scale, causal, cu_q, cu_k, workspace=bws,
                           bias=bias_dev, dbias=dbias, **vl)
