@@ -372,8 +372,10 @@ struct BwdArgs {
 attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float sm_scale,
                       int causal, void* ws, size_t ws_bytes, void* stream,
                       bool deterministic = false) {
-  // d_head 256: the key-tile kernel's dK and dV accumulators alone would fill TMEM
-  if (pr.D > 128) return ATTN_ERR_UNSUPPORTED;
+  // d_head 256: the key-tile kernel splits d over two CTAs per key tile; the deterministic
+  // dQ kernel has no such split (its dQ accumulator and S, dP would need 512 TMEM columns next
+  // to Q, dO, K and V in shared memory)
+  if (deterministic && pr.D > 128) return ATTN_ERR_UNSUPPORTED;
   const BwdWorkspace w = bwd_layout(pr.B, pr.H, pr.Sq, pr.D);
   // the fp32 sums of a shared bias's gradient follow the regular workspace
   const bool dbias_sum = a.bias != nullptr && a.dbias != nullptr && bias_shared(a.bias);
@@ -437,7 +439,8 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       p.scale_log2 = sm_scale * 1.4426950408889634f;
       p.sm_scale = sm_scale;
       p.status = status;
-      const int n_tiles = (pr.max_k + BN - 1) / BN;
+      // key tiles (two CTAs each at d_head 256, one per half of d)
+      const int n_tiles = (pr.max_k + BN - 1) / BN * bwd_ctas_per_key_tile(kernel_width(pr.D));
       // the operands every CTA of a head visits: Q, dO (16-bit) and, when this kernel
       // accumulates dQ, the fp32 accumulator
       p.tile_major = p.with_dq
@@ -596,7 +599,6 @@ attn_status bwd_check_args(const attn_tensor4* q, const attn_tensor4* k, const a
   Problem pr;
   attn_status s = bwd_validate(a, cu_seqlens_q, cu_seqlens_k, 0, -1, 0, 0, sm_scale, false, &pr);
   if (s != ATTN_OK) return s;
-  if (pr.D > 128) return ATTN_ERR_UNSUPPORTED;  // as bwd_stage
   return check_device();
 }
 

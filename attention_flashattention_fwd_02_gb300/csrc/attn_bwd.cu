@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant
 }
 
 // Power-of-two thread-group width covering head size D.
-static int pow2_width(int D) { return D <= 32 ? 32 : (D <= 64 ? 64 : 128); }
+static int pow2_width(int D) { return D <= 32 ? 32 : D <= 64 ? 64 : D <= 128 ? 128 : 256; }
 
 cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream) {
   const int W = pow2_width(p.D);
@@ -93,7 +93,10 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream) {
   const int max_len = p.seq.mode == kCompact ? p.seq.max_q : p.seq.Sq;
   dim3 grid((max_len + rows_per_block - 1) / rows_per_block, p.H, p.units);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  if (W == 128) {
+  if (W == 256) {
+    if (p.f16) attn_bwd_pre_kernel<256, true><<<grid, 256, 0, stream>>>(p);
+    else attn_bwd_pre_kernel<256, false><<<grid, 256, 0, stream>>>(p);
+  } else if (W == 128) {
     if (p.f16) attn_bwd_pre_kernel<128, true><<<grid, 256, 0, stream>>>(p);
     else attn_bwd_pre_kernel<128, false><<<grid, 256, 0, stream>>>(p);
   } else if (W == 64) {
@@ -135,7 +138,10 @@ cudaError_t launch_bwd_dq_epilogue(const BwdPostParams& p, cudaStream_t stream) 
   const int max_len = p.seq.mode == kCompact ? p.seq.max_q : p.seq.Sq;
   dim3 grid((max_len + rows_per_block - 1) / rows_per_block, p.H, p.units);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  if (W == 128) {
+  if (W == 256) {
+    if (p.f16) attn_bwd_post_kernel<256, true><<<grid, 256, 0, stream>>>(p);
+    else attn_bwd_post_kernel<256, false><<<grid, 256, 0, stream>>>(p);
+  } else if (W == 128) {
     if (p.f16) attn_bwd_post_kernel<128, true><<<grid, 256, 0, stream>>>(p);
     else attn_bwd_post_kernel<128, false><<<grid, 256, 0, stream>>>(p);
   } else if (W == 64) {
@@ -175,25 +181,36 @@ cudaError_t launch_dbias_epilogue(const DbiasPostParams& p, cudaStream_t stream)
 // =========================================================================== main kernel
 template <int D>
 struct BwdCfg {
+  // d_head 256: dK and dV of 128 keys would take all 512 TMEM columns, so a CTA accumulates
+  // dK, dV and the dQ partial for one half of d (DH = 128 columns) and recomputes S^T and dP^T
+  // over all 256 columns (its sibling CTA, with the other half, computes them too).
+  static constexpr bool DSPLIT = (D == 256);
+  static constexpr int DH = DSPLIT ? D / 2 : D;     // d columns a CTA accumulates
   static constexpr int BN = 128;                    // keys per CTA (MMA M for S^T, dP^T, dK, dV)
-  static constexpr int BM = (D == 128) ? 64 : 128;  // query rows per step
-  static constexpr bool DQ_T = (D == 128);          // dQ^T = K^T dS^T (M = D) vs dQ = dS K (M = BM)
+  static constexpr int BM = DSPLIT ? 32 : (D == 128) ? 64 : 128;  // query rows per step
+  static constexpr bool DQ_T = (D >= 128);          // dQ^T = K^T dS^T (M = DH) vs dQ = dS K (M = BM)
+  // dS is stored transposed, [key][query] in 128-byte swizzled slabs of 64 queries, except at
+  // d_head 256, whose 32-query steps are too short for such rows: there it is stored
+  // [query][key] (slabs of 64 keys), the MN-major A operand of dK and the K-major B of dQ^T.
+  static constexpr bool DS_QMAJOR = DSPLIT;
+  static constexpr int NCWG = DSPLIT ? 1 : 2;       // compute warpgroups (HALF columns each)
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int DS_BYTES = BN * BM * 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int QST = 3;                        // Q / dO / LSE / Delta stages
+  static constexpr int QST = DSPLIT ? 2 : 3;            // Q / dO / LSE / Delta stages
   static constexpr int OFF_Q = OFF_V + KV_BYTES;        // QST stages
   static constexpr int OFF_DO = OFF_Q + QST * Q_BYTES;  // QST stages
   static constexpr int OFF_DS = OFF_DO + QST * Q_BYTES; // 2 buffers
-  // dQ drain: a warpgroup of its own at d_head 128, staging in a dedicated area (8 KB per
-  // drain warp: two 32 x 32 fp32 blocks); at d_head 64 the compute warps, each staging its
+  // dQ drain: a warpgroup of its own at d_head 128 and 256, each warp staging BM / 32 blocks
+  // of 32 x 32 fp32 in an area of its own; at d_head 64 the compute warps, each staging its
   // 32 x 32 block in rows of the dS^T buffer it has just released (only that warp writes those
   // rows again, two steps later, after waiting for the reduce to read them).
   static constexpr bool DQ_WARPS = DQ_T;
+  static constexpr int DQ_BLOCKS = BM / 32;             // 32 x 32 blocks per drain warp
   static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;
-  static constexpr int STG_BYTES = DQ_WARPS ? 4 * 8192 : 0;
+  static constexpr int STG_BYTES = DQ_WARPS ? 4 * DQ_BLOCKS * 4096 : 0;
   // d_head 64: the score products also subtract LSE / sm_scale and Delta, through one more
   // K = 16 step that multiplies a tile of ones by those values (each split into three bf16
   // parts), so the compute warps read neither per column. The K = 16 operand tiles (32 bytes
@@ -205,17 +222,21 @@ struct BwdCfg {
   static_assert(!AUG || (BM == BN && QST <= 3), "augmented operand packing");
   static constexpr int LSE_ST = AUG ? 1 : QST;  // stages of the per-column LSE / Delta arrays
   static constexpr int SMEM_BYTES = OFF_AUG + AUG_BYTES + 1024;
-  // TMEM columns: dK, dV accumulators; S^T, dP^T of the current step; the dQ partial; and P^T
-  // (16-bit, two values per column) as the A operand of the dV MMA.
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
+  // TMEM columns: dK, dV accumulators (DH each); S^T, dP^T of the current step; the dQ
+  // partial; and P^T (16-bit, two values per column) as the A operand of the dV MMA.
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_DK = 0, COL_DV = D, COL_S = 2 * D, COL_DP = 2 * D + BM;
-  static constexpr uint32_t COL_DQ = 2 * D + 2 * BM;
+  static constexpr uint32_t COL_DK = 0, COL_DV = DH, COL_S = 2 * DH, COL_DP = 2 * DH + BM;
+  static constexpr uint32_t COL_DQ = 2 * DH + 2 * BM;
   static constexpr uint32_t COL_P = COL_DQ + (DQ_T ? BM : D);
   static_assert(COL_P + BM / 2 <= TMEM_COLS, "TMEM layout does not fit");
-  // warpgroups: 0, 1 compute; 2 producer (warp 8) and MMA issuer (warp 9); 3 (d_head 128)
-  // dQ drain. 512 threads leave 128 registers a thread, which the d_head 128 roles fit in
-  static constexpr int NTHREADS = DQ_WARPS ? 512 : 320;
-  static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_DRAIN0 = 12;
+  // Warps. d_head 64: 0..7 compute, 8 producer, 9 MMA (320 threads). d_head 128: 0..7
+  // compute, 8 producer, 9 MMA, 10..11 no role, 12..15 dQ drain (512 threads leave 128
+  // registers a thread, which these roles fit in). d_head 256: 0..3 compute, 4..7 dQ drain,
+  // 8 producer, 9 MMA (320 threads). A drain warp reaches the TMEM lanes of its index mod 4.
+  static constexpr int NTHREADS = (D == 128) ? 512 : 320;
+  static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_DRAIN0 = DSPLIT ? 4 : 12;
+  static constexpr int NCOMPUTE = 128 * NCWG;        // compute threads
 };
 
 template <int BM, int QST, int LSE_ST>
@@ -242,16 +263,20 @@ template <int D, bool F16, bool BIAS = false>
 __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
-  constexpr int BN = C::BN, BM = C::BM;
-  constexpr int HALF = BM / 2;  // score columns per compute warpgroup
+  static_assert(!BIAS || D <= 128, "no bias kernel at d_head 256");
+  constexpr int BN = C::BN, BM = C::BM, DH = C::DH;
+  constexpr int HALF = BM / C::NCWG;  // score columns per compute warpgroup
   extern __shared__ uint8_t smem_raw[];
   constexpr int QST = C::QST;
   __shared__ BwdBars<BM, QST, C::LSE_ST> bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // grid (key tiles, H, units), or (units, H, key tiles) for a longest-first causal order
+  // grid (key tiles, H, units), or (units, H, key tiles) for a longest-first causal order;
+  // at d_head 256 each key tile has two CTAs, one per half of d (index 2 tile + half)
   const int h = blockIdx.y;
-  const int n_tile = p.tile_major ? (int)blockIdx.z : (int)blockIdx.x;
+  const int kt = p.tile_major ? (int)blockIdx.z : (int)blockIdx.x;
+  const int n_tile = C::DSPLIT ? kt >> 1 : kt;
+  const int dh = C::DSPLIT ? kt & 1 : 0;  // the half of d this CTA accumulates
   const int z = p.tile_major ? (int)blockIdx.x : (int)blockIdx.z;
 
   SeqView sv;
@@ -278,7 +303,7 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
         const int64_t grow = sv.row0_k + key;
         uint16_t* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
         uint16_t* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
-        for (int d = 0; d < p.d_out; d += 8) {
+        for (int d = dh * DH; d < min(dh * DH + DH, p.d_out); d += 8) {
           *reinterpret_cast<uint4*>(kr + d) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(vr + d) = make_uint4(0, 0, 0, 0);
         }
@@ -300,10 +325,10 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
       mbar_init(smem_u32(&bars.q_full[s]), 33);  // producer lane 0 (tx) + 32 lanes (LSE/Delta)
       mbar_init(smem_u32(&bars.q_empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(smem_u32(&bars.ds_full[s]), 256);
+    for (int s = 0; s < 2; ++s) mbar_init(smem_u32(&bars.ds_full[s]), C::NCOMPUTE);
     mbar_init(smem_u32(&bars.s_full), 1);
-    mbar_init(smem_u32(&bars.s_free), 256);
-    mbar_init(smem_u32(&bars.p_full), 256);
+    mbar_init(smem_u32(&bars.s_free), C::NCOMPUTE);
+    mbar_init(smem_u32(&bars.p_full), C::NCOMPUTE);
     mbar_init(smem_u32(&bars.p_empty), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_empty), C::DQ_WARPS ? 128 : 256);  // the draining warps
@@ -409,16 +434,23 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
     // descriptor is warp-uniform; one elected lane issues.
     {
       constexpr uint32_t idS = idesc_f32acc(128, BM, false, false, F16);  // S^T, dP^T
-      constexpr uint32_t idG = idesc_f32acc(128, D, false, true, F16);    // dV, dK
-      constexpr uint32_t idQ = C::DQ_T ? idesc_f32acc(128, BM, true, true, F16)  // dQ^T
+      constexpr uint32_t idG = idesc_f32acc(128, DH, false, true, F16);   // dV (A from TMEM)
+      constexpr uint32_t idK = idesc_f32acc(128, DH, C::DS_QMAJOR, true, F16);  // dK
+      constexpr uint32_t idQ = C::DQ_T ? idesc_f32acc(128, BM, true, !C::DS_QMAJOR, F16)  // dQ^T
                                        : idesc_f32acc(128, D, true, true, F16);  // dQ
       const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP, tP = tmem + C::COL_P;
       const uint32_t tDK = tmem + C::COL_DK, tDV = tmem + C::COL_DV, tDQ = tmem + C::COL_DQ;
       const uint64_t k_kd = desc_kmajor(sK, BN, 0), v_kd = desc_kmajor(sV, BN, 0);
-      const uint64_t k_mn = desc_mnmajor(sK, BN, 0);
+      // the half of d this CTA accumulates starts at 64-column slab dh * DH / 64
+      const uint32_t dslab = (uint32_t)(dh * (DH / 64));
+      const uint64_t k_mn = desc_mnmajor(sK + dslab * BN * 128, BN, 0);
       const uint64_t q_kd = desc_kmajor(sQ, BM, 0), do_kd = desc_kmajor(sDO, BM, 0);
-      const uint64_t q_mn = desc_mnmajor(sQ, BM, 0), do_mn = desc_mnmajor(sDO, BM, 0);
-      const uint64_t ds_kd = desc_kmajor(sDS, BN, 0), ds_mn = desc_mnmajor(sDS, BN, 0);
+      const uint64_t q_mn = desc_mnmajor(sQ + dslab * BM * 128, BM, 0);
+      const uint64_t do_mn = desc_mnmajor(sDO + dslab * BM * 128, BM, 0);
+      // dS^T as the A operand of dK and the B operand of dQ: [key][query] slabs (K-major A,
+      // MN-major B), or [query][key] slabs (MN-major A, K-major B)
+      const uint64_t ds_a = C::DS_QMAJOR ? desc_mnmajor(sDS, BM, 0) : desc_kmajor(sDS, BN, 0);
+      const uint64_t ds_b = C::DS_QMAJOR ? desc_kmajor(sDS, BM, 0) : desc_mnmajor(sDS, BN, 0);
       const uint64_t aug_kd = desc_kmajor(sAUG, BN, 0);
       constexpr uint32_t QSTEP = C::Q_BYTES >> 4, DSSTEP = C::DS_BYTES >> 4;
       auto issue_sdp = [&](int it) -> bool {
@@ -461,8 +493,9 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ss_w(tDK, ds_kd + dso + kmajor_step(BN, kk), q_mn + qo + mnmajor_step(kk), idG,
-                    (it > 0 || kk > 0));
+          umma_ss_w(tDK,
+                    ds_a + dso + (C::DS_QMAJOR ? mnmajor_step(kk) : kmajor_step(BN, kk)),
+                    q_mn + qo + mnmajor_step(kk), idK, (it > 0 || kk > 0));
         if (p.with_dq) {
           if (it > 0 &&
               !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, p.timeout_ns))
@@ -471,9 +504,11 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             if (C::DQ_T)
-              umma_ss_w(tDQ, k_mn + mnmajor_step(kk), ds_mn + dso + mnmajor_step(kk), idQ, kk > 0);
+              umma_ss_w(tDQ, k_mn + mnmajor_step(kk),
+                        ds_b + dso + (C::DS_QMAJOR ? kmajor_step(BM, kk) : mnmajor_step(kk)),
+                        idQ, kk > 0);
             else
-              umma_ss_w(tDQ, ds_mn + dso + mnmajor_step(kk), k_mn + mnmajor_step(kk), idQ, kk > 0);
+              umma_ss_w(tDQ, ds_b + dso + mnmajor_step(kk), k_mn + mnmajor_step(kk), idQ, kk > 0);
           }
         }
         umma_commit_w(smem_u32(&bars.q_empty[st]));
@@ -484,9 +519,9 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
       umma_commit_w(smem_u32(&bars.mma_drain));
       mbar_wait_drain(smem_u32(&bars.mma_drain), 0, p.timeout_ns);
   }
-  } else if (warp < 8) {
+  } else if (warp < 4 * C::NCWG) {
     // ------------------------------------------------------------------ P^T / dS^T compute
-    // Two warpgroups; warpgroup g owns score columns [g*HALF, (g+1)*HALF) of every key row.
+    // NCWG warpgroups; warpgroup g owns score columns [g*HALF, (g+1)*HALF) of every key row.
     const int g = warp >> 2;
     const int j = (warp & 3) * 32 + lane;  // key row in tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -668,11 +703,20 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
           }
         }
         ATTN_TMEM_ST_X16(tmem + C::COL_P + lane_off + c0 / 2, pp);
+        if constexpr (C::DS_QMAJOR) {
+          // [query][key]: one 16-bit element per query row; the warp's 32 keys of one row
+          // are 64 contiguous bytes (one wavefront)
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          const uint32_t off = sw128_offset(j, c0 + c8 * 8, BN);
-          *reinterpret_cast<uint4*>(gDS + off) =
-              make_uint4(pd[c8 * 4 + 0], pd[c8 * 4 + 1], pd[c8 * 4 + 2], pd[c8 * 4 + 3]);
+          for (int e = 0; e < 32; ++e)
+            *reinterpret_cast<uint16_t*>(gDS + sw128_offset(c0 + e, j, BM)) =
+                (uint16_t)(pd[e >> 1] >> ((e & 1) * 16));
+        } else {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            const uint32_t off = sw128_offset(j, c0 + c8 * 8, BN);
+            *reinterpret_cast<uint4*>(gDS + off) =
+                make_uint4(pd[c8 * 4 + 0], pd[c8 * 4 + 1], pd[c8 * 4 + 2], pd[c8 * 4 + 3]);
+          }
         }
       }
       tmem_st_wait();
@@ -689,19 +733,21 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
     }
     if (!C::DQ_WARPS && p.with_dq && ok && n_steps > 0) ok = drain_dq(n_steps - 1);
     if (!C::DQ_WARPS && lane == 0) bulk_wait_group0();  // this warp's reduces are complete
-    // ---- epilogue: dK = sm_scale * acc, dV = acc; warpgroup g writes columns [g*D/2, +D/2)
+    // ---- epilogue: dK = sm_scale * acc, dV = acc; the CTA holds columns [dh DH, +DH) of
+    // them, warpgroup g writes its share [g DH / NCWG, +DH / NCWG) of those
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, p.timeout_ns);
     tc_fence_after();
     if (ok) {
       const int64_t grow = sv.row0_k + key;
-      uint16_t* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss;
-      uint16_t* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss;
+      uint16_t* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss + dh * DH;
+      uint16_t* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss + dh * DH;
       const float sc = p.sm_scale;
+      constexpr int CW = DH / C::NCWG;
 #pragma unroll
-      for (int c = g * (D / 2); c < (g + 1) * (D / 2); c += 32) {
+      for (int c = g * CW; c < (g + 1) * CW; c += 32) {
         uint32_t a[32], b[32];
         ATTN_TMEM_LD2_X32(tmem + C::COL_DK + lane_off + c, tmem + C::COL_DV + lane_off + c, a, b);
-        if (key_ok && c < p.d_out) {  // columns past the head size are zero padding
+        if (key_ok && dh * DH + c < p.d_out) {  // columns past the head size are zero padding
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 vk, vv;
@@ -719,15 +765,15 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
         }
       }
     }
-  } else if (C::DQ_WARPS && warp >= C::WARP_DRAIN0) {
-    // ------------------------------------------------------------------ dQ drain (d_head 128)
+  } else if (C::DQ_WARPS && warp >= C::WARP_DRAIN0 && warp < C::WARP_DRAIN0 + 4) {
+    // ------------------------------------------------------------------ dQ drain (d_head >= 128)
     // Each drain warp owns the 32 TMEM lanes its warp index reaches (quarter qw) of the dQ^T
-    // partial (lanes are d, the 64 columns the step's query rows). It loads them right after
-    // the products complete and releases the TMEM columns, stages two 32 x 32 fp32 blocks in
-    // its own shared-memory area (128-byte swizzle) and adds each to the fp32 accumulator
-    // with one TMA reduce-add. Query rows past the sequence hold exact zeros (their dS was
-    // masked), so whole blocks can be added; blocks wholly in the zero padding past the head
-    // size add nothing and are skipped.
+    // partial (lanes are d of the CTA's half, the BM columns the step's query rows). It loads
+    // them right after the products complete and releases the TMEM columns, stages BM / 32
+    // blocks of 32 x 32 fp32 in its own shared-memory area (128-byte swizzle) and adds each to
+    // the fp32 accumulator with one TMA reduce-add. Query rows past the sequence hold exact
+    // zeros (their dS was masked), so whole blocks can be added; blocks wholly in the zero
+    // padding past the head size add nothing and are skipped.
     const int qw = warp & 3;
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
     bool ok = p.with_dq != 0;
@@ -738,16 +784,16 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
       }
       tc_fence_after();
       const int q_lo = q_tile(it) * BM;
-      uint8_t* stage = smem + C::OFF_STG + qw * 8192;
+      uint8_t* stage = smem + C::OFF_STG + qw * (C::DQ_BLOCKS * 4096);
       // this warp's previous reduce-adds must have read the area before it is rewritten
       if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
       // one 32-column block at a time (32 registers of data live)
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < C::DQ_BLOCKS; ++b) {
         float v[32];
         ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + 32 * b, reinterpret_cast<uint32_t*>(v));
-        if (b == 1) {  // the dQ columns are free for the next step's product
+        if (b == C::DQ_BLOCKS - 1) {  // the dQ columns are free for the next step's product
           tc_fence_before();
           mbar_arrive(smem_u32(&bars.dq_empty));
         }
@@ -759,11 +805,12 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      // blocks: column d = 32 qw, query rows 32 b within the step
-      if (lane == 0 && qw * 32 < p.d_out) {
+      // blocks: column d = dh DH + 32 qw, query rows 32 b within the step
+      const int c0 = dh * DH + qw * 32;
+      if (lane == 0 && c0 < p.d_out) {
 #pragma unroll
-        for (int b = 0; b < 2; ++b)
-          tma_reduce_add_2d(&p.tm_dq, smem_u32(stage + b * 4096), qw * 32,
+        for (int b = 0; b < C::DQ_BLOCKS; ++b)
+          tma_reduce_add_2d(&p.tm_dq, smem_u32(stage + b * 4096), c0,
                             (int)(zh * p.rows_q + sv.row0_q + q_lo + b * 32));
         bulk_commit_group();
       }
@@ -806,6 +853,9 @@ cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, bool bias, dim3
     return f16 ? launch_bwd_main_impl<64, true, true>(p, grid, stream)
                : launch_bwd_main_impl<64, false, true>(p, grid, stream);
   }
+  if (D == 256)
+    return f16 ? launch_bwd_main_impl<256, true, false>(p, grid, stream)
+               : launch_bwd_main_impl<256, false, false>(p, grid, stream);
   if (D == 128)
     return f16 ? launch_bwd_main_impl<128, true, false>(p, grid, stream)
                : launch_bwd_main_impl<128, false, false>(p, grid, stream);
@@ -813,7 +863,10 @@ cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, bool bias, dim3
              : launch_bwd_main_impl<64, false, false>(p, grid, stream);
 }
 
-int bwd_block_m(int D) { return D == 128 ? BwdCfg<128>::BM : BwdCfg<64>::BM; }
+int bwd_block_m(int D) {
+  return D == 256 ? BwdCfg<256>::BM : D == 128 ? BwdCfg<128>::BM : BwdCfg<64>::BM;
+}
+int bwd_ctas_per_key_tile(int D) { return D == 256 ? 2 : 1; }
 int bwd_block_n() { return 128; }
 
 }  // namespace attn_sm103

@@ -23,8 +23,9 @@
  * queries and keys as a missing case; the AOTriton issue #12 page states that QKVO share a
  * dtype and shape except for seqlen_q vs seqlen_k). d_head must be 32, 64, 96 or 128 (32
  * and 96 run on the 64- and 128-wide kernels with zero-filled columns; only the real
- * columns of the outputs are written), or 256 for the forward calls without a bias (one
- * 128-row query tile per CTA); every backward call returns ATTN_ERR_UNSUPPORTED for 256.
+ * columns of the outputs are written), or 256 in the calls without a bias (the forward with
+ * one 128-row query tile per CTA; the backward with two CTAs per key tile, one per half of d);
+ * the deterministic backward returns ATTN_ERR_UNSUPPORTED for 256.
  *
  * Masking. causal != 0 applies a top-left aligned mask: query i sees key j iff j <= i,
  * indices local to the sequence. Keys at or past a sequence's length are never seen.
@@ -102,8 +103,8 @@ typedef enum {
   ATTN_ERR_SHAPE = 2,         /* inconsistent sizes (B, H, D, S), or compact batch != 1 */
   ATTN_ERR_STRIDE = 3,        /* D stride != 1, or a stride not a multiple of 8 elements */
   ATTN_ERR_ALIGN = 4,         /* base pointer not 16-byte aligned */
-  ATTN_ERR_UNSUPPORTED = 5,   /* d_head not 32/64/96/128 (256: forward only), device not
-                                 sm_103, or size limits */
+  ATTN_ERR_UNSUPPORTED = 5,   /* d_head not 32/64/96/128/256 (256: no bias and no
+                                 deterministic backward), device not sm_103, or size limits */
   ATTN_ERR_WORKSPACE = 6,     /* workspace NULL or smaller than the *_workspace_size value */
   ATTN_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed (launch, tensor map) */
   ATTN_ERR_DEVICE_BAD_SEQLENS = 8, /* device: cu_seqlens not monotone or past the tensor */

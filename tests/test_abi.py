@@ -158,10 +158,10 @@ def test_bwd_workspace_checked(lib):
     assert st == ERR_WORKSPACE
 
 
-def test_d_head_256_forward_only(lib):
+def test_d_head_256_checks(lib):
     """d_head 256 passes the forward's argument checks (a bad LSE shape is the first error,
-    not the head size) and is refused by every backward call before anything else (no
-    workspace would otherwise be the error)."""
+    not the head size); the backward takes it (a missing workspace is the first error); the
+    deterministic backward refuses it before anything else."""
     r = ctypes.byref
     shape = (1, 2, 128, 256)
     q = t4(shape)
@@ -169,15 +169,10 @@ def test_d_head_256_forward_only(lib):
     lse = t3(shape[:3])
     st = lib.attn_bwd(r(q), r(q), r(q), r(q), r(lse), r(q), None, None, 0.125, 0, r(q), r(q),
                       r(q), None, 0, None)
-    assert st == ERR_UNSUPPORTED
+    assert st == ERR_WORKSPACE
     st = lib.attn_bwd_deterministic(r(q), r(q), r(q), r(q), r(lse), r(q), None, None, 0.125,
                                     0, r(q), r(q), r(q), None, 0, None)
     assert st == ERR_UNSUPPORTED
-    # the same call at d_head 128 gets as far as the workspace check
-    q = t4((1, 2, 128, 128))
-    st = lib.attn_bwd(r(q), r(q), r(q), r(q), r(lse), r(q), None, None, 0.125, 0, r(q), r(q),
-                      r(q), None, 0, None)
-    assert st == ERR_WORKSPACE
 
 
 def test_padded_alias_requires_cu(lib):

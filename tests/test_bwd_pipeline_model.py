@@ -31,24 +31,24 @@ from _pipeline_sim import Sim
 
 
 def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
-                      stage_in_ds=True):
+                      stage_in_ds=True, n_wg=2):
     """The kernel's roles; `skip` names waits to leave out (to check that the model sees
     what they prevent; "read_wait" is the wait of a draining warp for its previous
     reduce-add to read its staging); withhold: a step whose Q / dO the producer skips (the
     kernel's failure-detection hook); stage_in_ds: the d_head 64 layout (the compute
     warpgroups drain dQ into the dS buffer they released), else the d_head 128 one (drain
-    warps with staging areas of their own)."""
+    warps with staging areas of their own); n_wg: compute warpgroups (1 at d_head 256)."""
     drains = ("wg0", "wg1") if stage_in_ds else ("dr0", "dr1")
     sim.barrier("kv_full", 1)
     for st in range(qst):
         sim.barrier(f"q_full{st}", 1)
         sim.barrier(f"q_empty{st}", 1)
     for b in range(2):
-        sim.barrier(f"ds_full{b}", 2)
-    for name, n in (("s_full", 1), ("s_free", 2), ("p_full", 2), ("p_empty", 1),
+        sim.barrier(f"ds_full{b}", n_wg)
+    for name, n in (("s_full", 1), ("s_free", n_wg), ("p_full", n_wg), ("p_empty", 1),
                     ("dq_full", 1), ("dq_empty", 2), ("dkdv_full", 1)):
         sim.barrier(name, n)
-    wg = ("wg0", "wg1")
+    wg = ("wg0", "wg1")[:n_wg]
     sim.buffer("KV", ())  # the key tile's K and V, loaded once
     for st in range(qst):  # Q / dO stage: the products of its step, and the LSE rows
         sim.buffer(f"QS{st}", ("SdP", "dV", "dK") + wg)
@@ -116,7 +116,7 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
             yield ("commit", "p_empty")
             if not (yield from wait(f"ds_full{bs}", it >> 1)):
                 break
-            ds = [(f"DS{bs}{h}", ("dS", it)) for h in range(2)]
+            ds = [(f"DS{bs}{h}", ("dS", it)) for h in range(n_wg)]
             yield ("mma", "dK", ds + [(f"QS{st}", it)], [])
             if with_dq:
                 if it > 0 and not (yield from wait("dq_empty", it - 1)):
@@ -192,7 +192,7 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
                 break
         yield ("wait_read", f"STG{h}", f"tma{h}")  # its reduce-adds complete before exit
 
-    agents = [producer(), mma(), warpgroup_role("wg0"), warpgroup_role("wg1")]
+    agents = [producer(), mma()] + [warpgroup_role(w) for w in wg]
     if not stage_in_ds:
         agents += [drain("dr0"), drain("dr1")]
     return agents
@@ -201,13 +201,13 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
 @pytest.mark.parametrize("n_steps", [1, 2, 3, 4, 7])
 @pytest.mark.parametrize("qst", [2, 3])
 @pytest.mark.parametrize("with_dq", [True, False])
-@pytest.mark.parametrize("stage_in_ds", [True, False])  # d_head 64, 128
-def test_backward_pipeline_is_exact_and_race_free(n_steps, qst, with_dq, stage_in_ds):
-    rng = random.Random(n_steps * 10 + qst + 100 * with_dq + 1000 * stage_in_ds)
+@pytest.mark.parametrize("stage_in_ds,n_wg", [(True, 2), (False, 2), (False, 1)])  # d_head 64, 128, 256
+def test_backward_pipeline_is_exact_and_race_free(n_steps, qst, with_dq, stage_in_ds, n_wg):
+    rng = random.Random(n_steps * 10 + qst + 100 * with_dq + 1000 * stage_in_ds + 7 * n_wg)
     for _ in range(120):
         sim = Sim(rng, exit_check=True)
         assert sim.run(backward_protocol(sim, n_steps, qst, with_dq, rng,
-                                         stage_in_ds=stage_in_ds)) == []
+                                         stage_in_ds=stage_in_ds, n_wg=n_wg)) == []
 
 
 @pytest.mark.parametrize("dropped,kind", [
