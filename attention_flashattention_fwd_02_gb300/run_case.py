@@ -38,6 +38,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--iters", type=int, default=10)
     ap.add_argument("--workload", choices=("padded", "compact"), default=None)
+    ap.add_argument("--bias", choices=("none", "full", "heads"), default="none",
+                    help="additive bias (B, H, Sq, Sk), or one shared by the heads (B, 1, Sq, "
+                         "Sk), whose gradient is then asked for too")
     a = ap.parse_args(argv)
     if a.workload:
         return run_varlen(a)
@@ -50,22 +53,28 @@ def main(argv=None):
     k, v = (torch.randn(a.B, a.H, Sk, a.D, device=dev, generator=g).to(dt) for _ in range(2))
     do = torch.randn(a.B, a.H, Sq, a.D, device=dev, generator=g).to(dt)
     c = 1.0 / math.sqrt(a.D)
+    bias = dbias = None
+    if a.bias != "none":
+        pad = (Sk + 7) // 8 * 8  # rows padded to a multiple of 8 keys (the stride rule)
+        hb = a.H if a.bias == "full" else 1
+        bias = torch.randn(a.B, hb, Sq, pad, device=dev, generator=g).to(dt)[..., :Sk]
+        dbias = torch.zeros(a.B, hb, Sq, pad, device=dev, dtype=dt)[..., :Sk]
     ws_f = torch.zeros(_lib.attn_fwd_workspace_size(a.B, a.H, Sq, a.D), dtype=torch.uint8,
                        device=dev)
-    o, lse = forward(q, k, v, c, a.causal, workspace=ws_f)
-    ws_b = None if a.fwd_only else bwd_workspace(q)
+    o, lse = forward(q, k, v, c, a.causal, workspace=ws_f, bias=bias)
+    ws_b = None if a.fwd_only else bwd_workspace(q, bias)
     grads = [torch.empty_like(t) for t in (q, k, v)]
 
     def run_fwd():
-        forward(q, k, v, c, a.causal, out=o, lse=lse, workspace=ws_f)
+        forward(q, k, v, c, a.causal, out=o, lse=lse, workspace=ws_f, bias=bias)
 
     def run_bwd():
         backward(q, k, v, o, lse, do, c, a.causal, dq=grads[0], dk=grads[1], dv=grads[2],
-                 workspace=ws_b, deterministic=a.deterministic)
+                 workspace=ws_b, deterministic=a.deterministic, bias=bias, dbias=dbias)
 
     pairs = a.B * a.H * unmasked_pairs(Sq, Sk, a.causal)
     out = {"B": a.B, "H": a.H, "Sq": Sq, "Sk": Sk, "D": a.D, "causal": a.causal,
-           "dtype": "fp16" if a.fp16 else "bf16"}
+           "dtype": "fp16" if a.fp16 else "bf16", "bias": a.bias}
     _time_and_report(a, run_fwd, None if a.fwd_only else run_bwd, a.D, pairs, out,
                      (ws_f, ws_b))
 
