@@ -380,8 +380,36 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
     int last_it[QST];  // last step loaded into each stage (-1: none)
 #pragma unroll
     for (int st = 0; st < QST; ++st) last_it[st] = -1;
+    // LSE log2(e) and Delta of a step's query rows (this lane's rows lane + 32 i; 0 off the
+    // sequence), loaded one step ahead: the loads of step it + 1 are issued before the wait
+    // for the stage they will fill, so their latency hides behind that wait instead of
+    // delaying every step's q_full
+    constexpr int NL = (BM + 31) / 32;
+    float nl2[NL], ndl[NL];
+    auto fetch_rows = [&](int itf, float* l2o, float* dlo) {
+      const int q_lo_f = q_tile(itf) * BM;
+#pragma unroll
+      for (int u = 0; u < NL; ++u) {
+        const int q = q_lo_f + lane + 32 * u;
+        l2o[u] = 0.f;
+        dlo[u] = 0.f;
+        if (lane + 32 * u < BM && q < sv.len_q) {
+          const int64_t grow = sv.row0_q + q;
+          l2o[u] = p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] * kLog2e;
+          dlo[u] = p.delta[zh * p.rows_q + grow];
+        }
+      }
+    };
+    if (n_steps > 0) fetch_rows(0, nl2, ndl);
     for (int it = 0; it < n_steps; ++it) {
       const int st = it % QST;
+      float cl2[NL], cdl[NL];  // this step's rows
+#pragma unroll
+      for (int u = 0; u < NL; ++u) {
+        cl2[u] = nl2[u];
+        cdl[u] = ndl[u];
+      }
+      if (it + 1 < n_steps) fetch_rows(it + 1, nl2, ndl);
       if (it == p.withhold_step) continue;  // failure-detection test: this stage never fills
       if (it >= QST &&
           !mbar_wait(smem_u32(&bars.q_empty[st]), ((it / QST) - 1) & 1, abort, p.timeout_ns))
@@ -399,14 +427,11 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
                       h, sv.batch);
         }
       }
-      for (int i = lane; i < BM; i += 32) {
-        const int q = q_lo + i;
-        float l2 = 0.f, dl = 0.f;
-        if (q < sv.len_q) {
-          const int64_t grow = sv.row0_q + q;
-          l2 = p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] * kLog2e;
-          dl = p.delta[zh * p.rows_q + grow];
-        }
+#pragma unroll
+      for (int u = 0; u < NL; ++u) {
+        const int i = lane + 32 * u;
+        if (i >= BM) break;
+        const float l2 = cl2[u], dl = cdl[u];
         if constexpr (C::AUG) {
           // c2 (S + a) = c2 S - LSE log2(e) with a = -LSE / sm_scale
           aug_split(1 + st, i, -l2 / p.scale_log2);
