@@ -240,12 +240,25 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(sK + st * C::KV_BYTES + s * BN * 128, &p.tm_k, kb, s * 64, krow, h, sv.batch);
+        // the tile that will next fill this stage: into L2 now, so that its load is not a
+        // DRAM round trip when the stage frees up
+        const bool pf = j + NST < n_max && j + NST != p.withhold_tile;
+        if (pf) {
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s)
+            tma_prefetch_l2_4d(&p.tm_k, s * 64, krow + NST * BN, h, sv.batch);
+        }
         if (C::SPLIT_KV) continue;  // V has its own producer warp
         const uint32_t vb = smem_u32(&bars.v_full[st]);
         mbar_arrive_expect_tx(vb, C::KV_BYTES);
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(sV + st * C::KV_BYTES + s * BN * 128, &p.tm_v, vb, s * 64, krow, h, sv.batch);
+        if (pf) {
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s)
+            tma_prefetch_l2_4d(&p.tm_v, s * 64, krow + NST * BN, h, sv.batch);
+        }
       }
       if (*abort) {  // the consumers gave up: let this lane's copies land before exiting
         mbar_wait_drain(qb, 0, p.timeout_ns);
@@ -277,6 +290,11 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(sV + st * C::KV_BYTES + s * BN * 128, &p.tm_v, vb, s * 64,
                       sv.row0_k + j * BN, h, sv.batch);
+        if (j + NST < n_max && j + NST != p.withhold_tile) {
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s)
+            tma_prefetch_l2_4d(&p.tm_v, s * 64, sv.row0_k + (j + NST) * BN, h, sv.batch);
+        }
       }
       if (*abort)
 #pragma unroll
