@@ -426,15 +426,6 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
           tma_load_4d(sDO + st * C::Q_BYTES + s * BM * 128, &p.tm_do, qb, s * 64, sv.row0_q + q_lo,
                       h, sv.batch);
         }
-        // the step that will next fill this stage: into L2 now
-        if (it + QST < n_steps) {
-          const int q_pf = sv.row0_q + q_tile(it + QST) * BM;
-#pragma unroll
-          for (int s = 0; s < D / 64; ++s) {
-            tma_prefetch_l2_4d(&p.tm_q, s * 64, q_pf, h, sv.batch);
-            tma_prefetch_l2_4d(&p.tm_do, s * 64, q_pf, h, sv.batch);
-          }
-        }
       }
 #pragma unroll
       for (int u = 0; u < NL; ++u) {
