@@ -222,29 +222,34 @@ attn_status make_map_acc(CUtensorMap* m, float* acc, int64_t rows, int64_t D) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Causal tiles differ in work. With the tile index as the slowest grid dimension the CTAs
-// are dispatched heaviest first across all (unit, head) pairs, which removes the tail that
-// a per-head heaviest-first order leaves (the last head's heaviest tile starts near the
-// end). It also spreads the CTAs of one head over the whole launch, so the operands they
-// share must stay in L2 (129 MB) between them: the order is used when those bytes are at
-// most the kernel's limit in the measured table of attn_tune_table.h and the tile count
-// fits grid z.
+// Causal tiles differ in work. Dispatched heaviest first across many (unit, head) pairs, they
+// leave no tail (a per-head heaviest-first order starts the last head's heaviest tile near
+// the end); but the CTAs of one head then spread over a longer stretch of the launch, and the
+// operands they share must stay in L2 (129 MB) between them. So the pairs are grouped: as
+// many per group as keep those operands within the kernel's measured limit in
+// attn_tune_table.h, heaviest first inside a group, one group after another (grid_group).
 // Head sizes 32 and 96 run on the kernels built for 64 and 128: the TMA loads (box 64
 // columns wide) fill the columns past the head size with zeros, which add nothing to any
 // product, and only the real columns are stored.
 int kernel_width(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : 256; }
 
-// Tuning hook: ATTN_GRID_ORDER = "<kernel>:tile" or "<kernel>:seq" (comma-separated
-// entries) forces the order of that kernel's causal grids; the sweep that writes the table
-// times both orders this way.
-int grid_order_override(const char* kernel) {
+// Tuning hook: ATTN_GRID_ORDER = "<kernel>:tile", "<kernel>:seq" or "<kernel>:g<N>"
+// (comma-separated entries) forces the order of that kernel's causal grids: longest-first
+// over the whole grid, each head's blocks together, or groups of N (unit, head) pairs; the
+// sweep that writes the table times these orders this way. Returns the forced group size, or
+// -1 (uh: the number of (unit, head) pairs).
+int grid_order_override(const char* kernel, int uh) {
   const char* v = getenv("ATTN_GRID_ORDER");
   if (v == nullptr) return -1;
   const size_t n = strlen(kernel);
   for (const char* e = v; *e;) {
     if (strncmp(e, kernel, n) == 0 && e[n] == ':') {
-      if (strncmp(e + n + 1, "tile", 4) == 0) return 1;
-      if (strncmp(e + n + 1, "seq", 3) == 0) return 0;
+      if (strncmp(e + n + 1, "tile", 4) == 0) return uh;
+      if (strncmp(e + n + 1, "seq", 3) == 0) return 1;
+      if (e[n + 1] == 'g') {
+        const int g = atoi(e + n + 2);
+        if (g >= 1) return g;
+      }
     }
     const char* c = strchr(e, ',');
     if (c == nullptr) break;
@@ -259,13 +264,18 @@ double tile_major_limit(const char* kernel, int width) {
   return 0.0;
 }
 
-// kernel: "fwd", "bwd_main", "bwd_main_nodq" or "bwd_dq"; width: 64 or 128.
-bool tile_major_order(const char* kernel, int width, int causal, double shared_bytes,
-                      int tiles) {
-  if (!causal || tiles > 65535) return false;
-  const int forced = grid_order_override(kernel);
-  if (forced >= 0) return forced == 1;
-  return shared_bytes <= tile_major_limit(kernel, width);
+// Group size of the CTA order (grid_pos in attn_common.cuh) for `uh` (unit, head) pairs whose
+// blocks share `shared_bytes` over all pairs. kernel: "fwd", "bwd_main", "bwd_main_nodq" or
+// "bwd_dq"; width: 64, 128 or 256. Causal grids: as many pairs per group as keep the operands
+// they share within the kernel's measured L2 limit (at least one); non-causal grids, whose
+// blocks are equally heavy, keep each pair's blocks together.
+int grid_group(const char* kernel, int width, int causal, double shared_bytes, int uh) {
+  if (!causal || uh <= 1) return 1;
+  const int forced = grid_order_override(kernel, uh);
+  if (forced >= 1) return forced < uh ? forced : uh;
+  const double per_pair = shared_bytes / uh;
+  const double g = per_pair > 0 ? tile_major_limit(kernel, width) / per_pair : uh;
+  return g >= uh ? uh : (g < 1 ? 1 : (int)g);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -349,9 +359,13 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   p.withhold_tile = withheld_tile_for_test();
   p.timeout_ns = p.withhold_tile >= 0 ? 50000000ull : kWaitTimeoutNs;
   const int n_blk = (pr.max_q + BM - 1) / BM;
-  p.tile_major = tile_major_order("fwd", kernel_width(pr.D), p.causal,
-                                  (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
-  const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_blk) : dim3(n_blk, pr.H, pr.units);
+  const int uh = pr.units * pr.H;
+  p.tiles = n_blk;
+  p.H = pr.H;
+  p.group = grid_group("fwd", kernel_width(pr.D), p.causal,
+                       (double)pr.units * pr.H * pr.max_k * pr.D * 4, uh);
+  if ((int64_t)n_blk * uh > kMaxI32) return ATTN_ERR_UNSUPPORTED;  // 1-D grid
+  const dim3 grid((unsigned)(n_blk * uh));
   p.d_out = pr.D;
   cudaError_t e = launch_attn_fwd(p, kernel_width(pr.D), pr.f16, bias != nullptr, grid,
                                   reinterpret_cast<cudaStream_t>(stream));
@@ -443,12 +457,15 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       const int n_tiles = (pr.max_k + BN - 1) / BN * bwd_ctas_per_key_tile(kernel_width(pr.D));
       // the operands every CTA of a head visits: Q, dO (16-bit) and, when this kernel
       // accumulates dQ, the fp32 accumulator
-      p.tile_major = p.with_dq
-          ? tile_major_order("bwd_main", kernel_width(pr.D), p.causal,
-                             (double)pr.units * pr.H * pr.max_q * pr.D * 8, n_tiles)
-          : tile_major_order("bwd_main_nodq", kernel_width(pr.D), p.causal,
-                             (double)pr.units * pr.H * pr.max_q * pr.D * 4, n_tiles);
-      const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_tiles) : dim3(n_tiles, pr.H, pr.units);
+      const int uh = pr.units * pr.H;
+      p.tiles = n_tiles;
+      p.group = p.with_dq
+          ? grid_group("bwd_main", kernel_width(pr.D), p.causal,
+                       (double)pr.units * pr.H * pr.max_q * pr.D * 8, uh)
+          : grid_group("bwd_main_nodq", kernel_width(pr.D), p.causal,
+                       (double)pr.units * pr.H * pr.max_q * pr.D * 4, uh);
+      if ((int64_t)n_tiles * uh > kMaxI32) return ATTN_ERR_UNSUPPORTED;  // 1-D grid
+      const dim3 grid((unsigned)(n_tiles * uh));
       p.d_out = pr.D;
       if (a.bias != nullptr) {
         // size-1 batch / head dimensions broadcast: stride 0
@@ -528,9 +545,12 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
     p.d_out = pr.D;
     const int n_blk = (pr.max_q + BMq - 1) / BMq;
     // the operands every CTA of a head visits: K and V
-    p.tile_major = tile_major_order("bwd_dq", kernel_width(pr.D), p.causal,
-                                    (double)pr.units * pr.H * pr.max_k * pr.D * 4, n_blk);
-    const dim3 grid = p.tile_major ? dim3(pr.units, pr.H, n_blk) : dim3(n_blk, pr.H, pr.units);
+    const int uh = pr.units * pr.H;
+    p.tiles = n_blk;
+    p.group = grid_group("bwd_dq", kernel_width(pr.D), p.causal,
+                         (double)pr.units * pr.H * pr.max_k * pr.D * 4, uh);
+    if ((int64_t)n_blk * uh > kMaxI32) return ATTN_ERR_UNSUPPORTED;  // 1-D grid
+    const dim3 grid((unsigned)(n_blk * uh));
     if (launch_bwd_dq(p, kernel_width(pr.D), pr.f16, grid, st) != cudaSuccess) return ATTN_ERR_CUDA;
   }
   return ATTN_OK;

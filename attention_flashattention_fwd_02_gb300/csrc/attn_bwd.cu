@@ -271,13 +271,14 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
   __shared__ BwdBars<BM, QST, C::LSE_ST> bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // grid (key tiles, H, units), or (units, H, key tiles) for a longest-first causal order;
-  // at d_head 256 each key tile has two CTAs, one per half of d (index 2 tile + half)
-  const int h = blockIdx.y;
-  const int kt = p.tile_major ? (int)blockIdx.z : (int)blockIdx.x;
+  // 1-D grid over (unit, head) pairs x key tiles (grid_pos; key tile 0, the heaviest of a
+  // causal grid, first); at d_head 256 each key tile has two CTAs, one per half of d
+  // (index 2 tile + half)
+  const GridPos gp = grid_pos((int)blockIdx.x, p.tiles, (int)(gridDim.x / p.tiles), p.group);
+  const int h = gp.zh % p.H, z = gp.zh / p.H;
+  const int kt = gp.rank;
   const int n_tile = C::DSPLIT ? kt >> 1 : kt;
   const int dh = C::DSPLIT ? kt & 1 : 0;  // the half of d this CTA accumulates
-  const int z = p.tile_major ? (int)blockIdx.x : (int)blockIdx.z;
 
   SeqView sv;
   if (!decode_seq(p.seq, z, threadIdx.x == 0 ? p.status : nullptr, sv)) return;

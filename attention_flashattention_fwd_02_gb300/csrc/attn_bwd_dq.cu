@@ -61,12 +61,11 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
   __shared__ DqBars<NST, NDS> bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // grid (query blocks, H, units), or (units, H, query blocks) for a longest-first order
-  const int h = blockIdx.y;
-  const int z = p.tile_major ? (int)blockIdx.x : (int)blockIdx.z;
-  const int blk = p.tile_major ? (int)blockIdx.z : (int)blockIdx.x;
-  const int n_blk = p.tile_major ? (int)gridDim.z : (int)gridDim.x;
-  const int m_blk = p.causal ? n_blk - 1 - blk : blk;  // causal: heaviest block first
+  // 1-D grid over (unit, head) pairs x query blocks (grid_pos)
+  const GridPos gp = grid_pos((int)blockIdx.x, p.tiles, (int)(gridDim.x / p.tiles), p.group);
+  const int h = gp.zh % p.H, z = gp.zh / p.H;
+  const int n_blk = p.tiles;
+  const int m_blk = p.causal ? n_blk - 1 - gp.rank : gp.rank;  // causal: heaviest block first
 
   SeqView sv;
   if (!decode_seq(p.seq, z, threadIdx.x == 0 ? p.status : nullptr, sv)) return;

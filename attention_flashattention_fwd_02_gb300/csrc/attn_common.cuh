@@ -57,6 +57,23 @@ __device__ __forceinline__ bool decode_seq(const SeqAddr& a, int z, int* status,
   return ok;
 }
 
+// CTA order of a launch over `tiles` tiles of each of `uh` (unit, head) pairs, 1-D grid in
+// launch order: groups of `group` pairs run one after another, and inside a group the tiles go
+// by rank (rank 0, the heaviest of a causal grid, first) across the group's pairs. A group
+// holds as many pairs as the operands their blocks share keep in L2 (the measured limits of
+// attn_tune_table.h); group >= uh is longest-first over the whole grid, group == 1 keeps each
+// pair's tiles together. Returns the pair index and the tile rank of block `linear`.
+struct GridPos {
+  int zh, rank;
+};
+__device__ __forceinline__ GridPos grid_pos(int linear, int tiles, int uh, int group) {
+  const int per = group * tiles;  // blocks of a full group
+  const int g = linear / per;
+  const int r = linear - g * per;
+  const int gs = min(group, uh - g * group);  // pairs in this group (the last may be short)
+  return GridPos{g * group + r % gs, r / gs};
+}
+
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;   // 4-D (D, S, H, B) 16-bit, box (64, 128, 1, 1), SW128
   CUtensorMap tm_b;               // bias kernels only: 4-D (Sk, Sq, Hb, Bb), box (64, 128, 1, 1)
@@ -71,7 +88,8 @@ struct FwdParams {
   int* status;                    // device status word, may be null
   uint64_t timeout_ns;            // bound on every pipeline wait
   int withhold_tile;              // test hook: key tile the producer never loads (-1: none)
-  int tile_major;                 // grid (units, H, tiles) instead of (tiles, H, units)
+  int tiles, group;               // query blocks per (unit, head) pair; CTA-order group size
+  int H;                          // heads
   int d_out;                      // head size of the tensors (<= the kernel's D; the TMA
                                   // loads fill the columns past it with zeros)
 };
@@ -114,7 +132,7 @@ struct BwdParams {
   uint64_t timeout_ns;            // bound on every pipeline wait
   int withhold_step;              // test hook: step whose Q / dO the producer never loads (-1)
   int with_dq;                    // 0: no dQ products (the deterministic dQ kernel makes dQ)
-  int tile_major;                 // grid (units, H, key tiles) instead of (key tiles, H, units)
+  int tiles, group;               // key-tile CTAs per (unit, head) pair; CTA-order group size
   float scale_log2;               // sm_scale * log2(e)
   float sm_scale;
   int* status;
@@ -155,7 +173,7 @@ struct BwdDqParams {
   float scale_log2;               // sm_scale * log2(e)
   float sm_scale;
   int* status;
-  int tile_major;                 // grid (units, H, query blocks) instead of (blocks, H, units)
+  int tiles, group;               // query blocks per (unit, head) pair; CTA-order group size
   int d_out;                      // head size of the tensors (<= the kernel's D)
 };
 

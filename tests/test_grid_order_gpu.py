@@ -1,5 +1,6 @@
-"""Both CTA orders of the causal grids give the same results (the order only changes which
-CTA runs when): forward O and LSE, dK and dV, and the deterministic dQ bit for bit; the
+"""Every CTA order of the causal grids gives the same results (the order only changes which
+CTA runs when): per-head, longest-first over the whole grid, and groups of (unit, head)
+pairs; forward O and LSE, dK and dV, and the deterministic dQ bit for bit; the
 reduction-order-dependent dQ of attn_bwd within the oracle tolerance. Forced through the
 library's ATTN_GRID_ORDER tuning hook."""
 import os
@@ -48,15 +49,16 @@ def test_orders_agree(D, padded):
     q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
     cu = x["cu_seqlens_q"].to(DEV) if padded else None
     a = _run("seq", q, k, v, do, wl.sm_scale, cu)
-    b = _run("tile", q, k, v, do, wl.sm_scale, cu)
-    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
-    for i in (1, 2):
-        assert torch.equal(a["reg"][i], b["reg"][i])
-    for i in range(3):
-        assert torch.equal(a["det"][i], b["det"][i])
+    others = [_run(order, q, k, v, do, wl.sm_scale, cu) for order in ("tile", "g2", "g4")]
+    for b in others:  # groups of 2 and 4 of the 6 (unit, head) pairs: a short last group too
+        assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
+        for i in (1, 2):
+            assert torch.equal(a["reg"][i], b["reg"][i])
+        for i in range(3):
+            assert torch.equal(a["det"][i], b["det"][i])
     cun = x["cu_seqlens_q"].numpy() if padded else None
     g_r = ref.bwd_bhsd(*(np64(x[n]) for n in ("q", "k", "v", "do")), wl.sm_scale, True, cun, cun)
-    for g in (a["reg"], b["reg"]):
+    for g in [a["reg"]] + [b["reg"] for b in others]:
         assert_grads_close(tuple(g), g_r, what=f"grid order D={D}")
 
 
@@ -66,14 +68,15 @@ def test_orders_agree_compact():
     q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
     cu = x["cu_seqlens_q"].to(DEV)
     a = _run("seq", q, k, v, do, wl.sm_scale, cu, compact=True)
-    b = _run("tile", q, k, v, do, wl.sm_scale, cu, compact=True)
-    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
-    for i in (1, 2):
-        assert torch.equal(a["reg"][i], b["reg"][i])
-    for i in range(3):
-        assert torch.equal(a["det"][i], b["det"][i])
+    others = [_run(order, q, k, v, do, wl.sm_scale, cu, compact=True) for order in ("tile", "g3")]
+    for b in others:  # groups of 3 of the 8 (sequence, head) pairs: a short last group too
+        assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
+        for i in (1, 2):
+            assert torch.equal(a["reg"][i], b["reg"][i])
+        for i in range(3):
+            assert torch.equal(a["det"][i], b["det"][i])
     cun = x["cu_seqlens_q"].numpy()
     g_r = ref.bwd_compact_varlen(*(np64(x[n]) for n in ("q", "k", "v", "do")), cun, cun,
                                  wl.sm_scale, True)
-    for g in (a["reg"], b["reg"]):
+    for g in [a["reg"]] + [b["reg"] for b in others]:
         assert_grads_close(tuple(g), g_r, what="grid order compact")

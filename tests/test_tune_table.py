@@ -60,7 +60,7 @@ def test_header_covers_every_kernel_and_width():
     api = open(os.path.join(ROOT, "attention_flashattention_fwd_02_gb300", "csrc",
                             "attn_api.cu")).read()
     for k in tg.FOOTPRINT_BYTES:
-        assert f'tile_major_order("{k}"' in api
+        assert f'grid_group("{k}"' in api
 
 
 def test_header_matches_stored_sweep():
