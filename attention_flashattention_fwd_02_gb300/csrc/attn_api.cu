@@ -222,12 +222,13 @@ attn_status make_map_acc(CUtensorMap* m, float* acc, int64_t rows, int64_t D) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Causal tiles differ in work. Dispatched heaviest first across many (unit, head) pairs, they
+// Causal tiles differ in work. Dispatched heaviest first across all (unit, head) pairs, they
 // leave no tail (a per-head heaviest-first order starts the last head's heaviest tile near
-// the end); but the CTAs of one head then spread over a longer stretch of the launch, and the
-// operands they share must stay in L2 (129 MB) between them. So the pairs are grouped: as
-// many per group as keep those operands within the kernel's measured limit in
-// attn_tune_table.h, heaviest first inside a group, one group after another (grid_group).
+// the end); but the CTAs of one head then spread over the whole launch, and the operands they
+// share must stay in L2 (129 MB) between them. So the whole grid runs longest-first when those
+// operands fit the kernel's measured limit in attn_tune_table.h, else each pair's blocks run
+// together (grid_group). Groups in between were measured too and lost to the per-head order
+// in the backward (the per-head operands' L2 reuse outweighs the tail).
 // Head sizes 32 and 96 run on the kernels built for 64 and 128: the TMA loads (box 64
 // columns wide) fill the columns past the head size with zeros, which add nothing to any
 // product, and only the real columns are stored.
@@ -266,16 +267,14 @@ double tile_major_limit(const char* kernel, int width) {
 
 // Group size of the CTA order (grid_pos in attn_common.cuh) for `uh` (unit, head) pairs whose
 // blocks share `shared_bytes` over all pairs. kernel: "fwd", "bwd_main", "bwd_main_nodq" or
-// "bwd_dq"; width: 64, 128 or 256. Causal grids: as many pairs per group as keep the operands
-// they share within the kernel's measured L2 limit (at least one); non-causal grids, whose
-// blocks are equally heavy, keep each pair's blocks together.
+// "bwd_dq"; width: 64, 128 or 256. Causal grids: all pairs (longest-first over the whole grid)
+// when the shared operands fit the kernel's measured L2 limit, else one; non-causal grids,
+// whose blocks are equally heavy, keep each pair's blocks together.
 int grid_group(const char* kernel, int width, int causal, double shared_bytes, int uh) {
   if (!causal || uh <= 1) return 1;
   const int forced = grid_order_override(kernel, uh);
   if (forced >= 1) return forced < uh ? forced : uh;
-  const double per_pair = shared_bytes / uh;
-  const double g = per_pair > 0 ? tile_major_limit(kernel, width) / per_pair : uh;
-  return g >= uh ? uh : (g < 1 ? 1 : (int)g);
+  return shared_bytes <= tile_major_limit(kernel, width) ? uh : 1;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

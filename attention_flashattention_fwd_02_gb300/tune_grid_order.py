@@ -63,13 +63,11 @@ def choose_threshold(points):
 
 def header_text(sweep) -> str:
     lines = [
-        "// CTA order of the causal grids, per kernel and kernel width: (unit, head) pairs run in",
-        "// groups, heaviest blocks first inside a group, as many pairs per group as keep the bytes",
-        "// their blocks share within max_tile_major_bytes (all pairs: longest-first over the",
-        "// whole grid; one: each head's blocks together). Written by tune_grid_order.py from a",
-        "// timing sweep of the two extreme orders on causal dense inputs on a GB300",
-        "// (" + sweep.get("device", "?") + "), the largest footprint at which the whole grid ran",
-        "// best longest-first; regenerate, do not edit.",
+        "// CTA order of the causal grids, per kernel and kernel width: the longest-first",
+        "// (tile-major) order is used when the bytes that the blocks of one head share, summed",
+        "// over all heads, are at most max_tile_major_bytes; otherwise each head's blocks run",
+        "// together. Written by tune_grid_order.py from a timing sweep of both orders on causal",
+        "// dense inputs on a GB300 (" + sweep.get("device", "?") + "); regenerate, do not edit.",
         "#pragma once",
         "",
         "namespace attn_sm103 {",
