@@ -47,6 +47,18 @@ attn_status check_device() {
   return ok ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
 }
 
+// Streaming multiprocessors of the current device (cached per device ordinal; 0 on error).
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
 // ----------------------------------------------------------------------------- validation
 attn_status check_tensor4(const attn_tensor4* t) {
   if (t == nullptr || t->data == nullptr) return ATTN_ERR_NULL;
@@ -277,6 +289,20 @@ int grid_group(const char* kernel, int width, int causal, double shared_bytes, i
   return shared_bytes <= tile_major_limit(kernel, width) ? uh : 1;
 }
 
+// Forward grid: one CTA per work item. With more items than SMs the running CTAs steal the
+// items of CTAs not yet launched (cluster launch control), so each SM's CTA walks items in the
+// grid's order until none are left, its pipeline running on across them. Tuning and test
+// hooks: ATTN_FWD_PERSISTENT=0 turns the stealing off; ATTN_FWD_CTAS=<n> launches n CTAs
+// (n >= 1), CTA c taking items c, c + n, ... Returns the grid size; *clc is the stealing flag.
+int fwd_grid_size(int n_items, int* clc) {
+  *clc = 0;
+  const char* c = getenv("ATTN_FWD_CTAS");
+  if (c != nullptr && atoi(c) >= 1) return atoi(c) < n_items ? atoi(c) : n_items;
+  const char* v = getenv("ATTN_FWD_PERSISTENT");
+  *clc = (v == nullptr || atoi(v) != 0) && n_items > sm_count();
+  return n_items;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct BwdWorkspace {
@@ -363,8 +389,10 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   p.H = pr.H;
   p.group = grid_group("fwd", kernel_width(pr.D), p.causal,
                        (double)pr.units * pr.H * pr.max_k * pr.D * 4, uh);
+  p.uh = uh;
   if ((int64_t)n_blk * uh > kMaxI32) return ATTN_ERR_UNSUPPORTED;  // 1-D grid
-  const dim3 grid((unsigned)(n_blk * uh));
+  const int n_items = n_blk * uh;
+  const dim3 grid((unsigned)fwd_grid_size(n_items, &p.clc));
   p.d_out = pr.D;
   cudaError_t e = launch_attn_fwd(p, kernel_width(pr.D), pr.f16, bias != nullptr, grid,
                                   reinterpret_cast<cudaStream_t>(stream));

@@ -89,6 +89,10 @@ struct FwdParams {
   uint64_t timeout_ns;            // bound on every pipeline wait
   int withhold_tile;              // test hook: key tile the producer never loads (-1: none)
   int tiles, group;               // query blocks per (unit, head) pair; CTA-order group size
+  int uh;                         // (unit, head) pairs: work items = uh * tiles
+  int clc;                        // 1: one CTA per item, CTAs steal the items of CTAs not yet
+                                  // launched (cluster launch control); 0: CTA c takes items
+                                  // c, c + gridDim.x, ...
   int H;                          // heads
   int d_out;                      // head size of the tensors (<= the kernel's D; the TMA
                                   // loads fill the columns past it with zeros)

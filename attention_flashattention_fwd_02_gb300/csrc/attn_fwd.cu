@@ -89,9 +89,15 @@ struct FwdCfg {
   static constexpr int NTHREADS = (SPLIT_ISSUE ? 352 : 320) + (BIAS ? 32 : 0);
 };
 
+constexpr int NCLC = 4;  // work-stealing response slots
+
 template <int NST, int NSB>
 struct FwdBars {
+  alignas(16) uint4 clc_resp[NCLC];      // work-stealing responses (cluster launch control)
+  uint64_t clc_full[NCLC], clc_empty[NCLC];
+  uint64_t tsync;         // the query tiles' warps meet (a block with one tile past the end)
   uint64_t q_full;
+  uint64_t q_empty;       // the score products of a block have read Q (persistent grids)
   uint64_t k_full[NST], v_full[NST], kv_empty[NST];
   uint64_t k_empty[NST];  // SPLIT_KV: K stage free (kv_empty then frees the V stage)
   uint64_t s_full[NSB], p_full[NSB], buf_free[NSB];
@@ -127,6 +133,13 @@ __device__ __forceinline__ int key_tiles(int q_lo, int q_hi, int len_k, int caus
   return n;
 }
 
+// Work item of a CTA: one query block (NQ tiles of 128 rows) of one (unit, head) pair.
+struct FwdItem {
+  SeqView sv;
+  int z, h, blk_lo;
+  int q_lo[2], q_hi[2], n_t[2], n_max;
+};
+
 template <int D, bool F16, bool BIAS>
 __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     attn_fwd_kernel(const __grid_constant__ FwdParams p) {
@@ -136,40 +149,61 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
   __shared__ FwdBars<NST, NSB> bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // 1-D grid over (unit, head) pairs x query blocks (grid_pos); causal blocks are visited from
-  // the last (heaviest) one down
-  const GridPos gp = grid_pos((int)blockIdx.x, p.tiles, (int)(gridDim.x / p.tiles), p.group);
-  const int h = gp.zh % p.H, z = gp.zh / p.H;
-  const int n_blk = p.tiles;
-  const int m_blk = p.causal ? n_blk - 1 - gp.rank : gp.rank;
-
-  SeqView sv;
-  if (!decode_seq(p.seq, z, threadIdx.x == 0 ? p.status : nullptr, sv)) return;
-  const int blk_lo = m_blk * (C::NQ * BM);
-  if (blk_lo >= sv.len_q) return;  // past this sequence's queries
-
-  int q_lo[2], q_hi[2], n_t[2];  // with one query tile per CTA, tile 1 is empty
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    q_lo[t] = blk_lo + t * BM;
-    q_hi[t] = t < C::NQ ? min(q_lo[t] + BM, sv.len_q) : q_lo[t];
-    n_t[t] = key_tiles(q_lo[t], q_hi[t], sv.len_k, p.causal, BN);
-  }
-  const int n_max = max(n_t[0], n_t[1]);
-  const ScoreOrder order(n_t[0], n_t[1]);
-
-  if (n_max == 0) {  // no visible keys: O = 0, LSE = -inf on the valid rows
-    if (warp < 4 * C::NQ) {
-      const int row = blk_lo + threadIdx.x;
-      if (row < sv.len_q) {
-        const int64_t grow = sv.row0_q + row;
-        uint16_t* orow = p.o + sv.batch * p.o_sb + h * p.o_sh + grow * p.o_ss;
-        for (int d = 0; d < p.d_out; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
-        p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] = -INFINITY;
-      }
+  // Work items: (unit, head) pairs x query blocks, numbered in the launch's CTA order
+  // (grid_pos); causal blocks are visited from the last (heaviest) one down. A CTA starts with
+  // item blockIdx.x and then takes, with work stealing (p.clc: a grid of one CTA per item), the
+  // item of a CTA whose launch it cancelled, or else items blockIdx.x + gridDim.x, ... (a
+  // grid of fewer CTAs than items). Every role walks the same items; the rings (K/V stages,
+  // score buffers, O completions, bias slots) are indexed by running counts over the CTA's
+  // items, so a CTA's pipeline runs on from one item into the next: the next block's Q loads
+  // once the score products of the block before are done (q_empty). O_t needs no barrier of
+  // its own: the next block's first PV_t waits for P_t(0), which tile t's warps publish only
+  // after their epilogue has read O_t.
+  const int n_items = p.uh * p.tiles;
+  // Readers of each work-stealing response (one arrival each on its slot's empty barrier):
+  // the MMA and S issuers, the V and bias producers, each softmax warp. The producer, which
+  // makes the requests, reads each response before it reuses the slot.
+  constexpr int CLC_READERS = 1 + (C::SPLIT_ISSUE ? 1 : 0) + (C::SPLIT_KV ? 1 : 0) +
+                              (BIAS ? 1 : 0) + 4 * C::NQ;
+  enum { kProducer, kLane, kWarp };
+  // The item after `item` for a role, or -1 when there is none (or a wait gave up). ci counts
+  // the responses this role has read: response ci sits in slot ci mod NCLC, phase
+  // (ci / NCLC) mod 2 of its full barrier.
+  auto next_item = [&](int item, int& ci, int who) -> int {
+    if (!p.clc) return item + (int)gridDim.x < n_items ? item + (int)gridDim.x : -1;
+    const int slot = ci % NCLC;
+    const uint32_t full = smem_u32(&bars.clc_full[slot]);
+    volatile int* ab = &bars.abort;
+    const bool landed = who == kWarp ? mbar_wait_warp(full, (ci / NCLC) & 1, ab, p.timeout_ns)
+                                     : mbar_wait(full, (ci / NCLC) & 1, ab, p.timeout_ns);
+    if (!landed) return -1;
+    const int nx = clc_cancelled_x(smem_u32(&bars.clc_resp[slot]));
+    if (who == kWarp) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars.clc_empty[slot]));
+    } else if (who == kLane) {
+      mbar_arrive(smem_u32(&bars.clc_empty[slot]));
     }
-    return;
-  }
+    ++ci;
+    return nx;
+  };
+  auto decode_item = [&](int item, FwdItem& w) -> bool {
+    const GridPos gp = grid_pos(item, p.tiles, p.uh, p.group);
+    w.h = gp.zh % p.H;
+    w.z = gp.zh / p.H;
+    const int m_blk = p.causal ? p.tiles - 1 - gp.rank : gp.rank;
+    if (!decode_seq(p.seq, w.z, threadIdx.x == 0 ? p.status : nullptr, w.sv)) return false;
+    w.blk_lo = m_blk * (C::NQ * BM);
+    if (w.blk_lo >= w.sv.len_q) return false;  // past this sequence's queries
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {  // with one query tile per CTA, tile 1 is empty
+      w.q_lo[t] = w.blk_lo + t * BM;
+      w.q_hi[t] = t < C::NQ ? min(w.q_lo[t] + BM, w.sv.len_q) : w.q_lo[t];
+      w.n_t[t] = key_tiles(w.q_lo[t], w.q_hi[t], w.sv.len_k, p.causal, BN);
+    }
+    w.n_max = max(w.n_t[0], w.n_t[1]);
+    return true;
+  };
 
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sQ = smem_u32(smem + C::OFF_Q);
@@ -178,7 +212,13 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
+    for (int i = 0; i < NCLC; ++i) {
+      mbar_init(smem_u32(&bars.clc_full[i]), 1);
+      mbar_init(smem_u32(&bars.clc_empty[i]), CLC_READERS);
+    }
+    mbar_init(smem_u32(&bars.tsync), 8);
     mbar_init(smem_u32(&bars.q_full), 1);
+    mbar_init(smem_u32(&bars.q_empty), 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 1);
       mbar_init(smem_u32(&bars.v_full[s]), 1);
@@ -215,119 +255,179 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       tma_prefetch_map(&p.tm_k);
       tma_prefetch_map(&p.tm_v);
       const uint32_t qb = smem_u32(&bars.q_full);
-      mbar_arrive_expect_tx(qb, C::NQ * C::Q_BYTES);
+      int kv_g = 0, q_n = 0;  // key tiles and query blocks loaded so far
+      int last_g[NST];        // last key tile (running count) loaded into each stage (-1: none)
 #pragma unroll
-      for (int t = 0; t < C::NQ; ++t)
+      for (int st = 0; st < NST; ++st) last_g[st] = -1;
+      bool go = true;
+      int ci = 0, issued = 0;  // work-stealing responses read, requests made
+      for (int item = blockIdx.x; go && item >= 0;
+           item = go ? next_item(item, ci, kProducer) : -1) {
+        if (p.clc) {
+          // request the item after this one now, so that the answer is in when this one ends;
+          // the slot is free once every reader has read the response it held before
+          const int slot = issued % NCLC, u = issued / NCLC;
+          if (u > 0 && !mbar_wait(smem_u32(&bars.clc_empty[slot]), (u - 1) & 1, abort,
+                                  p.timeout_ns))
+            break;
+          mbar_arrive_expect_tx(smem_u32(&bars.clc_full[slot]), 16);
+          clc_try_cancel(smem_u32(&bars.clc_resp[slot]), smem_u32(&bars.clc_full[slot]));
+          ++issued;
+        }
+        FwdItem w;
+        if (!decode_item(item, w) || w.n_max == 0) continue;
+        // the previous block's score products have read Q
+        if (q_n > 0 && !mbar_wait(smem_u32(&bars.q_empty), (q_n - 1) & 1, abort, p.timeout_ns))
+          break;
+        mbar_arrive_expect_tx(qb, C::NQ * C::Q_BYTES);
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_4d(sQ + t * C::Q_BYTES + s * BM * 128, &p.tm_q, qb, s * 64,
-                      sv.row0_q + q_lo[t], h, sv.batch);
-      int last_j[NST];  // last key tile loaded into each stage (-1: none)
-#pragma unroll
-      for (int st = 0; st < NST; ++st) last_j[st] = -1;
-      for (int j = 0; j < n_max; ++j) {
-        const int st = j % NST;
-        // failure-detection test: no key tile from this one on is loaded (skipping only this
-        // one would leave the next wait on its stage aiming at a phase that never completes)
-        if (j == p.withhold_tile) break;
-        const uint32_t empty = C::SPLIT_KV ? smem_u32(&bars.k_empty[st]) : smem_u32(&bars.kv_empty[st]);
-        if (j >= NST && !mbar_wait(empty, ((j / NST) - 1) & 1, abort, p.timeout_ns)) break;
-        last_j[st] = j;
-        const int krow = sv.row0_k + j * BN;
-        const uint32_t kb = smem_u32(&bars.k_full[st]);
-        mbar_arrive_expect_tx(kb, C::KV_BYTES);
-#pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_4d(sK + st * C::KV_BYTES + s * BN * 128, &p.tm_k, kb, s * 64, krow, h, sv.batch);
-        // the tile that will next fill this stage: into L2 now, so that its load is not a
-        // DRAM round trip when the stage frees up
-        const bool pf = j + NST < n_max && j + NST != p.withhold_tile;
-        if (pf) {
+        for (int t = 0; t < C::NQ; ++t)
 #pragma unroll
           for (int s = 0; s < D / 64; ++s)
-            tma_prefetch_l2_4d(&p.tm_k, s * 64, krow + NST * BN, h, sv.batch);
-        }
-        if (C::SPLIT_KV) continue;  // V has its own producer warp
-        const uint32_t vb = smem_u32(&bars.v_full[st]);
-        mbar_arrive_expect_tx(vb, C::KV_BYTES);
-#pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_4d(sV + st * C::KV_BYTES + s * BN * 128, &p.tm_v, vb, s * 64, krow, h, sv.batch);
-        if (pf) {
+            tma_load_4d(sQ + t * C::Q_BYTES + s * BM * 128, &p.tm_q, qb, s * 64,
+                        w.sv.row0_q + w.q_lo[t], w.h, w.sv.batch);
+        ++q_n;
+        for (int j = 0; j < w.n_max; ++j) {
+          const int g = kv_g + j, st = g % NST;
+          // failure-detection test: no key tile from this one on is loaded (skipping only this
+          // one would leave the next wait on its stage aiming at a phase that never completes)
+          if (j == p.withhold_tile) {
+            go = false;
+            break;
+          }
+          const uint32_t empty =
+              C::SPLIT_KV ? smem_u32(&bars.k_empty[st]) : smem_u32(&bars.kv_empty[st]);
+          if (g >= NST && !mbar_wait(empty, ((g / NST) - 1) & 1, abort, p.timeout_ns)) {
+            go = false;
+            break;
+          }
+          last_g[st] = g;
+          const int krow = w.sv.row0_k + j * BN;
+          const uint32_t kb = smem_u32(&bars.k_full[st]);
+          mbar_arrive_expect_tx(kb, C::KV_BYTES);
 #pragma unroll
           for (int s = 0; s < D / 64; ++s)
-            tma_prefetch_l2_4d(&p.tm_v, s * 64, krow + NST * BN, h, sv.batch);
+            tma_load_4d(sK + st * C::KV_BYTES + s * BN * 128, &p.tm_k, kb, s * 64, krow, w.h,
+                        w.sv.batch);
+          // the tile that will next fill this stage: into L2 now, so that its load is not a
+          // DRAM round trip when the stage frees up
+          const bool pf = j + NST < w.n_max && j + NST != p.withhold_tile;
+          if (pf) {
+#pragma unroll
+            for (int s = 0; s < D / 64; ++s)
+              tma_prefetch_l2_4d(&p.tm_k, s * 64, krow + NST * BN, w.h, w.sv.batch);
+          }
+          if (C::SPLIT_KV) continue;  // V has its own producer warp
+          const uint32_t vb = smem_u32(&bars.v_full[st]);
+          mbar_arrive_expect_tx(vb, C::KV_BYTES);
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(sV + st * C::KV_BYTES + s * BN * 128, &p.tm_v, vb, s * 64, krow, w.h,
+                        w.sv.batch);
+          if (pf) {
+#pragma unroll
+            for (int s = 0; s < D / 64; ++s)
+              tma_prefetch_l2_4d(&p.tm_v, s * 64, krow + NST * BN, w.h, w.sv.batch);
+          }
         }
+        kv_g += w.n_max;
       }
+      // a request whose response was not read: let it land before the CTA exits
+      if (issued > ci)
+        mbar_wait_drain(smem_u32(&bars.clc_full[(issued - 1) % NCLC]),
+                        ((issued - 1) / NCLC) & 1, p.timeout_ns);
       if (*abort) {  // the consumers gave up: let this lane's copies land before exiting
-        mbar_wait_drain(qb, 0, p.timeout_ns);
+        if (q_n > 0) mbar_wait_drain(qb, (q_n - 1) & 1, p.timeout_ns);
 #pragma unroll
         for (int st = 0; st < NST; ++st)
-          if (last_j[st] >= 0) {
-            mbar_wait_drain(smem_u32(&bars.k_full[st]), (last_j[st] / NST) & 1, p.timeout_ns);
+          if (last_g[st] >= 0) {
+            mbar_wait_drain(smem_u32(&bars.k_full[st]), (last_g[st] / NST) & 1, p.timeout_ns);
             if (!C::SPLIT_KV)
-              mbar_wait_drain(smem_u32(&bars.v_full[st]), (last_j[st] / NST) & 1, p.timeout_ns);
+              mbar_wait_drain(smem_u32(&bars.v_full[st]), (last_g[st] / NST) & 1, p.timeout_ns);
           }
       }
     }
   } else if (C::SPLIT_KV && warp == C::WARP_VPROD) {
     // ------------------------------------------------------------------ V producer (d_head 256)
     if (lane == 0) {
-      int last_j[NST];
+      int kv_g = 0;
+      int last_g[NST];
 #pragma unroll
-      for (int st = 0; st < NST; ++st) last_j[st] = -1;
-      for (int j = 0; j < n_max; ++j) {
-        const int st = j % NST;
-        if (j == p.withhold_tile) break;
-        if (j >= NST &&
-            !mbar_wait(smem_u32(&bars.kv_empty[st]), ((j / NST) - 1) & 1, abort, p.timeout_ns))
-          break;
-        last_j[st] = j;
-        const uint32_t vb = smem_u32(&bars.v_full[st]);
-        mbar_arrive_expect_tx(vb, C::KV_BYTES);
-#pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_4d(sV + st * C::KV_BYTES + s * BN * 128, &p.tm_v, vb, s * 64,
-                      sv.row0_k + j * BN, h, sv.batch);
-        if (j + NST < n_max && j + NST != p.withhold_tile) {
+      for (int st = 0; st < NST; ++st) last_g[st] = -1;
+      bool go = true;
+      int ci = 0;
+      for (int item = blockIdx.x; go && item >= 0; item = go ? next_item(item, ci, kLane) : -1) {
+        FwdItem w;
+        if (!decode_item(item, w) || w.n_max == 0) continue;
+        for (int j = 0; j < w.n_max; ++j) {
+          const int g = kv_g + j, st = g % NST;
+          if (j == p.withhold_tile ||
+              (g >= NST && !mbar_wait(smem_u32(&bars.kv_empty[st]), ((g / NST) - 1) & 1, abort,
+                                      p.timeout_ns))) {
+            go = false;
+            break;
+          }
+          last_g[st] = g;
+          const uint32_t vb = smem_u32(&bars.v_full[st]);
+          mbar_arrive_expect_tx(vb, C::KV_BYTES);
 #pragma unroll
           for (int s = 0; s < D / 64; ++s)
-            tma_prefetch_l2_4d(&p.tm_v, s * 64, sv.row0_k + (j + NST) * BN, h, sv.batch);
+            tma_load_4d(sV + st * C::KV_BYTES + s * BN * 128, &p.tm_v, vb, s * 64,
+                        w.sv.row0_k + j * BN, w.h, w.sv.batch);
+          if (j + NST < w.n_max && j + NST != p.withhold_tile) {
+#pragma unroll
+            for (int s = 0; s < D / 64; ++s)
+              tma_prefetch_l2_4d(&p.tm_v, s * 64, w.sv.row0_k + (j + NST) * BN, w.h, w.sv.batch);
+          }
         }
+        kv_g += w.n_max;
       }
       if (*abort)
 #pragma unroll
         for (int st = 0; st < NST; ++st)
-          if (last_j[st] >= 0)
-            mbar_wait_drain(smem_u32(&bars.v_full[st]), (last_j[st] / NST) & 1, p.timeout_ns);
+          if (last_g[st] >= 0)
+            mbar_wait_drain(smem_u32(&bars.v_full[st]), (last_g[st] / NST) & 1, p.timeout_ns);
     }
   } else if (BIAS && warp == C::WARP_BIAS) {
     // ------------------------------------------------------------------ bias producer
-    // bias tiles in score-tile order: key tile j of query tile t into slot
-    // t * BS_T + j mod BS_T (phase j / BS_T), each slot refilled once tile t's softmax warps
-    // have read its previous tile (they wait on nothing this warp does afterwards). A warp of
-    // its own, so that its waits never share a warp with the K/V producer's. Every unit
-    // (batch, or sequence of a compact batch) finds its bias block at offset 0 of its own
-    // slice of the bias's first dimension, so the key coordinate (the innermost, which a TMA
-    // copy needs 16-byte aligned) is always a multiple of 64 elements.
+    // bias tiles in score-tile order: key tile j of query tile t (running count b over the
+    // tile's key tiles) into slot t * BS_T + b mod BS_T (phase b / BS_T), each slot refilled
+    // once tile t's softmax warps have read its previous tile (they wait on nothing this warp
+    // does afterwards). A warp of its own, so that its waits never share a warp with the K/V
+    // producer's. Every unit (batch, or sequence of a compact batch) finds its bias block at
+    // offset 0 of its own slice of the bias's first dimension, so the key coordinate (the
+    // innermost, which a TMA copy needs 16-byte aligned) is always a multiple of 64 elements.
     if (lane == 0) {
       tma_prefetch_map(&p.tm_b);
       const uint32_t sB = smem_u32(smem + C::OFF_B);
-      const int hb = p.bias_h_bcast ? 0 : h, bb = p.bias_b_bcast ? 0 : z;
+      int b_g[2] = {0, 0};        // bias tiles of each query tile loaded so far
       int last_ph[2] = {-1, -1};  // last phase loaded into each slot
-      for (int k = 0; k < order.total; ++k) {
-        const int t = order.t_of(k), j = order.j_of(k);
-        const int slot = t * C::BS_T + j % C::BS_T, ph = j / C::BS_T;
-        if (ph >= 1 &&
-            !mbar_wait(smem_u32(&bars.b_empty[slot]), (ph - 1) & 1, abort, p.timeout_ns))
-          break;
-        const uint32_t bf = smem_u32(&bars.b_full[slot]);
-        mbar_arrive_expect_tx(bf, C::B_BYTES);
+      bool go = true;
+      int ci = 0;
+      for (int item = blockIdx.x; go && item >= 0; item = go ? next_item(item, ci, kLane) : -1) {
+        FwdItem w;
+        if (!decode_item(item, w) || w.n_max == 0) continue;
+        const ScoreOrder order(w.n_t[0], w.n_t[1]);
+        const int hb = p.bias_h_bcast ? 0 : w.h, bb = p.bias_b_bcast ? 0 : w.z;
+        for (int k = 0; k < order.total; ++k) {
+          const int t = order.t_of(k), j = order.j_of(k);
+          const int gb = b_g[t] + j;
+          const int slot = t * C::BS_T + gb % C::BS_T, ph = gb / C::BS_T;
+          if (ph >= 1 &&
+              !mbar_wait(smem_u32(&bars.b_empty[slot]), (ph - 1) & 1, abort, p.timeout_ns)) {
+            go = false;
+            break;
+          }
+          const uint32_t bf = smem_u32(&bars.b_full[slot]);
+          mbar_arrive_expect_tx(bf, C::B_BYTES);
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
-          tma_load_4d(sB + slot * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
-                      q_lo[t], hb, bb);
-        last_ph[slot] = ph;
+          for (int s = 0; s < 2; ++s)
+            tma_load_4d(sB + slot * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
+                        w.q_lo[t], hb, bb);
+          last_ph[slot] = ph;
+        }
+        b_g[0] += w.n_t[0];
+        b_g[1] += w.n_t[1];
       }
       if (*abort)  // let the copies in flight land before exiting
 #pragma unroll
@@ -338,59 +438,81 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ MMA issuer
     constexpr uint32_t idO = idesc_f32acc(128, D, false, true, F16);
-    const uint64_t v_desc = desc_mnmajor(sV, BN, 0);
-    const int total = order.total;
     constexpr uint32_t idS = idesc_f32acc(128, BN, false, false, F16);
+    const uint64_t v_desc = desc_mnmajor(sV, BN, 0);
     const uint64_t q_desc = desc_kmajor(sQ, BM, 0);
     const uint64_t k_desc = desc_kmajor(sK, BN, 0);
-    int k_seen = -1;  // key tile whose K stage was last seen full
-    // S number k into buffer k mod NSB (single-issuer schedule); false when a wait gave up.
-    auto issue_s = [&](int k) -> bool {
-      const int t = order.t_of(k), j = order.j_of(k), st = j % NST;
-      if (j != k_seen) {
-        if (!mbar_wait(smem_u32(&bars.k_full[st]), (j / NST) & 1, abort, p.timeout_ns))
-          return false;
-        k_seen = j;
-        tc_fence_after();
-      }
-      const int bsel = k % NSB;
-      const uint32_t tS = tmem + bsel * 128;
-      const uint64_t qd = q_desc + (uint32_t)(t * (C::Q_BYTES >> 4));
-      const uint64_t kd = k_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        umma_ss_w(tS, qd + kmajor_step(BM, kk), kd + kmajor_step(BN, kk), idS, kk > 0);
-      umma_commit_w(smem_u32(&bars.s_full[bsel]));
-      // one query tile: K_j has no other reader once this product has completed
-      if (C::SPLIT_KV) umma_commit_w(smem_u32(&bars.k_empty[st]));
-      return true;
-    };
+    int kv_g = 0, s_g = 0, q_n = 0;  // key tiles, score tiles, query blocks of earlier items
+    int pv_g0 = 0, pv_g1 = 0;        // PV products of query tile 0 / 1 in earlier items
+    int k_seen = -1, v_seen = -1;    // key tiles (running count) whose K / V were seen full
     bool ok = true;
-    if (!C::SPLIT_ISSUE) {
-      ok = mbar_wait(smem_u32(&bars.q_full), 0, abort, p.timeout_ns);
-      for (int k = 0; ok && k < min(NSB, total); ++k) ok = issue_s(k);
-    }
-    int v_seen = -1;  // key tile whose V stage was last seen full
-    for (int k = 0; ok && k < total; ++k) {
-      const int t = order.t_of(k), j = order.j_of(k), st = j % NST, bsel = k % NSB;
-      if (j != v_seen) {
-        if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / NST) & 1, abort, p.timeout_ns)) break;
-        v_seen = j;
-      }
-      if (!mbar_wait(smem_u32(&bars.p_full[bsel]), (k / NSB) & 1, abort, p.timeout_ns)) break;
-      tc_fence_after();
-      const uint32_t tS = tmem + bsel * 128;
-      const uint32_t tO = tmem + (t ? C::COL_O1 : C::COL_O0);
-      const uint64_t vd = v_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
+    int ci = 0;
+    for (int item = blockIdx.x; ok && item >= 0; item = ok ? next_item(item, ci, kWarp) : -1) {
+      FwdItem w;
+      if (!decode_item(item, w) || w.n_max == 0) continue;
+      const ScoreOrder order(w.n_t[0], w.n_t[1]);
+      const int total = order.total;
+      // S number k of this item into buffer (s_g + k) mod NSB (single-issuer schedule); false
+      // when a wait gave up
+      auto issue_s = [&](int k) -> bool {
+        const int t = order.t_of(k), j = order.j_of(k);
+        const int g = kv_g + j, st = g % NST;
+        if (g != k_seen) {
+          if (!mbar_wait_warp(smem_u32(&bars.k_full[st]), (g / NST) & 1, abort, p.timeout_ns))
+            return false;
+          k_seen = g;
+          tc_fence_after();
+        }
+        const int bsel = (s_g + k) % NSB;
+        const uint32_t tS = tmem + bsel * 128;
+        const uint64_t qd = q_desc + (uint32_t)(t * (C::Q_BYTES >> 4));
+        const uint64_t kd = k_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
-        umma_ts_w(tO, tS + kk * 8, vd + mnmajor_step(kk), idO, (j > 0 || kk > 0));
-      umma_commit_w(smem_u32(&bars.o_done[t][j & 1]));
-      if (C::SPLIT_ISSUE && k + NSB < total) umma_commit_w(smem_u32(&bars.buf_free[bsel]));
-      // Stage st is free once the last product reading V_j is done; the score products that
-      // read K_j finished before their P was published, hence before this PV.
-      if (k + 1 == total || order.j_of(k + 1) != j) umma_commit_w(smem_u32(&bars.kv_empty[st]));
-      if (!C::SPLIT_ISSUE && k + NSB < total) ok = issue_s(k + NSB);
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss_w(tS, qd + kmajor_step(BM, kk), kd + kmajor_step(BN, kk), idS, kk > 0);
+        umma_commit_w(smem_u32(&bars.s_full[bsel]));
+        // one query tile: K_j has no other reader once this product has completed
+        if (C::SPLIT_KV) umma_commit_w(smem_u32(&bars.k_empty[st]));
+        if (k == total - 1) umma_commit_w(smem_u32(&bars.q_empty));  // Q read for the last time
+        return true;
+      };
+      if (!C::SPLIT_ISSUE) {
+        ok = mbar_wait_warp(smem_u32(&bars.q_full), q_n & 1, abort, p.timeout_ns);
+        for (int k = 0; ok && k < min(NSB, total); ++k) ok = issue_s(k);
+      }
+      for (int k = 0; ok && k < total; ++k) {
+        const int t = order.t_of(k), j = order.j_of(k);
+        const int g = kv_g + j, st = g % NST, gs = s_g + k, bsel = gs % NSB;
+        if (g != v_seen) {
+          if (!mbar_wait_warp(smem_u32(&bars.v_full[st]), (g / NST) & 1, abort, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          v_seen = g;
+        }
+        if (!mbar_wait_warp(smem_u32(&bars.p_full[bsel]), (gs / NSB) & 1, abort, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tS = tmem + bsel * 128;
+        const uint32_t tO = tmem + (t ? C::COL_O1 : C::COL_O0);
+        const uint64_t vd = v_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ts_w(tO, tS + kk * 8, vd + mnmajor_step(kk), idO, (j > 0 || kk > 0));
+        umma_commit_w(smem_u32(&bars.o_done[t][((t ? pv_g1 : pv_g0) + j) & 1]));
+        if (C::SPLIT_ISSUE) umma_commit_w(smem_u32(&bars.buf_free[bsel]));
+        // Stage st is free once the last product reading V_j is done; the score products that
+        // read K_j finished before their P was published, hence before this PV.
+        if (k + 1 == total || order.j_of(k + 1) != j) umma_commit_w(smem_u32(&bars.kv_empty[st]));
+        if (!C::SPLIT_ISSUE && k + NSB < total) ok = issue_s(k + NSB);
+      }
+      s_g += total;
+      kv_g += w.n_max;
+      ++q_n;
+      pv_g0 += w.n_t[0];
+      pv_g1 += w.n_t[1];
     }
     // every product this warp issued has completed before tensor memory is released
     umma_commit_w(smem_u32(&bars.mma_drain[0]));
@@ -400,28 +522,47 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     constexpr uint32_t idS = idesc_f32acc(128, BN, false, false, F16);
     const uint64_t q_desc = desc_kmajor(sQ, BM, 0);
     const uint64_t k_desc = desc_kmajor(sK, BN, 0);
-    const int total = order.total;
-    bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort, p.timeout_ns);
-    int k_seen = -1;  // key tile whose K stage was last seen full
-    for (int k = 0; ok && k < total; ++k) {
-      const int t = order.t_of(k), j = order.j_of(k), st = j % NST, bsel = k % NSB;
-      // PV(k - NSB) read this buffer; its release cannot run a phase ahead, since the next
-      // release of the buffer needs S(k), issued below.
-      if (k >= NSB &&
-          !mbar_wait(smem_u32(&bars.buf_free[bsel]), ((k - NSB) / NSB) & 1, abort, p.timeout_ns))
-        break;
-      if (j != k_seen) {
-        if (!mbar_wait(smem_u32(&bars.k_full[st]), (j / NST) & 1, abort, p.timeout_ns)) break;
-        k_seen = j;
-      }
-      tc_fence_after();
-      const uint32_t tS = tmem + bsel * 128;
-      const uint64_t qd = q_desc + (uint32_t)(t * (C::Q_BYTES >> 4));
-      const uint64_t kd = k_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
+    int kv_g = 0, s_g = 0, q_n = 0;
+    int k_seen = -1;  // key tile (running count) whose K stage was last seen full
+    bool ok = true;
+    int ci = 0;
+    for (int item = blockIdx.x; ok && item >= 0; item = ok ? next_item(item, ci, kWarp) : -1) {
+      FwdItem w;
+      if (!decode_item(item, w) || w.n_max == 0) continue;
+      const ScoreOrder order(w.n_t[0], w.n_t[1]);
+      const int total = order.total;
+      ok = mbar_wait_warp(smem_u32(&bars.q_full), q_n & 1, abort, p.timeout_ns);
+      for (int k = 0; ok && k < total; ++k) {
+        const int t = order.t_of(k), j = order.j_of(k);
+        const int g = kv_g + j, st = g % NST, gs = s_g + k, bsel = gs % NSB;
+        // PV(gs - NSB) read this buffer; its release cannot run a phase ahead, since the next
+        // release of the buffer needs S(gs), issued below.
+        if (gs >= NSB &&
+            !mbar_wait_warp(smem_u32(&bars.buf_free[bsel]), ((gs - NSB) / NSB) & 1, abort,
+                       p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        if (g != k_seen) {
+          if (!mbar_wait_warp(smem_u32(&bars.k_full[st]), (g / NST) & 1, abort, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          k_seen = g;
+        }
+        tc_fence_after();
+        const uint32_t tS = tmem + bsel * 128;
+        const uint64_t qd = q_desc + (uint32_t)(t * (C::Q_BYTES >> 4));
+        const uint64_t kd = k_desc + (uint32_t)(st * (C::KV_BYTES >> 4));
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        umma_ss_w(tS, qd + kmajor_step(BM, kk), kd + kmajor_step(BN, kk), idS, kk > 0);
-      umma_commit_w(smem_u32(&bars.s_full[bsel]));
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss_w(tS, qd + kmajor_step(BM, kk), kd + kmajor_step(BN, kk), idS, kk > 0);
+        umma_commit_w(smem_u32(&bars.s_full[bsel]));
+        if (k == total - 1) umma_commit_w(smem_u32(&bars.q_empty));  // Q read for the last time
+      }
+      s_g += total;
+      kv_g += w.n_max;
+      ++q_n;
     }
     umma_commit_w(smem_u32(&bars.mma_drain[1]));
     mbar_wait_drain(smem_u32(&bars.mma_drain[1]), 0, p.timeout_ns);
@@ -430,173 +571,222 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     const int t = warp >> 2;                 // query tile of this warpgroup
     const int r = (warp & 3) * 32 + lane;    // row in tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int row = q_lo[t] + r;             // local query index
-    const int n = n_t[t];
     const uint32_t tOt = tmem + (t ? C::COL_O1 : C::COL_O0) + lane_off;
     const float c2 = p.scale_log2;
-    float m_use = -INFINITY, l = 0.f;
+    int s_g = 0, pv_g = 0;  // score tiles of earlier items; PVs of this query tile in them
     bool ok = true;
-    for (int j = 0; ok && j < n; ++j) {
-      const int k = order.k_of(t, j), bsel = k % NSB;
-      const uint32_t tSt = tmem + bsel * 128 + lane_off;
-      if (!mbar_wait(smem_u32(&bars.s_full[bsel]), (k / NSB) & 1, abort, p.timeout_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[BN];
-      static_assert(BN == 128, "one four-way TMEM load covers the score row");
-      ATTN_TMEM_LD4_X32(tSt, tSt + 32, tSt + 64, tSt + 96, reinterpret_cast<uint32_t*>(s),
-                        reinterpret_cast<uint32_t*>(s + 32), reinterpret_cast<uint32_t*>(s + 64),
-                        reinterpret_cast<uint32_t*>(s + 96));
-      if constexpr (BIAS) {
-        // s <- s c2 + bias log2(e): the scores in base-2 units, bias included
-        const int slot = t * C::BS_T + j % C::BS_T;  // phase j / BS_T
-        if (!mbar_wait(smem_u32(&bars.b_full[slot]), (j / C::BS_T) & 1, abort, p.timeout_ns)) {
-          ok = false;
-          break;
+    int ci = 0, n_sync = 0;  // work-stealing responses read; meetings of the two query tiles
+    for (int item = blockIdx.x; ok && item >= 0; item = ok ? next_item(item, ci, kWarp) : -1) {
+      int q_lo, n, len_k;
+      bool one_empty;  // a query block with one tile past the sequence's end
+      ScoreOrder order(0, 0);
+      {
+      FwdItem w;
+      if (!decode_item(item, w)) continue;
+      if (w.n_max == 0) {  // no visible keys: O = 0, LSE = -inf on the valid rows
+        const int row = w.blk_lo + (int)threadIdx.x;
+        if (row < w.sv.len_q) {
+          const int64_t grow = w.sv.row0_q + row;
+          uint16_t* orow = p.o + w.sv.batch * p.o_sb + w.h * p.o_sh + grow * p.o_ss;
+          for (int d = 0; d < p.d_out; d += 8)
+            *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+          p.lse[w.sv.batch * p.l_sb + w.h * p.l_sh + grow * p.l_ss] = -INFINITY;
         }
-        const uint8_t* brow = smem + C::OFF_B + slot * C::B_BYTES + r * 128;
-        const uint64_t c2x2b = f2_pack(c2, c2), l2e = f2_pack(1.4426950408889634f, 1.4426950408889634f);
-#pragma unroll
-        for (int sl = 0; sl < 2; ++sl)
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint4 w = *reinterpret_cast<const uint4*>(brow + sl * BM * 128 +
-                                                            16 * (ch ^ (r & 7)));
-            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = sl * 64 + ch * 8 + 2 * e;
-              const float2 bv = unpack2<F16>(wv[e]);
-              f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), c2x2b, f2_mul(f2_pack(bv.x, bv.y), l2e)),
-                        s[c], s[c + 1]);
-            }
-          }
-        mbar_arrive(smem_u32(&bars.b_empty[slot]));
+        continue;
       }
-      // with a bias the scores are already scaled
-      const float cs = BIAS ? 1.f : c2;
-      const int k0 = j * BN;
-      if (k0 + BN > sv.len_k || (p.causal && k0 + BN - 1 > q_lo[t])) {
-        const int kmax = p.causal ? min(row, sv.len_k - 1) : sv.len_k - 1;
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (k0 + c > kmax) s[c] = -INFINITY;
+      order = ScoreOrder(w.n_t[0], w.n_t[1]);
+      q_lo = t ? w.q_lo[1] : w.q_lo[0];
+      n = t ? w.n_t[1] : w.n_t[0];
+      len_k = w.sv.len_k;
+      one_empty = C::NQ == 2 && min(w.n_t[0], w.n_t[1]) == 0;
       }
-      // row maximum: four independent chains of three-input max
-      float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
-      float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
-#pragma unroll
-      for (int c = 12; c + 8 <= BN; c += 8) {
-        mx0 = fmax3(mx0, s[c], s[c + 1]);
-        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
-      }
-      mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
-      mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
-      const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs;
-      float m_new = m_use, scale = 1.f;
-      if (mxs > m_use + 8.f) {
-        m_new = mxs;
-        scale = ex2_approx(m_use - m_new);
-      }
-      const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
-      // p = 2^(s c2 - m): scale-and-shift and the row sum run on paired fp32 instructions
-      const uint64_t c2x2 = f2_pack(cs, cs), negm2 = f2_pack(neg_m, neg_m);
-      uint64_t rs0 = 0, rs1 = 0;  // two pairs of partial sums (0.0f bit pattern is 0)
-      uint32_t pk[BN / 2];
-#pragma unroll
-      for (int c = 0; c < BN / 2; c += 2) {
-        float x0, x1, x2, x3;
-        f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), c2x2, negm2), x0, x1);
-        f2_unpack(f2_fma(f2_pack(s[2 * c + 2], s[2 * c + 3]), c2x2, negm2), x2, x3);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-        rs0 = f2_add(rs0, f2_pack(p0, p1));
-        rs1 = f2_add(rs1, f2_pack(p2, p3));
-        pk[c] = pack2<F16>(p0, p1);
-        pk[c + 1] = pack2<F16>(p2, p3);
-      }
-      float a0, a1;
-      f2_unpack(f2_add(rs0, rs1), a0, a1);
-      l = l * scale + (a0 + a1);
-      m_use = m_new;
-      // O_t is rescaled only when the reference maximum moved; PV_t(j-1) must have finished
-      // first. PV_t(i) completes phase i / 2 of barrier [t][i mod 2], and the parity names the
-      // phase exactly: every schedule has completed PV(k - 3), hence PV_t(j - 3), once S_t(j)
-      // is in TMEM, and PV_t(j + 1) cannot run before this thread publishes P_t(j).
-      if (j > 0 && __any_sync(0xffffffffu, scale != 1.f)) {
-        if (!mbar_wait(smem_u32(&bars.o_done[t][(j - 1) & 1]), ((j - 1) >> 1) & 1, abort,
-                       p.timeout_ns)) {
+      const int row = q_lo + r;  // local query index
+      float m_use = -INFINITY, l = 0.f;
+      for (int j = 0; ok && j < n; ++j) {
+        const int gs = s_g + order.k_of(t, j), bsel = gs % NSB;
+        const uint32_t tSt = tmem + bsel * 128 + lane_off;
+        if (!mbar_wait_warp(smem_u32(&bars.s_full[bsel]), (gs / NSB) & 1, abort, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t sc2 = f2_pack(scale, scale);
+        float s[BN];
+        static_assert(BN == 128, "one four-way TMEM load covers the score row");
+        ATTN_TMEM_LD4_X32(tSt, tSt + 32, tSt + 64, tSt + 96, reinterpret_cast<uint32_t*>(s),
+                          reinterpret_cast<uint32_t*>(s + 32), reinterpret_cast<uint32_t*>(s + 64),
+                          reinterpret_cast<uint32_t*>(s + 96));
+        if constexpr (BIAS) {
+          // s <- s c2 + bias log2(e): the scores in base-2 units, bias included
+          const int gb = pv_g + j;  // this tile's key tiles so far (the bias producer's count)
+          const int slot = t * C::BS_T + gb % C::BS_T;
+          if (!mbar_wait_warp(smem_u32(&bars.b_full[slot]), (gb / C::BS_T) & 1, abort,
+                         p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* brow = smem + C::OFF_B + slot * C::B_BYTES + r * 128;
+          const uint64_t c2x2b = f2_pack(c2, c2), l2e = f2_pack(1.4426950408889634f, 1.4426950408889634f);
+#pragma unroll
+          for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint4 wv4 = *reinterpret_cast<const uint4*>(brow + sl * BM * 128 +
+                                                                16 * (ch ^ (r & 7)));
+              const uint32_t wv[4] = {wv4.x, wv4.y, wv4.z, wv4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = sl * 64 + ch * 8 + 2 * e;
+                const float2 bv = unpack2<F16>(wv[e]);
+                f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), c2x2b, f2_mul(f2_pack(bv.x, bv.y), l2e)),
+                          s[c], s[c + 1]);
+              }
+            }
+          mbar_arrive(smem_u32(&bars.b_empty[slot]));
+        }
+        // with a bias the scores are already scaled
+        const float cs = BIAS ? 1.f : c2;
+        const int k0 = j * BN;
+        if (k0 + BN > len_k || (p.causal && k0 + BN - 1 > q_lo)) {
+          const int kmax = p.causal ? min(row, len_k - 1) : len_k - 1;
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (k0 + c > kmax) s[c] = -INFINITY;
+        }
+        // row maximum: four independent chains of three-input max
+        float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+        float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+        for (int c = 12; c + 8 <= BN; c += 8) {
+          mx0 = fmax3(mx0, s[c], s[c + 1]);
+          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+        }
+        mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
+        mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
+        const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs;
+        float m_new = m_use, scale = 1.f;
+        if (mxs > m_use + 8.f) {
+          m_new = mxs;
+          scale = ex2_approx(m_use - m_new);
+        }
+        const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+        // p = 2^(s c2 - m): scale-and-shift and the row sum run on paired fp32 instructions
+        const uint64_t c2x2 = f2_pack(cs, cs), negm2 = f2_pack(neg_m, neg_m);
+        uint64_t rs0 = 0, rs1 = 0;  // two pairs of partial sums (0.0f bit pattern is 0)
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN / 2; c += 2) {
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), c2x2, negm2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(s[2 * c + 2], s[2 * c + 3]), c2x2, negm2), x2, x3);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          rs0 = f2_add(rs0, f2_pack(p0, p1));
+          rs1 = f2_add(rs1, f2_pack(p2, p3));
+          pk[c] = pack2<F16>(p0, p1);
+          pk[c + 1] = pack2<F16>(p2, p3);
+        }
+        float a0, a1;
+        f2_unpack(f2_add(rs0, rs1), a0, a1);
+        l = l * scale + (a0 + a1);
+        m_use = m_new;
+        // O_t is rescaled only when the reference maximum moved; PV_t(j-1) must have finished
+        // first. PV_t number i (running count over the CTA's items) completes phase i / 2 of
+        // barrier [t][i mod 2], and the parity names the phase exactly: every schedule has
+        // completed PV(k - 3), hence PV_t(j - 3), once S_t(j) is in TMEM, and PV_t(j + 1)
+        // cannot run before this thread publishes P_t(j).
+        if (j > 0 && __any_sync(0xffffffffu, scale != 1.f)) {
+          const int gp = pv_g + j - 1;
+          if (!mbar_wait_warp(smem_u32(&bars.o_done[t][gp & 1]), (gp >> 1) & 1, abort, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t sc2 = f2_pack(scale, scale);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            ATTN_TMEM_LD_X32(tOt + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float y0, y1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), sc2),
+                        y0, y1);
+              o[e] = __float_as_uint(y0);
+              o[e + 1] = __float_as_uint(y1);
+            }
+            ATTN_TMEM_ST_X32(tOt + c * 32, o);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) ATTN_TMEM_ST_X16(tSt + c * 16, (&pk[c * 16]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.p_full[bsel]));
+      }
+      // A tile without key tiles in this block waits here until the other tile's warps have
+      // seen all of the block's score tiles: its next wait, on the next block's score tile,
+      // is then at most one phase ahead of its buffer's barrier (a parity wait is exact only
+      // then; skipping the block alone could leave it further behind). Both tiles' warps
+      // arrive and wait (a bounded wait: a warpgroup that gave up leaves the other one free).
+      if (one_empty) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars.tsync));
+        ok = mbar_wait_warp(smem_u32(&bars.tsync), n_sync & 1, abort, p.timeout_ns) && ok;
+        ++n_sync;
+      }
+      if (n > 0 && ok) {
+        // PV_t(n-1) last. Its wait needs PV_t(n-3) complete, which S_t(n-1) in TMEM does not
+        // imply where the two issuing warps run one query tile's consecutive score tiles (it
+        // implies PV(k - 3) only); PV_t(n-2) first, whose wait needs PV_t(n-4) = PV(<= k - 3).
+        // No PV_t follows either (the next block's first PV_t needs this thread's next P), so
+        // neither barrier can run a phase ahead.
+        if (n > 1) {
+          const int gp = pv_g + n - 2;
+          ok = mbar_wait_warp(smem_u32(&bars.o_done[t][gp & 1]), (gp >> 1) & 1, abort, p.timeout_ns);
+        }
+        if (ok) {
+          const int gp = pv_g + n - 1;
+          ok = mbar_wait_warp(smem_u32(&bars.o_done[t][gp & 1]), (gp >> 1) & 1, abort, p.timeout_ns);
+        }
+        tc_fence_after();
+      }
+      if (ok) {
+        // the item's addresses, decoded again rather than held through the key loop
+        FwdItem w;
+        decode_item(item, w);
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const bool valid = row < w.sv.len_q;
+        const int64_t grow = w.sv.row0_q + row;
+        uint16_t* orow = p.o + w.sv.batch * p.o_sb + w.h * p.o_sh + grow * p.o_ss;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          ATTN_TMEM_LD_X32(tOt + c * 32, o);
+          if (n > 0) {
+            ATTN_TMEM_LD_X32(tOt + c * 32, o);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float y0, y1;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), sc2),
-                      y0, y1);
-            o[e] = __float_as_uint(y0);
-            o[e + 1] = __float_as_uint(y1);
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
           }
-          ATTN_TMEM_ST_X32(tOt + c * 32, o);
-        }
-      }
+          if (valid && c * 32 < p.d_out) {  // columns past the head size are zero padding
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) ATTN_TMEM_ST_X16(tSt + c * 16, (&pk[c * 16]));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars.p_full[bsel]));
-    }
-    if (n > 0) {
-      // PV_t(n-1) last. Its wait needs PV_t(n-3) complete, which S_t(n-1) in TMEM does not
-      // imply where the two issuing warps run one query tile's consecutive score tiles (it
-      // implies PV(k - 3) only); PV_t(n-2) first, whose wait needs PV_t(n-4) = PV(<= k - 3).
-      // No PV_t follows either, so neither barrier can run a phase ahead.
-      if (ok && n > 1)
-        ok = mbar_wait(smem_u32(&bars.o_done[t][(n - 2) & 1]), ((n - 2) >> 1) & 1, abort,
-                       p.timeout_ns);
-      if (ok) ok = mbar_wait(smem_u32(&bars.o_done[t][(n - 1) & 1]), ((n - 1) >> 1) & 1, abort,
-                             p.timeout_ns);
-      tc_fence_after();
-    }
-    if (ok) {
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const bool valid = row < sv.len_q;
-      const int64_t grow = sv.row0_q + row;
-      uint16_t* orow = p.o + sv.batch * p.o_sb + h * p.o_sh + grow * p.o_ss;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        if (n > 0) {
-          ATTN_TMEM_LD_X32(tOt + c * 32, o);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (valid && c * 32 < p.d_out) {  // columns past the head size are zero padding
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 v;
-            v.x = pack2<F16>(__uint_as_float(o[e + 0]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
-            v.y = pack2<F16>(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
-            v.z = pack2<F16>(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l);
-            v.w = pack2<F16>(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+            for (int e = 0; e < 32; e += 8) {
+              uint4 v;
+              v.x = pack2<F16>(__uint_as_float(o[e + 0]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
+              v.y = pack2<F16>(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+              v.z = pack2<F16>(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l);
+              v.w = pack2<F16>(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+            }
           }
         }
+        if (valid)
+          p.lse[w.sv.batch * p.l_sb + w.h * p.l_sh + grow * p.l_ss] =
+              (l > 0.f) ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
-      if (valid)
-        p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] =
-            (l > 0.f) ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      s_g += order.total;
+      pv_g += n;
     }
   }
 

@@ -73,6 +73,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait for a whole warp that goes on to warp-collective instructions (tcgen05.ld/st with
+// .sync.aligned): the lanes agree on the outcome, so that a wait that gave up in one lane
+// while the phase completed for another cannot split the warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               uint64_t timeout_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, timeout_ns));
+}
+
 // Bounded wait that ignores the abort flag: used when a role leaves (normally or after a wait
 // gave up) to let its own asynchronous copies or products finish, so that nothing still
 // writes shared memory or tensor memory once the CTA exits. Returns false on timeout.
@@ -101,6 +109,33 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Work stealing across a grid (sm_100 and later): a running CTA asks the hardware to cancel
+// the launch of a CTA of the same grid that has not started yet; the 16-byte response lands
+// in shared memory and completes 16 bytes of transactions on the mbarrier given (whose
+// expected count the caller raises by 16 first). After a response that cancelled nothing no
+// further request may be made.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+// The x index of the CTA a landed response cancelled, or -1 if it cancelled none.
+__device__ __forceinline__ int clc_cancelled_x(uint32_t resp) {
+  int x = -1;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%1];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "+r"(x)
+      : "r"(resp)
+      : "memory");
+  return x;
 }
 
 // Prefetch of a 4-D tile into L2 (no shared memory, no completion to wait for): a later load

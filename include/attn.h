@@ -59,11 +59,14 @@
  * workspace is allocated, and attn_read_device_status clears it after reading. A sequence
  * whose cu_seqlens are inconsistent is skipped, never read out of bounds.
  *
- * Environment. The library reads three variables, none needed in normal use:
- *   ATTN_GRID_ORDER="<kernel>:tile|seq[,...]" forces the CTA order of a kernel's causal grids
- *     (kernel = fwd, bwd_main, bwd_main_nodq or bwd_dq); otherwise the order comes from a
- *     table measured on GB300 (the sweep that writes the table sets it). Results do not
- *     depend on the order.
+ * Environment. The library reads these variables, none needed in normal use:
+ *   ATTN_GRID_ORDER="<kernel>:tile|seq|g<N>[,...]" forces the CTA order of a kernel's causal
+ *     grids (kernel = fwd, bwd_main, bwd_main_nodq or bwd_dq; g<N>: groups of N (unit, head)
+ *     pairs); otherwise the order comes from a table measured on GB300 (the sweep that
+ *     writes the table sets it). Results do not depend on the order.
+ *   ATTN_FWD_PERSISTENT=0|1 forces the forward grid to one CTA per query block (0) or to a
+ *     persistent grid of one CTA per SM walking the blocks (1); ATTN_FWD_CTAS=n launches n
+ *     persistent CTAs. Results do not depend on the grid.
  *   ATTN_TEST_WITHHOLD_KV_TILE=j / ATTN_TEST_WITHHOLD_Q_STEP=i (failure-detection tests):
  *     the forward loads no key tile from j on / the backward skips query step i, and every
  *     wait gives up after 50 ms, so the call ends with ATTN_ERR_DEVICE_TIMEOUT in the status

