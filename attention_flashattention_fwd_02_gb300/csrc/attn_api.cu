@@ -364,6 +364,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   if ((s = make_map(&p.tm_q, q, fwd_box_rows())) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_k, k, 128)) != ATTN_OK) return s;
   if ((s = make_map(&p.tm_v, v, 128)) != ATTN_OK) return s;
+  if ((s = make_map(&p.tm_o, o, 32)) != ATTN_OK) return s;
   if (bias != nullptr) {
     if ((s = make_map(&p.tm_b, bias, 128)) != ATTN_OK) return s;
     p.bias_b_bcast = bias->size[0] == 1 && pr.units > 1;

@@ -76,6 +76,7 @@ __device__ __forceinline__ GridPos grid_pos(int linear, int tiles, int uh, int g
 
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;   // 4-D (D, S, H, B) 16-bit, box (64, 128, 1, 1), SW128
+  CUtensorMap tm_o;               // O, box (64, 32, 1, 1), SW128: the staged epilogue's stores
   CUtensorMap tm_b;               // bias kernels only: 4-D (Sk, Sq, Hb, Bb), box (64, 128, 1, 1)
   int bias_b_bcast, bias_h_bcast; // bias broadcast over batch / head (size-1 dimension)
   uint16_t* o;                    // bf16 or fp16 elements (the kernel's element type)

@@ -75,7 +75,14 @@ struct FwdCfg {
   static constexpr int OFF_K = NQ * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
   static constexpr int OFF_B = OFF_V + NST * KV_BYTES;
-  static constexpr int SMEM_BYTES = OFF_B + NBS * B_BYTES + 1024;  // + alignment slack
+  // Epilogue staging (where shared memory has room: not with a bias): each softmax warp owns
+  // OST_SLABS slabs of 32 rows x 64 columns (4 KB, 128-byte swizzle) that it fills from TMEM
+  // and copies out with TMA stores.
+  static constexpr int OST_SLABS = (D == 256) ? 2 : 1;
+  static constexpr int OST_W_BYTES = OST_SLABS * 4096;
+  static constexpr int OFF_OST = OFF_B + NBS * B_BYTES;
+  static constexpr bool O_TMA = !BIAS;
+  static constexpr int SMEM_BYTES = OFF_OST + (O_TMA ? NQ * 4 * OST_W_BYTES : 0) + 1024;
   static constexpr int NSB = (D == 64) ? 3 : 2;  // rotating score / P buffers
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O0 = NSB * 128, COL_O1 = NSB * 128 + (NQ == 2 ? D : 0);
@@ -760,6 +767,49 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
         const bool valid = row < w.sv.len_q;
         const int64_t grow = w.sv.row0_q + row;
         uint16_t* orow = p.o + w.sv.batch * p.o_sb + w.h * p.o_sh + grow * p.o_ss;
+        // A query tile wholly inside its sequence leaves through shared memory: each warp
+        // writes its 32 rows as 64-column slabs (128-byte swizzle) and one lane copies each
+        // slab out with a TMA store, whole 128-byte rows at a time (row-per-thread global
+        // stores write 16 bytes into each of 32 rows per instruction). A tile reaching past
+        // the sequence's end is stored row by row: a copy would also write the rows past the
+        // end (the next sequence's, in a compact batch). The condition is the same for the
+        // whole warpgroup.
+        const bool staged = C::O_TMA && n > 0 && q_lo + BM <= w.sv.len_q;
+        if (staged) {
+          uint8_t* region = smem + C::OFF_OST + (t * 4 + (warp & 3)) * C::OST_W_BYTES;
+          const int row_w = w.sv.row0_q + q_lo + (warp & 3) * 32;  // first row of this warp
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            const int sub = h % C::OST_SLABS;
+            uint32_t o[64];
+            ATTN_TMEM_LD2_X32(tOt + 64 * h, tOt + 64 * h + 32, o, (o + 32));
+            if (sub == 0) {  // this warp's earlier copies out of the region have read it
+              if (lane == 0) bulk_wait_group_read0();
+              __syncwarp();
+            }
+            uint8_t* slab = region + sub * 4096 + lane * 128;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              uint4 v;
+              v.x = pack2<F16>(__uint_as_float(o[8 * e + 0]) * inv_l, __uint_as_float(o[8 * e + 1]) * inv_l);
+              v.y = pack2<F16>(__uint_as_float(o[8 * e + 2]) * inv_l, __uint_as_float(o[8 * e + 3]) * inv_l);
+              v.z = pack2<F16>(__uint_as_float(o[8 * e + 4]) * inv_l, __uint_as_float(o[8 * e + 5]) * inv_l);
+              v.w = pack2<F16>(__uint_as_float(o[8 * e + 6]) * inv_l, __uint_as_float(o[8 * e + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(slab + ((e ^ (lane & 7)) << 4)) = v;
+            }
+            if (sub == C::OST_SLABS - 1 || h == D / 64 - 1) {
+              fence_proxy_async_smem();  // the slabs, written by this warp, to the copy engine
+              __syncwarp();
+              if (lane == 0) {
+#pragma unroll
+                for (int s2 = 0; s2 <= sub; ++s2)
+                  tma_store_4d(&p.tm_o, smem_u32(region + s2 * 4096), (h - sub + s2) * 64, row_w,
+                               w.h, w.sv.batch);
+                bulk_commit_group();
+              }
+            }
+          }
+        } else {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -781,6 +831,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
             }
           }
         }
+        }
         if (valid)
           p.lse[w.sv.batch * p.l_sb + w.h * p.l_sh + grow * p.l_ss] =
               (l > 0.f) ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -788,6 +839,8 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       s_g += order.total;
       pv_g += n;
     }
+    // the staged epilogue's copies have completed (they read shared memory)
+    if (C::O_TMA && lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
