@@ -305,6 +305,25 @@ int fwd_grid_size(int n_items, int* clc) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace header shared by the forward and backward calls: the status word at offset 0 and,
+// at kSplitCntOff, the forward's split-block counters (each back at zero when its call ends;
+// no backward kernel writes the header, so one workspace can serve both passes).
+constexpr size_t kFwdMinWorkspace = 256;  // the forward's status word (and alignment room)
+constexpr size_t kWsHeader = 2048;
+constexpr size_t kSplitCntOff = 1024;
+constexpr int kSplitMaxBlocks = 256;  // a split grid has fewer blocks than SMs
+
+// Bytes of one partial-result slot of a split forward grid (FwdCfg::SLOT_FLOATS floats).
+size_t fwd_split_slot_bytes(int width) {
+  return (size_t)fwd_block_m(width, false) * (size_t)(width + 2) * 4;
+}
+// Workspace a split forward grid over n_items blocks needs (0: none can split): the header
+// and one slot per (block, CTA) pair that can hold a part.
+size_t fwd_split_ws_bytes(int64_t n_items, int width) {
+  if (n_items <= 0 || n_items >= kSplitMaxBlocks) return 0;
+  return kWsHeader + (size_t)(n_items + kSplitMaxBlocks) * fwd_split_slot_bytes(width);
+}
+
 struct BwdWorkspace {
   size_t delta_off, dq_off, total;
 };
@@ -312,7 +331,7 @@ struct BwdWorkspace {
 BwdWorkspace bwd_layout(int64_t B, int64_t H, int64_t rows, int64_t D) {
   BwdWorkspace w;
   const size_t n = (size_t)(B > 0 ? B : 0) * (size_t)(H > 0 ? H : 0) * (size_t)(rows > 0 ? rows : 0);
-  w.delta_off = 256;
+  w.delta_off = kWsHeader;
   w.dq_off = w.delta_off + align256(n * 4);
   w.total = w.dq_off + n * (size_t)D * 4;
   return w;
@@ -352,8 +371,7 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   if (!same_dtype(q, o)) return ATTN_ERR_DTYPE;
   if ((s = check_lse(lse, pr)) != ATTN_OK) return s;
   if (!valid_scale(sm_scale)) return ATTN_ERR_UNSUPPORTED;
-  if (ws != nullptr && ws_bytes < attn_fwd_workspace_size(pr.B, pr.H, pr.Sq, pr.D))
-    return ATTN_ERR_WORKSPACE;
+  if (ws != nullptr && ws_bytes < kFwdMinWorkspace) return ATTN_ERR_WORKSPACE;
   if (ws != nullptr && reinterpret_cast<uintptr_t>(ws) % 16 != 0) return ATTN_ERR_ALIGN;
   if ((s = check_device()) != ATTN_OK) return s;
   if (pr.units == 0 || pr.max_q == 0 || pr.H == 0) return ATTN_OK;
@@ -393,7 +411,30 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   p.uh = uh;
   if ((int64_t)n_blk * uh > kMaxI32) return ATTN_ERR_UNSUPPORTED;  // 1-D grid
   const int n_items = n_blk * uh;
-  const dim3 grid((unsigned)fwd_grid_size(n_items, &p.clc));
+  dim3 grid((unsigned)fwd_grid_size(n_items, &p.clc));
+  // At most half as many blocks as SMs (non-causal, dense, no bias): cut the (block, key
+  // tile) units into one equal range per SM, given the workspace for the partial results.
+  // With more blocks the partial results cost more than the idle SMs (measured on GB300).
+  // ATTN_FWD_SPLIT=0 turns it off, =1 splits any grid with fewer blocks than SMs.
+  const int sms = sm_count();
+  const int64_t nk = ((int64_t)pr.max_k + 127) / 128;
+  const size_t split_need = fwd_split_ws_bytes(n_items, kernel_width(pr.D));
+  const char* sv = getenv("ATTN_FWD_SPLIT");
+  const bool split_on = sv == nullptr ? 2 * n_items <= sms : atoi(sv) != 0;
+  if (!causal && bias == nullptr && pr.mode == kDense && sms > n_items && nk >= 2 &&
+      split_need > 0 && ws != nullptr && ws_bytes >= split_need && split_on) {
+    const int64_t units = (int64_t)n_items * nk;
+    const int G = units < sms ? (int)units : sms;
+    if (G > n_items) {
+      p.split = 1;
+      p.nk = (int)nk;
+      p.n_units = units;
+      p.part_cnt = reinterpret_cast<int*>(static_cast<char*>(ws) + kSplitCntOff);
+      p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+      p.clc = 0;
+      grid = dim3((unsigned)G);
+    }
+  }
   p.d_out = pr.D;
   cudaError_t e = launch_attn_fwd(p, kernel_width(pr.D), pr.f16, bias != nullptr, grid,
                                   reinterpret_cast<cudaStream_t>(stream));
@@ -656,8 +697,12 @@ attn_status bwd_check_args(const attn_tensor4* q, const attn_tensor4* k, const a
 extern "C" {
 
 size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D) {
-  (void)B; (void)H; (void)Sq; (void)D;
-  return 256;
+  if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0) return kFwdMinWorkspace;
+  const int width = kernel_width((int)D);
+  const int rows = fwd_block_m(width, false);
+  const int64_t n_items = B * H * ((Sq + rows - 1) / rows);
+  const size_t split = fwd_split_ws_bytes(n_items, width);
+  return split > kFwdMinWorkspace ? split : kFwdMinWorkspace;
 }
 
 size_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D) {

@@ -91,6 +91,14 @@ struct FwdParams {
   int withhold_tile;              // test hook: key tile the producer never loads (-1: none)
   int tiles, group;               // query blocks per (unit, head) pair; CTA-order group size
   int uh;                         // (unit, head) pairs: work items = uh * tiles
+  int split;                      // 1: non-causal dense grid with fewer blocks than SMs; the
+                                  // (block, key tile) units are cut into gridDim.x equal
+                                  // ranges, one per CTA, and blocks split over several CTAs
+                                  // merge their partial results
+  int nk;                         // split: key tiles per block
+  int64_t n_units;                // split: blocks x nk
+  float* part;                    // split: partial-result slots (one per (block, CTA) pair)
+  int* part_cnt;                  // split: parts of each block done (returns to 0)
   int clc;                        // 1: one CTA per item, CTAs steal the items of CTAs not yet
                                   // launched (cluster launch control); 0: CTA c takes items
                                   // c, c + gridDim.x, ...

@@ -83,6 +83,10 @@ struct FwdCfg {
   static constexpr int OFF_OST = OFF_B + NBS * B_BYTES;
   static constexpr bool O_TMA = !BIAS;
   static constexpr int SMEM_BYTES = OFF_OST + (O_TMA ? NQ * 4 * OST_W_BYTES : 0) + 1024;
+  // Split grids: one partial-result slot holds O (unnormalised, fp32, as [D / 4][NQ * BM][4]:
+  // a warp's 32 rows of 4 columns are 512 contiguous bytes) and the rows' running maximum and
+  // sum.
+  static constexpr int SLOT_FLOATS = NQ * BM * (D + 2);
   static constexpr int NSB = (D == 64) ? 3 : 2;  // rotating score / P buffers
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O0 = NSB * 128, COL_O1 = NSB * 128 + (NQ == 2 ? D : 0);
@@ -102,7 +106,8 @@ template <int NST, int NSB>
 struct FwdBars {
   alignas(16) uint4 clc_resp[NCLC];      // work-stealing responses (cluster launch control)
   uint64_t clc_full[NCLC], clc_empty[NCLC];
-  uint64_t tsync;         // the query tiles' warps meet (a block with one tile past the end)
+  uint64_t tsync;         // the softmax warps meet (a block with one tile past the end; the
+                          // parts of a block split over CTAs)
   uint64_t q_full;
   uint64_t q_empty;       // the score products of a block have read Q (persistent grids)
   uint64_t k_full[NST], v_full[NST], kv_empty[NST];
@@ -113,6 +118,7 @@ struct FwdBars {
   uint64_t mma_drain[2];           // completion of each issuing warp's last products
   uint32_t tmem_base;
   int abort;
+  int merge_last;  // split grids: this CTA finished a block's last part and merges its parts
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -145,9 +151,11 @@ struct FwdItem {
   SeqView sv;
   int z, h, blk_lo;
   int q_lo[2], q_hi[2], n_t[2], n_max;
+  int j0;        // first key tile (a split grid's segment of the key range; else 0)
+  bool partial;  // the segment is not the whole key range: the epilogue merges partial results
 };
 
-template <int D, bool F16, bool BIAS>
+template <int D, bool F16, bool BIAS, bool SPLIT>
 __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, BIAS>;
@@ -167,6 +175,14 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
   // its own: the next block's first PV_t waits for P_t(0), which tile t's warps publish only
   // after their epilogue has read O_t.
   const int n_items = p.uh * p.tiles;
+  // Split grid (p.split): the units (item, key tile) of all items, item-major, are cut into
+  // gridDim.x equal ranges, one per CTA; a CTA's items are the ones its range meets, each over
+  // the part of the key range inside the range.
+  // (computed where used: a first item held in a register from here on measured 2-3 % slower
+  // in the unsplit kernels)
+  auto u_lo = [&]() { return (int64_t)blockIdx.x * p.n_units / gridDim.x; };
+  auto u_hi = [&]() { return ((int64_t)blockIdx.x + 1) * p.n_units / gridDim.x; };
+  auto first_item = [&]() { return SPLIT ? (int)(u_lo() / p.nk) : (int)blockIdx.x; };
   // Readers of each work-stealing response (one arrival each on its slot's empty barrier):
   // the MMA and S issuers, the V and bias producers, each softmax warp. The producer, which
   // makes the requests, reads each response before it reuses the slot.
@@ -177,6 +193,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
   // the responses this role has read: response ci sits in slot ci mod NCLC, phase
   // (ci / NCLC) mod 2 of its full barrier.
   auto next_item = [&](int item, int& ci, int who) -> int {
+    if (SPLIT) return (int64_t)(item + 1) * p.nk < u_hi() ? item + 1 : -1;
     if (!p.clc) return item + (int)gridDim.x < n_items ? item + (int)gridDim.x : -1;
     const int slot = ci % NCLC;
     const uint32_t full = smem_u32(&bars.clc_full[slot]);
@@ -208,6 +225,17 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       w.q_hi[t] = t < C::NQ ? min(w.q_lo[t] + BM, w.sv.len_q) : w.q_lo[t];
       w.n_t[t] = key_tiles(w.q_lo[t], w.q_hi[t], w.sv.len_k, p.causal, BN);
     }
+    w.j0 = 0;
+    w.partial = false;
+    if (SPLIT) {  // non-causal dense grids: every tile of the block has the nk key tiles
+      const int64_t base = (int64_t)item * p.nk;
+      const int j_lo = (int)(max(u_lo(), base) - base);
+      const int j_hi = (int)(min(u_hi(), base + p.nk) - base);
+      w.j0 = j_lo;
+      w.partial = j_lo > 0 || j_hi < p.nk;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) w.n_t[t] = w.n_t[t] > 0 ? j_hi - j_lo : 0;
+    }
     w.n_max = max(w.n_t[0], w.n_t[1]);
     return true;
   };
@@ -223,7 +251,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       mbar_init(smem_u32(&bars.clc_full[i]), 1);
       mbar_init(smem_u32(&bars.clc_empty[i]), CLC_READERS);
     }
-    mbar_init(smem_u32(&bars.tsync), 8);
+    mbar_init(smem_u32(&bars.tsync), 4 * C::NQ);
     mbar_init(smem_u32(&bars.q_full), 1);
     mbar_init(smem_u32(&bars.q_empty), 1);
     for (int s = 0; s < NST; ++s) {
@@ -268,7 +296,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       for (int st = 0; st < NST; ++st) last_g[st] = -1;
       bool go = true;
       int ci = 0, issued = 0;  // work-stealing responses read, requests made
-      for (int item = blockIdx.x; go && item >= 0;
+      for (int item = first_item(); go && item >= 0;
            item = go ? next_item(item, ci, kProducer) : -1) {
         if (p.clc) {
           // request the item after this one now, so that the answer is in when this one ends;
@@ -309,7 +337,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
             break;
           }
           last_g[st] = g;
-          const int krow = w.sv.row0_k + j * BN;
+          const int krow = w.sv.row0_k + ((SPLIT ? w.j0 : 0) + j) * BN;
           const uint32_t kb = smem_u32(&bars.k_full[st]);
           mbar_arrive_expect_tx(kb, C::KV_BYTES);
 #pragma unroll
@@ -363,7 +391,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       for (int st = 0; st < NST; ++st) last_g[st] = -1;
       bool go = true;
       int ci = 0;
-      for (int item = blockIdx.x; go && item >= 0; item = go ? next_item(item, ci, kLane) : -1) {
+      for (int item = first_item(); go && item >= 0; item = go ? next_item(item, ci, kLane) : -1) {
         FwdItem w;
         if (!decode_item(item, w) || w.n_max == 0) continue;
         for (int j = 0; j < w.n_max; ++j) {
@@ -380,11 +408,13 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
 #pragma unroll
           for (int s = 0; s < D / 64; ++s)
             tma_load_4d(sV + st * C::KV_BYTES + s * BN * 128, &p.tm_v, vb, s * 64,
-                        w.sv.row0_k + j * BN, w.h, w.sv.batch);
+                        w.sv.row0_k + ((SPLIT ? w.j0 : 0) + j) * BN, w.h, w.sv.batch);
           if (j + NST < w.n_max && j + NST != p.withhold_tile) {
 #pragma unroll
             for (int s = 0; s < D / 64; ++s)
-              tma_prefetch_l2_4d(&p.tm_v, s * 64, w.sv.row0_k + (j + NST) * BN, w.h, w.sv.batch);
+              tma_prefetch_l2_4d(&p.tm_v, s * 64,
+                                 w.sv.row0_k + ((SPLIT ? w.j0 : 0) + j + NST) * BN, w.h,
+                                 w.sv.batch);
           }
         }
         kv_g += w.n_max;
@@ -411,7 +441,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       int last_ph[2] = {-1, -1};  // last phase loaded into each slot
       bool go = true;
       int ci = 0;
-      for (int item = blockIdx.x; go && item >= 0; item = go ? next_item(item, ci, kLane) : -1) {
+      for (int item = first_item(); go && item >= 0; item = go ? next_item(item, ci, kLane) : -1) {
         FwdItem w;
         if (!decode_item(item, w) || w.n_max == 0) continue;
         const ScoreOrder order(w.n_t[0], w.n_t[1]);
@@ -429,7 +459,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
           mbar_arrive_expect_tx(bf, C::B_BYTES);
 #pragma unroll
           for (int s = 0; s < 2; ++s)
-            tma_load_4d(sB + slot * C::B_BYTES + s * BM * 128, &p.tm_b, bf, j * BN + s * 64,
+            tma_load_4d(sB + slot * C::B_BYTES + s * BM * 128, &p.tm_b, bf, ((SPLIT ? w.j0 : 0) + j) * BN + s * 64,
                         w.q_lo[t], hb, bb);
           last_ph[slot] = ph;
         }
@@ -454,7 +484,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     int k_seen = -1, v_seen = -1;    // key tiles (running count) whose K / V were seen full
     bool ok = true;
     int ci = 0;
-    for (int item = blockIdx.x; ok && item >= 0; item = ok ? next_item(item, ci, kWarp) : -1) {
+    for (int item = first_item(); ok && item >= 0; item = ok ? next_item(item, ci, kWarp) : -1) {
       FwdItem w;
       if (!decode_item(item, w) || w.n_max == 0) continue;
       const ScoreOrder order(w.n_t[0], w.n_t[1]);
@@ -533,7 +563,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     int k_seen = -1;  // key tile (running count) whose K stage was last seen full
     bool ok = true;
     int ci = 0;
-    for (int item = blockIdx.x; ok && item >= 0; item = ok ? next_item(item, ci, kWarp) : -1) {
+    for (int item = first_item(); ok && item >= 0; item = ok ? next_item(item, ci, kWarp) : -1) {
       FwdItem w;
       if (!decode_item(item, w) || w.n_max == 0) continue;
       const ScoreOrder order(w.n_t[0], w.n_t[1]);
@@ -582,9 +612,18 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
     const float c2 = p.scale_log2;
     int s_g = 0, pv_g = 0;  // score tiles of earlier items; PVs of this query tile in them
     bool ok = true;
-    int ci = 0, n_sync = 0;  // work-stealing responses read; meetings of the two query tiles
-    for (int item = blockIdx.x; ok && item >= 0; item = ok ? next_item(item, ci, kWarp) : -1) {
-      int q_lo, n, len_k;
+    int ci = 0, n_sync = 0;  // work-stealing responses read; meetings of the softmax warps
+    // every softmax warp of the CTA meets here (a bounded wait: a warp that gave up leaves
+    // the others free); false when the wait gave up
+    auto tile_meet = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars.tsync));
+      const bool met = mbar_wait_warp(smem_u32(&bars.tsync), n_sync & 1, abort, p.timeout_ns);
+      ++n_sync;
+      return met;
+    };
+    for (int item = first_item(); ok && item >= 0; item = ok ? next_item(item, ci, kWarp) : -1) {
+      int q_lo, n, len_k, j0;
       bool one_empty;  // a query block with one tile past the sequence's end
       ScoreOrder order(0, 0);
       {
@@ -605,6 +644,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       q_lo = t ? w.q_lo[1] : w.q_lo[0];
       n = t ? w.n_t[1] : w.n_t[0];
       len_k = w.sv.len_k;
+      j0 = SPLIT ? w.j0 : 0;
       one_empty = C::NQ == 2 && min(w.n_t[0], w.n_t[1]) == 0;
       }
       const int row = q_lo + r;  // local query index
@@ -652,7 +692,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
         }
         // with a bias the scores are already scaled
         const float cs = BIAS ? 1.f : c2;
-        const int k0 = j * BN;
+        const int k0 = (j0 + j) * BN;
         if (k0 + BN > len_k || (p.causal && k0 + BN - 1 > q_lo)) {
           const int kmax = p.causal ? min(row, len_k - 1) : len_k - 1;
 #pragma unroll
@@ -737,12 +777,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       // is then at most one phase ahead of its buffer's barrier (a parity wait is exact only
       // then; skipping the block alone could leave it further behind). Both tiles' warps
       // arrive and wait (a bounded wait: a warpgroup that gave up leaves the other one free).
-      if (one_empty) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars.tsync));
-        ok = mbar_wait_warp(smem_u32(&bars.tsync), n_sync & 1, abort, p.timeout_ns) && ok;
-        ++n_sync;
-      }
+      if (one_empty) ok = tile_meet() && ok;
       if (n > 0 && ok) {
         // PV_t(n-1) last. Its wait needs PV_t(n-3) complete, which S_t(n-1) in TMEM does not
         // imply where the two issuing warps run one query tile's consecutive score tiles (it
@@ -763,10 +798,119 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
         // the item's addresses, decoded again rather than held through the key loop
         FwdItem w;
         decode_item(item, w);
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         const bool valid = row < w.sv.len_q;
         const int64_t grow = w.sv.row0_q + row;
         uint16_t* orow = p.o + w.sv.batch * p.o_sb + w.h * p.o_sh + grow * p.o_ss;
+        if (SPLIT && w.partial) {
+          // A part of a block split over CTAs: this part's unnormalised O and row statistics
+          // go to its slot (one per (block, CTA) pair); the CTA that completes the block's
+          // last part merges all parts, in part order, so that the result does not depend on
+          // which CTA finishes last.
+          constexpr int RB = C::NQ * BM;  // rows of a block
+          const int rr = t * BM + r;
+          const int64_t U = p.n_units;
+          const int G = (int)gridDim.x;
+          // CTA whose range holds unit u: the largest c with floor(c U / G) <= u
+          auto cta_of = [&](int64_t u) { return (int)(((u + 1) * G - 1) / U); };
+          const int c_first = cta_of((int64_t)item * p.nk);
+          const int c_last = cta_of((int64_t)(item + 1) * p.nk - 1);
+          float* own = p.part + (size_t)(item + blockIdx.x) * C::SLOT_FLOATS;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            if (n > 0) {
+              ATTN_TMEM_LD_X32(tOt + c * 32, o);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(own + ((c * 32 + e) / 4 * RB + rr) * 4) =
+                  make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                              __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+          }
+          own[D * RB + rr] = m_use;
+          own[(D + 1) * RB + rr] = l;
+          __threadfence();
+          ok = tile_meet();  // every row of this part is written
+          if (ok && threadIdx.x == 0) {
+            const int done = atomicAdd(p.part_cnt + item, 1);
+            bars.merge_last = done == c_last - c_first;
+            if (done == c_last - c_first) p.part_cnt[item] = 0;  // zero again for the next call
+          }
+          ok = ok && tile_meet();
+          if (ok && bars.merge_last) {
+            __threadfence();
+            float mx = -INFINITY;
+            for (int c2 = c_first; c2 <= c_last; ++c2) {
+              const float* sl = p.part + (size_t)(item + c2) * C::SLOT_FLOATS;
+              mx = fmaxf(mx, c2 == (int)blockIdx.x ? m_use : __ldcg(sl + D * RB + rr));
+            }
+            // part c2's weight: 2^(m - mx)
+            auto part_scale = [&](int c2, float& lp) {
+              const float* sl = p.part + (size_t)(item + c2) * C::SLOT_FLOATS;
+              const bool me = c2 == (int)blockIdx.x;
+              const float mp = me ? m_use : __ldcg(sl + D * RB + rr);
+              lp = me ? l : __ldcg(sl + (D + 1) * RB + rr);
+              return mp == -INFINITY ? 0.f : ex2_approx(mp - mx);
+            };
+            float lsum = 0.f;
+            for (int c2 = c_first; c2 <= c_last; ++c2) {
+              float lp;
+              const float sc = part_scale(c2, lp);
+              lsum += sc * lp;
+            }
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              float acc[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+              for (int c2 = c_first; c2 <= c_last; ++c2) {
+                float lp;
+                const float sc = part_scale(c2, lp);
+                if (c2 == (int)blockIdx.x) {
+                  uint32_t o[32];
+                  if (n > 0) {
+                    ATTN_TMEM_LD_X32(tOt + c * 32, o);
+                  } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                  }
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) acc[e] += sc * __uint_as_float(o[e]);
+                } else {
+                  const float* sl = p.part + (size_t)(item + c2) * C::SLOT_FLOATS;
+#pragma unroll
+                  for (int e = 0; e < 32; e += 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4*>(
+                        sl + ((c * 32 + e) / 4 * RB + rr) * 4));
+                    acc[e] += sc * x.x;
+                    acc[e + 1] += sc * x.y;
+                    acc[e + 2] += sc * x.z;
+                    acc[e + 3] += sc * x.w;
+                  }
+                }
+              }
+              if (valid && c * 32 < p.d_out) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                  uint4 v;
+                  v.x = pack2<F16>(acc[e + 0] * inv, acc[e + 1] * inv);
+                  v.y = pack2<F16>(acc[e + 2] * inv, acc[e + 3] * inv);
+                  v.z = pack2<F16>(acc[e + 4] * inv, acc[e + 5] * inv);
+                  v.w = pack2<F16>(acc[e + 6] * inv, acc[e + 7] * inv);
+                  *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+                }
+              }
+            }
+            if (valid)
+              p.lse[w.sv.batch * p.l_sb + w.h * p.l_sh + grow * p.l_ss] =
+                  lsum > 0.f ? (mx + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+          }
+        } else {
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         // A query tile wholly inside its sequence leaves through shared memory: each warp
         // writes its 32 rows as 64-column slabs (128-byte swizzle) and one lane copies each
         // slab out with a TMA store, whole 128-byte rows at a time (row-per-thread global
@@ -835,6 +979,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
         if (valid)
           p.lse[w.sv.batch * p.l_sb + w.h * p.l_sh + grow * p.l_ss] =
               (l > 0.f) ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
       }
       s_g += order.total;
       pv_g += n;
@@ -852,19 +997,19 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
   if (threadIdx.x == 0 && bars.abort && p.status != nullptr) atomicCAS(p.status, 0, kStatusTimeout);
 }
 
-template <int D, bool F16, bool BIAS>
+template <int D, bool F16, bool BIAS, bool SPLIT = false>
 static cudaError_t launch_fwd_impl(const FwdParams& p, dim3 grid, cudaStream_t stream) {
   using C = FwdCfg<D, BIAS>;
   static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F16, BIAS>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F16, BIAS, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
-  attn_fwd_kernel<D, F16, BIAS><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
+  attn_fwd_kernel<D, F16, BIAS, SPLIT><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -890,6 +1035,16 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3
     if (D != 64) return cudaErrorInvalidValue;
     return f16 ? launch_fwd_impl<64, true, true>(p, grid, stream)
                : launch_fwd_impl<64, false, true>(p, grid, stream);
+  }
+  if (p.split) {  // split grids (no bias): their own instantiations
+    if (D == 256)
+      return f16 ? launch_fwd_impl<256, true, false, true>(p, grid, stream)
+                 : launch_fwd_impl<256, false, false, true>(p, grid, stream);
+    if (D == 128)
+      return f16 ? launch_fwd_impl<128, true, false, true>(p, grid, stream)
+                 : launch_fwd_impl<128, false, false, true>(p, grid, stream);
+    return f16 ? launch_fwd_impl<64, true, false, true>(p, grid, stream)
+               : launch_fwd_impl<64, false, false, true>(p, grid, stream);
   }
   return launch_fwd_dispatch<false>(p, D, f16, grid, stream);
 }

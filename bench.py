@@ -177,7 +177,9 @@ def run_ours(args, rank, world, dist, clocks_on=True):
         o = torch.empty(q.shape, dtype=q.dtype, device=dev)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws = torch.zeros(_lib.attn_bwd_workspace_size(*q.shape), dtype=torch.uint8, device=dev)
+        # one workspace serves both passes (the forward's needs room for split-grid partials)
+        ws = torch.zeros(max(_lib.attn_bwd_workspace_size(*q.shape),
+                             _lib.attn_fwd_workspace_size(*q.shape)), dtype=torch.uint8, device=dev)
         compact = wl.layout == "compact"
         padded = wl.layout == "padded"
         cu_q = g.get("cu_seqlens_q")

@@ -248,3 +248,73 @@ def test_withheld_tile_with_stealing():
     o, lse = _fwd({}, {"q": q, "k": k, "v": v}, c, True)
     o_r, lse_r = ref.fwd_bhsd(np64(q[:, :2]), np64(k[:, :2]), np64(v[:, :2]), c, True)
     assert_fwd_close(o[:, :2], lse[:, :2], o_r, lse_r, what="stealing after timeout")
+
+
+def _fwd_ws(g, c, causal, ws, env=None):
+    """Forward with the given workspace; the split grid forced on (ATTN_FWD_SPLIT=1: every
+    grid with fewer blocks than SMs) unless env says otherwise."""
+    env = {"ATTN_FWD_SPLIT": "1"} if env is None else env
+    old = {n: os.environ.pop(n, None) for n in ("ATTN_FWD_SPLIT",)}
+    os.environ.update(env)
+    try:
+        o = torch.full_like(g["q"], float("nan"))
+        lse = torch.full(g["q"].shape[:3], float("nan"), device=DEV)
+        forward(g["q"], g["k"], g["v"], c, causal, out=o, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        assert _lib.attn_read_device_status(ws) == 0
+        return o, lse
+    finally:
+        for n in env:
+            os.environ.pop(n, None)
+        os.environ.update({n: v for n, v in old.items() if v is not None})
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,D,dtype,seed", [
+    (2, 16, 1024, 4096, 128, torch.bfloat16, 429),   # the cross-length workload: 128 blocks
+    (1, 4, 1000, 3000, 64, torch.bfloat16, 365),     # 16 blocks, ragged key tail, long parts
+    (1, 2, 512, 4096, 256, torch.bfloat16, 657),     # d_head 256: 8 blocks of 128 rows
+    (1, 3, 300, 2000, 96, torch.float16, 397),       # d_head 96, a block with an empty tile
+    (1, 1, 128, 256, 128, torch.bfloat16, 529)])     # one block, two key tiles
+def test_split_grid(B, H, Sq, Sk, D, dtype, seed):
+    """Fewer query blocks than SMs (non-causal, dense): the key range of each block is split
+    over CTAs and the parts merged. Matches the oracle, is bitwise reproducible (the parts
+    merge in a fixed order whichever CTA finishes last), leaves the split counters at zero
+    (a second call gives the same bits) and agrees with the unsplit grid within rounding."""
+    wl = WORKLOADS["cross"].replace(B=B, H=H, Sq=Sq, Sk=Sk, D=D, causal=False,
+                                    layout="bhsd", seed=seed)
+    x = make_inputs(wl, dtype=dtype)
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v")}
+    ws = torch.zeros(_lib.attn_fwd_workspace_size(*g["q"].shape), dtype=torch.uint8,
+                     device=DEV)
+    assert ws.numel() > 256  # room for the partial results
+    o1, l1 = _fwd_ws(g, wl.sm_scale, False, ws)
+    o2, l2 = _fwd_ws(g, wl.sm_scale, False, ws)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert int(ws[1024:2048].view(torch.int32).abs().sum()) == 0  # counters back at zero
+    o0, l0 = _fwd_ws(g, wl.sm_scale, False, ws, {"ATTN_FWD_SPLIT": "0"})
+    assert (o1.float() - o0.float()).abs().max() <= 2 ** -6
+    assert (l1 - l0).abs().max() <= 1e-4
+    qn, kn, vn = (np64(x[n]) for n in ("q", "k", "v"))
+    hs = slice(0, min(H, 4))
+    o_r, lse_r = ref.fwd_bhsd(qn[:, hs], kn[:, hs], vn[:, hs], wl.sm_scale, False)
+    assert_fwd_close(o1[:, hs], l1[:, hs], o_r, lse_r, what=f"split D={D}")
+
+
+def test_split_workspace_shared_with_backward():
+    """One workspace for the forward (split grid) and the backward, as a training step uses
+    it: the backward writes nothing into the header that holds the split counters."""
+    from attention_flashattention_fwd_02_gb300.attention import backward
+    wl = WORKLOADS["cross"].replace(B=1, H=4, Sq=512, Sk=2048, D=128, causal=False,
+                                    layout="bhsd", seed=529)
+    x = make_inputs(wl)
+    g = {n: x[n].to(DEV) for n in ("q", "k", "v", "do")}
+    n = max(_lib.attn_fwd_workspace_size(*g["q"].shape),
+            _lib.attn_bwd_workspace_size(*g["q"].shape))
+    ws = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    o1, l1 = _fwd_ws(g, wl.sm_scale, False, ws)
+    for _ in range(2):
+        dq, dk, dv = backward(g["q"], g["k"], g["v"], o1, l1, g["do"], wl.sm_scale, False,
+                              workspace=ws)
+        torch.cuda.synchronize()
+        o2, l2 = _fwd_ws(g, wl.sm_scale, False, ws)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
