@@ -27,7 +27,8 @@ def forward(q, k, v, sm_scale: Optional[float] = None, causal: bool = False,
     """bias: optional additive bias, its Sq stride a multiple of 8 elements: (Bb, Hb, Sq, Sk)
     with Bb in {1, B}, Hb in {1, H} for dense and padded inputs; (Bb, Hb, >= max_seqlen_q,
     >= max_seqlen_k) with Bb in {1, num_seqs} for compact inputs, sequence s's block at offset
-    0 of slice s."""
+    0 of slice s. workspace: zeroed uint8 device tensor, at least 256 bytes; one of
+    _lib.attn_fwd_workspace_size bytes lets small non-causal grids split their key ranges."""
     sm_scale = 1.0 / math.sqrt(q.shape[-1]) if sm_scale is None else sm_scale
     o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if out is None else out
     lse = _lse_like(q) if lse is None else lse

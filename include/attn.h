@@ -64,9 +64,13 @@
  *     grids (kernel = fwd, bwd_main, bwd_main_nodq or bwd_dq; g<N>: groups of N (unit, head)
  *     pairs); otherwise the order comes from a table measured on GB300 (the sweep that
  *     writes the table sets it). Results do not depend on the order.
- *   ATTN_FWD_PERSISTENT=0|1 forces the forward grid to one CTA per query block (0) or to a
- *     persistent grid of one CTA per SM walking the blocks (1); ATTN_FWD_CTAS=n launches n
- *     persistent CTAs. Results do not depend on the grid.
+ *   ATTN_FWD_PERSISTENT=0 turns off the forward's work stealing (with more query blocks
+ *     than SMs, running CTAs take over the blocks of CTAs not yet launched);
+ *     ATTN_FWD_CTAS=n launches n CTAs, CTA c taking blocks c, c + n, ... Results do not
+ *     depend on the grid.
+ *   ATTN_FWD_SPLIT=0|1 turns the forward's split grid off, or on for every non-causal dense
+ *     grid with fewer query blocks than SMs (default: at most half as many). Results agree
+ *     within rounding (the parts are merged in a fixed order).
  *   ATTN_TEST_WITHHOLD_KV_TILE=j / ATTN_TEST_WITHHOLD_Q_STEP=i (failure-detection tests):
  *     the forward loads no key tile from j on / the backward skips query step i, and every
  *     wait gives up after 50 ms, so the call ends with ATTN_ERR_DEVICE_TIMEOUT in the status
@@ -115,8 +119,14 @@ typedef enum {
   ATTN_ERR_DTYPE = 10          /* tensors of one call with different element types */
 } attn_status;
 
-/* Workspace bytes needed by attn_fwd* for Q of shape (B, H, Sq, D) (compact: B = 1,
- * Sq = total query tokens). Holds the device status word only. */
+/* Workspace bytes for attn_fwd* with Q of shape (B, H, Sq, D) (compact: B = 1, Sq = total
+ * query tokens). The forward calls need 256 bytes (the device status word); given this many
+ * (zeroed once, like every workspace), a non-causal dense call with at most half as many
+ * query blocks (256 rows; 128 at head size 256) as the GPU has SMs splits each block's key
+ * range over several CTAs and merges the parts (the blocks' counters at bytes 1024..2047
+ * return to zero at the end of every call; after ATTN_ERR_DEVICE_TIMEOUT zero the workspace
+ * again). One workspace of max(attn_fwd_workspace_size, attn_bwd_workspace_size) bytes
+ * serves both passes: no backward kernel writes bytes 4..2047. */
 size_t attn_fwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D);
 
 /* Workspace bytes needed by attn_bwd* (status word, per-row Delta = rowsum(dO * O) in fp32,
@@ -128,8 +138,8 @@ size_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t D);
  * non-NULL, int32 device arrays of B+1 prefix sums; only the differences are used).
  *   q: (B, H, Sq, D)          k, v: (B, H, Sk, D)          (bf16 or fp16, one type)
  *   o: (B, H, Sq, D) out      lse: (B, H, Sq) fp32 out (natural-log logsumexp)
- *   workspace: device, >= attn_fwd_workspace_size bytes (may be NULL with 0 bytes: device
- *   errors are then not reported). stream: cudaStream_t.
+ *   workspace: device, >= 256 bytes, attn_fwd_workspace_size bytes for the split grid (may
+ *   be NULL with 0 bytes: device errors are then not reported). stream: cudaStream_t.
  */
 attn_status attn_fwd(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, float sm_scale,
