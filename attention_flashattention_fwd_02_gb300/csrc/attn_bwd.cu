@@ -237,6 +237,15 @@ struct BwdCfg {
   static constexpr int NTHREADS = (D == 128) ? 512 : 320;
   static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_DRAIN0 = DSPLIT ? 4 : 12;
   static constexpr int NCOMPUTE = 128 * NCWG;        // compute threads
+  // Epilogue: a compute warp stores its 32 keys x CW columns of dK and of dV through shared
+  // memory (row-major, CW * 2 bytes a row) with TMA stores; the K and V tiles' space is free
+  // by then and holds the 2 x 4 NCWG warp areas. Not at d_head 128, where the staging code
+  // costs the key-tile loop a register (measured 1 % slower) and the row stores are cheap
+  // against a step's work; there, and on tiles reaching past the sequence, row stores.
+  static constexpr bool EPI_TMA = (D != 128);
+  static constexpr int CW = DH / NCWG;
+  static constexpr int EPI_W_BYTES = 32 * CW * 2;
+  static_assert(2 * 4 * NCWG * EPI_W_BYTES <= 2 * KV_BYTES, "epilogue staging");
 };
 
 template <int BM, int QST, int LSE_ST>
@@ -763,12 +772,50 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
     // them, warpgroup g writes its share [g DH / NCWG, +DH / NCWG) of those
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, p.timeout_ns);
     tc_fence_after();
-    if (ok) {
+    // A key tile inside its sequence leaves through shared memory: each warp writes its 32
+    // keys of dK and dV (its warpgroup's columns) as rows of its own areas, in the space of
+    // the K and V tiles (every product that read them has completed: dkdv_full), and one
+    // lane stores each area with a TMA copy. A tile reaching past the sequence's end is
+    // stored row by row (a copy would also write the keys past the end).
+    constexpr int CW = C::CW;
+    if (C::EPI_TMA && ok && k_lo + BN <= sv.len_k) {
+      const float sc = p.sm_scale;
+      const uint32_t ak = smem_u32(smem + C::OFF_K + warp * C::EPI_W_BYTES);
+      const uint32_t av = ak + 4 * C::NCWG * C::EPI_W_BYTES;
+#pragma unroll
+      for (int c = 0; c < CW; c += 32) {
+        uint32_t a[32], b[32];
+        ATTN_TMEM_LD2_X32(tmem + C::COL_DK + lane_off + g * CW + c,
+                          tmem + C::COL_DV + lane_off + g * CW + c, a, b);
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 vk, vv;
+          vk.x = pack2<F16>(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc);
+          vk.y = pack2<F16>(__uint_as_float(a[e + 2]) * sc, __uint_as_float(a[e + 3]) * sc);
+          vk.z = pack2<F16>(__uint_as_float(a[e + 4]) * sc, __uint_as_float(a[e + 5]) * sc);
+          vk.w = pack2<F16>(__uint_as_float(a[e + 6]) * sc, __uint_as_float(a[e + 7]) * sc);
+          vv.x = pack2<F16>(__uint_as_float(b[e]), __uint_as_float(b[e + 1]));
+          vv.y = pack2<F16>(__uint_as_float(b[e + 2]), __uint_as_float(b[e + 3]));
+          vv.z = pack2<F16>(__uint_as_float(b[e + 4]), __uint_as_float(b[e + 5]));
+          vv.w = pack2<F16>(__uint_as_float(b[e + 6]), __uint_as_float(b[e + 7]));
+          st_shared_v4(ak + lane * (CW * 2) + (c + e) * 2, vk);
+          st_shared_v4(av + lane * (CW * 2) + (c + e) * 2, vv);
+        }
+      }
+      fence_proxy_async_smem();  // the areas, written by this warp, to the copy engine
+      __syncwarp();
+      if (lane == 0) {
+        const int row = sv.row0_k + k_lo + (warp & 3) * 32;
+        tma_store_4d(&p.tm_dk, ak, dh * DH + g * CW, row, h, sv.batch);
+        tma_store_4d(&p.tm_dv, av, dh * DH + g * CW, row, h, sv.batch);
+        bulk_commit_group();
+        bulk_wait_group0();  // complete before the CTA exits
+      }
+    } else if (ok) {
       const int64_t grow = sv.row0_k + key;
       uint16_t* kr = p.dk + sv.batch * p.dk_sb + h * p.dk_sh + grow * p.dk_ss + dh * DH;
       uint16_t* vr = p.dv + sv.batch * p.dv_sb + h * p.dv_sh + grow * p.dv_ss + dh * DH;
       const float sc = p.sm_scale;
-      constexpr int CW = DH / C::NCWG;
 #pragma unroll
       for (int c = g * CW; c < (g + 1) * CW; c += 32) {
         uint32_t a[32], b[32];
@@ -892,6 +939,7 @@ cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, bool bias, dim3
 int bwd_block_m(int D) {
   return D == 256 ? BwdCfg<256>::BM : D == 128 ? BwdCfg<128>::BM : BwdCfg<64>::BM;
 }
+int bwd_epilogue_cols(int D) { return D == 256 ? 128 : D / 2; }
 int bwd_ctas_per_key_tile(int D) { return D == 256 ? 2 : 1; }
 int bwd_block_n() { return 128; }
 

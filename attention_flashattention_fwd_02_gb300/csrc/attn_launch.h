@@ -19,6 +19,7 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int D, bool f16, bool bias, dim3
 int bwd_block_m(int D);  // query rows per inner step of the main kernel
 int bwd_block_n();       // key rows per CTA of the main kernel
 int bwd_ctas_per_key_tile(int D);  // 2 at d_head 256 (one per half of d), else 1
+int bwd_epilogue_cols(int D);      // dK / dV columns a compute warpgroup stores
 cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int D, bool f16, bool bias, dim3 grid,
                             cudaStream_t stream);
