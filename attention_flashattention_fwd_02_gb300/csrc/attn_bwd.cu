@@ -230,6 +230,13 @@ struct BwdCfg {
   static constexpr uint32_t COL_DQ = 2 * DH + 2 * BM;
   static constexpr uint32_t COL_P = COL_DQ + (DQ_T ? BM : D);
   static_assert(COL_P + BM / 2 <= TMEM_COLS, "TMEM layout does not fit");
+  // d_head 128: dS^T also goes to the last 32 TMEM columns (16-bit, like P^T) and is the A
+  // operand of dK from there, which takes its 16 KB a step off the shared-memory reads (the
+  // step is bound by them); shared memory keeps dS^T for dQ. Elsewhere TMEM has no room
+  // (d_head 64) or dS is stored query-major for 32-query steps (d_head 256).
+  static constexpr bool DS_TMEM = (D == 128);
+  static constexpr uint32_t COL_DST = COL_P + BM / 2;
+  static_assert(!DS_TMEM || COL_DST + BM / 2 <= TMEM_COLS, "TMEM layout does not fit");
   // Warps. d_head 64: 0..7 compute, 8 producer, 9 MMA (320 threads). d_head 128: 0..7
   // compute, 8 producer, 9 MMA, 10..11 no role, 12..15 dQ drain (512 threads leave 128
   // registers a thread, which these roles fit in). d_head 256: 0..3 compute, 4..7 dQ drain,
@@ -523,14 +530,24 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           umma_ts_w(tDV, tP + kk * 8, do_mn + qo + mnmajor_step(kk), idG, (it > 0 || kk > 0));
-        umma_commit_w(smem_u32(&bars.p_empty));  // P^T of step it read: the next P may land
+        if (!C::DS_TMEM)
+          umma_commit_w(smem_u32(&bars.p_empty));  // P^T of step it read: the next P may land
         if (!mbar_wait(smem_u32(&bars.ds_full[bs]), (it >> 1) & 1, abort, p.timeout_ns)) break;
         tc_fence_after();
+        if constexpr (C::DS_TMEM) {
+          // dK = dS^T Q with dS^T from tensor memory; then P^T and dS^T of step it are read
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ss_w(tDK,
-                    ds_a + dso + (C::DS_QMAJOR ? mnmajor_step(kk) : kmajor_step(BN, kk)),
-                    q_mn + qo + mnmajor_step(kk), idK, (it > 0 || kk > 0));
+          for (int kk = 0; kk < BM / 16; ++kk)
+            umma_ts_w(tDK, tmem + C::COL_DST + kk * 8, q_mn + qo + mnmajor_step(kk), idK,
+                      (it > 0 || kk > 0));
+          umma_commit_w(smem_u32(&bars.p_empty));
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            umma_ss_w(tDK,
+                      ds_a + dso + (C::DS_QMAJOR ? mnmajor_step(kk) : kmajor_step(BN, kk)),
+                      q_mn + qo + mnmajor_step(kk), idK, (it > 0 || kk > 0));
+        }
         if (p.with_dq) {
           if (it > 0 &&
               !mbar_wait(smem_u32(&bars.dq_empty), (it - 1) & 1, abort, p.timeout_ns))
@@ -631,7 +648,8 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.s_free));  // the MMA warp may compute the next S^T / dP^T
-      // P^T of the previous step must have been read by its dV MMA before this step's lands
+      // P^T (and at d_head 128 dS^T) of the previous step must have been read by its dV (dK)
+      // MMA before this step's lands
       if (it > 0 && !mbar_wait(smem_u32(&bars.p_empty), (it - 1) & 1, abort, p.timeout_ns)) {
         ok = false;
         break;
@@ -738,6 +756,7 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
           }
         }
         ATTN_TMEM_ST_X16(tmem + C::COL_P + lane_off + c0 / 2, pp);
+        if constexpr (C::DS_TMEM) ATTN_TMEM_ST_X16(tmem + C::COL_DST + lane_off + c0 / 2, pd);
         if constexpr (C::DS_QMAJOR) {
           // [query][key]: one 16-bit element per query row; the warp's 32 keys of one row
           // are 64 contiguous bytes (one wavefront)

@@ -31,13 +31,16 @@ from _pipeline_sim import Sim
 
 
 def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
-                      stage_in_ds=True, n_wg=2):
+                      stage_in_ds=True, n_wg=2, ds_tmem=False):
     """The kernel's roles; `skip` names waits to leave out (to check that the model sees
     what they prevent; "read_wait" is the wait of a draining warp for its previous
     reduce-add to read its staging); withhold: a step whose Q / dO the producer skips (the
     kernel's failure-detection hook); stage_in_ds: the d_head 64 layout (the compute
     warpgroups drain dQ into the dS buffer they released), else the d_head 128 one (drain
-    warps with staging areas of their own); n_wg: compute warpgroups (1 at d_head 256)."""
+    warps with staging areas of their own); n_wg: compute warpgroups (1 at d_head 256);
+    ds_tmem: the d_head 128 kernel, whose compute warps also write dS^T to tensor memory (the
+    A operand of dK, next to P^T) and whose MMA warp commits p_empty after dK (both tensor
+    memory operands of step it read)."""
     drains = ("wg0", "wg1") if stage_in_ds else ("dr0", "dr1")
     sim.barrier("kv_full", 1)
     for st in range(qst):
@@ -54,10 +57,14 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
         sim.buffer(f"QS{st}", ("SdP", "dV", "dK") + wg)
     sim.buffer("SDP", wg)
     sim.buffer("P", ("dV",))
+    sim.buffer("DST", ("dK",))  # dS^T in tensor memory (ds_tmem)
     for b in range(2):
         for h in range(2):  # the halves the two warpgroups write
-            sim.buffer(f"DS{b}{h}", lambda c, h=h: ({"dK", "dQ"} if with_dq else {"dK"})
-                       if c[0] == "dS" else {f"tma{h}"})
+            # dS^T in shared memory: read by dK (unless it reads dS^T from tensor memory)
+            # and by dQ
+            ds_readers = ({"dQ"} if with_dq else set()) | (set() if ds_tmem else {"dK"})
+            sim.buffer(f"DS{b}{h}", lambda c, h=h, r=frozenset(ds_readers):
+                       set(r) if c[0] == "dS" else {f"tma{h}"})
     for h in range(2):
         sim.buffer(f"STG{h}", (f"tma{h}",))
     sim.buffer("DQ", drains)
@@ -113,11 +120,14 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
             if not (yield from wait("p_full", it)):
                 break
             yield ("mma", "dV", [("P", it), (f"QS{st}", it)], [])
-            yield ("commit", "p_empty")
+            if not ds_tmem:
+                yield ("commit", "p_empty")
             if not (yield from wait(f"ds_full{bs}", it >> 1)):
                 break
             ds = [(f"DS{bs}{h}", ("dS", it)) for h in range(n_wg)]
-            yield ("mma", "dK", ds + [(f"QS{st}", it)], [])
+            yield ("mma", "dK", ([("DST", it)] if ds_tmem else ds) + [(f"QS{st}", it)], [])
+            if ds_tmem:  # P^T and dS^T of step it are read
+                yield ("commit", "p_empty")
             if with_dq:
                 if it > 0 and not (yield from wait("dq_empty", it - 1)):
                     break
@@ -166,6 +176,8 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
             yield ("delay", rng.randint(1, 10))  # P and dS
             if me == "wg0":  # one write event stands for both warpgroups' halves
                 yield ("write", "P", it)
+                if ds_tmem:
+                    yield ("write", "DST", it)
             yield ("arrive", "p_full")
             # dS^T was stored with P^T, but the MMAs (async proxy) see it only after the
             # proxy fence that precedes the ds_full arrival
@@ -258,3 +270,31 @@ def test_staging_needs_the_reduce_read_wait(stage_in_ds):
         found += sim.run(backward_protocol(sim, 6, 3, True, rng, skip=("read_wait",),
                                            stage_in_ds=stage_in_ds))
     assert any(v[0] == "overwrite" for v in found)
+
+
+@pytest.mark.parametrize("n_steps", [1, 2, 3, 7])
+@pytest.mark.parametrize("qst", [2, 3])
+@pytest.mark.parametrize("with_dq", [True, False])
+def test_backward_ds_in_tensor_memory(n_steps, qst, with_dq):
+    """d_head 128 with dS^T also in tensor memory as dK's A operand: p_empty, committed after
+    dK, protects both tensor-memory operands; every wait exact, no buffer overwritten while
+    read, also with the hardware's parity waits."""
+    rng = random.Random(n_steps * 10 + qst + 100 * with_dq + 5000)
+    for parity in (False, True):
+        for _ in range(100):
+            sim = Sim(rng, exit_check=True, parity_waits=parity,
+                      timeout=5000 if parity else None)
+            assert sim.run(backward_protocol(sim, n_steps, qst, with_dq, rng,
+                                             stage_in_ds=False, ds_tmem=True)) == []
+
+
+def test_ds_in_tensor_memory_needs_p_empty_after_dk():
+    """Committing p_empty after dV alone (as without dS^T in tensor memory) lets the next
+    step's dS^T land while dK still reads the previous one."""
+    rng = random.Random(6)
+    found = []
+    for _ in range(300):
+        sim = Sim(rng, mma_ticks=(1, 12))
+        found += sim.run(backward_protocol(sim, 6, 3, True, rng, stage_in_ds=False,
+                                           ds_tmem=True, skip=("p_empty",)))
+    assert any(v[0] == "overwrite" and v[1] == "DST" for v in found), found[:3]
