@@ -415,9 +415,10 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   const int n_items = n_blk * uh;
   dim3 grid((unsigned)fwd_grid_size(n_items, &p.clc));
   // At most half as many blocks as SMs (non-causal, dense, no bias): cut the (block, key
-  // tile) units into one equal range per SM, given the workspace for the partial results.
-  // With more blocks the partial results cost more than the idle SMs (measured on GB300).
-  // ATTN_FWD_SPLIT=0 turns it off, =1 splits any grid with fewer blocks than SMs.
+  // tile) units into equal ranges, the same number for every block and at most one per SM,
+  // given the workspace for the partial results. With more blocks the partial results cost
+  // more than the idle SMs (measured on GB300). ATTN_FWD_SPLIT=0 turns it off, =1 splits any
+  // grid with fewer blocks than SMs (more than half as many: one range per SM).
   const int sms = sm_count();
   const int64_t nk = ((int64_t)pr.max_k + 127) / 128;
   const size_t split_need = fwd_split_ws_bytes(n_items, kernel_width(pr.D));
@@ -426,8 +427,19 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   if (!causal && bias == nullptr && pr.mode == kDense && sms > n_items && nk >= 2 &&
       split_need > 0 && ws != nullptr && ws_bytes >= split_need && split_on) {
     const int64_t units = (int64_t)n_items * nk;
-    const int G = units < sms ? (int)units : sms;
-    if (G > n_items) {
+    // a multiple of the block count: every block splits into the same number of parts and no
+    // CTA runs two (measured on GB300: 32 blocks over 128 CTAs 34 us, over 152 CTAs 42 us)
+    const int per_block = (int)(nk < sms / n_items ? nk : sms / n_items);
+    int G = per_block >= 2 ? n_items * per_block : (units < sms ? (int)units : sms);
+    // ATTN_FWD_CTAS=<n> sets the split grid's size too (a sweep hook; each CTA then runs
+    // units / n of the work, n at most the slots the workspace holds)
+    const char* cs = getenv("ATTN_FWD_CTAS");
+    const bool forced = cs != nullptr && atoi(cs) >= 1;
+    if (forced) {
+      const int64_t n = atoi(cs) < units ? atoi(cs) : units;
+      G = (int)(n < kSplitMaxBlocks ? n : kSplitMaxBlocks);
+    }
+    if (G > n_items || forced) {
       p.split = 1;
       p.nk = (int)nk;
       p.n_units = units;

@@ -842,24 +842,51 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
           ok = ok && tile_meet();
           if (ok && bars.merge_last) {
             __threadfence();
-            float mx = -INFINITY;
-            for (int c2 = c_first; c2 <= c_last; ++c2) {
-              const float* sl = p.part + (size_t)(item + c2) * C::SLOT_FLOATS;
-              mx = fmaxf(mx, c2 == (int)blockIdx.x ? m_use : __ldcg(sl + D * RB + rr));
-            }
-            // part c2's weight: 2^(m - mx)
-            auto part_scale = [&](int c2, float& lp) {
-              const float* sl = p.part + (size_t)(item + c2) * C::SLOT_FLOATS;
-              const bool me = c2 == (int)blockIdx.x;
-              const float mp = me ? m_use : __ldcg(sl + D * RB + rr);
-              lp = me ? l : __ldcg(sl + (D + 1) * RB + rr);
+            // The merge reads the other parts' slots from L2. Each group of loads below is
+            // issued before any of its values is used, so a row waits about one L2 round trip
+            // per group rather than one per load: the statistics of eight parts at a time,
+            // then per 32-column chunk two parts' values (and maxima) at a time. The parts
+            // are summed in part order whichever CTA merges.
+            const int me = (int)blockIdx.x;
+            auto slot = [&](int c2) { return p.part + (size_t)(item + c2) * C::SLOT_FLOATS; };
+            auto weight = [&](float mp, float mx) {  // a part's weight, 2^(m - mx)
               return mp == -INFINITY ? 0.f : ex2_approx(mp - mx);
             };
+            float m8[8], l8[8];  // the statistics of the first eight parts
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int c2 = c_first + u;
+              const bool in = c2 <= c_last, mine = c2 == me;
+              m8[u] = !in ? -INFINITY : mine ? m_use : __ldcg(slot(c2) + D * RB + rr);
+              l8[u] = !in ? 0.f : mine ? l : __ldcg(slot(c2) + (D + 1) * RB + rr);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx = fmaxf(mx, m8[u]);
+            for (int g0 = c_first + 8; g0 <= c_last; g0 += 8) {
+              float mv[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int c2 = g0 + u;
+                mv[u] = c2 > c_last ? -INFINITY : c2 == me ? m_use : __ldcg(slot(c2) + D * RB + rr);
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u) mx = fmaxf(mx, mv[u]);
+            }
             float lsum = 0.f;
-            for (int c2 = c_first; c2 <= c_last; ++c2) {
-              float lp;
-              const float sc = part_scale(c2, lp);
-              lsum += sc * lp;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) lsum += weight(m8[u], mx) * l8[u];
+            for (int g0 = c_first + 8; g0 <= c_last; g0 += 8) {
+              float mv[8], lv[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int c2 = g0 + u;
+                const bool in = c2 <= c_last, mine = c2 == me;
+                mv[u] = !in ? -INFINITY : mine ? m_use : __ldcg(slot(c2) + D * RB + rr);
+                lv[u] = !in ? 0.f : mine ? l : __ldcg(slot(c2) + (D + 1) * RB + rr);
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u) lsum += weight(mv[u], mx) * lv[u];
             }
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll 1
@@ -867,29 +894,47 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
               float acc[32];
 #pragma unroll
               for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-              for (int c2 = c_first; c2 <= c_last; ++c2) {
-                float lp;
-                const float sc = part_scale(c2, lp);
-                if (c2 == (int)blockIdx.x) {
-                  uint32_t o[32];
-                  if (n > 0) {
-                    ATTN_TMEM_LD_X32(tOt + c * 32, o);
+              for (int g0 = c_first; g0 <= c_last; g0 += 2) {
+                float4 x[2][8];
+                float mp[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int c2 = g0 + u;
+                  if (c2 == me) {  // this CTA's part, still in tensor memory
+                    mp[u] = m_use;
+                    uint32_t o[32];
+                    if (n > 0) {
+                      ATTN_TMEM_LD_X32(tOt + c * 32, o);
+                    } else {
+#pragma unroll
+                      for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                      x[u][e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                            __uint_as_float(o[4 * e + 2]),
+                                            __uint_as_float(o[4 * e + 3]));
+                  } else if (c2 <= c_last) {
+                    const float* sl = slot(c2);
+                    mp[u] = __ldcg(sl + D * RB + rr);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                      x[u][e] = __ldcg(reinterpret_cast<const float4*>(sl + ((c * 8 + e) * RB + rr) * 4));
                   } else {
+                    mp[u] = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    for (int e = 0; e < 8; ++e) x[u][e] = make_float4(0.f, 0.f, 0.f, 0.f);
                   }
+                }
 #pragma unroll
-                  for (int e = 0; e < 32; ++e) acc[e] += sc * __uint_as_float(o[e]);
-                } else {
-                  const float* sl = p.part + (size_t)(item + c2) * C::SLOT_FLOATS;
+                for (int u = 0; u < 2; ++u) {
+                  const float sc = weight(mp[u], mx);
 #pragma unroll
-                  for (int e = 0; e < 32; e += 4) {
-                    const float4 x = __ldcg(reinterpret_cast<const float4*>(
-                        sl + ((c * 32 + e) / 4 * RB + rr) * 4));
-                    acc[e] += sc * x.x;
-                    acc[e + 1] += sc * x.y;
-                    acc[e + 2] += sc * x.z;
-                    acc[e + 3] += sc * x.w;
+                  for (int e = 0; e < 8; ++e) {
+                    acc[4 * e] += sc * x[u][e].x;
+                    acc[4 * e + 1] += sc * x[u][e].y;
+                    acc[4 * e + 2] += sc * x[u][e].z;
+                    acc[4 * e + 3] += sc * x[u][e].w;
                   }
                 }
               }

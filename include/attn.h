@@ -70,7 +70,8 @@
  *     depend on the grid.
  *   ATTN_FWD_SPLIT=0|1 turns the forward's split grid off, or on for every non-causal dense
  *     grid with fewer query blocks than SMs (default: at most half as many). Results agree
- *     within rounding (the parts are merged in a fixed order).
+ *     within rounding (the parts are merged in a fixed order). A split grid takes its size
+ *     from ATTN_FWD_CTAS too (at most 256 CTAs).
  *   ATTN_TEST_WITHHOLD_KV_TILE=j / ATTN_TEST_WITHHOLD_Q_STEP=i (failure-detection tests):
  *     the forward loads no key tile from j on / the backward skips query step i, and every
  *     wait gives up after 50 ms, so the call ends with ATTN_ERR_DEVICE_TIMEOUT in the status

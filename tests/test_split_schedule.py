@@ -52,3 +52,24 @@ def test_split_schedule(n_items, nk, G):
     for u in range(U):
         c = cta_of(u, U, G)
         assert c * U // G <= u < (c + 1) * U // G
+
+
+def split_ctas(n_items, nk, sms):
+    """The host's split grid size (attn_fwd): a whole number of ranges per block, at most one
+    per SM; with more than half as many blocks as SMs (only when forced) one range per SM."""
+    per_block = min(nk, sms // n_items)
+    return n_items * per_block if per_block >= 2 else min(n_items * nk, sms)
+
+
+@pytest.mark.parametrize("n_items,nk", [(32, 32), (50, 9), (1, 512), (76, 2), (7, 3), (64, 33),
+                                        (3, 2)])
+def test_split_grid_size_gives_each_cta_one_block(n_items, nk):
+    G = split_ctas(n_items, nk, 152)
+    assert n_items < G <= 152 and G % n_items == 0
+    U, seen = schedule(n_items, nk, G)
+    visits = {}
+    for k, parts in seen.items():
+        assert len(parts) == G // n_items  # every block has the same number of parts
+        for c, j_lo, j_hi in parts:
+            visits[c] = visits.get(c, 0) + 1
+    assert sorted(visits) == list(range(G)) and set(visits.values()) == {1}
