@@ -291,6 +291,15 @@ int grid_group(const char* kernel, int width, int causal, double shared_bytes, i
   return shared_bytes <= tile_major_limit(kernel, width) ? uh : 1;
 }
 
+// The measured split rule for a forward of the given kernel width (no rule: no split).
+bool fwd_split_by_table(int width, int64_t n_items, int64_t key_tiles, int sms) {
+  for (const FwdSplitRule& r : kFwdSplitRules)
+    if (r.width == width)
+      return 2 * n_items <= sms && (double)n_items <= r.max_blocks_per_sm * sms &&
+             key_tiles >= r.min_key_tiles;
+  return false;
+}
+
 // Forward grid: one CTA per work item. With more items than SMs the running CTAs steal the
 // items of CTAs not yet launched (cluster launch control), so each SM's CTA walks items in the
 // grid's order until none are left, its pipeline running on across them. Tuning and test
@@ -414,16 +423,18 @@ attn_status fwd_common(const attn_tensor4* q, const attn_tensor4* k, const attn_
   if ((int64_t)n_blk * uh > kMaxI32) return ATTN_ERR_UNSUPPORTED;  // 1-D grid
   const int n_items = n_blk * uh;
   dim3 grid((unsigned)fwd_grid_size(n_items, &p.clc));
-  // At most half as many blocks as SMs (non-causal, dense, no bias): cut the (block, key
-  // tile) units into equal ranges, the same number for every block and at most one per SM,
-  // given the workspace for the partial results. With more blocks the partial results cost
-  // more than the idle SMs (measured on GB300). ATTN_FWD_SPLIT=0 turns it off, =1 splits any
-  // grid with fewer blocks than SMs (more than half as many: one range per SM).
+  // Few blocks (non-causal, dense, no bias): cut the (block, key tile) units into equal
+  // ranges, the same number for every block and at most one per SM, given the workspace for
+  // the partial results. The measured table (kFwdSplitRules) says when: at most about half as
+  // many blocks as SMs (every block then has two parts or more) and key ranges long enough
+  // to outweigh the partial results and their merge. ATTN_FWD_SPLIT=0 turns it off, =1
+  // splits any grid with fewer blocks than SMs (more than half as many: one range per SM).
   const int sms = sm_count();
   const int64_t nk = ((int64_t)pr.max_k + 127) / 128;
   const size_t split_need = fwd_split_ws_bytes(n_items, kernel_width(pr.D));
   const char* sv = getenv("ATTN_FWD_SPLIT");
-  const bool split_on = sv == nullptr ? 2 * n_items <= sms : atoi(sv) != 0;
+  const bool split_on = sv == nullptr ? fwd_split_by_table(kernel_width(pr.D), n_items, nk, sms)
+                                      : atoi(sv) != 0;
   if (!causal && bias == nullptr && pr.mode == kDense && sms > n_items && nk >= 2 &&
       split_need > 0 && ws != nullptr && ws_bytes >= split_need && split_on) {
     const int64_t units = (int64_t)n_items * nk;

@@ -24,4 +24,21 @@ static const GridOrderRule kGridOrderRules[] = {
     {"bwd_dq", 128, 67108864.0},  // mean slowdown 1.0006 over 10 points
 };
 
+// Split key ranges of a non-causal dense forward, per kernel width: used when the
+// query blocks are at most max_blocks_per_sm x the SM count (and at most half of
+// it, so that every block has the same number of parts) and each block has at
+// least min_key_tiles key tiles. Written by tune_grid_order.py --split from a
+// timing sweep of the forward with and without the split on a GB300 (NVIDIA GB300).
+struct FwdSplitRule {
+  int width;
+  double max_blocks_per_sm;
+  int min_key_tiles;
+};
+
+static const FwdSplitRule kFwdSplitRules[] = {
+    {64, 0.500000, 16},  // mean slowdown 1.0022 over 30 points
+    {128, 0.500000, 16},  // mean slowdown 1.0054 over 30 points
+    {256, 0.473684, 32},  // mean slowdown 1.0071 over 30 points
+};
+
 }  // namespace attn_sm103

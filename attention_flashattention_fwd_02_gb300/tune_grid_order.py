@@ -1,4 +1,5 @@
-"""Probe sweep behind the per-shape CTA-order table (csrc/attn_tune_table.h).
+"""Probe sweeps behind the per-shape table (csrc/attn_tune_table.h): the CTA order of causal
+grids, and when the forward splits the key range of a small non-causal grid.
 
 Every kernel of the library launches its causal grid in one of two orders:
   seq   (query or key blocks, H, units): the blocks of one (unit, head) run next to each
@@ -11,11 +12,20 @@ dense inputs over a range of footprints, for each kernel and kernel width, and k
 (kernel, width) the footprint threshold below which ``tile`` is chosen: the candidate that
 minimises the mean slowdown against the faster order over the measured points.
 
-  python -m attention_flashattention_fwd_02_gb300.tune_grid_order --out sweep.json   # GB300
-  python -m attention_flashattention_fwd_02_gb300.tune_grid_order --from-json sweep.json \
-         --write-header                                                              # any host
+Split grids. A non-causal dense forward with at most half as many query blocks as SMs can
+cut each block's key range into equal parts, one CTA each, and merge the parts (the parts'
+partial results go through the workspace). This pays when the parts are long enough to
+outweigh the partial writes and the merge. The split sweep times the forward with and without
+the split over block counts and key lengths, per kernel width, and keeps per width the largest
+block count (as a fraction of the SMs) and the smallest key-tile count at which the split is
+used: the pair that minimises the mean slowdown against the faster grid.
 
-The first form needs the GPU; the second only rewrites the C header from a stored sweep.
+  python -m attention_flashattention_fwd_02_gb300.tune_grid_order --out sweep.json   # GB300
+  python -m attention_flashattention_fwd_02_gb300.tune_grid_order --split --out split.json
+  python -m attention_flashattention_fwd_02_gb300.tune_grid_order --from-json sweep.json \
+         --split-json split.json --write-header                                      # any host
+
+The first two need the GPU; the third only rewrites the C header from the stored sweeps.
 """
 from __future__ import annotations
 
@@ -61,7 +71,48 @@ def choose_threshold(points):
     return best, best_cost
 
 
-def header_text(sweep) -> str:
+SPLIT_WIDTHS = (64, 128, 256)
+SPLIT_BLOCKS = (8, 16, 32, 48, 64, 76)  # query blocks (at most half of the 152 SMs)
+SPLIT_KEYS = (256, 1024, 2048, 4096, 16384)  # seqlen_k
+SMS = 152
+
+
+def choose_split_rule(points, sms=SMS):
+    """points: dicts with blocks, key_tiles, ms_one (one CTA per block) and ms_split. Returns
+    (max_blocks_per_sm, min_key_tiles, mean slowdown): the split is used when blocks <=
+    max_blocks_per_sm x sms and key_tiles >= min_key_tiles. The pair minimises the mean of
+    t_chosen / t_best; ties go to the pair that splits fewer points (no split: 0.0, and a
+    key-tile minimum above every point)."""
+    fracs = [0.0] + sorted({p["blocks"] / sms for p in points})
+    kts = sorted({p["key_tiles"] for p in points})
+    kts = kts + [kts[-1] + 1 if kts else 1]
+    best, best_key = None, None
+    for f in fracs:
+        for k in kts:
+            cost, n_split = 0.0, 0
+            for p in points:
+                split = p["blocks"] <= f * sms + 1e-9 and p["key_tiles"] >= k
+                n_split += split
+                t = p["ms_split"] if split else p["ms_one"]
+                cost += t / min(p["ms_split"], p["ms_one"])
+            cost /= max(1, len(points))
+            key = (round(cost, 9), n_split)
+            if best_key is None or key < best_key:
+                best, best_key = (f, k, cost), key
+    return best
+
+
+def split_rules_from_points(results, sms=SMS):
+    rules = []
+    for width in SPLIT_WIDTHS:
+        pts = [p for p in results if p["width"] == width]
+        f, k, cost = choose_split_rule(pts, sms)
+        rules.append({"width": width, "max_blocks_per_sm": round(f, 6), "min_key_tiles": k,
+                      "mean_slowdown": round(cost, 4), "points": len(pts)})
+    return rules
+
+
+def header_text(sweep, split_sweep=None) -> str:
     lines = [
         "// CTA order of the causal grids, per kernel and kernel width: the longest-first",
         "// (tile-major) order is used when the bytes that the blocks of one head share, summed",
@@ -84,7 +135,29 @@ def header_text(sweep) -> str:
         lines.append('    {"%s", %d, %.1f},  // mean slowdown %.4f over %d points' % (
             r["kernel"], r["width"], float(r["max_tile_major_bytes"]), r["mean_slowdown"],
             r["points"]))
-    lines += ["};", "", "}  // namespace attn_sm103", ""]
+    lines += ["};", ""]
+    if split_sweep is not None:
+        lines += [
+            "// Split key ranges of a non-causal dense forward, per kernel width: used when the",
+            "// query blocks are at most max_blocks_per_sm x the SM count (and at most half of",
+            "// it, so that every block has the same number of parts) and each block has at",
+            "// least min_key_tiles key tiles. Written by tune_grid_order.py --split from a",
+            "// timing sweep of the forward with and without the split on a GB300 (" +
+            split_sweep.get("device", "?") + ").",
+            "struct FwdSplitRule {",
+            "  int width;",
+            "  double max_blocks_per_sm;",
+            "  int min_key_tiles;",
+            "};",
+            "",
+            "static const FwdSplitRule kFwdSplitRules[] = {",
+        ]
+        for r in split_sweep["rules"]:
+            lines.append("    {%d, %.6f, %d},  // mean slowdown %.4f over %d points" % (
+                r["width"], float(r["max_blocks_per_sm"]), r["min_key_tiles"],
+                r["mean_slowdown"], r["points"]))
+        lines += ["};", ""]
+    lines += ["}  // namespace attn_sm103", ""]
     return "\n".join(lines)
 
 
@@ -168,25 +241,101 @@ def sweep_gpu():
             "rules": rules_from_points(results)}
 
 
+def split_block_rows(width: int) -> int:
+    return 128 if width == 256 else 256  # query rows of a forward block
+
+
+def sweep_split_gpu():
+    import torch
+    sys.path.insert(0, os.path.dirname(HERE))
+    from attention_flashattention_fwd_02_gb300 import _lib, attention
+
+    dev = torch.device("cuda")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
+    results = []
+    Sq = 1024
+    for D in SPLIT_WIDTHS:
+        for n in SPLIT_BLOCKS:
+            heads = n * split_block_rows(D) // Sq
+            for Sk in SPLIT_KEYS:
+                g = torch.Generator(device=dev).manual_seed(n * 100000 + Sk + D)
+                q = torch.randn(1, heads, Sq, D, device=dev, generator=g, dtype=torch.bfloat16)
+                k, v = (torch.randn(1, heads, Sk, D, device=dev, generator=g,
+                                    dtype=torch.bfloat16) for _ in range(2))
+                ws = torch.zeros(_lib.attn_fwd_workspace_size(1, heads, Sq, D),
+                                 dtype=torch.uint8, device=dev)
+                o, lse = attention.forward(q, k, v, D ** -0.5, False, workspace=ws)
+                ms = {}
+                for mode in ("0", "1"):
+                    os.environ["ATTN_FWD_SPLIT"] = mode
+                    run = lambda: attention.forward(q, k, v, D ** -0.5, False, out=o, lse=lse,
+                                                    workspace=ws)
+                    ts = []
+                    for _ in range(5):
+                        for _ in range(2):
+                            run()
+                        evs = []
+                        for _ in range(4):
+                            flush.zero_()
+                            a = torch.cuda.Event(enable_timing=True)
+                            b = torch.cuda.Event(enable_timing=True)
+                            a.record()
+                            run()
+                            b.record()
+                            evs.append((a, b))
+                        torch.cuda.synchronize()
+                        ts.append(sum(a.elapsed_time(b) for a, b in evs) / len(evs))
+                    ms[mode] = statistics.median(ts)
+                os.environ.pop("ATTN_FWD_SPLIT", None)
+                st = _lib.attn_read_device_status(ws)
+                if st != 0:
+                    raise RuntimeError(f"device status {_lib.attn_status_string(st)}")
+                results.append({"width": D, "blocks": heads * Sq // split_block_rows(D),
+                                "heads": heads, "Sq": Sq, "Sk": Sk,
+                                "key_tiles": (Sk + 127) // 128, "ms_one": round(ms["0"], 5),
+                                "ms_split": round(ms["1"], 5)})
+                print(json.dumps(results[-1]), flush=True)
+                del q, k, v, o, lse, ws
+                torch.cuda.empty_cache()
+    return {"device": torch.cuda.get_device_name(), "sms": SMS, "results": results,
+            "rules": split_rules_from_points(results)}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--out", help="write the sweep (measurements and rules) as JSON")
-    ap.add_argument("--from-json", help="take the sweep from this JSON instead of the GPU")
+    ap.add_argument("--from-json", help="take the CTA-order sweep from this JSON")
+    ap.add_argument("--split", action="store_true",
+                    help="run the split sweep on the GPU instead of the CTA-order one")
+    ap.add_argument("--split-json", help="take the split sweep from this JSON")
     ap.add_argument("--write-header", action="store_true", help="rewrite csrc/attn_tune_table.h")
     a = ap.parse_args(argv)
-    if a.from_json:
-        with open(a.from_json) as f:
-            sweep = json.load(f)
-        sweep["rules"] = rules_from_points(sweep["results"])
+    sweep = split_sweep = None
+    if a.split:
+        split_sweep = sweep_split_gpu()
+        out = split_sweep
     else:
-        sweep = sweep_gpu()
+        if a.from_json:
+            with open(a.from_json) as f:
+                sweep = json.load(f)
+            sweep["rules"] = rules_from_points(sweep["results"])
+        else:
+            sweep = sweep_gpu()
+        out = sweep
+    if a.split_json:
+        with open(a.split_json) as f:
+            split_sweep = json.load(f)
+        split_sweep["rules"] = split_rules_from_points(split_sweep["results"],
+                                                       split_sweep.get("sms", SMS))
     if a.out:
         with open(a.out, "w") as f:
-            json.dump(sweep, f, indent=1)
+            json.dump(out, f, indent=1)
     if a.write_header:
+        if sweep is None or split_sweep is None:
+            raise SystemExit("--write-header needs both sweeps (--from-json, --split-json)")
         with open(HEADER, "w") as f:
-            f.write(header_text(sweep))
-    for r in sweep["rules"]:
+            f.write(header_text(sweep, split_sweep))
+    for r in out["rules"]:
         print(json.dumps(r))
 
 

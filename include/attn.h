@@ -69,9 +69,10 @@
  *     ATTN_FWD_CTAS=n launches n CTAs, CTA c taking blocks c, c + n, ... Results do not
  *     depend on the grid.
  *   ATTN_FWD_SPLIT=0|1 turns the forward's split grid off, or on for every non-causal dense
- *     grid with fewer query blocks than SMs (default: at most half as many). Results agree
- *     within rounding (the parts are merged in a fixed order). A split grid takes its size
- *     from ATTN_FWD_CTAS too (at most 256 CTAs).
+ *     grid with fewer query blocks than SMs (default: the table measured on GB300 decides,
+ *     by the block count and the key tiles per block). Results agree within rounding (the
+ *     parts are merged in a fixed order). A split grid takes its size from ATTN_FWD_CTAS too
+ *     (at most 256 CTAs).
  *   ATTN_TEST_WITHHOLD_KV_TILE=j / ATTN_TEST_WITHHOLD_Q_STEP=i (failure-detection tests):
  *     the forward loads no key tile from j on / the backward skips query step i, and every
  *     wait gives up after 50 ms, so the call ends with ATTN_ERR_DEVICE_TIMEOUT in the status
@@ -123,8 +124,10 @@ typedef enum {
 /* Workspace bytes for attn_fwd* with Q of shape (B, H, Sq, D) (compact: B = 1, Sq = total
  * query tokens). The forward calls need 256 bytes (the device status word); given this many
  * (zeroed once, like every workspace), a non-causal dense call with at most half as many
- * query blocks (256 rows; 128 at head size 256) as the GPU has SMs splits each block's key
- * range over several CTAs and merges the parts (the blocks' counters at bytes 1024..2047
+ * query blocks (256 rows; 128 at head size 256) as the GPU has SMs and long enough key
+ * ranges (a table measured on GB300: at least 16 key tiles of 128 at head sizes up to 128,
+ * 32 at 256) splits each block's key range over several CTAs and merges the parts (the
+ * blocks' counters at bytes 1024..2047
  * return to zero at the end of every call; after ATTN_ERR_DEVICE_TIMEOUT zero the workspace
  * again). One workspace of max(attn_fwd_workspace_size, attn_bwd_workspace_size) bytes
  * serves both passes: no backward kernel writes bytes 4..2047. */

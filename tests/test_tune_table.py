@@ -13,6 +13,7 @@ from attention_flashattention_fwd_02_gb300 import tune_grid_order as tg
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SWEEP = os.path.join(ROOT, "profiles", "grid_order_sweep.json")
+SPLIT_SWEEP = os.path.join(ROOT, "profiles", "fwd_split_sweep.json")
 
 
 def _pts(crossover, sizes):
@@ -70,6 +71,58 @@ def test_header_matches_stored_sweep():
         sweep = json.load(f)
     sweep["rules"] = tg.rules_from_points(sweep["results"])
     text, _ = _header_rules()
-    assert text == tg.header_text(sweep)
+    split = None
+    if os.path.exists(SPLIT_SWEEP):
+        with open(SPLIT_SWEEP) as f:
+            split = json.load(f)
+        split["rules"] = tg.split_rules_from_points(split["results"], split.get("sms", tg.SMS))
+    assert text == tg.header_text(sweep, split)
     for p in sweep["results"]:
         assert p["footprint"] == tg.footprint(p["kernel"], p["B"], p["S"], p["width"])
+
+
+def _split_pts(min_kt, max_blocks, sms=152):
+    # the split is 30 % faster for long key ranges on few blocks, 20 % slower otherwise
+    pts = []
+    for n in (8, 32, 64, 76):
+        for kt in (2, 8, 16, 32, 128):
+            good = kt >= min_kt and n <= max_blocks
+            pts.append({"blocks": n, "key_tiles": kt, "ms_one": 1.0,
+                        "ms_split": 0.7 if good else 1.2})
+    return pts
+
+
+def test_split_rule_at_crossover():
+    for min_kt in (8, 16, 32):
+        for max_blocks in (32, 76):
+            f, k, cost = tg.choose_split_rule(_split_pts(min_kt, max_blocks))
+            assert k == min_kt and f == pytest.approx(max_blocks / 152)
+            assert cost == pytest.approx(1.0)
+
+
+def test_split_rule_never():
+    f, k, cost = tg.choose_split_rule(_split_pts(10 ** 9, 76))
+    assert (f == 0.0 or k > 128) and cost == pytest.approx(1.0)
+
+
+def test_header_split_rules_match_stored_sweep():
+    """The committed header holds the rules the generator fits from both stored sweeps, and
+    the split sweep's points are what the sweep measures (blocks from heads and rows)."""
+    if not (os.path.exists(SWEEP) and os.path.exists(SPLIT_SWEEP)):
+        pytest.skip("no stored sweeps")
+    with open(SWEEP) as f:
+        sweep = json.load(f)
+    sweep["rules"] = tg.rules_from_points(sweep["results"])
+    with open(SPLIT_SWEEP) as f:
+        split = json.load(f)
+    split["rules"] = tg.split_rules_from_points(split["results"], split.get("sms", tg.SMS))
+    with open(tg.HEADER) as f:
+        assert f.read() == tg.header_text(sweep, split)
+    widths = {r["width"] for r in split["rules"]}
+    assert widths == set(tg.SPLIT_WIDTHS)
+    for p in split["results"]:
+        assert p["blocks"] == p["heads"] * p["Sq"] // tg.split_block_rows(p["width"])
+        assert p["key_tiles"] == (p["Sk"] + 127) // 128
+    api = open(os.path.join(ROOT, "attention_flashattention_fwd_02_gb300", "csrc",
+                            "attn_api.cu")).read()
+    assert "kFwdSplitRules" in api
