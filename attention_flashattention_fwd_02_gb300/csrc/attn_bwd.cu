@@ -564,6 +564,8 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
           }
         }
         umma_commit_w(smem_u32(&bars.q_empty[st]));
+        // dq_full after dK as well as dQ: at d_head 64 the drain stages dQ in the dS^T buffer
+        // that dK reads
         if (p.with_dq) umma_commit_w(smem_u32(&bars.dq_full));
       }
       umma_commit_w(smem_u32(&bars.dkdv_full));

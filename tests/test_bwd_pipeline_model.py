@@ -34,7 +34,8 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
                       stage_in_ds=True, n_wg=2, ds_tmem=False):
     """The kernel's roles; `skip` names waits to leave out (to check that the model sees
     what they prevent; "read_wait" is the wait of a draining warp for its previous
-    reduce-add to read its staging); withhold: a step whose Q / dO the producer skips (the
+    reduce-add to read its staging; "dq_first" issues dQ before dK with dq_full committed
+    after dQ alone); withhold: a step whose Q / dO the producer skips (the
     kernel's failure-detection hook); stage_in_ds: the d_head 64 layout (the compute
     warpgroups drain dQ into the dS buffer they released), else the d_head 128 one (drain
     warps with staging areas of their own); n_wg: compute warpgroups (1 at d_head 256);
@@ -125,15 +126,21 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
             if not (yield from wait(f"ds_full{bs}", it >> 1)):
                 break
             ds = [(f"DS{bs}{h}", ("dS", it)) for h in range(n_wg)]
+            dq_first = "dq_first" in skip  # a mutation: dq_full after dQ alone, before dK
+            if with_dq and dq_first:
+                if it > 0 and not (yield from wait("dq_empty", it - 1)):
+                    break
+                yield ("mma", "dQ", ds, [("DQ", it)])
+                yield ("commit", "dq_full")
             yield ("mma", "dK", ([("DST", it)] if ds_tmem else ds) + [(f"QS{st}", it)], [])
             if ds_tmem:  # P^T and dS^T of step it are read
                 yield ("commit", "p_empty")
-            if with_dq:
+            if with_dq and not dq_first:
                 if it > 0 and not (yield from wait("dq_empty", it - 1)):
                     break
                 yield ("mma", "dQ", ds, [("DQ", it)])
             yield ("commit", f"q_empty{st}")
-            if with_dq:
+            if with_dq and not dq_first:
                 yield ("commit", "dq_full")
         yield ("commit", "dkdv_full")
         # every product this warp issued has completed before tensor memory is released
@@ -298,3 +305,16 @@ def test_ds_in_tensor_memory_needs_p_empty_after_dk():
         found += sim.run(backward_protocol(sim, 6, 3, True, rng, stage_in_ds=False,
                                            ds_tmem=True, skip=("p_empty",)))
     assert any(v[0] == "overwrite" and v[1] == "DST" for v in found), found[:3]
+
+
+def test_dq_full_must_follow_dk():
+    """d_head 64 stages each dQ partial in the dS^T buffer of its step: committing dq_full
+    after dQ alone (dQ issued before dK) lets the drain overwrite dS^T while dK reads it."""
+    rng = random.Random(9)
+    found = []
+    for _ in range(300):
+        sim = Sim(rng, mma_ticks=(1, 12))
+        found += sim.run(backward_protocol(sim, 6, 3, True, rng, skip=("dq_first",),
+                                           stage_in_ds=True))
+    assert any(v[0] == "overwrite" and v[1].startswith("DS") and v[4] == ("dK",)
+               for v in found), found[:3]
