@@ -22,6 +22,7 @@ __all__ = [
     "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_dq_epilogue",
     "attn_fwd_workspace_size", "attn_bwd_workspace_size",
     "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
+    "attn_noalloc_read_device_status",
     "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
     "attn_bwd_deterministic_workspace_size", "attn_fwd_bias", "attn_bwd_bias",
     "attn_fwd_compact_varlen_bias", "attn_bwd_compact_varlen_bias",
@@ -33,6 +34,7 @@ EXPORTED_SYMBOLS = (
     "attn_fwd_compact_varlen", "attn_bwd_compact_varlen", "attn_fwd_padded_varlen",
     "attn_bwd_padded_varlen", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_dq_epilogue",
     "attn_read_device_status", "attn_status_string", "attn_bwd_noalloc",
+    "attn_noalloc_read_device_status",
     "attn_bwd_deterministic", "attn_bwd_compact_varlen_deterministic",
     "attn_bwd_deterministic_workspace_size", "attn_fwd_bias", "attn_bwd_bias",
     "attn_fwd_compact_varlen_bias", "attn_bwd_compact_varlen_bias",
@@ -100,6 +102,7 @@ _SIGS = {
                             VP, SZ, VP]),
     "attn_bwd_dq_epilogue": (INT, [P4, I32P, I32, I32, F32, VP, SZ, VP]),
     "attn_read_device_status": (INT, [VP, VP, ctypes.POINTER(I32)]),
+    "attn_noalloc_read_device_status": (INT, [VP, ctypes.POINTER(I32)]),
     "attn_bwd_noalloc": (INT, [P4, P4, P4, P4, P3, P4, I32P, I32P, F32, INT, P4, P4, P4, VP]),
     "attn_status_string": (ctypes.c_char_p, [INT]),
 }
@@ -401,6 +404,14 @@ def attn_read_device_status(workspace, stream=None) -> int:
     out = I32(0)
     _check(load().attn_read_device_status(workspace.data_ptr(), _stream(stream),
                                           ctypes.byref(out)), "attn_read_device_status")
+    return int(out.value)
+
+
+def attn_noalloc_read_device_status(stream=None) -> int:
+    """The device status of the no-alloc calls since the last read (then cleared)."""
+    out = I32(0)
+    _check(load().attn_noalloc_read_device_status(_stream(stream), ctypes.byref(out)),
+           "attn_noalloc_read_device_status")
     return int(out.value)
 
 

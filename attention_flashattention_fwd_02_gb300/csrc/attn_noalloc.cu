@@ -112,3 +112,13 @@ extern "C" attn_status attn_bwd_noalloc(const attn_tensor4* q, const attn_tensor
   return attn_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, sm_scale, causal, dq, dk,
                   dv, scratch, kNoallocScratchBytes, stream);
 }
+
+// The status word of the array (offset 0): read after synchronising the stream, then cleared,
+// as attn_read_device_status does for a workspace.
+extern "C" attn_status attn_noalloc_read_device_status(void* stream, int32_t* out) {
+  if (out == nullptr) return ATTN_ERR_NULL;
+  void* scratch = nullptr;
+  const attn_status s = scratch_address(&scratch);
+  if (s != ATTN_OK) return s;
+  return attn_read_device_status(scratch, stream, out);
+}

@@ -351,8 +351,8 @@ attn_status attn_bwd_dq_epilogue(const attn_tensor4* dq, const int32_t* cu_seqle
  * ATTN_ERR_WORKSPACE when attn_bwd_workspace_size(B, H, Sq, D) exceeds that size. The first
  * call on each device looks up the array's device address (with that device current) and
  * should come before any stream capture. All calls share the array: calls whose executions
- * overlap on the GPU race. Device-side errors are not observable through this call (its
- * status word is cleared at the start of every call).
+ * overlap on the GPU race. The array's status word is cleared at the start of every call;
+ * attn_noalloc_read_device_status reads the device-side status of the last call.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 attn_status attn_bwd_noalloc(const attn_tensor4* q, const attn_tensor4* k, const attn_tensor4* v,
@@ -361,6 +361,10 @@ attn_status attn_bwd_noalloc(const attn_tensor4* q, const attn_tensor4* k, const
                              const int32_t* cu_seqlens_k, float sm_scale, int causal,
                              const attn_tensor4* dq, const attn_tensor4* dk,
                              const attn_tensor4* dv, void* stream);
+/* The device status word of the no-alloc array (ATTN_OK or an ATTN_ERR_DEVICE_* code of the
+ * calls since it was last read), read after synchronising `stream` and cleared, like
+ * attn_read_device_status. Returns ATTN_ERR_NULL when out is NULL. */
+attn_status attn_noalloc_read_device_status(void* stream, int32_t* out);
 
 /* Reads the device status word at offset 0 of `workspace` after synchronising `stream`
  * (the only blocking call of the library) and clears it. *out receives ATTN_OK or one of

@@ -77,6 +77,33 @@ def test_noalloc_padded_varlen_after_a_larger_call():
     assert_grads_close((dq, dk, dv), g_r, what="noalloc padded after a larger call")
 
 
+def test_noalloc_device_status():
+    """The array's device status word: a call whose key-tile kernel gives up a wait (test hook
+    ATTN_TEST_WITHHOLD_Q_STEP: the producer skips one query step) leaves
+    ATTN_ERR_DEVICE_TIMEOUT there for attn_noalloc_read_device_status; the next call starts
+    from a cleared word, re-initialises the array and is correct."""
+    import os
+    gen = torch.Generator().manual_seed(62)
+    q, do = (torch.randn(1, 1, 512, 64, generator=gen).bfloat16().cuda() for _ in range(2))
+    k, v = (torch.randn(1, 1, 128, 64, generator=gen).bfloat16().cuda() for _ in range(2))
+    scale = 1.0 / math.sqrt(64)
+    o, lse = forward(q, k, v, scale, False)
+    dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+    assert _lib.attn_noalloc_read_device_status() in (0, 9)  # whatever earlier calls left
+    os.environ["ATTN_TEST_WITHHOLD_Q_STEP"] = "1"
+    try:
+        _lib.attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, scale, False)
+        status = _lib.attn_noalloc_read_device_status()
+    finally:
+        del os.environ["ATTN_TEST_WITHHOLD_Q_STEP"]
+    assert status == 9  # ATTN_ERR_DEVICE_TIMEOUT
+    _lib.attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, scale, False)
+    assert _lib.attn_noalloc_read_device_status() == 0
+    g = oracle.attention_backward(np64(q[0, 0]), np64(k[0, 0]), np64(v[0, 0]), np64(do[0, 0]),
+                                  scale, False)
+    assert_grads_close((dq[0, 0], dk[0, 0], dv[0, 0]), g, what="noalloc after a timeout")
+
+
 def test_noalloc_argument_errors():
     """Argument errors come back before anything else (size, device address, stream)."""
     gen = torch.Generator().manual_seed(61)
