@@ -179,7 +179,7 @@ cudaError_t launch_dbias_epilogue(const DbiasPostParams& p, cudaStream_t stream)
 }
 
 // =========================================================================== main kernel
-template <int D>
+template <int D, bool BIAS = false>
 struct BwdCfg {
   // d_head 256: dK and dV of 128 keys would take all 512 TMEM columns, so a CTA accumulates
   // dK, dV and the dQ partial for one half of d (DH = 128 columns) and recomputes S^T and dP^T
@@ -209,8 +209,15 @@ struct BwdCfg {
   // rows again, two steps later, after waiting for the reduce to read them).
   static constexpr bool DQ_WARPS = DQ_T;
   static constexpr int DQ_BLOCKS = BM / 32;             // 32 x 32 blocks per drain warp
+  // d_head 128 with a bias: a warp of its own (warp 10) loads each step's bias tile (BM
+  // query rows x 128 keys, two 64-key slabs with the 128-byte swizzle) into a slot of shared
+  // memory by TMA; the room comes from the drain warps, which then stage one 32 x 32 block
+  // at a time (4 KB each).
+  static constexpr bool BIAS_TMA = BIAS && (D == 128);
+  static constexpr int WARP_BIAS = 10;
+  static constexpr int STG_BLOCKS = BIAS_TMA ? 1 : DQ_BLOCKS;  // blocks a drain warp stages at once
   static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;
-  static constexpr int STG_BYTES = DQ_WARPS ? 4 * DQ_BLOCKS * 4096 : 0;
+  static constexpr int STG_BYTES = DQ_WARPS ? 4 * STG_BLOCKS * 4096 : 0;
   // d_head 64: the score products also subtract LSE / sm_scale and Delta, through one more
   // K = 16 step that multiplies a tile of ones by those values (each split into three bf16
   // parts), so the compute warps read neither per column. The K = 16 operand tiles (32 bytes
@@ -221,7 +228,9 @@ struct BwdCfg {
   static constexpr int AUG_BYTES = AUG ? 2 * BN * 128 : 0;
   static_assert(!AUG || (BM == BN && QST <= 3), "augmented operand packing");
   static constexpr int LSE_ST = AUG ? 1 : QST;  // stages of the per-column LSE / Delta arrays
-  static constexpr int SMEM_BYTES = OFF_AUG + AUG_BYTES + 1024;
+  static constexpr int OFF_BIAS = OFF_AUG + AUG_BYTES;
+  static constexpr int BIAS_BYTES = BIAS_TMA ? BM * BN * 2 : 0;
+  static constexpr int SMEM_BYTES = OFF_BIAS + BIAS_BYTES + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
   // TMEM columns: dK, dV accumulators (DH each); S^T, dP^T of the current step; the dQ
   // partial; and P^T (16-bit, two values per column) as the A operand of the dV MMA.
@@ -262,6 +271,7 @@ struct BwdBars {
   uint64_t s_full, s_free, p_full, p_empty;
   uint64_t ds_full[2];
   uint64_t dq_full, dq_empty, dkdv_full;
+  uint64_t bias_full, bias_empty;  // d_head 128 bias kernels: the step's bias tile in its slot
   uint64_t mma_drain;  // completion of the MMA warp's last products
   uint32_t tmem_base;
   int abort;
@@ -276,9 +286,9 @@ struct BwdBars {
 // With p.dbias set, dS is written to the same places; with p.dbias_acc set (a bias shared by
 // several units or heads), dS is added in fp32 to an accumulator of the bias's shape.
 template <int D, bool F16, bool BIAS = false>
-__global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
+__global__ void __launch_bounds__(BwdCfg<D, BIAS>::NTHREADS, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, BIAS>;
   static_assert(!BIAS || D <= 128, "no bias kernel at d_head 256");
   constexpr int BN = C::BN, BM = C::BM, DH = C::DH;
   constexpr int HALF = BM / C::NCWG;  // score columns per compute warpgroup
@@ -351,6 +361,8 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
     mbar_init(smem_u32(&bars.dq_empty), C::DQ_WARPS ? 128 : 256);  // the draining warps
     mbar_init(smem_u32(&bars.dkdv_full), 1);
     mbar_init(smem_u32(&bars.mma_drain), 1);
+    mbar_init(smem_u32(&bars.bias_full), 1);
+    mbar_init(smem_u32(&bars.bias_empty), C::NCOMPUTE);
     mbar_fence_init();
   }
   if (warp == C::WARP_MMA) {
@@ -573,6 +585,31 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
       umma_commit_w(smem_u32(&bars.mma_drain));
       mbar_wait_drain(smem_u32(&bars.mma_drain), 0, p.timeout_ns);
   }
+  } else if (C::BIAS_TMA && warp == C::WARP_BIAS) {
+    // ------------------------------------------------------------------ bias tile loader
+    // Step it's bias tile (its BM query rows x this CTA's 128 keys, at the bias's own local
+    // coordinates; a size-1 batch or head dimension is read at index 0) into the one slot,
+    // once the compute warps have read the previous step's (bias_empty). Keys past the
+    // bias's extent read as zeros; rows and keys past the sequence are masked by the compute
+    // warps whatever they hold.
+    if (lane == 0) {
+      tma_prefetch_map(&p.tm_bias);
+      const int hb = p.b_sh == 0 ? 0 : h, bb = p.b_sb == 0 ? 0 : z;
+      const uint32_t bf = smem_u32(&bars.bias_full);
+      int loaded = 0;
+      for (int it = 0; it < n_steps; ++it) {
+        if (it > 0 && !mbar_wait(smem_u32(&bars.bias_empty), (it - 1) & 1, abort, p.timeout_ns))
+          break;
+        mbar_arrive_expect_tx(bf, C::BIAS_BYTES);
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          tma_load_4d(smem_u32(smem + C::OFF_BIAS + s * BM * 128), &p.tm_bias, bf, k_lo + s * 64,
+                      q_tile(it) * BM, hb, bb);
+        ++loaded;
+      }
+      if (*abort && loaded > 0)  // the consumers gave up: let the last copy land
+        mbar_wait_drain(bf, (loaded - 1) & 1, p.timeout_ns);
+    }
   } else if (warp < 4 * C::NCWG) {
     // ------------------------------------------------------------------ P^T / dS^T compute
     // NCWG warpgroups; warpgroup g owns score columns [g*HALF, (g+1)*HALF) of every key row.
@@ -657,6 +694,10 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
         break;
       }
       tc_fence_after();
+      if (C::BIAS_TMA && !mbar_wait(smem_u32(&bars.bias_full), it & 1, abort, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
 #pragma unroll
       for (int ch = 0; ch < HALF / 32; ++ch) {
         const int c0 = c_base + ch * 32;
@@ -667,12 +708,22 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
         // bias log2(e) of this key and the chunk's 32 query rows (0 off the sequence)
         float bl[BIAS ? 32 : 1];
         if constexpr (BIAS) {
-          const uint16_t* bcol = p.bias + z * p.b_sb + h * p.b_sh + key;
           uint16_t raw[32];
+          if constexpr (C::BIAS_TMA) {
+            // from the staged tile: this key's column, the chunk's 32 rows (a warp reads 64
+            // contiguous bytes of one row at a time)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int qq = q_lo + c0 + e;
-            raw[e] = (key_ok && qq < sv.len_q) ? bcol[(int64_t)qq * p.b_ss] : (uint16_t)0;
+            for (int e = 0; e < 32; ++e)
+              raw[e] = *reinterpret_cast<const uint16_t*>(smem + C::OFF_BIAS +
+                                                          sw128_offset(c0 + e, j, BM));
+            if (ch == HALF / 32 - 1) mbar_arrive(smem_u32(&bars.bias_empty));  // slot read
+          } else {
+            const uint16_t* bcol = p.bias + z * p.b_sb + h * p.b_sh + key;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int qq = q_lo + c0 + e;
+              raw[e] = (key_ok && qq < sv.len_q) ? bcol[(int64_t)qq * p.b_ss] : (uint16_t)0;
+            }
           }
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -878,6 +929,36 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
       }
       tc_fence_after();
       const int q_lo = q_tile(it) * BM;
+      if constexpr (C::STG_BLOCKS == 1 && C::DQ_BLOCKS > 1) {
+        // one 4 KB area a warp: every block of the partial first (the TMEM columns are then
+        // free), then block by block, each after the previous reduce-add has read the area
+        uint8_t* stage = smem + C::OFF_STG + qw * 4096;
+        float v[C::DQ_BLOCKS][32];
+#pragma unroll
+        for (int b = 0; b < C::DQ_BLOCKS; ++b)
+          ATTN_TMEM_LD_X32(tmem + C::COL_DQ + lane_off + 32 * b, reinterpret_cast<uint32_t*>(v[b]));
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dq_empty));
+        const int c0 = dh * DH + qw * 32;
+#pragma unroll
+        for (int b = 0; b < C::DQ_BLOCKS; ++b) {
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<float*>(stage + i * 128 + 16 * ((lane >> 2) ^ (i & 7)) +
+                                      4 * (lane & 3)) = v[b][i];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && c0 < p.d_out) {
+            tma_reduce_add_2d(&p.tm_dq, smem_u32(stage), c0,
+                              (int)(zh * p.rows_q + sv.row0_q + q_lo + b * 32));
+            bulk_commit_group();
+          }
+          __syncwarp();
+        }
+        continue;
+      }
       uint8_t* stage = smem + C::OFF_STG + qw * (C::DQ_BLOCKS * 4096);
       // this warp's previous reduce-adds must have read the area before it is rewritten
       if (lane == 0) bulk_wait_group_read0();
@@ -924,7 +1005,7 @@ __global__ void __launch_bounds__(D == 128 ? 512 : 320, 1)
 
 template <int D, bool F16, bool BIAS>
 static cudaError_t launch_bwd_main_impl(const BwdParams& p, dim3 grid, cudaStream_t stream) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, BIAS>;
   static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);

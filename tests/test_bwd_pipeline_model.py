@@ -31,7 +31,7 @@ from _pipeline_sim import Sim
 
 
 def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
-                      stage_in_ds=True, n_wg=2, ds_tmem=False):
+                      stage_in_ds=True, n_wg=2, ds_tmem=False, bias_tma=False):
     """The kernel's roles; `skip` names waits to leave out (to check that the model sees
     what they prevent; "read_wait" is the wait of a draining warp for its previous
     reduce-add to read its staging; "dq_first" issues dQ before dK with dq_full committed
@@ -41,7 +41,9 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
     warps with staging areas of their own); n_wg: compute warpgroups (1 at d_head 256);
     ds_tmem: the d_head 128 kernel, whose compute warps also write dS^T to tensor memory (the
     A operand of dK, next to P^T) and whose MMA warp commits p_empty after dK (both tensor
-    memory operands of step it read)."""
+    memory operands of step it read); bias_tma: the d_head 128 bias kernel, whose loader warp
+    stages each step's bias tile in one slot (bias_full / bias_empty) and whose drain warps
+    stage one 32 x 32 block at a time in their areas."""
     drains = ("wg0", "wg1") if stage_in_ds else ("dr0", "dr1")
     sim.barrier("kv_full", 1)
     for st in range(qst):
@@ -50,8 +52,10 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
     for b in range(2):
         sim.barrier(f"ds_full{b}", n_wg)
     for name, n in (("s_full", 1), ("s_free", n_wg), ("p_full", n_wg), ("p_empty", 1),
-                    ("dq_full", 1), ("dq_empty", 2), ("dkdv_full", 1)):
+                    ("dq_full", 1), ("dq_empty", 2), ("dkdv_full", 1), ("bias_full", 1),
+                    ("bias_empty", n_wg)):
         sim.barrier(name, n)
+    sim.buffer("BIAS", ("wg0", "wg1")[:n_wg])  # the bias slot: step it's tile
     wg = ("wg0", "wg1")[:n_wg]
     sim.buffer("KV", ())  # the key tile's K and V, loaded once
     for st in range(qst):  # Q / dO stage: the products of its step, and the LSE rows
@@ -156,13 +160,17 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
         yield ("read", "DQ", itd, me, rng.randint(1, 4))
         yield ("arrive", "dq_empty")
         if stage_in_ds:  # stage in this warpgroup's half of dS(itd), reduce-add from it
-            buf = f"DS{itd & 1}{h}"
-        else:  # an area of its own: its previous reduce-add must have read it
-            buf = f"STG{h}"
+            yield ("write", f"DS{itd & 1}{h}", ("stg", itd))
+            yield ("read_async", f"DS{itd & 1}{h}", ("stg", itd), f"tma{h}", rng.randint(1, 12))
+            return True
+        # an area of its own (one block at a time with the bias slot): its previous
+        # reduce-add must have read it
+        buf = f"STG{h}"
+        for blk in range(2 if bias_tma else 1):
             if "read_wait" not in skip:
                 yield ("wait_read", buf, f"tma{h}")
-        yield ("write", buf, ("stg", itd))
-        yield ("read_async", buf, ("stg", itd), f"tma{h}", rng.randint(1, 12))
+            yield ("write", buf, ("stg", itd, blk))
+            yield ("read_async", buf, ("stg", itd, blk), f"tma{h}", rng.randint(1, 12))
         return True
 
     def warpgroup(me):
@@ -180,6 +188,11 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
             yield ("arrive", "s_free")
             if it > 0 and not (yield from wait("p_empty", it - 1)):
                 return
+            if bias_tma:  # this step's bias tile, read into registers, then the slot is free
+                if not (yield from wait("bias_full", it)):
+                    return
+                yield ("read", "BIAS", it, me, rng.randint(1, 4))
+                yield ("arrive", "bias_empty")
             yield ("delay", rng.randint(1, 10))  # P and dS
             if me == "wg0":  # one write event stands for both warpgroups' halves
                 yield ("write", "P", it)
@@ -211,7 +224,21 @@ def backward_protocol(sim, n_steps, qst, with_dq, rng, skip=(), withhold=-1,
                 break
         yield ("wait_read", f"STG{h}", f"tma{h}")  # its reduce-adds complete before exit
 
+    def bias_loader():
+        loaded = 0
+        for it in range(n_steps):
+            if it > 0 and not (yield from wait("bias_empty", it - 1)):
+                break
+            land = rng.randint(1, 10)
+            yield ("write", "BIAS", it, land)
+            yield ("arrive_after", "bias_full", land)
+            loaded += 1
+        if sim.abort and loaded:
+            yield ("drain", "bias_full", loaded - 1)
+
     agents = [producer(), mma()] + [warpgroup_role(w) for w in wg]
+    if bias_tma:
+        agents.append(bias_loader())
     if not stage_in_ds:
         agents += [drain("dr0"), drain("dr1")]
     return agents
@@ -318,3 +345,43 @@ def test_dq_full_must_follow_dk():
                                            stage_in_ds=True))
     assert any(v[0] == "overwrite" and v[1].startswith("DS") and v[4] == ("dK",)
                for v in found), found[:3]
+
+
+@pytest.mark.parametrize("n_steps", [1, 2, 3, 7])
+@pytest.mark.parametrize("qst", [2, 3])
+@pytest.mark.parametrize("with_dq", [True, False])
+def test_backward_bias_tile_slot(n_steps, qst, with_dq):
+    """d_head 128 with a bias: the bias tile of each step is staged in one slot by a loader
+    warp (bias_full / bias_empty) and the drain warps stage one block at a time; every wait
+    exact, no buffer overwritten while read, also with the hardware's parity waits."""
+    rng = random.Random(n_steps * 10 + qst + 100 * with_dq + 7000)
+    for parity in (False, True):
+        for _ in range(100):
+            sim = Sim(rng, exit_check=True, parity_waits=parity,
+                      timeout=5000 if parity else None)
+            assert sim.run(backward_protocol(sim, n_steps, qst, with_dq, rng, stage_in_ds=False,
+                                             ds_tmem=True, bias_tma=True)) == []
+
+
+def test_bias_slot_needs_bias_empty():
+    """Without the wait on bias_empty the loader writes the next step's tile while the
+    compute warps still read the slot."""
+    rng = random.Random(12)
+    found = []
+    for _ in range(300):
+        sim = Sim(rng, mma_ticks=(1, 3))
+        found += sim.run(backward_protocol(sim, 6, 3, True, rng, stage_in_ds=False,
+                                           ds_tmem=True, bias_tma=True, skip=("bias_empty",)))
+    assert any(v[1] == "BIAS" for v in found), found[:3]
+
+
+@pytest.mark.parametrize("withhold", [0, 1, 3])
+def test_bias_slot_withheld_step(withhold):
+    """The failure-detection path with the bias loader: every role leaves, nothing in flight."""
+    rng = random.Random(withhold + 8000)
+    for _ in range(100):
+        sim = Sim(rng, timeout=200, exit_check=True)
+        v = sim.run(backward_protocol(sim, 6, 3, True, rng, withhold=withhold, stage_in_ds=False,
+                                      ds_tmem=True, bias_tma=True))
+        assert sim.abort
+        assert v == [], v[:3]
