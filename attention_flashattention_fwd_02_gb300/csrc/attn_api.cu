@@ -568,9 +568,8 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       if (a.bias != nullptr) {
         // size-1 batch / head dimensions broadcast: stride 0
         p.bias = reinterpret_cast<const uint16_t*>(a.bias->data);
-        // the 128-wide kernel stages each step's bias tile by TMA
-        if (kernel_width(pr.D) == 128 &&
-            (s = make_map(&p.tm_bias, a.bias, bwd_block_m(128))) != ATTN_OK)
+        // the kernel stages each step's bias tile (its query rows x 128 keys) by TMA
+        if ((s = make_map(&p.tm_bias, a.bias, bwd_block_m(kernel_width(pr.D)))) != ATTN_OK)
           return s;
         p.b_sb = a.bias->size[0] == 1 ? 0 : a.bias->stride[0];
         p.b_sh = a.bias->size[1] == 1 ? 0 : a.bias->stride[1];

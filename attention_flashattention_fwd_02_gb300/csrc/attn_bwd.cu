@@ -199,7 +199,9 @@ struct BwdCfg {
   static constexpr int DS_BYTES = BN * BM * 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int QST = DSPLIT ? 2 : 3;            // Q / dO / LSE / Delta stages
+  // Q / dO / LSE / Delta stages: two at d_head 256, and in the d_head 64 bias kernel, whose
+  // bias tile slot takes the third stage's room
+  static constexpr int QST = (DSPLIT || (D == 64 && BIAS)) ? 2 : 3;
   static constexpr int OFF_Q = OFF_V + KV_BYTES;        // QST stages
   static constexpr int OFF_DO = OFF_Q + QST * Q_BYTES;  // QST stages
   static constexpr int OFF_DS = OFF_DO + QST * Q_BYTES; // 2 buffers
@@ -209,11 +211,11 @@ struct BwdCfg {
   // rows again, two steps later, after waiting for the reduce to read them).
   static constexpr bool DQ_WARPS = DQ_T;
   static constexpr int DQ_BLOCKS = BM / 32;             // 32 x 32 blocks per drain warp
-  // d_head 128 with a bias: a warp of its own (warp 10) loads each step's bias tile (BM
-  // query rows x 128 keys, two 64-key slabs with the 128-byte swizzle) into a slot of shared
-  // memory by TMA; the room comes from the drain warps, which then stage one 32 x 32 block
-  // at a time (4 KB each).
-  static constexpr bool BIAS_TMA = BIAS && (D == 128);
+  // d_head 64 and 128 with a bias: a warp of its own (warp 10) loads each step's bias tile
+  // (BM query rows x 128 keys, two 64-key slabs with the 128-byte swizzle) into a slot of
+  // shared memory by TMA. The room comes at d_head 128 from the drain warps, which then stage
+  // one 32 x 32 block at a time (4 KB each), at d_head 64 from a third Q / dO stage.
+  static constexpr bool BIAS_TMA = BIAS && (D <= 128);
   static constexpr int WARP_BIAS = 10;
   static constexpr int STG_BLOCKS = BIAS_TMA ? 1 : DQ_BLOCKS;  // blocks a drain warp stages at once
   static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;
@@ -246,11 +248,13 @@ struct BwdCfg {
   static constexpr bool DS_TMEM = (D == 128);
   static constexpr uint32_t COL_DST = COL_P + BM / 2;
   static_assert(!DS_TMEM || COL_DST + BM / 2 <= TMEM_COLS, "TMEM layout does not fit");
-  // Warps. d_head 64: 0..7 compute, 8 producer, 9 MMA (320 threads). d_head 128: 0..7
-  // compute, 8 producer, 9 MMA, 10..11 no role, 12..15 dQ drain (512 threads leave 128
-  // registers a thread, which these roles fit in). d_head 256: 0..3 compute, 4..7 dQ drain,
-  // 8 producer, 9 MMA (320 threads). A drain warp reaches the TMEM lanes of its index mod 4.
-  static constexpr int NTHREADS = (D == 128) ? 512 : 320;
+  // Warps. d_head 64: 0..7 compute, 8 producer, 9 MMA (320 threads; with a bias also 10,
+  // the bias tile loader: 352). d_head 128: 0..7 compute, 8 producer, 9 MMA, 10 the bias
+  // tile loader of the bias kernel (else no role), 11 no role, 12..15 dQ drain (512 threads
+  // leave 128 registers a thread, which these roles fit in). d_head 256: 0..3 compute, 4..7
+  // dQ drain, 8 producer, 9 MMA (320 threads). A drain warp reaches the TMEM lanes of its
+  // index mod 4.
+  static constexpr int NTHREADS = (D == 128) ? 512 : (BIAS_TMA ? 352 : 320);
   static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_DRAIN0 = DSPLIT ? 4 : 12;
   static constexpr int NCOMPUTE = 128 * NCWG;        // compute threads
   // Epilogue: a compute warp stores its 32 keys x CW columns of dK and of dV through shared
@@ -295,6 +299,8 @@ __global__ void __launch_bounds__(BwdCfg<D, BIAS>::NTHREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   constexpr int QST = C::QST;
   __shared__ BwdBars<BM, QST, C::LSE_ST> bars;
+  static_assert(C::SMEM_BYTES + sizeof(BwdBars<BM, QST, C::LSE_ST>) <= 232448,
+                "static and dynamic shared memory (227 KB per CTA)");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // 1-D grid over (unit, head) pairs x key tiles (grid_pos; key tile 0, the heaviest of a

@@ -124,8 +124,8 @@ struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 4-D maps; Q/dO box rows = BM, K/V box rows = BN
   CUtensorMap tm_dq;                    // 2-D fp32 map over the dQ accumulator [rows][D]
                                         // (d_head 64), box (32, 128), 128-byte swizzle
-  CUtensorMap tm_bias;                  // d_head 128 bias kernels: 4-D (Sk, Sq, Hb, Bb) over
-                                        // the bias, box (64, 64 query rows), 128-byte swizzle
+  CUtensorMap tm_bias;                  // bias kernels: 4-D (Sk, Sq, Hb, Bb) over the bias,
+                                        // box (64, query rows a step), 128-byte swizzle
   CUtensorMap tm_dk, tm_dv;             // dK, dV: box (a warpgroup's columns, 32 keys), no
                                         // swizzle (the staged epilogue's stores)
   const float* lse;

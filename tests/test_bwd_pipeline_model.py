@@ -350,17 +350,20 @@ def test_dq_full_must_follow_dk():
 @pytest.mark.parametrize("n_steps", [1, 2, 3, 7])
 @pytest.mark.parametrize("qst", [2, 3])
 @pytest.mark.parametrize("with_dq", [True, False])
-def test_backward_bias_tile_slot(n_steps, qst, with_dq):
-    """d_head 128 with a bias: the bias tile of each step is staged in one slot by a loader
-    warp (bias_full / bias_empty) and the drain warps stage one block at a time; every wait
-    exact, no buffer overwritten while read, also with the hardware's parity waits."""
-    rng = random.Random(n_steps * 10 + qst + 100 * with_dq + 7000)
+@pytest.mark.parametrize("d128", [True, False])
+def test_backward_bias_tile_slot(n_steps, qst, with_dq, d128):
+    """With a bias the tile of each step is staged in one slot by a loader warp (bias_full /
+    bias_empty); at d_head 128 the drain warps stage one block at a time, at d_head 64 the
+    compute warps drain as without a bias. Every wait exact, no buffer overwritten while
+    read, also with the hardware's parity waits."""
+    rng = random.Random(n_steps * 10 + qst + 100 * with_dq + 7000 + 50 * d128)
     for parity in (False, True):
         for _ in range(100):
             sim = Sim(rng, exit_check=True, parity_waits=parity,
                       timeout=5000 if parity else None)
-            assert sim.run(backward_protocol(sim, n_steps, qst, with_dq, rng, stage_in_ds=False,
-                                             ds_tmem=True, bias_tma=True)) == []
+            assert sim.run(backward_protocol(sim, n_steps, qst, with_dq, rng,
+                                             stage_in_ds=not d128, ds_tmem=d128,
+                                             bias_tma=True)) == []
 
 
 def test_bias_slot_needs_bias_empty():
