@@ -21,10 +21,11 @@
 // the MMAs. Each step's dQ partial goes from TMEM into the global fp32 accumulator through
 // shared-memory staging and TMA reduce-adds: at d_head 128 (512 threads) warps 12..15 do this
 // (each the 32 TMEM lanes it can reach) while the compute warps already work on the next
-// step, and warps 10, 11 have no role; at d_head 64 (320 threads; the compute warps hold a
-// step's 128 score columns in registers, and a CTA of more warps would leave each fewer than
-// that needs) every compute warp drains its own 32 x 32 block after forming the next step's
-// P and dS. Tile sizes: 128 keys per CTA; 64 query rows per step when d_head = 128 (dQ is
+// step, and warp 11 has no role; at d_head 64 (320 threads; the compute warps hold a step's
+// 128 score columns in registers, and a CTA of more warps would leave each fewer than that
+// needs) every compute warp drains its own 32 x 32 block after forming the next step's P and
+// dS. With a bias, warp 10 loads each step's bias tile into shared memory by TMA (352
+// threads at d_head 64). Tile sizes: 128 keys per CTA; 64 query rows per step when d_head = 128 (dQ is
 // formed transposed, K_n^T dS^T, so that every MMA has M = 128), 128 when d_head = 64.
 #include <atomic>
 
