@@ -64,11 +64,15 @@ template <int D, bool BIAS = false>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int NQ = (D == 256 || (D == 128 && BIAS)) ? 1 : 2;  // query tiles per CTA
-  static constexpr int NST = (D == 256) ? 1 : (D == 128) ? 2 : 4;
-  static constexpr bool SPLIT_KV = (D == 256);   // K and V released and loaded separately
+  // d_head 128 with a bias: one query tile, one K and one V stage released separately (as at
+  // d_head 256) and four bias slots, so that the bias tiles, read once from DRAM, are loaded
+  // four key tiles ahead
+  static constexpr bool ONE_KV = (D == 256) || (D == 128 && BIAS);
+  static constexpr int NST = ONE_KV ? 1 : (D == 128) ? 2 : 4;
+  static constexpr bool SPLIT_KV = ONE_KV;   // K and V released and loaded separately
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NBS = BIAS ? 2 : 0;       // bias slots
+  static constexpr int NBS = BIAS ? (D == 128 ? 4 : 2) : 0;  // bias slots
   static constexpr int BS_T = NBS / NQ;            // bias slots per query tile
   static constexpr int B_BYTES = BM * BN * 2;      // one bias slot
   static constexpr int OFF_Q = 0;
@@ -114,7 +118,7 @@ struct FwdBars {
   uint64_t k_empty[NST];  // SPLIT_KV: K stage free (kv_empty then frees the V stage)
   uint64_t s_full[NSB], p_full[NSB], buf_free[NSB];
   uint64_t o_done[2][2];  // PV_t(j) completed: barrier [t][j mod 2] (see the rescale wait)
-  uint64_t b_full[2], b_empty[2];  // bias slots (NBS of them used)
+  uint64_t b_full[4], b_empty[4];  // bias slots (NBS of them used)
   uint64_t mma_drain[2];           // completion of each issuing warp's last products
   uint32_t tmem_base;
   int abort;
@@ -266,11 +270,11 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       mbar_init(smem_u32(&bars.buf_free[b]), 1);
     }
     for (int r = 0; r < 4; ++r) mbar_init(smem_u32(&bars.o_done[r >> 1][r & 1]), 1);
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < 4; ++t) {
       mbar_init(smem_u32(&bars.b_full[t]), 1);
       mbar_init(smem_u32(&bars.b_empty[t]), 128);
-      mbar_init(smem_u32(&bars.mma_drain[t]), 1);
     }
+    for (int t = 0; t < 2; ++t) mbar_init(smem_u32(&bars.mma_drain[t]), 1);
     mbar_fence_init();
   }
   if (warp == C::WARP_MMA) {
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       tma_prefetch_map(&p.tm_b);
       const uint32_t sB = smem_u32(smem + C::OFF_B);
       int b_g[2] = {0, 0};        // bias tiles of each query tile loaded so far
-      int last_ph[2] = {-1, -1};  // last phase loaded into each slot
+      int last_ph[4] = {-1, -1, -1, -1};  // last phase loaded into each slot
       bool go = true;
       int ci = 0;
       for (int item = first_item(); go && item >= 0; item = go ? next_item(item, ci, kLane) : -1) {
@@ -468,7 +472,7 @@ __global__ void __launch_bounds__((D == 64 ? 352 : 320) + (BIAS ? 32 : 0), 1)
       }
       if (*abort)  // let the copies in flight land before exiting
 #pragma unroll
-        for (int sl = 0; sl < 2; ++sl)
+        for (int sl = 0; sl < C::NBS; ++sl)
           if (last_ph[sl] >= 0)
             mbar_wait_drain(smem_u32(&bars.b_full[sl]), last_ph[sl] & 1, p.timeout_ns);
     }

@@ -251,8 +251,10 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
             return t, gb
         if bias_slots == "one":  # the first 128-wide scheme: one slot for both tiles
             return 0, s0[i] + k
-        if bias_slots == "tile2":  # one query tile with two slots (the 128-wide kernel)
+        if bias_slots == "tile2":  # one query tile with two slots
             return 2 * t + gb % 2, gb // 2
+        if bias_slots == "tile4":  # one query tile with four slots (the 128-wide kernel)
+            return 4 * t + gb % 4, gb // 4
         return (s0[i] + k) % 2, (s0[i] + k) // 2  # the earlier scheme: shared by the tiles
 
     def bias_producer():
@@ -458,11 +460,14 @@ def test_bias_forward_pipeline(n0, n1):
 
 @pytest.mark.parametrize("n0", [1, 2, 3, 6, 9])
 def test_bias_forward_pipeline_d128(n0):
-    """The 128-wide bias kernel: one query tile per CTA, its bias tiles alternating between
-    two slots (slot j mod 2, phase j / 2)."""
+    """The 128-wide bias kernel: one query tile per CTA, one K and one V stage released
+    separately (the one-tile layout), its bias tiles rotating through four slots (slot j
+    mod 4, phase j / 4); also two slots over two K/V stages."""
+    assert _runs(256, n0, 0, n0, 120, bias=True, bias_slots="tile4") == []
+    assert _runs(256, n0, 0, n0 + 1, 120, slow=True, bias=True, bias_slots="tile4") == []
     assert _runs(128, n0, 0, n0, 120, bias=True, bias_slots="tile2") == []
-    assert _runs(128, n0, 0, n0 + 1, 120, slow=True, bias=True, bias_slots="tile2") == []
     tiles = [(n0, 0)]
+    assert _parity_runs(256, tiles, "tile4", n0 + 2) == set()
     assert _parity_runs(128, tiles, "tile2", n0 + 2) == set()
 
 
@@ -600,7 +605,8 @@ def test_persistent_cta_over_several_items(D, which, steal):
 @pytest.mark.parametrize("steal", [False, True])
 @pytest.mark.parametrize("D,scheme,items", [
     (64, "tile", [(5, 6), (3, 4), (1, 2)]), (64, "tile", [(2, 1), (1, 0), (0, 0), (3, 3)]),
-    (128, "tile2", [(5, 0), (3, 0), (1, 0)]), (128, "tile2", [(2, 0), (0, 0), (1, 0), (4, 0)])])
+    (128, "tile2", [(5, 0), (3, 0), (1, 0)]), (256, "tile4", [(2, 0), (0, 0), (1, 0), (4, 0)]),
+    (256, "tile4", [(5, 0), (3, 0), (1, 0)])])
 def test_persistent_cta_with_bias(D, scheme, items, steal):
     assert _item_runs(D, items, 11, 100, bias=True, bias_slots=scheme, steal=steal) == []
     assert _item_runs(D, items, 12, 60, slow=True, parity=True, bias=True,
