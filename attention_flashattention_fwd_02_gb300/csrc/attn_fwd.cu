@@ -68,11 +68,12 @@ struct FwdCfg {
   // d_head 256) and four bias slots, so that the bias tiles, read once from DRAM, are loaded
   // four key tiles ahead
   static constexpr bool ONE_KV = (D == 256) || (D == 128 && BIAS);
-  static constexpr int NST = ONE_KV ? 1 : (D == 128) ? 2 : 4;
+  // d_head 64 with a bias: two K/V stages instead of four, for two bias slots per query tile
+  static constexpr int NST = ONE_KV ? 1 : (D == 128 || BIAS) ? 2 : 4;
   static constexpr bool SPLIT_KV = ONE_KV;   // K and V released and loaded separately
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NBS = BIAS ? (D == 128 ? 4 : 2) : 0;  // bias slots
+  static constexpr int NBS = BIAS ? 4 : 0;  // bias slots
   static constexpr int BS_T = NBS / NQ;            // bias slots per query tile
   static constexpr int B_BYTES = BM * BN * 2;      // one bias slot
   static constexpr int OFF_Q = 0;

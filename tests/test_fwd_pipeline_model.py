@@ -52,7 +52,7 @@ CONFIGS = {  # score buffers, K/V stages, split issue, split K/V release
 
 def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_slots="tile",
                      skip=(), copy_ticks=(1, 8), withhold=-1, hook="break", items=None,
-                     steal=False):
+                     steal=False, nst=None):
     """One CTA's roles over its work items: `items` lists the (n0, n1) key-tile counts of the
     query blocks a CTA takes in turn (default: the one block (n0, n1); (0, 0) is a block with
     nothing to do, past its sequence). Every ring runs on a count over the items (key tiles g,
@@ -68,7 +68,8 @@ def forward_protocol(sim, D, n0, n1, rng, bias=False, o_scheme="parity", bias_sl
     from which the producers stop loading (the kernel's failure-detection hook; hook=
     "continue" skips only that tile, as the hook once did), so that waits time out and roles
     leave."""
-    nsb, nst, split, split_kv = CONFIGS[D]
+    nsb, nst_d, split, split_kv = CONFIGS[D]
+    nst = nst_d if nst is None else nst  # K/V stages (the d_head 64 bias kernel: two)
     items = [(n0, n1)] if items is None else items
     n_items = len(items)
     live = [i for i, (a, b) in enumerate(items) if max(a, b) > 0]  # items with key tiles
@@ -450,6 +451,15 @@ def test_forward_pipeline_is_exact_and_race_free(D, n0, n1):
     seed = D * 1000 + n0 * 10 + n1
     assert _runs(D, n0, n1, seed, 120) == []
     assert _runs(D, n0, n1, seed + 1, 80, slow=True) == []
+
+
+@pytest.mark.parametrize("n0,n1", [(5, 5), (5, 6), (6, 0), (1, 2), (2, 3)])
+def test_bias_forward_pipeline_d64_two_slots_per_tile(n0, n1):
+    """The 64-wide bias kernel: two K/V stages and two bias slots per query tile (slot
+    2 t + j mod 2, phase j / 2), with exact and with parity waits."""
+    assert _runs(64, n0, n1, n0 * 10 + n1 + 5, 120, bias=True, bias_slots="tile2", nst=2) == []
+    assert _runs(64, n0, n1, n0 * 10 + n1 + 6, 80, slow=True, bias=True, bias_slots="tile2",
+                 nst=2) == []
 
 
 @pytest.mark.parametrize("n0,n1", [(5, 5), (5, 6), (6, 0), (2, 1), (2, 3)])
