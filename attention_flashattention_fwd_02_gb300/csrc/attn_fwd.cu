@@ -74,7 +74,7 @@ struct FwdCfg {
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int NBS = BIAS ? 4 : 0;  // bias slots
-  static constexpr int BS_T = NBS / NQ;            // bias slots per query tile
+  static constexpr int BS_T = BIAS ? NBS / NQ : 1; // bias slots per query tile (1: no bias role)
   static constexpr int B_BYTES = BM * BN * 2;      // one bias slot
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = NQ * Q_BYTES;
