@@ -5,6 +5,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/attn.h"
@@ -193,11 +194,12 @@ SeqAddr seq_addr(const Problem& pr) {
   return a;
 }
 
-// 4-D tensor map over a BHSD view: dims (D, S, H, B) innermost first, box (64, rows, 1, 1),
-// 128-byte swizzle. Strides of size-1 dimensions are never used; they are replaced by a
-// valid dummy so that any view of such a dimension is accepted.
+// 4-D tensor map over a BHSD view: dims (D, S, H, B) innermost first, box (box_cols, rows, 1,
+// 1), swizzle 128, 64 or 0 bytes (a swizzled box's rows are that long). Strides of size-1
+// dimensions are never used; they are replaced by a valid dummy so that any view of such a
+// dimension is accepted.
 attn_status make_map(CUtensorMap* m, const attn_tensor4* t, int box_rows, int box_cols = 64,
-                     bool swizzle = true) {
+                     int swizzle = 128) {
   auto enc = encode_fn();
   if (enc == nullptr) return ATTN_ERR_CUDA;
   const int64_t B = t->size[0], H = t->size[1], S = t->size[2], D = t->size[3];
@@ -215,7 +217,9 @@ attn_status make_map(CUtensorMap* m, const attn_tensor4* t, int box_rows, int bo
       t->dtype == ATTN_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = enc(m, ty, 4, t->data, dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   swizzle == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                   : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                   : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -526,10 +530,11 @@ attn_status bwd_stage(int stage_mask, const BwdArgs& a, const Problem& pr, float
       if ((s = make_map(&p.tm_do, a.dout, BM)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_k, a.k, BN)) != ATTN_OK) return s;
       if ((s = make_map(&p.tm_v, a.v, BN)) != ATTN_OK) return s;
-      // the epilogue's dK / dV stores: a compute warpgroup's columns x 32 keys
-      const int cw = bwd_epilogue_cols(kernel_width(pr.D));
-      if ((s = make_map(&p.tm_dk, a.dk, 32, cw, false)) != ATTN_OK) return s;
-      if ((s = make_map(&p.tm_dv, a.dv, 32, cw, false)) != ATTN_OK) return s;
+      // the epilogue's dK / dV stores: 32 keys x a slab of at most 64 of a compute
+      // warpgroup's columns, swizzled like the staged slab (128 or 64 bytes a row)
+      const int cw = std::min(bwd_epilogue_cols(kernel_width(pr.D)), 64);
+      if ((s = make_map(&p.tm_dk, a.dk, 32, cw, cw * 2)) != ATTN_OK) return s;
+      if ((s = make_map(&p.tm_dv, a.dv, 32, cw, cw * 2)) != ATTN_OK) return s;
       p.with_dq = deterministic ? 0 : 1;
       p.withhold_step = withheld_step_for_test();
       p.timeout_ns = p.withhold_step >= 0 ? 50000000ull : kWaitTimeoutNs;

@@ -259,13 +259,16 @@ struct BwdCfg {
   static constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_DRAIN0 = DSPLIT ? 4 : 12;
   static constexpr int NCOMPUTE = 128 * NCWG;        // compute threads
   // Epilogue: a compute warp stores its 32 keys x CW columns of dK and of dV through shared
-  // memory (row-major, CW * 2 bytes a row) with TMA stores; the K and V tiles' space is free
-  // by then and holds the 2 x 4 NCWG warp areas. Not at d_head 128, where the staging code
-  // costs the key-tile loop a register (measured 1 % slower) and the row stores are cheap
-  // against a step's work; there, and on tiles reaching past the sequence, row stores.
-  static constexpr bool EPI_TMA = (D != 128);
+  // memory with TMA stores; the K and V tiles' space is free by then and holds the 2 x 4 NCWG
+  // warp areas. A warp's area holds CW / EPI_SC slabs of 32 rows (keys) x EPI_SC columns (64
+  // or 128 bytes a row) whose 16-byte chunks are swizzled like the TMA's 64- or 128-byte
+  // modes, so that a warp's 16-byte stores (one row a lane) spread over all banks. Tiles
+  // reaching past the sequence leave with row stores.
+  static constexpr bool EPI_TMA = true;
   static constexpr int CW = DH / NCWG;
   static constexpr int EPI_W_BYTES = 32 * CW * 2;
+  static constexpr int EPI_SC = CW < 64 ? CW : 64;
+  static constexpr int EPI_SLAB_BYTES = 32 * EPI_SC * 2;
   static_assert(2 * 4 * NCWG * EPI_W_BYTES <= 2 * KV_BYTES, "epilogue staging");
 };
 
@@ -852,10 +855,10 @@ __global__ void __launch_bounds__(BwdCfg<D, BIAS>::NTHREADS, 1)
     if (ok) ok = mbar_wait(smem_u32(&bars.dkdv_full), 0, abort, p.timeout_ns);
     tc_fence_after();
     // A key tile inside its sequence leaves through shared memory: each warp writes its 32
-    // keys of dK and dV (its warpgroup's columns) as rows of its own areas, in the space of
-    // the K and V tiles (every product that read them has completed: dkdv_full), and one
-    // lane stores each area with a TMA copy. A tile reaching past the sequence's end is
-    // stored row by row (a copy would also write the keys past the end).
+    // keys of dK and dV (its warpgroup's columns) as rows of the swizzled slabs of its own
+    // areas, in the space of the K and V tiles (every product that read them has completed:
+    // dkdv_full), and one lane stores each slab with a TMA copy. A tile reaching past the
+    // sequence's end is stored row by row (a copy would also write the keys past the end).
     constexpr int CW = C::CW;
     if (C::EPI_TMA && ok && k_lo + BN <= sv.len_k) {
       const float sc = p.sm_scale;
@@ -877,16 +880,25 @@ __global__ void __launch_bounds__(BwdCfg<D, BIAS>::NTHREADS, 1)
           vv.y = pack2<F16>(__uint_as_float(b[e + 2]), __uint_as_float(b[e + 3]));
           vv.z = pack2<F16>(__uint_as_float(b[e + 4]), __uint_as_float(b[e + 5]));
           vv.w = pack2<F16>(__uint_as_float(b[e + 6]), __uint_as_float(b[e + 7]));
-          st_shared_v4(ak + lane * (CW * 2) + (c + e) * 2, vk);
-          st_shared_v4(av + lane * (CW * 2) + (c + e) * 2, vv);
+          const int col = c + e, j = (col % C::EPI_SC) / 8;
+          const int pj = C::EPI_SC == 64 ? (j ^ (lane & 7)) : (j ^ ((lane >> 1) & 3));
+          const uint32_t off =
+              (col / C::EPI_SC) * C::EPI_SLAB_BYTES + lane * (C::EPI_SC * 2) + pj * 16;
+          st_shared_v4(ak + off, vk);
+          st_shared_v4(av + off, vv);
         }
       }
       fence_proxy_async_smem();  // the areas, written by this warp, to the copy engine
       __syncwarp();
       if (lane == 0) {
         const int row = sv.row0_k + k_lo + (warp & 3) * 32;
-        tma_store_4d(&p.tm_dk, ak, dh * DH + g * CW, row, h, sv.batch);
-        tma_store_4d(&p.tm_dv, av, dh * DH + g * CW, row, h, sv.batch);
+#pragma unroll
+        for (int s = 0; s < CW / C::EPI_SC; ++s) {
+          tma_store_4d(&p.tm_dk, ak + s * C::EPI_SLAB_BYTES, dh * DH + g * CW + s * C::EPI_SC, row,
+                       h, sv.batch);
+          tma_store_4d(&p.tm_dv, av + s * C::EPI_SLAB_BYTES, dh * DH + g * CW + s * C::EPI_SC, row,
+                       h, sv.batch);
+        }
         bulk_commit_group();
         bulk_wait_group0();  // complete before the CTA exits
       }
