@@ -419,10 +419,12 @@ __global__ void __launch_bounds__(BwdCfg<D, BIAS>::NTHREADS, 1)
     int last_it[QST];  // last step loaded into each stage (-1: none)
 #pragma unroll
     for (int st = 0; st < QST; ++st) last_it[st] = -1;
-    // LSE log2(e) and Delta of a step's query rows (this lane's rows lane + 32 i; 0 off the
-    // sequence), loaded one step ahead: the loads of step it + 1 are issued before the wait
-    // for the stage they will fill, so their latency hides behind that wait instead of
-    // delaying every step's q_full
+    // LSE and Delta of a step's query rows (this lane's rows lane + 32 i; 0 off the
+    // sequence), loaded one step ahead: the loads of step it + 1 are issued right after the
+    // copies of step it, and nothing uses the values before they are written to shared
+    // memory (the LSE's scaling by log2(e) too), so their latency hides behind the copies and
+    // the next wait instead of holding up the copies (at a CTA's start that was two global
+    // round trips before its first Q / dO copy)
     constexpr int NL = (BM + 31) / 32;
     float nl2[NL], ndl[NL];
     auto fetch_rows = [&](int itf, float* l2o, float* dlo) {
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BIAS>::NTHREADS, 1)
         dlo[u] = 0.f;
         if (lane + 32 * u < BM && q < sv.len_q) {
           const int64_t grow = sv.row0_q + q;
-          l2o[u] = p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss] * kLog2e;
+          l2o[u] = p.lse[sv.batch * p.l_sb + h * p.l_sh + grow * p.l_ss];
           dlo[u] = p.delta[zh * p.rows_q + grow];
         }
       }
@@ -448,8 +450,10 @@ __global__ void __launch_bounds__(BwdCfg<D, BIAS>::NTHREADS, 1)
         cl2[u] = nl2[u];
         cdl[u] = ndl[u];
       }
-      if (it + 1 < n_steps) fetch_rows(it + 1, nl2, ndl);
-      if (it == p.withhold_step) continue;  // failure-detection test: this stage never fills
+      if (it == p.withhold_step) {  // failure-detection test: this stage never fills
+        if (it + 1 < n_steps) fetch_rows(it + 1, nl2, ndl);
+        continue;
+      }
       if (it >= QST &&
           !mbar_wait(smem_u32(&bars.q_empty[st]), ((it / QST) - 1) & 1, abort, p.timeout_ns))
         break;
@@ -466,11 +470,12 @@ __global__ void __launch_bounds__(BwdCfg<D, BIAS>::NTHREADS, 1)
                       h, sv.batch);
         }
       }
+      if (it + 1 < n_steps) fetch_rows(it + 1, nl2, ndl);
 #pragma unroll
       for (int u = 0; u < NL; ++u) {
         const int i = lane + 32 * u;
         if (i >= BM) break;
-        const float l2 = cl2[u], dl = cdl[u];
+        const float l2 = cl2[u] * kLog2e, dl = cdl[u];
         if constexpr (C::AUG) {
           // c2 (S + a) = c2 S - LSE log2(e) with a = -LSE / sm_scale
           aug_split(1 + st, i, -l2 / p.scale_log2);
