@@ -488,6 +488,26 @@ __global__ void __launch_bounds__(BwdCfg<D, BIAS>::NTHREADS, 1)
       if (C::AUG) fence_proxy_async_smem();  // the rows are read by the MMAs (async proxy)
       mbar_arrive(qb);
     }
+    // The K / V tile of the CTA one SM count further in launch order (likely the next to
+    // start on a freed SM) into L2: its first copies then come from L2
+    if (lane == 0 && !*abort) {
+      uint32_t nsm;
+      asm volatile("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+      const int nb = (int)blockIdx.x + (int)nsm;
+      if (nb < (int)gridDim.x) {
+        const GridPos gq = grid_pos(nb, p.tiles, (int)(gridDim.x / p.tiles), p.group);
+        const int hq = gq.zh % p.H, zq = gq.zh / p.H;
+        const int kq = (C::DSPLIT ? gq.rank >> 1 : gq.rank) * BN;
+        SeqView sq;
+        if (decode_seq(p.seq, zq, nullptr, sq) && kq < sq.len_k) {
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s) {
+            tma_prefetch_l2_4d(&p.tm_k, s * 64, sq.row0_k + kq, hq, sq.batch);
+            tma_prefetch_l2_4d(&p.tm_v, s * 64, sq.row0_k + kq, hq, sq.batch);
+          }
+        }
+      }
+    }
     if (lane == 0 && *abort) {  // the consumers gave up: let the copies in flight land
       mbar_wait_drain(smem_u32(&bars.kv_full), 0, p.timeout_ns);
 #pragma unroll
